@@ -1,0 +1,198 @@
+/*
+ * pt.h -- C ABI of libpt: exact softmax attention over a prefix-tree token
+ * layout, forward and backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * The method.  Many sequences that share prefixes are stored once, flat: a
+ * prefix tree whose nodes each own a contiguous run of tokens, every ancestor
+ * laid out before its descendants.  A token attends to every token of its
+ * ancestor nodes and causally to the tokens of its own node; nothing crosses
+ * sibling branches, groups or packed documents.  In the GRPO case one prompt
+ * of P tokens is followed by G completions, and each completion sees the
+ * whole prompt and itself causally ("cp=1 shared-prefix prefix-tree attention
+ * for rollouts", PR description; "prefix_grouper_kernel.py", module
+ * docstring and _make_mask_mod).  The result is identical to dense masked
+ * attention, but tiles whose pairs are all masked are never visited, so the
+ * cost is proportional to the kept pairs, O(P + G*R) per group rather than
+ * O(T^2) ("prefix_grouper_kernel.py", module docstring).
+ *
+ * Conventions shared by every call:
+ *  - Device pointers are raw CUDA device addresses on the current device,
+ *    16-byte aligned, densely packed (no strides).  Host pointers are plain
+ *    host memory.  The caller owns every buffer it passes in.
+ *  - Tensors are token-major: Q, dO, O, dQ are [T, Hq, D]; K, V, dK, dV are
+ *    [T, Hkv, D]; LSE is [Hq, T] fp32 (natural log).  This is the pages'
+ *    [1, T, H, D] layout without the batch dimension
+ *    ("prefix_grouper_kernel.py", flex_shared_prefix_attention).
+ *  - Grouped-query attention: q head h reads kv head h / (Hq / Hkv)
+ *    ("prefix_grouper_kernel.py", enable_gqa = n_heads != n_kv).
+ *  - Calls are ordered on the given stream.  Nothing is silently ignored or
+ *    replaced by a fallback: an argument the library cannot honour returns an
+ *    error status before anything is launched ("cp=1 shared-prefix prefix-tree
+ *    attention for rollouts": the HF path fails loudly rather than dropping
+ *    the mask).  pt_last_error() gives a message for the calling thread.
+ *  - Every wait inside a kernel is bounded; a wait that runs out records
+ *    PT_ERR_TIMEOUT in a per-device status word, which pt_sync_status()
+ *    returns (and clears).
+ */
+#ifndef PT_H_
+#define PT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PT_OK = 0,
+  PT_ERR_INVALID_ARG = 1, /* malformed tree or labels, bad sizes, null pointers */
+  PT_ERR_UNSUPPORTED = 2, /* valid but not implemented (head_dim, dtype, tile) */
+  PT_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+  PT_ERR_TIMEOUT = 4,     /* a bounded in-kernel wait ran out */
+  PT_ERR_NOMEM = 5        /* device or host allocation failed */
+} pt_status;
+
+typedef enum { PT_BF16 = 0, PT_F32 = 1 } pt_dtype;
+
+/* Opaque, device-resident block map.  Owned by the library; free it with
+ * pt_blockmap_free.  It depends only on the tree and the tile sizes, so one
+ * map serves every layer and both passes ("prefix_grouper_kernel.py",
+ * get_block_mask: the mask is cached and reused across layers and steps). */
+typedef struct pt_blockmap pt_blockmap;
+
+/* ---------------------------------------------------------------------------
+ * pt_build_blockmap_tree -- block map from the tree form.
+ *
+ * Passage: "cp=1 shared-prefix prefix-tree attention for rollouts": the fold
+ * emits the tree as (node_lengths, sample_paths) and the mask is built by
+ * AttnMaskSpec.prefix_tree.
+ *
+ * node_lengths [n_nodes] (host): token count of node i (0 allowed).  Node i
+ *   occupies tokens [off_i, off_i + node_lengths[i]) with off the exclusive
+ *   prefix sum in id order; T = sum of node_lengths.
+ * path_ptr [n_samples + 1], path_nodes [path_ptr[n_samples]] (host): CSR list
+ *   of root->leaf paths.  Consecutive entries (a, b) of a path make a the
+ *   parent of b.
+ * block_m, block_n: q-tile rows and kv-block columns.  The tensor-core
+ *   kernels need 128 x 128; the fp32 kernels accept any positive size.
+ * stream: the build runs on it and synchronises it once before returning.
+ * out: receives the new map.
+ *
+ * Errors: PT_ERR_INVALID_ARG when a length is negative, a path is empty or
+ * names a node out of range, a parent does not have a smaller id than its
+ * child, two paths disagree on a parent, a path does not start at a root, or
+ * a node is on no path.  Nothing is launched in that case.
+ * ------------------------------------------------------------------------- */
+pt_status pt_build_blockmap_tree(const int32_t* node_lengths, int32_t n_nodes,
+                                 const int32_t* path_ptr, const int32_t* path_nodes,
+                                 int32_t n_samples, int32_t block_m, int32_t block_n,
+                                 cudaStream_t stream, pt_blockmap** out);
+
+/* ---------------------------------------------------------------------------
+ * pt_build_blockmap_seg -- block map from per-token segment labels.
+ *
+ * Passage: "prefix_grouper_kernel.py", PrefixSegInfo and
+ * build_seg_info_multigroup: per flat token a group id and a suffix id, -1 on
+ * the group's shared-prefix tokens, suffix ids unique across groups.
+ *
+ * group_id [T], suffix_id [T] (device int32).  Each maximal run of equal
+ * (group_id, suffix_id) is one tree node.  A run with suffix_id == -1 is its
+ * group's prompt and must open the group; completion runs are its children
+ * (roots when the group has no prompt).  Every group id and every suffix id
+ * forms exactly one contiguous run; ids lie in [0, T) (suffix ids may also be
+ * -1).  Errors: PT_ERR_INVALID_ARG for anything else, detected on the device
+ * and returned after the build synchronises the stream.
+ * ------------------------------------------------------------------------- */
+pt_status pt_build_blockmap_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T,
+                                int32_t block_m, int32_t block_n, cudaStream_t stream,
+                                pt_blockmap** out);
+
+/* ---------------------------------------------------------------------------
+ * pt_blockmap_dense -- the same tree with no tile skipping: every one of the
+ * nq x nk tiles is marked partial, so the kernels evaluate the mask on every
+ * pair of the T x T square.  This is the "dense masked O(T^2)" comparison the
+ * block-sparse map is measured against ("support sequence packing ..." and the
+ * drafter speed-up PR: the dense [B, 1, Q, KV] mask path it replaces).
+ * ------------------------------------------------------------------------- */
+pt_status pt_blockmap_dense(const pt_blockmap* src, cudaStream_t stream, pt_blockmap** out);
+
+/* Sizes of a map: T, nq = ceil(T / block_m), nk = ceil(T / block_n), the
+ * number of non-empty tiles and how many of them are full.  Any output
+ * pointer may be NULL. */
+pt_status pt_blockmap_info(const pt_blockmap* bm, int32_t* T, int32_t* block_m, int32_t* block_n,
+                           int32_t* nq, int32_t* nk, int64_t* nnz, int64_t* n_full);
+
+/* Host copies of the map, for tests: the q-major list (q_ptr [nq+1]; kv_idx
+ * and kind [nnz], kv blocks ascending within a q tile; kind 1 = full,
+ * 2 = partial) and its kv-major transpose (k_ptr [nk+1]; q_idx and kindT
+ * [nnz], q tiles ascending).  Every pointer is host memory sized by
+ * pt_blockmap_info; any may be NULL to skip it. */
+pt_status pt_blockmap_export(const pt_blockmap* bm, int32_t* q_ptr, int32_t* kv_idx, uint8_t* kind,
+                             int32_t* k_ptr, int32_t* q_idx, uint8_t* kindT);
+
+void pt_blockmap_free(pt_blockmap* bm);
+
+/* ---------------------------------------------------------------------------
+ * pt_attn_fwd -- O and LSE.
+ *
+ * Passage: "prefix_grouper_kernel.py", flex_shared_prefix_attention: softmax
+ * attention restricted to the kept pairs, scale 1/sqrt(head_dim) by default,
+ * identical in value to dense masked attention.
+ *
+ * Q [T,Hq,D], K/V [T,Hkv,D] (device, dtype).  O [T,Hq,D] (device, dtype);
+ * LSE [Hq,T] (device fp32): LSE = m + ln(sum exp(s - m)) over the kept scores
+ * s of the row.  scale <= 0 selects 1/sqrt(D).  The map must have been built
+ * for the same T.
+ * Supported: PT_BF16 with D in {64, 128, 256} and a 128 x 128 map (tensor
+ * cores); PT_F32 with 1 <= D <= 256 and any map (CUDA cores).  Hq % Hkv == 0.
+ * Anything else returns PT_ERR_UNSUPPORTED or PT_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtype, int32_t T,
+                      int32_t Hq, int32_t Hkv, int32_t D, float scale, const pt_blockmap* bm,
+                      void* O, float* LSE, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pt_attn_bwd -- dQ, dK, dV.
+ *
+ * Passage: the backward of the same attention ("prefix_grouper_kernel.py":
+ * the compiled backward; the drafter speed-up PR: the FlexAttention GQA
+ * backward).  With P = exp(s - LSE), Delta = rowsum(dO * O) and
+ * dS = P * (dO V^T - Delta): dV = sum P^T dO, dK = scale sum dS^T Q,
+ * dQ = scale dS K, with dK and dV summed over the q heads of each kv head.
+ *
+ * dO, Q, O [T,Hq,D]; K, V [T,Hkv,D]; LSE [Hq,T] fp32 as pt_attn_fwd wrote it
+ * (all device).  Outputs dQ [T,Hq,D], dK/dV [T,Hkv,D] (device, dtype).
+ * workspace: device scratch of at least pt_bwd_workspace_bytes(T, Hq, D)
+ * bytes, 256-byte aligned, owned by the caller; its contents on entry do not
+ * matter.  Calls that share one workspace must not overlap on the GPU.
+ * Supported shapes as for pt_attn_fwd.
+ * ------------------------------------------------------------------------- */
+pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+                      const float* LSE, pt_dtype dtype, int32_t T, int32_t Hq, int32_t Hkv,
+                      int32_t D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of scratch pt_attn_bwd needs: an fp32 dQ accumulator [T,Hq,D] and
+ * the fp32 row statistic Delta [Hq,T], each rounded up to 256 bytes. */
+size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
+
+/* Synchronise the stream, then return and clear the device status word:
+ * PT_ERR_TIMEOUT if an in-kernel wait ran out since the last check, PT_ERR_CUDA
+ * if the stream reported an error, else PT_OK. */
+pt_status pt_sync_status(cudaStream_t stream);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* pt_last_error(void);
+
+/* Number of kernel launches the library has issued in this process (all
+ * devices, all entry points).  Used by benchmarks to count launches. */
+uint64_t pt_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PT_H_ */

@@ -1,0 +1,251 @@
+"""prefix_tree_block_gb300 -- prefix-tree attention (forward and backward) for
+one NVIDIA GB300, as a C-ABI library (libpt.so, declared in include/pt.h)
+with this thin Python binding.
+
+The binding only marshals arguments: it passes raw device pointers and the
+current CUDA stream to the library and allocates outputs with PyTorch.  Every
+step of the computation runs in the library's CUDA kernels; if libpt.so is
+missing the calls raise, there is no other implementation behind them.
+Build the library with ``prefix_tree_block_gb300.build.build()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+__all__ = [
+    "PTError", "BlockMap", "load_library", "build_blockmap_tree", "build_blockmap_seg",
+    "attn_fwd", "attn_bwd", "bwd_workspace_bytes", "sync_status", "launch_count", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpt.so")
+
+PT_OK, PT_ERR_INVALID_ARG, PT_ERR_UNSUPPORTED, PT_ERR_CUDA, PT_ERR_TIMEOUT, PT_ERR_NOMEM = range(6)
+PT_BF16, PT_F32 = 0, 1
+_STATUS_NAMES = {0: "PT_OK", 1: "PT_ERR_INVALID_ARG", 2: "PT_ERR_UNSUPPORTED", 3: "PT_ERR_CUDA",
+                 4: "PT_ERR_TIMEOUT", 5: "PT_ERR_NOMEM"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PTError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def load_library(path: Optional[str] = None):
+    """Load libpt.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with prefix_tree_block_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        i32p, i64p = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+        sig = {
+            "pt_build_blockmap_tree": [vp, i32, vp, vp, i32, i32, i32, vp, pp],
+            "pt_build_blockmap_seg": [vp, vp, i32, i32, i32, vp, pp],
+            "pt_blockmap_dense": [vp, vp, pp],
+            "pt_blockmap_info": [vp, i32p, i32p, i32p, i32p, i32p, i64p, i64p],
+            "pt_blockmap_export": [vp, vp, vp, vp, vp, vp, vp],
+            "pt_attn_fwd": [vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp],
+            "pt_attn_bwd": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
+            "pt_sync_status": [vp],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.pt_blockmap_free.argtypes = [vp]
+        lib.pt_blockmap_free.restype = None
+        lib.pt_bwd_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.pt_bwd_workspace_bytes.restype = sz
+        lib.pt_last_error.argtypes = []
+        lib.pt_last_error.restype = ctypes.c_char_p
+        lib.pt_launch_count.argtypes = []
+        lib.pt_launch_count.restype = ctypes.c_uint64
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != PT_OK:
+        msg = load_library().pt_last_error()
+        raise PTError(rc, msg.decode() if msg else "")
+
+
+def _stream(stream=None) -> int:
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return int(t.data_ptr())
+
+
+class BlockMap:
+    """Owner of a device-resident block map built by the library."""
+
+    def __init__(self, handle: int):
+        self._h = ctypes.c_void_p(handle)
+        self._lib = load_library()
+        T, bm_, bn_, nq, nk = (ctypes.c_int32() for _ in range(5))
+        nnz, nfull = ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.pt_blockmap_info(self._h, ctypes.byref(T), ctypes.byref(bm_), ctypes.byref(bn_),
+                                          ctypes.byref(nq), ctypes.byref(nk), ctypes.byref(nnz), ctypes.byref(nfull)))
+        self.T, self.block_m, self.block_n = T.value, bm_.value, bn_.value
+        self.nq, self.nk, self.nnz, self.n_full = nq.value, nk.value, nnz.value, nfull.value
+
+    @property
+    def handle(self):
+        return self._h
+
+    def dense(self, stream=None) -> "BlockMap":
+        """The same tree with every tile marked partial (no skipping)."""
+        out = ctypes.c_void_p()
+        _check(self._lib.pt_blockmap_dense(self._h, ctypes.c_void_p(_stream(stream)), ctypes.byref(out)))
+        return BlockMap(out.value)
+
+    def export(self) -> dict:
+        """Host copies (numpy) of the q-major list and its kv-major transpose."""
+        import numpy as np
+
+        n = max(self.nnz, 1)
+        q_ptr = np.zeros(self.nq + 1, np.int32)
+        k_ptr = np.zeros(self.nk + 1, np.int32)
+        kv_idx = np.zeros(n, np.int32)
+        q_idx = np.zeros(n, np.int32)
+        kind = np.zeros(n, np.uint8)
+        kindT = np.zeros(n, np.uint8)
+        _check(self._lib.pt_blockmap_export(self._h, q_ptr.ctypes.data, kv_idx.ctypes.data, kind.ctypes.data,
+                                            k_ptr.ctypes.data, q_idx.ctypes.data, kindT.ctypes.data))
+        e = self.nnz
+        return dict(q_ptr=q_ptr, kv_idx=kv_idx[:e], kind=kind[:e], k_ptr=k_ptr, q_idx=q_idx[:e], kindT=kindT[:e],
+                    nnz=e, nq=self.nq, nk=self.nk)
+
+    def free(self):
+        if self._h is not None and self._h.value:
+            self._lib.pt_blockmap_free(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def build_blockmap_tree(node_lengths, path_ptr, path_nodes, block_m: int = 128, block_n: int = 128,
+                        stream=None) -> BlockMap:
+    """Block map from (node_lengths, CSR sample paths), all host int32 arrays."""
+    import numpy as np
+
+    lib = load_library()
+    nl = np.ascontiguousarray(np.asarray(node_lengths, dtype=np.int32))
+    pp = np.ascontiguousarray(np.asarray(path_ptr, dtype=np.int32))
+    pn = np.ascontiguousarray(np.asarray(path_nodes, dtype=np.int32))
+    out = ctypes.c_void_p()
+    _check(lib.pt_build_blockmap_tree(nl.ctypes.data if nl.size else None, int(nl.size), pp.ctypes.data,
+                                      pn.ctypes.data if pn.size else None, int(pp.size - 1), int(block_m),
+                                      int(block_n), ctypes.c_void_p(_stream(stream)), ctypes.byref(out)))
+    return BlockMap(out.value)
+
+
+def build_blockmap_seg(group_id, suffix_id, block_m: int = 128, block_n: int = 128, stream=None) -> BlockMap:
+    """Block map from per-token segment labels (CUDA int32 tensors [T])."""
+    import torch
+
+    lib = load_library()
+    for t in (group_id, suffix_id):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+            raise TypeError("group_id and suffix_id must be contiguous CUDA int32 tensors")
+    if group_id.numel() != suffix_id.numel():
+        raise ValueError("group_id and suffix_id differ in length")
+    out = ctypes.c_void_p()
+    T = int(group_id.numel())
+    _check(lib.pt_build_blockmap_seg(_ptr(group_id) if T else None, _ptr(suffix_id) if T else None, T,
+                                     int(block_m), int(block_n), ctypes.c_void_p(_stream(stream)),
+                                     ctypes.byref(out)))
+    return BlockMap(out.value)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return PT_BF16
+    if t.dtype == torch.float32:
+        return PT_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check_tensors(*ts):
+    import torch
+
+    dt = ts[0].dtype
+    for t in ts:
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+            raise TypeError("tensors must be contiguous CUDA tensors")
+        if t.dtype != dt:
+            raise TypeError("all tensors must share one dtype")
+
+
+def attn_fwd(Q, K, V, bm: BlockMap, scale: float = 0.0, O=None, LSE=None, stream=None) -> Tuple:
+    """O [T,Hq,D] and LSE [Hq,T] (fp32).  Q [T,Hq,D], K/V [T,Hkv,D]."""
+    import torch
+
+    _check_tensors(Q, K, V)
+    T, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty(Hq, T, dtype=torch.float32, device=Q.device)
+    lib = load_library()
+    _check(lib.pt_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _dtype_code(Q), T, Hq, Hkv, D, float(scale), bm.handle,
+                           _ptr(O), _ptr(LSE), ctypes.c_void_p(_stream(stream))))
+    return O, LSE
+
+
+def bwd_workspace_bytes(T: int, Hq: int, D: int) -> int:
+    return int(load_library().pt_bwd_workspace_bytes(int(T), int(Hq), int(D)))
+
+
+def attn_bwd(dO, Q, K, V, O, LSE, bm: BlockMap, scale: float = 0.0, dQ=None, dK=None, dV=None, workspace=None,
+             stream=None) -> Tuple:
+    """dQ [T,Hq,D], dK/dV [T,Hkv,D] from the upstream gradient dO."""
+    import torch
+
+    _check_tensors(dO, Q, K, V, O)
+    T, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    need = bwd_workspace_bytes(T, Hq, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    lib = load_library()
+    _check(lib.pt_attn_bwd(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _dtype_code(Q), T, Hq, Hkv, D,
+                           float(scale), bm.handle, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), ctypes.c_void_p(_stream(stream))))
+    return dQ, dK, dV
+
+
+def sync_status(stream=None):
+    """Synchronise and raise PTError if an in-kernel wait timed out."""
+    _check(load_library().pt_sync_status(ctypes.c_void_p(_stream(stream))))
+
+
+def launch_count() -> int:
+    return int(load_library().pt_launch_count())

@@ -1,0 +1,305 @@
+// pt_api.cu -- the extern "C" entry points declared in include/pt.h:
+// argument validation, error reporting, dispatch to the kernels, and the
+// TMA tensor-map helper.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pt.h"
+#include "pt_internal.h"
+
+namespace pt {
+
+namespace {
+thread_local char g_err[512] = "";
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+const char* g_err_ptr() { return g_err; }
+uint64_t launches() { return g_launches.load(std::memory_order_relaxed); }
+
+encode_tiled_fn get_encode_tiled() {
+  static encode_tiled_fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<encode_tiled_fn>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_thd(CUtensorMap* map, const void* base, int T, int H, int D, int rows) {
+  encode_tiled_fn enc = get_encode_tiled();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is unavailable from the driver");
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d) for T=%d H=%d D=%d", (int)r, T, H, D);
+    return false;
+  }
+  return true;
+}
+
+int num_sms(int device) {
+  static int cache[64] = {0};
+  if (device < 0 || device >= 64) return 148;
+  if (!cache[device]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device);
+    cache[device] = n > 0 ? n : 148;
+  }
+  return cache[device];
+}
+
+}  // namespace pt
+
+using pt::set_error;
+
+namespace {
+
+pt_status as_status(int rc) {
+  switch (rc) {
+    case 0: return PT_OK;
+    case 1: return PT_ERR_INVALID_ARG;
+    case 2: return PT_ERR_UNSUPPORTED;
+    case 4: return PT_ERR_TIMEOUT;
+    case 5: return PT_ERR_NOMEM;
+    default: return PT_ERR_CUDA;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared checks of the attention calls.
+pt_status check_attn(const char* who, pt_dtype dtype, int T, int Hq, int Hkv, int D, const pt_blockmap* bm,
+                     std::initializer_list<const void*> ptrs) {
+  if (!bm) {
+    set_error("%s: block map is NULL", who);
+    return PT_ERR_INVALID_ARG;
+  }
+  if (T != bm->T) {
+    set_error("%s: T = %d but the block map was built for T = %d", who, T, bm->T);
+    return PT_ERR_INVALID_ARG;
+  }
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) {
+    set_error("%s: Hq = %d must be a positive multiple of Hkv = %d", who, Hq, Hkv);
+    return PT_ERR_INVALID_ARG;
+  }
+  if (D <= 0 || D > 256) {
+    set_error("%s: head_dim %d outside 1..256", who, D);
+    return D <= 0 ? PT_ERR_INVALID_ARG : PT_ERR_UNSUPPORTED;
+  }
+  if (dtype != PT_BF16 && dtype != PT_F32) {
+    set_error("%s: unknown dtype %d", who, (int)dtype);
+    return PT_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != bm->device) {
+    set_error("%s: block map lives on device %d, current device is %d", who, bm->device, dev);
+    return PT_ERR_INVALID_ARG;
+  }
+  if (T == 0) return PT_OK;
+  for (const void* p : ptrs) {
+    if (!p) {
+      set_error("%s: a tensor pointer is NULL", who);
+      return PT_ERR_INVALID_ARG;
+    }
+    if (!aligned16(p)) {
+      set_error("%s: tensor pointers must be 16-byte aligned", who);
+      return PT_ERR_INVALID_ARG;
+    }
+  }
+  return PT_OK;
+}
+
+bool use_tensor_cores(pt_dtype dtype, int D, const pt_blockmap* bm) {
+  return dtype == PT_BF16 && (D == 64 || D == 128 || D == 256) && bm->BM == 128 && bm->BN == 128;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+pt_status pt_build_blockmap_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr,
+                                 const int32_t* path_nodes, int32_t n_samples, int32_t block_m, int32_t block_n,
+                                 cudaStream_t stream, pt_blockmap** out) {
+  if (!out) {
+    set_error("pt_build_blockmap_tree: out is NULL");
+    return PT_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  return as_status(pt::build_tree(node_lengths, n_nodes, path_ptr, path_nodes, n_samples, block_m, block_n, stream,
+                                  out));
+}
+
+pt_status pt_build_blockmap_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int32_t block_m,
+                                int32_t block_n, cudaStream_t stream, pt_blockmap** out) {
+  if (!out) {
+    set_error("pt_build_blockmap_seg: out is NULL");
+    return PT_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  return as_status(pt::build_seg(group_id, suffix_id, T, block_m, block_n, stream, out));
+}
+
+pt_status pt_blockmap_dense(const pt_blockmap* src, cudaStream_t stream, pt_blockmap** out) {
+  if (!src || !out) {
+    set_error("pt_blockmap_dense: NULL argument");
+    return PT_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  return as_status(pt::build_dense(src, stream, out));
+}
+
+pt_status pt_blockmap_info(const pt_blockmap* bm, int32_t* T, int32_t* block_m, int32_t* block_n, int32_t* nq,
+                           int32_t* nk, int64_t* nnz, int64_t* n_full) {
+  if (!bm) {
+    set_error("pt_blockmap_info: NULL map");
+    return PT_ERR_INVALID_ARG;
+  }
+  if (T) *T = bm->T;
+  if (block_m) *block_m = bm->BM;
+  if (block_n) *block_n = bm->BN;
+  if (nq) *nq = bm->nq;
+  if (nk) *nk = bm->nk;
+  if (nnz) *nnz = bm->nnz;
+  if (n_full) *n_full = bm->n_full;
+  return PT_OK;
+}
+
+pt_status pt_blockmap_export(const pt_blockmap* bm, int32_t* q_ptr, int32_t* kv_idx, uint8_t* kind, int32_t* k_ptr,
+                             int32_t* q_idx, uint8_t* kindT) {
+  if (!bm) {
+    set_error("pt_blockmap_export: NULL map");
+    return PT_ERR_INVALID_ARG;
+  }
+  struct Item {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } items[] = {
+      {q_ptr, bm->q_ptr, sizeof(int32_t) * (bm->nq + 1)}, {kv_idx, bm->kv_idx, sizeof(int32_t) * bm->nnz},
+      {kind, bm->kind, (size_t)bm->nnz},                  {k_ptr, bm->k_ptr, sizeof(int32_t) * (bm->nk + 1)},
+      {q_idx, bm->q_idx, sizeof(int32_t) * bm->nnz},      {kindT, bm->kindT, (size_t)bm->nnz},
+  };
+  for (const Item& it : items) {
+    if (!it.dst || it.bytes == 0) continue;
+    cudaError_t e = cudaMemcpy(it.dst, it.src, it.bytes, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+      set_error("pt_blockmap_export: %s", cudaGetErrorString(e));
+      return PT_ERR_CUDA;
+    }
+  }
+  return PT_OK;
+}
+
+void pt_blockmap_free(pt_blockmap* bm) { pt::free_map(bm); }
+
+pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtype, int32_t T, int32_t Hq,
+                      int32_t Hkv, int32_t D, float scale, const pt_blockmap* bm, void* O, float* LSE,
+                      cudaStream_t stream) {
+  pt_status st = check_attn("pt_attn_fwd", dtype, T, Hq, Hkv, D, bm, {Q, K, V, O, LSE});
+  if (st != PT_OK || T == 0) return st;
+  if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)D);
+  if (dtype == PT_BF16) {
+    if (use_tensor_cores(dtype, D, bm))
+      return as_status(pt::fwd_tc(Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, stream));
+    if (D % 8 != 0) {
+      set_error("pt_attn_fwd: bf16 needs head_dim %% 8 == 0 (got %d)", D);
+      return PT_ERR_UNSUPPORTED;
+    }
+    return as_status(pt::fwd_simt(true, Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, stream));
+  }
+  return as_status(pt::fwd_simt(false, Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, stream));
+}
+
+size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D) {
+  if (T <= 0 || Hq <= 0 || D <= 0) return 256;
+  return round256(sizeof(float) * (size_t)T * Hq * D) + round256(sizeof(float) * (size_t)T * Hq);
+}
+
+pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                      pt_dtype dtype, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float scale,
+                      const pt_blockmap* bm, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  pt_status st = check_attn("pt_attn_bwd", dtype, T, Hq, Hkv, D, bm, {dO, Q, K, V, O, LSE, dQ, dK, dV});
+  if (st != PT_OK || T == 0) return st;
+  size_t need = pt_bwd_workspace_bytes(T, Hq, D);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+    set_error("pt_attn_bwd: workspace must be 256-byte aligned and hold %zu bytes (got %zu)", need,
+              workspace_bytes);
+    return PT_ERR_INVALID_ARG;
+  }
+  if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)D);
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(sizeof(float) * (size_t)T * Hq * D));
+  if (dtype == PT_BF16) {
+    if (use_tensor_cores(dtype, D, bm))
+      return as_status(pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, dq_acc, delta, stream));
+    if (D % 8 != 0) {
+      set_error("pt_attn_bwd: bf16 needs head_dim %% 8 == 0 (got %d)", D);
+      return PT_ERR_UNSUPPORTED;
+    }
+    return as_status(pt::bwd_simt(true, dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, stream));
+  }
+  return as_status(pt::bwd_simt(false, dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, stream));
+}
+
+pt_status pt_sync_status(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    set_error("pt_sync_status: %s", cudaGetErrorString(e));
+    return PT_ERR_CUDA;
+  }
+  int worst = 0;
+  int codes[] = {pt::take_status_blockmap(stream), pt::take_status_fwd(stream), pt::take_status_bwd(stream),
+                 pt::take_status_simt(stream)};
+  for (int c : codes) {
+    if (c < 0) {
+      set_error("pt_sync_status: could not read the device status word");
+      return PT_ERR_CUDA;
+    }
+    if (c && !worst) worst = c;
+  }
+  if (worst == PT_STATUS_TIMEOUT) {
+    set_error("a bounded in-kernel wait ran out");
+    return PT_ERR_TIMEOUT;
+  }
+  if (worst) {
+    set_error("device status %d", worst);
+    return PT_ERR_CUDA;
+  }
+  return PT_OK;
+}
+
+const char* pt_last_error(void) { return pt::g_err_ptr(); }
+
+uint64_t pt_launch_count(void) { return pt::launches(); }
+
+}  // extern "C"

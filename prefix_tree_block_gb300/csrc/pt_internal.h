@@ -1,0 +1,100 @@
+// pt_internal.h -- definitions shared by the library's translation units
+// (host and device).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define PT_STATUS_OK 0
+#define PT_STATUS_INVALID 1
+#define PT_STATUS_TIMEOUT 4
+
+// Kinds of a (q tile, kv block) pair in the block map.
+#define PT_KIND_EMPTY 0
+#define PT_KIND_FULL 1
+#define PT_KIND_PARTIAL 2
+
+// Per-token tree coordinates.  A node's Euler-tour interval [tin, tout)
+// contains exactly the intervals of its descendants, so "node(kv) is an
+// ancestor-or-self of node(q)" is tin(kv) <= tin(q) < tout(kv).  Padding
+// tokens past T carry (INT32_MAX, 0): they keep nothing and nothing keeps them.
+struct pt_tok {
+  int32_t tin;
+  int32_t tout;
+};
+
+struct pt_blockmap {
+  int device;
+  int32_t T, BM, BN, nq, nk;
+  int32_t n_nodes;
+  int32_t tpad;  // entries of tok: max(nq*BM, nk*BN)
+  int64_t nnz, n_full;
+  bool dense;
+  pt_tok* tok;          // [tpad]
+  int32_t* node_of;     // [T]
+  int32_t* node_start;  // [n_nodes]
+  int32_t* node_end;    // [n_nodes]
+  int32_t* parent;      // [n_nodes], -1 for roots
+  // q-major list
+  int32_t* q_ptr;   // [nq + 1]
+  int32_t* kv_idx;  // [nnz]
+  uint8_t* kind;    // [nnz]
+  // kv-major transpose
+  int32_t* k_ptr;   // [nk + 1]
+  int32_t* q_idx;   // [nnz]
+  uint8_t* kindT;   // [nnz]
+  // longest-first processing orders
+  int32_t* q_order;  // [nq] q tiles, most kv blocks first
+  int32_t* k_order;  // [nk] kv blocks, most q tiles first
+};
+
+namespace pt {
+
+// Thread-local error message setter (pt_api.cu).
+void set_error(const char* fmt, ...);
+
+// Launch counter (pt_api.cu).
+void count_launch(int n = 1);
+
+// Device status word of each translation unit: read and clear.
+int take_status_blockmap(cudaStream_t s);
+int take_status_fwd(cudaStream_t s);
+int take_status_bwd(cudaStream_t s);
+int take_status_simt(cudaStream_t s);
+
+// Block-map builders (pt_blockmap.cu).  Return a PT_* status code.
+int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,
+               int32_t n_samples, int32_t BM, int32_t BN, cudaStream_t s, pt_blockmap** out);
+int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int32_t BM, int32_t BN,
+              cudaStream_t s, pt_blockmap** out);
+int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out);
+void free_map(pt_blockmap* bm);
+
+// Tensor-core bf16 kernels (pt_fwd_tc.cu, pt_bwd_tc.cu).
+int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
+           const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s);
+int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
+           int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* dq_acc,
+           float* delta, cudaStream_t s);
+
+// CUDA-core kernels (pt_simt.cu), fp32 or bf16 storage with fp32 math.
+int fwd_simt(bool bf16, const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
+             const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s);
+int bwd_simt(bool bf16, const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+             int T, int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV,
+             float* delta, cudaStream_t s);
+
+// Driver entry point for tensor-map encoding (pt_api.cu).
+typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+encode_tiled_fn get_encode_tiled();
+
+// A [T, H, D] bf16 tensor as a 3-D TMA map with boxes of 64 (d) x 1 (head) x
+// rows (tokens), 128-byte swizzle.  Returns false (and sets the error) on failure.
+bool make_tmap_thd(CUtensorMap* map, const void* base, int T, int H, int D, int rows);
+
+int num_sms(int device);
+
+}  // namespace pt

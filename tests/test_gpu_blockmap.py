@@ -1,0 +1,78 @@
+"""Block map on the GPU vs the oracle's brute-force map: bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import prefix_tree_block_gb300 as pt
+from oracle import oracle as orc
+from prefix_tree_block_gb300 import workloads as W
+from parity import compare_blockmap, ensure_built, gpu_blockmap
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+@pytest.mark.parametrize("c", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("form", ["tree", "seg"])
+def test_workload_blockmaps(c, form):
+    st = W.config_structure(c)
+    if form == "seg" and st.group_id is None:
+        pytest.skip("depth-3 tree has no segment form")
+    BM = BN = 16 if c == 1 else 128
+    got = gpu_blockmap(st, BM, BN, form)
+    want = orc.blockmap(orc.structure_labels(st), BM, BN)
+    compare_blockmap(got.export(), want)
+    assert got.n_full == int((want["kind"] == 1).sum())
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_trees(seed):
+    rng = np.random.default_rng(500 + seed)
+    st = W.random_tree(rng, n_nodes=int(rng.integers(1, 30)), max_len=int(rng.integers(1, 300)))
+    if st.T == 0:
+        pytest.skip("empty")
+    BM, BN = [(128, 128), (16, 16), (64, 32), (32, 128)][seed % 4]
+    want = orc.blockmap(orc.structure_labels(st), BM, BN)
+    compare_blockmap(gpu_blockmap(st, BM, BN).export(), want)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_grpo_seg_form(seed):
+    rng = np.random.default_rng(900 + seed)
+    specs = [(int(rng.integers(0, 400)), [int(x) for x in rng.integers(1, 300, int(rng.integers(1, 6)))])
+             for _ in range(int(rng.integers(1, 4)))]
+    st = W.grpo_structure(specs)
+    want = orc.blockmap(orc.seg_labels(st.group_id, st.suffix_id), 128, 128)
+    compare_blockmap(gpu_blockmap(st, 128, 128, "seg").export(), want)
+
+
+@pytest.mark.parametrize("g,s", [
+    ([0, 0, 0, 0], [1, 1, -1, -1]),
+    ([0, 0, 1, 1, 0], [-1, -1, -1, -1, -1]),
+    ([0, 0, 0, 1, 1], [-1, 3, 3, 4, 3]),
+    ([0, 0, 0], [-1, 2, -1]),
+    ([0, 7, 7], [-1, -1, -1]),  # group id out of [0, T)
+])
+def test_invalid_segments_rejected(g, s):
+    with pytest.raises(pt.PTError) as ei:
+        pt.build_blockmap_seg(torch.tensor(g, dtype=torch.int32).cuda(), torch.tensor(s, dtype=torch.int32).cuda())
+    assert ei.value.status == pt.PT_ERR_INVALID_ARG
+
+
+def test_dense_map_lists_every_tile():
+    st = W.grpo_structure([(300, [100, 50])])
+    d = gpu_blockmap(st).dense().export()
+    nq = nk = -(-st.T // 128)
+    assert d["nnz"] == nq * nk
+    assert (d["kind"] == 2).all()
+    np.testing.assert_array_equal(d["q_ptr"], np.arange(nq + 1) * nk)
+
+
+def test_empty_layout():
+    st = W.grpo_structure([(0, [0])])
+    bm = gpu_blockmap(st)
+    assert bm.T == 0 and bm.nnz == 0

@@ -1,0 +1,79 @@
+"""Backward parity: dQ, dK, dV vs the fp64 oracle (relative L2 norm), at
+small sizes over all elements and at the workload sizes on sampled rows and
+kv columns plus the sum invariants that hold at any size."""
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+from prefix_tree_block_gb300 import workloads as W
+from parity import GRAD_RL2, ensure_built, rel_l2, run_bwd, sample_rows
+from test_gpu_fwd import small_structures
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def check_bwd(st, Hq, Hkv, D, dtype, seed, **kw):
+    (q, k, v, do), (dQ, dK, dV) = run_bwd(st, Hq, Hkv, D, dtype, seed, **kw)
+    wq, wk, wv = orc.attn_bwd(q, k, v, do, orc.structure_labels(st))
+    errs = (rel_l2(dQ, wq), rel_l2(dK, wk), rel_l2(dV, wv))
+    assert max(errs) <= GRAD_RL2[dtype], errs
+    return errs
+
+
+def test_fp32_workload1():
+    cfg = W.CONFIGS[1]
+    check_bwd(W.config_structure(1), cfg["Hq"], cfg["Hkv"], cfg["D"], "f32", seed=1, BM=16, BN=16)
+
+
+@pytest.mark.parametrize("BM,BN", [(16, 16), (32, 64)])
+def test_fp32_random_tree(BM, BN):
+    rng = np.random.default_rng(77 + BM)
+    st = W.random_tree(rng, n_nodes=9, max_len=50)
+    check_bwd(st, 4, 2, 40, "f32", seed=4, BM=BM, BN=BN)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("name", ["grpo", "grpo_p0", "tree", "docs"])
+def test_tensor_core_bwd_small(D, name):
+    check_bwd(small_structures()[name], 4, 2, D, "bf16", seed=D + 1)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (8, 1)])
+def test_tensor_core_bwd_gqa(Hq, Hkv):
+    check_bwd(small_structures()["grpo"], Hq, Hkv, 128, "bf16", seed=Hq + 2)
+
+
+def test_tensor_core_bwd_dense_map_equal():
+    check_bwd(small_structures()["tree"], 2, 1, 64, "bf16", seed=6, dense=True)
+
+
+@pytest.mark.parametrize("c", [2, 3, 4, 5])
+def test_workload_sampled(c):
+    cfg = W.CONFIGS[c]
+    st = W.config_structure(c)
+    Hq, Hkv, D = cfg["Hq"], cfg["Hkv"], cfg["D"]
+    (q, k, v, do), (dQ, dK, dV) = run_bwd(st, Hq, Hkv, D, "bf16", seed=c)
+    lab = orc.structure_labels(st)
+    rows = sample_rows(st, st.T, n_random=24, seed=c)
+    wq, _, _ = orc.attn_bwd(q, k, v, do, lab, qrows=rows, want_dkv=False)
+    assert rel_l2(dQ[rows], wq) <= GRAD_RL2["bf16"]
+    # kv columns: the last token of each node (few rows see it) plus a few
+    starts = np.concatenate([[0], np.cumsum(st.node_lengths)[:-1]]).astype(int)
+    ends = [int(s + n - 1) for s, n in zip(starts, st.node_lengths) if n > 0]
+    rng = np.random.default_rng(c)
+    cols = np.array(sorted(set(list(rng.choice(ends, min(8, len(ends)), replace=False)) + [st.T - 1])), np.int64)
+    _, wk, wv = orc.attn_bwd(q, k, v, do, lab, kvcols=cols, want_dq=False)
+    assert rel_l2(dK[cols], wk) <= GRAD_RL2["bf16"]
+    assert rel_l2(dV[cols], wv) <= GRAD_RL2["bf16"]
+    # invariants at full size: sum_j dK_j = 0 and sum_j dV_j = sum of dO over
+    # rows and the kv head's q heads
+    g = Hq // Hkv
+    sdo = do.float().numpy().astype(np.float64).reshape(st.T, Hkv, g, D).sum(axis=(0, 2))
+    assert rel_l2(dV.sum(axis=0), sdo) <= GRAD_RL2["bf16"]
+    scale_k = np.abs(dK).sum(axis=0).max()
+    assert np.abs(dK.sum(axis=0)).max() <= 1e-2 * scale_k
