@@ -1,0 +1,359 @@
+#!/usr/bin/env python
+"""Benchmark: prefix-tree attention forward + backward, useful TFLOP/s.
+
+A step is one pass of the whole path over one batch of synthetic input:
+block map from the tree (labels + tile classes + lists), forward (O, LSE) and
+backward (Delta preprocess, dK/dV, dQ).  Useful work per step is
+4*D*Hq*pairs (forward) + 10*D*Hq*pairs (backward), where pairs is the number
+of kept (q, kv) token pairs per head; masked pairs inside partial tiles are
+not counted.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C] [--impl ours|reference]
+
+One JSON line is printed by rank 0.  Multi-GPU runs (torchrun, one process
+per GPU) run one replica of the workload per GPU: the groups of the path are
+independent, so nothing is exchanged on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefix-tree attn fwd+bwd useful TFLOP/s (unmasked pairs), % of bf16 peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def useful_pairs(st) -> int:
+    """Kept (q, kv) pairs per head, from the tree: each node's own causal
+    triangle plus its tokens times all ancestor tokens."""
+    parent = {}
+    for p in st.paths():
+        for a, b in zip(p[:-1], p[1:]):
+            parent[b] = a
+    total = 0
+    for n, ln in enumerate(int(x) for x in st.node_lengths):
+        anc = 0
+        a = parent.get(n)
+        while a is not None:
+            anc += int(st.node_lengths[a])
+            a = parent.get(a)
+        total += ln * (ln + 1) // 2 + ln * anc
+    return total
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names[1:], parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_run(st, cfg, seed, max_units=None):
+    """Run the fp64 oracle forward + backward on a prefix of the workload's
+    independent units (whole groups / documents) and return (useful flops, seconds,
+    threads, description)."""
+    from oracle import oracle as orc
+    from prefix_tree_block_gb300 import workloads as W
+
+    Hq, Hkv, D = cfg["Hq"], cfg["Hkv"], cfg["D"]
+    if "group_specs" in st.meta:
+        specs = st.meta["group_specs"][: max_units or len(st.meta["group_specs"])]
+        sub = W.grpo_structure(specs)
+        what = f"{len(specs)} of {len(st.meta['group_specs'])} groups"
+    elif "doc_lengths" in st.meta:
+        docs = st.meta["doc_lengths"][: max_units or len(st.meta["doc_lengths"])]
+        sub = W.docs_structure(docs)
+        what = f"{len(docs)} of {len(st.meta['doc_lengths'])} documents"
+    else:
+        sub = st
+        what = "the whole tree"
+    q, k, v, do = W.make_tensors(sub.T, Hq, Hkv, D, cfg["dtype"], seed)
+    lab = orc.structure_labels(sub)
+    nth = orc.default_threads()
+    t0 = time.perf_counter()
+    orc.attn_fwd(q, k, v, lab, n_threads=nth)
+    orc.attn_bwd(q, k, v, do, lab, n_threads=nth)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * D * Hq * useful_pairs(sub)
+    return flops, dt, nth, f"fp64 oracle forward+backward over {what} (T={sub.T}) of the workload, all {Hq} heads"
+
+
+def run_reference(args, cfg, st):
+    """The reference arm: the fp64 CPU oracle, timed on this host's cores, on
+    a bounded sample (one group) per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_oracle_run(st, cfg, args.workload, max_units=1)
+    flops = secs = 0.0
+    desc, nth = "", 1
+    for _ in range(args.steps):
+        f, s, nth, desc = cpu_oracle_run(st, cfg, args.workload, max_units=1)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["name"], "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nth, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, help="workload 1..5 (default 2: GRPO batch)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from prefix_tree_block_gb300 import workloads as W
+
+    cfg = dict(W.CONFIGS[args.workload])
+    st = W.config_structure(args.workload)
+    if args.impl == "reference":
+        run_reference(args, cfg, st)
+        return
+
+    import torch
+
+    import prefix_tree_block_gb300 as pt
+    from prefix_tree_block_gb300 import build as ptbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        ptbuild.build()
+    if dist is not None:
+        dist.barrier()
+    pt.load_library()
+
+    Hq, Hkv, D, dtype = cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["dtype"]
+    T = st.T
+    pairs = useful_pairs(st)
+    flops_fwd = 4.0 * D * Hq * pairs
+    flops_step = flops_fwd * 3.5
+    q, k, v, do = W.make_tensors(T, Hq, Hkv, D, dtype, args.workload)
+    dev = torch.device("cuda", local)
+    Q, K, V, dO = (x.to(dev) for x in (q, k, v, do))
+    O = torch.empty_like(Q)
+    LSE = torch.empty(Hq, T, dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ws = torch.empty(pt.bwd_workspace_bytes(T, Hq, D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    nl, pp, pn = st.node_lengths, st.path_ptr, st.path_nodes
+    stream = torch.cuda.current_stream()
+
+    def step(dense=False):
+        bm = pt.build_blockmap_tree(nl, pp, pn, 128, 128)
+        if dense:
+            d = bm.dense()
+            bm.free()
+            bm = d
+        pt.attn_fwd(Q, K, V, bm, O=O, LSE=LSE)
+        pt.attn_bwd(dO, Q, K, V, O, LSE, bm, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+        bm.free()
+
+    for _ in range(args.warmup):
+        step()
+    pt.sync_status()
+
+    def timed(n, fn):
+        evs = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # ---- device-resident timed region ---------------------------------------
+    sampler = ClockSampler(local)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = pt.launch_count()
+    pt.profile_reset()
+    pt.profile_enable(True)
+    times = timed(args.steps, step)
+    pt.profile_enable(False)
+    launches = pt.launch_count() - launches0
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    pt.sync_status()
+    total_ms = sum(times)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+
+    kernels = {}
+    for name in ("blockmap_classify", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dq", "bwd_simt"):
+        n, ms = pt.profile_read(name)
+        if n:
+            kernels[name] = {"launches": n, "ms_per_launch": ms / n}
+    pt.profile_reset()
+
+    # ---- roofline of the dominant kernel -----------------------------------
+    peak_tf, peak_gbs, peak_src = peaks()
+    per_launch_flops = {  # executed useful-pair flops of each kernel
+        "fwd_tc": 4.0 * D * Hq * pairs,
+        "bwd_dkdv": 8.0 * D * Hq * pairs,
+        "bwd_dq": 6.0 * D * Hq * pairs,
+    }
+    tc = {k: v for k, v in kernels.items() if k in per_launch_flops}
+    roofline = None
+    if tc:
+        dom = max(tc, key=lambda k: tc[k]["ms_per_launch"])
+        ach = per_launch_flops[dom] / (tc[dom]["ms_per_launch"] * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": ach / peak_tf, "traffic": None, "peak_source": f"{peak_src} bf16 burst"}
+
+    # ---- dense-masked comparison (same kernels, every tile partial) ---------
+    dense = None
+    if not args.no_dense:
+        step(dense=True)
+        dt = timed(max(2, min(5, args.steps)), lambda: step(dense=True))
+        dense = {"ms_per_step": sum(dt) / len(dt), "speedup": (sum(dt) / len(dt)) / ms_step}
+
+    # ---- end to end through the C ABI with host buffers ---------------------
+    hq, hk, hv, hdo = (x.pin_memory() for x in (q, k, v, do))
+    hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (Q, K, V))
+
+    def e2e_step():
+        Q.copy_(hq, non_blocking=True)
+        K.copy_(hk, non_blocking=True)
+        V.copy_(hv, non_blocking=True)
+        dO.copy_(hdo, non_blocking=True)
+        step()
+        hdq.copy_(dQ, non_blocking=True)
+        hdk.copy_(dK, non_blocking=True)
+        hdv.copy_(dV, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    et = timed(args.steps, e2e_step)
+    e2e_ms = sum(et)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do)) + 4 * (nl.size + pp.size + pn.size)
+    d2h = sum(x.numel() * x.element_size() for x in (dQ, dK, dV))
+    e2e = {"value": world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, s, nth, desc = cpu_oracle_run(st, cfg, args.workload)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": nth, "kind": "oracle", "sample": desc,
+               "seconds": s}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "frac_of_peak": value / world / peak_tf,
+            "config": {"workload": cfg["name"], "T": T, "Hq": Hq, "Hkv": Hkv, "head_dim": D,
+                       "useful_pairs_per_head": pairs, "useful_tflop_per_step": flops_step / 1e12,
+                       "tiles": "128x128", "l2": "flushed before every step (256 MB write, untimed)",
+                       "parallelism": f"replicas x{world}"},
+            "kernels": kernels, "roofline": roofline, "dense_masked": dense, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

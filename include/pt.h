@@ -175,8 +175,10 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
                       int32_t D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Bytes of scratch pt_attn_bwd needs: an fp32 dQ accumulator [T,Hq,D] and
- * the fp32 row statistic Delta [Hq,T], each rounded up to 256 bytes. */
+/* Bytes of scratch pt_attn_bwd needs: two fp32 row statistics of [Hq, Tpad]
+ * entries each, Tpad = ceil(T / 128) * 128 -- Delta = rowsum(dO * O) and
+ * LSE * log2(e) -- each rounded up to 256 bytes.  D is accepted for future
+ * layouts and does not change the size today. */
 size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
 
 /* Synchronise the stream, then return and clear the device status word:
@@ -190,6 +192,18 @@ const char* pt_last_error(void);
 /* Number of kernel launches the library has issued in this process (all
  * devices, all entry points).  Used by benchmarks to count launches. */
 uint64_t pt_launch_count(void);
+
+/* Optional per-kernel timing, for benchmarks and profiling.  While enabled,
+ * each kernel launch is bracketed by two CUDA events on its stream (a few
+ * microseconds of overhead per launch); disabled (the default) costs one
+ * branch.  pt_profile_read synchronises the recorded events and returns the
+ * number of launches and their summed duration for one kernel name:
+ * "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dq", "bwd_simt",
+ * "blockmap_classify" (the whole tail of a block-map build).
+ * pt_profile_reset drops every record. */
+void pt_profile_enable(int on);
+pt_status pt_profile_read(const char* kernel, int64_t* launches, double* total_ms);
+void pt_profile_reset(void);
 
 #ifdef __cplusplus
 }

@@ -18,6 +18,7 @@ from typing import Optional, Tuple
 __all__ = [
     "PTError", "BlockMap", "load_library", "build_blockmap_tree", "build_blockmap_seg",
     "attn_fwd", "attn_bwd", "bwd_workspace_bytes", "sync_status", "launch_count", "LIB_PATH",
+    "profile_enable", "profile_read", "profile_reset",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpt.so")
@@ -72,6 +73,12 @@ def load_library(path: Optional[str] = None):
         lib.pt_last_error.restype = ctypes.c_char_p
         lib.pt_launch_count.argtypes = []
         lib.pt_launch_count.restype = ctypes.c_uint64
+        lib.pt_profile_enable.argtypes = [ctypes.c_int]
+        lib.pt_profile_enable.restype = None
+        lib.pt_profile_read.argtypes = [ctypes.c_char_p, i64p, ctypes.POINTER(ctypes.c_double)]
+        lib.pt_profile_read.restype = ctypes.c_int
+        lib.pt_profile_reset.argtypes = []
+        lib.pt_profile_reset.restype = None
         _lib = lib
         return lib
 
@@ -249,3 +256,19 @@ def sync_status(stream=None):
 
 def launch_count() -> int:
     return int(load_library().pt_launch_count())
+
+
+def profile_enable(on: bool = True):
+    """Start (or stop) per-kernel CUDA-event timing inside the library."""
+    load_library().pt_profile_enable(1 if on else 0)
+
+
+def profile_read(kernel: str):
+    """(launches, total milliseconds) recorded for one kernel name."""
+    n, ms = ctypes.c_int64(), ctypes.c_double()
+    _check(load_library().pt_profile_read(kernel.encode(), ctypes.byref(n), ctypes.byref(ms)))
+    return int(n.value), float(ms.value)
+
+
+def profile_reset():
+    load_library().pt_profile_reset()

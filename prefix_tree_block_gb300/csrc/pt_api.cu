@@ -6,7 +6,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "../../include/pt.h"
 #include "pt_internal.h"
@@ -28,6 +31,33 @@ void set_error(const char* fmt, ...) {
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 const char* g_err_ptr() { return g_err; }
 uint64_t launches() { return g_launches.load(std::memory_order_relaxed); }
+
+namespace {
+struct ProfRecord {
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pairs;
+};
+std::mutex g_prof_mu;
+std::atomic<bool> g_prof_on{false};
+std::map<std::string, ProfRecord> g_prof;
+}  // namespace
+
+ProfScope::ProfScope(cudaStream_t s, const char* n) : stream(s), name(n), end_event(nullptr) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  cudaEvent_t a, b;
+  if (cudaEventCreate(&a) != cudaSuccess) return;
+  if (cudaEventCreate(&b) != cudaSuccess) {
+    cudaEventDestroy(a);
+    return;
+  }
+  cudaEventRecord(a, s);
+  end_event = b;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof[name].pairs.emplace_back(a, b);
+}
+
+ProfScope::~ProfScope() {
+  if (end_event) cudaEventRecord(static_cast<cudaEvent_t>(end_event), stream);
+}
 
 encode_tiled_fn get_encode_tiled() {
   static encode_tiled_fn fn = nullptr;
@@ -240,8 +270,10 @@ pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtyp
 }
 
 size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D) {
-  if (T <= 0 || Hq <= 0 || D <= 0) return 256;
-  return round256(sizeof(float) * (size_t)T * Hq * D) + round256(sizeof(float) * (size_t)T * Hq);
+  (void)D;
+  if (T <= 0 || Hq <= 0) return 256;
+  const size_t tpad = ((size_t)T + 127) / 128 * 128;
+  return 2 * round256(sizeof(float) * tpad * Hq);
 }
 
 pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
@@ -257,11 +289,12 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
     return PT_ERR_INVALID_ARG;
   }
   if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)D);
-  float* dq_acc = static_cast<float*>(workspace);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(sizeof(float) * (size_t)T * Hq * D));
+  const size_t tpad = ((size_t)T + 127) / 128 * 128;
+  float* delta = static_cast<float*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(sizeof(float) * tpad * Hq));
   if (dtype == PT_BF16) {
-    if (use_tensor_cores(dtype, D, bm))
-      return as_status(pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, dq_acc, delta, stream));
+    if (use_tensor_cores(dtype, D, bm) && pt::bwd_tc_supported(D))
+      return as_status(pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, lse2, stream));
     if (D % 8 != 0) {
       set_error("pt_attn_bwd: bf16 needs head_dim %% 8 == 0 (got %d)", D);
       return PT_ERR_UNSUPPORTED;
@@ -301,5 +334,43 @@ pt_status pt_sync_status(cudaStream_t stream) {
 const char* pt_last_error(void) { return pt::g_err_ptr(); }
 
 uint64_t pt_launch_count(void) { return pt::launches(); }
+
+void pt_profile_enable(int on) { pt::g_prof_on.store(on != 0); }
+
+pt_status pt_profile_read(const char* kernel, int64_t* launches, double* total_ms) {
+  if (!kernel) {
+    set_error("pt_profile_read: NULL kernel name");
+    return PT_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lk(pt::g_prof_mu);
+  int64_t n = 0;
+  double ms = 0.0;
+  auto it = pt::g_prof.find(kernel);
+  if (it != pt::g_prof.end()) {
+    for (auto& pr : it->second.pairs) {
+      if (cudaEventSynchronize(pr.second) != cudaSuccess) {
+        set_error("pt_profile_read: event failed");
+        return PT_ERR_CUDA;
+      }
+      float t = 0.f;
+      cudaEventElapsedTime(&t, pr.first, pr.second);
+      ms += t;
+      ++n;
+    }
+  }
+  if (launches) *launches = n;
+  if (total_ms) *total_ms = ms;
+  return PT_OK;
+}
+
+void pt_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(pt::g_prof_mu);
+  for (auto& kv : pt::g_prof)
+    for (auto& pr : kv.second.pairs) {
+      cudaEventDestroy(pr.first);
+      cudaEventDestroy(pr.second);
+    }
+  pt::g_prof.clear();
+}
 
 }  // extern "C"

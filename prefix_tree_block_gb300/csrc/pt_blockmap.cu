@@ -335,6 +335,7 @@ void lpt_order(const std::vector<int>& cnt, std::vector<int>& order) {
 // Shared tail of every builder: given tok, node_of and node tables on the
 // device, classify, count, list and order.
 int finish_map(pt_blockmap* bm, cudaStream_t s) {
+  ProfScope ps(s, "blockmap_classify");
   const int nq = bm->nq, nk = bm->nk;
   const long long ntiles = (long long)nq * nk;
   uint8_t* kinds = nullptr;

@@ -435,7 +435,10 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
   const int n_items = bm->nq * Hq;
   const int grid = n_items < num_sms(dev) ? n_items : num_sms(dev);
   if (grid <= 0) return 0;
-  k_fwd_tc<D><<<grid, 192, C::SMEM_BYTES, s>>>(mQ, mK, mV, p);
+  {
+    ProfScope ps(s, "fwd_tc");
+    k_fwd_tc<D><<<grid, 192, C::SMEM_BYTES, s>>>(mQ, mK, mV, p);
+  }
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -57,6 +57,18 @@ void set_error(const char* fmt, ...);
 // Launch counter (pt_api.cu).
 void count_launch(int n = 1);
 
+// Optional per-kernel timing (pt_api.cu).  While enabled with
+// pt_profile_enable(1), every kernel launch site brackets its launch with a
+// pair of CUDA events on the launching stream; pt_profile_read() sums them.
+// Disabled (the default), a scope costs one branch.
+struct ProfScope {
+  ProfScope(cudaStream_t s, const char* name);
+  ~ProfScope();
+  cudaStream_t stream;
+  const char* name;
+  void* end_event;
+};
+
 // Device status word of each translation unit: read and clear.
 int take_status_blockmap(cudaStream_t s);
 int take_status_fwd(cudaStream_t s);
@@ -75,8 +87,9 @@ void free_map(pt_blockmap* bm);
 int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
            const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s);
 int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
-           int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* dq_acc,
-           float* delta, cudaStream_t s);
+           int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
+           float* lse2, cudaStream_t s);
+bool bwd_tc_supported(int D);
 
 // CUDA-core kernels (pt_simt.cu), fp32 or bf16 storage with fp32 math.
 int fwd_simt(bool bf16, const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,

@@ -220,6 +220,7 @@ template <class E>
 int fwd_impl(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
              const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
   const int block = 256;
+  ProfScope ps(s, "fwd_simt");
   k_fwd<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
       (const E*)Q, (const E*)K, (const E*)V, T, Hq, Hkv, D, scale, bm->q_ptr, bm->kv_idx, bm->kind, bm->tok, bm->BM,
       bm->BN, (E*)O, LSE);
@@ -237,6 +238,7 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
              int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
              cudaStream_t s) {
   const int block = 256;
+  ProfScope ps(s, "bwd_simt");
   k_delta<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>((const E*)dO, (const E*)O, T, Hq, D, delta);
   k_dq<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
       (const E*)dO, (const E*)Q, (const E*)K, (const E*)V, LSE, delta, T, Hq, Hkv, D, scale, bm->q_ptr, bm->kv_idx,

@@ -40,7 +40,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_workspace_size(lib):
     T, Hq, D = 1000, 14, 64
     n = pt.bwd_workspace_bytes(T, Hq, D)
-    assert n >= 4 * T * Hq * D + 4 * T * Hq
+    tpad = -(-T // 128) * 128
+    assert n >= 2 * 4 * tpad * Hq  # Delta and LSE*log2(e), [Hq, Tpad] fp32 each
     assert n % 256 == 0
 
 
