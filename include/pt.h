@@ -181,6 +181,40 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
  * layouts and does not change the size today. */
 size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
 
+/* ---------------------------------------------------------------------------
+ * pt_attn_bwd_noalloc -- pt_attn_bwd for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a deployment convenience.
+ *
+ * Who needs it: a program that embeds this library but owns every byte of
+ * device memory through its own allocator (a serving process, a training
+ * framework's caching allocator) and offers no way to hand out scratch, or a
+ * latency-critical caller for which cudaMalloc, which may synchronise the
+ * device, is off limits.  The call takes the same inputs and outputs as
+ * pt_attn_bwd but no workspace: its scratch (the Delta and LSE*log2(e) rows)
+ * lives in a fixed array inside the library, and it calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Limit: the array holds pt_bwd_noalloc_max_scratch_bytes() bytes (8 MiB);
+ * shapes that need more (2 * Hq * ceil(T/128)*128 fp32 values, each half
+ * rounded up to 256 bytes) return PT_ERR_INVALID_ARG with a message, and
+ * pt_attn_bwd with a caller workspace must be used instead.  Every GPU that
+ * loads the library keeps the array until the process exits.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the one array:
+ * calls whose kernels overlap on the GPU (different streams, or different host
+ * threads) race and give wrong results, so order them.  Each call overwrites
+ * the scratch it reads, so no clearing between calls is needed.
+ * Shapes, dtypes, layouts and errors are otherwise those of pt_attn_bwd.
+ * ------------------------------------------------------------------------- */
+pt_status pt_attn_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V, const void* O,
+                              const float* LSE, pt_dtype dtype, int32_t T, int32_t Hq, int32_t Hkv,
+                              int32_t D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV,
+                              cudaStream_t stream);
+
+/* Capacity in bytes of the built-in scratch array of pt_attn_bwd_noalloc. */
+size_t pt_bwd_noalloc_max_scratch_bytes(void);
+
 /* Synchronise the stream, then return and clear the device status word:
  * PT_ERR_TIMEOUT if an in-kernel wait ran out since the last check, PT_ERR_CUDA
  * if the stream reported an error, else PT_OK. */

@@ -18,7 +18,7 @@ from typing import Optional, Tuple
 __all__ = [
     "PTError", "BlockMap", "load_library", "build_blockmap_tree", "build_blockmap_seg",
     "attn_fwd", "attn_bwd", "bwd_workspace_bytes", "sync_status", "launch_count", "LIB_PATH",
-    "profile_enable", "profile_read", "profile_reset",
+    "profile_enable", "profile_read", "profile_reset", "attn_bwd_noalloc",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpt.so")
@@ -60,6 +60,8 @@ def load_library(path: Optional[str] = None):
             "pt_attn_fwd": [vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp],
             "pt_attn_bwd": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
             "pt_sync_status": [vp],
+            "pt_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp,
+                                    vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -73,6 +75,8 @@ def load_library(path: Optional[str] = None):
         lib.pt_last_error.restype = ctypes.c_char_p
         lib.pt_launch_count.argtypes = []
         lib.pt_launch_count.restype = ctypes.c_uint64
+        lib.pt_bwd_noalloc_max_scratch_bytes.argtypes = []
+        lib.pt_bwd_noalloc_max_scratch_bytes.restype = sz
         lib.pt_profile_enable.argtypes = [ctypes.c_int]
         lib.pt_profile_enable.restype = None
         lib.pt_profile_read.argtypes = [ctypes.c_char_p, i64p, ctypes.POINTER(ctypes.c_double)]
@@ -246,6 +250,26 @@ def attn_bwd(dO, Q, K, V, O, LSE, bm: BlockMap, scale: float = 0.0, dQ=None, dK=
     _check(lib.pt_attn_bwd(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _dtype_code(Q), T, Hq, Hkv, D,
                            float(scale), bm.handle, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), ctypes.c_void_p(_stream(stream))))
+    return dQ, dK, dV
+
+
+def attn_bwd_noalloc(dO, Q, K, V, O, LSE, bm: BlockMap, scale: float = 0.0, dQ=None, dK=None, dV=None,
+                     stream=None) -> Tuple:
+    """attn_bwd without a workspace: the library's built-in scratch array is
+    used instead (for callers that cannot allocate device memory; calls that
+    overlap on the GPU race on that array)."""
+    import torch
+
+    _check_tensors(dO, Q, K, V, O)
+    T, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    lib = load_library()
+    _check(lib.pt_attn_bwd_noalloc(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _dtype_code(Q), T, Hq,
+                                   Hkv, D, float(scale), bm.handle, _ptr(dQ), _ptr(dK), _ptr(dV),
+                                   ctypes.c_void_p(_stream(stream))))
     return dQ, dK, dV
 
 

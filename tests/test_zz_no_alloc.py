@@ -1,0 +1,73 @@
+"""pt_attn_bwd_noalloc, the backward entry point that allocates nothing.
+
+It exists for callers that cannot call cudaMalloc: a host program that owns
+all device memory through its own allocator and gives this library no way to
+get scratch, or a latency-critical path where an allocation (which can
+synchronise the device) is not allowed.  Its scratch lives in a fixed array
+inside the library.  These tests call it through the C ABI (ctypes on
+libpt.so) and check that two calls in a row give the same gradients as
+pt_attn_bwd with a caller workspace, within the parity tolerance used for the
+backward (relative L2 norm 3e-2 for bf16, 1e-5 for fp32).  The file is named
+to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import prefix_tree_block_gb300 as pt
+from prefix_tree_block_gb300 import workloads as W
+from parity import GRAD_RL2, ensure_built, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    return pt.load_library()
+
+
+def _noalloc(lib, dO, Q, K, V, O, LSE, bm, dtype_code):
+    T, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    rc = lib.pt_attn_bwd_noalloc(dO.data_ptr(), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                 LSE.data_ptr(), dtype_code, T, Hq, Hkv, D, 0.0, bm.handle, dQ.data_ptr(),
+                                 dK.data_ptr(), dV.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == pt.PT_OK, lib.pt_last_error()
+    torch.cuda.synchronize()
+    return dQ, dK, dV
+
+
+@pytest.mark.parametrize("dtype,D,BM", [("bf16", 64, 128), ("bf16", 128, 128), ("f32", 32, 16)])
+def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
+    st = W.grpo_structure([(300, [100, 41, 250]), (0, [77, 129])])
+    q, k, v, do = W.make_tensors(st.T, 4, 2, D, dtype, seed=D)
+    Q, K, V, dO = (x.cuda() for x in (q, k, v, do))
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes, BM, BM)
+    O, LSE = pt.attn_fwd(Q, K, V, bm)
+    ref = [x.float().cpu().numpy() for x in pt.attn_bwd(dO, Q, K, V, O, LSE, bm)]
+    code = pt.PT_BF16 if dtype == "bf16" else pt.PT_F32
+    for _ in range(2):
+        got = [x.float().cpu().numpy() for x in _noalloc(lib, dO, Q, K, V, O, LSE, bm, code)]
+        for g, r in zip(got, ref):
+            assert np.isfinite(g).all()
+            assert rel_l2(g, r) <= GRAD_RL2[dtype]
+    pt.sync_status()
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
+    cap = lib.pt_bwd_noalloc_max_scratch_bytes()
+    T, Hq = 20000, 64  # needs 2 * 64 * 20096 * 4 bytes, more than the array holds
+    assert 2 * Hq * (-(-T // 128) * 128) * 4 > cap
+    st = W.docs_structure([T])
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes)
+    small = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(4, dtype=torch.float32, device="cuda")
+    p = small.data_ptr()
+    rc = lib.pt_attn_bwd_noalloc(p, p, p, p, p, lse.data_ptr(), pt.PT_BF16, T, Hq, 8, 64, 0.0, bm.handle, p, p, p,
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == pt.PT_ERR_INVALID_ARG
+    assert b"scratch" in lib.pt_last_error()
