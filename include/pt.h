@@ -133,6 +133,17 @@ pt_status pt_blockmap_info(const pt_blockmap* bm, int32_t* T, int32_t* block_m, 
 pt_status pt_blockmap_export(const pt_blockmap* bm, int32_t* q_ptr, int32_t* kv_idx, uint8_t* kind,
                              int32_t* k_ptr, int32_t* q_idx, uint8_t* kindT);
 
+/* Host copies of the keep bitmasks the tensor-core kernels use (128 x 128
+ * maps only), for tests.  Every partial tile has a mask slot; pidx [nnz] and
+ * pidxT [nnz] give the slot of each q-major and kv-major entry (-1 for full
+ * tiles).  mask_rows [n_partial * 128 * 4]: for slot s, q row r of the tile,
+ * word w, bit b is keep(q = 128 i + r, kv = 128 j + 32 w + b); mask_cols
+ * [n_partial * 128 * 4] holds the transpose (kv column r, bit over q rows).
+ * n_partial = nnz - n_full.  Any pointer may be NULL to skip it;
+ * PT_ERR_UNSUPPORTED if the map has no masks (tile sizes other than 128). */
+pt_status pt_blockmap_export_masks(const pt_blockmap* bm, int32_t* pidx, int32_t* pidxT, uint32_t* mask_rows,
+                                   uint32_t* mask_cols);
+
 void pt_blockmap_free(pt_blockmap* bm);
 
 /* ---------------------------------------------------------------------------

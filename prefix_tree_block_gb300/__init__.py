@@ -57,6 +57,7 @@ def load_library(path: Optional[str] = None):
             "pt_blockmap_dense": [vp, vp, pp],
             "pt_blockmap_info": [vp, i32p, i32p, i32p, i32p, i32p, i64p, i64p],
             "pt_blockmap_export": [vp, vp, vp, vp, vp, vp, vp],
+            "pt_blockmap_export_masks": [vp, vp, vp, vp, vp],
             "pt_attn_fwd": [vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp],
             "pt_attn_bwd": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
             "pt_sync_status": [vp],
@@ -143,6 +144,19 @@ class BlockMap:
         e = self.nnz
         return dict(q_ptr=q_ptr, kv_idx=kv_idx[:e], kind=kind[:e], k_ptr=k_ptr, q_idx=q_idx[:e], kindT=kindT[:e],
                     nnz=e, nq=self.nq, nk=self.nk)
+
+    def export_masks(self) -> dict:
+        """Host copies (numpy) of the partial tiles' keep bitmasks."""
+        import numpy as np
+
+        npart = self.nnz - self.n_full
+        pidx = np.zeros(max(self.nnz, 1), np.int32)
+        pidxT = np.zeros(max(self.nnz, 1), np.int32)
+        rows = np.zeros((max(npart, 1), 128, 4), np.uint32)
+        cols = np.zeros((max(npart, 1), 128, 4), np.uint32)
+        _check(self._lib.pt_blockmap_export_masks(self._h, pidx.ctypes.data, pidxT.ctypes.data, rows.ctypes.data,
+                                                  cols.ctypes.data))
+        return dict(pidx=pidx[: self.nnz], pidxT=pidxT[: self.nnz], mask_rows=rows[:npart], mask_cols=cols[:npart])
 
     def free(self):
         if self._h is not None and self._h.value:

@@ -249,6 +249,37 @@ pt_status pt_blockmap_export(const pt_blockmap* bm, int32_t* q_ptr, int32_t* kv_
   return PT_OK;
 }
 
+pt_status pt_blockmap_export_masks(const pt_blockmap* bm, int32_t* pidx, int32_t* pidxT, uint32_t* mask_rows,
+                                   uint32_t* mask_cols) {
+  if (!bm) {
+    set_error("pt_blockmap_export_masks: NULL map");
+    return PT_ERR_INVALID_ARG;
+  }
+  if (bm->n_partial > 0 && (!bm->mask_rows || !bm->mask_cols)) {
+    set_error("pt_blockmap_export_masks: this map has no tile masks (tile sizes other than 128 x 128)");
+    return PT_ERR_UNSUPPORTED;
+  }
+  struct Item {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } items[] = {
+      {pidx, bm->pidx, sizeof(int32_t) * bm->nnz},
+      {pidxT, bm->pidxT, sizeof(int32_t) * bm->nnz},
+      {mask_rows, bm->mask_rows, sizeof(uint32_t) * 512 * bm->n_partial},
+      {mask_cols, bm->mask_cols, sizeof(uint32_t) * 512 * bm->n_partial},
+  };
+  for (const Item& it : items) {
+    if (!it.dst || it.bytes == 0 || !it.src) continue;
+    cudaError_t e = cudaMemcpy(it.dst, it.src, it.bytes, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+      set_error("pt_blockmap_export_masks: %s", cudaGetErrorString(e));
+      return PT_ERR_CUDA;
+    }
+  }
+  return PT_OK;
+}
+
 void pt_blockmap_free(pt_blockmap* bm) { pt::free_map(bm); }
 
 pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtype, int32_t T, int32_t Hq,

@@ -272,8 +272,11 @@ __global__ void k_counts(const uint8_t* kinds, int nq, int nk, bool by_col, int*
   }
 }
 
-// ordered compaction of each row (or column) into its list slot
-__global__ void k_fill(const uint8_t* kinds, int nq, int nk, bool by_col, const int* ptr, int* idx, uint8_t* kd) {
+// ordered compaction of each row (or column) into its list slot.  For the
+// kv-major lists, `q_ptr`/`kv_idx`/`pidx` of the finished q-major list give
+// each tile's mask slot (binary search of the kv block in the q tile's row).
+__global__ void k_fill(const uint8_t* kinds, int nq, int nk, bool by_col, const int* ptr, int* idx, uint8_t* kd,
+                       int* pflag, const int* q_ptr, const int* kv_idx, const int* pidx, int* pidxT) {
   int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   int nrows = by_col ? nk : nq, len = by_col ? nq : nk;
   if (w >= nrows) return;
@@ -287,21 +290,84 @@ __global__ void k_fill(const uint8_t* kinds, int nq, int nk, bool by_col, const 
       int off = __popc(m & ((1u << lane) - 1));
       idx[pos + off] = x;
       kd[pos + off] = k;
+      if (!by_col) {
+        pflag[pos + off] = (k == PT_KIND_PARTIAL);
+      } else {
+        int lo = q_ptr[x], hi = q_ptr[x + 1] - 1;  // row x holds kv block w
+        while (lo < hi) {
+          int mid = (lo + hi) >> 1;
+          if (kv_idx[mid] < w)
+            lo = mid + 1;
+          else
+            hi = mid;
+        }
+        pidxT[pos + off] = pidx[lo];
+      }
     }
     pos += __popc(m);
   }
 }
 
-// dense map: every tile partial
+// q-major: mask slot of each partial entry (exclusive scan of partial flags),
+// and the (q tile, kv block) of every slot.
+__global__ void k_slots(int nq, const int* q_ptr, const int* kv_idx, const uint8_t* kind, const int* pscan,
+                        int* pidx, int2* slot_tile) {
+  int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= nq) return;
+  for (int e = q_ptr[w] + lane; e < q_ptr[w + 1]; e += 32) {
+    if (kind[e] == PT_KIND_PARTIAL) {
+      int s = pscan[e];
+      pidx[e] = s;
+      slot_tile[s] = make_int2(w, kv_idx[e]);
+    } else {
+      pidx[e] = -1;
+    }
+  }
+}
+
+// Keep bitmasks of every partial 128 x 128 tile, both orientations:
+// mask_rows[slot][r][w] bit b = keep(q = i*128 + r, kv = j*128 + 32w + b),
+// mask_cols[slot][c][w] bit b = keep(q = i*128 + 32w + b, kv = j*128 + c).
+// Pairs outside [0, T) are never kept.
+__global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols) {
+  __shared__ pt_tok tq[128], tk[128];
+  const int s = blockIdx.x, r = threadIdx.x;
+  const int2 ij = slot_tile[s];
+  const int q0 = ij.x * 128, k0 = ij.y * 128;
+  tq[r] = tok[q0 + r];
+  tk[r] = tok[k0 + r];
+  __syncthreads();
+  uint32_t row[4] = {0, 0, 0, 0}, col[4] = {0, 0, 0, 0};
+  const int q = q0 + r, kv = k0 + r;
+  const pt_tok mq = tq[r], mk = tk[r];
+  for (int c = 0; c < 128; ++c) {
+    const int kvc = k0 + c;
+    const pt_tok t = tk[c];
+    if (q < T && kvc < T && kvc <= q && t.tin <= mq.tin && mq.tin < t.tout) row[c >> 5] |= 1u << (c & 31);
+    const int qc = q0 + c;
+    const pt_tok u = tq[c];
+    if (qc < T && kv < T && kv <= qc && mk.tin <= u.tin && u.tin < mk.tout) col[c >> 5] |= 1u << (c & 31);
+  }
+  uint4* mr = reinterpret_cast<uint4*>(mask_rows) + (size_t)s * 128 + r;
+  uint4* mc = reinterpret_cast<uint4*>(mask_cols) + (size_t)s * 128 + r;
+  *mr = make_uint4(row[0], row[1], row[2], row[3]);
+  *mc = make_uint4(col[0], col[1], col[2], col[3]);
+}
+
+// dense map: every tile partial; slot = row-major tile index
 __global__ void k_dense_lists(int nq, int nk, int* q_ptr, int* kv_idx, uint8_t* kind, int* k_ptr, int* q_idx,
-                              uint8_t* kindT) {
+                              uint8_t* kindT, int* pidx, int* pidxT, int2* slot_tile) {
   long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   long long n = (long long)nq * nk;
   if (e < n) {
     kv_idx[e] = (int)(e % nk);
     kind[e] = PT_KIND_PARTIAL;
-    q_idx[e] = (int)(e % nq);
+    pidx[e] = (int)e;
+    slot_tile[e] = make_int2((int)(e / nk), (int)(e % nk));
+    const int j = (int)(e / nq), i = (int)(e % nq);  // kv-major entry e: column j, row i
+    q_idx[e] = i;
     kindT[e] = PT_KIND_PARTIAL;
+    pidxT[e] = i * nk + j;
   }
   if (e <= nq) q_ptr[e] = (int)(e * nk);
   if (e <= nk) k_ptr[e] = (int)(e * nq);
@@ -380,10 +446,53 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
     if ((rc = dalloc(&bm->kindT, nnz))) break;
     if ((rc = dalloc(&bm->q_order, nq))) break;
     if ((rc = dalloc(&bm->k_order, nk))) break;
-    if (ntiles > 0) {
-      k_fill<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, bm->q_ptr, bm->kv_idx, bm->kind);
-      k_fill<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, bm->k_ptr, bm->q_idx, bm->kindT);
-      count_launch(2);
+    if ((rc = dalloc(&bm->pidx, nnz))) break;
+    if ((rc = dalloc(&bm->pidxT, nnz))) break;
+    bm->n_partial = nnz - nfull;
+    const bool masks = bm->BM == 128 && bm->BN == 128 && bm->n_partial > 0;
+    if (masks) {
+      if ((rc = dalloc(&bm->mask_rows, (size_t)bm->n_partial * 512))) break;
+      if ((rc = dalloc(&bm->mask_cols, (size_t)bm->n_partial * 512))) break;
+    }
+    if (ntiles > 0 && nnz > 0) {
+      int* pflag = nullptr;
+      int* pscan = nullptr;
+      int* stmp = nullptr;
+      int2* slot_tile = nullptr;
+      if ((rc = dalloc(&pflag, nnz))) break;
+      if ((rc = dalloc(&pscan, (size_t)nnz + 1)) || (rc = dalloc(&stmp, (size_t)nnz / kScanBlock + 2)) ||
+          (rc = dalloc(&slot_tile, std::max<int64_t>(bm->n_partial, 1)))) {
+        cudaFree(pflag);
+        cudaFree(pscan);
+        cudaFree(stmp);
+        break;
+      }
+      k_fill<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, bm->q_ptr, bm->kv_idx, bm->kind, pflag,
+                                                     nullptr, nullptr, nullptr, nullptr);
+      count_launch();
+      rc = exclusive_scan(pflag, nnz, pscan, stmp, s);
+      if (!rc) {
+        k_slots<<<(nq * 32 + 255) / 256, 256, 0, s>>>(nq, bm->q_ptr, bm->kv_idx, bm->kind, pscan, bm->pidx,
+                                                       slot_tile);
+        k_fill<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, bm->k_ptr, bm->q_idx, bm->kindT, nullptr,
+                                                       bm->q_ptr, bm->kv_idx, bm->pidx, bm->pidxT);
+        count_launch(2);
+        if (masks) {
+          k_masks<<<(unsigned)bm->n_partial, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
+          count_launch();
+        }
+      }
+      cudaError_t le = cudaStreamSynchronize(s);
+      cudaFree(pflag);
+      cudaFree(pscan);
+      cudaFree(stmp);
+      cudaFree(slot_tile);
+      if (rc) break;
+      if (le != cudaSuccess) {
+        set_error("block map lists failed: %s", cudaGetErrorString(le));
+        rc = 3;
+        break;
+      }
     }
     std::vector<int> oq, ok;
     lpt_order(hq, oq);
@@ -423,7 +532,8 @@ pt_blockmap* new_map(int T, int BM, int BN) {
 void free_map(pt_blockmap* bm) {
   if (!bm) return;
   void* ptrs[] = {bm->tok, bm->node_of, bm->node_start, bm->node_end, bm->parent, bm->q_ptr, bm->kv_idx,
-                  bm->kind, bm->k_ptr, bm->q_idx, bm->kindT, bm->q_order, bm->k_order};
+                  bm->kind, bm->k_ptr, bm->q_idx, bm->kindT, bm->q_order, bm->k_order, bm->pidx, bm->pidxT,
+                  bm->mask_rows, bm->mask_cols};
   for (void* p : ptrs) cudaFree(p);
   delete bm;
 }
@@ -671,10 +781,30 @@ int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out) {
       rc = 3;
       break;
     }
+    if ((rc = dalloc(&bm->pidx, n))) break;
+    if ((rc = dalloc(&bm->pidxT, n))) break;
+    int2* slot_tile = nullptr;
+    if ((rc = dalloc(&slot_tile, n))) break;
+    const bool masks = bm->BM == 128 && bm->BN == 128 && n > 0;
+    if (masks && ((rc = dalloc(&bm->mask_rows, (size_t)n * 512)) || (rc = dalloc(&bm->mask_cols, (size_t)n * 512)))) {
+      cudaFree(slot_tile);
+      break;
+    }
     long long cnt = std::max<long long>(n, std::max(nq, nk) + 1);
     k_dense_lists<<<(unsigned)((cnt + 255) / 256), 256, 0, s>>>(nq, nk, bm->q_ptr, bm->kv_idx, bm->kind, bm->k_ptr,
-                                                                bm->q_idx, bm->kindT);
+                                                                bm->q_idx, bm->kindT, bm->pidx, bm->pidxT, slot_tile);
     count_launch();
+    if (masks) {
+      k_masks<<<(unsigned)n, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
+      count_launch();
+    }
+    bm->n_partial = n;
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+      cudaFree(slot_tile);
+      rc = 3;
+      break;
+    }
+    cudaFree(slot_tile);
     // every row has the same length: natural order (last tiles first is no better)
     std::vector<int> oq(nq), ok(nk);
     std::iota(oq.begin(), oq.end(), 0);

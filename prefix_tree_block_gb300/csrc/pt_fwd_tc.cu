@@ -3,26 +3,30 @@
 // "prefix_grouper_kernel.py", flex_shared_prefix_attention and its block
 // mask: exact softmax attention in which every (q tile, kv block) pair the
 // block map lists as empty is skipped, full pairs run unmasked, and partial
-// pairs apply the tree mask element by element.
+// pairs apply the tree mask element by element (here: one bit per pair from
+// the block map's precomputed 128 x 128 keep masks).
 //
-// Design (sm_103a, one persistent CTA per SM, 192 threads):
-//   warp 4      TMA producer: Q tile once per work item, then K and V tiles
-//               of each listed kv block through separate multi-stage rings
-//               (128-byte swizzled 64-column panels), plus the kv block's
-//               per-token tree coordinates by 1-D bulk copy with V.
-//   warp 5      MMA issuer (one lane): S = Q K^T into one of two TMEM
-//               buffers (M = 128 q rows, N = 128 kv, K = D), then
-//               O += P V with P read from TMEM (M = 128, N = D, K = 128).
-//               S of block j+1 is issued before PV of block j so the tensor
-//               pipe has work while the softmax runs.
-//   warps 0-3   softmax: thread t owns q row t of the tile; it loads its S
-//               row from TMEM, masks partial blocks in registers, keeps the
-//               running max and sum (base-2, scale folded in), writes P as
-//               bf16 back over its S columns, and rescales O in TMEM only
-//               when the running max grows by more than 2^8 (the final
-//               division by l makes any fixed reference exact).
-// TMEM: S0 cols [0,128), S1 [128,256), O [256, 256+D).  D = 256 fills all 512.
-// Every wait is bounded; a timeout raises a CTA abort flag, records
+// Design (sm_103a, one persistent CTA per SM):
+//   NH softmax warpgroups (NH = 2 for head_dim <= 128, else 1).  A work item
+//   is one q tile and NH q heads that share a kv head (grouped-query
+//   attention), so every K/V tile loaded serves NH heads.  Warpgroup h owns
+//   head h of the item; thread t of it owns q row t of the tile.
+//   producer warp   TMA: the NH Q tiles once per item, then K and V of each
+//                   listed kv block through separate multi-stage rings
+//                   (128-byte swizzled 64-column panels); with V, the tile's
+//                   keep mask (partial tiles) and its slot id.
+//   MMA warp        one lane issues tcgen05.mma: S_h = Q_h K^T into TMEM
+//                   (M = 128 q rows, N = 128 kv, K = D) and O_h += P_h V with
+//                   P_h read from TMEM (M = 128, N = D, K = 128).  With two
+//                   heads, head A's MMAs run while head B's softmax works and
+//                   vice versa; with one head, S is double-buffered and S of
+//                   block j+1 is issued before PV of block j.
+//   softmax         load the S row from TMEM, clear masked entries, keep the
+//                   running max and sum in base 2 with the scale folded in,
+//                   write P as bf16 over the S columns, and rescale O in TMEM
+//                   only when the running max grows by more than 2^8 (the
+//                   final division by l makes any fixed reference exact).
+// Every wait is bounded: a timeout raises a CTA abort flag, records
 // PT_ERR_TIMEOUT, drains copies and MMAs in flight and frees TMEM.
 #include <cuda_bf16.h>
 
@@ -38,48 +42,78 @@ int take_status_fwd(cudaStream_t s) { return take_status_here(s); }
 
 namespace {
 
-template <int D>
+template <int D, int NH>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int NP = D / 64;        // 64-column panels per row
   static constexpr int PANEL = 128 * 128;  // bytes: 128 rows x 128 B
   static constexpr int TILE = NP * PANEL;
-  static constexpr int KS = D == 64 ? 4 : (D == 128 ? 3 : 1);
+  static constexpr int SB = NH == 1 ? 2 : 1;  // S buffers per head
+  static constexpr int KS = D == 64 ? 4 : (D == 128 ? (NH == 2 ? 2 : 3) : 1);
   static constexpr int VS = D == 64 ? 4 : (D == 128 ? 2 : 1);
-  static constexpr int TOKB = BN * (int)sizeof(pt_tok);
+  static constexpr int MASKB = 128 * 16;  // one partial tile's row masks
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_K = OFF_Q + NH * TILE;
   static constexpr int OFF_V = OFF_K + KS * TILE;
-  static constexpr int OFF_TOK = OFF_V + VS * TILE;
-  static constexpr int OFF_BAR = OFF_TOK + VS * TOKB;
-  // q_full q_empty k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2] p_full[2] o_full o_free mma_done
-  static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 2 + 3;
+  static constexpr int OFF_MASK = OFF_V + VS * TILE;
+  static constexpr int OFF_META = OFF_MASK + VS * MASKB;
+  static constexpr int OFF_BAR = OFF_META + 16 * ((VS * 4 + 15) / 16);
+  // q_full q_empty k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
+  // s_full[NH*SB] p_full[NH*SB] o_full[NH] o_free[NH] mma_done
+  static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 * NH * SB + 2 * NH + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int TM_S0 = 0, TM_S1 = 128, TM_O = 256;
+  static constexpr int TM_S = 0;                 // S(h, b) at (h * SB + b) * 128
+  static constexpr int TM_O = NH * SB * 128;     // O(h) at TM_O + h * D
+  static constexpr int THREADS = NH * 128 + 64;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(TM_O + D <= 512, "TMEM budget");
+  static_assert(TM_O + NH * D <= 512, "TMEM budget");
 };
 
 struct FwdParams {
   const int* q_ptr;
   const int* kv_idx;
-  const uint8_t* kind;
+  const int* pidx;
   const int* q_order;
-  const pt_tok* tok;
+  const uint32_t* mask_rows;
   __nv_bfloat16* O;
   float* LSE;
   int T, Hq, Hkv, nq;
   float scale_log2;  // softmax scale * log2(e)
 };
 
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
-__global__ void __launch_bounds__(192, 1)
+// Work item w -> q tile, first head, number of heads (1..NH).
+template <int NH>
+__device__ __forceinline__ void decode_item(const FwdParams& p, int w, int& tile, int& h0, int& nh) {
+  const int g = p.Hq / p.Hkv;
+  if (NH == 1) {
+    tile = p.q_order[w / p.Hq];
+    h0 = w % p.Hq;
+    nh = 1;
+  } else {
+    const int np = (g + 1) >> 1;
+    const int per_tile = p.Hkv * np;
+    tile = p.q_order[w / per_tile];
+    const int rem = w % per_tile, hk = rem / np, pr = rem % np;
+    h0 = hk * g + 2 * pr;
+    nh = min(2, g - 2 * pr);
+  }
+}
+
+template <int NH>
+__host__ __device__ __forceinline__ int fwd_items(int nq, int Hq, int Hkv) {
+  if (NH == 1) return nq * Hq;
+  const int g = Hq / Hkv;
+  return nq * Hkv * ((g + 1) / 2);
+}
+
+template <int D, int NH>
+__global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
              const __grid_constant__ CUtensorMap mV, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -89,19 +123,20 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* k_empty = k_full + C::KS;
   uint64_t* v_full = k_empty + C::KS;
   uint64_t* v_empty = v_full + C::VS;
-  uint64_t* s_full = v_empty + C::VS;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_full = p_full + 2;
-  uint64_t* o_free = o_full + 1;
-  uint64_t* mma_done = o_free + 1;
+  uint64_t* s_full = v_empty + C::VS;       // [NH][SB]
+  uint64_t* p_full = s_full + NH * C::SB;   // [NH][SB]
+  uint64_t* o_full = p_full + NH * C::SB;   // [NH]
+  uint64_t* o_free = o_full + NH;           // [NH]
+  uint64_t* mma_done = o_free + NH;
+  int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = p.Hq / p.Hkv;
-  const int n_items = p.nq * p.Hq;
+  const int n_items = fwd_items<NH>(p.nq, p.Hq, p.Hkv);
+  constexpr int PRODUCER = NH * 4, ISSUER = NH * 4 + 1;
 
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == PRODUCER * 32) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < C::KS; ++s) {
@@ -112,12 +147,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(v_full + s, 1);
       mbar_init(v_empty + s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NH * C::SB; ++b) {
       mbar_init(s_full + b, 1);
       mbar_init(p_full + b, 128);
     }
-    mbar_init(o_full, 1);
-    mbar_init(o_free, 128);
+    for (int h = 0; h < NH; ++h) {
+      mbar_init(o_full + h, 1);
+      mbar_init(o_free + h, 128);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -125,7 +162,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&mK);
     prefetch_tmap(&mV);
   }
-  if (warp == 5) {
+  if (warp == ISSUER) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -134,23 +171,27 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t kc = 0, vc = 0, it = 0;
       bool ok = true, q_issued = false;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const int tile = p.q_order[w / p.Hq], h = w % p.Hq, hk = h / g;
+        int tile, h0, nh;
+        decode_item<NH>(p, w, tile, h0, nh);
         const int e0 = p.q_ptr[tile], e1 = p.q_ptr[tile + 1];
         if (e1 == e0) continue;
         if (it > 0 && !(ok = mbar_wait(q_empty, (it - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(q_full, C::TILE);
+        mbar_expect_tx(q_full, nh * C::TILE);
+        for (int h = 0; h < nh; ++h)
 #pragma unroll
-        for (int pn = 0; pn < C::NP; ++pn)
-          tma_load_3d(smem + C::OFF_Q + pn * C::PANEL, &mQ, q_full, pn * 64, h, tile * C::BM);
+          for (int pn = 0; pn < C::NP; ++pn)
+            tma_load_3d(smem + C::OFF_Q + h * C::TILE + pn * C::PANEL, &mQ, q_full, pn * 64, h0 + h, tile * C::BM);
         q_issued = true;
+        const int hk = h0 / (p.Hq / p.Hkv);
         for (int e = e0; e < e1; ++e) {
           const int j = p.kv_idx[e];
+          const int slot = p.pidx[e];
           {
             const uint32_t s = kc % C::KS, u = kc / C::KS;
             if (u > 0 && !(ok = mbar_wait(k_empty + s, (u - 1) & 1, abort_flag))) break;
@@ -163,20 +204,21 @@ __global__ void __launch_bounds__(192, 1)
           {
             const uint32_t s = vc % C::VS, u = vc / C::VS;
             if (u > 0 && !(ok = mbar_wait(v_empty + s, (u - 1) & 1, abort_flag))) break;
-            mbar_expect_tx(v_full + s, C::TILE + C::TOKB);
+            meta[s] = slot;  // made visible by the arrive below (release)
+            mbar_expect_tx(v_full + s, C::TILE + (slot >= 0 ? C::MASKB : 0));
 #pragma unroll
             for (int pn = 0; pn < C::NP; ++pn)
               tma_load_3d(smem + C::OFF_V + s * C::TILE + pn * C::PANEL, &mV, v_full + s, pn * 64, hk, j * C::BN);
-            bulk_load(smem + C::OFF_TOK + s * C::TOKB, p.tok + (size_t)j * C::BN, C::TOKB, v_full + s);
+            if (slot >= 0)
+              bulk_load(smem + C::OFF_MASK + s * C::MASKB, p.mask_rows + (size_t)slot * 512, C::MASKB, v_full + s);
             ++vc;
           }
         }
         ++it;
       }
       if (!ok) {
-        // drain: wait (bounded) for the last copy issued into each slot
         const long long lim = 20000000;
-        if (q_issued) mbar_wait_drain(q_full, (it) & 1, lim);
+        if (q_issued) mbar_wait_drain(q_full, (it)&1, lim);
         for (uint32_t s = 0; s < C::KS && s < kc; ++s) {
           uint32_t last = kc - 1 - ((kc - 1 - s) % C::KS);
           mbar_wait_drain(k_full + s, (last / C::KS) & 1, lim);
@@ -188,7 +230,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == ISSUER) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
@@ -196,128 +238,170 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sK = smem_u32(smem + C::OFF_K);
       const uint32_t sV = smem_u32(smem + C::OFF_V);
-      uint32_t kc = 0, vc = 0, sc = 0, it = 0;
+      uint32_t kc = 0, vc = 0, it = 0;
+      uint32_t sc[NH], itv[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) sc[h] = itv[h] = 0;
       bool ok = true;
+
+      auto issue_s = [&](int h, uint32_t u, uint32_t ks) {
+        const uint32_t b = u % C::SB;
+        const uint32_t d_tmem = tbase + C::TM_S + (h * C::SB + b) * 128;
+        const uint32_t qa = sQ + h * C::TILE, ka = sK + ks * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+          mma_ss(d_tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+        }
+        mma_commit(s_full + h * C::SB + b);
+      };
+      auto issue_pv = [&](int h, uint32_t u, uint32_t vs, bool first) {
+        const uint32_t b = u % C::SB;
+        const uint32_t a_tmem = tbase + C::TM_S + (h * C::SB + b) * 128;
+        const uint32_t va = sV + vs * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(tbase + C::TM_O + h * D, a_tmem + kk * 8, sdesc_sw128(va + kk * 2048, C::PANEL, 1024), IDESC_PV,
+                 (!first || kk > 0));
+        mma_commit(o_full + h);
+      };
+
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const int tile = p.q_order[w / p.Hq];
-        const int e0 = p.q_ptr[tile], e1 = p.q_ptr[tile + 1];
-        const int n = e1 - e0;
+        int tile, h0, nh;
+        decode_item<NH>(p, w, tile, h0, nh);
+        const int n = p.q_ptr[tile + 1] - p.q_ptr[tile];
         if (n == 0) continue;
         if (!(ok = mbar_wait(q_full, it & 1, abort_flag))) break;
         tc_fence_after();
         for (int jj = 0; jj <= n && ok; ++jj) {
+          const uint32_t ks = (kc + jj) % C::KS;
           if (jj < n) {
-            const uint32_t x = kc + jj, s = x % C::KS;
-            if (!(ok = mbar_wait(k_full + s, (x / C::KS) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(k_full + ks, ((kc + jj) / C::KS) & 1, abort_flag))) break;
             tc_fence_after();
-            const uint32_t b = (sc + jj) & 1;
-            const uint32_t d_tmem = tbase + (b ? C::TM_S1 : C::TM_S0);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-              mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + s * C::TILE + off, 16, 1024), IDESC_S,
-                     kk > 0);
-            }
-            mma_commit(k_empty + s);
-            mma_commit(s_full + b);
-            if (jj == n - 1) mma_commit(q_empty);
           }
-          if (jj >= 1) {
-            const int i = jj - 1;
-            const uint32_t b = (sc + i) & 1;
-            if (!(ok = mbar_wait(p_full + b, ((sc + i) >> 1) & 1, abort_flag))) break;
-            const uint32_t x = vc + i, s = x % C::VS;
-            if (!(ok = mbar_wait(v_full + s, (x / C::VS) & 1, abort_flag))) break;
-            if (i == 0 && it > 0 && !(ok = mbar_wait(o_free, (it - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            const uint32_t a_tmem = tbase + (b ? C::TM_S1 : C::TM_S0);
-#pragma unroll
-            for (int kk = 0; kk < C::BN / 16; ++kk) {
-              mma_ts(tbase + C::TM_O, a_tmem + kk * 8, sdesc_sw128(sV + s * C::TILE + kk * 2048, C::PANEL, 1024),
-                     IDESC_PV, (i > 0 || kk > 0));
+          if (NH == 1) {
+            if (jj < n) {
+              issue_s(0, sc[0] + jj, ks);
+              mma_commit(k_empty + ks);
+              if (jj == n - 1) mma_commit(q_empty);
             }
-            mma_commit(v_empty + s);
-            mma_commit(o_full);
+            if (jj >= 1) {
+              const int i = jj - 1;
+              const uint32_t u = sc[0] + i, vs = (vc + i) % C::VS;
+              if (!(ok = mbar_wait(p_full + (u % C::SB), (u / C::SB) & 1, abort_flag))) break;
+              if (!(ok = mbar_wait(v_full + vs, ((vc + i) / C::VS) & 1, abort_flag))) break;
+              if (i == 0 && itv[0] > 0 && !(ok = mbar_wait(o_free, (itv[0] - 1) & 1, abort_flag))) break;
+              tc_fence_after();
+              issue_pv(0, u, vs, i == 0);
+              mma_commit(v_empty + vs);
+            }
+          } else {
+            for (int h = 0; h < nh && ok; ++h) {
+              if (jj >= 1) {
+                const int i = jj - 1;
+                const uint32_t u = sc[h] + i, vs = (vc + i) % C::VS;
+                if (!(ok = mbar_wait(p_full + h * C::SB, u & 1, abort_flag))) break;
+                if (h == 0 && !(ok = mbar_wait(v_full + vs, ((vc + i) / C::VS) & 1, abort_flag))) break;
+                if (i == 0 && itv[h] > 0 && !(ok = mbar_wait(o_free + h, (itv[h] - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_pv(h, u, vs, i == 0);
+                if (h == nh - 1) mma_commit(v_empty + vs);
+              }
+              if (jj < n) {
+                issue_s(h, sc[h] + jj, ks);
+                if (h == nh - 1) {
+                  mma_commit(k_empty + ks);
+                  if (jj == n - 1) mma_commit(q_empty);
+                }
+              }
+            }
           }
         }
         kc += n;
         vc += n;
-        sc += n;
+        for (int h = 0; h < nh; ++h) {
+          sc[h] += n;
+          itv[h] += 1;
+        }
         ++it;
       }
-      // every MMA issued so far must finish before TMEM is freed
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, 200000000);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x;  // q row within the tile, TMEM lane
-    const uint32_t tl = tbase + ((uint32_t)(warp * 32) << 16);
+    const int h = warp >> 2;                   // head slot of this warpgroup
+    const int r = threadIdx.x & 127;           // q row within the tile, TMEM lane
+    const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t o_col = C::TM_O + h * D;
     uint32_t sc = 0, vc = 0, pvc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const int tile = p.q_order[w / p.Hq], h = w % p.Hq;
-      const int e0 = p.q_ptr[tile], e1 = p.q_ptr[tile + 1];
-      const int n = e1 - e0;
-      const int q = tile * C::BM + t;
+      int tile, h0, nh;
+      decode_item<NH>(p, w, tile, h0, nh);
+      const int e0 = p.q_ptr[tile], n = p.q_ptr[tile + 1] - e0;
+      if (h >= nh) {  // this warpgroup has no head in the item; the V ring still advances
+        vc += n;
+        continue;
+      }
+      const int head = h0 + h;
+      const int q = tile * C::BM + r;
       if (n == 0) {
         if (q < p.T) {
           uint4 z = make_uint4(0, 0, 0, 0);
-          uint4* dst = reinterpret_cast<uint4*>(p.O + ((size_t)q * p.Hq + h) * D);
+          uint4* dst = reinterpret_cast<uint4*>(p.O + ((size_t)q * p.Hq + head) * D);
           for (int c = 0; c < D / 8; ++c) dst[c] = z;
-          p.LSE[(size_t)h * p.T + q] = -INFINITY;
+          p.LSE[(size_t)head * p.T + q] = -INFINITY;
         }
         continue;
       }
-      const int q_tin = p.tok[q].tin;
       float m_use = -INFINITY, l = 0.f;
       for (int jj = 0; jj < n; ++jj) {
-        const int e = e0 + jj;
-        const int kd = p.kind[e];
-        const int k0 = p.kv_idx[e] * C::BN;
-        const uint32_t b = (sc + jj) & 1;
-        ok = mbar_wait(s_full + b, ((sc + jj) >> 1) & 1, abort_flag);
+        const uint32_t u = sc + jj, b = u % C::SB;
+        const uint32_t x = vc + jj, vs = x % C::VS;
+        ok = mbar_wait(s_full + h * C::SB + b, (u / C::SB) & 1, abort_flag) &&
+             mbar_wait(v_full + vs, (x / C::VS) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sb = tl + (b ? C::TM_S1 : C::TM_S0);
+        const uint32_t sb = tl + C::TM_S + (h * C::SB + b) * 128;
         uint32_t sr[128];
         tmem_ld32(sb + 0, sr + 0);
         tmem_ld32(sb + 32, sr + 32);
         tmem_ld32(sb + 64, sr + 64);
         tmem_ld32(sb + 96, sr + 96);
+        const int slot = meta[vs];
+        uint4 mk = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+        if (slot >= 0) mk = reinterpret_cast<const uint4*>(smem + C::OFF_MASK + vs * C::MASKB)[r];
         tmem_ld_wait();
-        float mx = -INFINITY;
-        if (kd == PT_KIND_PARTIAL) {
-          const uint32_t x = vc + jj, s = x % C::VS;
-          ok = mbar_wait(v_full + s, (x / C::VS) & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          const pt_tok* tk = reinterpret_cast<const pt_tok*>(smem + C::OFF_TOK + s * C::TOKB);
+        // eight independent max chains (instruction-level parallelism)
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+        if (slot >= 0) {
+          const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
-            const pt_tok kt = tk[c];
-            const bool keep = (k0 + c <= q) && (kt.tin <= q_tin) && (q_tin < kt.tout);
-            float v = keep ? __uint_as_float(sr[c]) : -INFINITY;
+            const float v = ((mw[c >> 5] >> (c & 31)) & 1u) ? __uint_as_float(sr[c]) : -INFINITY;
             sr[c] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
+            m8[c & 7] = fmaxf(m8[c & 7], v);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+          for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
         }
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float m_blk = mx * p.scale_log2;
         const bool grow = m_blk > m_use + kRescaleThreshold;
-        float m_new = grow ? m_blk : m_use;
+        const float m_new = grow ? m_blk : m_use;
         if (__any_sync(0xffffffffu, grow && l > 0.f)) {
           // O holds contributions scaled to the old reference: wait for the PV
           // in flight, then rescale this warp's rows in place.
-          ok = mbar_wait(o_full, (pvc + jj - 1) & 1, abort_flag);
+          ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -327,53 +411,55 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t orr[32];
-            tmem_ld32(tl + C::TM_O + c * 32, orr);
+            tmem_ld32(tl + o_col + c * 32, orr);
             tmem_ld_wait();
 #pragma unroll
             for (int k = 0; k < 32; ++k) orr[k] = __float_as_uint(__uint_as_float(orr[k]) * alpha);
-            tmem_st32(tl + C::TM_O + c * 32, orr);
+            tmem_st32(tl + o_col + c * 32, orr);
           }
           tmem_st_wait();
           l *= alpha;
         }
         m_use = m_new;
         const float ref = (m_use == -INFINITY) ? 0.f : m_use;
-        float rs = 0.f;
+        float r8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) r8[k] = 0.f;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
           const float p0 = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -ref));
           const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -ref));
-          rs += p0 + p1;
+          r8[(c >> 1) & 7] += p0 + p1;
           sr[c >> 1] = pack_bf16(p0, p1);
         }
-        l += rs;
+        l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
         tmem_st32(sb + 0, sr + 0);
         tmem_st32(sb + 32, sr + 32);
         tmem_st_wait();
         if (jj > 0) {
-          ok = mbar_wait(o_full, (pvc + jj - 1) & 1, abort_flag);
+          ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
         }
         tc_fence_before();
-        mbar_arrive(p_full + b);
+        mbar_arrive(p_full + h * C::SB + b);
       }
       if (!ok) break;
       // epilogue: O / l and LSE
-      ok = mbar_wait(o_full, (pvc + n - 1) & 1, abort_flag);
+      ok = mbar_wait(o_full + h, (pvc + n - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.O + ((size_t)q * p.Hq + h) * D;
+      __nv_bfloat16* orow = p.O + ((size_t)q * p.Hq + head) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t orr[32];
-        tmem_ld32(tl + C::TM_O + c * 32, orr);
+        tmem_ld32(tl + o_col + c * 32, orr);
         tmem_ld_wait();
         if (q < p.T) {
           uint32_t pk[16];
@@ -385,9 +471,9 @@ __global__ void __launch_bounds__(192, 1)
           for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
-      if (q < p.T) p.LSE[(size_t)h * p.T + q] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (q < p.T) p.LSE[(size_t)head * p.T + q] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
-      mbar_arrive(o_free);
+      mbar_arrive(o_free + h);
       sc += n;
       vc += n;
       pvc += n;
@@ -398,22 +484,27 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tbase, 512);
+  if (warp == ISSUER) tmem_dealloc(tbase, 512);
 }
 
-template <int D>
+template <int D, int NH>
 int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, float scale,
                const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, NH>;
   static int attr_set[64] = {0};
   int dev = bm->device;
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_fwd_tc<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) {
       set_error("forward kernel: cannot reserve %d bytes of shared memory: %s", C::SMEM_BYTES, cudaGetErrorString(e));
       return 3;
     }
     attr_set[dev] = 1;
+  }
+  if (bm->n_partial > 0 && !bm->mask_rows) {
+    set_error("forward kernel: block map has no tile masks");
+    return 1;
   }
   CUtensorMap mQ, mK, mV;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mK, K, T, Hkv, D, 128) ||
@@ -422,9 +513,9 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
   FwdParams p;
   p.q_ptr = bm->q_ptr;
   p.kv_idx = bm->kv_idx;
-  p.kind = bm->kind;
+  p.pidx = bm->pidx;
   p.q_order = bm->q_order;
-  p.tok = bm->tok;
+  p.mask_rows = bm->mask_rows;
   p.O = static_cast<__nv_bfloat16*>(O);
   p.LSE = LSE;
   p.T = T;
@@ -432,12 +523,12 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
   p.Hkv = Hkv;
   p.nq = bm->nq;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const int n_items = bm->nq * Hq;
+  const int n_items = fwd_items<NH>(bm->nq, Hq, Hkv);
   const int grid = n_items < num_sms(dev) ? n_items : num_sms(dev);
   if (grid <= 0) return 0;
   {
     ProfScope ps(s, "fwd_tc");
-    k_fwd_tc<D><<<grid, 192, C::SMEM_BYTES, s>>>(mQ, mK, mV, p);
+    k_fwd_tc<D, NH><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mQ, mK, mV, p);
   }
   count_launch();
   cudaError_t e = cudaGetLastError();
@@ -453,9 +544,9 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
 int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
            const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
   switch (D) {
-    case 64: return launch_fwd<64>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
-    case 128: return launch_fwd<128>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
-    case 256: return launch_fwd<256>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
+    case 64: return launch_fwd<64, 2>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
+    case 128: return launch_fwd<128, 2>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
+    case 256: return launch_fwd<256, 1>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
     default: set_error("tensor-core forward: head_dim %d not built", D); return 2;
   }
 }

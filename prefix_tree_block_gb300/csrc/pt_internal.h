@@ -47,6 +47,12 @@ struct pt_blockmap {
   // longest-first processing orders
   int32_t* q_order;  // [nq] q tiles, most kv blocks first
   int32_t* k_order;  // [nk] kv blocks, most q tiles first
+  // keep bitmasks of the partial tiles (128 x 128 maps only)
+  int64_t n_partial;
+  int32_t* pidx;        // [nnz] mask slot of each q-major entry, -1 when full
+  int32_t* pidxT;       // [nnz] mask slot of each kv-major entry, -1 when full
+  uint32_t* mask_rows;  // [n_partial][128 q rows][4 words]: bit c = keep(row, kv column c)
+  uint32_t* mask_cols;  // [n_partial][128 kv columns][4 words]: bit r = keep(q row r, column)
 };
 
 namespace pt {

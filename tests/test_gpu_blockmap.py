@@ -76,3 +76,48 @@ def test_empty_layout():
     st = W.grpo_structure([(0, [0])])
     bm = gpu_blockmap(st)
     assert bm.T == 0 and bm.nnz == 0
+
+
+def unpack_bits(words):
+    """[n, 128, 4] uint32 -> [n, 128, 128] bool (bit b of word w = column 32w + b)."""
+    w = np.asarray(words, np.uint32)
+    bits = (w[..., None] >> np.arange(32, dtype=np.uint32)) & 1
+    return bits.reshape(w.shape[0], 128, 128).astype(bool)
+
+
+@pytest.mark.parametrize("case", ["c2", "tree", "ragged", "dense"])
+def test_tile_masks_bit_exact(case):
+    rng = np.random.default_rng(31)
+    st = {"c2": lambda: W.config_structure(2),
+          "tree": lambda: W.config_structure(4),
+          "ragged": lambda: W.random_tree(rng, n_nodes=17, max_len=200),
+          "dense": lambda: W.grpo_structure([(150, [90, 33]), (0, [200])])}[case]()
+    bm = gpu_blockmap(st)
+    if case == "dense":
+        bm = bm.dense()
+    lst = bm.export()
+    mk = bm.export_masks()
+    dense = orc.dense_mask(orc.structure_labels(st)).astype(bool)
+    T = st.T
+    pad = np.zeros((bm.nq * 128, bm.nk * 128), bool)
+    pad[:T, :T] = dense
+    rows, cols = unpack_bits(mk["mask_rows"]), unpack_bits(mk["mask_cols"])
+    seen = set()
+    for i in range(bm.nq):
+        for e in range(lst["q_ptr"][i], lst["q_ptr"][i + 1]):
+            j, kind, s = lst["kv_idx"][e], lst["kind"][e], mk["pidx"][e]
+            want = pad[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
+            if kind == 1:
+                assert s == -1 and want.all()
+                continue
+            assert s >= 0 and s not in seen
+            seen.add(s)
+            np.testing.assert_array_equal(rows[s], want)
+            np.testing.assert_array_equal(cols[s], want.T)
+    assert len(seen) == bm.nnz - bm.n_full
+    # the kv-major list points at the same slots
+    for j in range(bm.nk):
+        for e in range(lst["k_ptr"][j], lst["k_ptr"][j + 1]):
+            i, s = lst["q_idx"][e], mk["pidxT"][e]
+            row_e = lst["q_ptr"][i] + np.searchsorted(lst["kv_idx"][lst["q_ptr"][i]:lst["q_ptr"][i + 1]], j)
+            assert s == mk["pidx"][row_e]
