@@ -144,6 +144,11 @@ pt_status pt_blockmap_export(const pt_blockmap* bm, int32_t* q_ptr, int32_t* kv_
 pt_status pt_blockmap_export_masks(const pt_blockmap* bm, int32_t* pidx, int32_t* pidxT, uint32_t* mask_rows,
                                    uint32_t* mask_cols);
 
+/* Release a map.  Its device memory comes from a stream-ordered pool private
+ * to the library and is returned in the order of the stream the map was built
+ * on, so no device synchronisation happens here.  That stream must still
+ * exist, and work that uses the map on other streams must be complete (or
+ * ordered before this call on the build stream).  NULL is ignored. */
 void pt_blockmap_free(pt_blockmap* bm);
 
 /* ---------------------------------------------------------------------------
@@ -188,8 +193,11 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
 
 /* Bytes of scratch pt_attn_bwd needs: two fp32 row statistics of [Hq, Tpad]
  * entries each, Tpad = ceil(T / 128) * 128 -- Delta = rowsum(dO * O) and
- * LSE * log2(e) -- each rounded up to 256 bytes.  D is accepted for future
- * layouts and does not change the size today. */
+ * LSE * log2(e) -- then room for fp32 partial sums, 128 x 2D floats per slot,
+ * min(256, 2 * ceil(T/128) * Hq) slots, each part rounded up to 256 bytes.
+ * The partial sums let the tensor-core backward split long kv-major columns
+ * across SMs; a smaller workspace (at least the two statistics) is accepted
+ * and only splits less. */
 size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
 
 /* ---------------------------------------------------------------------------

@@ -1,6 +1,7 @@
 // pt_api.cu -- the extern "C" entry points declared in include/pt.h:
 // argument validation, error reporting, dispatch to the kernels, and the
 // TMA tensor-map helper.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -172,6 +173,13 @@ bool use_tensor_cores(pt_dtype dtype, int D, const pt_blockmap* bm) {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Partial-sum slots the backward may use to split long kv-major columns
+// across SMs: enough for a few chunks per SM, never more than the columns.
+size_t partial_slots(int T, int Hq) {
+  const size_t cols = ((size_t)T + 127) / 128 * (size_t)Hq;
+  return std::min<size_t>(256, 2 * cols);
+}
+
 }  // namespace
 
 extern "C" {
@@ -301,10 +309,9 @@ pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtyp
 }
 
 size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D) {
-  (void)D;
-  if (T <= 0 || Hq <= 0) return 256;
+  if (T <= 0 || Hq <= 0 || D <= 0) return 256;
   const size_t tpad = ((size_t)T + 127) / 128 * 128;
-  return 2 * round256(sizeof(float) * tpad * Hq);
+  return 2 * round256(sizeof(float) * tpad * Hq) + round256(partial_slots(T, Hq) * 128 * 2 * sizeof(float) * D);
 }
 
 pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
@@ -313,19 +320,24 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
                       cudaStream_t stream) {
   pt_status st = check_attn("pt_attn_bwd", dtype, T, Hq, Hkv, D, bm, {dO, Q, K, V, O, LSE, dQ, dK, dV});
   if (st != PT_OK || T == 0) return st;
-  size_t need = pt_bwd_workspace_bytes(T, Hq, D);
+  // the two row statistics are required; partial-sum room beyond them is optional
+  const size_t need = 2 * round256(sizeof(float) * (((size_t)T + 127) / 128 * 128) * Hq);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
-    set_error("pt_attn_bwd: workspace must be 256-byte aligned and hold %zu bytes (got %zu)", need,
-              workspace_bytes);
+    set_error("pt_attn_bwd: workspace must be 256-byte aligned and hold at least %zu bytes (got %zu; %zu advised)",
+              need, workspace_bytes, pt_bwd_workspace_bytes(T, Hq, D));
     return PT_ERR_INVALID_ARG;
   }
   if (!(scale > 0.0f)) scale = 1.0f / sqrtf((float)D);
   const size_t tpad = ((size_t)T + 127) / 128 * 128;
+  const size_t stats = round256(sizeof(float) * tpad * Hq);
   float* delta = static_cast<float*>(workspace);
-  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(sizeof(float) * tpad * Hq));
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + stats);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * stats);
+  const size_t partial_bytes = workspace_bytes - 2 * stats;
   if (dtype == PT_BF16) {
     if (use_tensor_cores(dtype, D, bm) && pt::bwd_tc_supported(D))
-      return as_status(pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, lse2, stream));
+      return as_status(pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, lse2, partial,
+                                  partial_bytes, stream));
     if (D % 8 != 0) {
       set_error("pt_attn_bwd: bf16 needs head_dim %% 8 == 0 (got %d)", D);
       return PT_ERR_UNSUPPORTED;

@@ -12,6 +12,7 @@
 #include <climits>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <numeric>
 #include <vector>
 
@@ -373,168 +374,296 @@ __global__ void k_dense_lists(int nq, int nk, int* q_ptr, int* kv_idx, uint8_t* 
   if (e <= nk) k_ptr[e] = (int)(e * nq);
 }
 
-template <class T>
-int dalloc(T** p, size_t n) {
-  if (n == 0) n = 1;
-  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T));
+// Longest-first order on the device: element i goes to position
+// #{j : cnt[j] > cnt[i] or (cnt[j] == cnt[i] and j < i)}.  One warp per element.
+__global__ void k_lpt(const int* cnt, int n, int* order) {
+  int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (i >= n) return;
+  const int ci = cnt[i];
+  int rank = 0;
+  for (int j = lane; j < n; j += 32) {
+    const int cj = cnt[j];
+    rank += (cj > ci) || (cj == ci && j < i);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+  if (lane == 0) order[rank] = i;
+}
+
+}  // namespace
+
+constexpr int kMaxDev = 64;
+
+// ---------------------------------------------------------------------------
+// host side: memory
+// ---------------------------------------------------------------------------
+// Device memory comes from a private stream-ordered pool per device that
+// keeps freed blocks for reuse, so building and freeing maps never
+// synchronises the device.
+
+cudaMemPool_t pool_for(int dev) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDev] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 0 || dev >= kMaxDev) return nullptr;
+  if (!pools[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p;
+    if (cudaMemPoolCreate(&p, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = UINT64_MAX;
+    cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev] = p;
+  }
+  return pools[dev];
+}
+
+int pool_alloc(void** p, size_t bytes, int dev, cudaStream_t s) {
+  *p = nullptr;
+  cudaMemPool_t pool = pool_for(dev);
+  if (!pool) {
+    set_error("cannot create a device memory pool on device %d", dev);
+    return 3;
+  }
+  cudaError_t e = cudaMallocFromPoolAsync(p, bytes ? bytes : 256, pool, s);
   if (e != cudaSuccess) {
     *p = nullptr;
-    set_error("cudaMalloc of %zu bytes failed: %s", n * sizeof(T), cudaGetErrorString(e));
+    set_error("device allocation of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
     return 5;
   }
   return 0;
 }
 
-#define PT_TRY(x)         \
-  do {                    \
-    int rc_ = (x);        \
-    if (rc_) return rc_;  \
-  } while (0)
-
-// Longest-first order: most entries first, ties by index.
-void lpt_order(const std::vector<int>& cnt, std::vector<int>& order) {
-  order.resize(cnt.size());
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cnt[a] > cnt[b]; });
+void pool_free(void* p, cudaStream_t s) {
+  if (p) cudaFreeAsync(p, s);
 }
 
-// Shared tail of every builder: given tok, node_of and node tables on the
-// device, classify, count, list and order.
-int finish_map(pt_blockmap* bm, cudaStream_t s) {
-  ProfScope ps(s, "blockmap_classify");
-  const int nq = bm->nq, nk = bm->nk;
-  const long long ntiles = (long long)nq * nk;
-  uint8_t* kinds = nullptr;
-  int *row_cnt = nullptr, *col_cnt = nullptr, *counters = nullptr, *tmp = nullptr;
-  int rc = 0;
-  do {
-    if ((rc = dalloc(&kinds, (size_t)ntiles))) break;
-    if ((rc = dalloc(&row_cnt, nq))) break;
-    if ((rc = dalloc(&col_cnt, nk))) break;
-    if ((rc = dalloc(&counters, 4))) break;
-    if ((rc = dalloc(&tmp, (size_t)std::max(nq, nk) / kScanBlock + 2))) break;
-    if ((rc = dalloc(&bm->q_ptr, nq + 1))) break;
-    if ((rc = dalloc(&bm->k_ptr, nk + 1))) break;
-    if (cudaMemsetAsync(counters, 0, 4 * sizeof(int), s) != cudaSuccess) { rc = 3; break; }
-    if (ntiles > 0) {
-      long long threads = ntiles * 32;
-      k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
-                                                                   bm->node_start, bm->node_end, bm->parent, kinds);
-      k_counts<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, row_cnt, counters);
-      k_counts<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, col_cnt, counters);
-      count_launch(3);
-    }
-    if ((rc = exclusive_scan(row_cnt, nq, bm->q_ptr, tmp, s))) break;
-    if ((rc = exclusive_scan(col_cnt, nk, bm->k_ptr, tmp, s))) break;
-    std::vector<int> hq(nq), hk(nk);
-    int nnz = 0, nfull = 0;
-    if (nq && cudaMemcpyAsync(hq.data(), row_cnt, nq * sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) { rc = 3; break; }
-    if (nk && cudaMemcpyAsync(hk.data(), col_cnt, nk * sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) { rc = 3; break; }
-    if (cudaMemcpyAsync(&nnz, bm->q_ptr + nq, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) { rc = 3; break; }
-    if (cudaMemcpyAsync(&nfull, counters, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) { rc = 3; break; }
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) {
-      set_error("block map build failed: %s", cudaGetErrorString(e));
-      rc = 3;
-      break;
-    }
-    bm->nnz = nnz;
-    bm->n_full = nfull;
-    if ((rc = dalloc(&bm->kv_idx, nnz))) break;
-    if ((rc = dalloc(&bm->kind, nnz))) break;
-    if ((rc = dalloc(&bm->q_idx, nnz))) break;
-    if ((rc = dalloc(&bm->kindT, nnz))) break;
-    if ((rc = dalloc(&bm->q_order, nq))) break;
-    if ((rc = dalloc(&bm->k_order, nk))) break;
-    if ((rc = dalloc(&bm->pidx, nnz))) break;
-    if ((rc = dalloc(&bm->pidxT, nnz))) break;
-    bm->n_partial = nnz - nfull;
-    const bool masks = bm->BM == 128 && bm->BN == 128 && bm->n_partial > 0;
-    if (masks) {
-      if ((rc = dalloc(&bm->mask_rows, (size_t)bm->n_partial * 512))) break;
-      if ((rc = dalloc(&bm->mask_cols, (size_t)bm->n_partial * 512))) break;
-    }
-    if (ntiles > 0 && nnz > 0) {
-      int* pflag = nullptr;
-      int* pscan = nullptr;
-      int* stmp = nullptr;
-      int2* slot_tile = nullptr;
-      if ((rc = dalloc(&pflag, nnz))) break;
-      if ((rc = dalloc(&pscan, (size_t)nnz + 1)) || (rc = dalloc(&stmp, (size_t)nnz / kScanBlock + 2)) ||
-          (rc = dalloc(&slot_tile, std::max<int64_t>(bm->n_partial, 1)))) {
-        cudaFree(pflag);
-        cudaFree(pscan);
-        cudaFree(stmp);
-        break;
-      }
-      k_fill<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, bm->q_ptr, bm->kv_idx, bm->kind, pflag,
-                                                     nullptr, nullptr, nullptr, nullptr);
-      count_launch();
-      rc = exclusive_scan(pflag, nnz, pscan, stmp, s);
-      if (!rc) {
-        k_slots<<<(nq * 32 + 255) / 256, 256, 0, s>>>(nq, bm->q_ptr, bm->kv_idx, bm->kind, pscan, bm->pidx,
-                                                       slot_tile);
-        k_fill<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, bm->k_ptr, bm->q_idx, bm->kindT, nullptr,
-                                                       bm->q_ptr, bm->kv_idx, bm->pidx, bm->pidxT);
-        count_launch(2);
-        if (masks) {
-          k_masks<<<(unsigned)bm->n_partial, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
-          count_launch();
-        }
-      }
-      cudaError_t le = cudaStreamSynchronize(s);
-      cudaFree(pflag);
-      cudaFree(pscan);
-      cudaFree(stmp);
-      cudaFree(slot_tile);
-      if (rc) break;
-      if (le != cudaSuccess) {
-        set_error("block map lists failed: %s", cudaGetErrorString(le));
-        rc = 3;
-        break;
-      }
-    }
-    std::vector<int> oq, ok;
-    lpt_order(hq, oq);
-    lpt_order(hk, ok);
-    if (nq && cudaMemcpyAsync(bm->q_order, oq.data(), nq * sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess) { rc = 3; break; }
-    if (nk && cudaMemcpyAsync(bm->k_order, ok.data(), nk * sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess) { rc = 3; break; }
-    e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) {
-      set_error("block map build failed: %s", cudaGetErrorString(e));
-      rc = 3;
-      break;
-    }
-  } while (0);
-  cudaFree(kinds);
-  cudaFree(row_cnt);
-  cudaFree(col_cnt);
-  cudaFree(counters);
-  cudaFree(tmp);
-  return rc;
+// Sub-array layout inside one allocation, 256-byte aligned pieces.
+struct Layout {
+  size_t off = 0;
+  template <class T>
+  size_t add(size_t n) {
+    size_t o = off;
+    off += (n * sizeof(T) + 255) & ~size_t(255);
+    return o;
+  }
+};
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
 
-pt_blockmap* new_map(int T, int BM, int BN) {
+// Pinned staging for host->device uploads of node tables (avoids the stream
+// synchronisation a pageable copy implies).  Reused across builds; an event
+// guards against overwriting data a previous upload has not read yet.
+int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
+  struct Staging {
+    void* host = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;
+  };
+  static std::mutex mu;
+  static Staging st[kMaxDev];
+  if (bytes == 0) return 0;
+  if (dev < 0 || dev >= kMaxDev) return 3;
+  std::lock_guard<std::mutex> lk(mu);
+  Staging& g = st[dev];
+  if (g.done) cudaEventSynchronize(g.done);
+  else if (cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming) != cudaSuccess) return 3;
+  if (g.cap < bytes) {
+    if (g.host) cudaFreeHost(g.host);
+    g.host = nullptr;
+    g.cap = 0;
+    size_t cap = bytes < (1u << 20) ? (1u << 20) : bytes;
+    if (cudaHostAlloc(&g.host, cap, cudaHostAllocDefault) != cudaSuccess) {
+      set_error("pinned staging allocation of %zu bytes failed", cap);
+      return 5;
+    }
+    g.cap = cap;
+  }
+  std::memcpy(g.host, src, bytes);
+  if (cudaMemcpyAsync(dst, g.host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    set_error("block map upload failed");
+    return 3;
+  }
+  cudaEventRecord(g.done, s);
+  return 0;
+}
+
+namespace {
+
+// The part of a map whose size is known before classification: token
+// coordinates, node tables, list pointers and orders.
+int new_map(int T, int BM, int BN, int node_cap, cudaStream_t s, pt_blockmap** out) {
   pt_blockmap* bm = new pt_blockmap;
   std::memset(bm, 0, sizeof(*bm));
   cudaGetDevice(&bm->device);
+  bm->stream = s;
   bm->T = T;
   bm->BM = BM;
   bm->BN = BN;
   bm->nq = (T + BM - 1) / BM;
   bm->nk = (T + BN - 1) / BN;
   bm->tpad = std::max(bm->nq * BM, bm->nk * BN);
-  return bm;
+  Layout L;
+  size_t o_tok = L.add<pt_tok>(bm->tpad), o_node = L.add<int>(T), o_ns = L.add<int>(node_cap),
+         o_ne = L.add<int>(node_cap), o_par = L.add<int>(node_cap), o_qp = L.add<int>(bm->nq + 1),
+         o_kp = L.add<int>(bm->nk + 1), o_qo = L.add<int>(bm->nq), o_ko = L.add<int>(bm->nk);
+  int rc = pool_alloc(&bm->mem_fixed, L.off, bm->device, s);
+  if (rc) {
+    delete bm;
+    return rc;
+  }
+  bm->tok = at<pt_tok>(bm->mem_fixed, o_tok);
+  bm->node_of = at<int>(bm->mem_fixed, o_node);
+  bm->node_start = at<int>(bm->mem_fixed, o_ns);
+  bm->node_end = at<int>(bm->mem_fixed, o_ne);
+  bm->parent = at<int>(bm->mem_fixed, o_par);
+  bm->q_ptr = at<int>(bm->mem_fixed, o_qp);
+  bm->k_ptr = at<int>(bm->mem_fixed, o_kp);
+  bm->q_order = at<int>(bm->mem_fixed, o_qo);
+  bm->k_order = at<int>(bm->mem_fixed, o_ko);
+  *out = bm;
+  return 0;
+}
+
+// The lists part, once nnz and the number of partial tiles are known.
+int alloc_lists(pt_blockmap* bm, cudaStream_t s) {
+  const int64_t nnz = bm->nnz;
+  const bool masks = bm->BM == 128 && bm->BN == 128 && bm->n_partial > 0;
+  Layout L;
+  size_t o_kv = L.add<int>(nnz), o_kd = L.add<uint8_t>(nnz), o_pi = L.add<int>(nnz), o_qi = L.add<int>(nnz),
+         o_kt = L.add<uint8_t>(nnz), o_pt = L.add<int>(nnz);
+  size_t o_mr = masks ? L.add<uint32_t>((size_t)bm->n_partial * 512) : 0;
+  size_t o_mc = masks ? L.add<uint32_t>((size_t)bm->n_partial * 512) : 0;
+  int rc = pool_alloc(&bm->mem_lists, L.off, bm->device, s);
+  if (rc) return rc;
+  bm->kv_idx = at<int>(bm->mem_lists, o_kv);
+  bm->kind = at<uint8_t>(bm->mem_lists, o_kd);
+  bm->pidx = at<int>(bm->mem_lists, o_pi);
+  bm->q_idx = at<int>(bm->mem_lists, o_qi);
+  bm->kindT = at<uint8_t>(bm->mem_lists, o_kt);
+  bm->pidxT = at<int>(bm->mem_lists, o_pt);
+  bm->mask_rows = masks ? at<uint32_t>(bm->mem_lists, o_mr) : nullptr;
+  bm->mask_cols = masks ? at<uint32_t>(bm->mem_lists, o_mc) : nullptr;
+  return 0;
+}
+
+#define PT_LAUNCHED(n)                                                          \
+  do {                                                                          \
+    count_launch(n);                                                            \
+    cudaError_t le_ = cudaGetLastError();                                       \
+    if (le_ != cudaSuccess) {                                                   \
+      set_error("block map kernel launch failed: %s", cudaGetErrorString(le_)); \
+      rc = 3;                                                                   \
+      break;                                                                    \
+    }                                                                           \
+  } while (0)
+
+// Shared tail of the builders: given tok, node_of and node tables on the
+// device, classify, count, list, order and mask.  Synchronises the stream
+// once (to size the lists); everything after that is asynchronous.
+int finish_map(pt_blockmap* bm, cudaStream_t s) {
+  ProfScope ps(s, "blockmap_classify");
+  const int nq = bm->nq, nk = bm->nk, dev = bm->device;
+  const long long ntiles = (long long)nq * nk;
+  void* tmpA = nullptr;
+  void* tmpB = nullptr;
+  int rc = 0;
+  do {
+    Layout LA;
+    // counters | row counts | column counts, contiguous so one copy brings them to the host
+    size_t o_kinds = LA.add<uint8_t>((size_t)ntiles), o_cnt = LA.add<int>((size_t)4 + nq + nk),
+           o_st = LA.add<int>((size_t)std::max(nq, nk) / kScanBlock + 2);
+    if ((rc = pool_alloc(&tmpA, LA.off, dev, s))) break;
+    uint8_t* kinds = at<uint8_t>(tmpA, o_kinds);
+    int* counters = at<int>(tmpA, o_cnt);
+    int* row_cnt = counters + 4;
+    int* col_cnt = row_cnt + nq;
+    int* stmp = at<int>(tmpA, o_st);
+    if (cudaMemsetAsync(counters, 0, 4 * sizeof(int), s) != cudaSuccess) {
+      rc = 3;
+      break;
+    }
+    if (ntiles > 0) {
+      long long threads = ntiles * 32;
+      k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
+                                                                   bm->node_start, bm->node_end, bm->parent, kinds);
+      k_counts<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, row_cnt, counters);
+      k_counts<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, col_cnt, counters);
+      PT_LAUNCHED(3);
+      k_lpt<<<(nq * 32 + 255) / 256, 256, 0, s>>>(row_cnt, nq, bm->q_order);
+      k_lpt<<<(nk * 32 + 255) / 256, 256, 0, s>>>(col_cnt, nk, bm->k_order);
+      PT_LAUNCHED(2);
+    }
+    if ((rc = exclusive_scan(row_cnt, nq, bm->q_ptr, stmp, s))) break;
+    if ((rc = exclusive_scan(col_cnt, nk, bm->k_ptr, stmp, s))) break;
+    // the one synchronisation of the build: list sizes to the host
+    bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * (4 + (size_t)nq + nk)));
+    if (!bm->h_counts) {
+      rc = 5;
+      break;
+    }
+    if (cudaMemcpyAsync(bm->h_counts, counters, sizeof(int) * (4 + (size_t)nq + nk), cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess) {
+      rc = 3;
+      break;
+    }
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+      set_error("block map build failed: %s", cudaGetErrorString(e));
+      rc = 3;
+      break;
+    }
+    bm->h_row_cnt = bm->h_counts + 4;
+    bm->h_col_cnt = bm->h_row_cnt + nq;
+    int64_t nnz_h = 0;
+    for (int i = 0; i < nq; ++i) nnz_h += bm->h_row_cnt[i];
+    bm->nnz = nnz_h;
+    bm->n_full = bm->h_counts[0];
+    bm->n_partial = bm->nnz - bm->n_full;
+    if ((rc = alloc_lists(bm, s))) break;
+    const int64_t nnz = bm->nnz;
+    if (ntiles > 0 && nnz > 0) {
+      Layout LB;
+      size_t o_pf = LB.add<int>(nnz), o_ps = LB.add<int>(nnz + 1), o_s2 = LB.add<int>(nnz / kScanBlock + 2),
+             o_sl = LB.add<int2>(std::max<int64_t>(bm->n_partial, 1));
+      if ((rc = pool_alloc(&tmpB, LB.off, dev, s))) break;
+      int* pflag = at<int>(tmpB, o_pf);
+      int* pscan = at<int>(tmpB, o_ps);
+      int* stmp2 = at<int>(tmpB, o_s2);
+      int2* slot_tile = at<int2>(tmpB, o_sl);
+      k_fill<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, bm->q_ptr, bm->kv_idx, bm->kind, pflag,
+                                                     nullptr, nullptr, nullptr, nullptr);
+      PT_LAUNCHED(1);
+      if ((rc = exclusive_scan(pflag, (int)nnz, pscan, stmp2, s))) break;
+      k_slots<<<(nq * 32 + 255) / 256, 256, 0, s>>>(nq, bm->q_ptr, bm->kv_idx, bm->kind, pscan, bm->pidx, slot_tile);
+      k_fill<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, bm->k_ptr, bm->q_idx, bm->kindT, nullptr,
+                                                     bm->q_ptr, bm->kv_idx, bm->pidx, bm->pidxT);
+      PT_LAUNCHED(2);
+      if (bm->mask_rows) {
+        k_masks<<<(unsigned)bm->n_partial, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
+        PT_LAUNCHED(1);
+      }
+    }
+  } while (0);
+  pool_free(tmpA, s);
+  pool_free(tmpB, s);
+  return rc;
 }
 
 }  // namespace
 
 void free_map(pt_blockmap* bm) {
   if (!bm) return;
-  void* ptrs[] = {bm->tok, bm->node_of, bm->node_start, bm->node_end, bm->parent, bm->q_ptr, bm->kv_idx,
-                  bm->kind, bm->k_ptr, bm->q_idx, bm->kindT, bm->q_order, bm->k_order, bm->pidx, bm->pidxT,
-                  bm->mask_rows, bm->mask_cols};
-  for (void* p : ptrs) cudaFree(p);
+  pool_free(bm->bwd_mem, bm->stream);
+  std::free(bm->h_counts);
+  pool_free(bm->mem_lists, bm->stream);
+  pool_free(bm->mem_fixed, bm->stream);
   delete bm;
 }
 
@@ -595,21 +724,29 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
       set_error("pt_build_blockmap_tree: node %d is on no sample path", i);
       return 1;
     }
-  // Euler tour: tin = pre-order index, tout = tin + subtree size.
-  std::vector<int> start(n_nodes), end(n_nodes), tin(n_nodes), tout(n_nodes), subtree(n_nodes, 1);
-  long long off = 0;
-  for (int i = 0; i < n_nodes; ++i) {
-    start[i] = (int)off;
-    off += node_lengths[i];
-    end[i] = (int)off;
+  if (BM <= 0 || BN <= 0) {
+    set_error("pt_build_blockmap_tree: tile sizes must be positive (got %d x %d)", BM, BN);
+    return 1;
   }
-  for (int i = n_nodes - 1; i >= 0; --i)
-    if (parent[i] >= 0) subtree[parent[i]] += subtree[i];
+  // Node tables in one host block: start | end | parent | tin | tout.
+  // Euler tour: tin = pre-order index (children in id order), tout = tin + subtree size.
+  const int N = n_nodes;
+  std::vector<int> tab((size_t)5 * std::max(N, 1));
+  int *start = tab.data(), *end = start + N, *par = end + N, *tin = par + N, *tout = tin + N;
   {
-    // children in id order; pre-order numbering
-    std::vector<std::vector<int>> ch(n_nodes);
+    long long off = 0;
+    for (int i = 0; i < N; ++i) {
+      start[i] = (int)off;
+      off += node_lengths[i];
+      end[i] = (int)off;
+      par[i] = parent[i];
+    }
+    std::vector<int> subtree(N, 1);
+    for (int i = N - 1; i >= 0; --i)
+      if (parent[i] >= 0) subtree[parent[i]] += subtree[i];
+    std::vector<std::vector<int>> ch(N);
     std::vector<int> roots;
-    for (int i = 0; i < n_nodes; ++i) (parent[i] < 0 ? roots : ch[parent[i]]).push_back(i);
+    for (int i = 0; i < N; ++i) (parent[i] < 0 ? roots : ch[parent[i]]).push_back(i);
     int counter = 0;
     std::vector<int> stack(roots.rbegin(), roots.rend());
     while (!stack.empty()) {
@@ -620,43 +757,29 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
       for (auto it = ch[u].rbegin(); it != ch[u].rend(); ++it) stack.push_back(*it);
     }
   }
-  if (BM <= 0 || BN <= 0) {
-    set_error("pt_build_blockmap_tree: tile sizes must be positive (got %d x %d)", BM, BN);
-    return 1;
-  }
-  pt_blockmap* bm = new_map((int)T, BM, BN);
-  bm->n_nodes = n_nodes;
-  int* d_tin = nullptr;
-  int* d_tout = nullptr;
-  int rc = 0;
+  pt_blockmap* bm = nullptr;
+  int rc = new_map((int)T, BM, BN, N, s, &bm);
+  if (rc) return rc;
+  bm->n_nodes = N;
+  void* dtab = nullptr;
   do {
-    if ((rc = dalloc(&bm->tok, bm->tpad))) break;
-    if ((rc = dalloc(&bm->node_of, T))) break;
-    if ((rc = dalloc(&bm->node_start, n_nodes))) break;
-    if ((rc = dalloc(&bm->node_end, n_nodes))) break;
-    if ((rc = dalloc(&bm->parent, n_nodes))) break;
-    if ((rc = dalloc(&d_tin, n_nodes))) break;
-    if ((rc = dalloc(&d_tout, n_nodes))) break;
-    size_t nb = sizeof(int) * n_nodes;
-    if (n_nodes &&
-        (cudaMemcpyAsync(bm->node_start, start.data(), nb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-         cudaMemcpyAsync(bm->node_end, end.data(), nb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-         cudaMemcpyAsync(bm->parent, parent.data(), nb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-         cudaMemcpyAsync(d_tin, tin.data(), nb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-         cudaMemcpyAsync(d_tout, tout.data(), nb, cudaMemcpyHostToDevice, s) != cudaSuccess)) {
-      set_error("pt_build_blockmap_tree: upload failed");
-      rc = 3;
-      break;
+    if ((rc = pool_alloc(&dtab, sizeof(int) * (size_t)2 * std::max(N, 1), bm->device, s))) break;
+    // start, end, parent go straight into the map; tin, tout into a temporary
+    if (N > 0) {
+      if ((rc = upload(bm->node_start, start, sizeof(int) * N, bm->device, s))) break;
+      if ((rc = upload(bm->node_end, end, sizeof(int) * N, bm->device, s))) break;
+      if ((rc = upload(bm->parent, par, sizeof(int) * N, bm->device, s))) break;
+      if ((rc = upload(dtab, tin, sizeof(int) * (size_t)2 * N, bm->device, s))) break;
     }
     if (bm->tpad > 0) {
-      k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>((int)T, bm->tpad, n_nodes, bm->node_end, d_tin, d_tout,
+      int* d_tin = static_cast<int*>(dtab);
+      k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>((int)T, bm->tpad, N, bm->node_end, d_tin, d_tin + N,
                                                            bm->tok, bm->node_of);
-      count_launch();
+      PT_LAUNCHED(1);
     }
-    rc = finish_map(bm, s);  // synchronises s
+    rc = finish_map(bm, s);
   } while (0);
-  cudaFree(d_tin);
-  cudaFree(d_tout);
+  pool_free(dtab, s);
   if (rc) {
     free_map(bm);
     return rc;
@@ -675,28 +798,23 @@ int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int3
     set_error("pt_build_blockmap_seg: tile sizes must be positive (got %d x %d)", BM, BN);
     return 1;
   }
-  pt_blockmap* bm = new_map(T, BM, BN);
-  int *flags = nullptr, *excl = nullptr, *gseen = nullptr, *sseen = nullptr, *err = nullptr, *tmp = nullptr;
-  int *gfirst = nullptr, *glast = nullptr, *tin = nullptr, *tout = nullptr;
-  int rc = 0;
+  pt_blockmap* bm = nullptr;
+  int rc = new_map(T, BM, BN, std::max(T, 1), s, &bm);
+  if (rc) return rc;
+  void* tmp = nullptr;
   do {
-    if ((rc = dalloc(&bm->tok, bm->tpad))) break;
-    if ((rc = dalloc(&bm->node_of, T))) break;
-    if ((rc = dalloc(&bm->node_start, T))) break;
-    if ((rc = dalloc(&bm->node_end, T))) break;
-    if ((rc = dalloc(&bm->parent, T))) break;
-    if ((rc = dalloc(&flags, T))) break;
-    if ((rc = dalloc(&excl, (size_t)T + 1))) break;
-    if ((rc = dalloc(&gseen, T))) break;
-    if ((rc = dalloc(&sseen, T))) break;
-    if ((rc = dalloc(&gfirst, T))) break;
-    if ((rc = dalloc(&glast, T))) break;
-    if ((rc = dalloc(&tin, T))) break;
-    if ((rc = dalloc(&tout, T))) break;
-    if ((rc = dalloc(&err, 1))) break;
-    if ((rc = dalloc(&tmp, (size_t)T / kScanBlock + 2))) break;
-    if (cudaMemsetAsync(gseen, 0, sizeof(int) * std::max(T, 1), s) != cudaSuccess ||
-        cudaMemsetAsync(sseen, 0, sizeof(int) * std::max(T, 1), s) != cudaSuccess ||
+    Layout L;
+    const int Tc = std::max(T, 1);
+    size_t o_fl = L.add<int>(Tc), o_ex = L.add<int>((size_t)Tc + 1), o_gs = L.add<int>(Tc), o_ss = L.add<int>(Tc),
+           o_gf = L.add<int>(Tc), o_gl = L.add<int>(Tc), o_ti = L.add<int>(Tc), o_to = L.add<int>(Tc),
+           o_er = L.add<int>(1), o_st = L.add<int>((size_t)Tc / kScanBlock + 2);
+    if ((rc = pool_alloc(&tmp, L.off, bm->device, s))) break;
+    int *flags = at<int>(tmp, o_fl), *excl = at<int>(tmp, o_ex), *gseen = at<int>(tmp, o_gs),
+        *sseen = at<int>(tmp, o_ss), *gfirst = at<int>(tmp, o_gf), *glast = at<int>(tmp, o_gl),
+        *tin = at<int>(tmp, o_ti), *tout = at<int>(tmp, o_to), *err = at<int>(tmp, o_er),
+        *stmp = at<int>(tmp, o_st);
+    if (cudaMemsetAsync(gseen, 0, sizeof(int) * Tc, s) != cudaSuccess ||
+        cudaMemsetAsync(sseen, 0, sizeof(int) * Tc, s) != cudaSuccess ||
         cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) {
       rc = 3;
       break;
@@ -706,8 +824,8 @@ int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int3
       int nb = (T + 255) / 256;
       k_seg_flags<<<nb, 256, 0, s>>>(group_id, suffix_id, T, flags, gseen, sseen, err);
       k_seen_check<<<nb, 256, 0, s>>>(gseen, sseen, T, err);
-      count_launch(2);
-      if ((rc = exclusive_scan(flags, T, excl, tmp, s))) break;
+      PT_LAUNCHED(2);
+      if ((rc = exclusive_scan(flags, T, excl, stmp, s))) break;
       if (cudaMemcpyAsync(&R, excl + T, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
           cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
           cudaStreamSynchronize(s) != cudaSuccess) {
@@ -727,17 +845,16 @@ int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int3
                                      gfirst, glast);
       k_seg_tree<<<(R + 255) / 256, 256, 0, s>>>(group_id, suffix_id, R, bm->node_start, gfirst, glast, bm->parent,
                                                  tin, tout);
-      count_launch(2);
+      PT_LAUNCHED(2);
     }
     bm->n_nodes = R;
     if (bm->tpad > 0) {
       k_seg_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>(T, bm->tpad, bm->node_of, tin, tout, bm->tok);
-      count_launch();
+      PT_LAUNCHED(1);
     }
     rc = finish_map(bm, s);
   } while (0);
-  int* tmps[] = {flags, excl, gseen, sseen, err, tmp, gfirst, glast, tin, tout};
-  for (int* p : tmps) cudaFree(p);
+  pool_free(tmp, s);
   if (rc) {
     free_map(bm);
     return rc;
@@ -747,79 +864,67 @@ int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int3
 }
 
 int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out) {
-  pt_blockmap* bm = new_map(src->T, src->BM, src->BN);
+  pt_blockmap* bm = nullptr;
+  int rc = new_map(src->T, src->BM, src->BN, std::max(src->n_nodes, 1), s, &bm);
+  if (rc) return rc;
   bm->n_nodes = src->n_nodes;
   bm->dense = true;
   const int nq = bm->nq, nk = bm->nk;
   const long long n = (long long)nq * nk;
-  int rc = 0;
+  void* tmp = nullptr;
   do {
-    if (n > INT_MAX) {
+    if (n > INT_MAX / 32) {
       set_error("pt_blockmap_dense: %lld tiles is too many", n);
       rc = 2;
       break;
     }
-    if ((rc = dalloc(&bm->tok, bm->tpad))) break;
-    if ((rc = dalloc(&bm->node_of, bm->T))) break;
-    if ((rc = dalloc(&bm->node_start, std::max(1, bm->n_nodes)))) break;
-    if ((rc = dalloc(&bm->node_end, std::max(1, bm->n_nodes)))) break;
-    if ((rc = dalloc(&bm->parent, std::max(1, bm->n_nodes)))) break;
-    if ((rc = dalloc(&bm->q_ptr, nq + 1))) break;
-    if ((rc = dalloc(&bm->k_ptr, nk + 1))) break;
-    if ((rc = dalloc(&bm->kv_idx, n))) break;
-    if ((rc = dalloc(&bm->kind, n))) break;
-    if ((rc = dalloc(&bm->q_idx, n))) break;
-    if ((rc = dalloc(&bm->kindT, n))) break;
-    if ((rc = dalloc(&bm->q_order, nq))) break;
-    if ((rc = dalloc(&bm->k_order, nk))) break;
     if (cudaMemcpyAsync(bm->tok, src->tok, sizeof(pt_tok) * bm->tpad, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
-        (bm->T && cudaMemcpyAsync(bm->node_of, src->node_of, sizeof(int) * bm->T, cudaMemcpyDeviceToDevice, s) != cudaSuccess) ||
+        (bm->T &&
+         cudaMemcpyAsync(bm->node_of, src->node_of, sizeof(int) * bm->T, cudaMemcpyDeviceToDevice, s) != cudaSuccess) ||
         (bm->n_nodes &&
-         (cudaMemcpyAsync(bm->node_start, src->node_start, sizeof(int) * bm->n_nodes, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
-          cudaMemcpyAsync(bm->node_end, src->node_end, sizeof(int) * bm->n_nodes, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
-          cudaMemcpyAsync(bm->parent, src->parent, sizeof(int) * bm->n_nodes, cudaMemcpyDeviceToDevice, s) != cudaSuccess))) {
-      rc = 3;
-      break;
-    }
-    if ((rc = dalloc(&bm->pidx, n))) break;
-    if ((rc = dalloc(&bm->pidxT, n))) break;
-    int2* slot_tile = nullptr;
-    if ((rc = dalloc(&slot_tile, n))) break;
-    const bool masks = bm->BM == 128 && bm->BN == 128 && n > 0;
-    if (masks && ((rc = dalloc(&bm->mask_rows, (size_t)n * 512)) || (rc = dalloc(&bm->mask_cols, (size_t)n * 512)))) {
-      cudaFree(slot_tile);
-      break;
-    }
-    long long cnt = std::max<long long>(n, std::max(nq, nk) + 1);
-    k_dense_lists<<<(unsigned)((cnt + 255) / 256), 256, 0, s>>>(nq, nk, bm->q_ptr, bm->kv_idx, bm->kind, bm->k_ptr,
-                                                                bm->q_idx, bm->kindT, bm->pidx, bm->pidxT, slot_tile);
-    count_launch();
-    if (masks) {
-      k_masks<<<(unsigned)n, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
-      count_launch();
-    }
-    bm->n_partial = n;
-    if (cudaStreamSynchronize(s) != cudaSuccess) {
-      cudaFree(slot_tile);
-      rc = 3;
-      break;
-    }
-    cudaFree(slot_tile);
-    // every row has the same length: natural order (last tiles first is no better)
-    std::vector<int> oq(nq), ok(nk);
-    std::iota(oq.begin(), oq.end(), 0);
-    std::iota(ok.begin(), ok.end(), 0);
-    if ((nq && cudaMemcpyAsync(bm->q_order, oq.data(), nq * sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess) ||
-        (nk && cudaMemcpyAsync(bm->k_order, ok.data(), nk * sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess) ||
-        cudaStreamSynchronize(s) != cudaSuccess) {
+         (cudaMemcpyAsync(bm->node_start, src->node_start, sizeof(int) * bm->n_nodes, cudaMemcpyDeviceToDevice, s) !=
+              cudaSuccess ||
+          cudaMemcpyAsync(bm->node_end, src->node_end, sizeof(int) * bm->n_nodes, cudaMemcpyDeviceToDevice, s) !=
+              cudaSuccess ||
+          cudaMemcpyAsync(bm->parent, src->parent, sizeof(int) * bm->n_nodes, cudaMemcpyDeviceToDevice, s) !=
+              cudaSuccess))) {
+      set_error("pt_blockmap_dense: copy failed");
       rc = 3;
       break;
     }
     bm->nnz = n;
     bm->n_full = 0;
+    bm->n_partial = n;
+    bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * (4 + (size_t)nq + nk)));
+    if (!bm->h_counts) {
+      rc = 5;
+      break;
+    }
+    bm->h_row_cnt = bm->h_counts + 4;
+    bm->h_col_cnt = bm->h_row_cnt + nq;
+    for (int i = 0; i < nq; ++i) bm->h_row_cnt[i] = nk;
+    for (int j = 0; j < nk; ++j) bm->h_col_cnt[j] = nq;
+    if ((rc = alloc_lists(bm, s))) break;
+    if ((rc = pool_alloc(&tmp, sizeof(int2) * (size_t)std::max<long long>(n, 1), bm->device, s))) break;
+    int2* slot_tile = static_cast<int2*>(tmp);
+    long long cnt = std::max<long long>(n, std::max(nq, nk) + 1);
+    k_dense_lists<<<(unsigned)((cnt + 255) / 256), 256, 0, s>>>(nq, nk, bm->q_ptr, bm->kv_idx, bm->kind, bm->k_ptr,
+                                                                bm->q_idx, bm->kindT, bm->pidx, bm->pidxT, slot_tile);
+    PT_LAUNCHED(1);
+    if (bm->mask_rows && n > 0) {
+      k_masks<<<(unsigned)n, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
+      PT_LAUNCHED(1);
+    }
+    // every row has the same length: natural order
+    if (nq > 0 && nk > 0) {
+      std::vector<int> idx(std::max(nq, nk));
+      std::iota(idx.begin(), idx.end(), 0);
+      if ((rc = upload(bm->q_order, idx.data(), sizeof(int) * nq, bm->device, s))) break;
+      if ((rc = upload(bm->k_order, idx.data(), sizeof(int) * nk, bm->device, s))) break;
+    }
   } while (0);
+  pool_free(tmp, s);
   if (rc) {
-    if (rc == 3) set_error("pt_blockmap_dense: CUDA failure");
     free_map(bm);
     return rc;
   }

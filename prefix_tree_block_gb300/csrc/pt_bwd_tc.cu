@@ -32,8 +32,11 @@
 // accumulators (dV, dK: 2D; dQ: D) -- at most 512.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
+#include <mutex>
+#include <vector>
 
 #include "pt_device.cuh"
 #include "pt_internal.h"
@@ -108,9 +111,38 @@ struct BwdParams {
   const float* lse2;      // [Hq, Tpad]
   __nv_bfloat16* out0;    // dK (dkdv) or dQ (dq)
   __nv_bfloat16* out1;    // dV (dkdv)
-  int T, Tpad, Hq, Hkv, n_major;
+  const DkdvItem* items;  // dkdv work items
+  float* partial;         // dkdv: fp32 partial sums of split columns, [slot][128][2D]
+  int T, Tpad, Hq, Hkv, n_major, n_items;
   float scale, scale_log2;
 };
+
+// Sum the chunk partials of every split kv-major column, in chunk order, and
+// write dV (first D columns of a slot row) and dK (last D) as bf16.
+template <int D>
+__global__ void k_dkdv_finalize(const int4* __restrict__ splits, const float* __restrict__ partial, int T, int Hkv,
+                                __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV) {
+  const int4 sp = splits[blockIdx.x];  // kv block, kv head, first slot, slot count
+  for (int idx = threadIdx.x; idx < 128 * 2 * D / 4; idx += blockDim.x) {
+    const int r = idx / (2 * D / 4), c = (idx % (2 * D / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < sp.w; ++k) {
+      const float4 v = *reinterpret_cast<const float4*>(partial + ((size_t)(sp.z + k) * 128 + r) * (2 * D) + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int kv = sp.x * 128 + r;
+    if (kv >= T) continue;
+    __nv_bfloat16* dst = (c < D ? dV : dK) + ((size_t)kv * Hkv + sp.y) * D + (c < D ? c : c - D);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  }
+}
 
 // 64 fp32 values (as bits) -> 32 bf16x2 words.
 __device__ __forceinline__ void pack64(const uint32_t* v, uint32_t* out) {
@@ -189,7 +221,7 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.Hq / p.Hkv;
-  const int n_items = p.n_major * p.Hkv;
+  const int n_items = p.n_items;
 
   if (threadIdx.x == 256) {
     init_bars<S>(B);
@@ -215,9 +247,10 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t sc = 0, it = 0;
       bool ok = true, res_issued = false;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const int jb = p.order[w / p.Hkv], hk = w % p.Hkv;
+        const DkdvItem itm = p.items[w];
+        const int jb = itm.jb, hk = itm.hk;
         const int e0 = p.ptr[jb], ncol = p.ptr[jb + 1] - e0;
-        if (ncol == 0) continue;
+        if (itm.x1 == itm.x0) continue;
         if (it > 0 && !(ok = mbar_wait(&B->res_empty, (it - 1) & 1, abort_flag))) break;
         mbar_expect_tx(&B->res_full, 2 * C::TILE);
 #pragma unroll
@@ -226,10 +259,10 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(smem + L::OFF_V + pn * C::PANEL, &mV, &B->res_full, pn * 64, hk, jb * 128);
         }
         res_issued = true;
-        const int n = g * ncol;
+        const int n = itm.x1 - itm.x0;
         for (int x = 0; x < n; ++x) {
-          const int e = e0 + x % ncol;
-          const int h = hk * g + x / ncol, i = p.idx[e], slot = p.pidx[e];
+          const int e = e0 + (itm.x0 + x) % ncol;
+          const int h = hk * g + (itm.x0 + x) / ncol, i = p.idx[e], slot = p.pidx[e];
           const uint32_t s = sc % S, u = sc / S;
           if (u > 0 && !(ok = mbar_wait(&B->st_empty[s], (u - 1) & 1, abort_flag))) break;
           uint8_t* st = smem + L::OFF_ST + s * L::ST_BYTES;
@@ -267,10 +300,10 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t sc = 0, it = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const int jb = p.order[w / p.Hkv];
-        const int ncol = p.ptr[jb + 1] - p.ptr[jb];
-        if (ncol == 0) continue;
-        const int n = g * ncol;
+        const DkdvItem itm = p.items[w];
+        const int n = itm.x1 - itm.x0;
+        if (n == 0) continue;
+        
         if (!(ok = mbar_wait(&B->res_full, it & 1, abort_flag))) break;
         tc_fence_after();
         for (int x = 0; x <= n && ok; ++x) {
@@ -334,18 +367,19 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t sc = 0, it = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const int jb = p.order[w / p.Hkv], hk = w % p.Hkv;
-      const int ncol = p.ptr[jb + 1] - p.ptr[jb];
+      const DkdvItem itm = p.items[w];
+      const int jb = itm.jb, hk = itm.hk;
+      const int n = itm.x1 - itm.x0;
       const int kv = jb * 128 + r;
       __nv_bfloat16* orow = (hw ? p.out0 : p.out1) + ((size_t)kv * p.Hkv + hk) * D;  // wg0: dV, wg1: dK
-      if (ncol == 0) {
+      if (n == 0) {
         if (kv < p.T) {
           uint4 z = make_uint4(0, 0, 0, 0);
           for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
         }
         continue;
       }
-      const int n = g * ncol;
+      
       for (int x = 0; x < n; ++x) {
         const uint32_t y = sc + x, s = y % S;
         ok = mbar_wait(&B->s_full[hw], y & 1, abort_flag) && mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag);
@@ -403,7 +437,16 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t v[32];
         tmem_ld32(tl + acc + c * 32, v);
         tmem_ld_wait();
-        if (kv < p.T) store_row32(orow + c * 32, v, mul);
+        if (itm.slot < 0) {
+          if (kv < p.T) store_row32(orow + c * 32, v, mul);
+        } else {  // one chunk of a split column: fp32 partial sums, summed later in chunk order
+          float4* prow = reinterpret_cast<float4*>(p.partial + ((size_t)itm.slot * 128 + r) * (2 * D) + (hw ? D : 0) +
+                                                   c * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            prow[k] = make_float4(__uint_as_float(v[4 * k]) * mul, __uint_as_float(v[4 * k + 1]) * mul,
+                                  __uint_as_float(v[4 * k + 2]) * mul, __uint_as_float(v[4 * k + 3]) * mul);
+        }
       }
       tc_fence_before();
       mbar_arrive(&B->acc_free);
@@ -680,10 +723,78 @@ int reserve_smem(K kernel, int bytes, int dev, int* flags) {
   return 0;
 }
 
+// Work items of the kv-major kernel for one head layout, cached on the map.
+// Columns with more steps than about one SM's share are cut into chunks that
+// write fp32 partials to workspace slots (at most max_slots of them); items
+// are ordered longest first.
+std::mutex g_items_mu;
+
+int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, cudaStream_t s) {
+  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
+  std::lock_guard<std::mutex> lk(g_items_mu);
+  if (bm->bwd_items && bm->bwd_g == g && bm->bwd_hkv == Hkv && bm->bwd_max_slots == max_slots) return 0;
+  const int nk = bm->nk;
+  long long total = 0;
+  for (int j = 0; j < nk; ++j) total += (long long)g * bm->h_col_cnt[j] * Hkv;
+  long long cap = std::max<long long>(4, (total + sms - 1) / std::max(sms, 1));
+  auto slots_for = [&](long long c) {
+    long long n_slots = 0;
+    for (int j = 0; j < nk; ++j) {
+      const long long n = (long long)g * bm->h_col_cnt[j];
+      const long long nch = (n + c - 1) / c;
+      if (nch > 1) n_slots += nch * Hkv;
+    }
+    return n_slots;
+  };
+  if (max_slots <= 0)
+    cap = LLONG_MAX / 4;
+  else
+    while (slots_for(cap) > max_slots) cap *= 2;
+  std::vector<DkdvItem> items;
+  std::vector<int4> splits;
+  int slot = 0;
+  for (int j = 0; j < nk; ++j) {
+    const int n = g * bm->h_col_cnt[j];
+    const int nch = n == 0 ? 1 : (int)((n + cap - 1) / cap);
+    for (int hk = 0; hk < Hkv; ++hk) {
+      if (nch <= 1) {
+        items.push_back(DkdvItem{j, hk, 0, n, -1, 0, 0, 0});
+      } else {
+        splits.push_back(make_int4(j, hk, slot, nch));
+        for (int c = 0; c < nch; ++c)
+          items.push_back(DkdvItem{j, hk, (int)((long long)c * n / nch), (int)((long long)(c + 1) * n / nch), slot + c,
+                                   0, 0, 0});
+        slot += nch;
+      }
+    }
+  }
+  std::stable_sort(items.begin(), items.end(),
+                   [](const DkdvItem& a, const DkdvItem& b) { return (a.x1 - a.x0) > (b.x1 - b.x0); });
+  pool_free(bm->bwd_mem, s);
+  bm->bwd_mem = nullptr;
+  bm->bwd_items = nullptr;
+  const size_t bi = sizeof(DkdvItem) * std::max<size_t>(items.size(), 1);
+  const size_t bs = sizeof(int4) * std::max<size_t>(splits.size(), 1);
+  int rc = pool_alloc(&bm->bwd_mem, bi + bs, bm->device, s);
+  if (rc) return rc;
+  bm->bwd_items = bm->bwd_mem;
+  bm->bwd_splits = static_cast<char*>(bm->bwd_mem) + bi;
+  if ((rc = upload(bm->bwd_items, items.data(), sizeof(DkdvItem) * items.size(), bm->device, s))) return rc;
+  if (!splits.empty() && (rc = upload(bm->bwd_splits, splits.data(), sizeof(int4) * splits.size(), bm->device, s)))
+    return rc;
+  bm->bwd_g = g;
+  bm->bwd_hkv = Hkv;
+  bm->bwd_max_slots = max_slots;
+  bm->bwd_n_items = (int)items.size();
+  bm->bwd_n_splits = (int)splits.size();
+  bm->bwd_n_slots = slot;
+  return 0;
+}
+
 template <int D>
 int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
                int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
-               float* lse2, cudaStream_t s) {
+               float* lse2, float* partial, size_t partial_bytes, cudaStream_t s) {
   static int set_dkdv[64] = {0}, set_dq[64] = {0};
   const int dev = bm->device;
   int rc = reserve_smem(k_bwd_dkdv<D>, DkdvL<D>::BYTES, dev, set_dkdv);
@@ -693,6 +804,9 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
     set_error("backward kernel: block map has no tile masks");
     return 1;
   }
+  const int sms = num_sms(dev);
+  const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, s))) return rc;
   const int Tpad = bm->nq * 128;
   {
     const long long threads = (long long)Hq * Tpad * (D / 8);
@@ -713,7 +827,6 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   p.Hkv = Hkv;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
-  const int sms = num_sms(dev);
   // dK, dV
   p.ptr = bm->k_ptr;
   p.idx = bm->q_idx;
@@ -723,10 +836,21 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   p.out0 = static_cast<__nv_bfloat16*>(dK);
   p.out1 = static_cast<__nv_bfloat16*>(dV);
   p.n_major = bm->nk;
-  int items = bm->nk * Hkv;
-  if (items > 0) {
+  p.items = static_cast<const DkdvItem*>(bm->bwd_items);
+  p.n_items = bm->bwd_n_items;
+  p.partial = partial;
+  int launches = 1;
+  if (p.n_items > 0) {
     ProfScope ps(s, "bwd_dkdv");
-    k_bwd_dkdv<D><<<items < sms ? items : sms, 320, DkdvL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    k_bwd_dkdv<D><<<p.n_items < sms ? p.n_items : sms, 320, DkdvL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    ++launches;
+  }
+  if (bm->bwd_n_splits > 0) {
+    ProfScope ps(s, "bwd_dkdv_finalize");
+    k_dkdv_finalize<D><<<bm->bwd_n_splits, 256, 0, s>>>(static_cast<const int4*>(bm->bwd_splits), partial, T, Hkv,
+                                                        static_cast<__nv_bfloat16*>(dK),
+                                                        static_cast<__nv_bfloat16*>(dV));
+    ++launches;
   }
   // dQ
   p.ptr = bm->q_ptr;
@@ -737,12 +861,15 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   p.out0 = static_cast<__nv_bfloat16*>(dQ);
   p.out1 = nullptr;
   p.n_major = bm->nq;
-  items = bm->nq * Hq;
+  p.items = nullptr;
+  p.partial = nullptr;
+  const int items = bm->nq * Hq;
   if (items > 0) {
     ProfScope ps(s, "bwd_dq");
     k_bwd_dq<D><<<items < sms ? items : sms, 320, DqL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    ++launches;
   }
-  count_launch(3);
+  count_launch(launches);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("backward launch failed: %s", cudaGetErrorString(e));
@@ -757,10 +884,14 @@ bool bwd_tc_supported(int D) { return D == 64 || D == 128; }
 
 int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T, int Hq,
            int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta, float* lse2,
-           cudaStream_t s) {
+           float* partial, size_t partial_bytes, cudaStream_t s) {
   switch (D) {
-    case 64: return launch_bwd<64>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, s);
-    case 128: return launch_bwd<128>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, s);
+    case 64:
+      return launch_bwd<64>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial,
+                            partial_bytes, s);
+    case 128:
+      return launch_bwd<128>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial,
+                             partial_bytes, s);
     default: set_error("tensor-core backward: head_dim %d not built", D); return 2;
   }
 }

@@ -26,6 +26,9 @@ struct pt_tok {
 
 struct pt_blockmap {
   int device;
+  cudaStream_t stream;  // the build stream; memory is returned to the pool in its order
+  void* mem_fixed;      // one pool allocation for the arrays sized before classification
+  void* mem_lists;      // one pool allocation for the lists and masks
   int32_t T, BM, BN, nq, nk;
   int32_t n_nodes;
   int32_t tpad;  // entries of tok: max(nq*BM, nk*BN)
@@ -53,6 +56,22 @@ struct pt_blockmap {
   int32_t* pidxT;       // [nnz] mask slot of each kv-major entry, -1 when full
   uint32_t* mask_rows;  // [n_partial][128 q rows][4 words]: bit c = keep(row, kv column c)
   uint32_t* mask_cols;  // [n_partial][128 kv columns][4 words]: bit r = keep(q row r, column)
+  // host copies of the list lengths (one allocation: 4 counters | rows | columns)
+  int* h_counts;
+  int* h_row_cnt;  // [nq]
+  int* h_col_cnt;  // [nk]
+  // backward work items of the kv-major kernel, cached for one head layout
+  void* bwd_mem;
+  int bwd_g, bwd_hkv, bwd_max_slots, bwd_n_items, bwd_n_splits, bwd_n_slots;
+  void* bwd_items;   // DkdvItem[bwd_n_items] (device)
+  void* bwd_splits;  // int4[bwd_n_splits]: kv block, kv head, first slot, slot count (device)
+};
+
+// Work item of the kv-major backward kernel: steps [x0, x1) of the (kv block,
+// kv head) column; slot >= 0 means the item is one chunk of a split column and
+// writes fp32 partial sums to that slot instead of the outputs.
+struct DkdvItem {
+  int jb, hk, x0, x1, slot, pad0, pad1, pad2;
 };
 
 namespace pt {
@@ -75,6 +94,12 @@ struct ProfScope {
   void* end_event;
 };
 
+// Stream-ordered device memory from the library's private pool, and pinned
+// staging for small host-to-device uploads (pt_blockmap.cu).
+int pool_alloc(void** p, size_t bytes, int dev, cudaStream_t s);
+void pool_free(void* p, cudaStream_t s);
+int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s);
+
 // Device status word of each translation unit: read and clear.
 int take_status_blockmap(cudaStream_t s);
 int take_status_fwd(cudaStream_t s);
@@ -94,7 +119,7 @@ int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, 
            const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s);
 int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
            int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
-           float* lse2, cudaStream_t s);
+           float* lse2, float* partial, size_t partial_bytes, cudaStream_t s);
 bool bwd_tc_supported(int D);
 
 // CUDA-core kernels (pt_simt.cu), fp32 or bf16 storage with fp32 math.
