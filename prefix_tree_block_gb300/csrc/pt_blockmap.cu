@@ -224,7 +224,8 @@ __device__ __forceinline__ long long overlap(long long a0, long long a1, long lo
 }
 
 __global__ void k_classify(int T, int BM, int BN, int nq, int nk, const int* node_of, const int* node_start,
-                           const int* node_end, const int* parent, uint8_t* kinds) {
+                           const int* node_end, const int* parent, uint8_t* kinds, int* counters, int* row_cnt,
+                           int* col_cnt, int* row_part) {
   long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (w >= (long long)nq * nk) return;
@@ -248,81 +249,100 @@ __global__ void k_classify(int T, int BM, int BN, int nq, int nk, const int* nod
     uint8_t kd = kept == 0 ? PT_KIND_EMPTY
                            : ((in_range && kept == (long long)BM * BN) ? PT_KIND_FULL : PT_KIND_PARTIAL);
     kinds[w] = kd;
+    if (kd != PT_KIND_EMPTY) {
+      atomicAdd(&row_cnt[i], 1);
+      atomicAdd(&col_cnt[j], 1);
+      if (kd == PT_KIND_FULL)
+        atomicAdd(&counters[0], 1);
+      else
+        atomicAdd(&row_part[i], 1);
+    }
   }
 }
 
-// one warp per row (q tile) or per column (kv block): counts of non-empty and full
-__global__ void k_counts(const uint8_t* kinds, int nq, int nk, bool by_col, int* cnt, int* n_full) {
-  int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  int nrows = by_col ? nk : nq, len = by_col ? nq : nk;
-  if (w >= nrows) return;
-  int c = 0, f = 0;
-  for (int x = lane; x < len; x += 32) {
-    uint8_t k = by_col ? kinds[(long long)x * nk + w] : kinds[(long long)w * nk + x];
-    c += (k != 0);
-    f += (k == PT_KIND_FULL);
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    c += __shfl_xor_sync(0xffffffffu, c, o);
-    f += __shfl_xor_sync(0xffffffffu, f, o);
-  }
-  if (lane == 0) {
-    cnt[w] = c;
-    if (!by_col) atomicAdd(n_full, f);
+// Exclusive scans of up to three small arrays in one block (lengths up to a
+// few hundred thousand): out[0..n] with out[n] the total.
+__global__ void k_scan3(const int* a, int na, int* oa, const int* b, int nb, int* ob, const int* c, int nc, int* oc) {
+  __shared__ int sh[32];
+  __shared__ int carry;
+  const int* in[3] = {a, b, c};
+  int* out[3] = {oa, ob, oc};
+  const int n[3] = {na, nb, nc};
+  for (int k = 0; k < 3; ++k) {
+    if (!out[k]) continue;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < n[k]; base += kScanBlock) {
+      const int idx = base + threadIdx.x;
+      const int v = idx < n[k] ? in[k][idx] : 0;
+      const int incl = block_incl_scan(v, sh);
+      const int cy = carry;
+      if (idx < n[k]) out[k][idx] = cy + incl - v;
+      __syncthreads();
+      if (threadIdx.x == kScanBlock - 1) carry = cy + incl;
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) out[k][n[k]] = carry;
+    __syncthreads();
   }
 }
 
-// ordered compaction of each row (or column) into its list slot.  For the
-// kv-major lists, `q_ptr`/`kv_idx`/`pidx` of the finished q-major list give
-// each tile's mask slot (binary search of the kv block in the q tile's row).
-__global__ void k_fill(const uint8_t* kinds, int nq, int nk, bool by_col, const int* ptr, int* idx, uint8_t* kd,
-                       int* pflag, const int* q_ptr, const int* kv_idx, const int* pidx, int* pidxT) {
+// q-major lists: one warp per q tile compacts its row in kv order, numbering
+// partial tiles row-major (slot = partial tiles in earlier rows + rank in row).
+__global__ void k_fill_rows(const uint8_t* kinds, int nq, int nk, const int* q_ptr, const int* prow_ptr, int* kv_idx,
+                            uint8_t* kd, int* pidx, int2* slot_tile) {
   int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  int nrows = by_col ? nk : nq, len = by_col ? nq : nk;
-  if (w >= nrows) return;
-  int pos = ptr[w];
-  for (int base = 0; base < len; base += 32) {
+  if (w >= nq) return;
+  int pos = q_ptr[w], ppos = prow_ptr[w];
+  for (int base = 0; base < nk; base += 32) {
     int x = base + lane;
-    uint8_t k = 0;
-    if (x < len) k = by_col ? kinds[(long long)x * nk + w] : kinds[(long long)w * nk + x];
+    uint8_t k = x < nk ? kinds[(long long)w * nk + x] : 0;
     unsigned m = __ballot_sync(0xffffffffu, k != 0);
+    unsigned mp = __ballot_sync(0xffffffffu, k == PT_KIND_PARTIAL);
     if (k) {
-      int off = __popc(m & ((1u << lane) - 1));
-      idx[pos + off] = x;
+      const unsigned below = (1u << lane) - 1;
+      const int off = __popc(m & below);
+      kv_idx[pos + off] = x;
       kd[pos + off] = k;
-      if (!by_col) {
-        pflag[pos + off] = (k == PT_KIND_PARTIAL);
+      if (k == PT_KIND_PARTIAL) {
+        const int slot = ppos + __popc(mp & below);
+        pidx[pos + off] = slot;
+        slot_tile[slot] = make_int2(w, x);
       } else {
-        int lo = q_ptr[x], hi = q_ptr[x + 1] - 1;  // row x holds kv block w
-        while (lo < hi) {
-          int mid = (lo + hi) >> 1;
-          if (kv_idx[mid] < w)
-            lo = mid + 1;
-          else
-            hi = mid;
-        }
-        pidxT[pos + off] = pidx[lo];
+        pidx[pos + off] = -1;
       }
     }
     pos += __popc(m);
+    ppos += __popc(mp);
   }
 }
 
-// q-major: mask slot of each partial entry (exclusive scan of partial flags),
-// and the (q tile, kv block) of every slot.
-__global__ void k_slots(int nq, const int* q_ptr, const int* kv_idx, const uint8_t* kind, const int* pscan,
-                        int* pidx, int2* slot_tile) {
+// kv-major lists: one warp per kv block compacts its column in q order; each
+// entry's mask slot is found in the q tile's row (binary search by kv block).
+__global__ void k_fill_cols(const uint8_t* kinds, int nq, int nk, const int* k_ptr, int* q_idx, uint8_t* kdT,
+                            const int* q_ptr, const int* kv_idx, const int* pidx, int* pidxT) {
   int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (w >= nq) return;
-  for (int e = q_ptr[w] + lane; e < q_ptr[w + 1]; e += 32) {
-    if (kind[e] == PT_KIND_PARTIAL) {
-      int s = pscan[e];
-      pidx[e] = s;
-      slot_tile[s] = make_int2(w, kv_idx[e]);
-    } else {
-      pidx[e] = -1;
+  if (w >= nk) return;
+  int pos = k_ptr[w];
+  for (int base = 0; base < nq; base += 32) {
+    int x = base + lane;
+    uint8_t k = x < nq ? kinds[(long long)x * nk + w] : 0;
+    unsigned m = __ballot_sync(0xffffffffu, k != 0);
+    if (k) {
+      const int off = __popc(m & ((1u << lane) - 1));
+      q_idx[pos + off] = x;
+      kdT[pos + off] = k;
+      int lo = q_ptr[x], hi = q_ptr[x + 1] - 1;  // row x holds kv block w
+      while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (kv_idx[mid] < w)
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      pidxT[pos + off] = pidx[lo];
     }
+    pos += __popc(m);
   }
 }
 
@@ -375,10 +395,15 @@ __global__ void k_dense_lists(int nq, int nk, int* q_ptr, int* kv_idx, uint8_t* 
 }
 
 // Longest-first order on the device: element i goes to position
-// #{j : cnt[j] > cnt[i] or (cnt[j] == cnt[i] and j < i)}.  One warp per element.
-__global__ void k_lpt(const int* cnt, int n, int* order) {
-  int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (i >= n) return;
+// #{j : cnt[j] > cnt[i] or (cnt[j] == cnt[i] and j < i)}.  One warp per
+// element; warps [0, na) order array a, the rest array b.
+__global__ void k_lpt2(const int* a, int na, int* oa, const int* b, int nb, int* ob) {
+  int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= na + nb) return;
+  const int* cnt = w < na ? a : b;
+  int* order = w < na ? oa : ob;
+  const int n = w < na ? na : nb;
+  const int i = w < na ? w : w - na;
   const int ci = cnt[i];
   int rank = 0;
   for (int j = lane; j < n; j += 32) {
@@ -575,41 +600,44 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
   void* tmpB = nullptr;
   int rc = 0;
   do {
+    // counters | row counts | column counts are contiguous so one copy brings
+    // them to the host; partial counts per row and their scan stay on the device
     Layout LA;
-    // counters | row counts | column counts, contiguous so one copy brings them to the host
-    size_t o_kinds = LA.add<uint8_t>((size_t)ntiles), o_cnt = LA.add<int>((size_t)4 + nq + nk),
-           o_st = LA.add<int>((size_t)std::max(nq, nk) / kScanBlock + 2);
+    const size_t ncnt = (size_t)4 + nq + nk;
+    size_t o_kinds = LA.add<uint8_t>((size_t)ntiles), o_cnt = LA.add<int>(ncnt + nq),
+           o_pp = LA.add<int>((size_t)nq + 1);
     if ((rc = pool_alloc(&tmpA, LA.off, dev, s))) break;
     uint8_t* kinds = at<uint8_t>(tmpA, o_kinds);
     int* counters = at<int>(tmpA, o_cnt);
     int* row_cnt = counters + 4;
     int* col_cnt = row_cnt + nq;
-    int* stmp = at<int>(tmpA, o_st);
-    if (cudaMemsetAsync(counters, 0, 4 * sizeof(int), s) != cudaSuccess) {
+    int* row_part = col_cnt + nk;
+    int* prow_ptr = at<int>(tmpA, o_pp);
+    if (cudaMemsetAsync(counters, 0, sizeof(int) * (ncnt + nq), s) != cudaSuccess) {
       rc = 3;
       break;
     }
     if (ntiles > 0) {
       long long threads = ntiles * 32;
       k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
-                                                                   bm->node_start, bm->node_end, bm->parent, kinds);
-      k_counts<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, row_cnt, counters);
-      k_counts<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, col_cnt, counters);
-      PT_LAUNCHED(3);
-      k_lpt<<<(nq * 32 + 255) / 256, 256, 0, s>>>(row_cnt, nq, bm->q_order);
-      k_lpt<<<(nk * 32 + 255) / 256, 256, 0, s>>>(col_cnt, nk, bm->k_order);
-      PT_LAUNCHED(2);
+                                                                   bm->node_start, bm->node_end, bm->parent, kinds,
+                                                                   counters, row_cnt, col_cnt, row_part);
+      PT_LAUNCHED(1);
     }
-    if ((rc = exclusive_scan(row_cnt, nq, bm->q_ptr, stmp, s))) break;
-    if ((rc = exclusive_scan(col_cnt, nk, bm->k_ptr, stmp, s))) break;
+    k_scan3<<<1, kScanBlock, 0, s>>>(row_cnt, nq, bm->q_ptr, col_cnt, nk, bm->k_ptr, row_part, nq, prow_ptr);
+    PT_LAUNCHED(1);
+    if (ntiles > 0) {
+      k_lpt2<<<(unsigned)(((long long)(nq + nk) * 32 + 255) / 256), 256, 0, s>>>(row_cnt, nq, bm->q_order, col_cnt,
+                                                                              nk, bm->k_order);
+      PT_LAUNCHED(1);
+    }
     // the one synchronisation of the build: list sizes to the host
-    bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * (4 + (size_t)nq + nk)));
+    bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * ncnt));
     if (!bm->h_counts) {
       rc = 5;
       break;
     }
-    if (cudaMemcpyAsync(bm->h_counts, counters, sizeof(int) * (4 + (size_t)nq + nk), cudaMemcpyDeviceToHost, s) !=
-        cudaSuccess) {
+    if (cudaMemcpyAsync(bm->h_counts, counters, sizeof(int) * ncnt, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
       rc = 3;
       break;
     }
@@ -627,23 +655,13 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
     bm->n_full = bm->h_counts[0];
     bm->n_partial = bm->nnz - bm->n_full;
     if ((rc = alloc_lists(bm, s))) break;
-    const int64_t nnz = bm->nnz;
-    if (ntiles > 0 && nnz > 0) {
-      Layout LB;
-      size_t o_pf = LB.add<int>(nnz), o_ps = LB.add<int>(nnz + 1), o_s2 = LB.add<int>(nnz / kScanBlock + 2),
-             o_sl = LB.add<int2>(std::max<int64_t>(bm->n_partial, 1));
-      if ((rc = pool_alloc(&tmpB, LB.off, dev, s))) break;
-      int* pflag = at<int>(tmpB, o_pf);
-      int* pscan = at<int>(tmpB, o_ps);
-      int* stmp2 = at<int>(tmpB, o_s2);
-      int2* slot_tile = at<int2>(tmpB, o_sl);
-      k_fill<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, false, bm->q_ptr, bm->kv_idx, bm->kind, pflag,
-                                                     nullptr, nullptr, nullptr, nullptr);
-      PT_LAUNCHED(1);
-      if ((rc = exclusive_scan(pflag, (int)nnz, pscan, stmp2, s))) break;
-      k_slots<<<(nq * 32 + 255) / 256, 256, 0, s>>>(nq, bm->q_ptr, bm->kv_idx, bm->kind, pscan, bm->pidx, slot_tile);
-      k_fill<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, true, bm->k_ptr, bm->q_idx, bm->kindT, nullptr,
-                                                     bm->q_ptr, bm->kv_idx, bm->pidx, bm->pidxT);
+    if (ntiles > 0 && bm->nnz > 0) {
+      if ((rc = pool_alloc(&tmpB, sizeof(int2) * (size_t)std::max<int64_t>(bm->n_partial, 1), dev, s))) break;
+      int2* slot_tile = static_cast<int2*>(tmpB);
+      k_fill_rows<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, bm->q_ptr, prow_ptr, bm->kv_idx, bm->kind,
+                                                         bm->pidx, slot_tile);
+      k_fill_cols<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, bm->k_ptr, bm->q_idx, bm->kindT, bm->q_ptr,
+                                                         bm->kv_idx, bm->pidx, bm->pidxT);
       PT_LAUNCHED(2);
       if (bm->mask_rows) {
         k_masks<<<(unsigned)bm->n_partial, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
