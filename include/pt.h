@@ -246,6 +246,14 @@ const char* pt_last_error(void);
  * devices, all entry points).  Used by benchmarks to count launches. */
 uint64_t pt_launch_count(void);
 
+/* Failure-path check: launch a one-thread kernel that waits on a barrier
+ * nothing will complete, using the same bounded wait as the attention
+ * kernels.  The wait gives up after about one second and the kernel returns
+ * normally, so the context stays usable; the next pt_sync_status on this
+ * stream returns PT_ERR_TIMEOUT.  Meant for tests of error reporting; the
+ * pages have no counterpart. */
+pt_status pt_debug_wait_timeout(cudaStream_t stream);
+
 /* Optional per-kernel timing, for benchmarks and profiling.  While enabled,
  * each kernel launch is bracketed by two CUDA events on its stream (a few
  * microseconds of overhead per launch); disabled (the default) costs one

@@ -61,6 +61,7 @@ def load_library(path: Optional[str] = None):
             "pt_attn_fwd": [vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp],
             "pt_attn_bwd": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
             "pt_sync_status": [vp],
+            "pt_debug_wait_timeout": [vp],
             "pt_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp,
                                     vp],
         }

@@ -12,7 +12,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/pt.h"
+#include "pt.h"
 #include "pt_internal.h"
 
 namespace pt {
@@ -377,6 +377,8 @@ pt_status pt_sync_status(cudaStream_t stream) {
 const char* pt_last_error(void) { return pt::g_err_ptr(); }
 
 uint64_t pt_launch_count(void) { return pt::launches(); }
+
+pt_status pt_debug_wait_timeout(cudaStream_t stream) { return as_status(pt::wait_timeout_probe(stream)); }
 
 void pt_profile_enable(int on) { pt::g_prof_on.store(on != 0); }
 

@@ -263,7 +263,6 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         for (int kk = 0; kk < C::BN / 16; ++kk)
           mma_ts(tbase + C::TM_O + h * D, a_tmem + kk * 8, sdesc_sw128(va + kk * 2048, C::PANEL, 1024), IDESC_PV,
                  (!first || kk > 0));
-        mma_commit(o_full + h);
       };
 
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -293,6 +292,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
               if (i == 0 && itv[0] > 0 && !(ok = mbar_wait(o_free, (itv[0] - 1) & 1, abort_flag))) break;
               tc_fence_after();
               issue_pv(0, u, vs, i == 0);
+              mma_commit(o_full);
               mma_commit(v_empty + vs);
             }
           } else {
@@ -305,6 +305,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
                 if (i == 0 && itv[h] > 0 && !(ok = mbar_wait(o_free + h, (itv[h] - 1) & 1, abort_flag))) break;
                 tc_fence_after();
                 issue_pv(h, u, vs, i == 0);
+                // two heads: O is committed once per item; S_h(jj), issued
+                // next, is committed after this PV, which the softmax relies on
+                if (i == n - 1) mma_commit(o_full + h);
                 if (h == nh - 1) mma_commit(v_empty + vs);
               }
               if (jj < n) {
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     const int r = threadIdx.x & 127;           // q row within the tile, TMEM lane
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t o_col = C::TM_O + h * D;
-    uint32_t sc = 0, vc = 0, pvc = 0;
+    uint32_t sc = 0, vc = 0, pvc = 0, itv = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       int tile, h0, nh;
@@ -399,12 +402,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         const bool grow = m_blk > m_use + kRescaleThreshold;
         const float m_new = grow ? m_blk : m_use;
         if (__any_sync(0xffffffffu, grow && l > 0.f)) {
-          // O holds contributions scaled to the old reference: wait for the PV
-          // in flight, then rescale this warp's rows in place.
-          ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
+          // O holds contributions scaled to the old reference: rescale this
+          // warp's rows in place once the PV in flight is done.  With two
+          // heads that is already known (S(j) was committed after PV(j-1));
+          // with one head, wait for it.
+          if (NH == 1) {
+            ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
           }
           tc_fence_after();
           const float alpha = (grow && l > 0.f) ? ex2(m_use - m_new) : 1.f;
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         tmem_st32(sb + 0, sr + 0);
         tmem_st32(sb + 32, sr + 32);
         tmem_st_wait();
-        if (jj > 0) {
+        if (NH == 1 && jj > 0) {
           ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
@@ -447,8 +454,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         mbar_arrive(p_full + h * C::SB + b);
       }
       if (!ok) break;
-      // epilogue: O / l and LSE
-      ok = mbar_wait(o_full + h, (pvc + n - 1) & 1, abort_flag);
+      // epilogue: O / l and LSE (one head: O committed per PV; two heads: once per item)
+      ok = mbar_wait(o_full + h, (NH == 1 ? (pvc + n - 1) : itv) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -477,6 +484,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       sc += n;
       vc += n;
       pvc += n;
+      ++itv;
     }
     if (!ok) *abort_flag = 1;
   }
@@ -540,6 +548,33 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
 }
 
 }  // namespace
+
+namespace {
+// One thread waits on an mbarrier that nothing will ever complete: the same
+// bounded wait the attention kernels use runs out after about a second,
+// records PT_ERR_TIMEOUT in this unit's status word and the kernel returns.
+__global__ void k_wait_timeout_probe() {
+  __shared__ uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait(&bar, 0, &abort_flag);
+  }
+}
+}  // namespace
+
+int wait_timeout_probe(cudaStream_t s) {
+  k_wait_timeout_probe<<<1, 32, 0, s>>>();
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("timeout probe launch failed: %s", cudaGetErrorString(e));
+    return 3;
+  }
+  return 0;
+}
 
 int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
            const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {

@@ -121,6 +121,7 @@ int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const vo
            int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
            float* lse2, float* partial, size_t partial_bytes, cudaStream_t s);
 bool bwd_tc_supported(int D);
+int wait_timeout_probe(cudaStream_t s);
 
 // CUDA-core kernels (pt_simt.cu), fp32 or bf16 storage with fp32 math.
 int fwd_simt(bool bf16, const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,

@@ -18,7 +18,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/pt.h"
+#include "pt.h"
 #include "pt_internal.h"
 
 namespace {
