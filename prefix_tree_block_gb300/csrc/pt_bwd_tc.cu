@@ -96,9 +96,10 @@ struct BwdCfg {
   static constexpr int HALF = 64 * 128;    // rows 64..127 of a panel start here
   static constexpr int TILE = NP * PANEL;
   static constexpr int STAGES = D == 64 ? 4 : 2;
-  // TMEM columns: warpgroup w owns S at 128w and dP at 128w + 64 (64 each);
-  // accumulators from 256.
-  static constexpr int TM_ACC0 = 256, TM_ACC1 = 256 + D;
+  // TMEM columns: S (or S^T) at 0 and dP (or dP^T) at 128, 128 columns each;
+  // warpgroup w reads columns [64w, 64w + 64) of both and writes its packed
+  // bf16 results to the first 32 of them.  Accumulators from 256.
+  static constexpr int TM_S = 0, TM_DP = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
 };
 
 struct BwdParams {
@@ -179,7 +180,7 @@ __device__ __forceinline__ void init_bars(BwdBars<S>* b) {
   }
   for (int w = 0; w < 2; ++w) {
     mbar_init(&b->s_full[w], 1);
-    mbar_init(&b->p_full[w], 128);
+    mbar_init(&b->p_full[w], 256);  // both compute warpgroups arrive
   }
   mbar_init(&b->acc_full, 1);
   mbar_init(&b->acc_free, 256);
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
       constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);
       const uint32_t sK = smem_u32(smem + L::OFF_K), sV = smem_u32(smem + L::OFF_V);
       const uint32_t sST = smem_u32(smem + L::OFF_ST);
@@ -312,42 +313,42 @@ __global__ void __launch_bounds__(320, 1)
             if (!(ok = mbar_wait(&B->st_full[s], ((sc + x) / S) & 1, abort_flag))) break;
             tc_fence_after();
           }
-          for (int hw = 0; hw < 2 && ok; ++hw) {
-            if (x >= 1) {
-              // dV += P^T dO_half, dK += dS^T Q_half for the previous step
-              const uint32_t sp = (sc + x - 1) % S;
-              if (!(ok = mbar_wait(&B->p_full[hw], (sc + x - 1) & 1, abort_flag))) break;
-              if (x == 1 && hw == 0 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
-              tc_fence_after();
-              const uint32_t stp = sST + sp * L::ST_BYTES;
+          if (x >= 1) {
+            // dV += P^T dO, dK += dS^T Q for the previous step (K = 128 q rows:
+            // the two warpgroups' packed halves sit at columns 0 and 64)
+            const uint32_t sp = (sc + x - 1) % S;
+            if (!(ok = mbar_wait(&B->p_full[0], (sc + x - 1) & 1, abort_flag))) break;
+            if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t stp = sST + sp * L::ST_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t acc = (x > 1 || hw > 0 || kk > 0);
-                mma_ts(tbase + C::TM_ACC0, tbase + 128 * hw + kk * 8,
-                       sdesc_sw128(stp + L::ST_DO + hw * C::HALF + kk * 2048, C::PANEL, 1024), IDESC_ACC, acc);
-                mma_ts(tbase + C::TM_ACC1, tbase + 128 * hw + 64 + kk * 8,
-                       sdesc_sw128(stp + L::ST_Q + hw * C::HALF + kk * 2048, C::PANEL, 1024), IDESC_ACC, acc);
-              }
-              if (hw == 1) mma_commit(&B->st_empty[sp]);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t acc = (x > 1 || kk > 0);
+              const uint32_t acol = kk * 8 + (kk >= 4 ? 32 : 0);
+              mma_ts(tbase + C::TM_ACC0, tbase + C::TM_S + acol,
+                     sdesc_sw128(stp + L::ST_DO + kk * 2048, C::PANEL, 1024), IDESC_ACC, acc);
+              mma_ts(tbase + C::TM_ACC1, tbase + C::TM_DP + acol,
+                     sdesc_sw128(stp + L::ST_Q + kk * 2048, C::PANEL, 1024), IDESC_ACC, acc);
             }
-            if (x < n) {
-              // S^T = K Q_half^T and dP^T = V dO_half^T for this step
-              const uint32_t st = sST + s * L::ST_BYTES;
+            mma_commit(&B->st_empty[sp]);
+          }
+          if (x < n) {
+            // S^T = K Q^T and dP^T = V dO^T for this step (M = 128 kv, N = 128 q)
+            const uint32_t st = sST + s * L::ST_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-                mma_ss(tbase + 128 * hw, sdesc_sw128(sK + off, 16, 1024),
-                       sdesc_sw128(st + L::ST_Q + off + hw * C::HALF, 16, 1024), IDESC_S, kk > 0);
-              }
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-                mma_ss(tbase + 128 * hw + 64, sdesc_sw128(sV + off, 16, 1024),
-                       sdesc_sw128(st + L::ST_DO + off + hw * C::HALF, 16, 1024), IDESC_S, kk > 0);
-              }
-              mma_commit(&B->s_full[hw]);
-              if (x == n - 1 && hw == 1) mma_commit(&B->res_empty);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+              mma_ss(tbase + C::TM_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(st + L::ST_Q + off, 16, 1024),
+                     IDESC_S, kk > 0);
             }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+              mma_ss(tbase + C::TM_DP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(st + L::ST_DO + off, 16, 1024),
+                     IDESC_S, kk > 0);
+            }
+            mma_commit(&B->s_full[0]);
+            if (x == n - 1) mma_commit(&B->res_empty);
           }
         }
         if (ok) mma_commit(&B->acc_full);
@@ -360,10 +361,10 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute (kv row per thread)
-    const int hw = warp >> 2;  // which half of each q tile this warpgroup takes
+    const int hw = warp >> 2;  // which 64 q columns of each step this warpgroup takes
     const int r = threadIdx.x & 127;
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t tS = tl + 128 * hw, tP = tl + 128 * hw + 64;
+    const uint32_t tS = tl + C::TM_S + 64 * hw, tP = tl + C::TM_DP + 64 * hw;
     uint32_t sc = 0, it = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(320, 1)
       
       for (int x = 0; x < n; ++x) {
         const uint32_t y = sc + x, s = y % S;
-        ok = mbar_wait(&B->s_full[hw], y & 1, abort_flag) && mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag);
+        ok = mbar_wait(&B->s_full[0], y & 1, abort_flag) && mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(320, 1)
         tmem_st32(tP, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B->p_full[hw]);
+        mbar_arrive(&B->p_full[0]);
       }
       if (!ok) break;
       ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
       constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);
       const uint32_t sQ = smem_u32(smem + L::OFF_Q), sdO = smem_u32(smem + L::OFF_DO);
       const uint32_t sST = smem_u32(smem + L::OFF_ST);
@@ -582,39 +583,37 @@ __global__ void __launch_bounds__(320, 1)
             if (!(ok = mbar_wait(&B->st_full[s], ((sc + x) / S) & 1, abort_flag))) break;
             tc_fence_after();
           }
-          for (int hw = 0; hw < 2 && ok; ++hw) {
-            if (x >= 1) {
-              // dQ += dS_half K_half for the previous block
-              const uint32_t sp = (sc + x - 1) % S;
-              if (!(ok = mbar_wait(&B->p_full[hw], (sc + x - 1) & 1, abort_flag))) break;
-              if (x == 1 && hw == 0 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
-              tc_fence_after();
-              const uint32_t stp = sST + sp * L::ST_BYTES;
+          if (x >= 1) {
+            // dQ += dS K for the previous block (K = 128 kv: the two
+            // warpgroups' packed halves sit at columns 0 and 64 of dP)
+            const uint32_t sp = (sc + x - 1) % S;
+            if (!(ok = mbar_wait(&B->p_full[0], (sc + x - 1) & 1, abort_flag))) break;
+            if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t stp = sST + sp * L::ST_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tbase + C::TM_ACC0, tbase + 128 * hw + 64 + kk * 8,
-                       sdesc_sw128(stp + L::ST_K + hw * C::HALF + kk * 2048, C::PANEL, 1024), IDESC_ACC,
-                       (x > 1 || hw > 0 || kk > 0));
-              if (hw == 1) mma_commit(&B->st_empty[sp]);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tbase + C::TM_ACC0, tbase + C::TM_DP + kk * 8 + (kk >= 4 ? 32 : 0),
+                     sdesc_sw128(stp + L::ST_K + kk * 2048, C::PANEL, 1024), IDESC_ACC, (x > 1 || kk > 0));
+            mma_commit(&B->st_empty[sp]);
+          }
+          if (x < n) {
+            // S = Q K^T and dP = dO V^T for this block (M = 128 q, N = 128 kv)
+            const uint32_t st = sST + s * L::ST_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+              mma_ss(tbase + C::TM_S, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(st + L::ST_K + off, 16, 1024),
+                     IDESC_S, kk > 0);
             }
-            if (x < n) {
-              // S = Q K_half^T and dP = dO V_half^T for this block
-              const uint32_t st = sST + s * L::ST_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-                mma_ss(tbase + 128 * hw, sdesc_sw128(sQ + off, 16, 1024),
-                       sdesc_sw128(st + L::ST_K + off + hw * C::HALF, 16, 1024), IDESC_S, kk > 0);
-              }
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-                mma_ss(tbase + 128 * hw + 64, sdesc_sw128(sdO + off, 16, 1024),
-                       sdesc_sw128(st + L::ST_V + off + hw * C::HALF, 16, 1024), IDESC_S, kk > 0);
-              }
-              mma_commit(&B->s_full[hw]);
-              if (x == n - 1 && hw == 1) mma_commit(&B->res_empty);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+              mma_ss(tbase + C::TM_DP, sdesc_sw128(sdO + off, 16, 1024), sdesc_sw128(st + L::ST_V + off, 16, 1024),
+                     IDESC_S, kk > 0);
             }
+            mma_commit(&B->s_full[0]);
+            if (x == n - 1) mma_commit(&B->res_empty);
           }
         }
         if (ok) mma_commit(&B->acc_full);
@@ -627,10 +626,10 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ compute (q row per thread)
-    const int hw = warp >> 2;  // which half of each kv block this warpgroup takes
+    const int hw = warp >> 2;  // which 64 kv columns of each block this warpgroup takes
     const int r = threadIdx.x & 127;
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t tS = tl + 128 * hw, tP = tl + 128 * hw + 64;
+    const uint32_t tS = tl + C::TM_S + 64 * hw, tP = tl + C::TM_DP + 64 * hw;
     uint32_t sc = 0, it = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -649,7 +648,7 @@ __global__ void __launch_bounds__(320, 1)
       const float dl = p.delta[(size_t)h * p.Tpad + q];
       for (int x = 0; x < n; ++x) {
         const uint32_t y = sc + x, s = y % S;
-        ok = mbar_wait(&B->s_full[hw], y & 1, abort_flag) && mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag);
+        ok = mbar_wait(&B->s_full[0], y & 1, abort_flag) && mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -677,7 +676,7 @@ __global__ void __launch_bounds__(320, 1)
         tmem_st32(tP, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B->p_full[hw]);
+        mbar_arrive(&B->p_full[0]);
       }
       if (!ok) break;
       ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
