@@ -100,6 +100,12 @@ struct BwdCfg {
   // warpgroup w reads columns [64w, 64w + 64) of both and writes its packed
   // bf16 results to the first 32 of them.  Accumulators from 256.
   static constexpr int TM_S = 0, TM_DP = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
+  // With room in TMEM the packed P (or P^T) and dS (or dS^T) go to their own
+  // 64-column regions, so the next step's S/dP can be computed while this
+  // step's math runs: dQ (one accumulator) always has room; dK/dV only at D = 64.
+  static constexpr bool DQ_OVL = true, DKDV_OVL = (D == 64);
+  static constexpr int TM_DQ_DS = 256 + D;                    // dq: packed dS
+  static constexpr int TM_KV_P = 256 + 2 * D, TM_KV_DS = 320 + 2 * D;  // dkdv: packed P^T, dS^T
 };
 
 struct BwdParams {
@@ -168,6 +174,8 @@ struct BwdBars {
   uint64_t st_full[S], st_empty[S];
   uint64_t s_full[2], p_full[2];
   uint64_t acc_full, acc_free, mma_done;
+  uint64_t s_free;   // compute warpgroups have loaded S/dP: the MMA may overwrite them
+  uint64_t ps_free;  // the accumulate MMAs have read the packed P/dS region
 };
 
 template <int S>
@@ -185,6 +193,8 @@ __device__ __forceinline__ void init_bars(BwdBars<S>* b) {
   mbar_init(&b->acc_full, 1);
   mbar_init(&b->acc_free, 256);
   mbar_init(&b->mma_done, 1);
+  mbar_init(&b->s_free, 256);
+  mbar_init(&b->ps_free, 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -204,6 +214,7 @@ struct DkdvL {
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(C::TM_ACC1 + D <= 512, "TMEM budget");
+  static_assert(!C::DKDV_OVL || C::TM_KV_DS + 64 <= 512, "TMEM budget");
 };
 
 template <int D>
@@ -313,27 +324,11 @@ __global__ void __launch_bounds__(320, 1)
             if (!(ok = mbar_wait(&B->st_full[s], ((sc + x) / S) & 1, abort_flag))) break;
             tc_fence_after();
           }
-          if (x >= 1) {
-            // dV += P^T dO, dK += dS^T Q for the previous step (K = 128 q rows:
-            // the two warpgroups' packed halves sit at columns 0 and 64)
-            const uint32_t sp = (sc + x - 1) % S;
-            if (!(ok = mbar_wait(&B->p_full[0], (sc + x - 1) & 1, abort_flag))) break;
-            if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            const uint32_t stp = sST + sp * L::ST_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t acc = (x > 1 || kk > 0);
-              const uint32_t acol = kk * 8 + (kk >= 4 ? 32 : 0);
-              mma_ts(tbase + C::TM_ACC0, tbase + C::TM_S + acol,
-                     sdesc_sw128(stp + L::ST_DO + kk * 2048, C::PANEL, 1024), IDESC_ACC, acc);
-              mma_ts(tbase + C::TM_ACC1, tbase + C::TM_DP + acol,
-                     sdesc_sw128(stp + L::ST_Q + kk * 2048, C::PANEL, 1024), IDESC_ACC, acc);
-            }
-            mma_commit(&B->st_empty[sp]);
-          }
-          if (x < n) {
-            // S^T = K Q^T and dP^T = V dO^T for this step (M = 128 kv, N = 128 q)
+          // S^T(x) first when the packed operands have their own TMEM region
+          // (it only has to wait until the compute warpgroups have loaded
+          // S^T(x-1)); otherwise after the accumulate MMAs of step x-1, which
+          // read P^T and dS^T in place.
+          auto issue_sdp = [&]() {
             const uint32_t st = sST + s * L::ST_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -349,7 +344,35 @@ __global__ void __launch_bounds__(320, 1)
             }
             mma_commit(&B->s_full[0]);
             if (x == n - 1) mma_commit(&B->res_empty);
+          };
+          const uint32_t y = sc + x;  // global step index of this CTA
+          if (C::DKDV_OVL && x < n) {
+            if (y >= 1 && !(ok = mbar_wait(&B->s_free, (y - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_sdp();
           }
+          if (x >= 1) {
+            // dV += P^T dO, dK += dS^T Q for the previous step (K = 128 q rows)
+            const uint32_t sp = (sc + x - 1) % S;
+            if (!(ok = mbar_wait(&B->p_full[0], (y - 1) & 1, abort_flag))) break;
+            if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t stp = sST + sp * L::ST_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t acc = (x > 1 || kk > 0);
+              const uint32_t acol = kk * 8 + (kk >= 4 ? 32 : 0);  // in place: halves at columns 0 and 64
+              const uint32_t a_p = C::DKDV_OVL ? C::TM_KV_P + kk * 8 : C::TM_S + acol;
+              const uint32_t a_ds = C::DKDV_OVL ? C::TM_KV_DS + kk * 8 : C::TM_DP + acol;
+              mma_ts(tbase + C::TM_ACC0, tbase + a_p, sdesc_sw128(stp + L::ST_DO + kk * 2048, C::PANEL, 1024),
+                     IDESC_ACC, acc);
+              mma_ts(tbase + C::TM_ACC1, tbase + a_ds, sdesc_sw128(stp + L::ST_Q + kk * 2048, C::PANEL, 1024),
+                     IDESC_ACC, acc);
+            }
+            if (C::DKDV_OVL) mma_commit(&B->ps_free);
+            mma_commit(&B->st_empty[sp]);
+          }
+          if (!C::DKDV_OVL && x < n) issue_sdp();
         }
         if (ok) mma_commit(&B->acc_full);
         sc += n;
@@ -401,6 +424,10 @@ __global__ void __launch_bounds__(320, 1)
         uint2 mk = make_uint2(0xffffffffu, 0xffffffffu);
         if (slot >= 0) mk = reinterpret_cast<const uint2*>(st + L::ST_M)[2 * r + hw];
         tmem_ld_wait();
+        if (C::DKDV_OVL) {  // S^T and dP^T are in registers: the MMA may reuse them
+          tc_fence_before();
+          mbar_arrive(&B->s_free);
+        }
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 lv = l2[c4], dv = dl[c4];
@@ -415,11 +442,25 @@ __global__ void __launch_bounds__(320, 1)
             dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - da[k]));
           }
         }
-        uint32_t pk[32];
+        uint32_t pk[32], pk2[32];
         pack64(sr, pk);
-        tmem_st32(tS, pk);
-        pack64(dr, pk);
-        tmem_st32(tP, pk);
+        pack64(dr, pk2);
+        if (C::DKDV_OVL) {
+          // the previous step's accumulate MMAs must be done reading the region
+          if (y > 0) {
+            ok = mbar_wait(&B->ps_free, (y - 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st32(tl + C::TM_KV_P + 32 * hw, pk);
+          tmem_st32(tl + C::TM_KV_DS + 32 * hw, pk2);
+        } else {
+          tmem_st32(tS, pk);
+          tmem_st32(tP, pk2);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&B->p_full[0]);
@@ -480,6 +521,7 @@ struct DqL {
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(C::TM_ACC0 + D <= 512, "TMEM budget");
+  static_assert(C::TM_DQ_DS + 64 <= 512, "TMEM budget");
 };
 
 template <int D>
@@ -583,22 +625,12 @@ __global__ void __launch_bounds__(320, 1)
             if (!(ok = mbar_wait(&B->st_full[s], ((sc + x) / S) & 1, abort_flag))) break;
             tc_fence_after();
           }
-          if (x >= 1) {
-            // dQ += dS K for the previous block (K = 128 kv: the two
-            // warpgroups' packed halves sit at columns 0 and 64 of dP)
-            const uint32_t sp = (sc + x - 1) % S;
-            if (!(ok = mbar_wait(&B->p_full[0], (sc + x - 1) & 1, abort_flag))) break;
-            if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            const uint32_t stp = sST + sp * L::ST_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tbase + C::TM_ACC0, tbase + C::TM_DP + kk * 8 + (kk >= 4 ? 32 : 0),
-                     sdesc_sw128(stp + L::ST_K + kk * 2048, C::PANEL, 1024), IDESC_ACC, (x > 1 || kk > 0));
-            mma_commit(&B->st_empty[sp]);
-          }
+          const uint32_t y = sc + x;  // global block index of this CTA
           if (x < n) {
-            // S = Q K^T and dP = dO V^T for this block (M = 128 q, N = 128 kv)
+            // S = Q K^T and dP = dO V^T (M = 128 q, N = 128 kv) as soon as the
+            // compute warpgroups have loaded the previous S and dP
+            if (y >= 1 && !(ok = mbar_wait(&B->s_free, (y - 1) & 1, abort_flag))) break;
+            tc_fence_after();
             const uint32_t st = sST + s * L::ST_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -614,6 +646,20 @@ __global__ void __launch_bounds__(320, 1)
             }
             mma_commit(&B->s_full[0]);
             if (x == n - 1) mma_commit(&B->res_empty);
+          }
+          if (x >= 1) {
+            // dQ += dS K for the previous block (K = 128 kv; dS packed in its own region)
+            const uint32_t sp = (sc + x - 1) % S;
+            if (!(ok = mbar_wait(&B->p_full[0], (y - 1) & 1, abort_flag))) break;
+            if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t stp = sST + sp * L::ST_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tbase + C::TM_ACC0, tbase + C::TM_DQ_DS + kk * 8,
+                     sdesc_sw128(stp + L::ST_K + kk * 2048, C::PANEL, 1024), IDESC_ACC, (x > 1 || kk > 0));
+            mma_commit(&B->ps_free);
+            mma_commit(&B->st_empty[sp]);
           }
         }
         if (ok) mma_commit(&B->acc_full);
@@ -664,6 +710,8 @@ __global__ void __launch_bounds__(320, 1)
         uint2 mk = make_uint2(0xffffffffu, 0xffffffffu);
         if (slot >= 0) mk = reinterpret_cast<const uint2*>(st + L::ST_M)[2 * r + hw];
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&B->s_free);  // S and dP are in registers: the MMA may reuse them
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const uint32_t word = c < 32 ? mk.x : mk.y;
@@ -673,7 +721,15 @@ __global__ void __launch_bounds__(320, 1)
         }
         uint32_t pk[32];
         pack64(dr, pk);
-        tmem_st32(tP, pk);
+        if (y > 0) {  // the previous dQ MMA must be done reading the dS region
+          ok = mbar_wait(&B->ps_free, (y - 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(tl + C::TM_DQ_DS + 32 * hw, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&B->p_full[0]);
