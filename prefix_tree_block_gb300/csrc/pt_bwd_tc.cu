@@ -36,6 +36,7 @@
 #include <climits>
 #include <cmath>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "pt_device.cuh"
@@ -103,6 +104,9 @@ struct BwdCfg {
   // With room in TMEM the packed P (or P^T) and dS (or dS^T) go to their own
   // 64-column regions, so the next step's S/dP can be computed while this
   // step's math runs: dQ (one accumulator) always has room; dK/dV only at D = 64.
+  // Without that room (dK/dV at D = 128) the kv-major kernel runs each step
+  // as S^T, dK of the previous step, dP^T, dV: P^T is computed while the
+  // tensor core works through the two middle products.
   static constexpr bool DQ_OVL = true, DKDV_OVL = (D == 64);
   static constexpr int TM_DQ_DS = 256 + D;                    // dq: packed dS
   static constexpr int TM_KV_P = 256 + 2 * D, TM_KV_DS = 320 + 2 * D;  // dkdv: packed P^T, dS^T
@@ -118,7 +122,8 @@ struct BwdParams {
   const float* lse2;      // [Hq, Tpad]
   __nv_bfloat16* out0;    // dK (dkdv) or dQ (dq)
   __nv_bfloat16* out1;    // dV (dkdv)
-  const DkdvItem* items;  // dkdv work items
+  const DkdvItem* items;  // dkdv work items, grouped by CTA
+  const int* cta_ptr;     // dkdv: CTA b runs items [cta_ptr[b], cta_ptr[b + 1])
   float* partial;         // dkdv: fp32 partial sums of split columns, [slot][128][2D]
   int T, Tpad, Hq, Hkv, n_major, n_items;
   float scale, scale_log2;
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.Hq / p.Hkv;
-  const int n_items = p.n_items;
+  const int w_begin = p.cta_ptr[blockIdx.x], w_end = p.cta_ptr[blockIdx.x + 1];
 
   if (threadIdx.x == 256) {
     init_bars<S>(B);
@@ -258,7 +263,7 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       uint32_t sc = 0, it = 0;
       bool ok = true, res_issued = false;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      for (int w = w_begin; w < w_end && ok; ++w) {
         const DkdvItem itm = p.items[w];
         const int jb = itm.jb, hk = itm.hk;
         const int e0 = p.ptr[jb], ncol = p.ptr[jb + 1] - e0;
@@ -311,68 +316,94 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t sST = smem_u32(smem + L::OFF_ST);
       uint32_t sc = 0, it = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      for (int w = w_begin; w < w_end && ok; ++w) {
         const DkdvItem itm = p.items[w];
         const int n = itm.x1 - itm.x0;
         if (n == 0) continue;
         
         if (!(ok = mbar_wait(&B->res_full, it & 1, abort_flag))) break;
         tc_fence_after();
-        for (int x = 0; x <= n && ok; ++x) {
-          const uint32_t s = (sc + x) % S;
-          if (x < n) {
-            if (!(ok = mbar_wait(&B->st_full[s], ((sc + x) / S) & 1, abort_flag))) break;
-            tc_fence_after();
+        const auto mma_s = [&](uint32_t st) {  // S^T = K Q^T (M = 128 kv, N = 128 q)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+            mma_ss(tbase + C::TM_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(st + L::ST_Q + off, 16, 1024),
+                   IDESC_S, kk > 0);
           }
-          // S^T(x) first when the packed operands have their own TMEM region
-          // (it only has to wait until the compute warpgroups have loaded
-          // S^T(x-1)); otherwise after the accumulate MMAs of step x-1, which
-          // read P^T and dS^T in place.
-          auto issue_sdp = [&]() {
+        };
+        const auto mma_dp = [&](uint32_t st) {  // dP^T = V dO^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+            mma_ss(tbase + C::TM_DP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(st + L::ST_DO + off, 16, 1024),
+                   IDESC_S, kk > 0);
+          }
+        };
+        // dV += P^T dO or dK += dS^T Q (K = 128 q rows), A read from TMEM
+        const auto mma_acc = [&](uint32_t acc_col, uint32_t a_col, bool packed_region, uint32_t b_tile, bool first) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t acol = packed_region ? kk * 8 : kk * 8 + (kk >= 4 ? 32 : 0);  // in place: halves at 0, 64
+            mma_ts(tbase + acc_col, tbase + a_col + acol, sdesc_sw128(b_tile + kk * 2048, C::PANEL, 1024), IDESC_ACC,
+                   !first || kk > 0);
+          }
+        };
+        if constexpr (C::DKDV_OVL) {
+          for (int x = 0; x <= n && ok; ++x) {
+            const uint32_t y = sc + x, s = y % S;  // global step index of this CTA
+            if (x < n) {
+              // S^T(x) as soon as the compute warpgroups have loaded S^T(x-1)
+              if (!(ok = mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag))) break;
+              if (y >= 1 && !(ok = mbar_wait(&B->s_free, (y - 1) & 1, abort_flag))) break;
+              tc_fence_after();
+              const uint32_t st = sST + s * L::ST_BYTES;
+              mma_s(st);
+              mma_dp(st);
+              mma_commit(&B->s_full[0]);
+              if (x == n - 1) mma_commit(&B->res_empty);
+            }
+            if (x >= 1) {
+              // dV, dK of the previous step from the packed region
+              const uint32_t sp = (y - 1) % S;
+              if (!(ok = mbar_wait(&B->p_full[0], (y - 1) & 1, abort_flag))) break;
+              if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
+              tc_fence_after();
+              const uint32_t stp = sST + sp * L::ST_BYTES;
+              mma_acc(C::TM_ACC0, C::TM_KV_P, true, stp + L::ST_DO, x == 1);
+              mma_acc(C::TM_ACC1, C::TM_KV_DS, true, stp + L::ST_Q, x == 1);
+              mma_commit(&B->ps_free);
+              mma_commit(&B->st_empty[sp]);
+            }
+          }
+        } else {
+          for (int x = 0; x <= n && ok; ++x) {
+            const uint32_t y = sc + x, s = y % S;
             const uint32_t st = sST + s * L::ST_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-              mma_ss(tbase + C::TM_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(st + L::ST_Q + off, 16, 1024),
-                     IDESC_S, kk > 0);
+            if (x < n) {
+              if (!(ok = mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag))) break;
+              tc_fence_after();
+              mma_s(st);  // P^T(x-1), read by dV(x-1) before, is no longer needed
+              mma_commit(&B->s_full[0]);
             }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-              mma_ss(tbase + C::TM_DP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(st + L::ST_DO + off, 16, 1024),
-                     IDESC_S, kk > 0);
+            if (x >= 1) {
+              // dK(x-1) from dS^T packed in place over dP^T(x-1)
+              const uint32_t sp = (y - 1) % S;
+              if (!(ok = mbar_wait(&B->p_full[1], (y - 1) & 1, abort_flag))) break;
+              tc_fence_after();
+              mma_acc(C::TM_ACC1, C::TM_DP, false, sST + sp * L::ST_BYTES + L::ST_Q, x == 1);
+              mma_commit(&B->st_empty[sp]);
             }
-            mma_commit(&B->s_full[0]);
-            if (x == n - 1) mma_commit(&B->res_empty);
-          };
-          const uint32_t y = sc + x;  // global step index of this CTA
-          if (C::DKDV_OVL && x < n) {
-            if (y >= 1 && !(ok = mbar_wait(&B->s_free, (y - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_sdp();
+            if (x < n) {
+              mma_dp(st);  // after dK(x-1) has read dS^T(x-1)
+              mma_commit(&B->s_full[1]);
+              if (x == n - 1) mma_commit(&B->res_empty);
+              // dV(x) from P^T packed in place over S^T(x)
+              if (!(ok = mbar_wait(&B->p_full[0], y & 1, abort_flag))) break;
+              if (x == 0 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
+              tc_fence_after();
+              mma_acc(C::TM_ACC0, C::TM_S, false, st + L::ST_DO, x == 0);
+            }
           }
-          if (x >= 1) {
-            // dV += P^T dO, dK += dS^T Q for the previous step (K = 128 q rows)
-            const uint32_t sp = (sc + x - 1) % S;
-            if (!(ok = mbar_wait(&B->p_full[0], (y - 1) & 1, abort_flag))) break;
-            if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            const uint32_t stp = sST + sp * L::ST_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t acc = (x > 1 || kk > 0);
-              const uint32_t acol = kk * 8 + (kk >= 4 ? 32 : 0);  // in place: halves at columns 0 and 64
-              const uint32_t a_p = C::DKDV_OVL ? C::TM_KV_P + kk * 8 : C::TM_S + acol;
-              const uint32_t a_ds = C::DKDV_OVL ? C::TM_KV_DS + kk * 8 : C::TM_DP + acol;
-              mma_ts(tbase + C::TM_ACC0, tbase + a_p, sdesc_sw128(stp + L::ST_DO + kk * 2048, C::PANEL, 1024),
-                     IDESC_ACC, acc);
-              mma_ts(tbase + C::TM_ACC1, tbase + a_ds, sdesc_sw128(stp + L::ST_Q + kk * 2048, C::PANEL, 1024),
-                     IDESC_ACC, acc);
-            }
-            if (C::DKDV_OVL) mma_commit(&B->ps_free);
-            mma_commit(&B->st_empty[sp]);
-          }
-          if (!C::DKDV_OVL && x < n) issue_sdp();
         }
         if (ok) mma_commit(&B->acc_full);
         sc += n;
@@ -390,7 +421,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tS = tl + C::TM_S + 64 * hw, tP = tl + C::TM_DP + 64 * hw;
     uint32_t sc = 0, it = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+    for (int w = w_begin; w < w_end && ok; ++w) {
       const DkdvItem itm = p.items[w];
       const int jb = itm.jb, hk = itm.hk;
       const int n = itm.x1 - itm.x0;
@@ -412,40 +443,41 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
-        uint32_t sr[64], dr[64];
-        tmem_ld32(tS, sr);
-        tmem_ld32(tS + 32, sr + 32);
-        tmem_ld32(tP, dr);
-        tmem_ld32(tP + 32, dr + 32);
         const uint8_t* st = smem + L::OFF_ST + s * L::ST_BYTES;
         const float4* l2 = reinterpret_cast<const float4*>(st + L::ST_L) + hw * 16;
         const float4* dl = reinterpret_cast<const float4*>(st + L::ST_D) + hw * 16;
         const int slot = meta[s];
         uint2 mk = make_uint2(0xffffffffu, 0xffffffffu);
         if (slot >= 0) mk = reinterpret_cast<const uint2*>(st + L::ST_M)[2 * r + hw];
-        tmem_ld_wait();
-        if (C::DKDV_OVL) {  // S^T and dP^T are in registers: the MMA may reuse them
+        uint32_t sr[64], pk[32];
+        if constexpr (C::DKDV_OVL) {
+          uint32_t dr[64];
+          tmem_ld32(tS, sr);
+          tmem_ld32(tS + 32, sr + 32);
+          tmem_ld32(tP, dr);
+          tmem_ld32(tP + 32, dr + 32);
+          tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&B->s_free);
-        }
+          mbar_arrive(&B->s_free);  // S^T and dP^T are in registers: the MMA may reuse them
+          uint32_t pk2[32];
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 lv = l2[c4], dv = dl[c4];
-          const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 lv = l2[c4], dv = dl[c4];
+            const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+            float pv[4], dsv[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int c = c4 * 4 + k;
-            const uint32_t word = c < 32 ? mk.x : mk.y;
-            float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]));
-            pr = ((word >> (c & 31)) & 1u) ? pr : 0.f;
-            sr[c] = __float_as_uint(pr);
-            dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - da[k]));
+            for (int k = 0; k < 4; ++k) {
+              const int c = c4 * 4 + k;
+              const uint32_t word = c < 32 ? mk.x : mk.y;
+              float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]));
+              pv[k] = ((word >> (c & 31)) & 1u) ? pr : 0.f;
+              dsv[k] = pv[k] * (__uint_as_float(dr[c]) - da[k]);
+            }
+            pk[2 * c4] = pack_bf16(pv[0], pv[1]);
+            pk[2 * c4 + 1] = pack_bf16(pv[2], pv[3]);
+            pk2[2 * c4] = pack_bf16(dsv[0], dsv[1]);
+            pk2[2 * c4 + 1] = pack_bf16(dsv[2], dsv[3]);
           }
-        }
-        uint32_t pk[32], pk2[32];
-        pack64(sr, pk);
-        pack64(dr, pk2);
-        if (C::DKDV_OVL) {
           // the previous step's accumulate MMAs must be done reading the region
           if (y > 0) {
             ok = mbar_wait(&B->ps_free, (y - 1) & 1, abort_flag);
@@ -457,13 +489,60 @@ __global__ void __launch_bounds__(320, 1)
           }
           tmem_st32(tl + C::TM_KV_P + 32 * hw, pk);
           tmem_st32(tl + C::TM_KV_DS + 32 * hw, pk2);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&B->p_full[0]);
         } else {
-          tmem_st32(tS, pk);
-          tmem_st32(tP, pk2);
+          // P^T first: the MMA runs dK of the previous step and dP^T meanwhile
+          tmem_ld32(tS, sr);
+          tmem_ld32(tS + 32, sr + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 lv = l2[c4];
+            const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int c = c4 * 4 + k;
+              const uint32_t word = c < 32 ? mk.x : mk.y;
+              float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]));
+              sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
+            }
+          }
+          pack64(sr, pk);
+          tmem_st32(tS, pk);  // in place over this warpgroup's S^T columns
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&B->p_full[0]);
+          // then dS^T = P^T (dP^T - Delta)
+          ok = mbar_wait(&B->s_full[1], y & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          {
+            uint32_t dr[64];
+            tmem_ld32(tP, dr);
+            tmem_ld32(tP + 32, dr + 32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4) {
+              const float4 dv = dl[c4];
+              const float da[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int c = c4 * 4 + k;
+                sr[c] = __float_as_uint(__uint_as_float(sr[c]) * (__uint_as_float(dr[c]) - da[k]));
+              }
+            }
+          }
+          pack64(sr, pk);
+          tmem_st32(tP, pk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&B->p_full[1]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&B->p_full[0]);
       }
       if (!ok) break;
       ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
@@ -763,6 +842,361 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
+// 3b. dQ, q-major, software-pipelined three blocks deep
+//
+// One loop iteration of the MMA thread issues S(y) = Q K_y^T, then
+// dQ += dS(y-2) K_{y-2}, then dP(y-1) = dO V_{y-1}^T, for consecutive kv
+// blocks of the CTA's block stream (which runs across items).  dQ comes
+// before dP so that the last dQ of an item, which the compute warpgroups
+// wait for before starting the next item, never waits on that next item.  Each block owns one of
+// three TMEM buffers for its life: S lands there, the compute warpgroups
+// load it and release the buffer for dP, which lands in the same columns,
+// and they write the packed dS over it.  K blocks live in a three-slot ring
+// (read by S and, two iterations later, by dQ) and V blocks in a two-slot
+// ring (read by dP only), so every wait of the MMA thread is on work that
+// was issued an iteration earlier: the tensor pipe, which accepts only a few
+// MMAs ahead of the one executing, never drains on a round trip.  Tile masks
+// are read from global memory, one word pair per thread, a block ahead.
+// ---------------------------------------------------------------------------
+template <int D>
+struct Dq3Cfg {
+  static constexpr int NP = D / 64;
+  static constexpr int PANEL = 128 * 128;  // 128 rows x 128 B
+  static constexpr int TILE = NP * PANEL;
+  static constexpr int KS = 3, VS = 2, NB = 3;  // K ring, V ring, TMEM buffers
+  static constexpr int TM_ACC = NB * 128;
+  static_assert(TM_ACC + D <= 512, "TMEM budget");
+};
+
+template <int D>
+struct Dq3L {
+  using C = Dq3Cfg<D>;
+  static constexpr int OFF_Q = 0, OFF_DO = C::TILE, OFF_K = 2 * C::TILE, OFF_V = OFF_K + C::KS * C::TILE;
+  static constexpr int OFF_BAR = OFF_V + C::VS * C::TILE;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int BYTES = OFF_MISC + 16 + 1024;
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+struct Dq3Bars {
+  uint64_t q_full, q_empty, do_full, do_empty;
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[3], s_loaded[3], dp_full[3], p_full[3];
+  uint64_t acc_full, acc_free, mma_done;
+};
+
+// Walks the CTA's non-empty items and their kv blocks in order.
+struct BlockCursor {
+  int w, x, n, e0, tile, h;
+  uint32_t it;  // index of the current item among the CTA's non-empty items
+  bool valid;
+  __device__ __forceinline__ void next_item(const BwdParams& p, int n_items) {
+    for (w += gridDim.x; w < n_items; w += gridDim.x) {
+      tile = p.order[w / p.Hq];
+      h = w % p.Hq;
+      e0 = p.ptr[tile];
+      n = p.ptr[tile + 1] - e0;
+      if (n > 0) {
+        x = 0;
+        ++it;
+        valid = true;
+        return;
+      }
+    }
+    valid = false;
+  }
+  __device__ __forceinline__ void start(const BwdParams& p, int n_items) {
+    w = (int)blockIdx.x - (int)gridDim.x;
+    it = 0xffffffffu;
+    next_item(p, n_items);
+  }
+  __device__ __forceinline__ void next(const BwdParams& p, int n_items) {
+    if (++x >= n) next_item(p, n_items);
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    k_bwd_dq3(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
+              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const BwdParams p) {
+  using C = Dq3Cfg<D>;
+  using L = Dq3L<D>;
+  static_assert(sizeof(Dq3Bars) <= 256, "barrier block");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Dq3Bars* B = reinterpret_cast<Dq3Bars*>(smem + L::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = p.Hq / p.Hkv;
+  const int n_items = p.n_major * p.Hq;
+
+  if (threadIdx.x == 256) {
+    mbar_init(&B->q_full, 1);
+    mbar_init(&B->q_empty, 1);
+    mbar_init(&B->do_full, 1);
+    mbar_init(&B->do_empty, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&B->k_full[i], 1);
+      mbar_init(&B->k_empty[i], 1);
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->s_loaded[i], 256);
+      mbar_init(&B->dp_full[i], 1);
+      mbar_init(&B->p_full[i], 256);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->v_full[i], 1);
+      mbar_init(&B->v_empty[i], 1);
+    }
+    mbar_init(&B->acc_full, 1);
+    mbar_init(&B->acc_free, 256);
+    mbar_init(&B->mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mQ);
+    prefetch_tmap(&mdO);
+    prefetch_tmap(&mK);
+    prefetch_tmap(&mV);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      BlockCursor c;
+      c.start(p, n_items);
+      // loads issued: K and V blocks, Q and dO tiles
+      uint32_t y = 0, nk = 0, nv = 0, nq = 0, ndo = 0;
+      bool ok = true;
+      for (; c.valid && ok; c.next(p, n_items), ++y) {
+        const int hk = c.h / g, j = p.idx[c.e0 + c.x];
+        if (c.x == 0) {
+          if (c.it > 0 && !(ok = mbar_wait(&B->q_empty, (c.it - 1) & 1, abort_flag))) break;
+          mbar_expect_tx(&B->q_full, C::TILE);
+#pragma unroll
+          for (int pn = 0; pn < C::NP; ++pn)
+            tma_load_3d(smem + L::OFF_Q + pn * C::PANEL, &mQ, &B->q_full, pn * 64, c.h, c.tile * 128);
+          ++nq;
+        }
+        const uint32_t ks = y % 3;
+        if (y >= 3 && !(ok = mbar_wait(&B->k_empty[ks], (y / 3 - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(&B->k_full[ks], C::TILE);
+#pragma unroll
+        for (int pn = 0; pn < C::NP; ++pn)
+          tma_load_3d(smem + L::OFF_K + ks * C::TILE + pn * C::PANEL, &mK, &B->k_full[ks], pn * 64, hk, j * 128);
+        ++nk;
+        if (c.x == 0) {
+          if (c.it > 0 && !(ok = mbar_wait(&B->do_empty, (c.it - 1) & 1, abort_flag))) break;
+          mbar_expect_tx(&B->do_full, C::TILE);
+#pragma unroll
+          for (int pn = 0; pn < C::NP; ++pn)
+            tma_load_3d(smem + L::OFF_DO + pn * C::PANEL, &mdO, &B->do_full, pn * 64, c.h, c.tile * 128);
+          ++ndo;
+        }
+        const uint32_t vs = y % 2;
+        if (y >= 2 && !(ok = mbar_wait(&B->v_empty[vs], (y / 2 - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(&B->v_full[vs], C::TILE);
+#pragma unroll
+        for (int pn = 0; pn < C::NP; ++pn)
+          tma_load_3d(smem + L::OFF_V + vs * C::TILE + pn * C::PANEL, &mV, &B->v_full[vs], pn * 64, hk, j * 128);
+        ++nv;
+      }
+      if (!ok) {
+        // let every load already issued land before the CTA exits
+        const long long lim = 20000000;
+        if (nq > 0) mbar_wait_drain(&B->q_full, (nq - 1) & 1, lim);
+        if (ndo > 0) mbar_wait_drain(&B->do_full, (ndo - 1) & 1, lim);
+        for (uint32_t k = 0; k < 3 && k < nk; ++k) {
+          const uint32_t last = nk - 1 - ((nk - 1 - k) % 3);
+          mbar_wait_drain(&B->k_full[k], (last / 3) & 1, lim);
+        }
+        for (uint32_t k = 0; k < 2 && k < nv; ++k) {
+          const uint32_t last = nv - 1 - ((nv - 1 - k) % 2);
+          mbar_wait_drain(&B->v_full[k], (last / 2) & 1, lim);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);
+      const uint32_t sQ = smem_u32(smem + L::OFF_Q), sdO = smem_u32(smem + L::OFF_DO);
+      const uint32_t sK = smem_u32(smem + L::OFF_K), sV = smem_u32(smem + L::OFF_V);
+      BlockCursor cs, cp, cq;  // blocks for S, dP and dQ
+      cs.start(p, n_items);
+      cp = cs;
+      cq = cs;
+      uint32_t ys = 0, yp = 0, yq = 0;
+      bool ok = true;
+      for (uint32_t t = 0; cq.valid && ok; ++t) {
+        if (cs.valid) {
+          // S(ys) into TMEM buffer ys % 3; the buffer's previous block has
+          // had its dQ issued an iteration ago
+          if (cs.x == 0 && !(ok = mbar_wait(&B->q_full, cs.it & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(&B->k_full[ys % 3], (ys / 3) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t kb = sK + (ys % 3) * C::TILE, buf = (ys % 3) * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+            mma_ss(tbase + buf, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), IDESC_S, kk > 0);
+          }
+          mma_commit(&B->s_full[ys % 3]);
+          if (cs.x == cs.n - 1) mma_commit(&B->q_empty);
+          cs.next(p, n_items);
+          ++ys;
+        }
+        if (t >= 2) {
+          // dQ += dS(yq) K(yq) (K = 128 kv rows), dS packed over the buffer:
+          // warpgroup w's 64 columns of dS at buffer columns [64w, 64w + 32)
+          if (!(ok = mbar_wait(&B->p_full[yq % 3], (yq / 3) & 1, abort_flag))) break;
+          if (cq.x == 0 && cq.it > 0 && !(ok = mbar_wait(&B->acc_free, (cq.it - 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t kb = sK + (yq % 3) * C::TILE, buf = (yq % 3) * 128;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tbase + C::TM_ACC, tbase + buf + kk * 8 + (kk >= 4 ? 32 : 0),
+                   sdesc_sw128(kb + kk * 2048, C::PANEL, 1024), IDESC_ACC, (cq.x > 0 || kk > 0));
+          mma_commit(&B->k_empty[yq % 3]);
+          if (cq.x == cq.n - 1) mma_commit(&B->acc_full);
+          cq.next(p, n_items);
+          ++yq;
+        }
+        if (t >= 1 && cp.valid) {
+          // dP(yp) over S(yp), once the compute warpgroups hold S(yp)
+          if (cp.x == 0 && !(ok = mbar_wait(&B->do_full, cp.it & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(&B->v_full[yp % 2], (yp / 2) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(&B->s_loaded[yp % 3], (yp / 3) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t vb = sV + (yp % 2) * C::TILE, buf = (yp % 3) * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+            mma_ss(tbase + buf, sdesc_sw128(sdO + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024), IDESC_S, kk > 0);
+          }
+          mma_commit(&B->dp_full[yp % 3]);
+          mma_commit(&B->v_empty[yp % 2]);
+          if (cp.x == cp.n - 1) mma_commit(&B->do_empty);
+          cp.next(p, n_items);
+          ++yp;
+        }
+      }
+      mma_commit(&B->mma_done);
+      mbar_wait_drain(&B->mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute (q row per thread)
+    const int hw = warp >> 2;  // which 64 kv columns of each block this warpgroup takes
+    const int r = threadIdx.x & 127;
+    const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + 64 * hw;
+    const uint2* masks = reinterpret_cast<const uint2*>(p.masks);
+    uint32_t y = 0, it = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const int tile = p.order[w / p.Hq], h = w % p.Hq;
+      const int e0 = p.ptr[tile], n = p.ptr[tile + 1] - e0;
+      const int q = tile * 128 + r;
+      __nv_bfloat16* orow = p.out0 + ((size_t)q * p.Hq + h) * D + hw * (D / 2);  // this warpgroup's columns
+      if (n == 0) {
+        if (q < p.T) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < D / 16; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+        }
+        continue;
+      }
+      const float l2 = p.lse2[(size_t)h * p.Tpad + q];
+      const float dl = p.delta[(size_t)h * p.Tpad + q];
+      int slot = p.pidx[e0];
+      uint2 mk = slot >= 0 ? masks[(size_t)slot * 256 + 2 * r + hw] : make_uint2(0xffffffffu, 0xffffffffu);
+      for (int x = 0; x < n; ++x, ++y) {
+        // the next block's mask, a block ahead
+        uint2 mk_next = make_uint2(0xffffffffu, 0xffffffffu);
+        if (x + 1 < n) {
+          const int sn = p.pidx[e0 + x + 1];
+          if (sn >= 0) mk_next = masks[(size_t)sn * 256 + 2 * r + hw];
+        }
+        const uint32_t b = y % 3, ph = (y / 3) & 1, col = b * 128;
+        ok = mbar_wait(&B->s_full[b], ph, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(tl + col, sr);
+        tmem_ld32(tl + col + 32, sr + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&B->s_loaded[b]);  // dP may now overwrite S
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const uint32_t word = c < 32 ? mk.x : mk.y;
+          const float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2));
+          sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
+        }
+        ok = mbar_wait(&B->dp_full[b], ph, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t pk[32];
+        {
+          uint32_t dr[64];
+          tmem_ld32(tl + col, dr);
+          tmem_ld32(tl + col + 32, dr + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2)
+            pk[c2] = pack_bf16(__uint_as_float(sr[2 * c2]) * (__uint_as_float(dr[2 * c2]) - dl),
+                               __uint_as_float(sr[2 * c2 + 1]) * (__uint_as_float(dr[2 * c2 + 1]) - dl));
+        }
+        tmem_st32(tl + col, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&B->p_full[b]);
+        mk = mk_next;
+      }
+      if (!ok) break;
+      ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t ta = tbase + ((uint32_t)((warp & 3) * 32) << 16) + C::TM_ACC + hw * (D / 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld32(ta + c * 32, v);
+        tmem_ld_wait();
+        if (q < p.T) store_row32(orow + c * 32, v, p.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(&B->acc_free);
+      ++it;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tbase, 512);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 template <class K>
@@ -780,14 +1214,17 @@ int reserve_smem(K kernel, int bytes, int dev, int* flags) {
 
 // Work items of the kv-major kernel for one head layout, cached on the map.
 // Columns with more steps than about one SM's share are cut into chunks that
-// write fp32 partials to workspace slots (at most max_slots of them); items
-// are ordered longest first.
+// write fp32 partial sums to workspace slots (at most max_slots of them).  The
+// items are then packed onto the grid's CTAs longest first, each to the CTA
+// with the least work so far (LPT list scheduling), and stored grouped by CTA.
 std::mutex g_items_mu;
 
 int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, cudaStream_t s) {
   pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
   std::lock_guard<std::mutex> lk(g_items_mu);
-  if (bm->bwd_items && bm->bwd_g == g && bm->bwd_hkv == Hkv && bm->bwd_max_slots == max_slots) return 0;
+  if (bm->bwd_items && bm->bwd_g == g && bm->bwd_hkv == Hkv && bm->bwd_max_slots == max_slots &&
+      bm->bwd_sms == sms)
+    return 0;
   const int nk = bm->nk;
   long long total = 0;
   for (int j = 0; j < nk; ++j) total += (long long)g * bm->h_col_cnt[j] * Hkv;
@@ -825,22 +1262,51 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
   }
   std::stable_sort(items.begin(), items.end(),
                    [](const DkdvItem& a, const DkdvItem& b) { return (a.x1 - a.x0) > (b.x1 - b.x0); });
+  // LPT packing; an item costs its steps plus about two steps of fixed work
+  // (the resident K/V tile and the epilogue).
+  const int grid = std::min<int>(sms, std::max<int>((int)items.size(), 1));
+  std::vector<std::vector<int>> bins(grid);
+  {
+    using Load = std::pair<long long, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int b = 0; b < grid; ++b) heap.push(Load(0, b));
+    for (int i = 0; i < (int)items.size(); ++i) {
+      Load l = heap.top();
+      heap.pop();
+      bins[l.second].push_back(i);
+      l.first += (items[i].x1 - items[i].x0) + 2;
+      heap.push(l);
+    }
+  }
+  std::vector<DkdvItem> packed;
+  std::vector<int> cta(grid + 1, 0);
+  packed.reserve(items.size());
+  for (int b = 0; b < grid; ++b) {
+    for (int i : bins[b]) packed.push_back(items[i]);
+    cta[b + 1] = (int)packed.size();
+  }
   pool_free(bm->bwd_mem, s);
   bm->bwd_mem = nullptr;
   bm->bwd_items = nullptr;
-  const size_t bi = sizeof(DkdvItem) * std::max<size_t>(items.size(), 1);
+  const size_t bi = sizeof(DkdvItem) * std::max<size_t>(packed.size(), 1);
   const size_t bs = sizeof(int4) * std::max<size_t>(splits.size(), 1);
-  int rc = pool_alloc(&bm->bwd_mem, bi + bs, bm->device, s);
+  const size_t bc = sizeof(int) * (grid + 1);
+  int rc = pool_alloc(&bm->bwd_mem, bi + bs + bc, bm->device, s);
   if (rc) return rc;
   bm->bwd_items = bm->bwd_mem;
   bm->bwd_splits = static_cast<char*>(bm->bwd_mem) + bi;
-  if ((rc = upload(bm->bwd_items, items.data(), sizeof(DkdvItem) * items.size(), bm->device, s))) return rc;
+  bm->bwd_cta = static_cast<char*>(bm->bwd_mem) + bi + bs;
+  if (!packed.empty() && (rc = upload(bm->bwd_items, packed.data(), sizeof(DkdvItem) * packed.size(), bm->device, s)))
+    return rc;
   if (!splits.empty() && (rc = upload(bm->bwd_splits, splits.data(), sizeof(int4) * splits.size(), bm->device, s)))
     return rc;
+  if ((rc = upload(bm->bwd_cta, cta.data(), bc, bm->device, s))) return rc;
   bm->bwd_g = g;
   bm->bwd_hkv = Hkv;
   bm->bwd_max_slots = max_slots;
-  bm->bwd_n_items = (int)items.size();
+  bm->bwd_n_items = (int)packed.size();
+  bm->bwd_grid = grid;
+  bm->bwd_sms = sms;
   bm->bwd_n_splits = (int)splits.size();
   bm->bwd_n_slots = slot;
   return 0;
@@ -853,7 +1319,12 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   static int set_dkdv[64] = {0}, set_dq[64] = {0};
   const int dev = bm->device;
   int rc = reserve_smem(k_bwd_dkdv<D>, DkdvL<D>::BYTES, dev, set_dkdv);
-  if (!rc) rc = reserve_smem(k_bwd_dq<D>, DqL<D>::BYTES, dev, set_dq);
+  if (!rc) {
+    if constexpr (D == 128)
+      rc = reserve_smem(k_bwd_dq3<D>, Dq3L<D>::BYTES, dev, set_dq);
+    else
+      rc = reserve_smem(k_bwd_dq<D>, DqL<D>::BYTES, dev, set_dq);
+  }
   if (rc) return rc;
   if (bm->n_partial > 0 && (!bm->mask_rows || !bm->mask_cols)) {
     set_error("backward kernel: block map has no tile masks");
@@ -893,11 +1364,12 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   p.n_major = bm->nk;
   p.items = static_cast<const DkdvItem*>(bm->bwd_items);
   p.n_items = bm->bwd_n_items;
+  p.cta_ptr = static_cast<const int*>(bm->bwd_cta);
   p.partial = partial;
   int launches = 1;
   if (p.n_items > 0) {
     ProfScope ps(s, "bwd_dkdv");
-    k_bwd_dkdv<D><<<p.n_items < sms ? p.n_items : sms, 320, DkdvL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    k_bwd_dkdv<D><<<bm->bwd_grid, 320, DkdvL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
     ++launches;
   }
   if (bm->bwd_n_splits > 0) {
@@ -917,11 +1389,16 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   p.out1 = nullptr;
   p.n_major = bm->nq;
   p.items = nullptr;
+  p.cta_ptr = nullptr;
   p.partial = nullptr;
   const int items = bm->nq * Hq;
   if (items > 0) {
     ProfScope ps(s, "bwd_dq");
-    k_bwd_dq<D><<<items < sms ? items : sms, 320, DqL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    if constexpr (D == 128) {
+      k_bwd_dq3<D><<<items < sms ? items : sms, 320, Dq3L<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    } else {
+      k_bwd_dq<D><<<items < sms ? items : sms, 320, DqL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    }
     ++launches;
   }
   count_launch(launches);

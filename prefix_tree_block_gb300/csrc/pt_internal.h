@@ -62,8 +62,9 @@ struct pt_blockmap {
   int* h_col_cnt;  // [nk]
   // backward work items of the kv-major kernel, cached for one head layout
   void* bwd_mem;
-  int bwd_g, bwd_hkv, bwd_max_slots, bwd_n_items, bwd_n_splits, bwd_n_slots;
-  void* bwd_items;   // DkdvItem[bwd_n_items] (device)
+  int bwd_g, bwd_hkv, bwd_max_slots, bwd_n_items, bwd_n_splits, bwd_n_slots, bwd_grid, bwd_sms;
+  void* bwd_items;   // DkdvItem[bwd_n_items] (device), grouped by the CTA that runs them
+  void* bwd_cta;     // int[bwd_grid + 1]: CTA b runs items [bwd_cta[b], bwd_cta[b + 1])
   void* bwd_splits;  // int4[bwd_n_splits]: kv block, kv head, first slot, slot count (device)
 };
 
