@@ -679,6 +679,8 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
 void free_map(pt_blockmap* bm) {
   if (!bm) return;
   pool_free(bm->bwd_mem, bm->stream);
+  pool_free(bm->dq_mem, bm->stream);
+  std::free(bm->h_dq_empty);
   std::free(bm->h_counts);
   pool_free(bm->mem_lists, bm->stream);
   pool_free(bm->mem_fixed, bm->stream);

@@ -124,6 +124,8 @@ struct BwdParams {
   __nv_bfloat16* out1;    // dV (dkdv)
   const DkdvItem* items;  // dkdv work items, grouped by CTA
   const int* cta_ptr;     // dkdv: CTA b runs items [cta_ptr[b], cta_ptr[b + 1])
+  const int4* dq_items;   // pipelined dq: q tile, head, first list entry, kv blocks; grouped by CTA
+  const int4* dq_cta;     // pipelined dq: first item, end item, kv blocks of each CTA
   float* partial;         // dkdv: fp32 partial sums of split columns, [slot][128][2D]
   int T, Tpad, Hq, Hkv, n_major, n_items;
   float scale, scale_log2;
@@ -842,112 +844,90 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
-// 3b. dQ, q-major, software-pipelined three blocks deep
+// 3b. dQ, q-major, software-pipelined three blocks deep (D = 128)
 //
-// One loop iteration of the MMA thread issues S(y) = Q K_y^T, then
-// dQ += dS(y-2) K_{y-2}, then dP(y-1) = dO V_{y-1}^T, for consecutive kv
-// blocks of the CTA's block stream (which runs across items).  dQ comes
-// before dP so that the last dQ of an item, which the compute warpgroups
-// wait for before starting the next item, never waits on that next item.  Each block owns one of
-// three TMEM buffers for its life: S lands there, the compute warpgroups
-// load it and release the buffer for dP, which lands in the same columns,
-// and they write the packed dS over it.  K blocks live in a three-slot ring
-// (read by S and, two iterations later, by dQ) and V blocks in a two-slot
-// ring (read by dP only), so every wait of the MMA thread is on work that
-// was issued an iteration earlier: the tensor pipe, which accepts only a few
-// MMAs ahead of the one executing, never drains on a round trip.  Tile masks
-// are read from global memory, one word pair per thread, a block ahead.
+// Each CTA runs a host-built list of (q tile, head) items, packed longest
+// first onto the CTAs, as one stream of kv blocks.  One loop iteration of the
+// MMA thread issues S(t) = Q K_t^T, dP(t-1) = dO V_{t-1}^T and dQ += dS(t-2)
+// K_{t-2}; the last dQ of an item goes before the dP, since the compute
+// warpgroups finish an item (its epilogue) before they load the next block's
+// S, which that dP waits for.  Each block owns one of three TMEM buffers for
+// its life: S lands there, the compute warpgroups load it and release the
+// buffer for dP, which lands in the same columns, and they write the packed
+// dS over it.  K blocks live in a four-slot ring (read by S and, two
+// iterations later, by dQ, so K(t+4) loads while S(t+1)..S(t+3) run) and V
+// blocks in a one-slot ring (read by dP only), each filled by its own
+// producer warp; an item's Q and dO travel with its first K and V block.
+//
+// The tensor pipe accepts only a few MMAs ahead of the one executing, and a
+// barrier check issued right after a group of MMAs completes only when the
+// group has drained; so the MMA thread checks everything a group needs in one
+// batch, keeps item boundaries in registers and does as little else as it can
+// between groups.  Tile masks are read from global memory, a block ahead.
 // ---------------------------------------------------------------------------
 template <int D>
-struct Dq3Cfg {
+struct DqpCfg {
   static constexpr int NP = D / 64;
   static constexpr int PANEL = 128 * 128;  // 128 rows x 128 B
   static constexpr int TILE = NP * PANEL;
-  static constexpr int KS = 3, VS = 2, NB = 3;  // K ring, V ring, TMEM buffers
+  static constexpr int KS = 4, NB = 3;     // K ring slots, TMEM buffers (V ring: one slot)
+  static constexpr int THREADS = 352;      // 8 compute warps, K producer, MMA, V producer
   static constexpr int TM_ACC = NB * 128;
   static_assert(TM_ACC + D <= 512, "TMEM budget");
 };
 
 template <int D>
-struct Dq3L {
-  using C = Dq3Cfg<D>;
+struct DqpL {
+  using C = DqpCfg<D>;
   static constexpr int OFF_Q = 0, OFF_DO = C::TILE, OFF_K = 2 * C::TILE, OFF_V = OFF_K + C::KS * C::TILE;
-  static constexpr int OFF_BAR = OFF_V + C::VS * C::TILE;
+  static constexpr int OFF_BAR = OFF_V + C::TILE;
   static constexpr int OFF_MISC = OFF_BAR + 256;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
-struct Dq3Bars {
-  uint64_t q_full, q_empty, do_full, do_empty;
-  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+struct DqpBars {
+  uint64_t k_full[4], k_empty[4], v_full, v_empty, q_empty, do_empty;
   uint64_t s_full[3], s_loaded[3], dp_full[3], p_full[3];
   uint64_t acc_full, acc_free, mma_done;
 };
 
-// Walks the CTA's non-empty items and their kv blocks in order.
-struct BlockCursor {
-  int w, x, n, e0, tile, h;
-  uint32_t it;  // index of the current item among the CTA's non-empty items
-  bool valid;
-  __device__ __forceinline__ void next_item(const BwdParams& p, int n_items) {
-    for (w += gridDim.x; w < n_items; w += gridDim.x) {
-      tile = p.order[w / p.Hq];
-      h = w % p.Hq;
-      e0 = p.ptr[tile];
-      n = p.ptr[tile + 1] - e0;
-      if (n > 0) {
-        x = 0;
-        ++it;
-        valid = true;
-        return;
-      }
-    }
-    valid = false;
-  }
-  __device__ __forceinline__ void start(const BwdParams& p, int n_items) {
-    w = (int)blockIdx.x - (int)gridDim.x;
-    it = 0xffffffffu;
-    next_item(p, n_items);
-  }
-  __device__ __forceinline__ void next(const BwdParams& p, int n_items) {
-    if (++x >= n) next_item(p, n_items);
-  }
-};
+// 64-bit shared-memory descriptor plus a byte offset that keeps the address
+// below 256 KB (no carry out of the 14-bit start-address field).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
-    k_bwd_dq3(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
-              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const BwdParams p) {
-  using C = Dq3Cfg<D>;
-  using L = Dq3L<D>;
-  static_assert(sizeof(Dq3Bars) <= 256, "barrier block");
+__global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
+    k_bwd_dq_pipe(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
+                  const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const BwdParams p) {
+  using C = DqpCfg<D>;
+  using L = DqpL<D>;
+  static_assert(sizeof(DqpBars) <= 256, "barrier block");
+  constexpr uint32_t FIRST = 1, LAST = 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Dq3Bars* B = reinterpret_cast<Dq3Bars*>(smem + L::OFF_BAR);
+  DqpBars* B = reinterpret_cast<DqpBars*>(smem + L::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.Hq / p.Hkv;
-  const int n_items = p.n_major * p.Hq;
+  const int4 cta = p.dq_cta[blockIdx.x];  // first item, end item, kv blocks
 
   if (threadIdx.x == 256) {
-    mbar_init(&B->q_full, 1);
-    mbar_init(&B->q_empty, 1);
-    mbar_init(&B->do_full, 1);
-    mbar_init(&B->do_empty, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&B->k_full[i], 1);
       mbar_init(&B->k_empty[i], 1);
+    }
+    mbar_init(&B->v_full, 1);
+    mbar_init(&B->v_empty, 1);
+    mbar_init(&B->q_empty, 1);
+    mbar_init(&B->do_empty, 1);
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&B->s_full[i], 1);
       mbar_init(&B->s_loaded[i], 256);
       mbar_init(&B->dp_full[i], 1);
       mbar_init(&B->p_full[i], 256);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&B->v_full[i], 1);
-      mbar_init(&B->v_empty[i], 1);
     }
     mbar_init(&B->acc_full, 1);
     mbar_init(&B->acc_free, 256);
@@ -968,59 +948,51 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // warp 8: the K ring (and each item's Q); warp 10: the V slot (and dO)
     if (lane == 0) {
-      BlockCursor c;
-      c.start(p, n_items);
-      // loads issued: K and V blocks, Q and dO tiles
-      uint32_t y = 0, nk = 0, nv = 0, nq = 0, ndo = 0;
+      const bool kp = warp == 8;
+      uint32_t y = 0;  // blocks whose loads were issued
       bool ok = true;
-      for (; c.valid && ok; c.next(p, n_items), ++y) {
-        const int hk = c.h / g, j = p.idx[c.e0 + c.x];
-        if (c.x == 0) {
-          if (c.it > 0 && !(ok = mbar_wait(&B->q_empty, (c.it - 1) & 1, abort_flag))) break;
-          mbar_expect_tx(&B->q_full, C::TILE);
+      for (int k = cta.x; k < cta.y && ok; ++k) {
+        const int4 itm = p.dq_items[k];  // q tile, head, first entry, blocks
+        const int hk = itm.y / g, ki = k - cta.x;
+        for (int x = 0; x < itm.w; ++x) {
+          const int j = p.idx[itm.z + x];
+          if (kp) {
+            const uint32_t sl = y % C::KS;
+            if (y >= C::KS && !(ok = mbar_wait(&B->k_empty[sl], (y / C::KS - 1) & 1, abort_flag))) break;
+            if (x == 0 && ki > 0 && !(ok = mbar_wait(&B->q_empty, (ki - 1) & 1, abort_flag))) break;
+            mbar_expect_tx(&B->k_full[sl], x == 0 ? 2 * C::TILE : C::TILE);
 #pragma unroll
-          for (int pn = 0; pn < C::NP; ++pn)
-            tma_load_3d(smem + L::OFF_Q + pn * C::PANEL, &mQ, &B->q_full, pn * 64, c.h, c.tile * 128);
-          ++nq;
+            for (int pn = 0; pn < C::NP; ++pn) {
+              if (x == 0) tma_load_3d(smem + L::OFF_Q + pn * C::PANEL, &mQ, &B->k_full[sl], pn * 64, itm.y, itm.x * 128);
+              tma_load_3d(smem + L::OFF_K + sl * C::TILE + pn * C::PANEL, &mK, &B->k_full[sl], pn * 64, hk, j * 128);
+            }
+          } else {
+            if (y >= 1 && !(ok = mbar_wait(&B->v_empty, (y - 1) & 1, abort_flag))) break;
+            if (x == 0 && ki > 0 && !(ok = mbar_wait(&B->do_empty, (ki - 1) & 1, abort_flag))) break;
+            mbar_expect_tx(&B->v_full, x == 0 ? 2 * C::TILE : C::TILE);
+#pragma unroll
+            for (int pn = 0; pn < C::NP; ++pn) {
+              if (x == 0) tma_load_3d(smem + L::OFF_DO + pn * C::PANEL, &mdO, &B->v_full, pn * 64, itm.y, itm.x * 128);
+              tma_load_3d(smem + L::OFF_V + pn * C::PANEL, &mV, &B->v_full, pn * 64, hk, j * 128);
+            }
+          }
+          ++y;
         }
-        const uint32_t ks = y % 3;
-        if (y >= 3 && !(ok = mbar_wait(&B->k_empty[ks], (y / 3 - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(&B->k_full[ks], C::TILE);
-#pragma unroll
-        for (int pn = 0; pn < C::NP; ++pn)
-          tma_load_3d(smem + L::OFF_K + ks * C::TILE + pn * C::PANEL, &mK, &B->k_full[ks], pn * 64, hk, j * 128);
-        ++nk;
-        if (c.x == 0) {
-          if (c.it > 0 && !(ok = mbar_wait(&B->do_empty, (c.it - 1) & 1, abort_flag))) break;
-          mbar_expect_tx(&B->do_full, C::TILE);
-#pragma unroll
-          for (int pn = 0; pn < C::NP; ++pn)
-            tma_load_3d(smem + L::OFF_DO + pn * C::PANEL, &mdO, &B->do_full, pn * 64, c.h, c.tile * 128);
-          ++ndo;
-        }
-        const uint32_t vs = y % 2;
-        if (y >= 2 && !(ok = mbar_wait(&B->v_empty[vs], (y / 2 - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(&B->v_full[vs], C::TILE);
-#pragma unroll
-        for (int pn = 0; pn < C::NP; ++pn)
-          tma_load_3d(smem + L::OFF_V + vs * C::TILE + pn * C::PANEL, &mV, &B->v_full[vs], pn * 64, hk, j * 128);
-        ++nv;
       }
       if (!ok) {
         // let every load already issued land before the CTA exits
         const long long lim = 20000000;
-        if (nq > 0) mbar_wait_drain(&B->q_full, (nq - 1) & 1, lim);
-        if (ndo > 0) mbar_wait_drain(&B->do_full, (ndo - 1) & 1, lim);
-        for (uint32_t k = 0; k < 3 && k < nk; ++k) {
-          const uint32_t last = nk - 1 - ((nk - 1 - k) % 3);
-          mbar_wait_drain(&B->k_full[k], (last / 3) & 1, lim);
-        }
-        for (uint32_t k = 0; k < 2 && k < nv; ++k) {
-          const uint32_t last = nv - 1 - ((nv - 1 - k) % 2);
-          mbar_wait_drain(&B->v_full[k], (last / 2) & 1, lim);
+        if (kp) {
+          for (uint32_t k = 0; k < C::KS && k < y; ++k) {
+            const uint32_t last = y - 1 - ((y - 1 - k) % C::KS);
+            mbar_wait_drain(&B->k_full[k], (last / C::KS) & 1, lim);
+          }
+        } else if (y > 0) {
+          mbar_wait_drain(&B->v_full, (y - 1) & 1, lim);
         }
       }
     }
@@ -1030,66 +1002,91 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
       constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);
-      const uint32_t sQ = smem_u32(smem + L::OFF_Q), sdO = smem_u32(smem + L::OFF_DO);
-      const uint32_t sK = smem_u32(smem + L::OFF_K), sV = smem_u32(smem + L::OFF_V);
-      BlockCursor cs, cp, cq;  // blocks for S, dP and dQ
-      cs.start(p, n_items);
-      cp = cs;
-      cq = cs;
-      uint32_t ys = 0, yp = 0, yq = 0;
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
+      const uint64_t dO0 = sdesc_sw128(smem_u32(smem + L::OFF_DO), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + L::OFF_V), 16, 1024);
+      const uint64_t dKt0 = sdesc_sw128(smem_u32(smem + L::OFF_K), C::PANEL, 1024);  // K as the MN-major B of dQ
+      const uint32_t total = (uint32_t)cta.z;
+      // item boundaries of the S stream: [s_beg, s_end), the next item's size prefetched
+      int k = cta.x;
+      uint32_t s_beg = 0, s_end = total > 0 ? (uint32_t)p.dq_items[k].w : 0;
+      int n_next = k + 1 < cta.y ? p.dq_items[k + 1].w : 0;
+      uint32_t fp = 0, fq = 0, itq = 0;  // flags of blocks t-1 and t-2; items whose dQ is done
       bool ok = true;
-      for (uint32_t t = 0; cq.valid && ok; ++t) {
-        if (cs.valid) {
-          // S(ys) into TMEM buffer ys % 3; the buffer's previous block has
-          // had its dQ issued an iteration ago
-          if (cs.x == 0 && !(ok = mbar_wait(&B->q_full, cs.it & 1, abort_flag))) break;
-          if (!(ok = mbar_wait(&B->k_full[ys % 3], (ys / 3) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t kb = sK + (ys % 3) * C::TILE, buf = (ys % 3) * 128;
+      for (uint32_t t = 0; t < total + 2 && ok; ++t) {
+        const bool has_s = t < total, has_dp = t >= 1 && t <= total, has_dq = t >= 2;
+        uint32_t fs = 0;
+        if (has_s) {
+          if (t == s_end) {
+            s_beg = s_end;
+            s_end += (uint32_t)n_next;
+            ++k;
+            n_next = k + 1 < cta.y ? p.dq_items[k + 1].w : 0;
+          }
+          fs = (t == s_beg ? FIRST : 0u) | (t + 1 == s_end ? LAST : 0u);
+        }
+        const bool dq_first = has_dq && (fq & LAST);
+        const bool dp_now = has_dp && !dq_first;
+        const uint32_t bs = t % 3, bp = (t + 2) % 3, bq = (t + 1) % 3;  // TMEM buffers of t, t-1, t-2
+        {
+          uint64_t* const bars[3] = {has_s ? &B->k_full[t % C::KS] : nullptr, dp_now ? &B->v_full : nullptr,
+                                     dp_now ? &B->s_loaded[bp] : nullptr};
+          const uint32_t par[3] = {(t / C::KS) & 1, (t - 1) & 1, ((t - 1) / 3) & 1};
+          if (!(ok = mbar_wait_all(bars, par, abort_flag))) break;
+        }
+        tc_fence_after();
+        if (has_s) {
+          const uint64_t db = sdesc_add(dK0, (t % C::KS) * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-            mma_ss(tbase + buf, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), IDESC_S, kk > 0);
+            mma_ss(tbase + bs * 128, sdesc_add(dQ0, off), sdesc_add(db, off), IDESC_S, kk > 0);
           }
-          mma_commit(&B->s_full[ys % 3]);
-          if (cs.x == cs.n - 1) mma_commit(&B->q_empty);
-          cs.next(p, n_items);
-          ++ys;
+          mma_commit(&B->s_full[bs]);
+          if (fs & LAST) mma_commit(&B->q_empty);
         }
-        if (t >= 2) {
-          // dQ += dS(yq) K(yq) (K = 128 kv rows), dS packed over the buffer:
-          // warpgroup w's 64 columns of dS at buffer columns [64w, 64w + 32)
-          if (!(ok = mbar_wait(&B->p_full[yq % 3], (yq / 3) & 1, abort_flag))) break;
-          if (cq.x == 0 && cq.it > 0 && !(ok = mbar_wait(&B->acc_free, (cq.it - 1) & 1, abort_flag))) break;
+        const auto issue_dp = [&]() {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
+            mma_ss(tbase + bp * 128, sdesc_add(dO0, off), sdesc_add(dV0, off), IDESC_S, kk > 0);
+          }
+          mma_commit(&B->dp_full[bp]);
+          mma_commit(&B->v_empty);
+          if (fp & LAST) mma_commit(&B->do_empty);
+        };
+        if (dp_now) issue_dp();
+        if (has_dq) {
+          // dQ += dS(t-2) K(t-2) (K = 128 kv rows); warpgroup w's packed dS
+          // at buffer columns [64w, 64w + 32)
+          const bool first = fq & FIRST;
+          {
+            uint64_t* const bars[2] = {&B->p_full[bq], first && itq > 0 ? &B->acc_free : nullptr};
+            const uint32_t par[2] = {((t - 2) / 3) & 1, (itq - 1) & 1};
+            if (!(ok = mbar_wait_all(bars, par, abort_flag))) break;
+          }
           tc_fence_after();
-          const uint32_t kb = sK + (yq % 3) * C::TILE, buf = (yq % 3) * 128;
+          const uint64_t db = sdesc_add(dKt0, ((t - 2) % C::KS) * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tbase + C::TM_ACC, tbase + buf + kk * 8 + (kk >= 4 ? 32 : 0),
-                   sdesc_sw128(kb + kk * 2048, C::PANEL, 1024), IDESC_ACC, (cq.x > 0 || kk > 0));
-          mma_commit(&B->k_empty[yq % 3]);
-          if (cq.x == cq.n - 1) mma_commit(&B->acc_full);
-          cq.next(p, n_items);
-          ++yq;
-        }
-        if (t >= 1 && cp.valid) {
-          // dP(yp) over S(yp), once the compute warpgroups hold S(yp)
-          if (cp.x == 0 && !(ok = mbar_wait(&B->do_full, cp.it & 1, abort_flag))) break;
-          if (!(ok = mbar_wait(&B->v_full[yp % 2], (yp / 2) & 1, abort_flag))) break;
-          if (!(ok = mbar_wait(&B->s_loaded[yp % 3], (yp / 3) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t vb = sV + (yp % 2) * C::TILE, buf = (yp % 3) * 128;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
-            mma_ss(tbase + buf, sdesc_sw128(sdO + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024), IDESC_S, kk > 0);
+            mma_ts(tbase + C::TM_ACC, tbase + bq * 128 + kk * 8 + (kk >= 4 ? 32 : 0), sdesc_add(db, kk * 2048),
+                   IDESC_ACC, !first || kk > 0);
+          mma_commit(&B->k_empty[(t - 2) % C::KS]);
+          if (fq & LAST) {
+            mma_commit(&B->acc_full);
+            ++itq;
           }
-          mma_commit(&B->dp_full[yp % 3]);
-          mma_commit(&B->v_empty[yp % 2]);
-          if (cp.x == cp.n - 1) mma_commit(&B->do_empty);
-          cp.next(p, n_items);
-          ++yp;
         }
+        if (has_dp && dq_first) {
+          uint64_t* const bars[2] = {&B->v_full, &B->s_loaded[bp]};
+          const uint32_t par[2] = {(t - 1) & 1, ((t - 1) / 3) & 1};
+          if (!(ok = mbar_wait_all(bars, par, abort_flag))) break;
+          tc_fence_after();
+          issue_dp();
+        }
+        fq = fp;
+        fp = fs;
       }
       mma_commit(&B->mma_done);
       mbar_wait_drain(&B->mma_done, 0, 200000000);
@@ -1101,30 +1098,25 @@ __global__ void __launch_bounds__(320, 1)
     const int r = threadIdx.x & 127;
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + 64 * hw;
     const uint2* masks = reinterpret_cast<const uint2*>(p.masks);
-    uint32_t y = 0, it = 0;
+    uint32_t y = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const int tile = p.order[w / p.Hq], h = w % p.Hq;
-      const int e0 = p.ptr[tile], n = p.ptr[tile + 1] - e0;
-      const int q = tile * 128 + r;
+    for (int k = cta.x; k < cta.y && ok; ++k) {
+      const int4 itm = p.dq_items[k];  // q tile, head, first entry, blocks
+      const int h = itm.y, e0 = itm.z, n = itm.w;
+      const int q = itm.x * 128 + r;
       __nv_bfloat16* orow = p.out0 + ((size_t)q * p.Hq + h) * D + hw * (D / 2);  // this warpgroup's columns
-      if (n == 0) {
-        if (q < p.T) {
-          uint4 z = make_uint4(0, 0, 0, 0);
-          for (int c = 0; c < D / 16; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-        }
-        continue;
-      }
       const float l2 = p.lse2[(size_t)h * p.Tpad + q];
       const float dl = p.delta[(size_t)h * p.Tpad + q];
       int slot = p.pidx[e0];
       uint2 mk = slot >= 0 ? masks[(size_t)slot * 256 + 2 * r + hw] : make_uint2(0xffffffffu, 0xffffffffu);
       for (int x = 0; x < n; ++x, ++y) {
+        const bool full = slot < 0;  // uniform over the CTA
         // the next block's mask, a block ahead
         uint2 mk_next = make_uint2(0xffffffffu, 0xffffffffu);
+        int slot_next = -1;
         if (x + 1 < n) {
-          const int sn = p.pidx[e0 + x + 1];
-          if (sn >= 0) mk_next = masks[(size_t)sn * 256 + 2 * r + hw];
+          slot_next = p.pidx[e0 + x + 1];
+          if (slot_next >= 0) mk_next = masks[(size_t)slot_next * 256 + 2 * r + hw];
         }
         const uint32_t b = y % 3, ph = (y / 3) & 1, col = b * 128;
         ok = mbar_wait(&B->s_full[b], ph, abort_flag);
@@ -1139,11 +1131,16 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&B->s_loaded[b]);  // dP may now overwrite S
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const uint32_t word = c < 32 ? mk.x : mk.y;
-          const float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2));
-          sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
+          for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2)));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const uint32_t word = c < 32 ? mk.x : mk.y;
+            const float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2));
+            sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
+          }
         }
         ok = mbar_wait(&B->dp_full[b], ph, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -1167,9 +1164,10 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         mbar_arrive(&B->p_full[b]);
         mk = mk_next;
+        slot = slot_next;
       }
       if (!ok) break;
-      ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
+      ok = mbar_wait(&B->acc_full, (uint32_t)(k - cta.x) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -1185,7 +1183,6 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive(&B->acc_free);
-      ++it;
     }
     if (!ok) *abort_flag = 1;
   }
@@ -1312,6 +1309,83 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
   return 0;
 }
 
+// Work items of the pipelined q-major kernel, cached on the map: every
+// (q tile, head) with at least one kv block, packed longest first onto the
+// grid's CTAs by LPT list scheduling and stored grouped by CTA, plus the q
+// tiles with no kv block at all (their dQ rows are zero).
+int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, cudaStream_t s) {
+  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
+  std::lock_guard<std::mutex> lk(g_items_mu);
+  if (bm->dq_items && bm->dq_hq == Hq && bm->dq_sms == sms) return 0;
+  const int nq = bm->nq;
+  std::vector<int4> items;
+  std::vector<int> empty;
+  int e0 = 0;
+  for (int t = 0; t < nq; ++t) {
+    const int n = bm->h_row_cnt[t];
+    if (n == 0) empty.push_back(t);
+    for (int h = 0; h < Hq && n > 0; ++h) items.push_back(make_int4(t, h, e0, n));
+    e0 += n;
+  }
+  std::stable_sort(items.begin(), items.end(), [](const int4& a, const int4& b) { return a.w > b.w; });
+  const int grid = std::max(1, std::min<int>(sms, (int)items.size()));
+  std::vector<std::vector<int>> bins(grid);
+  std::vector<long long> blocks(grid, 0);
+  {
+    using Load = std::pair<long long, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int b = 0; b < grid; ++b) heap.push(Load(0, b));
+    for (int i = 0; i < (int)items.size(); ++i) {
+      Load l = heap.top();
+      heap.pop();
+      bins[l.second].push_back(i);
+      blocks[l.second] += items[i].w;
+      l.first += items[i].w + 2;  // about two blocks of fixed work per item
+      heap.push(l);
+    }
+  }
+  std::vector<int4> packed, cta(grid);
+  packed.reserve(items.size());
+  for (int b = 0; b < grid; ++b) {
+    cta[b].x = (int)packed.size();
+    for (int i : bins[b]) packed.push_back(items[i]);
+    cta[b].y = (int)packed.size();
+    if (blocks[b] > INT32_MAX) {
+      set_error("backward kernel: too many kv blocks for one CTA");
+      return 1;
+    }
+    cta[b].z = (int)blocks[b];
+    cta[b].w = 0;
+  }
+  pool_free(bm->dq_mem, s);
+  bm->dq_mem = nullptr;
+  bm->dq_items = nullptr;
+  std::free(bm->h_dq_empty);
+  bm->h_dq_empty = nullptr;
+  const size_t bi = sizeof(int4) * std::max<size_t>(packed.size(), 1), bc = sizeof(int4) * grid;
+  int rc = pool_alloc(&bm->dq_mem, bi + bc, bm->device, s);
+  if (rc) return rc;
+  bm->dq_items = bm->dq_mem;
+  bm->dq_cta = static_cast<char*>(bm->dq_mem) + bi;
+  if (!packed.empty() && (rc = upload(bm->dq_items, packed.data(), sizeof(int4) * packed.size(), bm->device, s)))
+    return rc;
+  if ((rc = upload(bm->dq_cta, cta.data(), bc, bm->device, s))) return rc;
+  if (!empty.empty()) {
+    bm->h_dq_empty = static_cast<int*>(std::malloc(sizeof(int) * empty.size()));
+    if (!bm->h_dq_empty) {
+      set_error("out of host memory");
+      return 4;
+    }
+    std::copy(empty.begin(), empty.end(), bm->h_dq_empty);
+  }
+  bm->dq_n_empty = (int)empty.size();
+  bm->dq_hq = Hq;
+  bm->dq_sms = sms;
+  bm->dq_grid = grid;
+  bm->dq_n_items = (int)packed.size();
+  return 0;
+}
+
 template <int D>
 int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
                int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
@@ -1321,7 +1395,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   int rc = reserve_smem(k_bwd_dkdv<D>, DkdvL<D>::BYTES, dev, set_dkdv);
   if (!rc) {
     if constexpr (D == 128)
-      rc = reserve_smem(k_bwd_dq3<D>, Dq3L<D>::BYTES, dev, set_dq);
+      rc = reserve_smem(k_bwd_dq_pipe<D>, DqpL<D>::BYTES, dev, set_dq);
     else
       rc = reserve_smem(k_bwd_dq<D>, DqL<D>::BYTES, dev, set_dq);
   }
@@ -1395,7 +1469,19 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   if (items > 0) {
     ProfScope ps(s, "bwd_dq");
     if constexpr (D == 128) {
-      k_bwd_dq3<D><<<items < sms ? items : sms, 320, Dq3L<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+      if ((rc = prepare_dq_items(bm, Hq, sms, s))) return rc;
+      for (int i = 0; i < bm->dq_n_empty; ++i) {  // q tiles that attend to nothing
+        const int t0 = bm->h_dq_empty[i] * 128, t1 = std::min(T, t0 + 128);
+        if (cudaMemsetAsync(static_cast<__nv_bfloat16*>(dQ) + (size_t)t0 * Hq * D, 0,
+                            sizeof(__nv_bfloat16) * (size_t)(t1 - t0) * Hq * D, s) != cudaSuccess) {
+          set_error("backward: cudaMemsetAsync failed");
+          return 3;
+        }
+      }
+      p.dq_items = static_cast<const int4*>(bm->dq_items);
+      p.dq_cta = static_cast<const int4*>(bm->dq_cta);
+      if (bm->dq_n_items > 0)
+        k_bwd_dq_pipe<D><<<bm->dq_grid, DqpCfg<D>::THREADS, DqpL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
     } else {
       k_bwd_dq<D><<<items < sms ? items : sms, 320, DqL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
     }

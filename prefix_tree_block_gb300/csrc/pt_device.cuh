@@ -133,6 +133,24 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// Waits for up to N barrier phases at once.  The phases are first tested
+// together (their latencies overlap); only if one is still pending does the
+// thread fall back to bounded waits on each.  Entries with a null barrier
+// are skipped.
+template <int N>
+__device__ __forceinline__ bool mbar_wait_all(uint64_t* const (&bars)[N], const uint32_t (&par)[N],
+                                              volatile int* abort_flag) {
+  bool ready = true;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (bars[i]) ready &= mbar_test(bars[i], par[i]);
+  if (ready) return true;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (bars[i] && !mbar_wait(bars[i], par[i], abort_flag)) return false;
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------

@@ -66,6 +66,12 @@ struct pt_blockmap {
   void* bwd_items;   // DkdvItem[bwd_n_items] (device), grouped by the CTA that runs them
   void* bwd_cta;     // int[bwd_grid + 1]: CTA b runs items [bwd_cta[b], bwd_cta[b + 1])
   void* bwd_splits;  // int4[bwd_n_splits]: kv block, kv head, first slot, slot count (device)
+  // work items of the pipelined q-major (dQ) kernel, cached for one head count
+  void* dq_mem;
+  int dq_hq, dq_sms, dq_grid, dq_n_items, dq_n_empty;
+  void* dq_items;   // int4[dq_n_items]: q tile, head, first list entry, kv blocks; grouped by CTA
+  void* dq_cta;     // int4[dq_grid]: first item, end item, kv blocks of the CTA
+  int* h_dq_empty;  // q tiles without any kv block (their dQ rows are zero)
 };
 
 // Work item of the kv-major backward kernel: steps [x0, x1) of the (kv block,
