@@ -254,6 +254,17 @@ uint64_t pt_launch_count(void);
  * pages have no counterpart. */
 pt_status pt_debug_wait_timeout(cudaStream_t stream);
 
+/* Accuracy check of the kernels' two exp2 paths: y[i] = 2^x[i] for i < n,
+ * computed with the MUFU instruction (method 0) or with the FMA-pipe
+ * polynomial (method 1: Cody-Waite range reduction and a degree-3 minimax
+ * polynomial, max relative error 7.8e-5 on [-125, 0], a value in
+ * [0, 2^-124] below -125, including -inf) that the softmax loops use for a
+ * fixed share of the columns.
+ * x and y are device pointers to n floats, owned by the caller.  Returns
+ * PT_ERR_INVALID_ARG for n < 0, NULL pointers with n > 0 or another method.
+ * Meant for tests; the pages have no counterpart. */
+pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cudaStream_t stream);
+
 /* Optional per-kernel timing, for benchmarks and profiling.  While enabled,
  * each kernel launch is bracketed by two CUDA events on its stream (a few
  * microseconds of overhead per launch); disabled (the default) costs one

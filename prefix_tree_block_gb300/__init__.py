@@ -62,6 +62,7 @@ def load_library(path: Optional[str] = None):
             "pt_attn_bwd": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
             "pt_sync_status": [vp],
             "pt_debug_wait_timeout": [vp],
+            "pt_debug_exp2": [vp, vp, i64, i32, vp],
             "pt_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp,
                                     vp],
         }
@@ -291,6 +292,19 @@ def attn_bwd_noalloc(dO, Q, K, V, O, LSE, bm: BlockMap, scale: float = 0.0, dQ=N
 def sync_status(stream=None):
     """Synchronise and raise PTError if an in-kernel wait timed out."""
     _check(load_library().pt_sync_status(ctypes.c_void_p(_stream(stream))))
+
+
+def debug_exp2(x, method: int):
+    """2^x on the device with the MUFU instruction (method 0) or the kernels'
+    FMA-pipe polynomial (method 1); x is a contiguous float32 CUDA tensor."""
+    import torch
+
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y = torch.empty_like(x)
+    _check(load_library().pt_debug_exp2(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), x.numel(),
+                                        method, ctypes.c_void_p(_stream(None))))
+    return y
 
 
 def launch_count() -> int:

@@ -380,6 +380,14 @@ uint64_t pt_launch_count(void) { return pt::launches(); }
 
 pt_status pt_debug_wait_timeout(cudaStream_t stream) { return as_status(pt::wait_timeout_probe(stream)); }
 
+pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !y)) || (method != 0 && method != 1)) {
+    set_error("pt_debug_exp2: bad arguments (n=%lld, method=%d)", (long long)n, method);
+    return PT_ERR_INVALID_ARG;
+  }
+  return as_status(pt::exp2_probe(x, y, n, method, stream));
+}
+
 void pt_profile_enable(int on) { pt::g_prof_on.store(on != 0); }
 
 pt_status pt_profile_read(const char* kernel, int64_t* launches, double* total_ms) {

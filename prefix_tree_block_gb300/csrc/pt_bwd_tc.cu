@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int k = 0; k < 4; ++k) {
               const int c = c4 * 4 + k;
               const uint32_t word = c < 32 ? mk.x : mk.y;
-              float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]));
+              float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
               pv[k] = ((word >> (c & 31)) & 1u) ? pr : 0.f;
               dsv[k] = pv[k] * (__uint_as_float(dr[c]) - da[k]);
             }
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int k = 0; k < 4; ++k) {
               const int c = c4 * 4 + k;
               const uint32_t word = c < 32 ? mk.x : mk.y;
-              float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]));
+              float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
               sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
             }
           }
@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const uint32_t word = c < 32 ? mk.x : mk.y;
-          float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2));
+          float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
           pr = ((word >> (c & 31)) & 1u) ? pr : 0.f;
           dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - dl));
         }
@@ -1133,12 +1133,12 @@ __global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
         mbar_arrive(&B->s_loaded[b]);  // dP may now overwrite S
         if (full) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2)));
+          for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c));
         } else {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const uint32_t word = c < 32 ? mk.x : mk.y;
-            const float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2));
+            const float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
             sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
           }
         }

@@ -284,6 +284,33 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipes instead of the MUFU unit, which the softmax of a
+// 128-column tile otherwise saturates (one warp-wide ex2 per 8 cycles per
+// SM sub-partition).  Cody-Waite range reduction x = n + f, n = round(x),
+// f in [-1/2, 1/2], and a degree-3 minimax polynomial for 2^f (coefficients
+// from exp2_poly_fit.py); 2^n is added into the exponent field.  Adding
+// 1.5 * 2^23 rounds x to an integer held in the low mantissa bits, so the
+// shift of that float's bit pattern by 23 is n in the exponent position.
+// x is clamped to -126 first, so the exponent field never wraps: arguments
+// below -125 (masked entries are -inf) give at most 2^-124 instead of 0.
+// Max relative error 7.8e-5 for x in [-125, 0]; x must not exceed 127.
+__device__ __forceinline__ float ex2_poly(float x) {
+  x = fmaxf(x, -126.f);
+  const float t = __fadd_rn(x, 12582912.f);
+  const float f = __fsub_rn(x, __fsub_rn(t, 12582912.f));
+  const float p = fmaf(fmaf(fmaf(5.517132208e-02f, f, 2.426105440e-01f), f, 6.932609677e-01f), f, 9.999281168e-01f);
+  return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
+}
+
+// Which columns of a softmax row take ex2_poly: kPolyEighths of every eight
+// (a compile-time split, so the choice costs nothing at run time).  Zero on
+// this part: with 2/8, 3/8 and 4/8 of the exponentials on the FMA pipes the
+// forward and both backward kernels got slower at head_dim 64 and 128 (the
+// softmax loops are bound by instruction issue and latency, not by MUFU).
+constexpr int kPolyEighths = 0;
+__device__ __forceinline__ constexpr bool poly_col(int c) { return (c & 7) < kPolyEighths; }
+__device__ __forceinline__ float ex2_mix(float x, int c) { return poly_col(c) ? ex2_poly(x) : ex2(x); }
+
 // Pack two floats to bf16x2 (round to nearest even): `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;

@@ -434,8 +434,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         for (int k = 0; k < 8; ++k) r8[k] = 0.f;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -ref));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -ref));
+          const float p0 = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -ref), c);
+          const float p1 = ex2_mix(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -ref), c + 1);
           r8[(c >> 1) & 7] += p0 + p1;
           sr[c >> 1] = pack_bf16(p0, p1);
         }
@@ -563,7 +563,27 @@ __global__ void k_wait_timeout_probe() {
     mbar_wait(&bar, 0, &abort_flag);
   }
 }
+
+// y = 2^x with the MUFU instruction (method 0) or the FMA-pipe polynomial
+// (method 1) the softmax loops can mix, for tests of the polynomial's accuracy.
+__global__ void k_exp2_probe(const float* __restrict__ x, float* __restrict__ y, long long n, int method) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    y[i] = method == 0 ? ex2(x[i]) : ex2_poly(x[i]);
+}
 }  // namespace
+
+int exp2_probe(const float* x, float* y, long long n, int method, cudaStream_t s) {
+  if (n <= 0) return 0;
+  const long long blocks = (n + 255) / 256;
+  k_exp2_probe<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(x, y, n, method);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("exp2 probe launch failed: %s", cudaGetErrorString(e));
+    return 3;
+  }
+  return 0;
+}
 
 int wait_timeout_probe(cudaStream_t s) {
   k_wait_timeout_probe<<<1, 32, 0, s>>>();

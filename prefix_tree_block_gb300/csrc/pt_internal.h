@@ -129,6 +129,7 @@ int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const vo
            float* lse2, float* partial, size_t partial_bytes, cudaStream_t s);
 bool bwd_tc_supported(int D);
 int wait_timeout_probe(cudaStream_t s);
+int exp2_probe(const float* x, float* y, long long n, int method, cudaStream_t s);
 
 // CUDA-core kernels (pt_simt.cu), fp32 or bf16 storage with fp32 math.
 int fwd_simt(bool bf16, const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
