@@ -50,6 +50,17 @@ def useful_pairs(st) -> int:
     return total
 
 
+# DRAM bytes (read + write) per launch of the tensor-core kernels, from one
+# `ncu --set full` capture of the current kernels on each workload: see
+# profiles/kernels_grpo_batch_workload2.md and
+# profiles/kernels_long_prompt_grpo_workload3.md.  A kernel changed since its
+# capture must be removed from this table (its traffic is then reported null).
+MEASURED_TRAFFIC = {
+    (2, "fwd_tc"): 35.2e6, (2, "bwd_dkdv"): 66.97e6, (2, "bwd_dq"): 65.63e6,
+    (3, "fwd_tc"): 953.9e6, (3, "bwd_dkdv"): 3011.5e6, (3, "bwd_dq"): 1196.4e6,
+}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -275,7 +286,8 @@ def main():
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
     kernels = {}
-    for name in ("blockmap_classify", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dq", "bwd_simt"):
+    for name in ("blockmap_classify", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dkdv_finalize", "bwd_dq",
+                 "bwd_simt"):
         n, ms = pt.profile_read(name)
         if n:
             kernels[name] = {"launches": n, "ms_per_launch": ms / n}
@@ -294,7 +306,8 @@ def main():
         dom = max(tc, key=lambda k: tc[k]["ms_per_launch"])
         ach = per_launch_flops[dom] / (tc[dom]["ms_per_launch"] * 1e-3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": ach / peak_tf, "traffic": None, "peak_source": f"{peak_src} bf16 burst"}
+                    "frac": ach / peak_tf, "traffic": MEASURED_TRAFFIC.get((args.workload, dom)),
+                    "peak_source": f"{peak_src} bf16 burst"}
 
     # ---- dense-masked comparison (same kernels, every tile partial) ---------
     dense = None
