@@ -63,6 +63,7 @@ def load_library(path: Optional[str] = None):
             "pt_sync_status": [vp],
             "pt_debug_wait_timeout": [vp],
             "pt_debug_exp2": [vp, vp, i64, i32, vp],
+            "pt_blockmap_prepare_bwd": [vp, i32, i32, i32, vp],
             "pt_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp,
                                     vp],
         }
@@ -123,6 +124,10 @@ class BlockMap:
     @property
     def handle(self):
         return self._h
+
+    def prepare_bwd(self, Hq: int, Hkv: int, D: int, stream=None):
+        """Build the work lists attn_bwd_noalloc needs for this head layout."""
+        _check(load_library().pt_blockmap_prepare_bwd(self._h, Hq, Hkv, D, ctypes.c_void_p(_stream(stream))))
 
     def dense(self, stream=None) -> "BlockMap":
         """The same tree with every tile marked partial (no skipping)."""

@@ -337,7 +337,7 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
   if (dtype == PT_BF16) {
     if (use_tensor_cores(dtype, D, bm) && pt::bwd_tc_supported(D))
       return as_status(pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, lse2, partial,
-                                  partial_bytes, stream));
+                                  partial_bytes, true, stream));
     if (D % 8 != 0) {
       set_error("pt_attn_bwd: bf16 needs head_dim %% 8 == 0 (got %d)", D);
       return PT_ERR_UNSUPPORTED;
@@ -379,6 +379,14 @@ const char* pt_last_error(void) { return pt::g_err_ptr(); }
 uint64_t pt_launch_count(void) { return pt::launches(); }
 
 pt_status pt_debug_wait_timeout(cudaStream_t stream) { return as_status(pt::wait_timeout_probe(stream)); }
+
+pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv, int32_t D, cudaStream_t stream) {
+  if (!bm || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || D > 256) {
+    set_error("pt_blockmap_prepare_bwd: bad map or head layout (Hq=%d, Hkv=%d, D=%d)", Hq, Hkv, D);
+    return PT_ERR_INVALID_ARG;
+  }
+  return as_status(pt::prepare_bwd_noalloc(bm, Hq, Hkv, D, stream));
+}
 
 pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cudaStream_t stream) {
   if (n < 0 || (n > 0 && (!x || !y)) || (method != 0 && method != 1)) {

@@ -1216,12 +1216,18 @@ int reserve_smem(K kernel, int bytes, int dev, int* flags) {
 // with the least work so far (LPT list scheduling), and stored grouped by CTA.
 std::mutex g_items_mu;
 
-int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, cudaStream_t s) {
+int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, bool allow_build,
+                       cudaStream_t s) {
   pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
   std::lock_guard<std::mutex> lk(g_items_mu);
   if (bm->bwd_items && bm->bwd_g == g && bm->bwd_hkv == Hkv && bm->bwd_max_slots == max_slots &&
       bm->bwd_sms == sms)
     return 0;
+  if (!allow_build) {
+    set_error("block map's backward work lists are not prepared for this head layout "
+              "(call pt_blockmap_prepare_bwd first)");
+    return 1;
+  }
   const int nk = bm->nk;
   long long total = 0;
   for (int j = 0; j < nk; ++j) total += (long long)g * bm->h_col_cnt[j] * Hkv;
@@ -1313,10 +1319,14 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
 // (q tile, head) with at least one kv block, packed longest first onto the
 // grid's CTAs by LPT list scheduling and stored grouped by CTA, plus the q
 // tiles with no kv block at all (their dQ rows are zero).
-int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, cudaStream_t s) {
+int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, cudaStream_t s) {
   pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
   std::lock_guard<std::mutex> lk(g_items_mu);
   if (bm->dq_items && bm->dq_hq == Hq && bm->dq_sms == sms) return 0;
+  if (!allow_build) {
+    set_error("block map's dQ work lists are not prepared for this head count (call pt_blockmap_prepare_bwd first)");
+    return 1;
+  }
   const int nq = bm->nq;
   std::vector<int4> items;
   std::vector<int> empty;
@@ -1389,7 +1399,7 @@ int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, cudaStream_t s) {
 template <int D>
 int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
                int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
-               float* lse2, float* partial, size_t partial_bytes, cudaStream_t s) {
+               float* lse2, float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s) {
   static int set_dkdv[64] = {0}, set_dq[64] = {0};
   const int dev = bm->device;
   int rc = reserve_smem(k_bwd_dkdv<D>, DkdvL<D>::BYTES, dev, set_dkdv);
@@ -1406,7 +1416,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   }
   const int sms = num_sms(dev);
   const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, s))) return rc;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s))) return rc;
   const int Tpad = bm->nq * 128;
   {
     const long long threads = (long long)Hq * Tpad * (D / 8);
@@ -1469,7 +1479,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   if (items > 0) {
     ProfScope ps(s, "bwd_dq");
     if constexpr (D == 128) {
-      if ((rc = prepare_dq_items(bm, Hq, sms, s))) return rc;
+      if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s))) return rc;
       for (int i = 0; i < bm->dq_n_empty; ++i) {  // q tiles that attend to nothing
         const int t0 = bm->h_dq_empty[i] * 128, t1 = std::min(T, t0 + 128);
         if (cudaMemsetAsync(static_cast<__nv_bfloat16*>(dQ) + (size_t)t0 * Hq * D, 0,
@@ -1500,16 +1510,24 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
 
 bool bwd_tc_supported(int D) { return D == 64 || D == 128; }
 
+int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStream_t s) {
+  if (!bwd_tc_supported(D) || bm->BM != 128 || bm->BN != 128) return 0;  // those paths keep no lists
+  const int sms = num_sms(bm->device);
+  int rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, true, s);
+  if (!rc && D == 128) rc = prepare_dq_items(bm, Hq, sms, true, s);
+  return rc;
+}
+
 int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T, int Hq,
            int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta, float* lse2,
-           float* partial, size_t partial_bytes, cudaStream_t s) {
+           float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s) {
   switch (D) {
     case 64:
       return launch_bwd<64>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial,
-                            partial_bytes, s);
+                            partial_bytes, allow_build, s);
     case 128:
       return launch_bwd<128>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial,
-                             partial_bytes, s);
+                             partial_bytes, allow_build, s);
     default: set_error("tensor-core backward: head_dim %d not built", D); return 2;
   }
 }

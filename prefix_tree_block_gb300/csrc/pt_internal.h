@@ -124,9 +124,13 @@ void free_map(pt_blockmap* bm);
 // Tensor-core bf16 kernels (pt_fwd_tc.cu, pt_bwd_tc.cu).
 int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
            const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s);
+// allow_build: whether the call may build the map's work lists (from the
+// library's pool) when they do not match the head layout yet.
 int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
            int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
-           float* lse2, float* partial, size_t partial_bytes, cudaStream_t s);
+           float* lse2, float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s);
+// Builds the work lists the allocation-free backward needs for a head layout.
+int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStream_t s);
 bool bwd_tc_supported(int D);
 int wait_timeout_probe(cudaStream_t s);
 int exp2_probe(const float* x, float* y, long long n, int method, cudaStream_t s);

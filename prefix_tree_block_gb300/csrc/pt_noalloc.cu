@@ -101,7 +101,7 @@ extern "C" pt_status pt_attn_bwd_noalloc(const void* dO, const void* Q, const vo
   // the previous call's contents never need clearing.
   int rc;
   if (dtype == PT_BF16 && bm->BM == 128 && bm->BN == 128 && pt::bwd_tc_supported(D))
-    rc = pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, lse2, nullptr, 0, stream);
+    rc = pt::bwd_tc(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, lse2, nullptr, 0, false, stream);
   else if (dtype == PT_BF16 && D % 8 != 0) {
     pt::set_error("pt_attn_bwd_noalloc: bf16 needs head_dim %% 8 == 0 (got %d)", D);
     return PT_ERR_UNSUPPORTED;

@@ -29,14 +29,14 @@ def lib():
     return pt.load_library()
 
 
-def _noalloc(lib, dO, Q, K, V, O, LSE, bm, dtype_code):
+def _noalloc(lib, dO, Q, K, V, O, LSE, bm, dtype_code, expect=pt.PT_OK):
     T, Hq, D = Q.shape
     Hkv = K.shape[1]
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     rc = lib.pt_attn_bwd_noalloc(dO.data_ptr(), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
                                  LSE.data_ptr(), dtype_code, T, Hq, Hkv, D, 0.0, bm.handle, dQ.data_ptr(),
                                  dK.data_ptr(), dV.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    assert rc == pt.PT_OK, lib.pt_last_error()
+    assert rc == expect, lib.pt_last_error()
     torch.cuda.synchronize()
     return dQ, dK, dV
 
@@ -50,6 +50,11 @@ def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
     O, LSE = pt.attn_fwd(Q, K, V, bm)
     ref = [x.float().cpu().numpy() for x in pt.attn_bwd(dO, Q, K, V, O, LSE, bm)]
     code = pt.PT_BF16 if dtype == "bf16" else pt.PT_F32
+    if dtype == "bf16":  # the tensor-core path reads per-map work lists: refused until prepared
+        _noalloc(lib, dO, Q, K, V, O, LSE, bm, code, expect=pt.PT_ERR_INVALID_ARG)
+        assert b"pt_blockmap_prepare_bwd" in lib.pt_last_error()
+    bm.prepare_bwd(Q.shape[1], K.shape[1], D)
+    bm.prepare_bwd(Q.shape[1], K.shape[1], D)  # idempotent
     for _ in range(2):
         got = [x.float().cpu().numpy() for x in _noalloc(lib, dO, Q, K, V, O, LSE, bm, code)]
         for g, r in zip(got, ref):
