@@ -136,9 +136,12 @@ struct BwdParams {
 template <int D>
 __global__ void k_dkdv_finalize(const int4* __restrict__ splits, const float* __restrict__ partial, int T, int Hkv,
                                 __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV) {
+  // block (x, y): split column x, rows [8y, 8y + 8) of its 128; one float4 of
+  // 2D columns per thread and row pass
   const int4 sp = splits[blockIdx.x];  // kv block, kv head, first slot, slot count
-  for (int idx = threadIdx.x; idx < 128 * 2 * D / 4; idx += blockDim.x) {
-    const int r = idx / (2 * D / 4), c = (idx % (2 * D / 4)) * 4;
+  constexpr int Q4 = 2 * D / 4;        // float4 per row
+  for (int idx = threadIdx.x; idx < 8 * Q4; idx += blockDim.x) {
+    const int r = blockIdx.y * 8 + idx / Q4, c = (idx % Q4) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < sp.w; ++k) {
       const float4 v = *reinterpret_cast<const float4*>(partial + ((size_t)(sp.z + k) * 128 + r) * (2 * D) + c);
@@ -1458,7 +1461,8 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   }
   if (bm->bwd_n_splits > 0) {
     ProfScope ps(s, "bwd_dkdv_finalize");
-    k_dkdv_finalize<D><<<bm->bwd_n_splits, 256, 0, s>>>(static_cast<const int4*>(bm->bwd_splits), partial, T, Hkv,
+    k_dkdv_finalize<D><<<dim3(bm->bwd_n_splits, 16), 256, 0, s>>>(static_cast<const int4*>(bm->bwd_splits), partial,
+                                                                   T, Hkv,
                                                         static_cast<__nv_bfloat16*>(dK),
                                                         static_cast<__nv_bfloat16*>(dV));
     ++launches;

@@ -49,22 +49,29 @@ struct FwdCfg {
   static constexpr int PANEL = 128 * 128;  // bytes: 128 rows x 128 B
   static constexpr int TILE = NP * PANEL;
   static constexpr int SB = NH == 1 ? 2 : 1;  // S buffers per head
+  // With TMEM to spare (head_dim 64, two heads) P goes to its own columns, so
+  // S of the next block can be computed as soon as the softmax has loaded S,
+  // and the next item's Q tiles load while this item runs.
+  static constexpr bool OVL = D == 64 && NH == 2;
+  static constexpr int QB = OVL ? 2 : 1;  // Q buffers
   static constexpr int KS = D == 64 ? 4 : (D == 128 ? (NH == 2 ? 2 : 3) : 1);
   static constexpr int VS = D == 64 ? 4 : (D == 128 ? 2 : 1);
   static constexpr int MASKB = 128 * 16;  // one partial tile's row masks
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + NH * TILE;
+  static constexpr int OFF_K = OFF_Q + QB * NH * TILE;
   static constexpr int OFF_V = OFF_K + KS * TILE;
   static constexpr int OFF_MASK = OFF_V + VS * TILE;
   static constexpr int OFF_META = OFF_MASK + VS * MASKB;
   static constexpr int OFF_BAR = OFF_META + 16 * ((VS * 4 + 15) / 16);
-  // q_full q_empty k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
+  // q_full[QB] q_empty[QB] k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
   // s_full[NH*SB] p_full[NH*SB] o_full[NH] o_free[NH] mma_done
-  static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 * NH * SB + 2 * NH + 1;
+  // (OVL) s_free[NH] p_free[NH]
+  static constexpr int NBAR = 2 * QB + 2 * KS + 2 * VS + 2 * NH * SB + 2 * NH + 1 + (OVL ? 2 * NH : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int TM_S = 0;                 // S(h, b) at (h * SB + b) * 128
-  static constexpr int TM_O = NH * SB * 128;     // O(h) at TM_O + h * D
+  static constexpr int TM_S = 0;                            // S(h, b) at (h * SB + b) * 128
+  static constexpr int TM_P = NH * SB * 128;                // (OVL) packed P(h) at TM_P + h * 64
+  static constexpr int TM_O = TM_P + (OVL ? NH * 64 : 0);  // O(h) at TM_O + h * D
   static constexpr int THREADS = NH * 128 + 64;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TM_O + NH * D <= 512, "TMEM budget");
@@ -117,9 +124,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
+  uint64_t* q_full = bars + 0;              // [QB]
+  uint64_t* q_empty = q_full + C::QB;       // [QB]
+  uint64_t* k_full = q_empty + C::QB;
   uint64_t* k_empty = k_full + C::KS;
   uint64_t* v_full = k_empty + C::KS;
   uint64_t* v_empty = v_full + C::VS;
@@ -128,6 +135,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   uint64_t* o_full = p_full + NH * C::SB;   // [NH]
   uint64_t* o_free = o_full + NH;           // [NH]
   uint64_t* mma_done = o_free + NH;
+  uint64_t* s_free = mma_done + 1;          // [NH] (OVL) S(h) loaded by the softmax
+  uint64_t* p_free = s_free + NH;           // [NH] (OVL) PV(h) done reading P(h)
   int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -137,8 +146,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   constexpr int PRODUCER = NH * 4, ISSUER = NH * 4 + 1;
 
   if (threadIdx.x == PRODUCER * 32) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int b = 0; b < C::QB; ++b) {
+      mbar_init(q_full + b, 1);
+      mbar_init(q_empty + b, 1);
+    }
+    if (C::OVL)
+      for (int h = 0; h < NH; ++h) {
+        mbar_init(s_free + h, 128);
+        mbar_init(p_free + h, 1);
+      }
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -181,12 +197,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         decode_item<NH>(p, w, tile, h0, nh);
         const int e0 = p.q_ptr[tile], e1 = p.q_ptr[tile + 1];
         if (e1 == e0) continue;
-        if (it > 0 && !(ok = mbar_wait(q_empty, (it - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(q_full, nh * C::TILE);
+        const uint32_t qb = it % C::QB;
+        q_issued = false;  // this item's Q not issued yet
+        if (it >= C::QB && !(ok = mbar_wait(q_empty + qb, (it / C::QB - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(q_full + qb, nh * C::TILE);
         for (int h = 0; h < nh; ++h)
 #pragma unroll
           for (int pn = 0; pn < C::NP; ++pn)
-            tma_load_3d(smem + C::OFF_Q + h * C::TILE + pn * C::PANEL, &mQ, q_full, pn * 64, h0 + h, tile * C::BM);
+            tma_load_3d(smem + C::OFF_Q + (qb * NH + h) * C::TILE + pn * C::PANEL, &mQ, q_full + qb, pn * 64, h0 + h,
+                        tile * C::BM);
         q_issued = true;
         const int hk = h0 / (p.Hq / p.Hkv);
         for (int e = e0; e < e1; ++e) {
@@ -218,7 +237,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       }
       if (!ok) {
         const long long lim = 20000000;
-        if (q_issued) mbar_wait_drain(q_full, (it)&1, lim);
+        // Q loads issued: `it` items completed, plus this one if its Q went out
+        const uint32_t nql = it + (q_issued ? 1 : 0);
+        for (uint32_t b = 0; b < C::QB && b < nql; ++b) {
+          const uint32_t last = nql - 1 - ((nql - 1 - b) % C::QB);
+          mbar_wait_drain(q_full + b, (last / C::QB) & 1, lim);
+        }
         for (uint32_t s = 0; s < C::KS && s < kc; ++s) {
           uint32_t last = kc - 1 - ((kc - 1 - s) % C::KS);
           mbar_wait_drain(k_full + s, (last / C::KS) & 1, lim);
@@ -244,10 +268,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       for (int h = 0; h < NH; ++h) sc[h] = itv[h] = 0;
       bool ok = true;
 
+      uint32_t qb = 0;  // Q buffer of the current item
       auto issue_s = [&](int h, uint32_t u, uint32_t ks) {
         const uint32_t b = u % C::SB;
         const uint32_t d_tmem = tbase + C::TM_S + (h * C::SB + b) * 128;
-        const uint32_t qa = sQ + h * C::TILE, ka = sK + ks * C::TILE;
+        const uint32_t qa = sQ + (qb * NH + h) * C::TILE, ka = sK + ks * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::PANEL + (kk & 3) * 32;
@@ -257,7 +282,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       };
       auto issue_pv = [&](int h, uint32_t u, uint32_t vs, bool first) {
         const uint32_t b = u % C::SB;
-        const uint32_t a_tmem = tbase + C::TM_S + (h * C::SB + b) * 128;
+        // P packed in place over S, or in its own columns
+        const uint32_t a_tmem = tbase + (C::OVL ? C::TM_P + h * 64 : C::TM_S + (h * C::SB + b) * 128);
         const uint32_t va = sV + vs * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
@@ -270,7 +296,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         decode_item<NH>(p, w, tile, h0, nh);
         const int n = p.q_ptr[tile + 1] - p.q_ptr[tile];
         if (n == 0) continue;
-        if (!(ok = mbar_wait(q_full, it & 1, abort_flag))) break;
+        qb = it % C::QB;
+        if (!(ok = mbar_wait(q_full + qb, (it / C::QB) & 1, abort_flag))) break;
         tc_fence_after();
         for (int jj = 0; jj <= n && ok; ++jj) {
           const uint32_t ks = (kc + jj) % C::KS;
@@ -278,11 +305,42 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
             if (!(ok = mbar_wait(k_full + ks, ((kc + jj) / C::KS) & 1, abort_flag))) break;
             tc_fence_after();
           }
-          if (NH == 1) {
+          if constexpr (C::OVL) {
+            // S of block jj for every head, each as soon as the softmax has
+            // loaded the head's previous S; then PV of block jj-1 as the P
+            // tiles arrive
+            if (jj < n) {
+              for (int h = 0; h < nh && ok; ++h) {
+                const uint32_t u = sc[h] + jj;
+                if (u >= 1 && !(ok = mbar_wait(s_free + h, (u - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_s(h, u, ks);
+              }
+              if (!ok) break;
+              mma_commit(k_empty + ks);
+              if (jj == n - 1) mma_commit(q_empty + qb);
+            }
+            if (jj >= 1) {
+              const int i = jj - 1;
+              const uint32_t vs = (vc + i) % C::VS;
+              if (!(ok = mbar_wait(v_full + vs, ((vc + i) / C::VS) & 1, abort_flag))) break;
+              for (int h = 0; h < nh && ok; ++h) {
+                const uint32_t u = sc[h] + i;
+                if (!(ok = mbar_wait(p_full + h, u & 1, abort_flag))) break;
+                if (i == 0 && itv[h] > 0 && !(ok = mbar_wait(o_free + h, (itv[h] - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_pv(h, u, vs, i == 0);
+                mma_commit(p_free + h);
+                if (i == n - 1) mma_commit(o_full + h);
+              }
+              if (!ok) break;
+              mma_commit(v_empty + vs);
+            }
+          } else if (NH == 1) {
             if (jj < n) {
               issue_s(0, sc[0] + jj, ks);
               mma_commit(k_empty + ks);
-              if (jj == n - 1) mma_commit(q_empty);
+              if (jj == n - 1) mma_commit(q_empty + qb);
             }
             if (jj >= 1) {
               const int i = jj - 1;
@@ -314,7 +372,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
                 issue_s(h, sc[h] + jj, ks);
                 if (h == nh - 1) {
                   mma_commit(k_empty + ks);
-                  if (jj == n - 1) mma_commit(q_empty);
+                  if (jj == n - 1) mma_commit(q_empty + qb);
                 }
               }
             }
@@ -380,6 +438,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         uint4 mk = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
         if (slot >= 0) mk = reinterpret_cast<const uint4*>(smem + C::OFF_MASK + vs * C::MASKB)[r];
         tmem_ld_wait();
+        if (C::OVL) {  // S is in registers: the MMA may compute the next S over it
+          tc_fence_before();
+          mbar_arrive(s_free + h);
+        }
         // eight independent max chains (instruction-level parallelism)
         float m8[8];
 #pragma unroll
@@ -401,6 +463,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         const float m_blk = mx * p.scale_log2;
         const bool grow = m_blk > m_use + kRescaleThreshold;
         const float m_new = grow ? m_blk : m_use;
+        if (C::OVL && u >= 1) {
+          // PV of the previous block must be done: it reads the P columns
+          // written below and accumulates into the O a rescale touches
+          ok = mbar_wait(p_free + h, (u - 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         if (__any_sync(0xffffffffu, grow && l > 0.f)) {
           // O holds contributions scaled to the old reference: rescale this
           // warp's rows in place once the PV in flight is done.  With two
@@ -440,8 +512,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
           sr[c >> 1] = pack_bf16(p0, p1);
         }
         l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
-        tmem_st32(sb + 0, sr + 0);
-        tmem_st32(sb + 32, sr + 32);
+        const uint32_t pb = C::OVL ? tl + C::TM_P + h * 64 : sb;  // P: own columns, or over S
+        tmem_st32(pb + 0, sr + 0);
+        tmem_st32(pb + 32, sr + 32);
         tmem_st_wait();
         if (NH == 1 && jj > 0) {
           ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
