@@ -286,8 +286,8 @@ def main():
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
     kernels = {}
-    for name in ("blockmap_classify", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dkdv_finalize", "bwd_dq",
-                 "bwd_simt"):
+    for name in ("blockmap_classify", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dkdv_finalize", "bwd_dv",
+                 "bwd_dk", "bwd_dq", "bwd_simt"):
         n, ms = pt.profile_read(name)
         if n:
             kernels[name] = {"launches": n, "ms_per_launch": ms / n}
@@ -298,6 +298,8 @@ def main():
     per_launch_flops = {  # executed useful-pair flops of each kernel
         "fwd_tc": 4.0 * D * Hq * pairs,
         "bwd_dkdv": 8.0 * D * Hq * pairs,
+        "bwd_dv": 4.0 * D * Hq * pairs,  # head_dim 256: S^T and dV
+        "bwd_dk": 6.0 * D * Hq * pairs,  # head_dim 256: S^T, dP^T and dK
         "bwd_dq": 6.0 * D * Hq * pairs,
     }
     tc = {k: v for k, v in kernels.items() if k in per_launch_flops}

@@ -1197,6 +1197,385 @@ __global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// 4. head_dim 256: three passes of one half-step kernel
+//
+// At D = 256 one 128-row tile of Q, K, V or dO takes 64 KB of shared memory
+// and one 128 x 256 fp32 accumulator takes 256 TMEM columns, so dK and dV
+// cannot both be accumulated in one CTA, nor can all four operand tiles be
+// resident.  The backward therefore runs three passes of one kernel:
+//   WIDE_DV (kv-major): S^T = K Q^T, P^T, dV += P^T dO;
+//   WIDE_DK (kv-major): S^T = K Q^T, dP^T = V dO^T, dS^T, dK += dS^T Q;
+//   WIDE_DQ (q-major):  S = Q K^T, dP = dO V^T, dS, dQ += dS K.
+// The 128-row A operands (K and V, or Q and dO) stay in shared memory for the
+// item; the other side streams in half tiles of 64 rows (N = 64 products), so
+// each step of the item is two half-steps.  Half-step y lands in TMEM buffer
+// y & 1 (S and dP, 64 columns each) and is worked on by compute warpgroup
+// y & 1, which is always the same half of the step.  The operand the
+// accumulating product reads ("late": Q or K, or dO for dV) lives in a two-slot
+// ring and is released when that product is done; the other ("early") in its
+// own ring, released right after S or dP.  Row statistics and tile masks are
+// read from global memory: the rings fill the shared memory.
+// ---------------------------------------------------------------------------
+enum { WIDE_DV = 0, WIDE_DK = 1, WIDE_DQ = 2 };
+
+template <int MODE>
+struct WideCfg {
+  static constexpr int D = 256, NP = 4;
+  static constexpr int RPANEL = 128 * 128;  // resident panel: 128 rows x 128 B
+  static constexpr int RTILE = NP * RPANEL;
+  static constexpr int HPANEL = 64 * 128;   // half-tile panel: 64 rows x 128 B
+  static constexpr int HTILE = NP * HPANEL;
+  static constexpr bool HAS_DP = MODE != WIDE_DV;
+  static constexpr bool KV_MAJOR = MODE != WIDE_DQ;
+  static constexpr int NR = HAS_DP ? 2 : 1;     // resident tiles
+  static constexpr int LS = 2;                  // late ring slots
+  static constexpr int ES = HAS_DP ? 1 : 2;     // early ring slots
+  static constexpr int OFF_R = 0;
+  static constexpr int OFF_L = NR * RTILE;
+  static constexpr int OFF_E = OFF_L + LS * HTILE;
+  static constexpr int OFF_BAR = OFF_E + ES * HTILE;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TM_ACC = 256;  // buffers b at 128 b: S at +0, dP at +64
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+struct WideBars {
+  uint64_t r_full, r_empty, l_full[2], l_empty[2], e_full[2], e_empty[2];
+  uint64_t s_full[2], p_full[2], acc_full, acc_free, mma_done;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(320, 1)
+    k_bwd_wide(const __grid_constant__ CUtensorMap mR1, const __grid_constant__ CUtensorMap mR2,
+               const __grid_constant__ CUtensorMap mL, const __grid_constant__ CUtensorMap mE, const BwdParams p) {
+  using C = WideCfg<MODE>;
+  constexpr int D = C::D;
+  static_assert(sizeof(WideBars) <= 256, "barrier block");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  WideBars* B = reinterpret_cast<WideBars*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = p.Hq / p.Hkv;
+  // items: kv-major from the packed DkdvItem list, q-major from the dq list
+  const int i_begin = C::KV_MAJOR ? p.cta_ptr[blockIdx.x] : p.dq_cta[blockIdx.x].x;
+  const int i_end = C::KV_MAJOR ? p.cta_ptr[blockIdx.x + 1] : p.dq_cta[blockIdx.x].y;
+  // item k -> (major tile, its kv head or q head, steps); step x -> half-step pair
+  const auto item = [&](int k, int& major, int& hh, int& n) {
+    if (C::KV_MAJOR) {
+      const DkdvItem it = p.items[k];
+      major = it.jb;
+      hh = it.hk;
+      n = it.x1 - it.x0;
+    } else {
+      const int4 it = p.dq_items[k];
+      major = it.x;
+      hh = it.y;
+      n = it.w;
+    }
+  };
+  // step x of item k: streamed tile (q tile or kv block), q head, mask slot
+  const auto step = [&](int k, int x, int& minor, int& head, int& slot) {
+    if (C::KV_MAJOR) {
+      const DkdvItem it = p.items[k];
+      const int e0 = p.ptr[it.jb], ncol = p.ptr[it.jb + 1] - e0;
+      const int e = e0 + (it.x0 + x) % ncol;
+      head = it.hk * g + (it.x0 + x) / ncol;
+      minor = p.idx[e];
+      slot = p.pidx[e];
+    } else {
+      const int4 it = p.dq_items[k];
+      minor = p.idx[it.z + x];
+      head = it.y;
+      slot = p.pidx[it.z + x];
+    }
+  };
+
+  if (threadIdx.x == 256) {
+    mbar_init(&B->r_full, 1);
+    mbar_init(&B->r_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->l_full[i], 1);
+      mbar_init(&B->l_empty[i], 1);
+      mbar_init(&B->e_full[i], 1);
+      mbar_init(&B->e_empty[i], 1);
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->p_full[i], 128);  // one warpgroup per buffer
+    }
+    mbar_init(&B->acc_full, 1);
+    mbar_init(&B->acc_free, 256);
+    mbar_init(&B->mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mR1);
+    if (C::HAS_DP) prefetch_tmap(&mR2);
+    prefetch_tmap(&mL);
+    prefetch_tmap(&mE);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t y = 0, nl = 0, ne = 0, it = 0;  // half-steps, late / early loads, items
+      bool ok = true, r_issued = false;
+      for (int k = i_begin; k < i_end && ok; ++k) {
+        int major, hh, n;
+        item(k, major, hh, n);
+        if (n == 0) continue;
+        r_issued = false;
+        if (it > 0 && !(ok = mbar_wait(&B->r_empty, (it - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(&B->r_full, C::NR * C::RTILE);
+        // residents: K (and V) of kv block `major` and kv head hh, or Q (and
+        // dO) of q tile `major` and q head hh
+#pragma unroll
+        for (int pn = 0; pn < C::NP; ++pn) {
+          tma_load_3d(smem + C::OFF_R + pn * C::RPANEL, &mR1, &B->r_full, pn * 64, hh, major * 128);
+          if (C::HAS_DP)
+            tma_load_3d(smem + C::OFF_R + C::RTILE + pn * C::RPANEL, &mR2, &B->r_full, pn * 64, hh, major * 128);
+        }
+        r_issued = true;
+        for (int x = 0; x < n && ok; ++x) {
+          int minor, head, slot;
+          step(k, x, minor, head, slot);
+          const int hs = C::KV_MAJOR ? head : hh / g;  // head of the streamed tiles
+          for (int hf = 0; hf < 2; ++hf, ++y) {
+            const int row = minor * 128 + 64 * hf;
+            {
+              const uint32_t s = y % C::LS;
+              if (y >= C::LS && !(ok = mbar_wait(&B->l_empty[s], (y / C::LS - 1) & 1, abort_flag))) break;
+              mbar_expect_tx(&B->l_full[s], C::HTILE);
+#pragma unroll
+              for (int pn = 0; pn < C::NP; ++pn)
+                tma_load_3d(smem + C::OFF_L + s * C::HTILE + pn * C::HPANEL, &mL, &B->l_full[s], pn * 64, hs, row);
+              ++nl;
+            }
+            {
+              const uint32_t s = y % C::ES;
+              if (y >= C::ES && !(ok = mbar_wait(&B->e_empty[s], (y / C::ES - 1) & 1, abort_flag))) break;
+              mbar_expect_tx(&B->e_full[s], C::HTILE);
+#pragma unroll
+              for (int pn = 0; pn < C::NP; ++pn)
+                tma_load_3d(smem + C::OFF_E + s * C::HTILE + pn * C::HPANEL, &mE, &B->e_full[s], pn * 64, hs, row);
+              ++ne;
+            }
+          }
+        }
+        if (!ok) break;
+        ++it;
+      }
+      if (!ok) {
+        const long long lim = 20000000;
+        if (r_issued) mbar_wait_drain(&B->r_full, it & 1, lim);
+        for (uint32_t s = 0; s < C::LS && s < nl; ++s) {
+          const uint32_t last = nl - 1 - ((nl - 1 - s) % C::LS);
+          mbar_wait_drain(&B->l_full[s], (last / C::LS) & 1, lim);
+        }
+        for (uint32_t s = 0; s < C::ES && s < ne; ++s) {
+          const uint32_t last = ne - 1 - ((ne - 1 - s) % C::ES);
+          mbar_wait_drain(&B->e_full[s], (last / C::ES) & 1, lim);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t IDESC_OUT = idesc_bf16(128, D, false, true);
+      const uint32_t sR1 = smem_u32(smem + C::OFF_R), sR2 = sR1 + C::RTILE;
+      const uint32_t sL = smem_u32(smem + C::OFF_L), sE = smem_u32(smem + C::OFF_E);
+      uint32_t y = 0, it = 0;
+      bool ok = true;
+      for (int k = i_begin; k < i_end && ok; ++k) {
+        int major, hh, n;
+        item(k, major, hh, n);
+        if (n == 0) continue;
+        if (!(ok = mbar_wait(&B->r_full, it & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t n2 = 2 * (uint32_t)n;
+        for (uint32_t x = 0; x <= n2 && ok; ++x) {
+          const uint32_t yy = y + x;
+          if (x < n2) {
+            // S (and dP) of half-step yy into buffer yy & 1; the buffer's
+            // previous half-step had its accumulate product issued before
+            const uint32_t b = yy & 1, ls = yy % C::LS, es = yy % C::ES;
+            {
+              uint64_t* const bars[2] = {&B->l_full[ls], &B->e_full[es]};
+              const uint32_t par[2] = {(yy / C::LS) & 1, (yy / C::ES) & 1};
+              if (!(ok = mbar_wait_all(bars, par, abort_flag))) break;
+            }
+            tc_fence_after();
+            // S from the late ring (Q or K), except for dV, where the late
+            // ring holds dO and S reads Q from the early ring
+            const uint32_t src = C::HAS_DP ? sL + ls * C::HTILE : sE + es * C::HTILE;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t offr = (kk >> 2) * C::RPANEL + (kk & 3) * 32, offh = (kk >> 2) * C::HPANEL + (kk & 3) * 32;
+              mma_ss(tbase + b * 128, sdesc_sw128(sR1 + offr, 16, 1024), sdesc_sw128(src + offh, 16, 1024), IDESC_S,
+                     kk > 0);
+            }
+            if (C::HAS_DP) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t offr = (kk >> 2) * C::RPANEL + (kk & 3) * 32,
+                               offh = (kk >> 2) * C::HPANEL + (kk & 3) * 32;
+                mma_ss(tbase + b * 128 + 64, sdesc_sw128(sR2 + offr, 16, 1024),
+                       sdesc_sw128(sE + es * C::HTILE + offh, 16, 1024), IDESC_S, kk > 0);
+              }
+            }
+            mma_commit(&B->e_empty[es]);
+            mma_commit(&B->s_full[b]);
+            if (x == n2 - 1) mma_commit(&B->r_empty);
+          }
+          if (x >= 1) {
+            // accumulate the previous half-step: OUT += X late (K = 64 rows,
+            // N = 256), X = P or dS packed over that buffer's first S or dP columns
+            const uint32_t yp = yy - 1, bp = yp & 1, lp = yp % C::LS;
+            {
+              uint64_t* const bars[2] = {&B->p_full[bp], x == 1 && it > 0 ? &B->acc_free : nullptr};
+              const uint32_t par[2] = {(yp >> 1) & 1, (it - 1) & 1};
+              if (!(ok = mbar_wait_all(bars, par, abort_flag))) break;
+            }
+            tc_fence_after();
+            const uint32_t a = tbase + bp * 128 + (C::HAS_DP ? 64 : 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tbase + C::TM_ACC, a + kk * 8, sdesc_sw128(sL + lp * C::HTILE + kk * 2048, C::HPANEL, 1024),
+                     IDESC_OUT, (x > 1 || kk > 0));
+            mma_commit(&B->l_empty[lp]);
+          }
+        }
+        if (ok) mma_commit(&B->acc_full);
+        y += n2;
+        ++it;
+      }
+      mma_commit(&B->mma_done);
+      mbar_wait_drain(&B->mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute (major row per thread)
+    const int hw = warp >> 2;  // half of every step, and TMEM buffer, of this warpgroup
+    const int r = threadIdx.x & 127;
+    const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint2* masks = reinterpret_cast<const uint2*>(p.masks);
+    uint32_t y = 0, it = 0;
+    bool ok = true;
+    for (int k = i_begin; k < i_end && ok; ++k) {
+      int major, hh, n;
+      item(k, major, hh, n);
+      const int row = major * 128 + r;  // kv token (kv-major) or q token (q-major)
+      __nv_bfloat16* out = MODE == WIDE_DQ ? p.out0 + ((size_t)row * p.Hq + hh) * D + hw * 128
+                                           : (MODE == WIDE_DV ? p.out1 : p.out0) + ((size_t)row * p.Hkv + hh) * D +
+                                                 hw * 128;  // this warpgroup's 128 columns of the output row
+      if (n == 0) {
+        if (row < p.T) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 16; ++c) reinterpret_cast<uint4*>(out)[c] = z;
+        }
+        continue;
+      }
+      float l2r = 0.f, dlr = 0.f;  // q-major: this row's statistics
+      if (!C::KV_MAJOR) {
+        l2r = p.lse2[(size_t)hh * p.Tpad + row];
+        dlr = p.delta[(size_t)hh * p.Tpad + row];
+      }
+      for (int x = 0; x < n; ++x) {
+        int minor, head, slot;
+        step(k, x, minor, head, slot);
+        const uint32_t yy = y + 2 * x + hw, b = yy & 1;
+        uint2 mk = make_uint2(0xffffffffu, 0xffffffffu);
+        if (slot >= 0) mk = masks[(size_t)slot * 256 + 2 * r + hw];
+        // kv-major: statistics of this half's 64 q columns (uniform over the warp)
+        const float4* l4 = reinterpret_cast<const float4*>(p.lse2 + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
+        const float4* d4 = reinterpret_cast<const float4*>(p.delta + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
+        ok = mbar_wait(&B->s_full[b], (yy >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[64], dr[64];
+        tmem_ld32(tl + b * 128, sr);
+        tmem_ld32(tl + b * 128 + 32, sr + 32);
+        if (C::HAS_DP) {
+          tmem_ld32(tl + b * 128 + 64, dr);
+          tmem_ld32(tl + b * 128 + 96, dr + 32);
+        }
+        tmem_ld_wait();
+        uint32_t pk[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          float la[4], da[4];
+          if (C::KV_MAJOR) {
+            const float4 lv = l4[c4];
+            la[0] = lv.x, la[1] = lv.y, la[2] = lv.z, la[3] = lv.w;
+            if (C::HAS_DP) {
+              const float4 dv = d4[c4];
+              da[0] = dv.x, da[1] = dv.y, da[2] = dv.z, da[3] = dv.w;
+            }
+          } else {
+            la[0] = la[1] = la[2] = la[3] = l2r;
+            da[0] = da[1] = da[2] = da[3] = dlr;
+          }
+          float v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * c4 + j;
+            const uint32_t word = c < 32 ? mk.x : mk.y;
+            float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[j]));
+            pr = ((word >> (c & 31)) & 1u) ? pr : 0.f;
+            v[j] = C::HAS_DP ? pr * (__uint_as_float(dr[c]) - da[j]) : pr;
+          }
+          pk[2 * c4] = pack_bf16(v[0], v[1]);
+          pk[2 * c4 + 1] = pack_bf16(v[2], v[3]);
+        }
+        tmem_st32(tl + b * 128 + (C::HAS_DP ? 64 : 0), pk);  // over the columns just read
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&B->p_full[b]);
+      }
+      if (!ok) break;
+      ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float mul = MODE == WIDE_DV ? 1.f : p.scale;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tl + C::TM_ACC + hw * 128 + c * 32, v);
+        tmem_ld_wait();
+        if (row < p.T) store_row32(out + c * 32, v, mul);
+      }
+      tc_fence_before();
+      mbar_arrive(&B->acc_free);
+      y += 2 * (uint32_t)n;
+      ++it;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tbase, 512);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 template <class K>
@@ -1510,15 +1889,110 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   return 0;
 }
 
+// head_dim 256: preprocess, then the dV, dK and dQ passes of k_bwd_wide.
+int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
+                    int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
+                    float* lse2, bool allow_build, cudaStream_t s) {
+  constexpr int D = 256;
+  static int set_v[64] = {0}, set_k[64] = {0}, set_q[64] = {0};
+  const int dev = bm->device;
+  int rc = reserve_smem(k_bwd_wide<WIDE_DV>, WideCfg<WIDE_DV>::BYTES, dev, set_v);
+  if (!rc) rc = reserve_smem(k_bwd_wide<WIDE_DK>, WideCfg<WIDE_DK>::BYTES, dev, set_k);
+  if (!rc) rc = reserve_smem(k_bwd_wide<WIDE_DQ>, WideCfg<WIDE_DQ>::BYTES, dev, set_q);
+  if (rc) return rc;
+  if (bm->n_partial > 0 && (!bm->mask_rows || !bm->mask_cols)) {
+    set_error("backward kernel: block map has no tile masks");
+    return 1;
+  }
+  const int sms = num_sms(dev);
+  // kv-major items without split columns (each pass writes its outputs once)
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, allow_build, s))) return rc;
+  if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s))) return rc;
+  const int Tpad = bm->nq * 128;
+  {
+    const long long threads = (long long)Hq * Tpad * (D / 8);
+    ProfScope ps(s, "bwd_prep");
+    k_bwd_prep<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
+  }
+  CUtensorMap mQ, mdO, mK, mV, mQh, mdOh, mKh, mVh;
+  if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128) ||
+      !make_tmap_thd(&mK, K, T, Hkv, D, 128) || !make_tmap_thd(&mV, V, T, Hkv, D, 128) ||
+      !make_tmap_thd(&mQh, Q, T, Hq, D, 64) || !make_tmap_thd(&mdOh, dO, T, Hq, D, 64) ||
+      !make_tmap_thd(&mKh, K, T, Hkv, D, 64) || !make_tmap_thd(&mVh, V, T, Hkv, D, 64))
+    return 3;
+  BwdParams p{};
+  p.delta = delta;
+  p.lse2 = lse2;
+  p.T = T;
+  p.Tpad = Tpad;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  int launches = 1;
+  // dV and dK: kv-major lists and column masks
+  p.ptr = bm->k_ptr;
+  p.idx = bm->q_idx;
+  p.pidx = bm->pidxT;
+  p.masks = bm->mask_cols;
+  p.items = static_cast<const DkdvItem*>(bm->bwd_items);
+  p.cta_ptr = static_cast<const int*>(bm->bwd_cta);
+  p.n_items = bm->bwd_n_items;
+  p.out0 = static_cast<__nv_bfloat16*>(dK);
+  p.out1 = static_cast<__nv_bfloat16*>(dV);
+  if (p.n_items > 0) {
+    {
+      ProfScope ps(s, "bwd_dv");
+      k_bwd_wide<WIDE_DV><<<bm->bwd_grid, 320, WideCfg<WIDE_DV>::BYTES, s>>>(mK, mK, mdOh, mQh, p);
+    }
+    {
+      ProfScope ps(s, "bwd_dk");
+      k_bwd_wide<WIDE_DK><<<bm->bwd_grid, 320, WideCfg<WIDE_DK>::BYTES, s>>>(mK, mV, mQh, mdOh, p);
+    }
+    launches += 2;
+  }
+  // dQ: q-major lists and row masks
+  p.idx = bm->kv_idx;
+  p.pidx = bm->pidx;
+  p.masks = bm->mask_rows;
+  p.items = nullptr;
+  p.cta_ptr = nullptr;
+  p.dq_items = static_cast<const int4*>(bm->dq_items);
+  p.dq_cta = static_cast<const int4*>(bm->dq_cta);
+  p.out0 = static_cast<__nv_bfloat16*>(dQ);
+  p.out1 = nullptr;
+  for (int i = 0; i < bm->dq_n_empty; ++i) {  // q tiles that attend to nothing
+    const int t0 = bm->h_dq_empty[i] * 128, t1 = std::min(T, t0 + 128);
+    if (cudaMemsetAsync(static_cast<__nv_bfloat16*>(dQ) + (size_t)t0 * Hq * D, 0,
+                        sizeof(__nv_bfloat16) * (size_t)(t1 - t0) * Hq * D, s) != cudaSuccess) {
+      set_error("backward: cudaMemsetAsync failed");
+      return 3;
+    }
+  }
+  if (bm->dq_n_items > 0) {
+    ProfScope ps(s, "bwd_dq");
+    k_bwd_wide<WIDE_DQ><<<bm->dq_grid, 320, WideCfg<WIDE_DQ>::BYTES, s>>>(mQ, mdO, mKh, mVh, p);
+    ++launches;
+  }
+  count_launch(launches);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("backward launch failed: %s", cudaGetErrorString(e));
+    return 3;
+  }
+  return 0;
+}
+
 }  // namespace
 
-bool bwd_tc_supported(int D) { return D == 64 || D == 128; }
+bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
 
 int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStream_t s) {
   if (!bwd_tc_supported(D) || bm->BM != 128 || bm->BN != 128) return 0;  // those paths keep no lists
   const int sms = num_sms(bm->device);
   int rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, true, s);
-  if (!rc && D == 128) rc = prepare_dq_items(bm, Hq, sms, true, s);
+  if (!rc && D >= 128) rc = prepare_dq_items(bm, Hq, sms, true, s);
   return rc;
 }
 
@@ -1532,6 +2006,8 @@ int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const vo
     case 128:
       return launch_bwd<128>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial,
                              partial_bytes, allow_build, s);
+    case 256:
+      return launch_bwd_wide(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, allow_build, s);
     default: set_error("tensor-core backward: head_dim %d not built", D); return 2;
   }
 }
