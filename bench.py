@@ -286,7 +286,7 @@ def main():
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
     kernels = {}
-    for name in ("blockmap_classify", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dkdv_finalize", "bwd_dv",
+    for name in ("blockmap_classify", "blockmap_lists", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dkdv_finalize", "bwd_dv",
                  "bwd_dk", "bwd_dq", "bwd_simt"):
         n, ms = pt.profile_read(name)
         if n:

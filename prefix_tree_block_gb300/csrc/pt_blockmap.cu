@@ -482,23 +482,32 @@ T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
 
-// Pinned staging for host->device uploads of node tables (avoids the stream
-// synchronisation a pageable copy implies).  Reused across builds; an event
-// guards against overwriting data a previous upload has not read yet.
+// Pinned staging for host->device uploads (avoids the stream synchronisation
+// a pageable copy implies).  A ring of slots per device: a slot is refilled
+// only once the copy that last read it has run, so the host blocks only when
+// it is several uploads ahead of the GPU.
 int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
-  struct Staging {
+  constexpr int kSlots = 4;
+  struct Slot {
     void* host = nullptr;
     size_t cap = 0;
     cudaEvent_t done = nullptr;
+    bool used = false;
+  };
+  struct Ring {
+    Slot slot[kSlots];
+    int next = 0;
   };
   static std::mutex mu;
-  static Staging st[kMaxDev];
+  static Ring rings[kMaxDev];
   if (bytes == 0) return 0;
   if (dev < 0 || dev >= kMaxDev) return 3;
   std::lock_guard<std::mutex> lk(mu);
-  Staging& g = st[dev];
-  if (g.done) cudaEventSynchronize(g.done);
-  else if (cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming) != cudaSuccess) return 3;
+  Ring& rg = rings[dev];
+  Slot& g = rg.slot[rg.next];
+  rg.next = (rg.next + 1) % kSlots;
+  if (!g.done && cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming) != cudaSuccess) return 3;
+  if (g.used) cudaEventSynchronize(g.done);  // usually long complete
   if (g.cap < bytes) {
     if (g.host) cudaFreeHost(g.host);
     g.host = nullptr;
@@ -516,6 +525,7 @@ int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
     return 3;
   }
   cudaEventRecord(g.done, s);
+  g.used = true;
   return 0;
 }
 
@@ -593,7 +603,6 @@ int alloc_lists(pt_blockmap* bm, cudaStream_t s) {
 // device, classify, count, list, order and mask.  Synchronises the stream
 // once (to size the lists); everything after that is asynchronous.
 int finish_map(pt_blockmap* bm, cudaStream_t s) {
-  ProfScope ps(s, "blockmap_classify");
   const int nq = bm->nq, nk = bm->nk, dev = bm->device;
   const long long ntiles = (long long)nq * nk;
   void* tmpA = nullptr;
@@ -613,24 +622,28 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
     int* col_cnt = row_cnt + nq;
     int* row_part = col_cnt + nk;
     int* prow_ptr = at<int>(tmpA, o_pp);
-    if (cudaMemsetAsync(counters, 0, sizeof(int) * (ncnt + nq), s) != cudaSuccess) {
-      rc = 3;
-      break;
-    }
-    if (ntiles > 0) {
-      long long threads = ntiles * 32;
-      k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
-                                                                   bm->node_start, bm->node_end, bm->parent, kinds,
-                                                                   counters, row_cnt, col_cnt, row_part);
+    {
+      ProfScope ps(s, "blockmap_classify");  // tile classes, list sizes, longest-first orders
+      if (cudaMemsetAsync(counters, 0, sizeof(int) * (ncnt + nq), s) != cudaSuccess) {
+        rc = 3;
+        break;
+      }
+      if (ntiles > 0) {
+        long long threads = ntiles * 32;
+        k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
+                                                                     bm->node_start, bm->node_end, bm->parent, kinds,
+                                                                     counters, row_cnt, col_cnt, row_part);
+        PT_LAUNCHED(1);
+      }
+      k_scan3<<<1, kScanBlock, 0, s>>>(row_cnt, nq, bm->q_ptr, col_cnt, nk, bm->k_ptr, row_part, nq, prow_ptr);
       PT_LAUNCHED(1);
+      if (ntiles > 0) {
+        k_lpt2<<<(unsigned)(((long long)(nq + nk) * 32 + 255) / 256), 256, 0, s>>>(row_cnt, nq, bm->q_order, col_cnt,
+                                                                                nk, bm->k_order);
+        PT_LAUNCHED(1);
+      }
     }
-    k_scan3<<<1, kScanBlock, 0, s>>>(row_cnt, nq, bm->q_ptr, col_cnt, nk, bm->k_ptr, row_part, nq, prow_ptr);
-    PT_LAUNCHED(1);
-    if (ntiles > 0) {
-      k_lpt2<<<(unsigned)(((long long)(nq + nk) * 32 + 255) / 256), 256, 0, s>>>(row_cnt, nq, bm->q_order, col_cnt,
-                                                                              nk, bm->k_order);
-      PT_LAUNCHED(1);
-    }
+    if (rc) break;
     // the one synchronisation of the build: list sizes to the host
     bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * ncnt));
     if (!bm->h_counts) {
@@ -656,6 +669,7 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
     bm->n_partial = bm->nnz - bm->n_full;
     if ((rc = alloc_lists(bm, s))) break;
     if (ntiles > 0 && bm->nnz > 0) {
+      ProfScope ps(s, "blockmap_lists");  // the lists and the partial tiles' masks
       if ((rc = pool_alloc(&tmpB, sizeof(int2) * (size_t)std::max<int64_t>(bm->n_partial, 1), dev, s))) break;
       int2* slot_tile = static_cast<int2*>(tmpB);
       k_fill_rows<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, bm->q_ptr, prow_ptr, bm->kv_idx, bm->kind,
@@ -783,16 +797,23 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
   bm->n_nodes = N;
   void* dtab = nullptr;
   do {
-    if ((rc = pool_alloc(&dtab, sizeof(int) * (size_t)2 * std::max(N, 1), bm->device, s))) break;
-    // start, end, parent go straight into the map; tin, tout into a temporary
+    // one upload of start | end | parent | tin | tout; the first three are
+    // then copied into the map on the device
+    if ((rc = pool_alloc(&dtab, sizeof(int) * (size_t)5 * std::max(N, 1), bm->device, s))) break;
     if (N > 0) {
-      if ((rc = upload(bm->node_start, start, sizeof(int) * N, bm->device, s))) break;
-      if ((rc = upload(bm->node_end, end, sizeof(int) * N, bm->device, s))) break;
-      if ((rc = upload(bm->parent, par, sizeof(int) * N, bm->device, s))) break;
-      if ((rc = upload(dtab, tin, sizeof(int) * (size_t)2 * N, bm->device, s))) break;
+      if ((rc = upload(dtab, tab.data(), sizeof(int) * (size_t)5 * N, bm->device, s))) break;
+      const int* d = static_cast<const int*>(dtab);
+      if (cudaMemcpyAsync(bm->node_start, d, sizeof(int) * N, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+          cudaMemcpyAsync(bm->node_end, d + N, sizeof(int) * N, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+          cudaMemcpyAsync(bm->parent, d + 2 * (size_t)N, sizeof(int) * N, cudaMemcpyDeviceToDevice, s) !=
+              cudaSuccess) {
+        set_error("block map: device copy of node tables failed");
+        rc = 3;
+        break;
+      }
     }
     if (bm->tpad > 0) {
-      int* d_tin = static_cast<int*>(dtab);
+      int* d_tin = static_cast<int*>(dtab) + 3 * (size_t)N;
       k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>((int)T, bm->tpad, N, bm->node_end, d_tin, d_tin + N,
                                                            bm->tok, bm->node_of);
       PT_LAUNCHED(1);
