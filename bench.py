@@ -61,6 +61,24 @@ MEASURED_TRAFFIC = {
 }
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank runs the same per-GPU workload (replicas,
+    weak scaling), so the job processes world x the units of one rank in the
+    slowest rank's time."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -277,13 +295,9 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     pt.sync_status()
-    total_ms = sum(times)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times), dist, dev)
     ms_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, args.steps, total_ms)
 
     kernels = {}
     for name in ("blockmap_classify", "blockmap_lists", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dkdv_finalize", "bwd_dv",
@@ -335,14 +349,10 @@ def main():
     e2e_step()
     torch.cuda.synchronize()
     et = timed(args.steps, e2e_step)
-    e2e_ms = sum(et)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(et), dist, dev)
     h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do)) + 4 * (nl.size + pp.size + pn.size)
     d2h = sum(x.numel() * x.element_size() for x in (dQ, dK, dV))
-    e2e = {"value": world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    e2e = {"value": whole_job_tflops(world, flops_step, args.steps, e2e_ms), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     cpu = None
