@@ -78,7 +78,14 @@ typedef struct pt_blockmap pt_blockmap;
  *   parent of b.
  * block_m, block_n: q-tile rows and kv-block columns.  The tensor-core
  *   kernels need 128 x 128; the fp32 kernels accept any positive size.
- * stream: the build runs on it and synchronises it once before returning.
+ * stream: the build runs on it.  With 128 x 128 tiles the build does not
+ *   wait for the device: the lists are allocated at bounds the host computes
+ *   from the node lengths (list entries: the causal tile count; partial
+ *   tiles: those in a row or column of tiles holding a node boundary, plus
+ *   the diagonal) when those take at most 1 GiB, and the exact list sizes
+ *   reach the host behind an event, read on first use (pt_blockmap_info's
+ *   nnz and n_full, the exports, the backward's work lists).  Otherwise the
+ *   build synchronises the stream once before returning.
  * out: receives the new map.
  *
  * Errors: PT_ERR_INVALID_ARG when a length is negative, a path is empty or
@@ -121,7 +128,9 @@ pt_status pt_blockmap_dense(const pt_blockmap* src, cudaStream_t stream, pt_bloc
 
 /* Sizes of a map: T, nq = ceil(T / block_m), nk = ceil(T / block_n), the
  * number of non-empty tiles and how many of them are full.  Any output
- * pointer may be NULL. */
+ * pointer may be NULL.  Asking for nnz or n_full waits for the build's device
+ * work if the list sizes have not reached the host yet; the other sizes never
+ * wait. */
 pt_status pt_blockmap_info(const pt_blockmap* bm, int32_t* T, int32_t* block_m, int32_t* block_n,
                            int32_t* nq, int32_t* nk, int64_t* nnz, int64_t* n_full);
 

@@ -115,11 +115,30 @@ class BlockMap:
         self._h = ctypes.c_void_p(handle)
         self._lib = load_library()
         T, bm_, bn_, nq, nk = (ctypes.c_int32() for _ in range(5))
-        nnz, nfull = ctypes.c_int64(), ctypes.c_int64()
         _check(self._lib.pt_blockmap_info(self._h, ctypes.byref(T), ctypes.byref(bm_), ctypes.byref(bn_),
-                                          ctypes.byref(nq), ctypes.byref(nk), ctypes.byref(nnz), ctypes.byref(nfull)))
+                                          ctypes.byref(nq), ctypes.byref(nk), None, None))
         self.T, self.block_m, self.block_n = T.value, bm_.value, bn_.value
-        self.nq, self.nk, self.nnz, self.n_full = nq.value, nk.value, nnz.value, nfull.value
+        self.nq, self.nk = nq.value, nk.value
+        self._counts = None
+
+    def _list_sizes(self):
+        # the list sizes reach the host after the build's device work: asked for lazily
+        if self._counts is None:
+            nnz, nfull = ctypes.c_int64(), ctypes.c_int64()
+            _check(self._lib.pt_blockmap_info(self._h, None, None, None, None, None, ctypes.byref(nnz),
+                                              ctypes.byref(nfull)))
+            self._counts = (nnz.value, nfull.value)
+        return self._counts
+
+    @property
+    def nnz(self) -> int:
+        """Non-empty tiles (waits for the build on the device the first time)."""
+        return self._list_sizes()[0]
+
+    @property
+    def n_full(self) -> int:
+        """Fully kept tiles (waits for the build on the device the first time)."""
+        return self._list_sizes()[1]
 
     @property
     def handle(self):

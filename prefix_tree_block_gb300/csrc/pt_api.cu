@@ -221,6 +221,8 @@ pt_status pt_blockmap_info(const pt_blockmap* bm, int32_t* T, int32_t* block_m, 
     set_error("pt_blockmap_info: NULL map");
     return PT_ERR_INVALID_ARG;
   }
+  if (nnz || n_full)  // list sizes: may wait for the build on the device
+    if (int rc = pt::ensure_counts(bm)) return as_status(rc);
   if (T) *T = bm->T;
   if (block_m) *block_m = bm->BM;
   if (block_n) *block_n = bm->BN;
@@ -237,6 +239,7 @@ pt_status pt_blockmap_export(const pt_blockmap* bm, int32_t* q_ptr, int32_t* kv_
     set_error("pt_blockmap_export: NULL map");
     return PT_ERR_INVALID_ARG;
   }
+  if (int rc = pt::ensure_counts(bm)) return as_status(rc);
   struct Item {
     void* dst;
     const void* src;
@@ -263,6 +266,7 @@ pt_status pt_blockmap_export_masks(const pt_blockmap* bm, int32_t* pidx, int32_t
     set_error("pt_blockmap_export_masks: NULL map");
     return PT_ERR_INVALID_ARG;
   }
+  if (int rc = pt::ensure_counts(bm)) return as_status(rc);
   if (bm->n_partial > 0 && (!bm->mask_rows || !bm->mask_cols)) {
     set_error("pt_blockmap_export_masks: this map has no tile masks (tile sizes other than 128 x 128)");
     return PT_ERR_UNSUPPORTED;

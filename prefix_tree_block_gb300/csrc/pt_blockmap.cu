@@ -290,7 +290,7 @@ __global__ void k_scan3(const int* a, int na, int* oa, const int* b, int nb, int
 // q-major lists: one warp per q tile compacts its row in kv order, numbering
 // partial tiles row-major (slot = partial tiles in earlier rows + rank in row).
 __global__ void k_fill_rows(const uint8_t* kinds, int nq, int nk, const int* q_ptr, const int* prow_ptr, int* kv_idx,
-                            uint8_t* kd, int* pidx, int2* slot_tile) {
+                            uint8_t* kd, int* pidx, int2* slot_tile, long long slot_cap) {
   int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= nq) return;
   int pos = q_ptr[w], ppos = prow_ptr[w];
@@ -306,8 +306,13 @@ __global__ void k_fill_rows(const uint8_t* kinds, int nq, int nk, const int* q_p
       kd[pos + off] = k;
       if (k == PT_KIND_PARTIAL) {
         const int slot = ppos + __popc(mp & below);
-        pidx[pos + off] = slot;
-        slot_tile[slot] = make_int2(w, x);
+        if (slot < slot_cap) {
+          pidx[pos + off] = slot;
+          slot_tile[slot] = make_int2(w, x);
+        } else {  // more partial tiles than the allocation's bound: never written past it
+          pidx[pos + off] = -1;
+          record_status(PT_STATUS_INVALID);
+        }
       } else {
         pidx[pos + off] = -1;
       }
@@ -346,33 +351,106 @@ __global__ void k_fill_cols(const uint8_t* kinds, int nq, int nk, const int* k_p
   }
 }
 
-// Keep bitmasks of every partial 128 x 128 tile, both orientations:
+// First run start at or after `from` in a 128-bit set of run starts (128 if none).
+__device__ __forceinline__ int next_run(const uint32_t* w, int from) {
+  if (from >= 128) return 128;
+  int i = from >> 5;
+  uint32_t m = w[i] & (0xffffffffu << (from & 31));
+  while (m == 0) {
+    if (++i == 4) return 128;
+    m = w[i];
+  }
+  return (i << 5) + __ffs(m) - 1;
+}
+
+// bits[a, b) of a 128-bit mask, 0 <= a < b <= 128
+__device__ __forceinline__ void set_bits(uint32_t* bits, int a, int b) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int lo = max(a - 32 * w, 0), hi = min(b - 32 * w, 32);
+    if (lo < hi) bits[w] |= (hi == 32 ? 0xffffffffu : ((1u << hi) - 1u)) & (0xffffffffu << lo);
+  }
+}
+
+// Keep bitmasks of one partial 128 x 128 tile, both orientations:
 // mask_rows[slot][r][w] bit b = keep(q = i*128 + r, kv = j*128 + 32w + b),
 // mask_cols[slot][c][w] bit b = keep(q = i*128 + 32w + b, kv = j*128 + c).
 // Pairs outside [0, T) are never kept.
-__global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols) {
-  __shared__ pt_tok tq[128], tk[128];
-  const int s = blockIdx.x, r = threadIdx.x;
+__device__ __forceinline__ void tile_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_t* mask_rows,
+                                           uint32_t* mask_cols, long long s, pt_tok* tq, pt_tok* tk,
+                                           uint32_t* kstart, uint32_t* qstart) {
+  const int r = threadIdx.x;
   const int2 ij = slot_tile[s];
   const int q0 = ij.x * 128, k0 = ij.y * 128;
   tq[r] = tok[q0 + r];
   tk[r] = tok[k0 + r];
   __syncthreads();
+  // Runs: maximal ranges of tokens with the same (tin, tout), i.e. of one node
+  // (padding past T is one more run that sees and is seen by nothing).  Every
+  // key of a run passes or fails the ancestor test together, so a row sees a
+  // run's keys up to the causal limit: one bit range per run.
+  const bool ks = r == 0 || tk[r].tin != tk[r - 1].tin || tk[r].tout != tk[r - 1].tout;
+  const bool qs = r == 0 || tq[r].tin != tq[r - 1].tin || tq[r].tout != tq[r - 1].tout;
+  const uint32_t kb = __ballot_sync(0xffffffffu, ks), qb = __ballot_sync(0xffffffffu, qs);
+  if ((r & 31) == 0) {
+    kstart[r >> 5] = kb;
+    qstart[r >> 5] = qb;
+  }
+  __syncthreads();
+  const int runs = __popc(kstart[0]) + __popc(kstart[1]) + __popc(kstart[2]) + __popc(kstart[3]) +
+                   __popc(qstart[0]) + __popc(qstart[1]) + __popc(qstart[2]) + __popc(qstart[3]);
   uint32_t row[4] = {0, 0, 0, 0}, col[4] = {0, 0, 0, 0};
   const int q = q0 + r, kv = k0 + r;
   const pt_tok mq = tq[r], mk = tk[r];
-  for (int c = 0; c < 128; ++c) {
-    const int kvc = k0 + c;
-    const pt_tok t = tk[c];
-    if (q < T && kvc < T && kvc <= q && t.tin <= mq.tin && mq.tin < t.tout) row[c >> 5] |= 1u << (c & 31);
-    const int qc = q0 + c;
-    const pt_tok u = tq[c];
-    if (qc < T && kv < T && kv <= qc && mk.tin <= u.tin && u.tin < mk.tout) col[c >> 5] |= 1u << (c & 31);
+  if (runs <= 48) {
+    if (q < T)
+      for (int c = 0; c < 128;) {
+        const int c1 = next_run(kstart, c + 1);
+        const pt_tok t = tk[c];
+        if (k0 + c < T && t.tin <= mq.tin && mq.tin < t.tout) {
+          const int hi = min(c1, q - k0 + 1);  // k0 + c' <= q
+          if (hi > c) set_bits(row, c, hi);
+        }
+        c = c1;
+      }
+    if (kv < T)
+      for (int c = 0; c < 128;) {
+        const int c1 = next_run(qstart, c + 1);
+        const pt_tok u = tq[c];
+        if (q0 + c < T && mk.tin <= u.tin && u.tin < mk.tout) {
+          const int lo = max(c, kv - q0);  // kv <= q0 + c'
+          const int hi = min(c1, T - q0);
+          if (lo < hi) set_bits(col, lo, hi);
+        }
+        c = c1;
+      }
+  } else {  // many short nodes: pair by pair
+    for (int c = 0; c < 128; ++c) {
+      const int kvc = k0 + c;
+      const pt_tok t = tk[c];
+      if (q < T && kvc < T && kvc <= q && t.tin <= mq.tin && mq.tin < t.tout) row[c >> 5] |= 1u << (c & 31);
+      const int qc = q0 + c;
+      const pt_tok u = tq[c];
+      if (qc < T && kv < T && kv <= qc && mk.tin <= u.tin && u.tin < mk.tout) col[c >> 5] |= 1u << (c & 31);
+    }
   }
   uint4* mr = reinterpret_cast<uint4*>(mask_rows) + (size_t)s * 128 + r;
   uint4* mc = reinterpret_cast<uint4*>(mask_cols) + (size_t)s * 128 + r;
   *mr = make_uint4(row[0], row[1], row[2], row[3]);
   *mc = make_uint4(col[0], col[1], col[2], col[3]);
+}
+
+// All partial tiles, grid-stride: slots 0 .. n_partial - 1, n_partial = n_known
+// when that is >= 0, else nnz - n_full read on the device (at most p_cap).
+__global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols,
+                        long long n_known, const int* nnz_total, const int* n_full, long long p_cap) {
+  __shared__ pt_tok tq[128], tk[128];
+  __shared__ uint32_t kstart[4], qstart[4];
+  const long long n_part = min(n_known >= 0 ? n_known : (long long)(*nnz_total - *n_full), p_cap);
+  for (long long s = blockIdx.x; s < n_part; s += gridDim.x) {
+    tile_masks(T, tok, slot_tile, mask_rows, mask_cols, s, tq, tk, kstart, qstart);
+    __syncthreads();
+  }
 }
 
 // dense map: every tile partial; slot = row-major tile index
@@ -486,8 +564,90 @@ T* at(void* base, size_t off) {
 // a pageable copy implies).  A ring of slots per device: a slot is refilled
 // only once the copy that last read it has run, so the host blocks only when
 // it is several uploads ahead of the GPU.
+// Device-to-host copy that waits for the stream: through a pinned buffer
+// per device (a copy to pageable memory is staged by the driver and slower).
+int download_sync(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
+  struct Buf {
+    void* host = nullptr;
+    size_t cap = 0;
+  };
+  static std::mutex mu;
+  static Buf bufs[kMaxDev];
+  if (dev < 0 || dev >= kMaxDev) return 3;
+  std::lock_guard<std::mutex> lk(mu);
+  Buf& b = bufs[dev];
+  if (b.cap < bytes) {
+    if (b.host) cudaFreeHost(b.host);
+    b.host = nullptr;
+    b.cap = 0;
+    size_t cap = bytes < (1u << 16) ? (1u << 16) : bytes;
+    if (cudaHostAlloc(&b.host, cap, cudaHostAllocDefault) != cudaSuccess) {
+      set_error("pinned download buffer of %zu bytes failed", cap);
+      return 5;
+    }
+    b.cap = cap;
+  }
+  if (bytes && cudaMemcpyAsync(b.host, src, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    set_error("block map download failed");
+    return 3;
+  }
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    set_error("block map build failed: %s", cudaGetErrorString(e));
+    return 3;
+  }
+  std::memcpy(dst, b.host, bytes);
+  return 0;
+}
+
+// Pinned host buffers, each with an event, reused across builds: a build's
+// list lengths are copied into one behind its event, and the map holds the
+// slot until the lengths are read on the host.
+struct PinnedSlot {
+  void* host = nullptr;
+  size_t cap = 0;
+  cudaEvent_t ev = nullptr;
+};
+std::mutex g_pinned_mu;
+std::vector<PinnedSlot> g_pinned_free[kMaxDev];
+
+int pinned_acquire(int dev, size_t bytes, PinnedSlot* out) {
+  if (dev < 0 || dev >= kMaxDev) return 3;
+  {
+    std::lock_guard<std::mutex> lk(g_pinned_mu);
+    std::vector<PinnedSlot>& fl = g_pinned_free[dev];
+    for (size_t i = 0; i < fl.size(); ++i)
+      if (fl[i].cap >= bytes) {
+        *out = fl[i];
+        fl[i] = fl.back();
+        fl.pop_back();
+        return 0;
+      }
+  }
+  PinnedSlot sl;
+  sl.cap = bytes < (1u << 16) ? (1u << 16) : bytes;
+  if (cudaHostAlloc(&sl.host, sl.cap, cudaHostAllocDefault) != cudaSuccess) {
+    set_error("pinned staging allocation of %zu bytes failed", sl.cap);
+    return 5;
+  }
+  if (cudaEventCreateWithFlags(&sl.ev, cudaEventDisableTiming) != cudaSuccess) {
+    cudaFreeHost(sl.host);
+    set_error("event creation failed");
+    return 3;
+  }
+  *out = sl;
+  return 0;
+}
+
+void pinned_release(int dev, const PinnedSlot& sl) {
+  if (!sl.host || dev < 0 || dev >= kMaxDev) return;
+  std::lock_guard<std::mutex> lk(g_pinned_mu);
+  g_pinned_free[dev].push_back(sl);
+}
+
 int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
-  constexpr int kSlots = 4;
+  // enough slots that a slot's previous copy (several steps back) is done
+  constexpr int kSlots = 16;
   struct Slot {
     void* host = nullptr;
     size_t cap = 0;
@@ -545,8 +705,10 @@ int new_map(int T, int BM, int BN, int node_cap, cudaStream_t s, pt_blockmap** o
   bm->nk = (T + BN - 1) / BN;
   bm->tpad = std::max(bm->nq * BM, bm->nk * BN);
   Layout L;
-  size_t o_tok = L.add<pt_tok>(bm->tpad), o_node = L.add<int>(T), o_ns = L.add<int>(node_cap),
-         o_ne = L.add<int>(node_cap), o_par = L.add<int>(node_cap), o_qp = L.add<int>(bm->nq + 1),
+  // node tables: start | end | parent | tin | tout, node_cap entries each
+  // (the tree build uploads all five at once; tin and tout feed the token table)
+  size_t o_tok = L.add<pt_tok>(bm->tpad), o_node = L.add<int>(T), o_ns = L.add<int>((size_t)5 * node_cap),
+         o_qp = L.add<int>(bm->nq + 1),
          o_kp = L.add<int>(bm->nk + 1), o_qo = L.add<int>(bm->nq), o_ko = L.add<int>(bm->nk);
   int rc = pool_alloc(&bm->mem_fixed, L.off, bm->device, s);
   if (rc) {
@@ -556,8 +718,8 @@ int new_map(int T, int BM, int BN, int node_cap, cudaStream_t s, pt_blockmap** o
   bm->tok = at<pt_tok>(bm->mem_fixed, o_tok);
   bm->node_of = at<int>(bm->mem_fixed, o_node);
   bm->node_start = at<int>(bm->mem_fixed, o_ns);
-  bm->node_end = at<int>(bm->mem_fixed, o_ne);
-  bm->parent = at<int>(bm->mem_fixed, o_par);
+  bm->node_end = bm->node_start + node_cap;
+  bm->parent = bm->node_end + node_cap;
   bm->q_ptr = at<int>(bm->mem_fixed, o_qp);
   bm->k_ptr = at<int>(bm->mem_fixed, o_kp);
   bm->q_order = at<int>(bm->mem_fixed, o_qo);
@@ -567,14 +729,17 @@ int new_map(int T, int BM, int BN, int node_cap, cudaStream_t s, pt_blockmap** o
 }
 
 // The lists part, once nnz and the number of partial tiles are known.
-int alloc_lists(pt_blockmap* bm, cudaStream_t s) {
-  const int64_t nnz = bm->nnz;
-  const bool masks = bm->BM == 128 && bm->BN == 128 && bm->n_partial > 0;
+// `nnz` list entries and `n_part` mask slots: the exact sizes, or bounds when
+// the build does not wait for them.
+int alloc_lists(pt_blockmap* bm, int64_t nnz, int64_t n_part, cudaStream_t s) {
+  const bool masks = bm->BM == 128 && bm->BN == 128 && n_part > 0;
+  bm->nnz_cap = nnz;
+  bm->p_cap = masks ? n_part : 0;
   Layout L;
   size_t o_kv = L.add<int>(nnz), o_kd = L.add<uint8_t>(nnz), o_pi = L.add<int>(nnz), o_qi = L.add<int>(nnz),
          o_kt = L.add<uint8_t>(nnz), o_pt = L.add<int>(nnz);
-  size_t o_mr = masks ? L.add<uint32_t>((size_t)bm->n_partial * 512) : 0;
-  size_t o_mc = masks ? L.add<uint32_t>((size_t)bm->n_partial * 512) : 0;
+  size_t o_mr = masks ? L.add<uint32_t>((size_t)n_part * 512) : 0;
+  size_t o_mc = masks ? L.add<uint32_t>((size_t)n_part * 512) : 0;
   int rc = pool_alloc(&bm->mem_lists, L.off, bm->device, s);
   if (rc) return rc;
   bm->kv_idx = at<int>(bm->mem_lists, o_kv);
@@ -602,9 +767,21 @@ int alloc_lists(pt_blockmap* bm, cudaStream_t s) {
 // Shared tail of the builders: given tok, node_of and node tables on the
 // device, classify, count, list, order and mask.  Synchronises the stream
 // once (to size the lists); everything after that is asynchronous.
-int finish_map(pt_blockmap* bm, cudaStream_t s) {
+int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
   const int nq = bm->nq, nk = bm->nk, dev = bm->device;
   const long long ntiles = (long long)nq * nk;
+  // Causal bound on the non-empty tiles: q tile i meets kv blocks j with
+  // j * BN <= its last row.  With a bound on the partial tiles as well, the
+  // lists are allocated at the bounds and nothing waits for the device.
+  int64_t nnz_bound = 0;
+  for (int i = 0; i < nq; ++i) {
+    const long long qlast = std::min<long long>((long long)(i + 1) * bm->BM, bm->T) - 1;
+    nnz_bound += std::min<long long>(nk, qlast / bm->BN + 1);
+  }
+  const bool tiles128 = bm->BM == 128 && bm->BN == 128;
+  const int64_t p_bound_c = std::min<int64_t>(p_bound, nnz_bound);
+  const bool lazy = tiles128 && p_bound >= 0 &&
+                    nnz_bound * 18 + (int64_t)p_bound_c * 4096 <= ((int64_t)1 << 30);
   void* tmpA = nullptr;
   void* tmpB = nullptr;
   int rc = 0;
@@ -644,41 +821,56 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
       }
     }
     if (rc) break;
-    // the one synchronisation of the build: list sizes to the host
-    bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * ncnt));
-    if (!bm->h_counts) {
-      rc = 5;
-      break;
+    int64_t nnz_alloc, p_alloc;
+    if (lazy) {
+      // list sizes to pinned staging behind an event; read on first use
+      PinnedSlot sl;
+      if ((rc = pinned_acquire(dev, sizeof(int) * ncnt, &sl))) break;
+      bm->counts_host = sl.host;
+      bm->counts_cap = sl.cap;
+      bm->counts_ev = sl.ev;
+      if (cudaMemcpyAsync(sl.host, counters, sizeof(int) * ncnt, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+          cudaEventRecord(sl.ev, s) != cudaSuccess) {
+        set_error("block map: copy of the list sizes failed");
+        rc = 3;
+        break;
+      }
+      bm->counts_ready = false;
+      nnz_alloc = nnz_bound;
+      p_alloc = p_bound_c;
+    } else {
+      // the one synchronisation of the build: list sizes to the host
+      bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * ncnt));
+      if (!bm->h_counts) {
+        rc = 5;
+        break;
+      }
+      if ((rc = download_sync(bm->h_counts, counters, sizeof(int) * ncnt, dev, s))) break;
+      bm->h_row_cnt = bm->h_counts + 4;
+      bm->h_col_cnt = bm->h_row_cnt + nq;
+      int64_t nnz_h = 0;
+      for (int i = 0; i < nq; ++i) nnz_h += bm->h_row_cnt[i];
+      bm->nnz = nnz_h;
+      bm->n_full = bm->h_counts[0];
+      bm->n_partial = bm->nnz - bm->n_full;
+      bm->counts_ready = true;
+      nnz_alloc = bm->nnz;
+      p_alloc = bm->n_partial;
     }
-    if (cudaMemcpyAsync(bm->h_counts, counters, sizeof(int) * ncnt, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
-      rc = 3;
-      break;
-    }
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) {
-      set_error("block map build failed: %s", cudaGetErrorString(e));
-      rc = 3;
-      break;
-    }
-    bm->h_row_cnt = bm->h_counts + 4;
-    bm->h_col_cnt = bm->h_row_cnt + nq;
-    int64_t nnz_h = 0;
-    for (int i = 0; i < nq; ++i) nnz_h += bm->h_row_cnt[i];
-    bm->nnz = nnz_h;
-    bm->n_full = bm->h_counts[0];
-    bm->n_partial = bm->nnz - bm->n_full;
-    if ((rc = alloc_lists(bm, s))) break;
-    if (ntiles > 0 && bm->nnz > 0) {
+    if ((rc = alloc_lists(bm, nnz_alloc, p_alloc, s))) break;
+    if (ntiles > 0 && nnz_alloc > 0) {
       ProfScope ps(s, "blockmap_lists");  // the lists and the partial tiles' masks
-      if ((rc = pool_alloc(&tmpB, sizeof(int2) * (size_t)std::max<int64_t>(bm->n_partial, 1), dev, s))) break;
+      if ((rc = pool_alloc(&tmpB, sizeof(int2) * (size_t)std::max<int64_t>(p_alloc, 1), dev, s))) break;
       int2* slot_tile = static_cast<int2*>(tmpB);
       k_fill_rows<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, bm->q_ptr, prow_ptr, bm->kv_idx, bm->kind,
-                                                         bm->pidx, slot_tile);
+                                                         bm->pidx, slot_tile, (long long)p_alloc);
       k_fill_cols<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, bm->k_ptr, bm->q_idx, bm->kindT, bm->q_ptr,
                                                          bm->kv_idx, bm->pidx, bm->pidxT);
       PT_LAUNCHED(2);
       if (bm->mask_rows) {
-        k_masks<<<(unsigned)bm->n_partial, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
+        const long long grid = std::min<long long>(p_alloc, (long long)num_sms(dev) * 16);
+        k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, -1LL,
+                                               bm->q_ptr + nq, counters, (long long)bm->p_cap);
         PT_LAUNCHED(1);
       }
     }
@@ -690,8 +882,55 @@ int finish_map(pt_blockmap* bm, cudaStream_t s) {
 
 }  // namespace
 
+std::mutex g_counts_mu;
+
+int ensure_counts(const pt_blockmap* cbm) {
+  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the host copy of the sizes is filled in lazily
+  std::lock_guard<std::mutex> lk(g_counts_mu);
+  if (bm->counts_ready) return 0;
+  cudaEvent_t ev = static_cast<cudaEvent_t>(bm->counts_ev);
+  cudaError_t e = cudaEventSynchronize(ev);
+  if (e != cudaSuccess) {
+    set_error("block map build failed: %s", cudaGetErrorString(e));
+    return 3;
+  }
+  const size_t ncnt = (size_t)4 + bm->nq + bm->nk;
+  bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * ncnt));
+  if (!bm->h_counts) return 5;
+  std::memcpy(bm->h_counts, bm->counts_host, sizeof(int) * ncnt);
+  PinnedSlot sl;
+  sl.host = bm->counts_host;
+  sl.cap = bm->counts_cap;
+  sl.ev = ev;
+  pinned_release(bm->device, sl);
+  bm->counts_host = nullptr;
+  bm->counts_ev = nullptr;
+  bm->h_row_cnt = bm->h_counts + 4;
+  bm->h_col_cnt = bm->h_row_cnt + bm->nq;
+  int64_t nnz = 0;
+  for (int i = 0; i < bm->nq; ++i) nnz += bm->h_row_cnt[i];
+  bm->nnz = nnz;
+  bm->n_full = bm->h_counts[0];
+  bm->n_partial = nnz - bm->n_full;
+  bm->counts_ready = true;
+  if (bm->nnz > bm->nnz_cap || bm->n_partial > bm->p_cap) {
+    set_error("block map: %lld list entries and %lld partial tiles exceed the allocation's bounds (%lld, %lld)",
+              (long long)bm->nnz, (long long)bm->n_partial, (long long)bm->nnz_cap, (long long)bm->p_cap);
+    return 3;
+  }
+  return 0;
+}
+
 void free_map(pt_blockmap* bm) {
   if (!bm) return;
+  if (bm->counts_host) {  // sizes never read: the copy may still be in flight
+    cudaEventSynchronize(static_cast<cudaEvent_t>(bm->counts_ev));
+    PinnedSlot sl;
+    sl.host = bm->counts_host;
+    sl.cap = bm->counts_cap;
+    sl.ev = static_cast<cudaEvent_t>(bm->counts_ev);
+    pinned_release(bm->device, sl);
+  }
   pool_free(bm->bwd_mem, bm->stream);
   pool_free(bm->dq_mem, bm->stream);
   std::free(bm->h_dq_empty);
@@ -791,36 +1030,37 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
       for (auto it = ch[u].rbegin(); it != ch[u].rend(); ++it) stack.push_back(*it);
     }
   }
+  // A partial 128 x 128 tile has its q rows or its kv columns in a 128-token
+  // tile that holds a node boundary (or the end of the sequence), or lies on
+  // the diagonal: a tile whose rows all belong to one node and whose columns
+  // all belong to one node is uniform off the diagonal.  That bounds the
+  // partial tiles without waiting for the device.
+  int64_t p_bound = -1;
+  if (BM == 128 && BN == 128) {
+    const long long nt = (T + 127) / 128;
+    std::vector<char> split((size_t)nt, 0);
+    for (int i = 0; i < N; ++i)
+      if (node_lengths[i] > 0 && start[i] % 128 != 0) split[(size_t)(start[i] / 128)] = 1;
+    if (T % 128 != 0 && nt > 0) split[(size_t)nt - 1] = 1;
+    long long m = 0;
+    for (char c : split) m += c;
+    p_bound = 2 * m * nt + nt;
+  }
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, N, s, &bm);
   if (rc) return rc;
   bm->n_nodes = N;
-  void* dtab = nullptr;
   do {
-    // one upload of start | end | parent | tin | tout; the first three are
-    // then copied into the map on the device
-    if ((rc = pool_alloc(&dtab, sizeof(int) * (size_t)5 * std::max(N, 1), bm->device, s))) break;
-    if (N > 0) {
-      if ((rc = upload(dtab, tab.data(), sizeof(int) * (size_t)5 * N, bm->device, s))) break;
-      const int* d = static_cast<const int*>(dtab);
-      if (cudaMemcpyAsync(bm->node_start, d, sizeof(int) * N, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
-          cudaMemcpyAsync(bm->node_end, d + N, sizeof(int) * N, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
-          cudaMemcpyAsync(bm->parent, d + 2 * (size_t)N, sizeof(int) * N, cudaMemcpyDeviceToDevice, s) !=
-              cudaSuccess) {
-        set_error("block map: device copy of node tables failed");
-        rc = 3;
-        break;
-      }
-    }
+    // one upload of start | end | parent | tin | tout into the map's node tables
+    if (N > 0 && (rc = upload(bm->node_start, tab.data(), sizeof(int) * (size_t)5 * N, bm->device, s))) break;
     if (bm->tpad > 0) {
-      int* d_tin = static_cast<int*>(dtab) + 3 * (size_t)N;
+      const int* d_tin = bm->node_start + 3 * (size_t)N;
       k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>((int)T, bm->tpad, N, bm->node_end, d_tin, d_tin + N,
                                                            bm->tok, bm->node_of);
       PT_LAUNCHED(1);
     }
-    rc = finish_map(bm, s);
+    rc = finish_map(bm, s, p_bound);
   } while (0);
-  pool_free(dtab, s);
   if (rc) {
     free_map(bm);
     return rc;
@@ -893,7 +1133,7 @@ int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int3
       k_seg_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>(T, bm->tpad, bm->node_of, tin, tout, bm->tok);
       PT_LAUNCHED(1);
     }
-    rc = finish_map(bm, s);
+    rc = finish_map(bm, s, -1);
   } while (0);
   pool_free(tmp, s);
   if (rc) {
@@ -945,7 +1185,8 @@ int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out) {
     bm->h_col_cnt = bm->h_row_cnt + nq;
     for (int i = 0; i < nq; ++i) bm->h_row_cnt[i] = nk;
     for (int j = 0; j < nk; ++j) bm->h_col_cnt[j] = nq;
-    if ((rc = alloc_lists(bm, s))) break;
+    bm->counts_ready = true;
+    if ((rc = alloc_lists(bm, n, n, s))) break;
     if ((rc = pool_alloc(&tmp, sizeof(int2) * (size_t)std::max<long long>(n, 1), bm->device, s))) break;
     int2* slot_tile = static_cast<int2*>(tmp);
     long long cnt = std::max<long long>(n, std::max(nq, nk) + 1);
@@ -953,7 +1194,9 @@ int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out) {
                                                                 bm->q_idx, bm->kindT, bm->pidx, bm->pidxT, slot_tile);
     PT_LAUNCHED(1);
     if (bm->mask_rows && n > 0) {
-      k_masks<<<(unsigned)n, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols);
+      const long long grid = std::min<long long>(n, (long long)num_sms(bm->device) * 16);
+      k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, n, nullptr,
+                                             nullptr, n);
       PT_LAUNCHED(1);
     }
     // every row has the same length: natural order

@@ -1610,6 +1610,7 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
               "(call pt_blockmap_prepare_bwd first)");
     return 1;
   }
+  if (int rc = ensure_counts(bm)) return rc;
   const int nk = bm->nk;
   long long total = 0;
   for (int j = 0; j < nk; ++j) total += (long long)g * bm->h_col_cnt[j] * Hkv;
@@ -1709,6 +1710,7 @@ int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, 
     set_error("block map's dQ work lists are not prepared for this head count (call pt_blockmap_prepare_bwd first)");
     return 1;
   }
+  if (int rc = ensure_counts(bm)) return rc;
   const int nq = bm->nq;
   std::vector<int4> items;
   std::vector<int> empty;
@@ -1792,7 +1794,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       rc = reserve_smem(k_bwd_dq<D>, DqL<D>::BYTES, dev, set_dq);
   }
   if (rc) return rc;
-  if (bm->n_partial > 0 && (!bm->mask_rows || !bm->mask_cols)) {
+  if (masks_missing(bm)) {
     set_error("backward kernel: block map has no tile masks");
     return 1;
   }
@@ -1900,7 +1902,7 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   if (!rc) rc = reserve_smem(k_bwd_wide<WIDE_DK>, WideCfg<WIDE_DK>::BYTES, dev, set_k);
   if (!rc) rc = reserve_smem(k_bwd_wide<WIDE_DQ>, WideCfg<WIDE_DQ>::BYTES, dev, set_q);
   if (rc) return rc;
-  if (bm->n_partial > 0 && (!bm->mask_rows || !bm->mask_cols)) {
+  if (masks_missing(bm)) {
     set_error("backward kernel: block map has no tile masks");
     return 1;
   }

@@ -463,6 +463,21 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         const float m_blk = mx * p.scale_log2;
         const bool grow = m_blk > m_use + kRescaleThreshold;
         const float m_new = grow ? m_blk : m_use;
+        // P of this block against the new reference first: the O rescale
+        // below then holds only the packed P, not the 128 scores, and the
+        // exponentials overlap the PV still in flight
+        const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+        float r8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) r8[k] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float p0 = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -ref), c);
+          const float p1 = ex2_mix(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -ref), c + 1);
+          r8[(c >> 1) & 7] += p0 + p1;
+          sr[c >> 1] = pack_bf16(p0, p1);
+        }
+        const float l_blk = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
         if (C::OVL && u >= 1) {
           // PV of the previous block must be done: it reads the P columns
           // written below and accumulates into the O a rescale touches
@@ -500,18 +515,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
           l *= alpha;
         }
         m_use = m_new;
-        const float ref = (m_use == -INFINITY) ? 0.f : m_use;
-        float r8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) r8[k] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float p0 = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -ref), c);
-          const float p1 = ex2_mix(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -ref), c + 1);
-          r8[(c >> 1) & 7] += p0 + p1;
-          sr[c >> 1] = pack_bf16(p0, p1);
-        }
-        l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+        l += l_blk;
         const uint32_t pb = C::OVL ? tl + C::TM_P + h * 64 : sb;  // P: own columns, or over S
         tmem_st32(pb + 0, sr + 0);
         tmem_st32(pb + 32, sr + 32);
@@ -583,7 +587,7 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
     }
     attr_set[dev] = 1;
   }
-  if (bm->n_partial > 0 && !bm->mask_rows) {
+  if (masks_missing(bm)) {
     set_error("forward kernel: block map has no tile masks");
     return 1;
   }

@@ -56,10 +56,19 @@ struct pt_blockmap {
   int32_t* pidxT;       // [nnz] mask slot of each kv-major entry, -1 when full
   uint32_t* mask_rows;  // [n_partial][128 q rows][4 words]: bit c = keep(row, kv column c)
   uint32_t* mask_cols;  // [n_partial][128 kv columns][4 words]: bit r = keep(q row r, column)
-  // host copies of the list lengths (one allocation: 4 counters | rows | columns)
+  // host copies of the list lengths (one allocation: 4 counters | rows | columns),
+  // valid once counts_ready.  A build that does not wait for the device leaves
+  // them in pinned staging behind counts_ev; pt::ensure_counts fills them in
+  // (and nnz, n_full, n_partial) on first use.
   int* h_counts;
   int* h_row_cnt;  // [nq]
   int* h_col_cnt;  // [nk]
+  bool counts_ready;
+  void* counts_host;  // pinned staging (until counts_ready)
+  size_t counts_cap;
+  void* counts_ev;    // cudaEvent_t recorded after the copy to counts_host
+  int64_t nnz_cap;    // list entries allocated (>= nnz)
+  int64_t p_cap;      // mask slots allocated (>= n_partial)
   // backward work items of the kv-major kernel, cached for one head layout
   void* bwd_mem;
   int bwd_g, bwd_hkv, bwd_max_slots, bwd_n_items, bwd_n_splits, bwd_n_slots, bwd_grid, bwd_sms;
@@ -100,6 +109,15 @@ struct ProfScope {
   const char* name;
   void* end_event;
 };
+
+// Host list lengths of a map: waits for the build's copy if it has not
+// arrived yet.  Returns a PT_* status code (pt_blockmap.cu).
+int ensure_counts(const pt_blockmap* bm);
+
+// True when the map could have partial tiles but carries no masks.
+inline bool masks_missing(const pt_blockmap* bm) {
+  return !bm->mask_rows && (bm->counts_ready ? bm->n_partial > 0 : bm->p_cap > 0);
+}
 
 // Stream-ordered device memory from the library's private pool, and pinned
 // staging for small host-to-device uploads (pt_blockmap.cu).
