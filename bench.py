@@ -286,10 +286,16 @@ def main():
     torch.cuda.synchronize()
     launches0 = pt.launch_count()
     pt.profile_reset()
-    pt.profile_enable(True)
+    # the step time: no events inside the step (an event between two kernels
+    # costs the launch overlap, about 3 us per boundary)
     times = timed(args.steps, step)
-    pt.profile_enable(False)
     launches = pt.launch_count() - launches0
+    torch.cuda.synchronize()
+    # per-kernel durations: the same K steps again, each kernel bracketed by
+    # CUDA events on its stream
+    pt.profile_enable(True)
+    timed(args.steps, step)
+    pt.profile_enable(False)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -371,7 +377,8 @@ def main():
                        "useful_pairs_per_head": pairs, "useful_tflop_per_step": flops_step / 1e12,
                        "tiles": "128x128", "l2": "flushed before every step (256 MB write, untimed)",
                        "parallelism": f"replicas x{world}"},
-            "kernels": kernels, "roofline": roofline, "dense_masked": dense, "e2e": e2e,
+            "kernels": kernels, "kernel_timing": "second pass of the same steps with an event pair per kernel",
+            "roofline": roofline, "dense_masked": dense, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

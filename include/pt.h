@@ -292,13 +292,15 @@ pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv
 pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cudaStream_t stream);
 
 /* Optional per-kernel timing, for benchmarks and profiling.  While enabled,
- * each kernel launch is bracketed by two CUDA events on its stream (a few
- * microseconds of overhead per launch); disabled (the default) costs one
- * branch.  pt_profile_read synchronises the recorded events and returns the
- * number of launches and their summed duration for one kernel name:
- * "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dq", "bwd_simt",
- * "blockmap_classify" (the whole tail of a block-map build).
- * pt_profile_reset drops every record. */
+ * each kernel launch is bracketed by two CUDA events on its stream, taken
+ * from a per-device pool that enabling stocks with 1024 events; disabled
+ * (the default) costs one branch.  pt_profile_read synchronises the recorded
+ * events and returns the number of launches and their summed duration for
+ * one scope name: "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
+ * "bwd_dkdv_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt",
+ * "blockmap_classify" (tile classes, list sizes, orders) and
+ * "blockmap_lists" (lists and masks).  pt_profile_reset drops every record
+ * (its events go back to the pool once they have completed). */
 void pt_profile_enable(int on);
 pt_status pt_profile_read(const char* kernel, int64_t* launches, double* total_ms);
 void pt_profile_reset(void);

@@ -34,26 +34,47 @@ const char* g_err_ptr() { return g_err; }
 uint64_t launches() { return g_launches.load(std::memory_order_relaxed); }
 
 namespace {
+struct ProfPair {
+  cudaEvent_t first, second;
+  int dev;
+};
 struct ProfRecord {
-  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pairs;
+  std::vector<ProfPair> pairs;
 };
 std::mutex g_prof_mu;
 std::atomic<bool> g_prof_on{false};
 std::map<std::string, ProfRecord> g_prof;
+// Timing events are recycled, per device: creating two per scope costs the
+// host more than the launches they bracket.
+constexpr int kProfDev = 64;
+std::vector<cudaEvent_t> g_ev_free[kProfDev];
+
+// Caller holds g_prof_mu.
+bool take_event(int dev, cudaEvent_t* e) {
+  if (dev < 0 || dev >= kProfDev) return false;
+  if (!g_ev_free[dev].empty()) {
+    *e = g_ev_free[dev].back();
+    g_ev_free[dev].pop_back();
+    return true;
+  }
+  return cudaEventCreate(e) == cudaSuccess;
+}
 }  // namespace
 
 ProfScope::ProfScope(cudaStream_t s, const char* n) : stream(s), name(n), end_event(nullptr) {
   if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  int dev = 0;
+  cudaGetDevice(&dev);
   cudaEvent_t a, b;
-  if (cudaEventCreate(&a) != cudaSuccess) return;
-  if (cudaEventCreate(&b) != cudaSuccess) {
-    cudaEventDestroy(a);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!take_event(dev, &a)) return;
+  if (!take_event(dev, &b)) {
+    g_ev_free[dev].push_back(a);
     return;
   }
   cudaEventRecord(a, s);
   end_event = b;
-  std::lock_guard<std::mutex> lk(g_prof_mu);
-  g_prof[name].pairs.emplace_back(a, b);
+  g_prof[name].pairs.push_back(ProfPair{a, b, dev});
 }
 
 ProfScope::~ProfScope() {
@@ -400,7 +421,20 @@ pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cud
   return as_status(pt::exp2_probe(x, y, n, method, stream));
 }
 
-void pt_profile_enable(int on) { pt::g_prof_on.store(on != 0); }
+void pt_profile_enable(int on) {
+  if (on) {  // stock the current device's event pool before the scopes need it
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(pt::g_prof_mu);
+    if (dev >= 0 && dev < pt::kProfDev)
+      while (pt::g_ev_free[dev].size() < 1024) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) break;
+        pt::g_ev_free[dev].push_back(e);
+      }
+  }
+  pt::g_prof_on.store(on != 0);
+}
 
 pt_status pt_profile_read(const char* kernel, int64_t* launches, double* total_ms) {
   if (!kernel) {
@@ -432,8 +466,15 @@ void pt_profile_reset(void) {
   std::lock_guard<std::mutex> lk(pt::g_prof_mu);
   for (auto& kv : pt::g_prof)
     for (auto& pr : kv.second.pairs) {
-      cudaEventDestroy(pr.first);
-      cudaEventDestroy(pr.second);
+      // an event back to its device's pool once its record has completed
+      cudaEventSynchronize(pr.second);
+      if (pr.dev >= 0 && pr.dev < pt::kProfDev) {
+        pt::g_ev_free[pr.dev].push_back(pr.first);
+        pt::g_ev_free[pr.dev].push_back(pr.second);
+      } else {
+        cudaEventDestroy(pr.first);
+        cudaEventDestroy(pr.second);
+      }
     }
   pt::g_prof.clear();
 }
