@@ -250,6 +250,41 @@ pt_status pt_attn_bwd_noalloc(const void* dO, const void* Q, const void* K, cons
 /* Capacity in bytes of the built-in scratch array of pt_attn_bwd_noalloc. */
 size_t pt_bwd_noalloc_max_scratch_bytes(void);
 
+/* ---------------------------------------------------------------------------
+ * pt_hoststep -- forward and backward from host memory, one step per call.
+ *
+ * Passage: "prefix_grouper_kernel.py", flex_shared_prefix_attention runs on
+ * tensors already on the GPU; a training step still moves each batch's
+ * inputs in and its gradients out.  This object holds two device copies of
+ * Q, K, V, dO, O, LSE, dQ, dK, dV (and one backward workspace) and
+ * alternates between them, so one call's uploads and the previous call's
+ * downloads overlap the kernels in between.
+ *
+ * pt_hoststep_create: buffers for one shape (layouts as pt_attn_fwd /
+ *   pt_attn_bwd: Q, dO, dQ [T, Hq, D]; K, V, dK, dV [T, Hkv, D]) on the
+ *   current device; two non-blocking copy streams of its own.  Errors:
+ *   PT_ERR_INVALID_ARG for a bad dtype or sizes, PT_ERR_NOMEM.
+ * pt_hoststep_run: hQ, hK, hV, hdO (host, read) and hdQ, hdK, hdV (host,
+ *   written) are the caller's; pinned memory (cudaHostAlloc or registered)
+ *   gives the overlap, pageable memory works but each copy then blocks.  The
+ *   uploads go on the object's upload stream, the forward and backward on
+ *   `stream` (after the uploads; the map must be built for the same T), the
+ *   downloads on the object's download stream after the kernels.  Returns
+ *   once everything is queued: the host buffers must stay untouched until
+ *   pt_hoststep_sync's stream point has been reached.  Errors: as
+ *   pt_attn_fwd / pt_attn_bwd, PT_ERR_INVALID_ARG for NULL pointers or a
+ *   map of another T.
+ * pt_hoststep_sync: makes `stream` wait for every download queued so far
+ *   (synchronise the stream, or record an event on it, to wait on the host).
+ * pt_hoststep_free: waits for the object's copies and frees it.
+ * ------------------------------------------------------------------------- */
+typedef struct pt_hoststep pt_hoststep;
+pt_status pt_hoststep_create(pt_dtype dtype, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, pt_hoststep** out);
+pt_status pt_hoststep_run(pt_hoststep* h, const void* hQ, const void* hK, const void* hV, const void* hdO,
+                          float scale, const pt_blockmap* bm, void* hdQ, void* hdK, void* hdV, cudaStream_t stream);
+pt_status pt_hoststep_sync(pt_hoststep* h, cudaStream_t stream);
+void pt_hoststep_free(pt_hoststep* h);
+
 /* Synchronise the stream, then return and clear the device status word:
  * PT_ERR_TIMEOUT if an in-kernel wait ran out since the last check, PT_ERR_CUDA
  * if the stream reported an error, else PT_OK. */

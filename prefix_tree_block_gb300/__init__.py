@@ -16,7 +16,7 @@ import threading
 from typing import Optional, Tuple
 
 __all__ = [
-    "PTError", "BlockMap", "load_library", "build_blockmap_tree", "build_blockmap_seg",
+    "PTError", "BlockMap", "HostStep", "load_library", "build_blockmap_tree", "build_blockmap_seg",
     "attn_fwd", "attn_bwd", "bwd_workspace_bytes", "sync_status", "launch_count", "LIB_PATH",
     "profile_enable", "profile_read", "profile_reset", "attn_bwd_noalloc",
 ]
@@ -66,6 +66,9 @@ def load_library(path: Optional[str] = None):
             "pt_blockmap_prepare_bwd": [vp, i32, i32, i32, vp],
             "pt_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, ctypes.c_int, i32, i32, i32, i32, f32, vp, vp, vp, vp,
                                     vp],
+            "pt_hoststep_create": [ctypes.c_int, i32, i32, i32, i32, pp],
+            "pt_hoststep_run": [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp],
+            "pt_hoststep_sync": [vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -73,6 +76,8 @@ def load_library(path: Optional[str] = None):
             fn.restype = ctypes.c_int
         lib.pt_blockmap_free.argtypes = [vp]
         lib.pt_blockmap_free.restype = None
+        lib.pt_hoststep_free.argtypes = [vp]
+        lib.pt_hoststep_free.restype = None
         lib.pt_bwd_workspace_bytes.argtypes = [i32, i32, i32]
         lib.pt_bwd_workspace_bytes.restype = sz
         lib.pt_last_error.argtypes = []
@@ -349,3 +354,48 @@ def profile_read(kernel: str):
 
 def profile_reset():
     load_library().pt_profile_reset()
+
+
+class HostStep:
+    """Forward and backward from pinned host tensors, double-buffered on the
+    device so that consecutive run() calls overlap their copies with the
+    kernels (pt_hoststep_*).  Host tensors: Q, dO, dQ [T, Hq, D]; K, V, dK,
+    dV [T, Hkv, D], contiguous, of the dtype given at creation."""
+
+    def __init__(self, dtype, T: int, Hq: int, Hkv: int, D: int):
+        import torch
+
+        self._lib = load_library()
+        self._dt = dtype
+        self._code = PT_BF16 if dtype == torch.bfloat16 else PT_F32 if dtype == torch.float32 else None
+        if self._code is None:
+            raise TypeError("HostStep: dtype must be torch.bfloat16 or torch.float32")
+        self.shape = (T, Hq, Hkv, D)
+        out = ctypes.c_void_p()
+        _check(self._lib.pt_hoststep_create(self._code, T, Hq, Hkv, D, ctypes.byref(out)))
+        self._h = out
+
+    def run(self, Q, K, V, dO, bm: BlockMap, dQ, dK, dV, scale: float = 0.0, stream=None):
+        """Queue one step; the host outputs are valid after sync() and a
+        synchronisation of the stream."""
+        T, Hq, Hkv, D = self.shape
+        for t, h in ((Q, Hq), (dO, Hq), (dQ, Hq), (K, Hkv), (V, Hkv), (dK, Hkv), (dV, Hkv)):
+            if t.is_cuda or t.dtype != self._dt or tuple(t.shape) != (T, h, D) or not t.is_contiguous():
+                raise ValueError("HostStep.run: host tensors of the creation dtype and shape expected")
+        _check(self._lib.pt_hoststep_run(self._h, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), float(scale), bm.handle,
+                                         _ptr(dQ), _ptr(dK), _ptr(dV), ctypes.c_void_p(_stream(stream))))
+
+    def sync(self, stream=None):
+        """Make the stream wait for every download queued so far."""
+        _check(self._lib.pt_hoststep_sync(self._h, ctypes.c_void_p(_stream(stream))))
+
+    def free(self):
+        if self._h is not None and self._h.value:
+            self._lib.pt_hoststep_free(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
