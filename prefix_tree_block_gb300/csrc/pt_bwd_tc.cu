@@ -53,35 +53,49 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------
 // 1. preprocess
 // ---------------------------------------------------------------------------
-// One group of D/8 threads per (row, head): 16-byte loads of dO and O.
+// A block takes 8 tokens x all heads: D/8 threads per (token, head) read
+// dO and O in their stored (token-major) order with 16-byte loads; the
+// per-row sums go through shared memory so that Delta and LSE2, head-major
+// [Hq][Tpad], are written (and LSE read) a 32-byte sector at a time.
+constexpr int kPrepTokens = 8;
 template <int D>
-__global__ void k_bwd_prep(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O,
-                           const float* __restrict__ LSE, int T, int Tpad, int Hq, float* __restrict__ delta,
-                           float* __restrict__ lse2) {
-  constexpr int TPR = D / 8;  // threads per row
-  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = gid / TPR;  // over Hq * Tpad, head-major
-  const int sub = (int)(gid % TPR);
-  if (row >= (long long)Hq * Tpad) return;
-  const int h = (int)(row / Tpad), q = (int)(row % Tpad);
-  float s = 0.f;
-  if (q < T) {
-    const uint4 a = *reinterpret_cast<const uint4*>(dO + ((size_t)q * Hq + h) * D + sub * 8);
-    const uint4 b = *reinterpret_cast<const uint4*>(O + ((size_t)q * Hq + h) * D + sub * 8);
-    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+__global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restrict__ dO,
+                                                  const __nv_bfloat16* __restrict__ O, const float* __restrict__ LSE,
+                                                  int T, int Tpad, int Hq, float* __restrict__ delta,
+                                                  float* __restrict__ lse2) {
+  constexpr int TPR = D / 8;  // threads per (token, head) row
+  extern __shared__ float sh_delta[];  // [kPrepTokens][Hq + 1]
+  const int q0 = blockIdx.x * kPrepTokens;
+  const int sub = threadIdx.x % TPR;
+  // rows is a multiple of 32 / TPR, the rows of one warp: a warp's lanes
+  // run the same trips, as the shuffles below need
+  const int rows = kPrepTokens * Hq;
+#pragma unroll 4
+  for (int r = threadIdx.x / TPR; r < rows; r += 256 / TPR) {
+    const int ql = r / Hq, h = r % Hq, q = q0 + ql;
+    float s = 0.f;
+    if (q < T) {
+      const uint4 a = *reinterpret_cast<const uint4*>(dO + ((size_t)q * Hq + h) * D + sub * 8);
+      const uint4 b = *reinterpret_cast<const uint4*>(O + ((size_t)q * Hq + h) * D + sub * 8);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float2 x = __bfloat1622float2(pa[k]), y = __bfloat1622float2(pb[k]);
-      s = fmaf(x.x, y.x, s);
-      s = fmaf(x.y, y.y, s);
+      for (int k = 0; k < 4; ++k) {
+        float2 x = __bfloat1622float2(pa[k]), y = __bfloat1622float2(pb[k]);
+        s = fmaf(x.x, y.x, s);
+        s = fmaf(x.y, y.y, s);
+      }
     }
-  }
 #pragma unroll
-  for (int o = TPR / 2; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o, TPR);
-  if (sub == 0) {
-    delta[row] = s;
-    float l = q < T ? LSE[(size_t)h * T + q] : -INFINITY;
+    for (int o = TPR / 2; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o, TPR);
+    if (sub == 0) sh_delta[ql * (Hq + 1) + h] = s;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows; i += 256) {
+    const int h = i / kPrepTokens, ql = i % kPrepTokens, q = q0 + ql;
+    const size_t row = (size_t)h * Tpad + q;  // q < Tpad: Tpad is a multiple of 128
+    delta[row] = sh_delta[ql * (Hq + 1) + h];
+    const float l = q < T ? LSE[(size_t)h * T + q] : -INFINITY;
     // rows that keep nothing (padding) get +inf so exp2(s - lse2) = 0
     lse2[row] = (l == -INFINITY) ? INFINITY : l * kLog2e;
   }
@@ -1803,9 +1817,14 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s))) return rc;
   const int Tpad = bm->nq * 128;
   {
-    const long long threads = (long long)Hq * Tpad * (D / 8);
+    const size_t sm = sizeof(float) * kPrepTokens * ((size_t)Hq + 1);
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(k_bwd_prep<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess) {
+      set_error("backward preprocess: %d heads need %zu bytes of shared memory", Hq, sm);
+      return 3;
+    }
     ProfScope ps(s, "bwd_prep");
-    k_bwd_prep<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+    k_bwd_prep<D><<<(unsigned)(Tpad / kPrepTokens), 256, sm, s>>>(
         static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
   }
   CUtensorMap mQ, mdO, mK, mV;
@@ -1912,9 +1931,14 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s))) return rc;
   const int Tpad = bm->nq * 128;
   {
-    const long long threads = (long long)Hq * Tpad * (D / 8);
+    const size_t sm = sizeof(float) * kPrepTokens * ((size_t)Hq + 1);
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(k_bwd_prep<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess) {
+      set_error("backward preprocess: %d heads need %zu bytes of shared memory", Hq, sm);
+      return 3;
+    }
     ProfScope ps(s, "bwd_prep");
-    k_bwd_prep<D><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+    k_bwd_prep<D><<<(unsigned)(Tpad / kPrepTokens), 256, sm, s>>>(
         static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
   }
   CUtensorMap mQ, mdO, mK, mV, mQh, mdOh, mKh, mVh;

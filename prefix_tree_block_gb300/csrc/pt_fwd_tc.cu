@@ -109,6 +109,11 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int w, int& tile
   }
 }
 
+// Item of CTA b in round r of a grid of G: rounds alternate direction over
+// the longest-first item order (boustrophedon), so no CTA takes the largest
+// item of every round.
+__device__ __forceinline__ int snake_item(int r, int b, int G) { return r * G + ((r & 1) ? G - 1 - b : b); }
+
 template <int NH>
 __host__ __device__ __forceinline__ int fwd_items(int nq, int Hq, int Hkv) {
   if (NH == 1) return nq * Hq;
@@ -192,7 +197,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     if (lane == 0) {
       uint32_t kc = 0, vc = 0, it = 0;
       bool ok = true, q_issued = false;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
+        const int w = snake_item(rr, blockIdx.x, gridDim.x);
+        if (w >= n_items) continue;
         int tile, h0, nh;
         decode_item<NH>(p, w, tile, h0, nh);
         const int e0 = p.q_ptr[tile], e1 = p.q_ptr[tile + 1];
@@ -291,7 +298,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
                  (!first || kk > 0));
       };
 
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
+        const int w = snake_item(rr, blockIdx.x, gridDim.x);
+        if (w >= n_items) continue;
         int tile, h0, nh;
         decode_item<NH>(p, w, tile, h0, nh);
         const int n = p.q_ptr[tile + 1] - p.q_ptr[tile];
@@ -398,7 +407,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     const uint32_t o_col = C::TM_O + h * D;
     uint32_t sc = 0, vc = 0, pvc = 0, itv = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+    for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
+      const int w = snake_item(rr, blockIdx.x, gridDim.x);
+      if (w >= n_items) continue;
       int tile, h0, nh;
       decode_item<NH>(p, w, tile, h0, nh);
       const int e0 = p.q_ptr[tile], n = p.q_ptr[tile + 1] - e0;
