@@ -37,6 +37,7 @@
 #include <cmath>
 #include <mutex>
 #include <queue>
+#include <type_traits>
 #include <vector>
 
 #include "pt_device.cuh"
@@ -516,18 +517,26 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld32(tS, sr);
           tmem_ld32(tS + 32, sr + 32);
           tmem_ld_wait();
+          const auto pmath = [&](auto masked) {
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 lv = l2[c4];
-            const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+            for (int c4 = 0; c4 < 16; ++c4) {
+              const float4 lv = l2[c4];
+              const float la[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int c = c4 * 4 + k;
-              const uint32_t word = c < 32 ? mk.x : mk.y;
-              float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
-              sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
+              for (int k = 0; k < 4; ++k) {
+                const int c = c4 * 4 + k;
+                const float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
+                if constexpr (decltype(masked)::value)
+                  sr[c] = __float_as_uint((((c < 32 ? mk.x : mk.y) >> (c & 31)) & 1u) ? pr : 0.f);
+                else
+                  sr[c] = __float_as_uint(pr);
+              }
             }
-          }
+          };
+          if (slot >= 0)
+            pmath(std::true_type{});
+          else
+            pmath(std::false_type{});
           pack64(sr, pk);
           tmem_st32(tS, pk);  // in place over this warpgroup's S^T columns
           tmem_st_wait();
@@ -810,12 +819,20 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&B->s_free);  // S and dP are in registers: the MMA may reuse them
+        if (slot >= 0) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const uint32_t word = c < 32 ? mk.x : mk.y;
-          float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
-          pr = ((word >> (c & 31)) & 1u) ? pr : 0.f;
-          dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - dl));
+          for (int c = 0; c < 64; ++c) {
+            const uint32_t word = c < 32 ? mk.x : mk.y;
+            float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
+            pr = ((word >> (c & 31)) & 1u) ? pr : 0.f;
+            dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - dl));
+          }
+        } else {  // full tile: no mask
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
+            dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - dl));
+          }
         }
         uint32_t pk[32];
         pack64(dr, pk);
