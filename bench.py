@@ -51,13 +51,12 @@ def useful_pairs(st) -> int:
 
 
 # DRAM bytes (read + write) per launch of the tensor-core kernels, from one
-# `ncu --set full` capture of the current kernels on each workload: see
-# profiles/kernels_grpo_batch_workload2.md and
-# profiles/kernels_long_prompt_grpo_workload3.md.  A kernel changed since its
+# `ncu --set full` capture of the current kernels on each workload (the
+# per-kernel counter summaries under profiles/).  A kernel changed since its
 # capture must be removed from this table (its traffic is then reported null).
 MEASURED_TRAFFIC = {
-    (2, "fwd_tc"): 35.2e6, (2, "bwd_dkdv"): 66.97e6, (2, "bwd_dq"): 65.63e6,
-    (3, "fwd_tc"): 953.9e6, (3, "bwd_dkdv"): 3011.5e6, (3, "bwd_dq"): 1196.4e6,
+    (2, "fwd_tc"): 35.24e6, (2, "bwd_dkdv"): 66.27e6, (2, "bwd_dq"): 65.55e6,
+    (3, "fwd_tc"): 943.7e6, (3, "bwd_dkdv"): 3020e6, (3, "bwd_dq"): 1204e6,
 }
 
 
@@ -315,7 +314,7 @@ def main():
 
     # ---- roofline of the dominant kernel -----------------------------------
     peak_tf, peak_gbs, peak_src = peaks()
-    per_launch_flops = {  # executed useful-pair flops of each kernel
+    per_launch_flops = {  # useful-pair flops of each kernel: 2D per pair and head for each of its products
         "fwd_tc": 4.0 * D * Hq * pairs,
         "bwd_dkdv": 8.0 * D * Hq * pairs,
         "bwd_dv": 4.0 * D * Hq * pairs,  # head_dim 256: S^T and dV
