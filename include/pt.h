@@ -118,6 +118,41 @@ pt_status pt_build_blockmap_seg(const int32_t* group_id, const int32_t* suffix_i
                                 pt_blockmap** out);
 
 /* ---------------------------------------------------------------------------
+ * pt_build_blockmap_draft -- block map of the draft-block (DFlash) mask.
+ *
+ * Passages: "support sequence packing in the Domino and JetSpec drafts" (the
+ * query side is the draft blocks only, the context is keys; a block's context
+ * prefix is restricted to its anchor's document, create_dflash_block_mask's
+ * anchor_positions / block_keep_mask / ctx_doc_id / anchor_doc_id) and the
+ * DFlash-family drafter PR (the visibility rule _draft_mask_mod: context
+ * before the block, a window counted from each query's real position,
+ * block-causal under causal in-block attention).
+ *
+ * Flat layout, T = ctx_len + n_blocks * block_size: the context tokens
+ * first, then block b's tokens at [ctx_len + b * block_size, ... + block_size).
+ * Block b's token k sits at real position anchors[b] + k.  Keep rule:
+ *   - context rows keep nothing (they are keys only);
+ *   - block b's token k keeps context key kv iff kv < anchors[b], and
+ *     ctx_doc[kv] == anchor_doc[b] when documents are given, and
+ *     (anchors[b] + k) - kv < window when window > 0;
+ *   - it keeps its own block's token k' always (causal == 0) or iff k' <= k
+ *     (causal != 0), and no other block;
+ *   - a block with block_keep[b] == 0 keeps nothing (its rows return 0).
+ * anchors [n_blocks] (host) in [0, ctx_len]; block_keep [n_blocks] (host) or
+ * NULL for all kept; ctx_doc [ctx_len] and anchor_doc [n_blocks] (host),
+ * both or neither; each document id must form one contiguous run of the
+ * context.  block_m = block_n = 128 (else PT_ERR_UNSUPPORTED): the kernels
+ * read the mask from the map's tile bitmasks.  The build synchronises the
+ * stream once.  Errors: PT_ERR_INVALID_ARG for negative sizes, block_size < 1,
+ * an anchor out of range, a document split into several runs or only one of
+ * the two document arrays.
+ * ------------------------------------------------------------------------- */
+pt_status pt_build_blockmap_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                                  const uint8_t* block_keep, int32_t causal, int32_t window,
+                                  const int32_t* ctx_doc, const int32_t* anchor_doc, int32_t block_m,
+                                  int32_t block_n, cudaStream_t stream, pt_blockmap** out);
+
+/* ---------------------------------------------------------------------------
  * pt_blockmap_dense -- the same tree with no tile skipping: every one of the
  * nq x nk tiles is marked partial, so the kernels evaluate the mask on every
  * pair of the T x T square.  This is the "dense masked O(T^2)" comparison the

@@ -17,6 +17,7 @@ from typing import Optional, Tuple
 
 __all__ = [
     "PTError", "BlockMap", "HostStep", "load_library", "build_blockmap_tree", "build_blockmap_seg",
+    "build_blockmap_draft",
     "attn_fwd", "attn_bwd", "bwd_workspace_bytes", "sync_status", "launch_count", "LIB_PATH",
     "profile_enable", "profile_read", "profile_reset", "attn_bwd_noalloc",
 ]
@@ -55,6 +56,7 @@ def load_library(path: Optional[str] = None):
             "pt_build_blockmap_tree": [vp, i32, vp, vp, i32, i32, i32, vp, pp],
             "pt_build_blockmap_seg": [vp, vp, i32, i32, i32, vp, pp],
             "pt_blockmap_dense": [vp, vp, pp],
+            "pt_build_blockmap_draft": [i32, i32, i32, vp, vp, i32, i32, vp, vp, i32, i32, vp, pp],
             "pt_blockmap_info": [vp, i32p, i32p, i32p, i32p, i32p, i64p, i64p],
             "pt_blockmap_export": [vp, vp, vp, vp, vp, vp, vp],
             "pt_blockmap_export_masks": [vp, vp, vp, vp, vp],
@@ -214,6 +216,26 @@ def build_blockmap_tree(node_lengths, path_ptr, path_nodes, block_m: int = 128, 
     _check(lib.pt_build_blockmap_tree(nl.ctypes.data if nl.size else None, int(nl.size), pp.ctypes.data,
                                       pn.ctypes.data if pn.size else None, int(pp.size - 1), int(block_m),
                                       int(block_n), ctypes.c_void_p(_stream(stream)), ctypes.byref(out)))
+    return BlockMap(out.value)
+
+
+def build_blockmap_draft(ctx_len: int, anchors, block_size: int, block_keep=None, causal: bool = False,
+                         window: int = 0, ctx_doc=None, anchor_doc=None, block_m: int = 128, block_n: int = 128,
+                         stream=None) -> BlockMap:
+    """Block map of the draft-block (DFlash) mask (pt_build_blockmap_draft):
+    context [ctx_len] then len(anchors) blocks of block_size tokens; host arrays."""
+    import numpy as np
+
+    lib = load_library()
+    an = np.ascontiguousarray(np.asarray(anchors, dtype=np.int32))
+    keep = None if block_keep is None else np.ascontiguousarray(np.asarray(block_keep, dtype=np.uint8))
+    cd = None if ctx_doc is None else np.ascontiguousarray(np.asarray(ctx_doc, dtype=np.int32))
+    ad = None if anchor_doc is None else np.ascontiguousarray(np.asarray(anchor_doc, dtype=np.int32))
+    ptr = lambda a: (a.ctypes.data if a.size else None) if a is not None else None
+    out = ctypes.c_void_p()
+    _check(lib.pt_build_blockmap_draft(int(ctx_len), int(an.size), int(block_size), ptr(an), ptr(keep), int(bool(causal)),
+                                       int(window), ptr(cd), ptr(ad), int(block_m), int(block_n),
+                                       ctypes.c_void_p(_stream(stream)), ctypes.byref(out)))
     return BlockMap(out.value)
 
 

@@ -227,6 +227,19 @@ pt_status pt_build_blockmap_seg(const int32_t* group_id, const int32_t* suffix_i
   return as_status(pt::build_seg(group_id, suffix_id, T, block_m, block_n, stream, out));
 }
 
+pt_status pt_build_blockmap_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                                  const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                                  const int32_t* anchor_doc, int32_t block_m, int32_t block_n, cudaStream_t stream,
+                                  pt_blockmap** out) {
+  if (!out) {
+    set_error("pt_build_blockmap_draft: NULL out");
+    return PT_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  return as_status(pt::build_draft(ctx_len, n_blocks, block_size, anchors, block_keep, causal, window, ctx_doc,
+                                   anchor_doc, block_m, block_n, stream, out));
+}
+
 pt_status pt_blockmap_dense(const pt_blockmap* src, cudaStream_t stream, pt_blockmap** out) {
   if (!src || !out) {
     set_error("pt_blockmap_dense: NULL argument");

@@ -14,6 +14,7 @@
 #include <cstring>
 #include <mutex>
 #include <numeric>
+#include <unordered_map>
 #include <vector>
 
 #include "pt_device.cuh"
@@ -453,6 +454,110 @@ __global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_
   }
 }
 
+// ---------------------------------------------------------------------------
+// draft-block form ("support sequence packing in the Domino and JetSpec
+// drafts" and the DFlash-family drafter PR: draft blocks attend to the context
+// before their anchor, optionally restricted to the anchor's document and to a
+// window counted from each query's real position, and to their own block,
+// bidirectionally or causally; context rows are keys only)
+// ---------------------------------------------------------------------------
+struct DraftParams {
+  int S, bs, causal, window;
+  const int4* blk;  // per block: kept context [x, y) before any window, anchor z, keep flag w
+};
+
+DraftParams draft_params(const pt_blockmap* bm) {
+  return DraftParams{bm->d_ctx, bm->d_bs, bm->d_causal, bm->d_window, static_cast<const int4*>(bm->d_blk)};
+}
+
+// Kept keys of row q: context [c0, c1) and its own block's [b0, b1) (empty
+// ranges for context rows and dropped blocks).
+__device__ __forceinline__ void draft_row(const DraftParams& d, int q, int& c0, int& c1, int& b0, int& b1) {
+  c0 = c1 = b0 = b1 = 0;
+  if (q < d.S) return;
+  const int b = (q - d.S) / d.bs, k = (q - d.S) % d.bs;
+  const int4 bl = d.blk[b];
+  if (!bl.w) return;
+  c0 = bl.x;
+  c1 = bl.y;
+  if (d.window > 0) c0 = max(c0, bl.z + k - d.window + 1);  // real position bl.z + k minus kv < window
+  if (c1 < c0) c1 = c0;
+  b0 = d.S + b * d.bs;
+  b1 = b0 + (d.causal ? k + 1 : d.bs);
+}
+
+// Tile classes and list sizes for a draft map: one warp per tile, kept pairs
+// counted per row from its two ranges (exact).
+__global__ void k_draft_classify(int T, int BM, int BN, int nq, int nk, DraftParams d, uint8_t* kinds, int* counters,
+                                 int* row_cnt, int* col_cnt, int* row_part) {
+  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= (long long)nq * nk) return;
+  const int i = (int)(w / nk), j = (int)(w % nk);
+  const long long q0 = (long long)i * BM, k0 = (long long)j * BN;
+  const long long k1 = k0 + BN < T ? k0 + BN : T;
+  const long long qend = q0 + BM < T ? q0 + BM : T;
+  long long kept = 0;
+  for (long long q = q0 + lane; q < qend; q += 32) {
+    int c0, c1, b0, b1;
+    draft_row(d, (int)q, c0, c1, b0, b1);
+    kept += overlap(c0, c1, k0, k1) + overlap(b0, b1, k0, k1);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
+  if (lane == 0) {
+    const bool in_range = (q0 + BM <= T) && (k0 + BN <= T);
+    const uint8_t kd = kept == 0 ? PT_KIND_EMPTY
+                                 : ((in_range && kept == (long long)BM * BN) ? PT_KIND_FULL : PT_KIND_PARTIAL);
+    kinds[w] = kd;
+    if (kd != PT_KIND_EMPTY) {
+      atomicAdd(&row_cnt[i], 1);
+      atomicAdd(&col_cnt[j], 1);
+      if (kd == PT_KIND_FULL)
+        atomicAdd(&counters[0], 1);
+      else
+        atomicAdd(&row_part[i], 1);
+    }
+  }
+}
+
+// Keep bitmasks of the partial tiles of a draft map (layout as k_masks):
+// a row's bits are its two ranges clipped to the tile; the column masks are
+// the transpose, one ballot per column over each warp's 32 rows.
+__global__ void k_draft_masks(int T, DraftParams d, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols,
+                              long long n_known, const int* nnz_total, const int* n_full, long long p_cap) {
+  const long long n_part = min(n_known >= 0 ? n_known : (long long)(*nnz_total - *n_full), p_cap);
+  const int r = threadIdx.x, lane = r & 31, wi = r >> 5;
+  for (long long s = blockIdx.x; s < n_part; s += gridDim.x) {
+    const int2 ij = slot_tile[s];
+    const int q0 = ij.x * 128, k0 = ij.y * 128, q = q0 + r;
+    const int kend = min(k0 + 128, T);
+    uint32_t row[4] = {0, 0, 0, 0};
+    if (q < T) {
+      int c0, c1, b0, b1;
+      draft_row(d, q, c0, c1, b0, b1);
+      int a = max(c0, k0), e = min(c1, kend);
+      if (a < e) set_bits(row, a - k0, e - k0);
+      a = max(b0, k0);
+      e = min(b1, kend);
+      if (a < e) set_bits(row, a - k0, e - k0);
+    }
+    reinterpret_cast<uint4*>(mask_rows)[(size_t)s * 128 + r] = make_uint4(row[0], row[1], row[2], row[3]);
+    uint32_t col[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      col[m] = 0;
+      for (int t = 0; t < 32; ++t) {
+        const uint32_t v = __ballot_sync(0xffffffffu, (row[m] >> t) & 1u);
+        if (t == lane) col[m] = v;
+      }
+    }
+    // lane holds kv column 32 m + lane, word wi (q rows 32 wi .. 32 wi + 31)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) mask_cols[((size_t)s * 128 + 32 * m + lane) * 4 + wi] = col[m];
+  }
+}
+
 // dense map: every tile partial; slot = row-major tile index
 __global__ void k_dense_lists(int nq, int nk, int* q_ptr, int* kv_idx, uint8_t* kind, int* k_ptr, int* q_idx,
                               uint8_t* kindT, int* pidx, int* pidxT, int2* slot_tile) {
@@ -807,9 +912,13 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
       }
       if (ntiles > 0) {
         long long threads = ntiles * 32;
-        k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
-                                                                     bm->node_start, bm->node_end, bm->parent, kinds,
-                                                                     counters, row_cnt, col_cnt, row_part);
+        if (bm->producer == PT_PRODUCER_DRAFT)
+          k_draft_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+              bm->T, bm->BM, bm->BN, nq, nk, draft_params(bm), kinds, counters, row_cnt, col_cnt, row_part);
+        else
+          k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
+                                                                       bm->node_start, bm->node_end, bm->parent,
+                                                                       kinds, counters, row_cnt, col_cnt, row_part);
         PT_LAUNCHED(1);
       }
       k_scan3<<<1, kScanBlock, 0, s>>>(row_cnt, nq, bm->q_ptr, col_cnt, nk, bm->k_ptr, row_part, nq, prow_ptr);
@@ -869,8 +978,13 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
       PT_LAUNCHED(2);
       if (bm->mask_rows) {
         const long long grid = std::min<long long>(p_alloc, (long long)num_sms(dev) * 16);
-        k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, -1LL,
-                                               bm->q_ptr + nq, counters, (long long)bm->p_cap);
+        if (bm->producer == PT_PRODUCER_DRAFT)
+          k_draft_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, draft_params(bm), slot_tile, bm->mask_rows,
+                                                       bm->mask_cols, -1LL, bm->q_ptr + nq, counters,
+                                                       (long long)bm->p_cap);
+        else
+          k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, -1LL,
+                                                 bm->q_ptr + nq, counters, (long long)bm->p_cap);
         PT_LAUNCHED(1);
       }
     }
@@ -923,6 +1037,7 @@ int ensure_counts(const pt_blockmap* cbm) {
 
 void free_map(pt_blockmap* bm) {
   if (!bm) return;
+  pool_free(bm->d_blk, bm->stream);
   if (bm->counts_host) {  // sizes never read: the copy may still be in flight
     cudaEventSynchronize(static_cast<cudaEvent_t>(bm->counts_ev));
     PinnedSlot sl;
@@ -1144,12 +1259,94 @@ int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int3
   return 0;
 }
 
+int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                const int32_t* anchor_doc, int32_t BM, int32_t BN, cudaStream_t s, pt_blockmap** out) {
+  if (ctx_len < 0 || n_blocks < 0 || block_size < 1 || window < 0 || (n_blocks > 0 && !anchors)) {
+    set_error("pt_build_blockmap_draft: negative length, block size < 1, negative window or null anchors");
+    return 1;
+  }
+  if ((ctx_doc == nullptr) != (anchor_doc == nullptr) || (ctx_doc && ctx_len > 0 && !ctx_doc)) {
+    set_error("pt_build_blockmap_draft: ctx_doc and anchor_doc must be given together");
+    return 1;
+  }
+  if (BM != 128 || BN != 128) {
+    set_error("pt_build_blockmap_draft: draft maps are built for 128 x 128 tiles only (got %d x %d)", BM, BN);
+    return 2;
+  }
+  const long long T = (long long)ctx_len + (long long)n_blocks * block_size;
+  if (T > INT_MAX / 2) {
+    set_error("pt_build_blockmap_draft: T = %lld too large", T);
+    return 1;
+  }
+  for (int b = 0; b < n_blocks; ++b)
+    if (anchors[b] < 0 || anchors[b] > ctx_len) {
+      set_error("pt_build_blockmap_draft: anchor %d of block %d outside [0, %d]", anchors[b], b, ctx_len);
+      return 1;
+    }
+  // documents: each id one contiguous run of the context
+  std::unordered_map<int32_t, std::pair<int32_t, int32_t>> runs;
+  if (ctx_doc) {
+    for (int32_t t = 0; t < ctx_len;) {
+      int32_t e = t + 1;
+      while (e < ctx_len && ctx_doc[e] == ctx_doc[t]) ++e;
+      if (!runs.emplace(ctx_doc[t], std::make_pair(t, e)).second) {
+        set_error("pt_build_blockmap_draft: document %d is not one contiguous run of the context", ctx_doc[t]);
+        return 1;
+      }
+      t = e;
+    }
+  }
+  // per block: the context it keeps before any window, [x, y); anchor; keep flag
+  std::vector<int4> blk((size_t)std::max(n_blocks, 1));
+  for (int b = 0; b < n_blocks; ++b) {
+    int lo = 0, hi = anchors[b];
+    if (ctx_doc) {
+      auto it = runs.find(anchor_doc[b]);
+      if (it == runs.end()) {
+        lo = hi = 0;
+      } else {
+        lo = it->second.first;
+        hi = std::min(it->second.second, anchors[b]);
+        if (lo >= hi) lo = hi = 0;
+      }
+    }
+    blk[b] = make_int4(lo, hi, anchors[b], (!block_keep || block_keep[b]) ? 1 : 0);
+  }
+  pt_blockmap* bm = nullptr;
+  int rc = new_map((int)T, BM, BN, 0, s, &bm);
+  if (rc) return rc;
+  bm->producer = PT_PRODUCER_DRAFT;
+  bm->d_ctx = ctx_len;
+  bm->d_bs = block_size;
+  bm->d_nb = n_blocks;
+  bm->d_causal = causal ? 1 : 0;
+  bm->d_window = window;
+  do {
+    if ((rc = pool_alloc(&bm->d_blk, sizeof(int4) * blk.size(), bm->device, s))) break;
+    if (n_blocks > 0 && (rc = upload(bm->d_blk, blk.data(), sizeof(int4) * (size_t)n_blocks, bm->device, s))) break;
+    rc = finish_map(bm, s, -1);
+  } while (0);
+  if (rc) {
+    free_map(bm);
+    return rc;
+  }
+  *out = bm;
+  return 0;
+}
+
 int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out) {
   pt_blockmap* bm = nullptr;
   int rc = new_map(src->T, src->BM, src->BN, std::max(src->n_nodes, 1), s, &bm);
   if (rc) return rc;
   bm->n_nodes = src->n_nodes;
   bm->dense = true;
+  bm->producer = src->producer;
+  bm->d_ctx = src->d_ctx;
+  bm->d_bs = src->d_bs;
+  bm->d_nb = src->d_nb;
+  bm->d_causal = src->d_causal;
+  bm->d_window = src->d_window;
   const int nq = bm->nq, nk = bm->nk;
   const long long n = (long long)nq * nk;
   void* tmp = nullptr;
@@ -1158,6 +1355,15 @@ int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out) {
       set_error("pt_blockmap_dense: %lld tiles is too many", n);
       rc = 2;
       break;
+    }
+    if (src->producer == PT_PRODUCER_DRAFT) {
+      const size_t bytes = sizeof(int4) * (size_t)std::max(src->d_nb, 1);
+      if ((rc = pool_alloc(&bm->d_blk, bytes, bm->device, s))) break;
+      if (cudaMemcpyAsync(bm->d_blk, src->d_blk, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess) {
+        set_error("pt_blockmap_dense: copy failed");
+        rc = 3;
+        break;
+      }
     }
     if (cudaMemcpyAsync(bm->tok, src->tok, sizeof(pt_tok) * bm->tpad, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
         (bm->T &&
@@ -1195,8 +1401,12 @@ int build_dense(const pt_blockmap* src, cudaStream_t s, pt_blockmap** out) {
     PT_LAUNCHED(1);
     if (bm->mask_rows && n > 0) {
       const long long grid = std::min<long long>(n, (long long)num_sms(bm->device) * 16);
-      k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, n, nullptr,
-                                             nullptr, n);
+      if (bm->producer == PT_PRODUCER_DRAFT)
+        k_draft_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, draft_params(bm), slot_tile, bm->mask_rows,
+                                                     bm->mask_cols, n, nullptr, nullptr, n);
+      else
+        k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, n, nullptr,
+                                               nullptr, n);
       PT_LAUNCHED(1);
     }
     // every row has the same length: natural order

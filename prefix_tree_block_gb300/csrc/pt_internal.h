@@ -69,6 +69,11 @@ struct pt_blockmap {
   void* counts_ev;    // cudaEvent_t recorded after the copy to counts_host
   int64_t nnz_cap;    // list entries allocated (>= nnz)
   int64_t p_cap;      // mask slots allocated (>= n_partial)
+  // Which rule the map encodes: tree/segment labels (tok, node tables) or
+  // draft blocks (pt_build_blockmap_draft: the per-block ranges below).
+  int producer;
+  int32_t d_ctx, d_bs, d_nb, d_causal, d_window;
+  void* d_blk;  // int4[d_nb] (device): kept context [x, y) before any window, anchor z, keep flag w
   // backward work items of the kv-major kernel, cached for one head layout
   void* bwd_mem;
   int bwd_g, bwd_hkv, bwd_max_slots, bwd_n_items, bwd_n_splits, bwd_n_slots, bwd_grid, bwd_sms;
@@ -109,6 +114,13 @@ struct ProfScope {
   const char* name;
   void* end_event;
 };
+
+constexpr int PT_PRODUCER_TREE = 0, PT_PRODUCER_DRAFT = 1;
+
+// Draft-block map builder (pt_blockmap.cu).  Returns a PT_* status code.
+int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                const int32_t* anchor_doc, int32_t BM, int32_t BN, cudaStream_t s, pt_blockmap** out);
 
 // Host list lengths of a map: waits for the build's copy if it has not
 // arrived yet.  Returns a PT_* status code (pt_blockmap.cu).

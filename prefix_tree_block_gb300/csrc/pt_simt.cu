@@ -65,6 +65,7 @@ template <class E>
 __global__ void k_fwd(const E* __restrict__ Q, const E* __restrict__ K, const E* __restrict__ V, int T, int Hq,
                       int Hkv, int D, float scale, const int* __restrict__ q_ptr, const int* __restrict__ kv_idx,
                       const uint8_t* __restrict__ kind, const pt_tok* __restrict__ tok, int BM, int BN,
+                      int generic, const uint32_t* __restrict__ masks, const int* __restrict__ pidx,
                       E* __restrict__ O, float* __restrict__ LSE) {
   long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -75,13 +76,17 @@ __global__ void k_fwd(const E* __restrict__ Q, const E* __restrict__ K, const E*
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) acc[i] = 0.f;
   float m = -INFINITY, l = 0.f;
-  const int qt = q / BM, q_tin = tok[q].tin;
+  // tree maps: ancestor test plus kv <= q; other maps (generic): the partial
+  // tile's keep bits, over the whole tile
+  const int qt = q / BM, q_tin = generic ? 0 : tok[q].tin;
   for (int e = q_ptr[qt]; e < q_ptr[qt + 1]; ++e) {
     const int k0 = kv_idx[e] * BN;
     const bool partial = kind[e] == PT_KIND_PARTIAL;
-    const int k1 = min(min(k0 + BN, T), q + 1);
+    const int k1 = generic ? min(k0 + BN, T) : min(min(k0 + BN, T), q + 1);
+    const uint32_t* mrow = (generic && partial) ? masks + ((size_t)pidx[e] * 128 + (q - qt * BM)) * 4 : nullptr;
     for (int kv = k0; kv < k1; ++kv) {
-      if (partial && !tree_keep(tok, q_tin, kv)) continue;
+      if (partial && (mrow ? !((mrow[(kv - k0) >> 5] >> ((kv - k0) & 31)) & 1u) : !tree_keep(tok, q_tin, kv)))
+        continue;
       const E* kr = K + ((long long)kv * Hkv + hk) * D;
       const E* vr = V + ((long long)kv * Hkv + hk) * D;
       float s = dot_row(qv, kr, D) * scale;
@@ -123,7 +128,8 @@ __global__ void k_dq(const E* __restrict__ dO, const E* __restrict__ Q, const E*
                      const E* __restrict__ V, const float* __restrict__ LSE, const float* __restrict__ delta, int T,
                      int Hq, int Hkv, int D, float scale, const int* __restrict__ q_ptr,
                      const int* __restrict__ kv_idx, const uint8_t* __restrict__ kind, const pt_tok* __restrict__ tok,
-                     int BM, int BN, E* __restrict__ dQ) {
+                     int BM, int BN, int generic, const uint32_t* __restrict__ masks,
+                     const int* __restrict__ pidx, E* __restrict__ dQ) {
   long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= (long long)T * Hq) return;
@@ -134,13 +140,15 @@ __global__ void k_dq(const E* __restrict__ dO, const E* __restrict__ Q, const E*
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) acc[i] = 0.f;
   const float lse = LSE[(long long)h * T + q], dl = delta[(long long)h * T + q];
-  const int qt = q / BM, q_tin = tok[q].tin;
+  const int qt = q / BM, q_tin = generic ? 0 : tok[q].tin;
   for (int e = q_ptr[qt]; e < q_ptr[qt + 1]; ++e) {
     const int k0 = kv_idx[e] * BN;
     const bool partial = kind[e] == PT_KIND_PARTIAL;
-    const int k1 = min(min(k0 + BN, T), q + 1);
+    const int k1 = generic ? min(k0 + BN, T) : min(min(k0 + BN, T), q + 1);
+    const uint32_t* mrow = (generic && partial) ? masks + ((size_t)pidx[e] * 128 + (q - qt * BM)) * 4 : nullptr;
     for (int kv = k0; kv < k1; ++kv) {
-      if (partial && !tree_keep(tok, q_tin, kv)) continue;
+      if (partial && (mrow ? !((mrow[(kv - k0) >> 5] >> ((kv - k0) & 31)) & 1u) : !tree_keep(tok, q_tin, kv)))
+        continue;
       const E* kr = K + ((long long)kv * Hkv + hk) * D;
       const E* vr = V + ((long long)kv * Hkv + hk) * D;
       float p = expf(dot_row(qv, kr, D) * scale - lse);
@@ -165,7 +173,9 @@ __global__ void k_dkv(const E* __restrict__ dO, const E* __restrict__ Q, const E
                       const E* __restrict__ V, const float* __restrict__ LSE, const float* __restrict__ delta, int T,
                       int Hq, int Hkv, int D, float scale, const int* __restrict__ k_ptr,
                       const int* __restrict__ q_idx, const uint8_t* __restrict__ kindT,
-                      const pt_tok* __restrict__ tok, int BM, int BN, E* __restrict__ dK, E* __restrict__ dV) {
+                      const pt_tok* __restrict__ tok, int BM, int BN, int generic,
+                      const uint32_t* __restrict__ masks, const int* __restrict__ pidxT, E* __restrict__ dK,
+                      E* __restrict__ dV) {
   long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= (long long)T * Hkv) return;
@@ -175,16 +185,21 @@ __global__ void k_dkv(const E* __restrict__ dO, const E* __restrict__ Q, const E
   load_row(V + ((long long)kv * Hkv + hk) * D, D, vr);
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) dk[i] = dv[i] = 0.f;
-  const pt_tok ktok = tok[kv];
+  const pt_tok ktok = generic ? pt_tok{0, 0} : tok[kv];
   const int kb = kv / BN;
   for (int e = k_ptr[kb]; e < k_ptr[kb + 1]; ++e) {
     const int q0 = q_idx[e] * BM;
     const bool partial = kindT[e] == PT_KIND_PARTIAL;
-    const int qa = max(q0, kv), qb = min(q0 + BM, T);
+    const int qa = generic ? q0 : max(q0, kv), qb = min(q0 + BM, T);
+    const uint32_t* mcol = (generic && partial) ? masks + ((size_t)pidxT[e] * 128 + (kv - kb * BN)) * 4 : nullptr;
     for (int q = qa; q < qb; ++q) {
       if (partial) {
-        int qt = tok[q].tin;
-        if (!(ktok.tin <= qt && qt < ktok.tout)) continue;
+        if (mcol) {
+          if (!((mcol[(q - q0) >> 5] >> ((q - q0) & 31)) & 1u)) continue;
+        } else {
+          int qt = tok[q].tin;
+          if (!(ktok.tin <= qt && qt < ktok.tout)) continue;
+        }
       }
       for (int h = hk * g; h < (hk + 1) * g; ++h) {
         const E* qrow = Q + ((long long)q * Hq + h) * D;
@@ -220,10 +235,11 @@ template <class E>
 int fwd_impl(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
              const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
   const int block = 256;
+  const bool generic = bm->producer != PT_PRODUCER_TREE;  // masks from the tile bitmasks
   ProfScope ps(s, "fwd_simt");
   k_fwd<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
       (const E*)Q, (const E*)K, (const E*)V, T, Hq, Hkv, D, scale, bm->q_ptr, bm->kv_idx, bm->kind, bm->tok, bm->BM,
-      bm->BN, (E*)O, LSE);
+      bm->BN, generic ? 1 : 0, bm->mask_rows, bm->pidx, (E*)O, LSE);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -238,14 +254,15 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
              int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
              cudaStream_t s) {
   const int block = 256;
+  const bool generic = bm->producer != PT_PRODUCER_TREE;  // masks from the tile bitmasks
   ProfScope ps(s, "bwd_simt");
   k_delta<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>((const E*)dO, (const E*)O, T, Hq, D, delta);
   k_dq<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
       (const E*)dO, (const E*)Q, (const E*)K, (const E*)V, LSE, delta, T, Hq, Hkv, D, scale, bm->q_ptr, bm->kv_idx,
-      bm->kind, bm->tok, bm->BM, bm->BN, (E*)dQ);
+      bm->kind, bm->tok, bm->BM, bm->BN, generic ? 1 : 0, bm->mask_rows, bm->pidx, (E*)dQ);
   k_dkv<E><<<grid_for_warps((long long)T * Hkv, block), block, 0, s>>>(
       (const E*)dO, (const E*)Q, (const E*)K, (const E*)V, LSE, delta, T, Hq, Hkv, D, scale, bm->k_ptr, bm->q_idx,
-      bm->kindT, bm->tok, bm->BM, bm->BN, (E*)dK, (E*)dV);
+      bm->kindT, bm->tok, bm->BM, bm->BN, generic ? 1 : 0, bm->mask_cols, bm->pidxT, (E*)dK, (E*)dV);
   count_launch(3);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
