@@ -32,9 +32,36 @@ METRIC = "prefix-tree attn fwd+bwd useful TFLOP/s (unmasked pairs), % of bf16 pe
 L2_FLUSH_BYTES = 256 << 20
 
 
+def draft_pairs(st) -> int:
+    """Kept (q, kv) pairs per head of a draft-block layout: per kept block and
+    token k, the context of the anchor's document before the anchor (within
+    the window of real position anchor + k, if any), plus the block itself
+    (k + 1 tokens when causal, all of it otherwise)."""
+    import numpy as np
+
+    total = 0
+    S, bs = int(st.ctx_len), int(st.block_size)
+    for b, a in enumerate(int(x) for x in st.anchors):
+        if st.block_keep is not None and not st.block_keep[b]:
+            continue
+        lo, hi = 0, a
+        if st.ctx_doc is not None:
+            idx = np.nonzero(np.asarray(st.ctx_doc) == st.anchor_doc[b])[0]
+            lo, hi = (int(idx[0]), min(int(idx[-1]) + 1, a)) if idx.size else (0, 0)
+            if lo >= hi:
+                lo = hi = 0
+        for k in range(bs):
+            c0 = max(lo, a + k - st.window + 1) if st.window > 0 else lo
+            total += max(hi - c0, 0) + (k + 1 if st.causal else bs)
+    return total
+
+
 def useful_pairs(st) -> int:
     """Kept (q, kv) pairs per head, from the tree: each node's own causal
-    triangle plus its tokens times all ancestor tokens."""
+    triangle plus its tokens times all ancestor tokens (draft-block layouts:
+    draft_pairs)."""
+    if hasattr(st, "anchors"):
+        return draft_pairs(st)
     parent = {}
     for p in st.paths():
         for a, b in zip(p[:-1], p[1:]):
@@ -147,6 +174,25 @@ def cpu_oracle_run(st, cfg, seed, max_units=None):
     from prefix_tree_block_gb300 import workloads as W
 
     Hq, Hkv, D = cfg["Hq"], cfg["Hkv"], cfg["D"]
+    if hasattr(st, "anchors"):  # draft blocks: the dense fp64 oracle on the first blocks
+        from oracle import draft as odr
+
+        nb = 64 if max_units is None else 16
+        sub = W.DraftStructure(ctx_len=int(st.anchors[nb - 1]), anchors=st.anchors[:nb], block_size=st.block_size,
+                               block_keep=None if st.block_keep is None else st.block_keep[:nb],
+                               causal=st.causal, window=st.window,
+                               ctx_doc=None if st.ctx_doc is None else st.ctx_doc[:int(st.anchors[nb - 1])],
+                               anchor_doc=None if st.anchor_doc is None else st.anchor_doc[:nb])
+        q, k, v, do = W.make_tensors(sub.T, Hq, Hkv, D, cfg["dtype"], seed)
+        mask = odr.draft_mask(**sub.kwargs())
+        t0 = time.perf_counter()
+        odr.masked_attn_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), mask)
+        odr.masked_attn_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), do.double().numpy(), mask)
+        dt = time.perf_counter() - t0
+        flops = 14.0 * D * Hq * useful_pairs(sub)
+        what = (f"fp64 dense-mask oracle forward+backward (numpy, BLAS on all cores) over the first {nb} of "
+                f"{st.anchors.size} blocks (T={sub.T}), all {Hq} heads")
+        return flops, dt, os.cpu_count() or 1, what
     if "group_specs" in st.meta:
         specs = st.meta["group_specs"][: max_units or len(st.meta["group_specs"])]
         sub = W.grpo_structure(specs)
@@ -200,7 +246,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, help="workload 1..5 (default 2: GRPO batch)")
+    ap.add_argument("--workload", type=int, default=2, help="workload 1..6 (default 2: GRPO batch)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
@@ -248,11 +294,18 @@ def main():
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     ws = torch.empty(pt.bwd_workspace_bytes(T, Hq, D), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    nl, pp, pn = st.node_lengths, st.path_ptr, st.path_nodes
+    draft = hasattr(st, "anchors")
+    if draft:
+        host_layout = [a for a in (st.anchors, st.block_keep, st.ctx_doc, st.anchor_doc) if a is not None]
+        make_map = lambda: pt.build_blockmap_draft(**st.kwargs())
+    else:
+        nl, pp, pn = st.node_lengths, st.path_ptr, st.path_nodes
+        host_layout = [nl, pp, pn]
+        make_map = lambda: pt.build_blockmap_tree(nl, pp, pn, 128, 128)
     stream = torch.cuda.current_stream()
 
     def step(dense=False):
-        bm = pt.build_blockmap_tree(nl, pp, pn, 128, 128)
+        bm = make_map()
         if dense:
             d = bm.dense()
             bm.free()
@@ -348,7 +401,7 @@ def main():
     hs = pt.HostStep(Q.dtype, T, Hq, Hkv, D)
 
     def e2e_step():
-        bm = pt.build_blockmap_tree(nl, pp, pn, 128, 128)
+        bm = make_map()
         hs.run(hq, hk, hv, hdo, bm, hdq, hdk, hdv)
         bm.free()
 
@@ -368,11 +421,11 @@ def main():
     pt.sync_status()
     hs.free()
     e2e_ms = max_over_ranks(ea.elapsed_time(eb), dist, dev)
-    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do)) + 4 * (nl.size + pp.size + pn.size)
+    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do)) + sum(int(a.nbytes) for a in host_layout)
     d2h = sum(x.numel() * x.element_size() for x in (dQ, dK, dV))
     e2e = {"value": whole_job_tflops(world, flops_step, args.steps, e2e_ms), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps,
-           "path": "pt_build_blockmap_tree + pt_hoststep_run from pinned host buffers, copies overlapped"}
+           "path": "map built from host arrays + pt_hoststep_run from pinned host buffers, copies overlapped"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1733,6 +1733,23 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
 // (q tile, head) with at least one kv block, packed longest first onto the
 // grid's CTAs by LPT list scheduling and stored grouped by CTA, plus the q
 // tiles with no kv block at all (their dQ rows are zero).
+// dQ rows of the q tiles that attend to nothing are zero: one memset per run
+// of consecutive such tiles (the list is ascending).
+int zero_empty_dq(const pt_blockmap* bm, void* dQ, int T, int Hq, int D, cudaStream_t s) {
+  for (int i = 0; i < bm->dq_n_empty;) {
+    int e = i + 1;
+    while (e < bm->dq_n_empty && bm->h_dq_empty[e] == bm->h_dq_empty[e - 1] + 1) ++e;
+    const int t0 = bm->h_dq_empty[i] * 128, t1 = std::min(T, bm->h_dq_empty[e - 1] * 128 + 128);
+    if (cudaMemsetAsync(static_cast<__nv_bfloat16*>(dQ) + (size_t)t0 * Hq * D, 0,
+                        sizeof(__nv_bfloat16) * (size_t)(t1 - t0) * Hq * D, s) != cudaSuccess) {
+      set_error("backward: cudaMemsetAsync failed");
+      return 3;
+    }
+    i = e;
+  }
+  return 0;
+}
+
 int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, cudaStream_t s) {
   pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
   std::lock_guard<std::mutex> lk(g_items_mu);
@@ -1901,14 +1918,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
     ProfScope ps(s, "bwd_dq");
     if constexpr (D == 128) {
       if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s))) return rc;
-      for (int i = 0; i < bm->dq_n_empty; ++i) {  // q tiles that attend to nothing
-        const int t0 = bm->h_dq_empty[i] * 128, t1 = std::min(T, t0 + 128);
-        if (cudaMemsetAsync(static_cast<__nv_bfloat16*>(dQ) + (size_t)t0 * Hq * D, 0,
-                            sizeof(__nv_bfloat16) * (size_t)(t1 - t0) * Hq * D, s) != cudaSuccess) {
-          set_error("backward: cudaMemsetAsync failed");
-          return 3;
-        }
-      }
+      if ((rc = zero_empty_dq(bm, dQ, T, Hq, D, s))) return rc;
       p.dq_items = static_cast<const int4*>(bm->dq_items);
       p.dq_cta = static_cast<const int4*>(bm->dq_cta);
       if (bm->dq_n_items > 0)
@@ -2005,14 +2015,7 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   p.dq_cta = static_cast<const int4*>(bm->dq_cta);
   p.out0 = static_cast<__nv_bfloat16*>(dQ);
   p.out1 = nullptr;
-  for (int i = 0; i < bm->dq_n_empty; ++i) {  // q tiles that attend to nothing
-    const int t0 = bm->h_dq_empty[i] * 128, t1 = std::min(T, t0 + 128);
-    if (cudaMemsetAsync(static_cast<__nv_bfloat16*>(dQ) + (size_t)t0 * Hq * D, 0,
-                        sizeof(__nv_bfloat16) * (size_t)(t1 - t0) * Hq * D, s) != cudaSuccess) {
-      set_error("backward: cudaMemsetAsync failed");
-      return 3;
-    }
-  }
+  if ((rc = zero_empty_dq(bm, dQ, T, Hq, D, s))) return rc;
   if (bm->dq_n_items > 0) {
     ProfScope ps(s, "bwd_dq");
     k_bwd_wide<WIDE_DQ><<<bm->dq_grid, 320, WideCfg<WIDE_DQ>::BYTES, s>>>(mQ, mdO, mKh, mVh, p);

@@ -15,6 +15,10 @@ Workload shapes follow the pages' settings:
   ("cp=1 shared-prefix prefix-tree attention for rollouts", ``AttnMaskSpec.prefix_tree``).
 * Packed documents, i.e. a forest of single-node trees (the doc-gated,
   block-causal mask of "support sequence packing in the Domino and JetSpec drafts").
+* Draft blocks (DFlash): a packed context of documents and one block of
+  ``block_size`` tokens per anchor, anchors drawn so that a whole block stays
+  inside its document ("support sequence packing in the Domino and JetSpec
+  drafts": anchor sampling keeps doc_remaining >= block_size - 1).
 
 Lengths come from ``numpy.random.default_rng(seed)`` with inclusive integer
 draws; tensors from a CPU ``torch.Generator`` seeded ``1000 + seed`` in fp32,
@@ -29,6 +33,7 @@ import numpy as np
 
 __all__ = [
     "Structure",
+    "DraftStructure",
     "grpo_structure",
     "tree_structure",
     "docs_structure",
@@ -197,7 +202,55 @@ def random_tree(rng: np.random.Generator, n_nodes: int, max_len: int, p_zero: fl
 
 
 # ---------------------------------------------------------------------------
-# The five reference workloads (synthetic, seeded)
+@dataclass
+class DraftStructure:
+    """A draft-block layout: ctx_len context tokens, then one block of
+    block_size tokens per anchor (block b's token k at real position
+    anchors[b] + k); ctx_doc / anchor_doc are the packed documents of the
+    context tokens and of the anchors."""
+
+    ctx_len: int
+    anchors: np.ndarray  # int32 [n_blocks]
+    block_size: int
+    block_keep: Optional[np.ndarray] = None  # bool [n_blocks], None: all kept
+    causal: bool = False
+    window: int = 0
+    ctx_doc: Optional[np.ndarray] = None  # int32 [ctx_len]
+    anchor_doc: Optional[np.ndarray] = None  # int32 [n_blocks]
+    name: str = ""
+
+    @property
+    def T(self) -> int:
+        return int(self.ctx_len + self.anchors.size * self.block_size)
+
+    def kwargs(self) -> dict:
+        """The layout as keyword arguments (the draft map builder and the oracle take the same names)."""
+        return dict(ctx_len=self.ctx_len, anchors=self.anchors, block_size=self.block_size,
+                    block_keep=self.block_keep, causal=self.causal, window=self.window,
+                    ctx_doc=self.ctx_doc, anchor_doc=self.anchor_doc)
+
+
+def draft_structure(rng: np.random.Generator, ctx_len: int, doc_min: int, doc_max: int, n_blocks: int,
+                    block_size: int, causal: bool = False, window: int = 0, name: str = "") -> DraftStructure:
+    """Context packed with documents U[doc_min, doc_max] (the last cut to fill
+    it); n_blocks anchors drawn without replacement from the positions whose
+    whole block stays inside the document, sorted."""
+    docs: List[int] = []
+    left = ctx_len
+    while left > 0:
+        d = min(int(rng.integers(doc_min, doc_max + 1)), left)
+        docs.append(d)
+        left -= d
+    ctx_doc = np.repeat(np.arange(len(docs), dtype=np.int32), docs)
+    ends = np.cumsum(docs)
+    doc_end = ends[ctx_doc]
+    valid = np.nonzero(doc_end - np.arange(ctx_len) >= block_size)[0]
+    anchors = np.sort(rng.choice(valid, size=n_blocks, replace=False)).astype(np.int32)
+    return DraftStructure(ctx_len=ctx_len, anchors=anchors, block_size=block_size, causal=causal, window=window,
+                          ctx_doc=ctx_doc, anchor_doc=ctx_doc[anchors].astype(np.int32), name=name)
+
+
+# The reference workloads (synthetic, seeded)
 # ---------------------------------------------------------------------------
 
 CONFIGS = {
@@ -211,11 +264,15 @@ CONFIGS = {
             Hq=16, Hkv=4, D=128, dtype="bf16"),
     5: dict(name="packed documents: 4 rows x 4096, docs U[64,2048] cut to fill the row, Hq=8, Hkv=2, D=256, bf16",
             Hq=8, Hkv=2, D=256, dtype="bf16"),
+    6: dict(name="DFlash draft blocks: context 4096 packed with docs U[256,2048], 256 in-document blocks of 16, "
+                 "bidirectional, document-gated, Hq=16, Hkv=4, D=128, bf16",
+            Hq=16, Hkv=4, D=128, dtype="bf16", kind="draft"),
 }
 
 
-def config_structure(c: int) -> Structure:
-    """The token layout of workload ``c`` (1..5), lengths drawn from default_rng(c)."""
+def config_structure(c: int):
+    """The token layout of workload ``c`` (1..6), lengths drawn from default_rng(c): a
+    Structure, or a DraftStructure for the draft-block workload."""
     rng = np.random.default_rng(c)
     if c == 1:
         return grpo_structure([(16, [8, 8, 8, 8])], name="c1")
@@ -246,6 +303,8 @@ def config_structure(c: int) -> Structure:
                 docs.append(d)
                 left -= d
         return docs_structure(docs, name="c5")
+    if c == 6:
+        return draft_structure(rng, 4096, 256, 2048, 256, 16, name="c6")
     raise ValueError(f"unknown workload {c}")
 
 
