@@ -250,6 +250,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-fold", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -427,6 +428,46 @@ def main():
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps,
            "path": "map built from host arrays + pt_hoststep_run from pinned host buffers, copies overlapped"}
 
+    # ---- shared-prefix fold of the rollouts (HBM-bound data movement) -------
+    # The workload's samples as rollout rows of hidden states (Hq*D per token,
+    # the attention's input width): fold (rollouts -> flat), unfold (flat ->
+    # rollouts, padding zeroed) and the adjoint of unfold (summed gradient).
+    # Algorithmic bytes: fold 2*T*W; unfold T*W + S*L*W; unfold_grad
+    # copies*W + T*W (copies = the rollout entries that hold a token).
+    fold = None
+    if not args.no_fold and not draft:
+        L = int(max(sum(int(st.node_lengths[n]) for n in p) for p in st.paths()))
+        plan = pt.fold_plan(nl, pp, pn, L)
+        width = Hq * D
+        hflat = torch.randn(T, width, device=dev).to(Q.dtype)
+        roll = plan.unfold(hflat)
+        flat_out = torch.empty_like(hflat)
+        droll = torch.randn(roll.shape, device=dev).to(Q.dtype)
+        S = plan.n_samples
+        es = hflat.element_size()
+        copies = int(sum(sum(int(st.node_lengths[n]) for n in p) for p in st.paths()))
+        algo = {"fold": 2 * T * width * es, "unfold": (T + S * L) * width * es,
+                "unfold_grad": (copies + T) * width * es}
+        calls = {"fold": lambda: plan.fold(roll, out=flat_out), "unfold": lambda: plan.unfold(hflat, out=roll),
+                 "unfold_grad": lambda: plan.unfold_grad(droll, out=flat_out)}
+        fold = {"workload": f"{S} rollout rows of {L} tokens x {width} {dtype} (T={T} flat tokens)"}
+        for name, fn in calls.items():
+            for _ in range(3):
+                fn()
+            pt.profile_reset()
+            pt.profile_enable(True)
+            timed(args.steps, fn)
+            pt.profile_enable(False)
+            n, ms = pt.profile_read(name)
+            ach = algo[name] / (ms / n * 1e-3) / 1e9
+            fold[name] = {"ms_per_launch": ms / n, "algorithmic_bytes": algo[name], "achieved_gbs": ach,
+                          "frac_of_hbm": ach / peak_gbs}
+        fold["hbm_peak_gbs"] = peak_gbs
+        fold["l2"] = "flushed before every launch (256 MB write, untimed)"
+        pt.profile_reset()
+        plan.free()
+        pt.sync_status()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, s, nth, desc = cpu_oracle_run(st, cfg, args.workload)
@@ -445,7 +486,7 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "kernels": kernels, "kernel_timing": "second pass of the same steps with an event pair per kernel",
             "roofline": roofline, "dense_masked": dense, "e2e": e2e,
-            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
+            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu, "fold": fold,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -320,6 +320,72 @@ pt_status pt_hoststep_run(pt_hoststep* h, const void* hQ, const void* hK, const 
 pt_status pt_hoststep_sync(pt_hoststep* h, cudaStream_t stream);
 void pt_hoststep_free(pt_hoststep* h);
 
+/* ---------------------------------------------------------------------------
+ * Shared-prefix fold of rollouts, and its inverse.
+ *
+ * Passage: "cp=1 shared-prefix prefix-tree attention for rollouts", PR
+ * description: a group of one prompt and N sampled completions is folded
+ * into one deduplicated flat sequence [prompt | c_0 | c_1 | ...] (the prompt
+ * is encoded once instead of N times), each completion gets position ids
+ * that continue from its prompt, and the tree is handed on as
+ * (node_lengths, sample_paths).  The plan takes that same tree, so one
+ * description drives the fold, pt_build_blockmap_tree and the unfold; the
+ * shared-prefix group is the depth-2 tree [prompt, c_i], multi-turn rollouts
+ * are deeper trees.
+ *
+ * Layouts.  Flat: node i owns tokens [off_i, off_i + node_lengths[i]), off
+ * the exclusive prefix sum in id order (the attention calls' layout).
+ * Rollouts: n_samples rows of row_len tokens; row s holds the tokens of its
+ * path's nodes, root first, at positions 0, 1, ..., then padding.  A token's
+ * data is one contiguous row of row_bytes bytes in both layouts (an id, a
+ * hidden state, a Q row...), so a flat tensor is [T, row] and a rollout
+ * tensor [n_samples, row_len, row], densely packed.
+ *
+ * pt_fold_plan: validates the tree as pt_build_blockmap_tree does (every
+ *   node on some path, one parent per node, parents before children) and
+ *   that no path is longer than row_len; builds the per-token and per-entry
+ *   maps on the device (stream-ordered, library-owned memory).  Host arrays
+ *   as pt_build_blockmap_tree.  Errors: PT_ERR_INVALID_ARG (malformed tree,
+ *   a path longer than row_len, n_samples * row_len >= 2^31), PT_ERR_NOMEM,
+ *   PT_ERR_CUDA.
+ * pt_fold: flat[t] = roll[the first sample holding token t][its position]:
+ *   the deduplication; the other samples are expected to hold the same
+ *   bytes there (pt_fold_mismatches checks).  roll is read, flat written.
+ * pt_unfold: roll[s][j] = flat[the token at position j of sample s]; shared
+ *   tokens are copied into every row that holds them; padding entries are
+ *   zero-filled.
+ * pt_unfold_grad: the adjoint of pt_unfold, for the backward pass of a loss
+ *   taken on the rollout rows: dflat[t] = sum over every copy of t of
+ *   droll[s][j] (padding ignored).  Elements are dtype (bf16 or fp32),
+ *   width per token; sums are taken in fp32 in sample order (deterministic)
+ *   and rounded once to dtype (round to nearest even).
+ * pt_fold_positions: pos[t] = the position of token t in the rows that hold
+ *   it (int64 [T], the RoPE position ids): a completion's positions continue
+ *   from its prompt's.
+ * pt_fold_mismatches: *count (device, one unsigned 64-bit counter, zeroed by
+ *   the call) = the number of rollout entries whose bytes differ from the
+ *   entry pt_fold keeps for their token; 0 when the rollouts really share
+ *   their prefixes.
+ * Device buffers are the caller's; any alignment works (the kernels move the
+ * widest unit that row_bytes and the base addresses allow).  Every call is
+ * ordered on `stream` and returns PT_ERR_INVALID_ARG for a NULL plan or
+ * buffer, a non-positive row_bytes or width, or a plan of another device.
+ * pt_foldplan_free returns the plan's memory in its build stream's order.
+ * ------------------------------------------------------------------------- */
+typedef struct pt_foldplan pt_foldplan;
+pt_status pt_fold_plan(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr,
+                       const int32_t* path_nodes, int32_t n_samples, int32_t row_len, cudaStream_t stream,
+                       pt_foldplan** out);
+pt_status pt_foldplan_info(const pt_foldplan* plan, int32_t* T, int32_t* n_samples, int32_t* row_len);
+void pt_foldplan_free(pt_foldplan* plan);
+pt_status pt_fold(const pt_foldplan* plan, const void* roll, int64_t row_bytes, void* flat, cudaStream_t stream);
+pt_status pt_unfold(const pt_foldplan* plan, const void* flat, int64_t row_bytes, void* roll, cudaStream_t stream);
+pt_status pt_unfold_grad(const pt_foldplan* plan, const void* droll, pt_dtype dtype, int64_t width, void* dflat,
+                         cudaStream_t stream);
+pt_status pt_fold_positions(const pt_foldplan* plan, int64_t* pos, cudaStream_t stream);
+pt_status pt_fold_mismatches(const pt_foldplan* plan, const void* roll, int64_t row_bytes, unsigned long long* count,
+                             cudaStream_t stream);
+
 /* Synchronise the stream, then return and clear the device status word:
  * PT_ERR_TIMEOUT if an in-kernel wait ran out since the last check, PT_ERR_CUDA
  * if the stream reported an error, else PT_OK. */
@@ -368,8 +434,9 @@ pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cud
  * events and returns the number of launches and their summed duration for
  * one scope name: "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
  * "bwd_dkdv_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt",
- * "blockmap_classify" (tile classes, list sizes, orders) and
- * "blockmap_lists" (lists and masks).  pt_profile_reset drops every record
+ * "blockmap_classify" (tile classes, list sizes, orders),
+ * "blockmap_lists" (lists and masks), and the fold calls' "fold_plan",
+ * "fold", "unfold", "unfold_grad", "fold_positions", "fold_mismatches".  pt_profile_reset drops every record
  * (its events go back to the pool once they have completed). */
 void pt_profile_enable(int on);
 pt_status pt_profile_read(const char* kernel, int64_t* launches, double* total_ms);

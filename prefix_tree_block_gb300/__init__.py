@@ -19,7 +19,7 @@ __all__ = [
     "PTError", "BlockMap", "HostStep", "load_library", "build_blockmap_tree", "build_blockmap_seg",
     "build_blockmap_draft",
     "attn_fwd", "attn_bwd", "bwd_workspace_bytes", "sync_status", "launch_count", "LIB_PATH",
-    "profile_enable", "profile_read", "profile_reset", "attn_bwd_noalloc",
+    "profile_enable", "profile_read", "profile_reset", "attn_bwd_noalloc", "FoldPlan", "fold_plan",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpt.so")
@@ -71,6 +71,13 @@ def load_library(path: Optional[str] = None):
             "pt_hoststep_create": [ctypes.c_int, i32, i32, i32, i32, pp],
             "pt_hoststep_run": [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp],
             "pt_hoststep_sync": [vp, vp],
+            "pt_fold_plan": [vp, i32, vp, vp, i32, i32, vp, pp],
+            "pt_foldplan_info": [vp, i32p, i32p, i32p],
+            "pt_fold": [vp, vp, i64, vp, vp],
+            "pt_unfold": [vp, vp, i64, vp, vp],
+            "pt_unfold_grad": [vp, vp, ctypes.c_int, i64, vp, vp],
+            "pt_fold_positions": [vp, vp, vp],
+            "pt_fold_mismatches": [vp, vp, i64, vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -78,6 +85,8 @@ def load_library(path: Optional[str] = None):
             fn.restype = ctypes.c_int
         lib.pt_blockmap_free.argtypes = [vp]
         lib.pt_blockmap_free.restype = None
+        lib.pt_foldplan_free.argtypes = [vp]
+        lib.pt_foldplan_free.restype = None
         lib.pt_hoststep_free.argtypes = [vp]
         lib.pt_hoststep_free.restype = None
         lib.pt_bwd_workspace_bytes.argtypes = [i32, i32, i32]
@@ -421,3 +430,106 @@ class HostStep:
             self.free()
         except Exception:
             pass
+
+
+class FoldPlan:
+    """Shared-prefix fold of rollouts and its inverse (pt_fold_plan and the
+    calls after it): the flat layout of the tree (node_lengths, CSR sample
+    paths) against n_samples rollout rows of row_len tokens.  Tensors carry
+    one row of data per token: flat [T, ...], rollouts [n_samples, row_len, ...]."""
+
+    def __init__(self, node_lengths, path_ptr, path_nodes, row_len: int, stream=None):
+        import numpy as np
+
+        self._lib = load_library()
+        nl = np.ascontiguousarray(np.asarray(node_lengths, dtype=np.int32))
+        pp = np.ascontiguousarray(np.asarray(path_ptr, dtype=np.int32))
+        pn = np.ascontiguousarray(np.asarray(path_nodes, dtype=np.int32))
+        out = ctypes.c_void_p()
+        _check(self._lib.pt_fold_plan(nl.ctypes.data if nl.size else None, int(nl.size), pp.ctypes.data,
+                                      pn.ctypes.data if pn.size else None, int(pp.size - 1), int(row_len),
+                                      ctypes.c_void_p(_stream(stream)), ctypes.byref(out)))
+        self._h = out
+        T, S, L = (ctypes.c_int32() for _ in range(3))
+        _check(self._lib.pt_foldplan_info(self._h, ctypes.byref(T), ctypes.byref(S), ctypes.byref(L)))
+        self.T, self.n_samples, self.row_len = T.value, S.value, L.value
+
+    @staticmethod
+    def _row_bytes(t, lead: int) -> int:
+        n = t.numel() * t.element_size()
+        per = 1
+        for d in t.shape[:lead]:
+            per *= d
+        return n // per if per else 0
+
+    def _need(self, t, shape, name):
+        if not t.is_cuda or not t.is_contiguous() or tuple(t.shape[:len(shape)]) != shape:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of leading shape {shape}")
+
+    def fold(self, roll, out=None, stream=None):
+        """flat[t] = roll[first sample holding t][its position]."""
+        import torch
+
+        self._need(roll, (self.n_samples, self.row_len), "roll")
+        rb = self._row_bytes(roll, 2)
+        out = torch.empty((self.T,) + tuple(roll.shape[2:]), dtype=roll.dtype, device=roll.device) \
+            if out is None else out
+        _check(self._lib.pt_fold(self._h, _ptr(roll), rb, _ptr(out), ctypes.c_void_p(_stream(stream))))
+        return out
+
+    def unfold(self, flat, out=None, stream=None):
+        """roll[s][j] = flat[token at position j of sample s]; padding zero."""
+        import torch
+
+        self._need(flat, (self.T,), "flat")
+        rb = self._row_bytes(flat, 1)
+        out = torch.empty((self.n_samples, self.row_len) + tuple(flat.shape[1:]), dtype=flat.dtype,
+                          device=flat.device) if out is None else out
+        _check(self._lib.pt_unfold(self._h, _ptr(flat), rb, _ptr(out), ctypes.c_void_p(_stream(stream))))
+        return out
+
+    def unfold_grad(self, droll, out=None, stream=None):
+        """dflat[t] = sum of droll over every copy of t (fp32 sums, rounded once)."""
+        import torch
+
+        self._need(droll, (self.n_samples, self.row_len), "droll")
+        width = droll.numel() // max(1, self.n_samples * self.row_len)
+        out = torch.empty((self.T,) + tuple(droll.shape[2:]), dtype=droll.dtype, device=droll.device) \
+            if out is None else out
+        _check(self._lib.pt_unfold_grad(self._h, _ptr(droll), _dtype_code(droll), width, _ptr(out),
+                                        ctypes.c_void_p(_stream(stream))))
+        return out
+
+    def positions(self, device=None, stream=None):
+        """Position ids of the flat tokens (int64 [T])."""
+        import torch
+
+        out = torch.empty(self.T, dtype=torch.int64, device=device or torch.device("cuda"))
+        _check(self._lib.pt_fold_positions(self._h, _ptr(out), ctypes.c_void_p(_stream(stream))))
+        return out
+
+    def mismatches(self, roll, stream=None) -> int:
+        """Rollout entries whose bytes differ from the entry the fold keeps (synchronises)."""
+        import torch
+
+        self._need(roll, (self.n_samples, self.row_len), "roll")
+        cnt = torch.empty(1, dtype=torch.int64, device=roll.device)
+        _check(self._lib.pt_fold_mismatches(self._h, _ptr(roll), self._row_bytes(roll, 2), _ptr(cnt),
+                                            ctypes.c_void_p(_stream(stream))))
+        return int(cnt.item())
+
+    def free(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.pt_foldplan_free(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def fold_plan(node_lengths, path_ptr, path_nodes, row_len: int, stream=None) -> FoldPlan:
+    """Plan of the shared-prefix fold for a tree and a rollout row length."""
+    return FoldPlan(node_lengths, path_ptr, path_nodes, row_len, stream)
