@@ -105,6 +105,16 @@ def whole_job_tflops(world: int, flops_per_step: float, steps: int, total_ms: fl
     return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
 
 
+FP32_LANES_PER_SM = 128  # fp32 FMA lanes per SM (4 sub-partitions x 32)
+SM_MAX_GHZ = 2.07  # maximum SM clock of the GB300
+
+
+def num_sms() -> int:
+    import torch
+
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -246,7 +256,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, help="workload 1..6 (default 2: GRPO batch)")
+    ap.add_argument("--workload", type=int, default=2, help="workload 1..7 (default 2: GRPO batch)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
@@ -374,15 +384,25 @@ def main():
         "bwd_dv": 4.0 * D * Hq * pairs,  # head_dim 256: S^T and dV
         "bwd_dk": 6.0 * D * Hq * pairs,  # head_dim 256: S^T, dP^T and dK
         "bwd_dq": 6.0 * D * Hq * pairs,
+        # CUDA-core kernels (fp32 inputs, head dims without a tensor-core path): useful flops
+        "fwd_simt": 4.0 * D * Hq * pairs,
+        "bwd_simt": 10.0 * D * Hq * pairs,
     }
     tc = {k: v for k, v in kernels.items() if k in per_launch_flops}
     roofline = None
     if tc:
         dom = max(tc, key=lambda k: tc[k]["ms_per_launch"])
         ach = per_launch_flops[dom] / (tc[dom]["ms_per_launch"] * 1e-3) / 1e12
-        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": ach / peak_tf, "traffic": MEASURED_TRAFFIC.get((args.workload, dom)),
-                    "peak_source": f"{peak_src} bf16 burst"}
+        if dom.endswith("_simt"):  # fp32 FMA pipes: SMs x 128 lanes x 2 flop x max SM clock
+            fp32_peak = FP32_LANES_PER_SM * num_sms() * 2 * SM_MAX_GHZ / 1e3
+            roofline = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                        "frac": ach / fp32_peak, "traffic": None,
+                        "peak_source": f"derived: {num_sms()} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 flop x "
+                                       f"{SM_MAX_GHZ} GHz"}
+        else:
+            roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                        "frac": ach / peak_tf, "traffic": MEASURED_TRAFFIC.get((args.workload, dom)),
+                        "peak_source": f"{peak_src} bf16 burst"}
 
     # ---- dense-masked comparison (same kernels, every tile partial) ---------
     dense = None

@@ -206,9 +206,14 @@ void pt_blockmap_free(pt_blockmap* bm);
  * LSE [Hq,T] (device fp32): LSE = m + ln(sum exp(s - m)) over the kept scores
  * s of the row.  scale <= 0 selects 1/sqrt(D).  The map must have been built
  * for the same T.
- * Supported: PT_BF16 with D in {64, 128, 256} and a 128 x 128 map (tensor
- * cores); PT_F32 with 1 <= D <= 256 and any map (CUDA cores).  Hq % Hkv == 0.
- * Anything else returns PT_ERR_UNSUPPORTED or PT_ERR_INVALID_ARG.
+ * Supported: PT_BF16 with D in {64, 128, 256} and a 128 x 128 map run on
+ * tensor cores; PT_BF16 with another D <= 512 that is a multiple of 8 (or
+ * another tile size), and PT_F32 with 1 <= D <= 512, run on CUDA cores with
+ * fp32 math.  Head dims above 256 have no tensor-core path here (a 128-row
+ * fp32 accumulator of more than 256 columns leaves no TMEM for the scores);
+ * the drafter PR notes that FlexAttention fails beyond 256 on sm_103.
+ * Hq % Hkv == 0.  Anything else returns PT_ERR_UNSUPPORTED or
+ * PT_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------- */
 pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtype, int32_t T,
                       int32_t Hq, int32_t Hkv, int32_t D, float scale, const pt_blockmap* bm,

@@ -160,8 +160,8 @@ pt_status check_attn(const char* who, pt_dtype dtype, int T, int Hq, int Hkv, in
     set_error("%s: Hq = %d must be a positive multiple of Hkv = %d", who, Hq, Hkv);
     return PT_ERR_INVALID_ARG;
   }
-  if (D <= 0 || D > 256) {
-    set_error("%s: head_dim %d outside 1..256", who, D);
+  if (D <= 0 || D > 512) {
+    set_error("%s: head_dim %d outside 1..512", who, D);
     return D <= 0 ? PT_ERR_INVALID_ARG : PT_ERR_UNSUPPORTED;
   }
   if (dtype != PT_BF16 && dtype != PT_F32) {

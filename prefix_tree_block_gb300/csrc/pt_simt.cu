@@ -21,7 +21,10 @@ int take_status_simt(cudaStream_t s) { return take_status_here(s); }
 
 namespace {
 
-constexpr int kMaxPerLane = 8;  // head_dim <= 256
+// NPL values of a head_dim row per lane: 8 up to head_dim 256, 16 up to 512
+// (head dims the tensor-core kernels do not take; "flex" fails beyond 256 on
+// sm_103, per the drafter PR's testing notes).
+constexpr int kMaxHeadDim = 512;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -34,22 +37,22 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <class E>
+template <int NPL, class E>
 __device__ __forceinline__ void load_row(const E* p, int D, float* r) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < NPL; ++i) {
     int d = lane + 32 * i;
     r[i] = d < D ? to_f(p[d]) : 0.f;
   }
 }
 
-template <class E>
+template <int NPL, class E>
 __device__ __forceinline__ float dot_row(const float* a, const E* p, int D) {
   const int lane = threadIdx.x & 31;
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < NPL; ++i) {
     int d = lane + 32 * i;
     if (d < D) s += a[i] * to_f(p[d]);
   }
@@ -61,7 +64,7 @@ __device__ __forceinline__ bool tree_keep(const pt_tok* tok, int q_tin, int kv) 
   return t.tin <= q_tin && q_tin < t.tout;
 }
 
-template <class E>
+template <class E, int NPL>
 __global__ void k_fwd(const E* __restrict__ Q, const E* __restrict__ K, const E* __restrict__ V, int T, int Hq,
                       int Hkv, int D, float scale, const int* __restrict__ q_ptr, const int* __restrict__ kv_idx,
                       const uint8_t* __restrict__ kind, const pt_tok* __restrict__ tok, int BM, int BN,
@@ -71,10 +74,10 @@ __global__ void k_fwd(const E* __restrict__ Q, const E* __restrict__ K, const E*
   const int lane = threadIdx.x & 31;
   if (w >= (long long)T * Hq) return;
   const int q = (int)(w / Hq), h = (int)(w % Hq), hk = h / (Hq / Hkv);
-  float qv[kMaxPerLane], acc[kMaxPerLane];
-  load_row(Q + ((long long)q * Hq + h) * D, D, qv);
+  float qv[NPL], acc[NPL];
+  load_row<NPL>(Q + ((long long)q * Hq + h) * D, D, qv);
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) acc[i] = 0.f;
+  for (int i = 0; i < NPL; ++i) acc[i] = 0.f;
   float m = -INFINITY, l = 0.f;
   // tree maps: ancestor test plus kv <= q; other maps (generic): the partial
   // tile's keep bits, over the whole tile
@@ -89,12 +92,12 @@ __global__ void k_fwd(const E* __restrict__ Q, const E* __restrict__ K, const E*
         continue;
       const E* kr = K + ((long long)kv * Hkv + hk) * D;
       const E* vr = V + ((long long)kv * Hkv + hk) * D;
-      float s = dot_row(qv, kr, D) * scale;
+      float s = dot_row<NPL>(qv, kr, D) * scale;
       float mn = fmaxf(m, s);
       float c = expf(m - mn), p = expf(s - mn);
       l = l * c + p;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < NPL; ++i) {
         int d = lane + 32 * i;
         acc[i] = acc[i] * c + (d < D ? p * to_f(vr[d]) : 0.f);
       }
@@ -104,26 +107,26 @@ __global__ void k_fwd(const E* __restrict__ Q, const E* __restrict__ K, const E*
   E* orow = O + ((long long)q * Hq + h) * D;
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < NPL; ++i) {
     int d = lane + 32 * i;
     if (d < D) from_f(orow + d, acc[i] * inv);
   }
   if (lane == 0) LSE[(long long)h * T + q] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
-template <class E>
+template <class E, int NPL>
 __global__ void k_delta(const E* __restrict__ dO, const E* __restrict__ O, int T, int Hq, int D,
                         float* __restrict__ delta) {
   long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (w >= (long long)T * Hq) return;
   const int q = (int)(w / Hq), h = (int)(w % Hq);
-  float a[kMaxPerLane];
-  load_row(dO + ((long long)q * Hq + h) * D, D, a);
-  float s = dot_row(a, O + ((long long)q * Hq + h) * D, D);
+  float a[NPL];
+  load_row<NPL>(dO + ((long long)q * Hq + h) * D, D, a);
+  float s = dot_row<NPL>(a, O + ((long long)q * Hq + h) * D, D);
   if ((threadIdx.x & 31) == 0) delta[(long long)h * T + q] = s;
 }
 
-template <class E>
+template <class E, int NPL>
 __global__ void k_dq(const E* __restrict__ dO, const E* __restrict__ Q, const E* __restrict__ K,
                      const E* __restrict__ V, const float* __restrict__ LSE, const float* __restrict__ delta, int T,
                      int Hq, int Hkv, int D, float scale, const int* __restrict__ q_ptr,
@@ -134,11 +137,11 @@ __global__ void k_dq(const E* __restrict__ dO, const E* __restrict__ Q, const E*
   const int lane = threadIdx.x & 31;
   if (w >= (long long)T * Hq) return;
   const int q = (int)(w / Hq), h = (int)(w % Hq), hk = h / (Hq / Hkv);
-  float qv[kMaxPerLane], dov[kMaxPerLane], acc[kMaxPerLane];
-  load_row(Q + ((long long)q * Hq + h) * D, D, qv);
-  load_row(dO + ((long long)q * Hq + h) * D, D, dov);
+  float qv[NPL], dov[NPL], acc[NPL];
+  load_row<NPL>(Q + ((long long)q * Hq + h) * D, D, qv);
+  load_row<NPL>(dO + ((long long)q * Hq + h) * D, D, dov);
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) acc[i] = 0.f;
+  for (int i = 0; i < NPL; ++i) acc[i] = 0.f;
   const float lse = LSE[(long long)h * T + q], dl = delta[(long long)h * T + q];
   const int qt = q / BM, q_tin = generic ? 0 : tok[q].tin;
   for (int e = q_ptr[qt]; e < q_ptr[qt + 1]; ++e) {
@@ -151,10 +154,10 @@ __global__ void k_dq(const E* __restrict__ dO, const E* __restrict__ Q, const E*
         continue;
       const E* kr = K + ((long long)kv * Hkv + hk) * D;
       const E* vr = V + ((long long)kv * Hkv + hk) * D;
-      float p = expf(dot_row(qv, kr, D) * scale - lse);
-      float ds = p * (dot_row(dov, vr, D) - dl);
+      float p = expf(dot_row<NPL>(qv, kr, D) * scale - lse);
+      float ds = p * (dot_row<NPL>(dov, vr, D) - dl);
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < NPL; ++i) {
         int d = lane + 32 * i;
         if (d < D) acc[i] += ds * to_f(kr[d]);
       }
@@ -162,13 +165,13 @@ __global__ void k_dq(const E* __restrict__ dO, const E* __restrict__ Q, const E*
   }
   E* out = dQ + ((long long)q * Hq + h) * D;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < NPL; ++i) {
     int d = lane + 32 * i;
     if (d < D) from_f(out + d, acc[i] * scale);
   }
 }
 
-template <class E>
+template <class E, int NPL>
 __global__ void k_dkv(const E* __restrict__ dO, const E* __restrict__ Q, const E* __restrict__ K,
                       const E* __restrict__ V, const float* __restrict__ LSE, const float* __restrict__ delta, int T,
                       int Hq, int Hkv, int D, float scale, const int* __restrict__ k_ptr,
@@ -180,11 +183,11 @@ __global__ void k_dkv(const E* __restrict__ dO, const E* __restrict__ Q, const E
   const int lane = threadIdx.x & 31;
   if (w >= (long long)T * Hkv) return;
   const int kv = (int)(w / Hkv), hk = (int)(w % Hkv), g = Hq / Hkv;
-  float kr[kMaxPerLane], vr[kMaxPerLane], dk[kMaxPerLane], dv[kMaxPerLane];
-  load_row(K + ((long long)kv * Hkv + hk) * D, D, kr);
-  load_row(V + ((long long)kv * Hkv + hk) * D, D, vr);
+  float kr[NPL], vr[NPL], dk[NPL], dv[NPL];
+  load_row<NPL>(K + ((long long)kv * Hkv + hk) * D, D, kr);
+  load_row<NPL>(V + ((long long)kv * Hkv + hk) * D, D, vr);
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) dk[i] = dv[i] = 0.f;
+  for (int i = 0; i < NPL; ++i) dk[i] = dv[i] = 0.f;
   const pt_tok ktok = generic ? pt_tok{0, 0} : tok[kv];
   const int kb = kv / BN;
   for (int e = k_ptr[kb]; e < k_ptr[kb + 1]; ++e) {
@@ -204,10 +207,10 @@ __global__ void k_dkv(const E* __restrict__ dO, const E* __restrict__ Q, const E
       for (int h = hk * g; h < (hk + 1) * g; ++h) {
         const E* qrow = Q + ((long long)q * Hq + h) * D;
         const E* dorow = dO + ((long long)q * Hq + h) * D;
-        float p = expf(dot_row(kr, qrow, D) * scale - LSE[(long long)h * T + q]);
-        float ds = p * (dot_row(vr, dorow, D) - delta[(long long)h * T + q]);
+        float p = expf(dot_row<NPL>(kr, qrow, D) * scale - LSE[(long long)h * T + q]);
+        float ds = p * (dot_row<NPL>(vr, dorow, D) - delta[(long long)h * T + q]);
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
+        for (int i = 0; i < NPL; ++i) {
           int d = lane + 32 * i;
           if (d < D) {
             dv[i] += p * to_f(dorow[d]);
@@ -220,7 +223,7 @@ __global__ void k_dkv(const E* __restrict__ dO, const E* __restrict__ Q, const E
   E* ko = dK + ((long long)kv * Hkv + hk) * D;
   E* vo = dV + ((long long)kv * Hkv + hk) * D;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < NPL; ++i) {
     int d = lane + 32 * i;
     if (d < D) {
       from_f(ko + d, dk[i] * scale);
@@ -231,13 +234,13 @@ __global__ void k_dkv(const E* __restrict__ dO, const E* __restrict__ Q, const E
 
 unsigned grid_for_warps(long long warps, int block) { return (unsigned)((warps * 32 + block - 1) / block); }
 
-template <class E>
+template <class E, int NPL>
 int fwd_impl(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
              const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
   const int block = 256;
   const bool generic = bm->producer != PT_PRODUCER_TREE;  // masks from the tile bitmasks
   ProfScope ps(s, "fwd_simt");
-  k_fwd<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
+  k_fwd<E, NPL><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
       (const E*)Q, (const E*)K, (const E*)V, T, Hq, Hkv, D, scale, bm->q_ptr, bm->kv_idx, bm->kind, bm->tok, bm->BM,
       bm->BN, generic ? 1 : 0, bm->mask_rows, bm->pidx, (E*)O, LSE);
   count_launch();
@@ -249,18 +252,18 @@ int fwd_impl(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv
   return 0;
 }
 
-template <class E>
+template <class E, int NPL>
 int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
              int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
              cudaStream_t s) {
   const int block = 256;
   const bool generic = bm->producer != PT_PRODUCER_TREE;  // masks from the tile bitmasks
   ProfScope ps(s, "bwd_simt");
-  k_delta<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>((const E*)dO, (const E*)O, T, Hq, D, delta);
-  k_dq<E><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
+  k_delta<E, NPL><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>((const E*)dO, (const E*)O, T, Hq, D, delta);
+  k_dq<E, NPL><<<grid_for_warps((long long)T * Hq, block), block, 0, s>>>(
       (const E*)dO, (const E*)Q, (const E*)K, (const E*)V, LSE, delta, T, Hq, Hkv, D, scale, bm->q_ptr, bm->kv_idx,
       bm->kind, bm->tok, bm->BM, bm->BN, generic ? 1 : 0, bm->mask_rows, bm->pidx, (E*)dQ);
-  k_dkv<E><<<grid_for_warps((long long)T * Hkv, block), block, 0, s>>>(
+  k_dkv<E, NPL><<<grid_for_warps((long long)T * Hkv, block), block, 0, s>>>(
       (const E*)dO, (const E*)Q, (const E*)K, (const E*)V, LSE, delta, T, Hq, Hkv, D, scale, bm->k_ptr, bm->q_idx,
       bm->kindT, bm->tok, bm->BM, bm->BN, generic ? 1 : 0, bm->mask_cols, bm->pidxT, (E*)dK, (E*)dV);
   count_launch(3);
@@ -276,15 +279,23 @@ int bwd_impl(const void* dO, const void* Q, const void* K, const void* V, const 
 
 int fwd_simt(bool bf16, const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
              const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
-  return bf16 ? fwd_impl<__nv_bfloat16>(Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, s)
-              : fwd_impl<float>(Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, s);
+  if (D > kMaxHeadDim) return 2;
+  if (D <= 256)
+    return bf16 ? fwd_impl<__nv_bfloat16, 8>(Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, s)
+                : fwd_impl<float, 8>(Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, s);
+  return bf16 ? fwd_impl<__nv_bfloat16, 16>(Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, s)
+              : fwd_impl<float, 16>(Q, K, V, T, Hq, Hkv, D, scale, bm, O, LSE, s);
 }
 
 int bwd_simt(bool bf16, const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
              int T, int Hq, int Hkv, int D, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV,
              float* delta, cudaStream_t s) {
-  return bf16 ? bwd_impl<__nv_bfloat16>(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, s)
-              : bwd_impl<float>(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, s);
+  if (D > kMaxHeadDim) return 2;
+  if (D <= 256)
+    return bf16 ? bwd_impl<__nv_bfloat16, 8>(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, s)
+                : bwd_impl<float, 8>(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, s);
+  return bf16 ? bwd_impl<__nv_bfloat16, 16>(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, s)
+              : bwd_impl<float, 16>(dO, Q, K, V, O, LSE, T, Hq, Hkv, D, scale, bm, dQ, dK, dV, delta, s);
 }
 
 }  // namespace pt

@@ -267,11 +267,14 @@ CONFIGS = {
     6: dict(name="DFlash draft blocks: context 4096 packed with docs U[256,2048], 256 in-document blocks of 16, "
                  "bidirectional, document-gated, Hq=16, Hkv=4, D=128, bf16",
             Hq=16, Hkv=4, D=128, dtype="bf16", kind="draft"),
+    7: dict(name="packed documents at head_dim 512: 4 rows x 4096, docs U[64,2048] cut to fill the row, "
+                 "Hq=8, Hkv=2, D=512, bf16",
+            Hq=8, Hkv=2, D=512, dtype="bf16"),
 }
 
 
 def config_structure(c: int):
-    """The token layout of workload ``c`` (1..6), lengths drawn from default_rng(c): a
+    """The token layout of workload ``c`` (1..7), lengths drawn from default_rng(c): a
     Structure, or a DraftStructure for the draft-block workload."""
     rng = np.random.default_rng(c)
     if c == 1:
@@ -293,7 +296,7 @@ def config_structure(c: int):
                 lengths.append(int(rng.integers(128, 384 + 1)))
                 paths.append([0, child, leaf])
         return tree_structure(lengths, paths, name="c4")
-    if c == 5:
+    if c in (5, 7):
         docs: List[int] = []
         for _ in range(4):
             left = 4096
@@ -302,7 +305,7 @@ def config_structure(c: int):
                 d = min(d, left)
                 docs.append(d)
                 left -= d
-        return docs_structure(docs, name="c5")
+        return docs_structure(docs, name=f"c{c}")
     if c == 6:
         return draft_structure(rng, 4096, 256, 2048, 256, 16, name="c6")
     raise ValueError(f"unknown workload {c}")
