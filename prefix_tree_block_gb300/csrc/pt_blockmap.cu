@@ -602,6 +602,39 @@ __global__ void k_lpt2(const int* a, int na, int* oa, const int* b, int nb, int*
 
 constexpr int kMaxDev = 64;
 
+// The small per-map transfers (node tables and work lists in, list sizes
+// out) go through the SMs, reading or writing the pinned staging through
+// its mapping in the device's address space, not through the copy engines.
+// A large copy that another stream has queued on an engine (a training
+// step's inputs and gradients) would otherwise hold them, and with them the
+// kernels queued behind them on this stream.
+__global__ void k_stage(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, long long bytes, int vec) {
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long nth = (long long)gridDim.x * blockDim.x;
+  long long done = 0;
+  if (vec) {
+    const long long n16 = bytes >> 4;
+    for (long long i = tid; i < n16; i += nth)
+      reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    done = n16 << 4;
+  }
+  for (long long i = done + tid; i < bytes; i += nth) dst[i] = src[i];
+}
+
+int stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  if (!bytes) return 0;
+  const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0) ? 1 : 0;
+  const long long units = vec ? (long long)(bytes >> 4) + 1 : (long long)bytes;
+  const int grid = (int)std::max(1LL, std::min<long long>((units + 255) / 256, 64));
+  k_stage<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), (long long)bytes, vec);
+  count_launch();
+  if (cudaGetLastError() != cudaSuccess) {
+    set_error("staging copy launch failed");
+    return 3;
+  }
+  return 0;
+}
+
 // ---------------------------------------------------------------------------
 // host side: memory
 // ---------------------------------------------------------------------------
@@ -710,6 +743,7 @@ int download_sync(void* dst, const void* src, size_t bytes, int dev, cudaStream_
 // slot until the lengths are read on the host.
 struct PinnedSlot {
   void* host = nullptr;
+  void* dev = nullptr;  // the same memory as the device addresses it
   size_t cap = 0;
   cudaEvent_t ev = nullptr;
 };
@@ -723,6 +757,12 @@ int pinned_acquire(int dev, size_t bytes, PinnedSlot* out) {
     std::vector<PinnedSlot>& fl = g_pinned_free[dev];
     for (size_t i = 0; i < fl.size(); ++i)
       if (fl[i].cap >= bytes) {
+        // a slot goes back to the pool with its last copy possibly in flight
+        // (a map freed before its sizes were read): take it once that is done
+        if (cudaEventQuery(fl[i].ev) == cudaErrorNotReady) {
+          if (cudaPeekAtLastError() == cudaErrorNotReady) cudaGetLastError();
+          continue;
+        }
         *out = fl[i];
         fl[i] = fl.back();
         fl.pop_back();
@@ -734,6 +774,11 @@ int pinned_acquire(int dev, size_t bytes, PinnedSlot* out) {
   if (cudaHostAlloc(&sl.host, sl.cap, cudaHostAllocDefault) != cudaSuccess) {
     set_error("pinned staging allocation of %zu bytes failed", sl.cap);
     return 5;
+  }
+  if (cudaHostGetDevicePointer(&sl.dev, sl.host, 0) != cudaSuccess) {
+    cudaFreeHost(sl.host);
+    set_error("pinned staging is not mapped into the device's address space");
+    return 3;
   }
   if (cudaEventCreateWithFlags(&sl.ev, cudaEventDisableTiming) != cudaSuccess) {
     cudaFreeHost(sl.host);
@@ -755,6 +800,7 @@ int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
   constexpr int kSlots = 16;
   struct Slot {
     void* host = nullptr;
+    void* dev = nullptr;  // the slot's device address
     size_t cap = 0;
     cudaEvent_t done = nullptr;
     bool used = false;
@@ -782,13 +828,16 @@ int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
       set_error("pinned staging allocation of %zu bytes failed", cap);
       return 5;
     }
+    if (cudaHostGetDevicePointer(&g.dev, g.host, 0) != cudaSuccess) {
+      cudaFreeHost(g.host);
+      g.host = nullptr;
+      set_error("pinned staging is not mapped into the device's address space");
+      return 3;
+    }
     g.cap = cap;
   }
   std::memcpy(g.host, src, bytes);
-  if (cudaMemcpyAsync(dst, g.host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
-    set_error("block map upload failed");
-    return 3;
-  }
+  if (int rc = stage_copy(g.dev, dst, bytes, s)) return rc;
   cudaEventRecord(g.done, s);
   g.used = true;
   return 0;
@@ -936,10 +985,10 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
       PinnedSlot sl;
       if ((rc = pinned_acquire(dev, sizeof(int) * ncnt, &sl))) break;
       bm->counts_host = sl.host;
+      bm->counts_dev = sl.dev;
       bm->counts_cap = sl.cap;
       bm->counts_ev = sl.ev;
-      if (cudaMemcpyAsync(sl.host, counters, sizeof(int) * ncnt, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-          cudaEventRecord(sl.ev, s) != cudaSuccess) {
+      if (stage_copy(counters, sl.dev, sizeof(int) * ncnt, s) != 0 || cudaEventRecord(sl.ev, s) != cudaSuccess) {
         set_error("block map: copy of the list sizes failed");
         rc = 3;
         break;
@@ -1014,6 +1063,7 @@ int ensure_counts(const pt_blockmap* cbm) {
   std::memcpy(bm->h_counts, bm->counts_host, sizeof(int) * ncnt);
   PinnedSlot sl;
   sl.host = bm->counts_host;
+  sl.dev = bm->counts_dev;
   sl.cap = bm->counts_cap;
   sl.ev = ev;
   pinned_release(bm->device, sl);
@@ -1027,6 +1077,14 @@ int ensure_counts(const pt_blockmap* cbm) {
   bm->n_full = bm->h_counts[0];
   bm->n_partial = nnz - bm->n_full;
   bm->counts_ready = true;
+  if (bm->h_rc_pred) {
+    for (int i = 0; i < bm->nq + bm->nk; ++i)
+      if (bm->h_rc_pred[i] != bm->h_row_cnt[i]) {
+        set_error("block map: the host-derived list length of %s %d is %d, the device's %d", i < bm->nq ? "q tile" : "kv block",
+                  i < bm->nq ? i : i - bm->nq, bm->h_rc_pred[i], bm->h_row_cnt[i]);
+        return 3;
+      }
+  }
   if (bm->nnz > bm->nnz_cap || bm->n_partial > bm->p_cap) {
     set_error("block map: %lld list entries and %lld partial tiles exceed the allocation's bounds (%lld, %lld)",
               (long long)bm->nnz, (long long)bm->n_partial, (long long)bm->nnz_cap, (long long)bm->p_cap);
@@ -1035,13 +1093,25 @@ int ensure_counts(const pt_blockmap* cbm) {
   return 0;
 }
 
+int rowcol_counts(const pt_blockmap* bm, const int** row, const int** col) {
+  if (bm->h_rc_pred) {  // exact, and identical to the device's (ensure_counts checks)
+    *row = bm->h_rc_pred;
+    *col = bm->h_rc_pred + bm->nq;
+    return 0;
+  }
+  if (int rc = ensure_counts(bm)) return rc;
+  *row = bm->h_row_cnt;
+  *col = bm->h_col_cnt;
+  return 0;
+}
+
 void free_map(pt_blockmap* bm) {
   if (!bm) return;
   pool_free(bm->d_blk, bm->stream);
-  if (bm->counts_host) {  // sizes never read: the copy may still be in flight
-    cudaEventSynchronize(static_cast<cudaEvent_t>(bm->counts_ev));
+  if (bm->counts_host) {  // sizes never read: the copy may still be in flight (the pool waits for it)
     PinnedSlot sl;
     sl.host = bm->counts_host;
+    sl.dev = bm->counts_dev;
     sl.cap = bm->counts_cap;
     sl.ev = static_cast<cudaEvent_t>(bm->counts_ev);
     pinned_release(bm->device, sl);
@@ -1049,6 +1119,7 @@ void free_map(pt_blockmap* bm) {
   pool_free(bm->bwd_mem, bm->stream);
   pool_free(bm->dq_mem, bm->stream);
   std::free(bm->h_dq_empty);
+  std::free(bm->h_rc_pred);
   std::free(bm->h_counts);
   pool_free(bm->mem_lists, bm->stream);
   pool_free(bm->mem_fixed, bm->stream);
@@ -1161,10 +1232,45 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
     for (char c : split) m += c;
     p_bound = 2 * m * nt + nt;
   }
+  // Exact list lengths from the tree, so that nothing downstream (the
+  // backward's work lists) waits for the device: q tile i meets the kv blocks
+  // that its rows' kept ranges touch.  The rows of node n in the tile keep
+  // every token of n's ancestors and n's own tokens up to the tile's last row
+  // of n (keep = ancestor-or-self and kv <= q; ancestors come first).
+  const int nq_h = (int)((T + BM - 1) / BM), nk_h = (int)((T + BN - 1) / BN);
+  std::vector<int> pred((size_t)nq_h + nk_h, 0);
+  {
+    std::vector<int> stamp((size_t)std::max(nk_h, 1), -1);
+    int n0 = 0;  // nodes are in token order: the first that may reach tile i
+    for (int i = 0; i < nq_h; ++i) {
+      const long long r_lo = (long long)i * BM, r_hi = std::min<long long>(r_lo + BM, T);
+      while (n0 < N && end[n0] <= r_lo) ++n0;
+      auto mark = [&](long long a, long long b) {  // kv tokens [a, b]
+        for (long long j = a / BN; j <= b / BN; ++j)
+          if (stamp[(size_t)j] != i) {
+            stamp[(size_t)j] = i;
+            ++pred[(size_t)i];
+            ++pred[(size_t)nq_h + j];
+          }
+      };
+      for (int n = n0; n < N && start[n] < r_hi; ++n) {
+        if (end[n] <= r_lo || node_lengths[n] == 0) continue;
+        mark(start[n], std::min<long long>(end[n], r_hi) - 1);
+        for (int a = parent[n]; a >= 0; a = parent[a])
+          if (node_lengths[a] > 0) mark(start[a], end[a] - 1);
+      }
+    }
+  }
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, N, s, &bm);
   if (rc) return rc;
   bm->n_nodes = N;
+  bm->h_rc_pred = static_cast<int*>(std::malloc(sizeof(int) * std::max<size_t>(pred.size(), 1)));
+  if (!bm->h_rc_pred) {
+    free_map(bm);
+    return 5;
+  }
+  std::copy(pred.begin(), pred.end(), bm->h_rc_pred);
   do {
     // one upload of start | end | parent | tin | tout into the map's node tables
     if (N > 0 && (rc = upload(bm->node_start, tab.data(), sizeof(int) * (size_t)5 * N, bm->device, s))) break;

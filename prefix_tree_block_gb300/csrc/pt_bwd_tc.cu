@@ -1641,15 +1641,16 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
               "(call pt_blockmap_prepare_bwd first)");
     return 1;
   }
-  if (int rc = ensure_counts(bm)) return rc;
+  const int *row_cnt = nullptr, *col_cnt = nullptr;
+  if (int rc = rowcol_counts(bm, &row_cnt, &col_cnt)) return rc;
   const int nk = bm->nk;
   long long total = 0;
-  for (int j = 0; j < nk; ++j) total += (long long)g * bm->h_col_cnt[j] * Hkv;
+  for (int j = 0; j < nk; ++j) total += (long long)g * col_cnt[j] * Hkv;
   long long cap = std::max<long long>(4, (total + sms - 1) / std::max(sms, 1));
   auto slots_for = [&](long long c) {
     long long n_slots = 0;
     for (int j = 0; j < nk; ++j) {
-      const long long n = (long long)g * bm->h_col_cnt[j];
+      const long long n = (long long)g * col_cnt[j];
       const long long nch = (n + c - 1) / c;
       if (nch > 1) n_slots += nch * Hkv;
     }
@@ -1663,7 +1664,7 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
   std::vector<int4> splits;
   int slot = 0;
   for (int j = 0; j < nk; ++j) {
-    const int n = g * bm->h_col_cnt[j];
+    const int n = g * col_cnt[j];
     const int nch = n == 0 ? 1 : (int)((n + cap - 1) / cap);
     for (int hk = 0; hk < Hkv; ++hk) {
       if (nch <= 1) {
@@ -1758,13 +1759,14 @@ int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, 
     set_error("block map's dQ work lists are not prepared for this head count (call pt_blockmap_prepare_bwd first)");
     return 1;
   }
-  if (int rc = ensure_counts(bm)) return rc;
+  const int *row_cnt = nullptr, *col_cnt = nullptr;
+  if (int rc = rowcol_counts(bm, &row_cnt, &col_cnt)) return rc;
   const int nq = bm->nq;
   std::vector<int4> items;
   std::vector<int> empty;
   int e0 = 0;
   for (int t = 0; t < nq; ++t) {
-    const int n = bm->h_row_cnt[t];
+    const int n = row_cnt[t];
     if (n == 0) empty.push_back(t);
     for (int h = 0; h < Hq && n > 0; ++h) items.push_back(make_int4(t, h, e0, n));
     e0 += n;

@@ -65,8 +65,13 @@ struct pt_blockmap {
   int* h_col_cnt;  // [nk]
   bool counts_ready;
   void* counts_host;  // pinned staging (until counts_ready)
+  void* counts_dev;   // the staging's device address
   size_t counts_cap;
   void* counts_ev;    // cudaEvent_t recorded after the copy to counts_host
+  // tree maps: the row and column list lengths derived on the host from the
+  // node intervals ([nq] rows | [nk] columns), usable before the device's
+  // arrive; ensure_counts checks them against the device's
+  int* h_rc_pred;
   int64_t nnz_cap;    // list entries allocated (>= nnz)
   int64_t p_cap;      // mask slots allocated (>= n_partial)
   // Which rule the map encodes: tree/segment labels (tok, node tables) or
@@ -125,6 +130,11 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
 // Host list lengths of a map: waits for the build's copy if it has not
 // arrived yet.  Returns a PT_* status code (pt_blockmap.cu).
 int ensure_counts(const pt_blockmap* bm);
+
+// Row and column list lengths of a map (host arrays of nq and nk): the
+// host-derived ones of a tree map while the device's are still in flight,
+// else the device's (waiting for them if needed).  Returns a PT_* status code.
+int rowcol_counts(const pt_blockmap* bm, const int** row, const int** col);
 
 // True when the map could have partial tiles but carries no masks.
 inline bool masks_missing(const pt_blockmap* bm) {
