@@ -924,13 +924,19 @@ int alloc_lists(pt_blockmap* bm, int64_t nnz, int64_t n_part, cudaStream_t s) {
 int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
   const int nq = bm->nq, nk = bm->nk, dev = bm->device;
   const long long ntiles = (long long)nq * nk;
-  // Causal bound on the non-empty tiles: q tile i meets kv blocks j with
-  // j * BN <= its last row.  With a bound on the partial tiles as well, the
-  // lists are allocated at the bounds and nothing waits for the device.
+  // Bound on the non-empty tiles: the exact count when the builder derived
+  // the list lengths on the host, else the causal bound (q tile i meets kv
+  // blocks j with j * BN <= its last row).  With a bound on the partial tiles
+  // as well, the lists are allocated at the bounds and nothing waits for the
+  // device.
   int64_t nnz_bound = 0;
-  for (int i = 0; i < nq; ++i) {
-    const long long qlast = std::min<long long>((long long)(i + 1) * bm->BM, bm->T) - 1;
-    nnz_bound += std::min<long long>(nk, qlast / bm->BN + 1);
+  if (bm->h_rc_pred) {  // exact list lengths are known on the host
+    for (int i = 0; i < nq; ++i) nnz_bound += bm->h_rc_pred[i];
+  } else {
+    for (int i = 0; i < nq; ++i) {
+      const long long qlast = std::min<long long>((long long)(i + 1) * bm->BM, bm->T) - 1;
+      nnz_bound += std::min<long long>(nk, qlast / bm->BN + 1);
+    }
   }
   const bool tiles128 = bm->BM == 128 && bm->BN == 128;
   const int64_t p_bound_c = std::min<int64_t>(p_bound, nnz_bound);
@@ -1419,9 +1425,50 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
     }
     blk[b] = make_int4(lo, hi, anchors[b], (!block_keep || block_keep[b]) ? 1 : 0);
   }
+  // Exact list lengths on the host, as for trees.  The rows of block b in q
+  // tile i are its tokens k0..k1; row k keeps the context [x, y) cut by the
+  // window to kv >= anchor + k - window + 1 (a range that shrinks as k grows,
+  // so the rows' union is row k0's), and its own block up to k (causal) or
+  // all of it.  Context rows keep nothing.
+  const int nq_h = (int)((T + BM - 1) / BM), nk_h = (int)((T + BN - 1) / BN);
+  std::vector<int> pred((size_t)nq_h + nk_h, 0);
+  {
+    std::vector<int> stamp((size_t)std::max(nk_h, 1), -1);
+    for (int i = 0; i < nq_h; ++i) {
+      const long long r_lo = std::max<long long>((long long)i * BM, ctx_len);
+      const long long r_hi = std::min<long long>((long long)(i + 1) * BM, T);
+      auto mark = [&](long long a, long long b) {  // kv tokens [a, b]
+        for (long long j = a / BN; j <= b / BN; ++j)
+          if (stamp[(size_t)j] != i) {
+            stamp[(size_t)j] = i;
+            ++pred[(size_t)i];
+            ++pred[(size_t)nq_h + j];
+          }
+      };
+      for (long long r = r_lo; r < r_hi;) {
+        const int b = (int)((r - ctx_len) / block_size);
+        const long long b0 = ctx_len + (long long)b * block_size;
+        const long long k0 = r - b0, k1 = std::min<long long>(b0 + block_size, r_hi) - 1 - b0;
+        r = b0 + k1 + 1;
+        if (!blk[b].w) continue;
+        long long x = blk[b].x;
+        if (window > 0) x = std::max<long long>(x, (long long)blk[b].z + k0 - window + 1);
+        if (x < blk[b].y) mark(x, blk[b].y - 1);
+        mark(b0, b0 + (causal ? k1 : block_size - 1));
+      }
+    }
+  }
+  long long nnz_exact = 0;
+  for (int i = 0; i < nq_h; ++i) nnz_exact += pred[(size_t)i];
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, 0, s, &bm);
   if (rc) return rc;
+  bm->h_rc_pred = static_cast<int*>(std::malloc(sizeof(int) * std::max<size_t>(pred.size(), 1)));
+  if (!bm->h_rc_pred) {
+    free_map(bm);
+    return 5;
+  }
+  std::copy(pred.begin(), pred.end(), bm->h_rc_pred);
   bm->producer = PT_PRODUCER_DRAFT;
   bm->d_ctx = ctx_len;
   bm->d_bs = block_size;
@@ -1431,7 +1478,7 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
   do {
     if ((rc = pool_alloc(&bm->d_blk, sizeof(int4) * blk.size(), bm->device, s))) break;
     if (n_blocks > 0 && (rc = upload(bm->d_blk, blk.data(), sizeof(int4) * (size_t)n_blocks, bm->device, s))) break;
-    rc = finish_map(bm, s, -1);
+    rc = finish_map(bm, s, nnz_exact);  // every listed tile may be partial
   } while (0);
   if (rc) {
     free_map(bm);
