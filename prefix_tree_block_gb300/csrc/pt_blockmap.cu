@@ -261,6 +261,123 @@ __global__ void k_classify(int T, int BM, int BN, int nq, int nk, const int* nod
   }
 }
 
+// Tree maps whose lists the host built (128 x 128 tiles): one launch writes
+// the token table (blocks [0, tok_blocks), as k_tree_tokens) and, in the
+// other blocks, copies the host lists from the packed upload into the map and
+// classifies every listed tile, full or partial, numbering partial tiles in
+// the order they are found (a mask slot is reached only through pidx and
+// pidxT).  Packed upload (ints): counters[4] (zero) | q_ptr[nq + 1] |
+// k_ptr[nk + 1] | q_order[nq] | k_order[nk] | kv_idx[nnz] | q_idx[nnz] |
+// eT[nnz] (kv-major position of each q-major entry).  counters[0] counts full
+// tiles and counters[1] hands out mask slots.  A listed tile that keeps
+// nothing would mean the host's lists are wrong: it is recorded as an error
+// and kept as a partial tile (its mask is empty, so results stay exact).
+__global__ void k_tree_listed(int T, int tpad, int N, const int* __restrict__ node_start,
+                              const int* __restrict__ node_end, const int* __restrict__ parent,
+                              const int* __restrict__ tin, const int* __restrict__ tout, pt_tok* __restrict__ tok,
+                              int* __restrict__ node_of, int tok_blocks, int* __restrict__ pk, int nq, int nk, int nnz,
+                              int* __restrict__ q_ptr, int* __restrict__ k_ptr, int* __restrict__ q_order,
+                              int* __restrict__ k_order, int* __restrict__ kv_idx, int* __restrict__ q_idx,
+                              uint8_t* __restrict__ kind, int* __restrict__ pidx, uint8_t* __restrict__ kindT,
+                              int* __restrict__ pidxT, int2* __restrict__ slot_tile, long long p_cap) {
+  if ((int)blockIdx.x < tok_blocks) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= tpad) return;
+    if (t >= T) {
+      tok[t] = pt_tok{INT_MAX, 0};
+      return;
+    }
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (node_end[mid] > t)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    tok[t] = pt_tok{tin[lo], tout[lo]};
+    node_of[t] = lo;
+    return;
+  }
+  int* counters = pk;
+  const int* s_qp = pk + 4;
+  const int* s_kp = s_qp + nq + 1;
+  const int* s_qo = s_kp + nk + 1;
+  const int* s_ko = s_qo + nq;
+  const int* s_kv = s_ko + nk;
+  const int* s_qi = s_kv + nnz;
+  const int* s_et = s_qi + nnz;
+  const long long tid = (long long)(blockIdx.x - tok_blocks) * blockDim.x + threadIdx.x;
+  const long long nth = (long long)(gridDim.x - tok_blocks) * blockDim.x;
+  // the host lists into the map
+  const long long n_small = (long long)2 * nq + 2 * nk + 2 + 2 * (long long)nnz;
+  for (long long x = tid; x < n_small; x += nth) {
+    long long y = x;
+    if (y < nq + 1) { q_ptr[y] = s_qp[y]; continue; }
+    y -= nq + 1;
+    if (y < nk + 1) { k_ptr[y] = s_kp[y]; continue; }
+    y -= nk + 1;
+    if (y < nq) { q_order[y] = s_qo[y]; continue; }
+    y -= nq;
+    if (y < nk) { k_order[y] = s_ko[y]; continue; }
+    y -= nk;
+    if (y < nnz) { kv_idx[y] = s_kv[y]; continue; }
+    y -= nnz;
+    q_idx[y] = s_qi[y];
+  }
+  // classes of the listed tiles: one warp per entry
+  const int lane = threadIdx.x & 31;
+  for (long long e = tid >> 5; e < nnz; e += nth >> 5) {
+    int lo = 0, hi = nq - 1;  // q tile of the entry: last i with q_ptr[i] <= e
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_qp[mid] <= e)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int i = lo, j = s_kv[e];
+    const long long q0 = (long long)i * 128, k0 = (long long)j * 128, k1 = k0 + 128;
+    const long long qlast = q0 + 127 < T - 1 ? q0 + 127 : T - 1;
+    long long kept = 0;
+    for (long long q = q0 + lane; q <= qlast; q += 32) {
+      int a = 0, b = N - 1;
+      while (a < b) {
+        const int mid = (a + b) >> 1;
+        if (node_end[mid] > q)
+          b = mid;
+        else
+          a = mid + 1;
+      }
+      kept += overlap(node_start[a], q + 1, k0, k1);
+      for (int u = parent[a]; u != -1; u = parent[u]) kept += overlap(node_start[u], node_end[u], k0, k1);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
+    if (lane == 0) {
+      const bool in_range = q0 + 128 <= T && k1 <= T;
+      const bool full = in_range && kept == 128LL * 128;
+      if (kept == 0) record_status(PT_STATUS_INVALID);
+      const int et = s_et[e];
+      if (full) {
+        kind[e] = kindT[et] = PT_KIND_FULL;
+        pidx[e] = pidxT[et] = -1;
+        atomicAdd(&counters[0], 1);
+      } else {
+        kind[e] = kindT[et] = PT_KIND_PARTIAL;
+        const int slot = atomicAdd(&counters[1], 1);
+        if (slot < p_cap) {
+          pidx[e] = pidxT[et] = slot;
+          slot_tile[slot] = make_int2(i, j);
+        } else {  // more partial tiles than the allocation's bound: never written past it
+          pidx[e] = pidxT[et] = -1;
+          record_status(PT_STATUS_INVALID);
+        }
+      }
+    }
+  }
+}
+
 // Exclusive scans of up to three small arrays in one block (lengths up to a
 // few hundred thousand): out[0..n] with out[n] the total.
 __global__ void k_scan3(const int* a, int na, int* oa, const int* b, int nb, int* ob, const int* c, int nc, int* oc) {
@@ -444,9 +561,12 @@ __device__ __forceinline__ void tile_masks(int T, const pt_tok* tok, const int2*
 // All partial tiles, grid-stride: slots 0 .. n_partial - 1, n_partial = n_known
 // when that is >= 0, else nnz - n_full read on the device (at most p_cap).
 __global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols,
-                        long long n_known, const int* nnz_total, const int* n_full, long long p_cap) {
+                        long long n_known, const int* nnz_total, const int* n_full, long long p_cap,
+                        int* host_counters = nullptr) {
   __shared__ pt_tok tq[128], tk[128];
   __shared__ uint32_t kstart[4], qstart[4];
+  // the full-tile count to the host's mapped staging (host-built lists)
+  if (host_counters && blockIdx.x == 0 && threadIdx.x < 4) host_counters[threadIdx.x] = n_full[threadIdx.x];
   const long long n_part = min(n_known >= 0 ? n_known : (long long)(*nnz_total - *n_full), p_cap);
   for (long long s = blockIdx.x; s < n_part; s += gridDim.x) {
     tile_masks(T, tok, slot_tile, mask_rows, mask_cols, s, tq, tk, kstart, qstart);
@@ -1051,6 +1171,105 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
 
 }  // namespace
 
+// Tail of the tree builder at 128 x 128 tiles when the host built the lists
+// (row_kv: kv blocks per q tile, ascending, lengths in bm->h_rc_pred):
+// derive the transpose, longest-first orders and each entry's kv-major
+// position on the host, upload them in one packed copy with zeroed counters,
+// then two launches: tokens plus tile classes, and masks.  Nothing waits for
+// the device; the full-tile count reaches the host's staging behind an event.
+int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const std::vector<int>& row_kv, int N) {
+  const int nq = bm->nq, nk = bm->nk, dev = bm->device;
+  const int* rc_row = bm->h_rc_pred;
+  const int* rc_col = bm->h_rc_pred + nq;
+  const int64_t nnz = (int64_t)row_kv.size();
+  const int64_t p_alloc = std::min<int64_t>(p_bound >= 0 ? p_bound : nnz, nnz);
+  if (nnz * 18 + p_alloc * 4096 > ((int64_t)1 << 30) || nnz > INT_MAX / 4) {
+    // too large to allocate at the bound: the device path, which sizes the lists exactly
+    k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>(bm->T, bm->tpad, N, bm->node_end,
+                                                         bm->node_start + 3 * (size_t)N,
+                                                         bm->node_start + 4 * (size_t)N, bm->tok, bm->node_of);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) {
+      set_error("block map kernel launch failed");
+      return 3;
+    }
+    return finish_map(bm, s, p_bound);
+  }
+  // packed: counters[4] | q_ptr | k_ptr | q_order | k_order | kv_idx | q_idx | eT
+  const size_t n_pk = 4 + (size_t)(nq + 1) + (nk + 1) + nq + nk + 3 * (size_t)nnz;
+  std::vector<int> pk(n_pk, 0);
+  int* qp = pk.data() + 4;
+  int* kp = qp + nq + 1;
+  int* qo = kp + nk + 1;
+  int* ko = qo + nq;
+  int* kv = ko + nk;
+  int* qi = kv + nnz;
+  int* et = qi + nnz;
+  for (int i = 0; i < nq; ++i) qp[i + 1] = qp[i] + rc_row[i];
+  for (int j = 0; j < nk; ++j) kp[j + 1] = kp[j] + rc_col[j];
+  std::copy(row_kv.begin(), row_kv.end(), kv);
+  {
+    std::vector<int> fill(kp, kp + nk);
+    for (int i = 0; i < nq; ++i)  // q tiles ascending within each kv block
+      for (int e = qp[i]; e < qp[i + 1]; ++e) {
+        const int pos = fill[(size_t)kv[e]]++;
+        qi[pos] = i;
+        et[e] = pos;
+      }
+  }
+  // longest first, ties by index (the device's orders use the same rule)
+  for (int i = 0; i < nq; ++i) qo[i] = i;
+  for (int j = 0; j < nk; ++j) ko[j] = j;
+  std::stable_sort(qo, qo + nq, [&](int a, int b) { return rc_row[a] > rc_row[b]; });
+  std::stable_sort(ko, ko + nk, [&](int a, int b) { return rc_col[a] > rc_col[b]; });
+  int rc = 0;
+  void* tmp = nullptr;
+  void* tmpB = nullptr;
+  do {
+    if ((rc = alloc_lists(bm, nnz, p_alloc, s))) break;
+    if ((rc = pool_alloc(&tmp, sizeof(int) * n_pk, dev, s))) break;
+    if ((rc = upload(tmp, pk.data(), sizeof(int) * n_pk, dev, s))) break;
+    if ((rc = pool_alloc(&tmpB, sizeof(int2) * (size_t)std::max<int64_t>(p_alloc, 1), dev, s))) break;
+    int2* slot_tile = static_cast<int2*>(tmpB);
+    int* counters = static_cast<int*>(tmp);
+    PinnedSlot sl;
+    if ((rc = pinned_acquire(dev, sizeof(int) * 4, &sl))) break;
+    bm->counts_host = sl.host;
+    bm->counts_dev = sl.dev;
+    bm->counts_cap = sl.cap;
+    bm->counts_ev = sl.ev;
+    bm->counts_ready = false;
+    bm->lists_on_host = true;
+    {
+      ProfScope ps(s, "blockmap_classify");  // tokens, the lists into place, tile classes
+      const int tok_blocks = (bm->tpad + 255) / 256;
+      const long long list_work = std::max<long long>((long long)nnz * 32, 2LL * nq + 2LL * nk + 2 + 2 * nnz);
+      const int list_blocks = (int)std::max(1LL, std::min<long long>((list_work + 255) / 256, (long long)num_sms(dev) * 8));
+      k_tree_listed<<<tok_blocks + list_blocks, 256, 0, s>>>(
+          bm->T, bm->tpad, N, bm->node_start, bm->node_end, bm->parent, bm->node_start + 3 * (size_t)N,
+          bm->node_start + 4 * (size_t)N, bm->tok, bm->node_of, tok_blocks, counters, nq, nk, (int)nnz, bm->q_ptr,
+          bm->k_ptr, bm->q_order, bm->k_order, bm->kv_idx, bm->q_idx, bm->kind, bm->pidx, bm->kindT, bm->pidxT,
+          slot_tile, (long long)bm->p_cap);
+      PT_LAUNCHED(1);
+    }
+    {
+      ProfScope ps(s, "blockmap_lists");  // the partial tiles' masks
+      const long long grid = std::max<long long>(1, std::min<long long>(p_alloc, (long long)num_sms(dev) * 16));
+      k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, -1LL,
+                                             bm->q_ptr + nq, counters, (long long)bm->p_cap,
+                                             static_cast<int*>(sl.dev));
+      PT_LAUNCHED(1);
+      if (cudaEventRecord(sl.ev, s) != cudaSuccess) {
+        rc = 3;
+        break;
+      }
+    }
+  } while (0);
+  pool_free(tmp, s);
+  pool_free(tmpB, s);
+  return rc;
+}
+
 std::mutex g_counts_mu;
 
 int ensure_counts(const pt_blockmap* cbm) {
@@ -1066,7 +1285,12 @@ int ensure_counts(const pt_blockmap* cbm) {
   const size_t ncnt = (size_t)4 + bm->nq + bm->nk;
   bm->h_counts = static_cast<int*>(std::malloc(sizeof(int) * ncnt));
   if (!bm->h_counts) return 5;
-  std::memcpy(bm->h_counts, bm->counts_host, sizeof(int) * ncnt);
+  if (bm->lists_on_host) {  // the device sent its four counters; the lengths are the host's own
+    std::memcpy(bm->h_counts, bm->counts_host, sizeof(int) * 4);
+    std::memcpy(bm->h_counts + 4, bm->h_rc_pred, sizeof(int) * (size_t)(bm->nq + bm->nk));
+  } else {
+    std::memcpy(bm->h_counts, bm->counts_host, sizeof(int) * ncnt);
+  }
   PinnedSlot sl;
   sl.host = bm->counts_host;
   sl.dev = bm->counts_dev;
@@ -1245,11 +1469,13 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
   // of n (keep = ancestor-or-self and kv <= q; ancestors come first).
   const int nq_h = (int)((T + BM - 1) / BM), nk_h = (int)((T + BN - 1) / BN);
   std::vector<int> pred((size_t)nq_h + nk_h, 0);
+  std::vector<int> row_kv;  // the q-major lists themselves, kv blocks ascending per q tile
   {
     std::vector<int> stamp((size_t)std::max(nk_h, 1), -1);
     int n0 = 0;  // nodes are in token order: the first that may reach tile i
     for (int i = 0; i < nq_h; ++i) {
       const long long r_lo = (long long)i * BM, r_hi = std::min<long long>(r_lo + BM, T);
+      const size_t row0 = row_kv.size();
       while (n0 < N && end[n0] <= r_lo) ++n0;
       auto mark = [&](long long a, long long b) {  // kv tokens [a, b]
         for (long long j = a / BN; j <= b / BN; ++j)
@@ -1257,6 +1483,7 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
             stamp[(size_t)j] = i;
             ++pred[(size_t)i];
             ++pred[(size_t)nq_h + j];
+            row_kv.push_back((int)j);
           }
       };
       for (int n = n0; n < N && start[n] < r_hi; ++n) {
@@ -1265,6 +1492,7 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
         for (int a = parent[n]; a >= 0; a = parent[a])
           if (node_lengths[a] > 0) mark(start[a], end[a] - 1);
       }
+      std::sort(row_kv.begin() + (long)row0, row_kv.end());
     }
   }
   pt_blockmap* bm = nullptr;
@@ -1280,13 +1508,14 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
   do {
     // one upload of start | end | parent | tin | tout into the map's node tables
     if (N > 0 && (rc = upload(bm->node_start, tab.data(), sizeof(int) * (size_t)5 * N, bm->device, s))) break;
-    if (bm->tpad > 0) {
+    if (bm->tpad > 0 && !(BM == 128 && BN == 128 && T > 0)) {  // the listed path writes the tokens itself
       const int* d_tin = bm->node_start + 3 * (size_t)N;
       k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>((int)T, bm->tpad, N, bm->node_end, d_tin, d_tin + N,
                                                            bm->tok, bm->node_of);
       PT_LAUNCHED(1);
     }
-    rc = finish_map(bm, s, p_bound);
+    rc = (BM == 128 && BN == 128 && T > 0) ? finish_map_listed(bm, s, p_bound, row_kv, N)
+                                           : finish_map(bm, s, p_bound);
   } while (0);
   if (rc) {
     free_map(bm);

@@ -72,6 +72,7 @@ struct pt_blockmap {
   // node intervals ([nq] rows | [nk] columns), usable before the device's
   // arrive; ensure_counts checks them against the device's
   int* h_rc_pred;
+  bool lists_on_host;  // the host built the lists; only the full-tile count comes from the device
   int64_t nnz_cap;    // list entries allocated (>= nnz)
   int64_t p_cap;      // mask slots allocated (>= n_partial)
   // Which rule the map encodes: tree/segment labels (tok, node tables) or
