@@ -263,23 +263,30 @@ __global__ void k_classify(int T, int BM, int BN, int nq, int nk, const int* nod
 
 // Tree maps whose lists the host built (128 x 128 tiles): one launch writes
 // the token table (blocks [0, tok_blocks), as k_tree_tokens) and, in the
-// other blocks, copies the host lists from the packed upload into the map and
-// classifies every listed tile, full or partial, numbering partial tiles in
-// the order they are found (a mask slot is reached only through pidx and
-// pidxT).  Packed upload (ints): counters[4] (zero) | q_ptr[nq + 1] |
+// other blocks, copies the node tables and the host lists from the packed
+// upload into the map and classifies every listed tile, full or partial,
+// numbering partial tiles in the order they are found (a mask slot is
+// reached only through pidx and pidxT).  Packed upload (ints): counters[4]
+// (zero) | node tables[5 * N] | q_ptr[nq + 1] |
 // k_ptr[nk + 1] | q_order[nq] | k_order[nk] | kv_idx[nnz] | q_idx[nnz] |
 // eT[nnz] (kv-major position of each q-major entry).  counters[0] counts full
 // tiles and counters[1] hands out mask slots.  A listed tile that keeps
 // nothing would mean the host's lists are wrong: it is recorded as an error
 // and kept as a partial tile (its mask is empty, so results stay exact).
-__global__ void k_tree_listed(int T, int tpad, int N, const int* __restrict__ node_start,
-                              const int* __restrict__ node_end, const int* __restrict__ parent,
-                              const int* __restrict__ tin, const int* __restrict__ tout, pt_tok* __restrict__ tok,
+__global__ void k_tree_listed(int T, int tpad, int N, int* __restrict__ map_tabs, pt_tok* __restrict__ tok,
                               int* __restrict__ node_of, int tok_blocks, int* __restrict__ pk, int nq, int nk, int nnz,
                               int* __restrict__ q_ptr, int* __restrict__ k_ptr, int* __restrict__ q_order,
                               int* __restrict__ k_order, int* __restrict__ kv_idx, int* __restrict__ q_idx,
                               uint8_t* __restrict__ kind, int* __restrict__ pidx, uint8_t* __restrict__ kindT,
                               int* __restrict__ pidxT, int2* __restrict__ slot_tile, long long p_cap) {
+  // node tables (start | end | parent | tin | tout) come in the packed upload
+  // and are read from there; the list blocks also copy them into the map
+  const int* tabs = pk + 4;
+  const int* node_start = tabs;
+  const int* node_end = tabs + N;
+  const int* parent = tabs + 2 * N;
+  const int* tin = tabs + 3 * N;
+  const int* tout = tabs + 4 * N;
   if ((int)blockIdx.x < tok_blocks) {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= tpad) return;
@@ -300,7 +307,7 @@ __global__ void k_tree_listed(int T, int tpad, int N, const int* __restrict__ no
     return;
   }
   int* counters = pk;
-  const int* s_qp = pk + 4;
+  const int* s_qp = tabs + 5 * N;
   const int* s_kp = s_qp + nq + 1;
   const int* s_qo = s_kp + nk + 1;
   const int* s_ko = s_qo + nq;
@@ -310,9 +317,11 @@ __global__ void k_tree_listed(int T, int tpad, int N, const int* __restrict__ no
   const long long tid = (long long)(blockIdx.x - tok_blocks) * blockDim.x + threadIdx.x;
   const long long nth = (long long)(gridDim.x - tok_blocks) * blockDim.x;
   // the host lists into the map
-  const long long n_small = (long long)2 * nq + 2 * nk + 2 + 2 * (long long)nnz;
+  const long long n_small = (long long)5 * N + 2 * nq + 2 * nk + 2 + 2 * (long long)nnz;
   for (long long x = tid; x < n_small; x += nth) {
     long long y = x;
+    if (y < 5LL * N) { map_tabs[y] = tabs[y]; continue; }
+    y -= 5LL * N;
     if (y < nq + 1) { q_ptr[y] = s_qp[y]; continue; }
     y -= nq + 1;
     if (y < nk + 1) { k_ptr[y] = s_kp[y]; continue; }
@@ -1177,7 +1186,8 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
 // position on the host, upload them in one packed copy with zeroed counters,
 // then two launches: tokens plus tile classes, and masks.  Nothing waits for
 // the device; the full-tile count reaches the host's staging behind an event.
-int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const std::vector<int>& row_kv, int N) {
+int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const std::vector<int>& row_kv, int N,
+                      const int* tab) {
   const int nq = bm->nq, nk = bm->nk, dev = bm->device;
   const int* rc_row = bm->h_rc_pred;
   const int* rc_col = bm->h_rc_pred + nq;
@@ -1185,6 +1195,7 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
   const int64_t p_alloc = std::min<int64_t>(p_bound >= 0 ? p_bound : nnz, nnz);
   if (nnz * 18 + p_alloc * 4096 > ((int64_t)1 << 30) || nnz > INT_MAX / 4) {
     // too large to allocate at the bound: the device path, which sizes the lists exactly
+    if (int rc = upload(bm->node_start, tab, sizeof(int) * (size_t)5 * N, dev, s)) return rc;
     k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>(bm->T, bm->tpad, N, bm->node_end,
                                                          bm->node_start + 3 * (size_t)N,
                                                          bm->node_start + 4 * (size_t)N, bm->tok, bm->node_of);
@@ -1195,10 +1206,11 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
     }
     return finish_map(bm, s, p_bound);
   }
-  // packed: counters[4] | q_ptr | k_ptr | q_order | k_order | kv_idx | q_idx | eT
-  const size_t n_pk = 4 + (size_t)(nq + 1) + (nk + 1) + nq + nk + 3 * (size_t)nnz;
+  // packed: counters[4] | node tables[5N] | q_ptr | k_ptr | q_order | k_order | kv_idx | q_idx | eT
+  const size_t n_pk = 4 + 5 * (size_t)N + (size_t)(nq + 1) + (nk + 1) + nq + nk + 3 * (size_t)nnz;
   std::vector<int> pk(n_pk, 0);
-  int* qp = pk.data() + 4;
+  std::copy(tab, tab + 5 * (size_t)N, pk.data() + 4);
+  int* qp = pk.data() + 4 + 5 * (size_t)N;
   int* kp = qp + nq + 1;
   int* qo = kp + nk + 1;
   int* ko = qo + nq;
@@ -1243,11 +1255,10 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
     {
       ProfScope ps(s, "blockmap_classify");  // tokens, the lists into place, tile classes
       const int tok_blocks = (bm->tpad + 255) / 256;
-      const long long list_work = std::max<long long>((long long)nnz * 32, 2LL * nq + 2LL * nk + 2 + 2 * nnz);
+      const long long list_work = std::max<long long>((long long)nnz * 32, 5LL * N + 2LL * nq + 2LL * nk + 2 + 2 * nnz);
       const int list_blocks = (int)std::max(1LL, std::min<long long>((list_work + 255) / 256, (long long)num_sms(dev) * 8));
       k_tree_listed<<<tok_blocks + list_blocks, 256, 0, s>>>(
-          bm->T, bm->tpad, N, bm->node_start, bm->node_end, bm->parent, bm->node_start + 3 * (size_t)N,
-          bm->node_start + 4 * (size_t)N, bm->tok, bm->node_of, tok_blocks, counters, nq, nk, (int)nnz, bm->q_ptr,
+          bm->T, bm->tpad, N, bm->node_start, bm->tok, bm->node_of, tok_blocks, counters, nq, nk, (int)nnz, bm->q_ptr,
           bm->k_ptr, bm->q_order, bm->k_order, bm->kv_idx, bm->q_idx, bm->kind, bm->pidx, bm->kindT, bm->pidxT,
           slot_tile, (long long)bm->p_cap);
       PT_LAUNCHED(1);
@@ -1507,15 +1518,16 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
   std::copy(pred.begin(), pred.end(), bm->h_rc_pred);
   do {
     // one upload of start | end | parent | tin | tout into the map's node tables
-    if (N > 0 && (rc = upload(bm->node_start, tab.data(), sizeof(int) * (size_t)5 * N, bm->device, s))) break;
-    if (bm->tpad > 0 && !(BM == 128 && BN == 128 && T > 0)) {  // the listed path writes the tokens itself
+    const bool listed = BM == 128 && BN == 128 && T > 0;  // tables go with the host lists
+    if (N > 0 && !listed && (rc = upload(bm->node_start, tab.data(), sizeof(int) * (size_t)5 * N, bm->device, s)))
+      break;
+    if (bm->tpad > 0 && !listed) {  // the listed path writes the tokens itself
       const int* d_tin = bm->node_start + 3 * (size_t)N;
       k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>((int)T, bm->tpad, N, bm->node_end, d_tin, d_tin + N,
                                                            bm->tok, bm->node_of);
       PT_LAUNCHED(1);
     }
-    rc = (BM == 128 && BN == 128 && T > 0) ? finish_map_listed(bm, s, p_bound, row_kv, N)
-                                           : finish_map(bm, s, p_bound);
+    rc = listed ? finish_map_listed(bm, s, p_bound, row_kv, N, tab.data()) : finish_map(bm, s, p_bound);
   } while (0);
   if (rc) {
     free_map(bm);

@@ -34,6 +34,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cstring>
 #include <cmath>
 #include <mutex>
 #include <queue>
@@ -1714,11 +1715,13 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
   bm->bwd_items = bm->bwd_mem;
   bm->bwd_splits = static_cast<char*>(bm->bwd_mem) + bi;
   bm->bwd_cta = static_cast<char*>(bm->bwd_mem) + bi + bs;
-  if (!packed.empty() && (rc = upload(bm->bwd_items, packed.data(), sizeof(DkdvItem) * packed.size(), bm->device, s)))
-    return rc;
-  if (!splits.empty() && (rc = upload(bm->bwd_splits, splits.data(), sizeof(int4) * splits.size(), bm->device, s)))
-    return rc;
-  if ((rc = upload(bm->bwd_cta, cta.data(), bc, bm->device, s))) return rc;
+  {  // one upload in the device layout: items | splits | CTA index
+    std::vector<char> host(bi + bs + bc, 0);
+    if (!packed.empty()) std::memcpy(host.data(), packed.data(), sizeof(DkdvItem) * packed.size());
+    if (!splits.empty()) std::memcpy(host.data() + bi, splits.data(), sizeof(int4) * splits.size());
+    std::memcpy(host.data() + bi + bs, cta.data(), bc);
+    if ((rc = upload(bm->bwd_mem, host.data(), host.size(), bm->device, s))) return rc;
+  }
   bm->bwd_g = g;
   bm->bwd_hkv = Hkv;
   bm->bwd_max_slots = max_slots;
@@ -1811,9 +1814,12 @@ int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, 
   if (rc) return rc;
   bm->dq_items = bm->dq_mem;
   bm->dq_cta = static_cast<char*>(bm->dq_mem) + bi;
-  if (!packed.empty() && (rc = upload(bm->dq_items, packed.data(), sizeof(int4) * packed.size(), bm->device, s)))
-    return rc;
-  if ((rc = upload(bm->dq_cta, cta.data(), bc, bm->device, s))) return rc;
+  {  // one upload in the device layout: items | CTA records
+    std::vector<char> host(bi + bc, 0);
+    if (!packed.empty()) std::memcpy(host.data(), packed.data(), sizeof(int4) * packed.size());
+    std::memcpy(host.data() + bi, cta.data(), bc);
+    if ((rc = upload(bm->dq_mem, host.data(), host.size(), bm->device, s))) return rc;
+  }
   if (!empty.empty()) {
     bm->h_dq_empty = static_cast<int*>(std::malloc(sizeof(int) * empty.size()));
     if (!bm->h_dq_empty) {
