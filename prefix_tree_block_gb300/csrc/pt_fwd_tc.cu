@@ -65,8 +65,8 @@ struct FwdCfg {
   static constexpr int OFF_BAR = OFF_META + 16 * ((VS * 4 + 15) / 16);
   // q_full[QB] q_empty[QB] k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
   // s_full[NH*SB] p_full[NH*SB] o_full[NH] o_free[NH] mma_done
-  // (OVL) s_free[NH] p_free[NH]
-  static constexpr int NBAR = 2 * QB + 2 * KS + 2 * VS + 2 * NH * SB + 2 * NH + 1 + (OVL ? 2 * NH : 0);
+  // (OVL) s_free[NH] p_free[NH] o_written[NH]
+  static constexpr int NBAR = 2 * QB + 2 * KS + 2 * VS + 2 * NH * SB + 2 * NH + 1 + (OVL ? 3 * NH : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TM_S = 0;                            // S(h, b) at (h * SB + b) * 128
@@ -124,7 +124,7 @@ __host__ __device__ __forceinline__ int fwd_items(int nq, int Hq, int Hkv) {
 template <int D, int NH>
 __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-             const __grid_constant__ CUtensorMap mV, const FwdParams p) {
+             const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, const FwdParams p) {
   using C = FwdCfg<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   uint64_t* mma_done = o_free + NH;
   uint64_t* s_free = mma_done + 1;          // [NH] (OVL) S(h) loaded by the softmax
   uint64_t* p_free = s_free + NH;           // [NH] (OVL) PV(h) done reading P(h)
+  uint64_t* o_written = p_free + NH;        // [NH] (OVL) the warpgroup's O rows are in shared memory
   int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -153,12 +154,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   if (threadIdx.x == PRODUCER * 32) {
     for (int b = 0; b < C::QB; ++b) {
       mbar_init(q_full + b, 1);
-      mbar_init(q_empty + b, 1);
+      // OVL: each softmax warpgroup's O store, made from the item's Q buffer,
+      // frees it; else the item's last S MMA does
+      mbar_init(q_empty + b, C::OVL ? NH : 1);
     }
     if (C::OVL)
       for (int h = 0; h < NH; ++h) {
         mbar_init(s_free + h, 128);
         mbar_init(p_free + h, 1);
+        mbar_init(o_written + h, 128);
       }
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(k_full + s, 1);
@@ -182,6 +186,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     prefetch_tmap(&mQ);
     prefetch_tmap(&mK);
     prefetch_tmap(&mV);
+    if (C::OVL) prefetch_tmap(&mO);
   }
   if (warp == ISSUER) {
     tmem_alloc(tmem_slot, 512);
@@ -326,8 +331,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
                 issue_s(h, u, ks);
               }
               if (!ok) break;
-              mma_commit(k_empty + ks);
-              if (jj == n - 1) mma_commit(q_empty + qb);
+              mma_commit(k_empty + ks);  // (OVL: the Q buffer is freed by the epilogue's O store)
             }
             if (jj >= 1) {
               const int i = jj - 1;
@@ -406,6 +410,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t o_col = C::TM_O + h * D;
     uint32_t sc = 0, vc = 0, pvc = 0, itv = 0;
+    uint32_t qi = 0;  // items with kv blocks so far: the Q buffer of an item is qi % QB
     bool ok = true;
     for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
       const int w = snake_item(rr, blockIdx.x, gridDim.x);
@@ -415,6 +420,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       const int e0 = p.q_ptr[tile], n = p.q_ptr[tile + 1] - e0;
       if (h >= nh) {  // this warpgroup has no head in the item; the V ring still advances
         vc += n;
+        qi += n > 0 ? 1 : 0;
         continue;
       }
       const int head = h0 + h;
@@ -550,20 +556,62 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       }
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.O + ((size_t)q * p.Hq + head) * D;
+      if constexpr (C::OVL) {
+        // O / l into this item's Q tile of the head (the MMAs that read it are
+        // done: o_full follows the last S), in the tile's 128-byte-swizzled
+        // layout, then one TMA store of the tile; the store's reads free the
+        // buffer (the warpgroup of a one-head item also arrives for the idle one)
+        const uint32_t qbuf = qi % C::QB;
+        uint8_t* obuf = smem + C::OFF_Q + (qbuf * NH + h) * C::TILE;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(tl + o_col + c * 32, orr);
-        tmem_ld_wait();
-        if (q < p.T) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tl + o_col + c * 32, orr);
+          tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             pk[k] = pack_bf16(__uint_as_float(orr[2 * k]) * inv, __uint_as_float(orr[2 * k + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          uint8_t* prow = obuf + (c >> 1) * C::PANEL + r * 128;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          for (int k = 0; k < 4; ++k) {
+            const int chunk = ((c & 1) * 4 + k) ^ (r & 7);
+            *reinterpret_cast<uint4*>(prow + chunk * 16) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                                                                      pk[4 * k + 3]);
+          }
+        }
+        fence_proxy_async_smem();  // the rows, written by this thread, for the TMA store
+        mbar_arrive(o_written + h);
+        if (r == 0) {  // one thread stores the tile once every row is in (a bounded wait)
+          ok = mbar_wait(o_written + h, itv & 1, abort_flag);
+          if (ok) {
+#pragma unroll
+            for (int pn = 0; pn < C::NP; ++pn) tma_store_3d(&mO, obuf + pn * C::PANEL, pn * 64, head, tile * C::BM);
+            bulk_commit();
+            bulk_wait_read0();
+            mbar_arrive_cnt(q_empty + qbuf, h == 0 ? (uint32_t)(NH - nh + 1) : 1u);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      } else {
+        __nv_bfloat16* orow = p.O + ((size_t)q * p.Hq + head) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tl + o_col + c * 32, orr);
+          tmem_ld_wait();
+          if (q < p.T) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              pk[k] = pack_bf16(__uint_as_float(orr[2 * k]) * inv, __uint_as_float(orr[2 * k + 1]) * inv);
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
         }
       }
       if (q < p.T) p.LSE[(size_t)head * p.T + q] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -573,8 +621,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       vc += n;
       pvc += n;
       ++itv;
+      ++qi;
     }
     if (!ok) *abort_flag = 1;
+    if (C::OVL && r == 0) bulk_wait0();  // this warpgroup's O stores have landed
   }
 
   tc_fence_before();
@@ -602,9 +652,9 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
     set_error("forward kernel: block map has no tile masks");
     return 1;
   }
-  CUtensorMap mQ, mK, mV;
+  CUtensorMap mQ, mK, mV, mO;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mK, K, T, Hkv, D, 128) ||
-      !make_tmap_thd(&mV, V, T, Hkv, D, 128))
+      !make_tmap_thd(&mV, V, T, Hkv, D, 128) || !make_tmap_thd(&mO, O, T, Hq, D, 128))
     return 3;
   FwdParams p;
   p.q_ptr = bm->q_ptr;
@@ -624,7 +674,7 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
   if (grid <= 0) return 0;
   {
     ProfScope ps(s, "fwd_tc");
-    k_fwd_tc<D, NH><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mQ, mK, mV, p);
+    k_fwd_tc<D, NH><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mQ, mK, mV, mO, p);
   }
   count_launch();
   cudaError_t e = cudaGetLastError();
