@@ -201,6 +201,8 @@ struct BwdBars {
   uint64_t s_full[2], p_full[2];
   uint64_t acc_full, acc_free, mma_done;
   uint64_t s_free;   // compute warpgroups have loaded S/dP: the MMA may overwrite them
+  uint64_t o_written;  // (dq) every compute thread has put its output rows into the staging tile
+  uint64_t o_stored;   // (dq) the staging tile's TMA store has read it
   uint64_t ps_free;  // the accumulate MMAs have read the packed P/dS region
 };
 
@@ -220,6 +222,8 @@ __device__ __forceinline__ void init_bars(BwdBars<S>* b) {
   mbar_init(&b->acc_free, 256);
   mbar_init(&b->mma_done, 1);
   mbar_init(&b->s_free, 256);
+  mbar_init(&b->o_written, 256);
+  mbar_init(&b->o_stored, 1);
   mbar_init(&b->ps_free, 1);
 }
 
@@ -623,7 +627,10 @@ struct DqL {
   static constexpr int OFF_ST = 2 * C::TILE;  // stages: K | V | row masks
   static constexpr int ST_K = 0, ST_V = C::TILE, ST_M = 2 * C::TILE;
   static constexpr int ST_BYTES = ST_M + 2048;
-  static constexpr int OFF_META = OFF_ST + C::STAGES * ST_BYTES;
+  // dQ tile staged for its TMA store (128-byte swizzled panels, 1024-aligned)
+  static constexpr int OFF_OST = OFF_ST + C::STAGES * ST_BYTES;
+  static_assert(OFF_OST % 1024 == 0, "staging tile alignment");
+  static constexpr int OFF_META = OFF_OST + C::TILE;
   static constexpr int OFF_BAR = OFF_META + 64;
   static constexpr int OFF_MISC = OFF_BAR + (int)sizeof(BwdBars<C::STAGES>);
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
@@ -635,7 +642,8 @@ struct DqL {
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     k_bwd_dq(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
-             const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const BwdParams p) {
+             const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+             const __grid_constant__ CUtensorMap mdQ, const BwdParams p) {
   using C = BwdCfg<D>;
   using L = DqL<D>;
   constexpr int S = C::STAGES;
@@ -658,6 +666,7 @@ __global__ void __launch_bounds__(320, 1)
     prefetch_tmap(&mdO);
     prefetch_tmap(&mK);
     prefetch_tmap(&mV);
+    prefetch_tmap(&mdQ);
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
@@ -857,19 +866,57 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
+      // dQ rows into the staging tile (this warpgroup's half of every row),
+      // once the previous item's store has read it; then one TMA store
+      if (it > 0) {
+        ok = mbar_wait(&B->o_stored, (it - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      uint8_t* ost = smem + L::OFF_OST;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
-        tmem_ld32(tl + C::TM_ACC0 + hw * (D / 2) + c * 32, v);
+        const int col = hw * (D / 2) + c * 32;  // first of these 32 columns
+        tmem_ld32(tl + C::TM_ACC0 + col, v);
         tmem_ld_wait();
-        if (q < p.T) store_row32(orow + c * 32, v, p.scale);
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          pk[k] = pack_bf16(__uint_as_float(v[2 * k]) * p.scale, __uint_as_float(v[2 * k + 1]) * p.scale);
+        uint8_t* prow = ost + (col >> 6) * C::PANEL + r * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int chunk = (((col & 63) >> 3) + k) ^ (r & 7);
+          *reinterpret_cast<uint4*>(prow + chunk * 16) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                                                                    pk[4 * k + 3]);
+        }
       }
       tc_fence_before();
       mbar_arrive(&B->acc_free);
+      fence_proxy_async_smem();
+      mbar_arrive(&B->o_written);
+      if (threadIdx.x == 0) {
+        ok = mbar_wait(&B->o_written, it & 1, abort_flag);
+        if (ok) {
+#pragma unroll
+          for (int pn = 0; pn < C::NP; ++pn) tma_store_3d(&mdQ, ost + pn * C::PANEL, pn * 64, h, tile * 128);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&B->o_stored);
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       sc += n;
       ++it;
     }
     if (!ok) *abort_flag = 1;
+    if (threadIdx.x == 0) bulk_wait0();  // the last dQ store has landed
   }
 
   tc_fence_before();
@@ -1869,9 +1916,10 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
     k_bwd_prep<D><<<(unsigned)(Tpad / kPrepTokens), 256, sm, s>>>(
         static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
   }
-  CUtensorMap mQ, mdO, mK, mV;
+  CUtensorMap mQ, mdO, mK, mV, mdQ;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128) ||
-      !make_tmap_thd(&mK, K, T, Hkv, D, 128) || !make_tmap_thd(&mV, V, T, Hkv, D, 128))
+      !make_tmap_thd(&mK, K, T, Hkv, D, 128) || !make_tmap_thd(&mV, V, T, Hkv, D, 128) ||
+      !make_tmap_thd(&mdQ, dQ, T, Hq, D, 128))
     return 3;
   BwdParams p{};
   p.delta = delta;
@@ -1932,7 +1980,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       if (bm->dq_n_items > 0)
         k_bwd_dq_pipe<D><<<bm->dq_grid, DqpCfg<D>::THREADS, DqpL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
     } else {
-      k_bwd_dq<D><<<items < sms ? items : sms, 320, DqL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+      k_bwd_dq<D><<<items < sms ? items : sms, 320, DqL<D>::BYTES, s>>>(mQ, mdO, mK, mV, mdQ, p);
     }
     ++launches;
   }
