@@ -393,7 +393,7 @@ pt_status pt_sync_status(cudaStream_t stream) {
   }
   int worst = 0;
   int codes[] = {pt::take_status_blockmap(stream), pt::take_status_fwd(stream), pt::take_status_bwd(stream),
-                 pt::take_status_simt(stream)};
+                 pt::take_status_simt(stream), pt::take_status_fold(stream)};
   for (int c : codes) {
     if (c < 0) {
       set_error("pt_sync_status: could not read the device status word");

@@ -30,7 +30,12 @@
 #include <vector>
 
 #include "pt.h"
+#include "pt_device.cuh"
 #include "pt_internal.h"
+
+namespace pt {
+int take_status_fold(cudaStream_t s) { return take_status_here(s); }
+}  // namespace pt
 
 struct pt_foldplan {
   int device;
@@ -53,10 +58,16 @@ struct pt_foldplan {
   int64_t T1, TM, copiesM;
   int2* cls1;  // [n1]
   int2* clsM;  // [nM]
+  // tasks of the bulk-copy gradient: {node, first token in the node, tokens, 0};
+  // a task brings about eight rows: eight tokens of a one-sample node (one
+  // contiguous copy), or one token of a shared node with all its copies
+  int32_t n_tasks;
+  int4* tasks;
 };
 
 namespace {
 
+using namespace pt;  // device helpers (mbarriers, bulk copies, bounded waits)
 using pt::set_error;
 
 // ---------------------------------------------------------------------------
@@ -296,6 +307,116 @@ __global__ void k_unfold_grad(const E* __restrict__ droll, E* __restrict__ dflat
   }
 }
 
+// The gradient through bulk copies (rows of at most 2 KB, 16-byte multiples),
+// a warp per task.  A task is m tokens of one node, m = 8 / (copies per
+// token) rounded down, at least 1: for each copy c of the node, tokens
+// k0..k0+m-1 sit in one contiguous run of sample c's rollout row, so one lane
+// brings them all in with one bulk copy per copy (one mbarrier), and the
+// lanes add the copies in sample order in fp32 (from the first copy on) and
+// write the m rows.  A token with more copies than a round holds (m = 1) takes
+// several rounds with the sums in registers.  Whole-row bulk copies keep many
+// bytes in flight per SM without holding them in registers.
+constexpr int kBulkC = 8;         // rows per bulk round
+constexpr int kBulkWarps = 4;     // warps per block
+constexpr int kBulkMaxRow = 2048; // bytes
+
+template <class E>
+__global__ void __launch_bounds__(kBulkWarps * 32) k_unfold_grad_bulk(
+    const char* __restrict__ droll, E* __restrict__ dflat, const int4* __restrict__ node,
+    const int32_t* __restrict__ node_sp, const int32_t* __restrict__ node_samp, const int4* __restrict__ tasks,
+    int n_tasks, int W, int L) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  __shared__ uint64_t bars[kBulkWarps];
+  __shared__ volatile int abort_flag;
+  constexpr int K = 16 / (int)sizeof(E);  // elements per 16-byte vector
+  struct alignas(16) Vec {
+    E e[K];
+  };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* slot = sm + (size_t)warp * kBulkC * W;
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (lane == 0) {
+    mbar_init(&bars[warp], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int nv = W / 16;  // vectors per row, at most 128: four per lane
+  const int width = W / (int)sizeof(E);
+  uint32_t phase = 0;
+  for (int ti = blockIdx.x * kBulkWarps + warp; ti < n_tasks; ti += gridDim.x * kBulkWarps) {
+    const int4 tk = tasks[ti];
+    const int4 nd = node[tk.x];
+    const int m = tk.z;
+    const long long j0 = nd.z + tk.y, t0 = nd.x + tk.y;
+    const int c0 = node_sp[tk.x], nc = node_sp[tk.x + 1] - c0;
+    const int per_round = m > 1 ? nc : kBulkC;  // m > 1: every copy fits in one round
+    float acc[4][K];
+    for (int cb = 0; cb < nc; cb += per_round) {
+      const int n = min(per_round, nc - cb);
+      if (lane == 0) {
+        mbar_expect_tx(&bars[warp], (uint32_t)(n * m * W));
+        for (int c = 0; c < n; ++c)
+          bulk_load(slot + (size_t)c * m * W, droll + ((long long)node_samp[c0 + cb + c] * L + j0) * W,
+                    (uint32_t)(m * W), &bars[warp]);
+      }
+      const bool ok = mbar_wait(&bars[warp], phase, &abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {  // copies may still be in flight: let them land, then leave
+        mbar_wait_drain(&bars[warp], phase, 20000000LL);
+        return;
+      }
+      phase ^= 1;
+      if (m > 1) {  // all copies are here: finish each of the m rows now
+        for (int u = 0; u < m; ++u)
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const int v = lane + 32 * a;
+            if (v >= nv) continue;
+            float sum[K];
+            for (int c = 0; c < n; ++c) {
+              const Vec x = *reinterpret_cast<const Vec*>(slot + ((size_t)c * m + u) * W + v * 16);
+#pragma unroll
+              for (int e = 0; e < K; ++e) {
+                const float y = Elem<E>::f(x.e[e]);
+                sum[e] = c == 0 ? y : sum[e] + y;
+              }
+            }
+            Vec o;
+#pragma unroll
+            for (int e = 0; e < K; ++e) o.e[e] = Elem<E>::out(sum[e]);
+            *reinterpret_cast<Vec*>(dflat + (t0 + u) * width + v * K) = o;
+          }
+      } else {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int v = lane + 32 * a;
+          if (v < nv)
+            for (int c = 0; c < n; ++c) {
+              const Vec x = *reinterpret_cast<const Vec*>(slot + (size_t)c * W + v * 16);
+#pragma unroll
+              for (int e = 0; e < K; ++e) {
+                const float y = Elem<E>::f(x.e[e]);
+                acc[a][e] = (cb + c == 0) ? y : acc[a][e] + y;
+              }
+            }
+        }
+      }
+      __syncwarp();  // every lane has read the slot before it is refilled
+    }
+    if (m == 1) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int v = lane + 32 * a;
+        if (v < nv) {
+          Vec o;
+#pragma unroll
+          for (int e = 0; e < K; ++e) o.e[e] = Elem<E>::out(acc[a][e]);
+          *reinterpret_cast<Vec*>(dflat + t0 * width + v * K) = o;
+        }
+      }
+    }
+  }
+}
+
 __global__ void k_fold_positions(const int32_t* __restrict__ tok_pos, int T, int64_t* __restrict__ pos) {
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) pos[t] = tok_pos[t];
 }
@@ -477,6 +598,13 @@ extern "C" pt_status pt_fold_plan(const int32_t* node_lengths, int32_t n_nodes, 
     for (int s = 0; s < S; ++s)  // ascending samples per node
       for (int k = path_ptr[s]; k < path_ptr[s + 1]; ++k) samp[fill[path_nodes[k]]++] = s;
   }
+  // tasks of the bulk-copy gradient (nodes with tokens only)
+  std::vector<int4> tasks;
+  for (int i = 0; i < N; ++i) {
+    if (node_lengths[i] == 0) continue;
+    const int m = std::max(1, kBulkC / std::max(n_through[i], 1));
+    for (int k0 = 0; k0 < node_lengths[i]; k0 += m) tasks.push_back(make_int4(i, k0, std::min(m, node_lengths[i] - k0), 0));
+  }
   // token classes of the gradient (nodes with tokens only)
   std::vector<int2> cls1, clsM;
   long long T1 = 0, TM = 0, copiesM = 0;
@@ -501,8 +629,9 @@ extern "C" pt_status pt_fold_plan(const int32_t* node_lengths, int32_t n_nodes, 
                b_pp = pad(4 * (size_t)(S + 1)), b_pn = pad(4 * (size_t)std::max(E, 1)), b_tok = pad(4 * (size_t)std::max(T, 1)),
                b_roll = pad(4 * std::max((size_t)S * L, (size_t)1));
   const size_t b_c1 = pad(sizeof(int2) * std::max<size_t>(cls1.size(), 1)),
-               b_cM = pad(sizeof(int2) * std::max<size_t>(clsM.size(), 1));
-  const size_t tables = b_node + b_sp + b_samp + b_pp + b_pn + b_c1 + b_cM;
+               b_cM = pad(sizeof(int2) * std::max<size_t>(clsM.size(), 1)),
+               b_tk = pad(sizeof(int4) * std::max<size_t>(tasks.size(), 1));
+  const size_t tables = b_node + b_sp + b_samp + b_pp + b_pn + b_c1 + b_cM + b_tk;
   const size_t total = tables + 3 * b_tok + b_roll;
   pt_foldplan* p = new pt_foldplan();
   p->device = dev;
@@ -516,6 +645,7 @@ extern "C" pt_status pt_fold_plan(const int32_t* node_lengths, int32_t n_nodes, 
   p->T1 = T1;
   p->TM = TM;
   p->copiesM = copiesM;
+  p->n_tasks = (int32_t)tasks.size();
   int rc = pt::pool_alloc(&p->mem, total, dev, stream);
   if (rc) {
     delete p;
@@ -530,6 +660,7 @@ extern "C" pt_status pt_fold_plan(const int32_t* node_lengths, int32_t n_nodes, 
   p->path_nodes = reinterpret_cast<int32_t*>(base + o), o += b_pn;
   p->cls1 = reinterpret_cast<int2*>(base + o), o += b_c1;
   p->clsM = reinterpret_cast<int2*>(base + o), o += b_cM;
+  p->tasks = reinterpret_cast<int4*>(base + o), o += b_tk;
   p->tok_node = reinterpret_cast<int32_t*>(base + o), o += b_tok;
   p->tok_src = reinterpret_cast<int32_t*>(base + o), o += b_tok;
   p->tok_pos = reinterpret_cast<int32_t*>(base + o), o += b_tok;
@@ -546,6 +677,8 @@ extern "C" pt_status pt_fold_plan(const int32_t* node_lengths, int32_t n_nodes, 
   if (!cls1.empty()) std::memcpy(host.data() + h, cls1.data(), sizeof(int2) * cls1.size());
   h += b_c1;
   if (!clsM.empty()) std::memcpy(host.data() + h, clsM.data(), sizeof(int2) * clsM.size());
+  h += b_cM;
+  if (!tasks.empty()) std::memcpy(host.data() + h, tasks.data(), sizeof(int4) * tasks.size());
   rc = pt::upload(p->mem, host.data(), tables, dev, stream);
   if (rc) {
     set_error("%s: upload of the plan tables failed", who);
@@ -669,6 +802,9 @@ extern "C" pt_status pt_unfold_grad(const pt_foldplan* p, const void* droll, pt_
   const int K = vec ? 16 / es : 1;
   const long long nv = width / K;
   RowGrid rg1 = row_grid(p->T1, nv);
+  // shared tokens by bulk copies when their rows allow it; the rest as below
+  const long long W = width * es;
+  const bool bulk = vec && W <= kBulkMaxRow && p->n_tasks > 0;
   // one wave of blocks, split between the copied and the summed tokens by bytes
   auto split = [&](auto kernel, int& blocks, int& blocks1) {
     int per_sm = 0;
@@ -685,11 +821,27 @@ extern "C" pt_status pt_unfold_grad(const pt_foldplan* p, const void* droll, pt_
     pt::ProfScope ps(stream, "unfold_grad");
 #define PT_GRAD(E, KK, A, B)                                                                                   \
   do {                                                                                                         \
-    int blocks, blocks1;                                                                                       \
-    split(k_unfold_grad<E, KK>, blocks, blocks1);                                                              \
-    k_unfold_grad<E, KK><<<blocks, 256, 0, stream>>>(static_cast<const E*>(A), static_cast<E*>(B), p->node,      \
-                                                     p->node_sp, p->node_samp, p->cls1, p->n1, p->clsM, p->nM,   \
-                                                     rg1, p->TM, blocks1, (int)width, p->L);                     \
+    if (bulk) {                                                                                                \
+      const size_t smem = (size_t)kBulkWarps * kBulkC * W;                                                     \
+      int per_sm = 0;                                                                                          \
+      if (cudaFuncSetAttribute(k_unfold_grad_bulk<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != \
+              cudaSuccess ||                                                                                   \
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_unfold_grad_bulk<E>, kBulkWarps * 32, smem) !=  \
+              cudaSuccess || per_sm < 1)                                                                       \
+        per_sm = 1;                                                                                            \
+      const long long need = ((long long)p->n_tasks + kBulkWarps - 1) / kBulkWarps;                              \
+      const int gb = (int)std::max(1LL, std::min<long long>(need, (long long)pt::num_sms(p->device) * per_sm)); \
+      k_unfold_grad_bulk<E><<<gb, kBulkWarps * 32, smem, stream>>>(static_cast<const char*>(A),               \
+                                                                   static_cast<E*>(B), p->node, p->node_sp,    \
+                                                                   p->node_samp, p->tasks, p->n_tasks, (int)W, \
+                                                                   p->L);                                      \
+    } else {                                                                                                   \
+      int blocks, blocks1;                                                                                     \
+      split(k_unfold_grad<E, KK>, blocks, blocks1);                                                            \
+      k_unfold_grad<E, KK><<<blocks, 256, 0, stream>>>(static_cast<const E*>(A), static_cast<E*>(B), p->node,    \
+                                                       p->node_sp, p->node_samp, p->cls1, p->n1, p->clsM, p->nM, \
+                                                       rg1, p->TM, blocks1, (int)width, p->L);                   \
+    }                                                                                                          \
   } while (0)
     if (dtype == PT_BF16) {
       if (vec)

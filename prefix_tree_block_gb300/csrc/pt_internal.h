@@ -153,6 +153,7 @@ int take_status_blockmap(cudaStream_t s);
 int take_status_fwd(cudaStream_t s);
 int take_status_bwd(cudaStream_t s);
 int take_status_simt(cudaStream_t s);
+int take_status_fold(cudaStream_t s);
 
 // Block-map builders (pt_blockmap.cu).  Return a PT_* status code.
 int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,

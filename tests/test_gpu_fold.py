@@ -33,6 +33,7 @@ def _structures():
     for i in range(3):
         yield f"random_tree{i}", W.random_tree(rng, int(rng.integers(3, 14)), 40), int(rng.integers(0, 5))
     yield "ragged_wide", W.grpo_structure([(131, [29, 100, 1, 64]), (1, [250, 3])]), 7
+    yield "twelve_samples", W.grpo_structure([(37, [5, 9, 1, 3, 12, 7, 2, 8, 4, 6, 10, 11])]), 2  # > 8 copies
 
 
 STRUCTS = list(_structures())
