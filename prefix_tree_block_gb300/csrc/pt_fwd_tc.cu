@@ -61,7 +61,13 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + QB * NH * TILE;
   static constexpr int OFF_V = OFF_K + KS * TILE;
   static constexpr int OFF_MASK = OFF_V + VS * TILE;
-  static constexpr int OFF_META = OFF_MASK + VS * MASKB;
+  // (head_dim 256) 2 KB per softmax warp to turn its 32 rows of a 32-column
+  // O chunk into 64-byte row segments for the stores (see the epilogue); at
+  // head_dim 128 the staging's registers cost the main loop more than it saves
+  static constexpr bool OST = NH == 1;
+  static constexpr int OFF_OST = OFF_MASK + VS * MASKB;
+  static constexpr int OST_BYTES = OST ? NH * 4 * 2048 : 0;
+  static constexpr int OFF_META = OFF_OST + OST_BYTES;
   static constexpr int OFF_BAR = OFF_META + 16 * ((VS * 4 + 15) / 16);
   // q_full[QB] q_empty[QB] k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
   // s_full[NH*SB] p_full[NH*SB] o_full[NH] o_free[NH] mma_done
@@ -595,6 +601,39 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
+        }
+      } else if constexpr (C::OST) {
+        // Each thread holds one row's 64 bytes of a 32-column chunk; stored
+        // as they are, a warp instruction writes 32 rows.  The warp stages the
+        // chunk in shared memory (16-byte pieces XOR-swizzled by row) and
+        // reads it back so that four lanes cover one row's 64 bytes: each
+        // store instruction then writes 8 rows of 64 contiguous bytes.
+        uint8_t* wst = smem + C::OFF_OST + (warp & (NH * 4 - 1)) * 2048;
+        const int lw = lane, rr = lw >> 2, kk = lw & 3;  // read-back: row rr (+ 8i), piece kk
+        const int row0 = tile * C::BM + (warp & 3) * 32;  // first q row of this warp
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tl + o_col + c * 32, orr);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            pk[k] = pack_bf16(__uint_as_float(orr[2 * k]) * inv, __uint_as_float(orr[2 * k + 1]) * inv);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(wst + lw * 64 + ((k ^ (lw & 3)) * 16)) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = rr + 8 * i;  // 0..31 within the warp
+            const uint4 v = *reinterpret_cast<const uint4*>(wst + row * 64 + ((kk ^ (row & 3)) * 16));
+            const int qr = row0 + row;
+            if (qr < p.T)
+              *reinterpret_cast<uint4*>(p.O + ((size_t)qr * p.Hq + head) * D + c * 32 + kk * 8) = v;
+          }
+          __syncwarp();
         }
       } else {
         __nv_bfloat16* orow = p.O + ((size_t)q * p.Hq + head) * D;
