@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(tl + acc + c * 32, v);
         tmem_ld_wait();
         if (itm.slot < 0) {
-          if (kv < p.T) store_row32(orow + c * 32, v, mul);
+          if (kv < p.T) store_row32(orow + c * 32, v, mul);  // few items per CTA: the direct stores are kept
         } else {  // one chunk of a split column: fp32 partial sums, summed later in chunk order
           float4* prow = reinterpret_cast<float4*>(p.partial + ((size_t)itm.slot * 128 + r) * (2 * D) + (hw ? D : 0) +
                                                    c * 32);
@@ -1261,7 +1261,7 @@ __global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
         uint32_t v[32];
         tmem_ld32(ta + c * 32, v);
         tmem_ld_wait();
-        if (q < p.T) store_row32(orow + c * 32, v, p.scale);
+        store_rows32(orow + c * 32, (size_t)p.Hq * D, q, p.T, v, p.scale);
       }
       tc_fence_before();
       mbar_arrive(&B->acc_free);
@@ -1638,7 +1638,7 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t v[32];
         tmem_ld32(tl + C::TM_ACC + hw * 128 + c * 32, v);
         tmem_ld_wait();
-        if (row < p.T) store_row32(out + c * 32, v, mul);
+        store_rows32(out + c * 32, (size_t)(MODE == WIDE_DQ ? p.Hq : p.Hkv) * D, row, p.T, v, mul);
       }
       tc_fence_before();
       mbar_arrive(&B->acc_free);

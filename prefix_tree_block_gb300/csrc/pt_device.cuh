@@ -342,6 +342,49 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// Stores 32 bf16 columns (v: 32 fp32 values, times mul) of a row per lane,
+// for a warp whose lanes hold 32 consecutive rows.  Stored as they are, one
+// warp instruction would write 32 rows; a 4 x 4 transpose of the 16-byte
+// pieces within each group of four lanes (two xor-shuffle stages) gives each
+// lane one piece of each of its group's four rows, so each of the four store
+// instructions writes 8 rows x 64 contiguous bytes.  own: this lane's row
+// start (row `row`), stride: elements between rows, rows >= T are skipped.
+// Every lane of the warp must call it.
+__device__ __forceinline__ void store_rows32(__nv_bfloat16* own, size_t stride, long long row, long long T,
+                                             const uint32_t* v, float mul) {
+  const int lane = threadIdx.x & 31, i = lane & 3, g = lane >> 2;
+  uint4 a[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    a[j] = make_uint4(pack_bf16(__uint_as_float(v[8 * j + 0]) * mul, __uint_as_float(v[8 * j + 1]) * mul),
+                      pack_bf16(__uint_as_float(v[8 * j + 2]) * mul, __uint_as_float(v[8 * j + 3]) * mul),
+                      pack_bf16(__uint_as_float(v[8 * j + 4]) * mul, __uint_as_float(v[8 * j + 5]) * mul),
+                      pack_bf16(__uint_as_float(v[8 * j + 6]) * mul, __uint_as_float(v[8 * j + 7]) * mul));
+#pragma unroll
+  for (int s = 1; s <= 2; s <<= 1)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j & s) continue;
+      const bool hi = (i & s) != 0;
+      const uint4 send = hi ? a[j] : a[j | s];
+      uint4 recv;
+      recv.x = __shfl_xor_sync(0xffffffffu, send.x, s);
+      recv.y = __shfl_xor_sync(0xffffffffu, send.y, s);
+      recv.z = __shfl_xor_sync(0xffffffffu, send.z, s);
+      recv.w = __shfl_xor_sync(0xffffffffu, send.w, s);
+      if (hi)
+        a[j] = recv;
+      else
+        a[j | s] = recv;
+    }
+  // a[k] = piece i of row (row - lane) + 4g + k
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int d = 4 * g + k - lane;  // that row, relative to this lane's
+    if (row + d < T) *reinterpret_cast<uint4*>(own + (long long)d * (long long)stride + i * 8) = a[k];
+  }
+}
+
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
 }  // namespace pt
