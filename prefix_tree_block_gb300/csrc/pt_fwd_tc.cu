@@ -642,15 +642,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
           uint32_t orr[32];
           tmem_ld32(tl + o_col + c * 32, orr);
           tmem_ld_wait();
-          if (q < p.T) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-              pk[k] = pack_bf16(__uint_as_float(orr[2 * k]) * inv, __uint_as_float(orr[2 * k + 1]) * inv);
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          }
+          store_rows32(orow + c * 32, (size_t)p.Hq * D, q, p.T, orr, inv);  // 8 row segments per store
         }
       }
       if (q < p.T) p.LSE[(size_t)head * p.T + q] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994531f : -INFINITY;
