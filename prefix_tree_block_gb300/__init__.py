@@ -456,11 +456,11 @@ class FoldPlan:
 
     @staticmethod
     def _row_bytes(t, lead: int) -> int:
-        n = t.numel() * t.element_size()
-        per = 1
-        for d in t.shape[:lead]:
-            per *= d
-        return n // per if per else 0
+        """Bytes of one token's row: the trailing dimensions (valid for empty leading ones)."""
+        n = t.element_size()
+        for d in t.shape[lead:]:
+            n *= d
+        return n
 
     def _need(self, t, shape, name):
         if not t.is_cuda or not t.is_contiguous() or tuple(t.shape[:len(shape)]) != shape:
@@ -493,7 +493,9 @@ class FoldPlan:
         import torch
 
         self._need(droll, (self.n_samples, self.row_len), "droll")
-        width = droll.numel() // max(1, self.n_samples * self.row_len)
+        width = 1
+        for d in droll.shape[2:]:
+            width *= d
         out = torch.empty((self.T,) + tuple(droll.shape[2:]), dtype=droll.dtype, device=droll.device) \
             if out is None else out
         _check(self._lib.pt_unfold_grad(self._h, _ptr(droll), _dtype_code(droll), width, _ptr(out),

@@ -121,3 +121,18 @@ def test_tile_masks_bit_exact(case):
             i, s = lst["q_idx"][e], mk["pidxT"][e]
             row_e = lst["q_ptr"][i] + np.searchsorted(lst["kv_idx"][lst["q_ptr"][i]:lst["q_ptr"][i + 1]], j)
             assert s == mk["pidx"][row_e]
+
+
+def test_empty_layout_attention_and_host_lists():
+    """T = 0 through the forward and backward (nothing launched, nothing to compare), and a tree whose
+    first sample holds only zero-length nodes: its lists, built on the host, must match the oracle."""
+    st = W.grpo_structure([(0, [0])])
+    bm = gpu_blockmap(st)
+    Q = torch.empty(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    K = torch.empty(0, 1, 64, dtype=torch.bfloat16, device="cuda")
+    O, L = pt.attn_fwd(Q, K, K, bm)
+    dQ, dK, dV = pt.attn_bwd(Q, Q, K, K, O, L, bm)
+    assert O.numel() == 0 and dQ.numel() == 0 and dK.numel() == 0
+    pt.sync_status()
+    st = W.tree_structure([0, 0, 130, 0, 300], [[0, 1], [0, 2], [0, 3, 4]])
+    compare_blockmap(gpu_blockmap(st).export(), orc.blockmap(orc.structure_labels(st), 128, 128))

@@ -162,3 +162,26 @@ def test_invalid_plans_rejected():
         pt.fold_plan(*_tree(st), 4)  # a 5-token row does not fit in 4
     with pytest.raises(pt.PTError):
         pt.fold_plan([2, 1, 1], [0, 2], [0, 1], 8)  # node 2 on no path
+
+
+def test_empty_and_padding_only_rows():
+    """No tokens at all, and a sample whose path holds only zero-length nodes (its row is all padding)."""
+    empty = W.grpo_structure([(0, [0, 0])])
+    plan = pt.fold_plan(*_tree(empty), 3)
+    assert plan.T == 0
+    roll = torch.full((2, 3, 4), 7, dtype=torch.int32, device="cuda")
+    assert plan.fold(roll).numel() == 0
+    assert torch.equal(plan.unfold(torch.empty(0, 4, dtype=torch.int32, device="cuda")).cpu(),
+                       torch.zeros(2, 3, 4, dtype=torch.int32))
+    assert plan.unfold_grad(torch.randn(2, 3, 8, device="cuda")).numel() == 0
+    assert plan.positions().numel() == 0 and plan.mismatches(roll) == 0
+    st = W.tree_structure([0, 0, 5, 3], [[0, 1], [0, 2, 3]])  # sample 0: zero-length nodes only
+    L = 9
+    flat, roll = _rollouts(st, L, (16,), torch.bfloat16, seed=4)
+    plan = pt.fold_plan(*_tree(st), L)
+    assert torch.equal(plan.fold(roll.cuda()).cpu(), flat)
+    assert torch.equal(plan.unfold(flat.cuda()).cpu(), roll)
+    droll = torch.randn(st.n_samples, L, 16).to(torch.bfloat16)
+    got = plan.unfold_grad(droll.cuda()).cpu().double().numpy()
+    want = OF.unfold_grad(droll.double().numpy(), *_tree(st))
+    np.testing.assert_allclose(got, want, rtol=2.0 ** -8, atol=0)
