@@ -279,6 +279,7 @@ __global__ void k_tree_listed(int T, int tpad, int N, int* __restrict__ map_tabs
                               int* __restrict__ k_order, int* __restrict__ kv_idx, int* __restrict__ q_idx,
                               uint8_t* __restrict__ kind, int* __restrict__ pidx, uint8_t* __restrict__ kindT,
                               int* __restrict__ pidxT, int2* __restrict__ slot_tile, long long p_cap) {
+  pdl_wait();  // launched with programmatic dependent launch
   // node tables (start | end | parent | tin | tout) come in the packed upload
   // and are read from there; the list blocks also copy them into the map
   const int* tabs = pk + 4;
@@ -572,6 +573,7 @@ __device__ __forceinline__ void tile_masks(int T, const pt_tok* tok, const int2*
 __global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols,
                         long long n_known, const int* nnz_total, const int* n_full, long long p_cap,
                         int* host_counters = nullptr) {
+  pdl_wait();  // launched with programmatic dependent launch
   __shared__ pt_tok tq[128], tk[128];
   __shared__ uint32_t kstart[4], qstart[4];
   // the full-tile count to the host's mapped staging (host-built lists)
@@ -738,6 +740,7 @@ constexpr int kMaxDev = 64;
 // step's inputs and gradients) would otherwise hold them, and with them the
 // kernels queued behind them on this stream.
 __global__ void k_stage(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, long long bytes, int vec) {
+  pdl_wait();  // launched with programmatic dependent launch
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long nth = (long long)gridDim.x * blockDim.x;
   long long done = 0;
@@ -755,7 +758,8 @@ int stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s) {
   const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0) ? 1 : 0;
   const long long units = vec ? (long long)(bytes >> 4) + 1 : (long long)bytes;
   const int grid = (int)std::max(1LL, std::min<long long>((units + 255) / 256, 64));
-  k_stage<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), (long long)bytes, vec);
+  launch_pdl(k_stage, dim3(grid), dim3(256), 0, s, static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst),
+             (long long)bytes, vec);
   count_launch();
   if (cudaGetLastError() != cudaSuccess) {
     set_error("staging copy launch failed");
@@ -1257,7 +1261,7 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
       const int tok_blocks = (bm->tpad + 255) / 256;
       const long long list_work = std::max<long long>((long long)nnz * 32, 5LL * N + 2LL * nq + 2LL * nk + 2 + 2 * nnz);
       const int list_blocks = (int)std::max(1LL, std::min<long long>((list_work + 255) / 256, (long long)num_sms(dev) * 8));
-      k_tree_listed<<<tok_blocks + list_blocks, 256, 0, s>>>(
+      launch_pdl(k_tree_listed, dim3(tok_blocks + list_blocks), dim3(256), 0, s,
           bm->T, bm->tpad, N, bm->node_start, bm->tok, bm->node_of, tok_blocks, counters, nq, nk, (int)nnz, bm->q_ptr,
           bm->k_ptr, bm->q_order, bm->k_order, bm->kv_idx, bm->q_idx, bm->kind, bm->pidx, bm->kindT, bm->pidxT,
           slot_tile, (long long)bm->p_cap);
@@ -1266,9 +1270,8 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
     {
       ProfScope ps(s, "blockmap_lists");  // the partial tiles' masks
       const long long grid = std::max<long long>(1, std::min<long long>(p_alloc, (long long)num_sms(dev) * 16));
-      k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, -1LL,
-                                             bm->q_ptr + nq, counters, (long long)bm->p_cap,
-                                             static_cast<int*>(sl.dev));
+      launch_pdl(k_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, bm->tok, slot_tile, bm->mask_rows,
+                 bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap, static_cast<int*>(sl.dev));
       PT_LAUNCHED(1);
       if (cudaEventRecord(sl.ev, s) != cudaSuccess) {
         rc = 3;

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restric
                                                   const __nv_bfloat16* __restrict__ O, const float* __restrict__ LSE,
                                                   int T, int Tpad, int Hq, float* __restrict__ delta,
                                                   float* __restrict__ lse2) {
+  pdl_wait();  // launched with programmatic dependent launch
   constexpr int TPR = D / 8;  // threads per (token, head) row
   extern __shared__ float sh_delta[];  // [kPrepTokens][Hq + 1]
   const int q0 = blockIdx.x * kPrepTokens;
@@ -152,6 +153,7 @@ struct BwdParams {
 template <int D>
 __global__ void k_dkdv_finalize(const int4* __restrict__ splits, const float* __restrict__ partial, int T, int Hkv,
                                 __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV) {
+  pdl_wait();  // launched with programmatic dependent launch
   // block (x, y): split column x, rows [8y, 8y + 8) of its 128; one float4 of
   // 2D columns per thread and row pass
   const int4 sp = splits[blockIdx.x];  // kv block, kv head, first slot, slot count
@@ -251,6 +253,7 @@ template <int D>
 __global__ void __launch_bounds__(320, 1)
     k_bwd_dkdv(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const BwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
   using C = BwdCfg<D>;
   using L = DkdvL<D>;
   constexpr int S = C::STAGES;
@@ -644,6 +647,7 @@ __global__ void __launch_bounds__(320, 1)
     k_bwd_dq(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
              const __grid_constant__ CUtensorMap mdQ, const BwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
   using C = BwdCfg<D>;
   using L = DqL<D>;
   constexpr int S = C::STAGES;
@@ -982,6 +986,7 @@ template <int D>
 __global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
     k_bwd_dq_pipe(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                   const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const BwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
   using C = DqpCfg<D>;
   using L = DqpL<D>;
   static_assert(sizeof(DqpBars) <= 256, "barrier block");
@@ -1328,6 +1333,7 @@ template <int MODE>
 __global__ void __launch_bounds__(320, 1)
     k_bwd_wide(const __grid_constant__ CUtensorMap mR1, const __grid_constant__ CUtensorMap mR2,
                const __grid_constant__ CUtensorMap mL, const __grid_constant__ CUtensorMap mE, const BwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
   using C = WideCfg<MODE>;
   constexpr int D = C::D;
   static_assert(sizeof(WideBars) <= 256, "barrier block");
@@ -1913,8 +1919,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       return 3;
     }
     ProfScope ps(s, "bwd_prep");
-    k_bwd_prep<D><<<(unsigned)(Tpad / kPrepTokens), 256, sm, s>>>(
-        static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
+    launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s, static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
   }
   CUtensorMap mQ, mdO, mK, mV, mdQ;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128) ||
@@ -1946,15 +1951,12 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   int launches = 1;
   if (p.n_items > 0) {
     ProfScope ps(s, "bwd_dkdv");
-    k_bwd_dkdv<D><<<bm->bwd_grid, 320, DkdvL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+    launch_pdl(k_bwd_dkdv<D>, dim3(bm->bwd_grid), dim3(320), DkdvL<D>::BYTES, s, mQ, mdO, mK, mV, p);
     ++launches;
   }
   if (bm->bwd_n_splits > 0) {
     ProfScope ps(s, "bwd_dkdv_finalize");
-    k_dkdv_finalize<D><<<dim3(bm->bwd_n_splits, 16), 256, 0, s>>>(static_cast<const int4*>(bm->bwd_splits), partial,
-                                                                   T, Hkv,
-                                                        static_cast<__nv_bfloat16*>(dK),
-                                                        static_cast<__nv_bfloat16*>(dV));
+    launch_pdl(k_dkdv_finalize<D>, dim3(dim3(bm->bwd_n_splits, 16)), dim3(256), 0, s, static_cast<const int4*>(bm->bwd_splits), partial, T, Hkv, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
     ++launches;
   }
   // dQ
@@ -1978,9 +1980,9 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       p.dq_items = static_cast<const int4*>(bm->dq_items);
       p.dq_cta = static_cast<const int4*>(bm->dq_cta);
       if (bm->dq_n_items > 0)
-        k_bwd_dq_pipe<D><<<bm->dq_grid, DqpCfg<D>::THREADS, DqpL<D>::BYTES, s>>>(mQ, mdO, mK, mV, p);
+        launch_pdl(k_bwd_dq_pipe<D>, dim3(bm->dq_grid), dim3(DqpCfg<D>::THREADS), DqpL<D>::BYTES, s, mQ, mdO, mK, mV, p);
     } else {
-      k_bwd_dq<D><<<items < sms ? items : sms, 320, DqL<D>::BYTES, s>>>(mQ, mdO, mK, mV, mdQ, p);
+      launch_pdl(k_bwd_dq<D>, dim3(items < sms ? items : sms), dim3(320), DqL<D>::BYTES, s, mQ, mdO, mK, mV, mdQ, p);
     }
     ++launches;
   }
@@ -2021,8 +2023,7 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
       return 3;
     }
     ProfScope ps(s, "bwd_prep");
-    k_bwd_prep<D><<<(unsigned)(Tpad / kPrepTokens), 256, sm, s>>>(
-        static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
+    launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s, static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
   }
   CUtensorMap mQ, mdO, mK, mV, mQh, mdOh, mKh, mVh;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128) ||
@@ -2053,11 +2054,11 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   if (p.n_items > 0) {
     {
       ProfScope ps(s, "bwd_dv");
-      k_bwd_wide<WIDE_DV><<<bm->bwd_grid, 320, WideCfg<WIDE_DV>::BYTES, s>>>(mK, mK, mdOh, mQh, p);
+      launch_pdl(k_bwd_wide<WIDE_DV>, dim3(bm->bwd_grid), dim3(320), WideCfg<WIDE_DV>::BYTES, s, mK, mK, mdOh, mQh, p);
     }
     {
       ProfScope ps(s, "bwd_dk");
-      k_bwd_wide<WIDE_DK><<<bm->bwd_grid, 320, WideCfg<WIDE_DK>::BYTES, s>>>(mK, mV, mQh, mdOh, p);
+      launch_pdl(k_bwd_wide<WIDE_DK>, dim3(bm->bwd_grid), dim3(320), WideCfg<WIDE_DK>::BYTES, s, mK, mV, mQh, mdOh, p);
     }
     launches += 2;
   }
@@ -2074,7 +2075,7 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   if ((rc = zero_empty_dq(bm, dQ, T, Hq, D, s))) return rc;
   if (bm->dq_n_items > 0) {
     ProfScope ps(s, "bwd_dq");
-    k_bwd_wide<WIDE_DQ><<<bm->dq_grid, 320, WideCfg<WIDE_DQ>::BYTES, s>>>(mQ, mdO, mKh, mVh, p);
+    launch_pdl(k_bwd_wide<WIDE_DQ>, dim3(bm->dq_grid), dim3(320), WideCfg<WIDE_DQ>::BYTES, s, mQ, mdO, mKh, mVh, p);
     ++launches;
   }
   count_launch(launches);

@@ -272,6 +272,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its memory is visible.  A kernel launched with the
+// attribute (launch_pdl) must call this before its first global memory
+// access (read or write: the stream-ordered pool may hand it memory the
+// preceding kernel still uses); without the attribute it returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `count` threads (ids other than 0, which __syncthreads uses).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

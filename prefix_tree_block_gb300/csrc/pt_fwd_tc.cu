@@ -131,6 +131,7 @@ template <int D, int NH>
 __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
              const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, const FwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
   using C = FwdCfg<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -705,7 +706,7 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
   if (grid <= 0) return 0;
   {
     ProfScope ps(s, "fwd_tc");
-    k_fwd_tc<D, NH><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mQ, mK, mV, mO, p);
+    launch_pdl(k_fwd_tc<D, NH>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, mQ, mK, mV, mO, p);
   }
   count_launch();
   cudaError_t e = cudaGetLastError();

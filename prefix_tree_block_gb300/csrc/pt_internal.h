@@ -196,4 +196,22 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int T, int H, int D, int 
 
 int num_sms(int device);
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the preceding kernel in the stream drains (its CTAs start on the SMs that
+// kernel has left) and must call pdl_wait() before touching global memory.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace pt
