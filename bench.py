@@ -116,6 +116,71 @@ def num_sms() -> int:
     return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
 
 
+def euler_intervals(st):
+    """Pre-order index (tin) and end of subtree (tout) of every node, children in id order."""
+    import numpy as np
+
+    n = int(st.node_lengths.size)
+    parent = [-1] * n
+    for p in st.paths():
+        for a, b in zip(p[:-1], p[1:]):
+            parent[b] = a
+    children = [[] for _ in range(n)]
+    for i in range(n):
+        if parent[i] >= 0:
+            children[parent[i]].append(i)
+    tin = np.zeros(n, np.int64)
+    tout = np.zeros(n, np.int64)
+    counter = 0
+    stack = [(r, False) for r in reversed([i for i in range(n) if parent[i] < 0])]
+    while stack:
+        u, done = stack.pop()
+        if done:
+            tout[u] = counter
+            continue
+        tin[u] = counter
+        counter += 1
+        stack.append((u, True))
+        stack.extend((c, False) for c in reversed(children[u]))
+    return tin, tout
+
+
+def sdpa_dense_mask(st, Q, K, V, dO, steps):
+    """torch scaled_dot_product_attention forward + backward with the dense [T, T] keep mask."""
+    import numpy as np
+    import torch
+    import torch.nn.functional as F
+
+    dev = Q.device
+    T = Q.shape[0]
+    tin, tout = euler_intervals(st)
+    node_of = np.repeat(np.arange(st.node_lengths.size), st.node_lengths)
+    ti = torch.as_tensor(tin[node_of], device=dev)
+    to = torch.as_tensor(tout[node_of], device=dev)
+    idx = torch.arange(T, device=dev)
+    mask = (ti[None, :] <= ti[:, None]) & (ti[:, None] < to[None, :]) & (idx[None, :] <= idx[:, None])
+    q4, k4, v4, g4 = (x.transpose(0, 1).unsqueeze(0).contiguous() for x in (Q, K, V, dO))
+    q4.requires_grad_()
+    k4.requires_grad_()
+    v4.requires_grad_()
+
+    def one():
+        q4.grad = k4.grad = v4.grad = None
+        o = F.scaled_dot_product_attention(q4, k4, v4, attn_mask=mask, enable_gqa=True)
+        o.backward(g4)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return {"ms_per_step": a.elapsed_time(b) / steps, "what": "torch SDPA forward + backward, dense bool mask, "
+            f"GQA, same inputs (torch {torch.__version__})", "mask_mb": T * T / 1e6}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -412,6 +477,19 @@ def main():
         dt = timed(max(2, min(5, args.steps)), lambda: step(dense=True))
         dense = {"ms_per_step": sum(dt) / len(dt), "speedup": (sum(dt) / len(dt)) / ms_step}
 
+    # ---- secondary context: torch SDPA over a dense [T, T] boolean mask ------
+    # (the pre-block-sparse path the drafter PR replaced).  The mask is
+    # keep(q, kv) = node(kv) is an ancestor-or-self of node(q) and kv <= q,
+    # from the tree's Euler intervals; forward and backward with GQA.
+    sdpa = None
+    if not args.no_dense and not draft and T <= 32768:
+        try:
+            sdpa = sdpa_dense_mask(st, Q, K, V, dO, max(2, min(3, args.steps)))
+            sdpa["speedup"] = sdpa["ms_per_step"] / ms_step
+        except Exception as e:  # noqa: BLE001 - context only: report why it could not run
+            sdpa = {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+        torch.cuda.empty_cache()
+
     # ---- end to end through the C ABI with host buffers ---------------------
     # Every step builds its map from the host tree arrays, uploads Q, K, V, dO
     # from pinned host memory and downloads dQ, dK, dV (pt_hoststep: two
@@ -506,7 +584,7 @@ def main():
                        "tiles": "128x128", "l2": "flushed before every step (256 MB write, untimed)",
                        "parallelism": f"replicas x{world}"},
             "kernels": kernels, "kernel_timing": "second pass of the same steps with an event pair per kernel",
-            "roofline": roofline, "dense_masked": dense, "e2e": e2e,
+            "roofline": roofline, "dense_masked": dense, "sdpa_dense_mask": sdpa, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu, "fold": fold,
         }
         print(json.dumps(line), flush=True)
