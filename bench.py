@@ -145,20 +145,27 @@ def euler_intervals(st):
     return tin, tout
 
 
+def dense_keep_mask(st, device):
+    """[T, T] bool: row q keeps column k when k's node is q's node or an ancestor of it (k's pre-order
+    interval holds q's) and k <= q in the flat order."""
+    import numpy as np
+    import torch
+
+    tin, tout = euler_intervals(st)
+    node_of = np.repeat(np.arange(st.node_lengths.size), st.node_lengths)
+    ti = torch.as_tensor(tin[node_of], device=device)
+    to = torch.as_tensor(tout[node_of], device=device)
+    idx = torch.arange(int(node_of.size), device=device)
+    return (ti[None, :] <= ti[:, None]) & (ti[:, None] < to[None, :]) & (idx[None, :] <= idx[:, None])
+
+
 def sdpa_dense_mask(st, Q, K, V, dO, steps):
     """torch scaled_dot_product_attention forward + backward with the dense [T, T] keep mask."""
-    import numpy as np
     import torch
     import torch.nn.functional as F
 
-    dev = Q.device
+    mask = dense_keep_mask(st, Q.device)
     T = Q.shape[0]
-    tin, tout = euler_intervals(st)
-    node_of = np.repeat(np.arange(st.node_lengths.size), st.node_lengths)
-    ti = torch.as_tensor(tin[node_of], device=dev)
-    to = torch.as_tensor(tout[node_of], device=dev)
-    idx = torch.arange(T, device=dev)
-    mask = (ti[None, :] <= ti[:, None]) & (ti[:, None] < to[None, :]) & (idx[None, :] <= idx[:, None])
     q4, k4, v4, g4 = (x.transpose(0, 1).unsqueeze(0).contiguous() for x in (Q, K, V, dO))
     q4.requires_grad_()
     k4.requires_grad_()

@@ -30,3 +30,19 @@ def test_draft_workload_anchors_keep_blocks_in_document():
     ends = np.cumsum(np.bincount(st.ctx_doc))
     assert np.all(st.anchors + st.block_size <= ends[st.anchor_doc])
     assert np.all(st.ctx_doc[st.anchors] == st.anchor_doc)
+
+
+@pytest.mark.parametrize("c", [1, 4])
+def test_dense_keep_mask_matches_oracle(c):
+    """The [T, T] mask the bench hands to torch SDPA (its secondary comparison) is the oracle's keep matrix."""
+    st = W.config_structure(c)
+    got = bench.dense_keep_mask(st, "cpu").numpy()
+    np.testing.assert_array_equal(got, OR.dense_mask(OR.structure_labels(st)).astype(bool))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_dense_keep_mask_random_trees(seed):
+    rng = np.random.default_rng(70 + seed)
+    st = W.random_tree(rng, n_nodes=int(rng.integers(1, 25)), max_len=int(rng.integers(1, 60)))
+    got = bench.dense_keep_mask(st, "cpu").numpy()
+    np.testing.assert_array_equal(got, OR.dense_mask(OR.structure_labels(st)).astype(bool))
