@@ -33,7 +33,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
     assert out[0] == out[1]
     total, value = out[0]
