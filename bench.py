@@ -83,7 +83,7 @@ def useful_pairs(st) -> int:
 # per-kernel counter summaries under profiles/).  A kernel changed since its
 # capture must be removed from this table (its traffic is then reported null).
 MEASURED_TRAFFIC = {
-    (2, "fwd_tc"): 35.09e6, (2, "bwd_dkdv"): 66.50e6, (2, "bwd_dq"): 66.80e6,
+    (2, "fwd_tc"): 35.10e6, (2, "bwd_dkdv"): 67.28e6, (2, "bwd_dq"): 66.93e6,
     (3, "fwd_tc"): 973.7e6, (3, "bwd_dkdv"): 3008e6, (3, "bwd_dq"): 1216e6,
 }
 
