@@ -84,7 +84,7 @@ def useful_pairs(st) -> int:
 # capture must be removed from this table (its traffic is then reported null).
 MEASURED_TRAFFIC = {
     (2, "fwd_tc"): 35.10e6, (2, "bwd_dkdv"): 67.28e6, (2, "bwd_dq"): 66.93e6,
-    (3, "fwd_tc"): 973.7e6, (3, "bwd_dkdv"): 3008e6, (3, "bwd_dq"): 1216e6,
+    (3, "fwd_tc"): 982.3e6, (3, "bwd_dkdv"): 3022e6, (3, "bwd_dq"): 1215e6,
 }
 
 
