@@ -278,8 +278,8 @@ size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
  * head layout by pt_blockmap_prepare_bwd, which allocates them in the map's
  * own memory; a call whose map has no lists for its (Hq, Hkv, D) returns
  * PT_ERR_INVALID_ARG without launching anything.  Maps used only with the
- * CUDA-core paths (fp32, tiles other than 128 x 128, head_dim 256) need no
- * lists, and preparing them is a no-op.
+ * CUDA-core paths (fp32, tiles other than 128 x 128, head dims other than
+ * 64, 128 and 256) need no lists, and preparing them is a no-op.
  * Shapes, dtypes, layouts and errors are otherwise those of pt_attn_bwd.
  * ------------------------------------------------------------------------- */
 pt_status pt_attn_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V, const void* O,
@@ -414,11 +414,13 @@ pt_status pt_debug_wait_timeout(cudaStream_t stream);
 /* Builds the work lists pt_attn_bwd_noalloc needs for block map bm and head
  * layout (Hq, Hkv, D): the kv-major items packed onto the SMs (no column is
  * split, since that call has no workspace for partial sums) and, at
- * head_dim 128, the q-major items of the pipelined dQ kernel.  Allocates them
+ * head_dims 128 and 256, the q-major items of the dQ kernels.  Allocates them
  * from the library's stream-ordered pool in the map's ownership (freed with
- * the map) and uploads them on `stream`.  Idempotent; returns
- * PT_ERR_INVALID_ARG for a NULL map or a bad head layout.  The pages have no
- * counterpart. */
+ * the map) and uploads them on `stream`.  A no-op where the backward runs on
+ * the CUDA-core kernels (fp32, tiles other than 128 x 128, head dims other
+ * than 64, 128 and 256).  Idempotent; returns PT_ERR_INVALID_ARG for a NULL
+ * map or a bad head layout and PT_ERR_UNSUPPORTED for head_dim above 512, as
+ * pt_attn_bwd does.  The pages have no counterpart. */
 pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv, int32_t D, cudaStream_t stream);
 
 /* Accuracy check of the kernels' two exp2 paths: y[i] = 2^x[i] for i < n,

@@ -419,9 +419,13 @@ uint64_t pt_launch_count(void) { return pt::launches(); }
 pt_status pt_debug_wait_timeout(cudaStream_t stream) { return as_status(pt::wait_timeout_probe(stream)); }
 
 pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv, int32_t D, cudaStream_t stream) {
-  if (!bm || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || D > 256) {
+  if (!bm || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0) {
     set_error("pt_blockmap_prepare_bwd: bad map or head layout (Hq=%d, Hkv=%d, D=%d)", Hq, Hkv, D);
     return PT_ERR_INVALID_ARG;
+  }
+  if (D > 512) {
+    set_error("pt_blockmap_prepare_bwd: head_dim %d outside 1..512", D);
+    return PT_ERR_UNSUPPORTED;
   }
   return as_status(pt::prepare_bwd_noalloc(bm, Hq, Hkv, D, stream));
 }

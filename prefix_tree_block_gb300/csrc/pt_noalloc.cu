@@ -65,11 +65,14 @@ extern "C" pt_status pt_attn_bwd_noalloc(const void* dO, const void* Q, const vo
     pt::set_error("pt_attn_bwd_noalloc: block map is NULL");
     return PT_ERR_INVALID_ARG;
   }
-  if (T != bm->T || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || D > 256 ||
-      (dtype != PT_BF16 && dtype != PT_F32)) {
+  if (T != bm->T || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || (dtype != PT_BF16 && dtype != PT_F32)) {
     pt::set_error("pt_attn_bwd_noalloc: bad shape or dtype (T=%d vs map T=%d, Hq=%d, Hkv=%d, D=%d)", T, bm->T, Hq,
                   Hkv, D);
     return PT_ERR_INVALID_ARG;
+  }
+  if (D > 512) {  // as pt_attn_bwd: head dims above 256 run on the CUDA-core kernels, up to 512
+    pt::set_error("pt_attn_bwd_noalloc: head_dim %d outside 1..512", D);
+    return PT_ERR_UNSUPPORTED;
   }
   if (T == 0) return PT_OK;
   const void* ptrs[] = {dO, Q, K, V, O, LSE, dQ, dK, dV};

@@ -41,7 +41,8 @@ def _noalloc(lib, dO, Q, K, V, O, LSE, bm, dtype_code, expect=pt.PT_OK):
     return dQ, dK, dV
 
 
-@pytest.mark.parametrize("dtype,D,BM", [("bf16", 64, 128), ("bf16", 128, 128), ("f32", 32, 16)])
+@pytest.mark.parametrize("dtype,D,BM", [("bf16", 64, 128), ("bf16", 128, 128), ("bf16", 256, 128), ("bf16", 96, 128),
+                                        ("bf16", 320, 128), ("f32", 32, 16)])
 def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
     st = W.grpo_structure([(300, [100, 41, 250]), (0, [77, 129])])
     q, k, v, do = W.make_tensors(st.T, 4, 2, D, dtype, seed=D)
@@ -50,9 +51,16 @@ def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
     O, LSE = pt.attn_fwd(Q, K, V, bm)
     ref = [x.float().cpu().numpy() for x in pt.attn_bwd(dO, Q, K, V, O, LSE, bm)]
     code = pt.PT_BF16 if dtype == "bf16" else pt.PT_F32
-    if dtype == "bf16":  # the tensor-core path reads per-map work lists: refused until prepared
+    # a fresh map of the same layout: the workspace backward above may already have built, on bm, the lists
+    # the allocation-free call reads (at head_dim 256 they are the same lists)
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes, BM, BM)
+    if dtype == "bf16" and D in (64, 128, 256):  # the tensor-core path reads per-map work lists: refused until prepared
         _noalloc(lib, dO, Q, K, V, O, LSE, bm, code, expect=pt.PT_ERR_INVALID_ARG)
         assert b"pt_blockmap_prepare_bwd" in lib.pt_last_error()
+    elif dtype == "bf16":  # the CUDA-core kernels keep no lists: no preparation needed
+        got = [x.float().cpu().numpy() for x in _noalloc(lib, dO, Q, K, V, O, LSE, bm, code)]
+        for g, r in zip(got, ref):
+            assert rel_l2(g, r) <= GRAD_RL2[dtype]
     bm.prepare_bwd(Q.shape[1], K.shape[1], D)
     bm.prepare_bwd(Q.shape[1], K.shape[1], D)  # idempotent
     for _ in range(2):
@@ -61,6 +69,23 @@ def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
             assert np.isfinite(g).all()
             assert rel_l2(g, r) <= GRAD_RL2[dtype]
     pt.sync_status()
+
+
+def test_noalloc_head_dim_limits(lib):
+    """Head dims as pt_attn_bwd takes them: 1..512; above that unsupported, 0 invalid."""
+    st = W.grpo_structure([(40, [9, 20])])
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes)
+    buf = torch.zeros(st.T * 2 * 520, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(2 * st.T, dtype=torch.float32, device="cuda")
+    p = buf.data_ptr()
+    for D, want in [(520, pt.PT_ERR_UNSUPPORTED), (0, pt.PT_ERR_INVALID_ARG)]:
+        rc = lib.pt_attn_bwd_noalloc(p, p, p, p, p, lse.data_ptr(), pt.PT_BF16, st.T, 2, 1, D, 0.0, bm.handle, p, p,
+                                     p, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == want, lib.pt_last_error()
+    bm.prepare_bwd(2, 1, 512)  # CUDA-core head dim: nothing to build
+    with pytest.raises(pt.PTError) as ei:
+        bm.prepare_bwd(2, 1, 520)
+    assert ei.value.status == pt.PT_ERR_UNSUPPORTED
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
