@@ -303,7 +303,9 @@ size_t pt_bwd_noalloc_max_scratch_bytes(void);
  * pt_hoststep_create: buffers for one shape (layouts as pt_attn_fwd /
  *   pt_attn_bwd: Q, dO, dQ [T, Hq, D]; K, V, dK, dV [T, Hkv, D]) on the
  *   current device; two non-blocking copy streams of its own.  Errors:
- *   PT_ERR_INVALID_ARG for a bad dtype or sizes, PT_ERR_NOMEM.
+ *   PT_ERR_INVALID_ARG for a bad dtype or sizes, PT_ERR_UNSUPPORTED for a
+ *   head_dim the attention calls do not take (above 512, or not a multiple
+ *   of 8 for bf16), PT_ERR_NOMEM.
  * pt_hoststep_run: hQ, hK, hV, hdO (host, read) and hdQ, hdK, hdV (host,
  *   written) are the caller's; pinned memory (cudaHostAlloc or registered)
  *   gives the overlap, pageable memory works but each copy then blocks.  The

@@ -69,6 +69,11 @@ pt_status pt_hoststep_create(pt_dtype dtype, int32_t T, int32_t Hq, int32_t Hkv,
     pt::set_error("pt_hoststep_create: bad dtype or sizes (T=%d Hq=%d Hkv=%d D=%d)", T, Hq, Hkv, D);
     return PT_ERR_INVALID_ARG;
   }
+  // the head dims pt_attn_fwd and pt_attn_bwd take, refused here before any buffer is made
+  if (D > 512 || (dtype == PT_BF16 && D % 8 != 0)) {
+    pt::set_error("pt_hoststep_create: head_dim %d unsupported (1..512, a multiple of 8 for bf16)", D);
+    return PT_ERR_UNSUPPORTED;
+  }
   pt_hoststep* h = new (std::nothrow) pt_hoststep;
   if (!h) return PT_ERR_NOMEM;
   std::memset(h, 0, sizeof(*h));

@@ -81,3 +81,18 @@ class _S:
 
 def _null_stream():
     return _S()
+
+
+def test_host_checks_before_any_device_work(lib):
+    """Argument checks that return before any CUDA call, so they run without a GPU."""
+    h = ctypes.c_void_p()
+    assert lib.pt_hoststep_create(pt.PT_BF16, 100, 4, 2, 520, ctypes.byref(h)) == pt.PT_ERR_UNSUPPORTED
+    assert b"head_dim" in lib.pt_last_error()
+    assert lib.pt_hoststep_create(pt.PT_BF16, 100, 4, 2, 100, ctypes.byref(h)) == pt.PT_ERR_UNSUPPORTED
+    assert lib.pt_hoststep_create(pt.PT_BF16, 100, 4, 3, 64, ctypes.byref(h)) == pt.PT_ERR_INVALID_ARG
+    assert lib.pt_hoststep_create(pt.PT_F32, 100, 4, 2, 0, ctypes.byref(h)) == pt.PT_ERR_INVALID_ARG
+    assert not h.value
+    rc = lib.pt_attn_bwd_noalloc(None, None, None, None, None, None, pt.PT_BF16, 10, 2, 2, 64, 0.0, None, None, None,
+                                 None, None)
+    assert rc == pt.PT_ERR_INVALID_ARG and b"NULL" in lib.pt_last_error()
+    assert lib.pt_blockmap_prepare_bwd(None, 2, 2, 64, None) == pt.PT_ERR_INVALID_ARG
