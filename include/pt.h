@@ -276,10 +276,19 @@ size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
  * The tensor-core backward also reads per-map work lists (which kv-major and
  * q-major work items each SM runs).  They are built once per block map and
  * head layout by pt_blockmap_prepare_bwd, which allocates them in the map's
- * own memory; a call whose map has no lists for its (Hq, Hkv, D) returns
- * PT_ERR_INVALID_ARG without launching anything.  Maps used only with the
- * CUDA-core paths (fp32, tiles other than 128 x 128, head dims other than
- * 64, 128 and 256) need no lists, and preparing them is a no-op.
+ * own memory; a call whose map has no lists for its layout returns
+ * PT_ERR_INVALID_ARG without launching anything.  The lists are kept per
+ * (Hq / Hkv, Hkv, the device's SM count) for the kv-major kernel and per
+ * (Hq, SM count) for the q-major kernels at head dims 128 and 256; head
+ * dims 64 and 128 share the kv-major lists.  pt_attn_bwd with a workspace
+ * builds lists of its own (long columns split across SMs) beside these and
+ * never replaces or frees them: every layout's lists stay with the map until
+ * pt_blockmap_free.  Maps used only with the CUDA-core paths (fp32, tiles
+ * other than 128 x 128, head dims other than 64, 128 and 256) need no lists,
+ * and preparing them is a no-op.
+ * After cudaDeviceReset the library must not be used again in the process:
+ * the array's looked-up address, like every map and pool, belongs to the
+ * context that the reset destroyed.
  * Shapes, dtypes, layouts and errors are otherwise those of pt_attn_bwd.
  * ------------------------------------------------------------------------- */
 pt_status pt_attn_bwd_noalloc(const void* dO, const void* Q, const void* K, const void* V, const void* O,
@@ -424,6 +433,14 @@ pt_status pt_debug_wait_timeout(cudaStream_t stream);
  * map or a bad head layout and PT_ERR_UNSUPPORTED for head_dim above 512, as
  * pt_attn_bwd does.  The pages have no counterpart. */
 pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv, int32_t D, cudaStream_t stream);
+
+/* Bytes of the library's private device memory pool on `device`: handed out
+ * now (*used_bytes) and held from the device (*reserved_bytes).  The pool is
+ * where block maps, fold plans and backward work lists live.  Meant for tests
+ * (for instance, that pt_attn_bwd_noalloc on a prepared map takes nothing
+ * from it); the pages have no counterpart.  PT_ERR_INVALID_ARG for NULL
+ * outputs or a negative device. */
+pt_status pt_debug_pool_usage(int32_t device, uint64_t* used_bytes, uint64_t* reserved_bytes);
 
 /* Accuracy check of the kernels' two exp2 paths: y[i] = 2^x[i] for i < n,
  * computed with the MUFU instruction (method 0) or with the FMA-pipe

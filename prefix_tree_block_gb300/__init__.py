@@ -78,6 +78,7 @@ def load_library(path: Optional[str] = None):
             "pt_unfold_grad": [vp, vp, ctypes.c_int, i64, vp, vp],
             "pt_fold_positions": [vp, vp, vp],
             "pt_fold_mismatches": [vp, vp, i64, vp, vp],
+            "pt_debug_pool_usage": [i32, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)

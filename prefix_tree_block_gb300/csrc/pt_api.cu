@@ -430,6 +430,14 @@ pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv
   return as_status(pt::prepare_bwd_noalloc(bm, Hq, Hkv, D, stream));
 }
 
+pt_status pt_debug_pool_usage(int32_t device, uint64_t* used_bytes, uint64_t* reserved_bytes) {
+  if (!used_bytes || !reserved_bytes || device < 0) {
+    set_error("pt_debug_pool_usage: bad arguments");
+    return PT_ERR_INVALID_ARG;
+  }
+  return as_status(pt::pool_usage(device, used_bytes, reserved_bytes));
+}
+
 pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cudaStream_t stream) {
   if (n < 0 || (n > 0 && (!x || !y)) || (method != 0 && method != 1)) {
     set_error("pt_debug_exp2: bad arguments (n=%lld, method=%d)", (long long)n, method);

@@ -816,6 +816,24 @@ void pool_free(void* p, cudaStream_t s) {
   if (p) cudaFreeAsync(p, s);
 }
 
+int pool_usage(int dev, uint64_t* used, uint64_t* reserved) {
+  *used = *reserved = 0;
+  cudaMemPool_t pool = pool_for(dev);
+  if (!pool) {
+    set_error("cannot create a device memory pool on device %d", dev);
+    return 3;
+  }
+  cuuint64_t u = 0, r = 0;
+  if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &u) != cudaSuccess ||
+      cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &r) != cudaSuccess) {
+    set_error("cannot read the memory pool's usage on device %d", dev);
+    return 3;
+  }
+  *used = u;
+  *reserved = r;
+  return 0;
+}
+
 // Sub-array layout inside one allocation, 256-byte aligned pieces.
 struct Layout {
   size_t off = 0;
@@ -1360,9 +1378,19 @@ void free_map(pt_blockmap* bm) {
     sl.ev = static_cast<cudaEvent_t>(bm->counts_ev);
     pinned_release(bm->device, sl);
   }
-  pool_free(bm->bwd_mem, bm->stream);
-  pool_free(bm->dq_mem, bm->stream);
-  std::free(bm->h_dq_empty);
+  for (pt_dkdv_lists* e = bm->dkdv_lists; e;) {
+    pt_dkdv_lists* nx = e->next;
+    pool_free(e->mem, bm->stream);
+    delete e;
+    e = nx;
+  }
+  for (pt_dq_lists* e = bm->dq_lists; e;) {
+    pt_dq_lists* nx = e->next;
+    pool_free(e->mem, bm->stream);
+    std::free(e->h_empty);
+    delete e;
+    e = nx;
+  }
   std::free(bm->h_rc_pred);
   std::free(bm->h_counts);
   pool_free(bm->mem_lists, bm->stream);

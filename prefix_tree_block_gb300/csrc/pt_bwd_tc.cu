@@ -1676,20 +1676,24 @@ int reserve_smem(K kernel, int bytes, int dev, int* flags) {
   return 0;
 }
 
-// Work items of the kv-major kernel for one head layout, cached on the map.
+// Work items of the kv-major kernel for one head layout, kept on the map.
 // Columns with more steps than about one SM's share are cut into chunks that
 // write fp32 partial sums to workspace slots (at most max_slots of them).  The
 // items are then packed onto the grid's CTAs longest first, each to the CTA
 // with the least work so far (LPT list scheduling), and stored grouped by CTA.
+// Every layout asked for gets its own entry, kept until the map is freed: a
+// call never frees lists that a kernel of another call may still be reading.
 std::mutex g_items_mu;
 
 int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, bool allow_build,
-                       cudaStream_t s) {
-  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
+                       cudaStream_t s, const pt_dkdv_lists** out) {
+  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the list cache is the map's only mutable part
   std::lock_guard<std::mutex> lk(g_items_mu);
-  if (bm->bwd_items && bm->bwd_g == g && bm->bwd_hkv == Hkv && bm->bwd_max_slots == max_slots &&
-      bm->bwd_sms == sms)
-    return 0;
+  for (const pt_dkdv_lists* e = bm->dkdv_lists; e; e = e->next)
+    if (e->g == g && e->hkv == Hkv && e->max_slots == max_slots && e->sms == sms) {
+      *out = e;
+      return 0;
+    }
   if (!allow_build) {
     set_error("block map's backward work lists are not prepared for this head layout "
               "(call pt_blockmap_prepare_bwd first)");
@@ -1757,46 +1761,50 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
     for (int i : bins[b]) packed.push_back(items[i]);
     cta[b + 1] = (int)packed.size();
   }
-  pool_free(bm->bwd_mem, s);
-  bm->bwd_mem = nullptr;
-  bm->bwd_items = nullptr;
+  pt_dkdv_lists* e = new pt_dkdv_lists();
   const size_t bi = sizeof(DkdvItem) * std::max<size_t>(packed.size(), 1);
   const size_t bs = sizeof(int4) * std::max<size_t>(splits.size(), 1);
   const size_t bc = sizeof(int) * (grid + 1);
-  int rc = pool_alloc(&bm->bwd_mem, bi + bs + bc, bm->device, s);
-  if (rc) return rc;
-  bm->bwd_items = bm->bwd_mem;
-  bm->bwd_splits = static_cast<char*>(bm->bwd_mem) + bi;
-  bm->bwd_cta = static_cast<char*>(bm->bwd_mem) + bi + bs;
+  int rc = pool_alloc(&e->mem, bi + bs + bc, bm->device, s);
+  if (rc) {
+    delete e;
+    return rc;
+  }
+  e->items = e->mem;
+  e->splits = static_cast<char*>(e->mem) + bi;
+  e->cta = static_cast<char*>(e->mem) + bi + bs;
   {  // one upload in the device layout: items | splits | CTA index
     std::vector<char> host(bi + bs + bc, 0);
     if (!packed.empty()) std::memcpy(host.data(), packed.data(), sizeof(DkdvItem) * packed.size());
     if (!splits.empty()) std::memcpy(host.data() + bi, splits.data(), sizeof(int4) * splits.size());
     std::memcpy(host.data() + bi + bs, cta.data(), bc);
-    if ((rc = upload(bm->bwd_mem, host.data(), host.size(), bm->device, s))) return rc;
+    if ((rc = upload(e->mem, host.data(), host.size(), bm->device, s))) {
+      pool_free(e->mem, s);
+      delete e;
+      return rc;
+    }
   }
-  bm->bwd_g = g;
-  bm->bwd_hkv = Hkv;
-  bm->bwd_max_slots = max_slots;
-  bm->bwd_n_items = (int)packed.size();
-  bm->bwd_grid = grid;
-  bm->bwd_sms = sms;
-  bm->bwd_n_splits = (int)splits.size();
-  bm->bwd_n_slots = slot;
+  e->g = g;
+  e->hkv = Hkv;
+  e->max_slots = max_slots;
+  e->sms = sms;
+  e->n_items = (int)packed.size();
+  e->grid = grid;
+  e->n_splits = (int)splits.size();
+  e->n_slots = slot;
+  e->next = bm->dkdv_lists;
+  bm->dkdv_lists = e;
+  *out = e;
   return 0;
 }
 
-// Work items of the pipelined q-major kernel, cached on the map: every
-// (q tile, head) with at least one kv block, packed longest first onto the
-// grid's CTAs by LPT list scheduling and stored grouped by CTA, plus the q
-// tiles with no kv block at all (their dQ rows are zero).
 // dQ rows of the q tiles that attend to nothing are zero: one memset per run
 // of consecutive such tiles (the list is ascending).
-int zero_empty_dq(const pt_blockmap* bm, void* dQ, int T, int Hq, int D, cudaStream_t s) {
-  for (int i = 0; i < bm->dq_n_empty;) {
+int zero_empty_dq(const pt_dq_lists* L, void* dQ, int T, int Hq, int D, cudaStream_t s) {
+  for (int i = 0; i < L->n_empty;) {
     int e = i + 1;
-    while (e < bm->dq_n_empty && bm->h_dq_empty[e] == bm->h_dq_empty[e - 1] + 1) ++e;
-    const int t0 = bm->h_dq_empty[i] * 128, t1 = std::min(T, bm->h_dq_empty[e - 1] * 128 + 128);
+    while (e < L->n_empty && L->h_empty[e] == L->h_empty[e - 1] + 1) ++e;
+    const int t0 = L->h_empty[i] * 128, t1 = std::min(T, L->h_empty[e - 1] * 128 + 128);
     if (cudaMemsetAsync(static_cast<__nv_bfloat16*>(dQ) + (size_t)t0 * Hq * D, 0,
                         sizeof(__nv_bfloat16) * (size_t)(t1 - t0) * Hq * D, s) != cudaSuccess) {
       set_error("backward: cudaMemsetAsync failed");
@@ -1807,10 +1815,19 @@ int zero_empty_dq(const pt_blockmap* bm, void* dQ, int T, int Hq, int D, cudaStr
   return 0;
 }
 
-int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, cudaStream_t s) {
-  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the item cache is the map's only mutable part
+// Work items of the pipelined q-major kernel, kept on the map per head count:
+// every (q tile, head) with at least one kv block, packed longest first onto
+// the grid's CTAs by LPT list scheduling and stored grouped by CTA, plus the
+// q tiles with no kv block at all (their dQ rows are zero).
+int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, cudaStream_t s,
+                     const pt_dq_lists** out) {
+  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the list cache is the map's only mutable part
   std::lock_guard<std::mutex> lk(g_items_mu);
-  if (bm->dq_items && bm->dq_hq == Hq && bm->dq_sms == sms) return 0;
+  for (const pt_dq_lists* e = bm->dq_lists; e; e = e->next)
+    if (e->hq == Hq && e->sms == sms) {
+      *out = e;
+      return 0;
+    }
   if (!allow_build) {
     set_error("block map's dQ work lists are not prepared for this head count (call pt_blockmap_prepare_bwd first)");
     return 1;
@@ -1857,35 +1874,44 @@ int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, 
     cta[b].z = (int)blocks[b];
     cta[b].w = 0;
   }
-  pool_free(bm->dq_mem, s);
-  bm->dq_mem = nullptr;
-  bm->dq_items = nullptr;
-  std::free(bm->h_dq_empty);
-  bm->h_dq_empty = nullptr;
+  pt_dq_lists* e = new pt_dq_lists();
+  if (!empty.empty()) {
+    e->h_empty = static_cast<int*>(std::malloc(sizeof(int) * empty.size()));
+    if (!e->h_empty) {
+      delete e;
+      set_error("out of host memory");
+      return 4;
+    }
+    std::copy(empty.begin(), empty.end(), e->h_empty);
+  }
   const size_t bi = sizeof(int4) * std::max<size_t>(packed.size(), 1), bc = sizeof(int4) * grid;
-  int rc = pool_alloc(&bm->dq_mem, bi + bc, bm->device, s);
-  if (rc) return rc;
-  bm->dq_items = bm->dq_mem;
-  bm->dq_cta = static_cast<char*>(bm->dq_mem) + bi;
+  int rc = pool_alloc(&e->mem, bi + bc, bm->device, s);
+  if (rc) {
+    std::free(e->h_empty);
+    delete e;
+    return rc;
+  }
+  e->items = e->mem;
+  e->cta = static_cast<char*>(e->mem) + bi;
   {  // one upload in the device layout: items | CTA records
     std::vector<char> host(bi + bc, 0);
     if (!packed.empty()) std::memcpy(host.data(), packed.data(), sizeof(int4) * packed.size());
     std::memcpy(host.data() + bi, cta.data(), bc);
-    if ((rc = upload(bm->dq_mem, host.data(), host.size(), bm->device, s))) return rc;
-  }
-  if (!empty.empty()) {
-    bm->h_dq_empty = static_cast<int*>(std::malloc(sizeof(int) * empty.size()));
-    if (!bm->h_dq_empty) {
-      set_error("out of host memory");
-      return 4;
+    if ((rc = upload(e->mem, host.data(), host.size(), bm->device, s))) {
+      pool_free(e->mem, s);
+      std::free(e->h_empty);
+      delete e;
+      return rc;
     }
-    std::copy(empty.begin(), empty.end(), bm->h_dq_empty);
   }
-  bm->dq_n_empty = (int)empty.size();
-  bm->dq_hq = Hq;
-  bm->dq_sms = sms;
-  bm->dq_grid = grid;
-  bm->dq_n_items = (int)packed.size();
+  e->n_empty = (int)empty.size();
+  e->hq = Hq;
+  e->sms = sms;
+  e->grid = grid;
+  e->n_items = (int)packed.size();
+  e->next = bm->dq_lists;
+  bm->dq_lists = e;
+  *out = e;
   return 0;
 }
 
@@ -1909,7 +1935,10 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   }
   const int sms = num_sms(dev);
   const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s))) return rc;
+  const pt_dkdv_lists* KL = nullptr;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s, &KL))) return rc;
+  const pt_dq_lists* QL = nullptr;
+  if (D == 128 && (rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
   const int Tpad = bm->nq * 128;
   {
     const size_t sm = sizeof(float) * kPrepTokens * ((size_t)Hq + 1);
@@ -1944,19 +1973,19 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   p.out0 = static_cast<__nv_bfloat16*>(dK);
   p.out1 = static_cast<__nv_bfloat16*>(dV);
   p.n_major = bm->nk;
-  p.items = static_cast<const DkdvItem*>(bm->bwd_items);
-  p.n_items = bm->bwd_n_items;
-  p.cta_ptr = static_cast<const int*>(bm->bwd_cta);
+  p.items = static_cast<const DkdvItem*>(KL->items);
+  p.n_items = KL->n_items;
+  p.cta_ptr = static_cast<const int*>(KL->cta);
   p.partial = partial;
   int launches = 1;
   if (p.n_items > 0) {
     ProfScope ps(s, "bwd_dkdv");
-    launch_pdl(k_bwd_dkdv<D>, dim3(bm->bwd_grid), dim3(320), DkdvL<D>::BYTES, s, mQ, mdO, mK, mV, p);
+    launch_pdl(k_bwd_dkdv<D>, dim3(KL->grid), dim3(320), DkdvL<D>::BYTES, s, mQ, mdO, mK, mV, p);
     ++launches;
   }
-  if (bm->bwd_n_splits > 0) {
+  if (KL->n_splits > 0) {
     ProfScope ps(s, "bwd_dkdv_finalize");
-    launch_pdl(k_dkdv_finalize<D>, dim3(dim3(bm->bwd_n_splits, 16)), dim3(256), 0, s, static_cast<const int4*>(bm->bwd_splits), partial, T, Hkv, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
+    launch_pdl(k_dkdv_finalize<D>, dim3(dim3(KL->n_splits, 16)), dim3(256), 0, s, static_cast<const int4*>(KL->splits), partial, T, Hkv, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
     ++launches;
   }
   // dQ
@@ -1975,12 +2004,11 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   if (items > 0) {
     ProfScope ps(s, "bwd_dq");
     if constexpr (D == 128) {
-      if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s))) return rc;
-      if ((rc = zero_empty_dq(bm, dQ, T, Hq, D, s))) return rc;
-      p.dq_items = static_cast<const int4*>(bm->dq_items);
-      p.dq_cta = static_cast<const int4*>(bm->dq_cta);
-      if (bm->dq_n_items > 0)
-        launch_pdl(k_bwd_dq_pipe<D>, dim3(bm->dq_grid), dim3(DqpCfg<D>::THREADS), DqpL<D>::BYTES, s, mQ, mdO, mK, mV, p);
+      if ((rc = zero_empty_dq(QL, dQ, T, Hq, D, s))) return rc;
+      p.dq_items = static_cast<const int4*>(QL->items);
+      p.dq_cta = static_cast<const int4*>(QL->cta);
+      if (QL->n_items > 0)
+        launch_pdl(k_bwd_dq_pipe<D>, dim3(QL->grid), dim3(DqpCfg<D>::THREADS), DqpL<D>::BYTES, s, mQ, mdO, mK, mV, p);
     } else {
       launch_pdl(k_bwd_dq<D>, dim3(items < sms ? items : sms), dim3(320), DqL<D>::BYTES, s, mQ, mdO, mK, mV, mdQ, p);
     }
@@ -2012,8 +2040,10 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   }
   const int sms = num_sms(dev);
   // kv-major items without split columns (each pass writes its outputs once)
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, allow_build, s))) return rc;
-  if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s))) return rc;
+  const pt_dkdv_lists* KL = nullptr;
+  const pt_dq_lists* QL = nullptr;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, allow_build, s, &KL))) return rc;
+  if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
   const int Tpad = bm->nq * 128;
   {
     const size_t sm = sizeof(float) * kPrepTokens * ((size_t)Hq + 1);
@@ -2046,19 +2076,19 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   p.idx = bm->q_idx;
   p.pidx = bm->pidxT;
   p.masks = bm->mask_cols;
-  p.items = static_cast<const DkdvItem*>(bm->bwd_items);
-  p.cta_ptr = static_cast<const int*>(bm->bwd_cta);
-  p.n_items = bm->bwd_n_items;
+  p.items = static_cast<const DkdvItem*>(KL->items);
+  p.cta_ptr = static_cast<const int*>(KL->cta);
+  p.n_items = KL->n_items;
   p.out0 = static_cast<__nv_bfloat16*>(dK);
   p.out1 = static_cast<__nv_bfloat16*>(dV);
   if (p.n_items > 0) {
     {
       ProfScope ps(s, "bwd_dv");
-      launch_pdl(k_bwd_wide<WIDE_DV>, dim3(bm->bwd_grid), dim3(320), WideCfg<WIDE_DV>::BYTES, s, mK, mK, mdOh, mQh, p);
+      launch_pdl(k_bwd_wide<WIDE_DV>, dim3(KL->grid), dim3(320), WideCfg<WIDE_DV>::BYTES, s, mK, mK, mdOh, mQh, p);
     }
     {
       ProfScope ps(s, "bwd_dk");
-      launch_pdl(k_bwd_wide<WIDE_DK>, dim3(bm->bwd_grid), dim3(320), WideCfg<WIDE_DK>::BYTES, s, mK, mV, mQh, mdOh, p);
+      launch_pdl(k_bwd_wide<WIDE_DK>, dim3(KL->grid), dim3(320), WideCfg<WIDE_DK>::BYTES, s, mK, mV, mQh, mdOh, p);
     }
     launches += 2;
   }
@@ -2068,14 +2098,14 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   p.masks = bm->mask_rows;
   p.items = nullptr;
   p.cta_ptr = nullptr;
-  p.dq_items = static_cast<const int4*>(bm->dq_items);
-  p.dq_cta = static_cast<const int4*>(bm->dq_cta);
+  p.dq_items = static_cast<const int4*>(QL->items);
+  p.dq_cta = static_cast<const int4*>(QL->cta);
   p.out0 = static_cast<__nv_bfloat16*>(dQ);
   p.out1 = nullptr;
-  if ((rc = zero_empty_dq(bm, dQ, T, Hq, D, s))) return rc;
-  if (bm->dq_n_items > 0) {
+  if ((rc = zero_empty_dq(QL, dQ, T, Hq, D, s))) return rc;
+  if (QL->n_items > 0) {
     ProfScope ps(s, "bwd_dq");
-    launch_pdl(k_bwd_wide<WIDE_DQ>, dim3(bm->dq_grid), dim3(320), WideCfg<WIDE_DQ>::BYTES, s, mQ, mdO, mKh, mVh, p);
+    launch_pdl(k_bwd_wide<WIDE_DQ>, dim3(QL->grid), dim3(320), WideCfg<WIDE_DQ>::BYTES, s, mQ, mdO, mKh, mVh, p);
     ++launches;
   }
   count_launch(launches);
@@ -2094,8 +2124,10 @@ bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
 int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStream_t s) {
   if (!bwd_tc_supported(D) || bm->BM != 128 || bm->BN != 128) return 0;  // those paths keep no lists
   const int sms = num_sms(bm->device);
-  int rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, true, s);
-  if (!rc && D >= 128) rc = prepare_dq_items(bm, Hq, sms, true, s);
+  const pt_dkdv_lists* KL = nullptr;
+  const pt_dq_lists* QL = nullptr;
+  int rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, true, s, &KL);
+  if (!rc && D >= 128) rc = prepare_dq_items(bm, Hq, sms, true, s, &QL);
   return rc;
 }
 

@@ -24,6 +24,28 @@ struct pt_tok {
   int32_t tout;
 };
 
+// Work lists of the kv-major backward kernel for one head layout.
+struct pt_dkdv_lists {
+  pt_dkdv_lists* next;
+  int g, hkv, max_slots, sms;  // the key: group size, kv heads, partial-sum slots allowed, SM count
+  int n_items, n_splits, n_slots, grid;
+  void* mem;     // one pool allocation: items | splits | CTA index
+  void* items;   // DkdvItem[n_items] (device), grouped by the CTA that runs them
+  void* splits;  // int4[n_splits]: kv block, kv head, first slot, slot count (device)
+  void* cta;     // int[grid + 1]: CTA b runs items [cta[b], cta[b + 1])
+};
+
+// Work lists of the q-major (dQ) kernels for one head count.
+struct pt_dq_lists {
+  pt_dq_lists* next;
+  int hq, sms;  // the key
+  int grid, n_items, n_empty;
+  void* mem;     // one pool allocation: items | CTA records
+  void* items;   // int4[n_items]: q tile, head, first list entry, kv blocks; grouped by CTA
+  void* cta;     // int4[grid]: first item, end item, kv blocks of the CTA
+  int* h_empty;  // [n_empty] q tiles without any kv block (their dQ rows are zero), ascending
+};
+
 struct pt_blockmap {
   int device;
   cudaStream_t stream;  // the build stream; memory is returned to the pool in its order
@@ -80,18 +102,11 @@ struct pt_blockmap {
   int producer;
   int32_t d_ctx, d_bs, d_nb, d_causal, d_window;
   void* d_blk;  // int4[d_nb] (device): kept context [x, y) before any window, anchor z, keep flag w
-  // backward work items of the kv-major kernel, cached for one head layout
-  void* bwd_mem;
-  int bwd_g, bwd_hkv, bwd_max_slots, bwd_n_items, bwd_n_splits, bwd_n_slots, bwd_grid, bwd_sms;
-  void* bwd_items;   // DkdvItem[bwd_n_items] (device), grouped by the CTA that runs them
-  void* bwd_cta;     // int[bwd_grid + 1]: CTA b runs items [bwd_cta[b], bwd_cta[b + 1])
-  void* bwd_splits;  // int4[bwd_n_splits]: kv block, kv head, first slot, slot count (device)
-  // work items of the pipelined q-major (dQ) kernel, cached for one head count
-  void* dq_mem;
-  int dq_hq, dq_sms, dq_grid, dq_n_items, dq_n_empty;
-  void* dq_items;   // int4[dq_n_items]: q tile, head, first list entry, kv blocks; grouped by CTA
-  void* dq_cta;     // int4[dq_grid]: first item, end item, kv blocks of the CTA
-  int* h_dq_empty;  // q tiles without any kv block (their dQ rows are zero)
+  // backward work lists, one entry per head layout asked for (built on first
+  // use, kept until the map is freed, so no call evicts lists another stream
+  // may still be reading)
+  struct pt_dkdv_lists* dkdv_lists;
+  struct pt_dq_lists* dq_lists;
 };
 
 // Work item of the kv-major backward kernel: steps [x0, x1) of the (kv block,
@@ -146,6 +161,8 @@ inline bool masks_missing(const pt_blockmap* bm) {
 // staging for small host-to-device uploads (pt_blockmap.cu).
 int pool_alloc(void** p, size_t bytes, int dev, cudaStream_t s);
 void pool_free(void* p, cudaStream_t s);
+// Bytes of the pool on `dev` handed out now and held from the device.
+int pool_usage(int dev, uint64_t* used, uint64_t* reserved);
 int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s);
 
 // Device status word of each translation unit: read and clear.

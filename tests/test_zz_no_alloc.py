@@ -6,9 +6,12 @@ get scratch, or a latency-critical path where an allocation (which can
 synchronise the device) is not allowed.  Its scratch lives in a fixed array
 inside the library.  These tests call it through the C ABI (ctypes on
 libpt.so) and check that two calls in a row give the same gradients as
-pt_attn_bwd with a caller workspace, within the parity tolerance used for the
-backward (relative L2 norm 3e-2 for bf16, 1e-5 for fp32).  The file is named
-to be collected last.
+pt_attn_bwd with a caller workspace, and the same gradients as the fp64
+oracle, within the parity tolerance used for the backward (relative L2 norm
+3e-2 for bf16, 1e-5 for fp32).  They also check that on a prepared map the
+calls take nothing from the library's device memory pool, and that a
+workspace backward on the same map leaves the prepared lists in place.  The
+file is named to be collected last.
 """
 import ctypes
 
@@ -17,6 +20,7 @@ import pytest
 import torch
 
 import prefix_tree_block_gb300 as pt
+from oracle import oracle as orc
 from prefix_tree_block_gb300 import workloads as W
 from parity import GRAD_RL2, ensure_built, rel_l2
 
@@ -41,6 +45,12 @@ def _noalloc(lib, dO, Q, K, V, O, LSE, bm, dtype_code, expect=pt.PT_OK):
     return dQ, dK, dV
 
 
+def _pool_usage(lib):
+    used, reserved = ctypes.c_uint64(), ctypes.c_uint64()
+    assert lib.pt_debug_pool_usage(torch.cuda.current_device(), ctypes.byref(used), ctypes.byref(reserved)) == 0
+    return used.value, reserved.value
+
+
 @pytest.mark.parametrize("dtype,D,BM", [("bf16", 64, 128), ("bf16", 128, 128), ("bf16", 256, 128), ("bf16", 96, 128),
                                         ("bf16", 320, 128), ("f32", 32, 16)])
 def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
@@ -63,11 +73,41 @@ def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
             assert rel_l2(g, r) <= GRAD_RL2[dtype]
     bm.prepare_bwd(Q.shape[1], K.shape[1], D)
     bm.prepare_bwd(Q.shape[1], K.shape[1], D)  # idempotent
+    torch.cuda.synchronize()
+    pool_before = _pool_usage(lib)
+    want = orc.attn_bwd(q, k, v, do, orc.structure_labels(st))
     for _ in range(2):
         got = [x.float().cpu().numpy() for x in _noalloc(lib, dO, Q, K, V, O, LSE, bm, code)]
-        for g, r in zip(got, ref):
+        for g, r, w in zip(got, ref, want):
             assert np.isfinite(g).all()
             assert rel_l2(g, r) <= GRAD_RL2[dtype]
+            assert rel_l2(g, w) <= GRAD_RL2[dtype]
+    assert _pool_usage(lib) == pool_before  # nothing taken from (or added to) the library's pool
+    pt.sync_status()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_noalloc_lists_survive_a_workspace_backward(lib, D):
+    """A workspace backward on a prepared map builds lists of its own (long
+    columns split across SMs) beside the prepared ones; the allocation-free
+    call must still find its lists afterwards."""
+    st = W.grpo_structure([(700, [300, 41, 250, 640]), (0, [77, 129])])
+    q, k, v, do = W.make_tensors(st.T, 4, 2, D, "bf16", seed=D + 1)
+    Q, K, V, dO = (x.cuda() for x in (q, k, v, do))
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes)
+    O, LSE = pt.attn_fwd(Q, K, V, bm)
+    bm.prepare_bwd(4, 2, D)
+    first = [x.float().cpu().numpy() for x in _noalloc(lib, dO, Q, K, V, O, LSE, bm, pt.PT_BF16)]
+    ws = [x.float().cpu().numpy() for x in pt.attn_bwd(dO, Q, K, V, O, LSE, bm)]
+    torch.cuda.synchronize()
+    pool_before = _pool_usage(lib)
+    again = [x.float().cpu().numpy() for x in _noalloc(lib, dO, Q, K, V, O, LSE, bm, pt.PT_BF16)]
+    assert _pool_usage(lib) == pool_before
+    want = orc.attn_bwd(q, k, v, do, orc.structure_labels(st))
+    for a, b, c, w in zip(first, again, ws, want):
+        np.testing.assert_array_equal(a, b)  # the same lists and kernels: bit-identical
+        assert rel_l2(a, w) <= GRAD_RL2["bf16"]
+        assert rel_l2(c, w) <= GRAD_RL2["bf16"]
     pt.sync_status()
 
 
