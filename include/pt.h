@@ -327,6 +327,12 @@ size_t pt_bwd_noalloc_max_scratch_bytes(void);
  *   map of another T.
  * pt_hoststep_sync: makes `stream` wait for every download queued so far
  *   (synchronise the stream, or record an event on it, to wait on the host).
+ * pt_hoststep_last_forward: copies the forward outputs of the most recent
+ *   pt_hoststep_run, O [T, Hq, D] (dtype) and LSE [Hq, T] (fp32), into host
+ *   memory hO and hLSE; waits for that step's kernels first (blocking).  For
+ *   tests and inspection: a training step needs only the gradients.  Must be
+ *   called before the next pt_hoststep_run reuses that step's buffers.
+ *   Errors: PT_ERR_INVALID_ARG for NULL pointers or before any run.
  * pt_hoststep_free: waits for the object's copies and frees it.
  * ------------------------------------------------------------------------- */
 typedef struct pt_hoststep pt_hoststep;
@@ -334,6 +340,7 @@ pt_status pt_hoststep_create(pt_dtype dtype, int32_t T, int32_t Hq, int32_t Hkv,
 pt_status pt_hoststep_run(pt_hoststep* h, const void* hQ, const void* hK, const void* hV, const void* hdO,
                           float scale, const pt_blockmap* bm, void* hdQ, void* hdK, void* hdV, cudaStream_t stream);
 pt_status pt_hoststep_sync(pt_hoststep* h, cudaStream_t stream);
+pt_status pt_hoststep_last_forward(pt_hoststep* h, void* hO, float* hLSE);
 void pt_hoststep_free(pt_hoststep* h);
 
 /* ---------------------------------------------------------------------------

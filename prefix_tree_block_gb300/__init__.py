@@ -71,6 +71,7 @@ def load_library(path: Optional[str] = None):
             "pt_hoststep_create": [ctypes.c_int, i32, i32, i32, i32, pp],
             "pt_hoststep_run": [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp],
             "pt_hoststep_sync": [vp, vp],
+            "pt_hoststep_last_forward": [vp, vp, vp],
             "pt_fold_plan": [vp, i32, vp, vp, i32, i32, vp, pp],
             "pt_foldplan_info": [vp, i32p, i32p, i32p],
             "pt_fold": [vp, vp, i64, vp, vp],
@@ -420,6 +421,17 @@ class HostStep:
     def sync(self, stream=None):
         """Make the stream wait for every download queued so far."""
         _check(self._lib.pt_hoststep_sync(self._h, ctypes.c_void_p(_stream(stream))))
+
+    def last_forward(self):
+        """O [T, Hq, D] and LSE [Hq, T] of the most recent run(), as new host
+        tensors (waits for that step's kernels)."""
+        import torch
+
+        T, Hq, Hkv, D = self.shape
+        O = torch.empty((T, Hq, D), dtype=self._dt)
+        L = torch.empty((Hq, T), dtype=torch.float32)
+        _check(self._lib.pt_hoststep_last_forward(self._h, _ptr(O), _ptr(L)))
+        return O, L
 
     def free(self):
         if self._h is not None and self._h.value:

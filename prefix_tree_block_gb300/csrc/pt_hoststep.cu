@@ -194,6 +194,21 @@ pt_status pt_hoststep_sync(pt_hoststep* h, cudaStream_t stream) {
   return PT_OK;
 }
 
+pt_status pt_hoststep_last_forward(pt_hoststep* h, void* hO, float* hLSE) {
+  if (!h || h->n == 0 || (h->T > 0 && (!hO || !hLSE))) {
+    pt::set_error("pt_hoststep_last_forward: NULL argument or no step run yet");
+    return PT_ERR_INVALID_ARG;
+  }
+  const int b = (int)((h->n - 1) & 1);
+  if (cudaEventSynchronize(h->computed[b]) != cudaSuccess ||
+      cudaMemcpy(hO, h->set[b].O, h->bq, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(hLSE, h->set[b].LSE, h->blse, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    pt::set_error("pt_hoststep_last_forward: %s", cudaGetErrorString(cudaGetLastError()));
+    return PT_ERR_CUDA;
+  }
+  return PT_OK;
+}
+
 void pt_hoststep_free(pt_hoststep* h) { destroy(h); }
 
 }  // extern "C"

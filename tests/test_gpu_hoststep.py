@@ -1,12 +1,16 @@
 """Forward and backward from host memory (pt_hoststep): every pipelined step's
-host gradients equal the device-resident path's on the same inputs."""
+host gradients equal the device-resident path's on the same inputs and the
+fp64 oracle's, and the last step's forward outputs (O, LSE) equal the
+oracle's."""
 import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
 
 import prefix_tree_block_gb300 as pt
+from oracle import oracle as orc
 from prefix_tree_block_gb300 import workloads as W
+from parity import FWD_ATOL, GRAD_RL2, LSE_ATOL, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -42,16 +46,24 @@ def test_hoststep_pipeline_matches_device_path(workload):
     hs.sync()
     torch.cuda.synchronize()
     pt.sync_status()
+    O_last, L_last = hs.last_forward()
     for bm in maps:
         bm.free()
     hs.free()
+    lab = orc.structure_labels(st)
+    q, k, v, do = steps[-1]
+    Ow, Lw = orc.attn_fwd(q, k, v, lab)
+    assert np.abs(O_last.float().numpy() - Ow).max() <= FWD_ATOL["bf16"]
+    assert np.abs(L_last.numpy() - Lw).max() <= LSE_ATOL["bf16"]
     for (q, k, v, do), (dq, dk, dv) in zip(steps, outs):
         rq, rk, rv = _device_grads(q, k, v, do, st)
-        for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        want = orc.attn_bwd(q, k, v, do, lab)
+        for got, ref, w in zip((dq, dk, dv), (rq, rk, rv), want):
             g, r = got.float().numpy(), ref.float().numpy()
             # same kernels on the same inputs: equal up to the order of fp32
             # partial sums of split columns
             assert np.linalg.norm(g - r) <= 1e-3 * np.linalg.norm(r) + 1e-6
+            assert rel_l2(g, w) <= GRAD_RL2["bf16"]
 
 
 def test_hoststep_rejects_bad_arguments():
