@@ -324,6 +324,150 @@ def run_reference(args, cfg, st):
     print(json.dumps(line), flush=True)
 
 
+def measure_device(workload, steps, warmup, with_dense, flush, dist, local, world):
+    """Device-resident measurement of one workload: the step (map build from
+    the host layout, forward, backward) timed over `steps` steps with the L2
+    flushed before each, the per-kernel durations from a second timed pass,
+    forward and backward fractions of the bf16 peak, the roofline of the
+    dominant kernel and the dense-masked comparison."""
+    import torch
+
+    import prefix_tree_block_gb300 as pt
+    from prefix_tree_block_gb300 import workloads as W
+
+    cfg = dict(W.CONFIGS[workload])
+    st = W.config_structure(workload)
+    Hq, Hkv, D, dtype = cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["dtype"]
+    T = st.T
+    pairs = useful_pairs(st)
+    flops_fwd = 4.0 * D * Hq * pairs
+    flops_step = flops_fwd * 3.5
+    q, k, v, do = W.make_tensors(T, Hq, Hkv, D, dtype, workload)
+    dev = torch.device("cuda", local)
+    Q, K, V, dO = (x.to(dev) for x in (q, k, v, do))
+    O = torch.empty_like(Q)
+    LSE = torch.empty(Hq, T, dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ws = torch.empty(pt.bwd_workspace_bytes(T, Hq, D), dtype=torch.uint8, device=dev)
+    draft = hasattr(st, "anchors")
+    if draft:
+        host_layout = [a for a in (st.anchors, st.block_keep, st.ctx_doc, st.anchor_doc) if a is not None]
+        make_map = lambda: pt.build_blockmap_draft(**st.kwargs())
+    else:
+        nl, pp, pn = st.node_lengths, st.path_ptr, st.path_nodes
+        host_layout = [nl, pp, pn]
+        make_map = lambda: pt.build_blockmap_tree(nl, pp, pn, 128, 128)
+    stream = torch.cuda.current_stream()
+
+    def step(dense=False):
+        bm = make_map()
+        if dense:
+            d = bm.dense()
+            bm.free()
+            bm = d
+        pt.attn_fwd(Q, K, V, bm, O=O, LSE=LSE)
+        pt.attn_bwd(dO, Q, K, V, O, LSE, bm, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+        bm.free()
+
+    for _ in range(warmup):
+        step()
+    pt.sync_status()
+
+    def timed(n, fn):
+        evs = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = pt.launch_count()
+    pt.profile_reset()
+    # the step time: no events inside the step (an event between two kernels
+    # costs the launch overlap, about 3 us per boundary)
+    times = timed(steps, step)
+    launches = pt.launch_count() - launches0
+    torch.cuda.synchronize()
+    # per-kernel durations: the same K steps again, each kernel bracketed by
+    # CUDA events on its stream
+    pt.profile_enable(True)
+    timed(steps, step)
+    pt.profile_enable(False)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    pt.sync_status()
+    total_ms = max_over_ranks(sum(times), dist, dev)
+    ms_step = total_ms / steps
+    value = whole_job_tflops(world, flops_step, steps, total_ms)
+
+    kernels = {}
+    for name in ("blockmap_classify", "blockmap_lists", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
+                 "bwd_dkdv_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt"):
+        n, ms = pt.profile_read(name)
+        if n:
+            kernels[name] = {"launches": n, "ms_per_launch": ms / n}
+    pt.profile_reset()
+
+    # ---- forward and backward fractions, roofline of the dominant kernel ----
+    peak_tf, peak_gbs, peak_src = peaks()
+    fwd_ms = sum(kernels[k]["ms_per_launch"] for k in ("fwd_tc", "fwd_simt") if k in kernels)
+    bwd_ms = sum(kernels[k]["ms_per_launch"] for k in kernels if k.startswith("bwd_"))
+    fwd_tf = flops_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None
+    bwd_tf = 2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None
+    per_launch_flops = {  # useful-pair flops of each kernel: 2D per pair and head for each of its products
+        "fwd_tc": 4.0 * D * Hq * pairs,
+        "bwd_dkdv": 8.0 * D * Hq * pairs,
+        "bwd_dv": 4.0 * D * Hq * pairs,  # head_dim 256: S^T and dV
+        "bwd_dk": 6.0 * D * Hq * pairs,  # head_dim 256: S^T, dP^T and dK
+        "bwd_dq": 6.0 * D * Hq * pairs,
+        # CUDA-core kernels (fp32 inputs, head dims without a tensor-core path): useful flops
+        "fwd_simt": 4.0 * D * Hq * pairs,
+        "bwd_simt": 10.0 * D * Hq * pairs,
+    }
+    tc = {k: v for k, v in kernels.items() if k in per_launch_flops}
+    roofline = None
+    if tc:
+        dom = max(tc, key=lambda k: tc[k]["ms_per_launch"])
+        ach = per_launch_flops[dom] / (tc[dom]["ms_per_launch"] * 1e-3) / 1e12
+        if dom.endswith("_simt"):  # fp32 FMA pipes: SMs x 128 lanes x 2 flop x max SM clock
+            fp32_peak = FP32_LANES_PER_SM * num_sms() * 2 * SM_MAX_GHZ / 1e3
+            roofline = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                        "frac": ach / fp32_peak, "traffic": None,
+                        "peak_source": f"derived: {num_sms()} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 flop x "
+                                       f"{SM_MAX_GHZ} GHz"}
+        else:
+            roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                        "frac": ach / peak_tf, "traffic": MEASURED_TRAFFIC.get((workload, dom)),
+                        "peak_source": f"{peak_src} bf16 burst"}
+
+    # ---- dense-masked comparison (same kernels, every tile partial) ---------
+    dense = None
+    if with_dense:
+        step(dense=True)
+        dt = timed(max(2, min(5, steps)), lambda: step(dense=True))
+        dense = {"ms_per_step": sum(dt) / len(dt), "speedup": (sum(dt) / len(dt)) / ms_step}
+    pt.sync_status()
+    out = {
+        "workload": cfg["name"], "T": T, "useful_pairs_per_head": pairs, "useful_tflop_per_step": flops_step / 1e12,
+        "steps": steps, "ms_per_step": ms_step, "value": value, "unit": "TFLOP/s",
+        "frac_of_peak": value / world / peak_tf,
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak_tf if fwd_tf else None},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak_tf if bwd_tf else None},
+        "kernels": kernels, "roofline": roofline, "dense_masked": dense, "gpu_launches": int(launches),
+        "_ctx": {"tensors": (Q, K, V, dO, q, k, v, do), "grads": (dQ, dK, dV), "make_map": make_map,
+                 "host_layout": host_layout, "stream": stream, "timed": timed},
+    }
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -334,6 +478,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-fold", action="store_true")
+    ap.add_argument("--no-other-workloads", dest="all_workloads", action="store_false",
+                    help="with the default workload 2, skip the workloads 3..7 section")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -365,124 +511,35 @@ def main():
         dist.barrier()
     pt.load_library()
 
-    Hq, Hkv, D, dtype = cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["dtype"]
-    T = st.T
-    pairs = useful_pairs(st)
-    flops_fwd = 4.0 * D * Hq * pairs
-    flops_step = flops_fwd * 3.5
-    q, k, v, do = W.make_tensors(T, Hq, Hkv, D, dtype, args.workload)
-    dev = torch.device("cuda", local)
-    Q, K, V, dO = (x.to(dev) for x in (q, k, v, do))
-    O = torch.empty_like(Q)
-    LSE = torch.empty(Hq, T, dtype=torch.float32, device=dev)
-    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    ws = torch.empty(pt.bwd_workspace_bytes(T, Hq, D), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    draft = hasattr(st, "anchors")
-    if draft:
-        host_layout = [a for a in (st.anchors, st.block_keep, st.ctx_doc, st.anchor_doc) if a is not None]
-        make_map = lambda: pt.build_blockmap_draft(**st.kwargs())
-    else:
-        nl, pp, pn = st.node_lengths, st.path_ptr, st.path_nodes
-        host_layout = [nl, pp, pn]
-        make_map = lambda: pt.build_blockmap_tree(nl, pp, pn, 128, 128)
-    stream = torch.cuda.current_stream()
-
-    def step(dense=False):
-        bm = make_map()
-        if dense:
-            d = bm.dense()
-            bm.free()
-            bm = d
-        pt.attn_fwd(Q, K, V, bm, O=O, LSE=LSE)
-        pt.attn_bwd(dO, Q, K, V, O, LSE, bm, dQ=dQ, dK=dK, dV=dV, workspace=ws)
-        bm.free()
-
-    for _ in range(args.warmup):
-        step()
-    pt.sync_status()
-
-    def timed(n, fn):
-        evs = []
-        for _ in range(n):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            evs.append((a, b))
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
-
-    # ---- device-resident timed region ---------------------------------------
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=torch.device("cuda", local))
     sampler = ClockSampler(local)
     sampler.start()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches0 = pt.launch_count()
-    pt.profile_reset()
-    # the step time: no events inside the step (an event between two kernels
-    # costs the launch overlap, about 3 us per boundary)
-    times = timed(args.steps, step)
-    launches = pt.launch_count() - launches0
-    torch.cuda.synchronize()
-    # per-kernel durations: the same K steps again, each kernel bracketed by
-    # CUDA events on its stream
-    pt.profile_enable(True)
-    timed(args.steps, step)
-    pt.profile_enable(False)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
+    res = measure_device(args.workload, args.steps, args.warmup, not args.no_dense, flush, dist, local, world)
+    ctx = res.pop("_ctx")
+    # the other workloads of the set, in the same run: the same measurement
+    # (fewer steps), each with its own inputs and map
+    others = {}
+    if args.all_workloads and args.workload == 2:
+        for c in (3, 4, 5, 6, 7):
+            n = max(3, min(args.steps, 20)) if c != 7 else 3
+            r = measure_device(c, n, 3, c != 7 and not args.no_dense, flush, dist, local, world)
+            r.pop("_ctx")
+            others[str(c)] = r
+            torch.cuda.empty_cache()
     clocks = sampler.stop()
-    pt.sync_status()
-    total_ms = max_over_ranks(sum(times), dist, dev)
-    ms_step = total_ms / args.steps
-    value = whole_job_tflops(world, flops_step, args.steps, total_ms)
-
-    kernels = {}
-    for name in ("blockmap_classify", "blockmap_lists", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv", "bwd_dkdv_finalize", "bwd_dv",
-                 "bwd_dk", "bwd_dq", "bwd_simt"):
-        n, ms = pt.profile_read(name)
-        if n:
-            kernels[name] = {"launches": n, "ms_per_launch": ms / n}
-    pt.profile_reset()
-
-    # ---- roofline of the dominant kernel -----------------------------------
+    Q, K, V, dO, q, k, v, do = ctx["tensors"]
+    dQ, dK, dV = ctx["grads"]
+    make_map, host_layout, stream, timed = ctx["make_map"], ctx["host_layout"], ctx["stream"], ctx["timed"]
+    Hq, Hkv, D, dtype = cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["dtype"]
+    T = st.T
+    draft = hasattr(st, "anchors")
+    flops_step = res["useful_tflop_per_step"] * 1e12
+    ms_step = res["ms_per_step"]
+    value = res["value"]
     peak_tf, peak_gbs, peak_src = peaks()
-    per_launch_flops = {  # useful-pair flops of each kernel: 2D per pair and head for each of its products
-        "fwd_tc": 4.0 * D * Hq * pairs,
-        "bwd_dkdv": 8.0 * D * Hq * pairs,
-        "bwd_dv": 4.0 * D * Hq * pairs,  # head_dim 256: S^T and dV
-        "bwd_dk": 6.0 * D * Hq * pairs,  # head_dim 256: S^T, dP^T and dK
-        "bwd_dq": 6.0 * D * Hq * pairs,
-        # CUDA-core kernels (fp32 inputs, head dims without a tensor-core path): useful flops
-        "fwd_simt": 4.0 * D * Hq * pairs,
-        "bwd_simt": 10.0 * D * Hq * pairs,
-    }
-    tc = {k: v for k, v in kernels.items() if k in per_launch_flops}
-    roofline = None
-    if tc:
-        dom = max(tc, key=lambda k: tc[k]["ms_per_launch"])
-        ach = per_launch_flops[dom] / (tc[dom]["ms_per_launch"] * 1e-3) / 1e12
-        if dom.endswith("_simt"):  # fp32 FMA pipes: SMs x 128 lanes x 2 flop x max SM clock
-            fp32_peak = FP32_LANES_PER_SM * num_sms() * 2 * SM_MAX_GHZ / 1e3
-            roofline = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
-                        "frac": ach / fp32_peak, "traffic": None,
-                        "peak_source": f"derived: {num_sms()} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 flop x "
-                                       f"{SM_MAX_GHZ} GHz"}
-        else:
-            roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
-                        "frac": ach / peak_tf, "traffic": MEASURED_TRAFFIC.get((args.workload, dom)),
-                        "peak_source": f"{peak_src} bf16 burst"}
-
-    # ---- dense-masked comparison (same kernels, every tile partial) ---------
-    dense = None
-    if not args.no_dense:
-        step(dense=True)
-        dt = timed(max(2, min(5, args.steps)), lambda: step(dense=True))
-        dense = {"ms_per_step": sum(dt) / len(dt), "speedup": (sum(dt) / len(dt)) / ms_step}
+    dev = torch.device("cuda", local)
+    if not draft:
+        nl, pp, pn = st.node_lengths, st.path_ptr, st.path_nodes
 
     # ---- secondary context: torch SDPA over a dense [T, T] boolean mask ------
     # (the pre-block-sparse path the drafter PR replaced).  The mask is
@@ -585,15 +642,18 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-            "frac_of_peak": value / world / peak_tf,
+            "frac_of_peak": res["frac_of_peak"], "fwd": res["fwd"], "bwd": res["bwd"],
             "config": {"workload": cfg["name"], "T": T, "Hq": Hq, "Hkv": Hkv, "head_dim": D,
-                       "useful_pairs_per_head": pairs, "useful_tflop_per_step": flops_step / 1e12,
+                       "useful_pairs_per_head": res["useful_pairs_per_head"],
+                       "useful_tflop_per_step": flops_step / 1e12,
                        "tiles": "128x128", "l2": "flushed before every step (256 MB write, untimed)",
                        "parallelism": f"replicas x{world}"},
-            "kernels": kernels, "kernel_timing": "second pass of the same steps with an event pair per kernel",
-            "roofline": roofline, "dense_masked": dense, "sdpa_dense_mask": sdpa, "e2e": e2e,
-            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu, "fold": fold,
+            "kernels": res["kernels"], "kernel_timing": "second pass of the same steps with an event pair per kernel",
+            "roofline": res["roofline"], "dense_masked": res["dense_masked"], "sdpa_dense_mask": sdpa, "e2e": e2e,
+            "gpu_launches": res["gpu_launches"], "clocks": clocks, "cpu_baseline": cpu, "fold": fold,
         }
+        if others:
+            line["workloads"] = others
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
