@@ -88,6 +88,14 @@ typedef struct pt_blockmap pt_blockmap;
  *   build synchronises the stream once before returning.
  * out: receives the new map.
  *
+ * With 128 x 128 tiles the host derives the q-major lists from the node
+ * intervals and the device classifies the listed tiles.  The device also
+ * sums the kept pairs it finds over the listed tiles and compares the sum
+ * with the tree's kept-pair count in closed form (each node's causal
+ * triangle plus its tokens times its ancestors' tokens): a listed tile that
+ * keeps nothing, or a non-empty tile missing from the lists, records a device
+ * error that the next pt_sync_status returns as PT_ERR_INVALID_ARG.
+ *
  * Errors: PT_ERR_INVALID_ARG when a length is negative, a path is empty or
  * names a node out of range, a parent does not have a smaller id than its
  * child, two paths disagree on a parent, a path does not start at a root, or
@@ -410,8 +418,10 @@ pt_status pt_fold_mismatches(const pt_foldplan* plan, const void* roll, int64_t 
                              cudaStream_t stream);
 
 /* Synchronise the stream, then return and clear the device status word:
- * PT_ERR_TIMEOUT if an in-kernel wait ran out since the last check, PT_ERR_CUDA
- * if the stream reported an error, else PT_OK. */
+ * PT_ERR_TIMEOUT if an in-kernel wait ran out since the last check,
+ * PT_ERR_INVALID_ARG if a device-side check of a block map failed (see
+ * pt_build_blockmap_tree and pt_build_blockmap_seg), PT_ERR_CUDA if the
+ * stream reported an error, else PT_OK. */
 pt_status pt_sync_status(cudaStream_t stream);
 
 /* Message for the last failing call on this thread ("" if none). */
@@ -440,6 +450,14 @@ pt_status pt_debug_wait_timeout(cudaStream_t stream);
  * map or a bad head layout and PT_ERR_UNSUPPORTED for head_dim above 512, as
  * pt_attn_bwd does.  The pages have no counterpart. */
 pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv, int32_t D, cudaStream_t stream);
+
+/* Test hook for the device-side check of host-built lists: the next n
+ * pt_build_blockmap_tree calls with 128 x 128 tiles each drop one non-empty
+ * tile (the last entry of the longest q-tile list) from the lists the host
+ * builds, keeping lengths and offsets consistent, so that only the kept-pair
+ * check can notice; n <= 0 cancels.  For tests only: the maps it makes are
+ * wrong.  The pages have no counterpart. */
+void pt_debug_drop_listed_tile(int32_t n);
 
 /* Bytes of the library's private device memory pool on `device`: handed out
  * now (*used_bytes) and held from the device (*reserved_bytes).  The pool is

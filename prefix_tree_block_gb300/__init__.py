@@ -99,6 +99,8 @@ def load_library(path: Optional[str] = None):
         lib.pt_launch_count.restype = ctypes.c_uint64
         lib.pt_bwd_noalloc_max_scratch_bytes.argtypes = []
         lib.pt_bwd_noalloc_max_scratch_bytes.restype = sz
+        lib.pt_debug_drop_listed_tile.argtypes = [i32]
+        lib.pt_debug_drop_listed_tile.restype = None
         lib.pt_profile_enable.argtypes = [ctypes.c_int]
         lib.pt_profile_enable.restype = None
         lib.pt_profile_read.argtypes = [ctypes.c_char_p, i64p, ctypes.POINTER(ctypes.c_double)]

@@ -405,6 +405,11 @@ pt_status pt_sync_status(cudaStream_t stream) {
     set_error("a bounded in-kernel wait ran out");
     return PT_ERR_TIMEOUT;
   }
+  if (worst == PT_STATUS_INVALID) {
+    set_error("a device-side check of a block map's lists or labels failed (a listed tile that keeps nothing, "
+              "kept pairs missing from the lists, or more partial tiles than the lists' bound)");
+    return PT_ERR_INVALID_ARG;
+  }
   if (worst) {
     set_error("device status %d", worst);
     return PT_ERR_CUDA;
@@ -429,6 +434,8 @@ pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv
   }
   return as_status(pt::prepare_bwd_noalloc(bm, Hq, Hkv, D, stream));
 }
+
+void pt_debug_drop_listed_tile(int32_t n) { pt::debug_drop_listed_tiles(n); }
 
 pt_status pt_debug_pool_usage(int32_t device, uint64_t* used_bytes, uint64_t* reserved_bytes) {
   if (!used_bytes || !reserved_bytes || device < 0) {

@@ -9,6 +9,7 @@
 // a kv range [k0, k1), the overlap with each proper ancestor node's tokens plus
 // the overlap with [start(node(q)), q].
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdio>
 #include <cstring>
@@ -368,6 +369,9 @@ __global__ void k_tree_listed(int T, int tpad, int N, int* __restrict__ map_tabs
       const bool in_range = q0 + 128 <= T && k1 <= T;
       const bool full = in_range && kept == 128LL * 128;
       if (kept == 0) record_status(PT_STATUS_INVALID);
+      // the kept pairs of every listed tile add up to all kept pairs of the
+      // tree only if no non-empty tile is missing from the host's lists
+      atomicAdd(reinterpret_cast<unsigned long long*>(counters + 2), (unsigned long long)kept);
       const int et = s_et[e];
       if (full) {
         kind[e] = kindT[et] = PT_KIND_FULL;
@@ -572,8 +576,13 @@ __device__ __forceinline__ void tile_masks(int T, const pt_tok* tok, const int2*
 // when that is >= 0, else nnz - n_full read on the device (at most p_cap).
 __global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols,
                         long long n_known, const int* nnz_total, const int* n_full, long long p_cap,
-                        int* host_counters = nullptr) {
+                        int* host_counters = nullptr, long long expect_pairs = -1) {
   pdl_wait();  // launched with programmatic dependent launch
+  // host-built lists: the kept pairs the classification found over the listed
+  // tiles (n_full[2..3], one 64-bit sum) must be every kept pair of the tree
+  if (expect_pairs >= 0 && blockIdx.x == 0 && threadIdx.x == 0 &&
+      *reinterpret_cast<const unsigned long long*>(n_full + 2) != (unsigned long long)expect_pairs)
+    record_status(PT_STATUS_INVALID);
   __shared__ pt_tok tq[128], tk[128];
   __shared__ uint32_t kstart[4], qstart[4];
   // the full-tile count to the host's mapped staging (host-built lists)
@@ -768,6 +777,10 @@ int stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s) {
   return 0;
 }
 
+// Test hook: the next n tree builds with host-built lists drop one listed
+// tile (pt_debug_drop_listed_tile).
+std::atomic<int> g_drop_listed_tiles{0};
+
 // ---------------------------------------------------------------------------
 // host side: memory
 // ---------------------------------------------------------------------------
@@ -815,6 +828,8 @@ int pool_alloc(void** p, size_t bytes, int dev, cudaStream_t s) {
 void pool_free(void* p, cudaStream_t s) {
   if (p) cudaFreeAsync(p, s);
 }
+
+void debug_drop_listed_tiles(int n) { g_drop_listed_tiles.store(n > 0 ? n : 0); }
 
 int pool_usage(int dev, uint64_t* used, uint64_t* reserved) {
   *used = *reserved = 0;
@@ -1228,7 +1243,22 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
     }
     return finish_map(bm, s, p_bound);
   }
-  // packed: counters[4] | node tables[5N] | q_ptr | k_ptr | q_order | k_order | kv_idx | q_idx | eT
+  // every kept pair of the tree, in closed form: each node's causal triangle
+  // plus its tokens times the tokens of its ancestors
+  long long expect_pairs = 0;
+  {
+    const int* start = tab;
+    const int* end = tab + N;
+    const int* parent = tab + 2 * (size_t)N;
+    std::vector<long long> anc(N, 0);  // tokens of the ancestors (parents have smaller ids)
+    for (int n = 0; n < N; ++n) {
+      const long long len = end[n] - start[n];
+      if (parent[n] >= 0) anc[n] = anc[parent[n]] + (end[parent[n]] - start[parent[n]]);
+      expect_pairs += len * (len + 1) / 2 + len * anc[n];
+    }
+  }
+  // packed: counters[4] (full tiles, partial tiles, the 64-bit kept-pair sum)
+  //   | node tables[5N] | q_ptr | k_ptr | q_order | k_order | kv_idx | q_idx | eT
   const size_t n_pk = 4 + 5 * (size_t)N + (size_t)(nq + 1) + (nk + 1) + nq + nk + 3 * (size_t)nnz;
   std::vector<int> pk(n_pk, 0);
   std::copy(tab, tab + 5 * (size_t)N, pk.data() + 4);
@@ -1289,7 +1319,8 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
       ProfScope ps(s, "blockmap_lists");  // the partial tiles' masks
       const long long grid = std::max<long long>(1, std::min<long long>(p_alloc, (long long)num_sms(dev) * 16));
       launch_pdl(k_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, bm->tok, slot_tile, bm->mask_rows,
-                 bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap, static_cast<int*>(sl.dev));
+                 bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap, static_cast<int*>(sl.dev),
+                 expect_pairs);
       PT_LAUNCHED(1);
       if (cudaEventRecord(sl.ev, s) != cudaSuccess) {
         rc = 3;
@@ -1536,6 +1567,20 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
       }
       std::sort(row_kv.begin() + (long)row0, row_kv.end());
     }
+  }
+  if (BM == 128 && BN == 128 && !row_kv.empty() && g_drop_listed_tiles.load() > 0 &&
+      g_drop_listed_tiles.fetch_sub(1) > 0) {
+    // test hook (pt_debug_drop_listed_tile): the last entry of the longest q
+    // list leaves the host's lists, consistently (lengths and offsets)
+    int i_max = 0;
+    for (int i = 1; i < nq_h; ++i)
+      if (pred[(size_t)i] > pred[(size_t)i_max]) i_max = i;
+    size_t pos = 0;
+    for (int i = 0; i <= i_max; ++i) pos += (size_t)pred[(size_t)i];
+    const int j = row_kv[pos - 1];
+    row_kv.erase(row_kv.begin() + (long)(pos - 1));
+    --pred[(size_t)i_max];
+    --pred[(size_t)nq_h + j];
   }
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, N, s, &bm);

@@ -161,6 +161,8 @@ inline bool masks_missing(const pt_blockmap* bm) {
 // staging for small host-to-device uploads (pt_blockmap.cu).
 int pool_alloc(void** p, size_t bytes, int dev, cudaStream_t s);
 void pool_free(void* p, cudaStream_t s);
+// Test hook: the next n tree builds with host-built lists each drop one tile.
+void debug_drop_listed_tiles(int n);
 // Bytes of the pool on `dev` handed out now and held from the device.
 int pool_usage(int dev, uint64_t* used, uint64_t* reserved);
 int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s);

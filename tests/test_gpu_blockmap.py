@@ -136,3 +136,28 @@ def test_empty_layout_attention_and_host_lists():
     pt.sync_status()
     st = W.tree_structure([0, 0, 130, 0, 300], [[0, 1], [0, 2], [0, 3, 4]])
     compare_blockmap(gpu_blockmap(st).export(), orc.blockmap(orc.structure_labels(st), 128, 128))
+
+
+@pytest.mark.parametrize("c", [2, 4])
+def test_tile_missing_from_host_lists_is_caught_on_device(c):
+    """For a tree at 128 x 128 tiles the host builds the lists and the device
+    only classifies the listed tiles.  The device sums the kept pairs over
+    them and checks the sum against the tree's closed-form count, so a
+    non-empty tile dropped from the host's lists (the test hook drops one)
+    shows up as PT_ERR_INVALID_ARG at the next sync; the next build is clean."""
+    lib = pt.load_library()
+    st = W.config_structure(c)
+    lib.pt_debug_drop_listed_tile(1)
+    try:
+        bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes, 128, 128)
+        with pytest.raises(pt.PTError) as ei:
+            pt.sync_status()
+        assert ei.value.status == pt.PT_ERR_INVALID_ARG
+        assert bm.nnz == orc.blockmap(orc.structure_labels(st), 128, 128)["nnz"] - 1
+        bm.free()
+    finally:
+        lib.pt_debug_drop_listed_tile(0)
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes, 128, 128)
+    pt.sync_status()
+    compare_blockmap(bm.export(), orc.blockmap(orc.structure_labels(st), 128, 128))
+    bm.free()
