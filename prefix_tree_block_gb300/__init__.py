@@ -31,6 +31,24 @@ _STATUS_NAMES = {0: "PT_OK", 1: "PT_ERR_INVALID_ARG", 2: "PT_ERR_UNSUPPORTED", 3
 
 _lib = None
 _lock = threading.Lock()
+_alloc_hook = None
+
+
+def set_output_allocator(fn=None):
+    """Route the binding's device output allocations (O, LSE, gradients,
+    workspaces, fold outputs) through fn(shape, dtype, device) -> tensor, or
+    back to torch.empty with None.  Tests use it to surround every output
+    with guard bands."""
+    global _alloc_hook
+    _alloc_hook = fn
+
+
+def _empty(shape, dtype, device):
+    import torch
+
+    if _alloc_hook is not None:
+        return _alloc_hook(tuple(shape), dtype, device)
+    return torch.empty(tuple(shape), dtype=dtype, device=device)
 
 
 class PTError(RuntimeError):
@@ -299,9 +317,9 @@ def attn_fwd(Q, K, V, bm: BlockMap, scale: float = 0.0, O=None, LSE=None, stream
     T, Hq, D = Q.shape
     Hkv = K.shape[1]
     if O is None:
-        O = torch.empty_like(Q)
+        O = _empty(Q.shape, Q.dtype, Q.device)
     if LSE is None:
-        LSE = torch.empty(Hq, T, dtype=torch.float32, device=Q.device)
+        LSE = _empty((Hq, T), torch.float32, Q.device)
     lib = load_library()
     _check(lib.pt_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _dtype_code(Q), T, Hq, Hkv, D, float(scale), bm.handle,
                            _ptr(O), _ptr(LSE), ctypes.c_void_p(_stream(stream))))
@@ -320,12 +338,12 @@ def attn_bwd(dO, Q, K, V, O, LSE, bm: BlockMap, scale: float = 0.0, dQ=None, dK=
     _check_tensors(dO, Q, K, V, O)
     T, Hq, D = Q.shape
     Hkv = K.shape[1]
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
+    dQ = _empty(Q.shape, Q.dtype, Q.device) if dQ is None else dQ
+    dK = _empty(K.shape, K.dtype, K.device) if dK is None else dK
+    dV = _empty(V.shape, V.dtype, V.device) if dV is None else dV
     need = bwd_workspace_bytes(T, Hq, D)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+        workspace = _empty((need,), torch.uint8, Q.device)
     lib = load_library()
     _check(lib.pt_attn_bwd(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _dtype_code(Q), T, Hq, Hkv, D,
                            float(scale), bm.handle, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
@@ -343,9 +361,9 @@ def attn_bwd_noalloc(dO, Q, K, V, O, LSE, bm: BlockMap, scale: float = 0.0, dQ=N
     _check_tensors(dO, Q, K, V, O)
     T, Hq, D = Q.shape
     Hkv = K.shape[1]
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
+    dQ = _empty(Q.shape, Q.dtype, Q.device) if dQ is None else dQ
+    dK = _empty(K.shape, K.dtype, K.device) if dK is None else dK
+    dV = _empty(V.shape, V.dtype, V.device) if dV is None else dV
     lib = load_library()
     _check(lib.pt_attn_bwd_noalloc(_ptr(dO), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _dtype_code(Q), T, Hq,
                                    Hkv, D, float(scale), bm.handle, _ptr(dQ), _ptr(dK), _ptr(dV),
@@ -365,7 +383,7 @@ def debug_exp2(x, method: int):
 
     if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous float32 CUDA tensor")
-    y = torch.empty_like(x)
+    y = _empty(x.shape, x.dtype, x.device)
     _check(load_library().pt_debug_exp2(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), x.numel(),
                                         method, ctypes.c_void_p(_stream(None))))
     return y
@@ -487,8 +505,7 @@ class FoldPlan:
 
         self._need(roll, (self.n_samples, self.row_len), "roll")
         rb = self._row_bytes(roll, 2)
-        out = torch.empty((self.T,) + tuple(roll.shape[2:]), dtype=roll.dtype, device=roll.device) \
-            if out is None else out
+        out = _empty((self.T,) + tuple(roll.shape[2:]), roll.dtype, roll.device) if out is None else out
         _check(self._lib.pt_fold(self._h, _ptr(roll), rb, _ptr(out), ctypes.c_void_p(_stream(stream))))
         return out
 
@@ -498,8 +515,8 @@ class FoldPlan:
 
         self._need(flat, (self.T,), "flat")
         rb = self._row_bytes(flat, 1)
-        out = torch.empty((self.n_samples, self.row_len) + tuple(flat.shape[1:]), dtype=flat.dtype,
-                          device=flat.device) if out is None else out
+        out = _empty((self.n_samples, self.row_len) + tuple(flat.shape[1:]), flat.dtype, flat.device) \
+            if out is None else out
         _check(self._lib.pt_unfold(self._h, _ptr(flat), rb, _ptr(out), ctypes.c_void_p(_stream(stream))))
         return out
 
@@ -511,8 +528,7 @@ class FoldPlan:
         width = 1
         for d in droll.shape[2:]:
             width *= d
-        out = torch.empty((self.T,) + tuple(droll.shape[2:]), dtype=droll.dtype, device=droll.device) \
-            if out is None else out
+        out = _empty((self.T,) + tuple(droll.shape[2:]), droll.dtype, droll.device) if out is None else out
         _check(self._lib.pt_unfold_grad(self._h, _ptr(droll), _dtype_code(droll), width, _ptr(out),
                                         ctypes.c_void_p(_stream(stream))))
         return out
@@ -521,7 +537,7 @@ class FoldPlan:
         """Position ids of the flat tokens (int64 [T])."""
         import torch
 
-        out = torch.empty(self.T, dtype=torch.int64, device=device or torch.device("cuda"))
+        out = _empty((self.T,), torch.int64, device or torch.device("cuda"))
         _check(self._lib.pt_fold_positions(self._h, _ptr(out), ctypes.c_void_p(_stream(stream))))
         return out
 
@@ -530,7 +546,7 @@ class FoldPlan:
         import torch
 
         self._need(roll, (self.n_samples, self.row_len), "roll")
-        cnt = torch.empty(1, dtype=torch.int64, device=roll.device)
+        cnt = _empty((1,), torch.int64, roll.device)
         _check(self._lib.pt_fold_mismatches(self._h, _ptr(roll), self._row_bytes(roll, 2), _ptr(cnt),
                                             ctypes.c_void_p(_stream(stream))))
         return int(cnt.item())

@@ -36,7 +36,7 @@ def lib():
 def _noalloc(lib, dO, Q, K, V, O, LSE, bm, dtype_code, expect=pt.PT_OK):
     T, Hq, D = Q.shape
     Hkv = K.shape[1]
-    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    dQ, dK, dV = (pt._empty(x.shape, x.dtype, x.device) for x in (Q, K, V))  # guarded in the tests
     rc = lib.pt_attn_bwd_noalloc(dO.data_ptr(), Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
                                  LSE.data_ptr(), dtype_code, T, Hq, Hkv, D, 0.0, bm.handle, dQ.data_ptr(),
                                  dK.data_ptr(), dV.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
