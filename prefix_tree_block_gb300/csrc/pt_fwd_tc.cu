@@ -15,12 +15,18 @@
 //                   listed kv block through separate multi-stage rings
 //                   (128-byte swizzled 64-column panels); with V, the tile's
 //                   keep mask (partial tiles) and its slot id.
-//   MMA warp        one lane issues tcgen05.mma: S_h = Q_h K^T into TMEM
+//   MMA warp(s)     one lane issues tcgen05.mma: S_h = Q_h K^T into TMEM
 //                   (M = 128 q rows, N = 128 kv, K = D) and O_h += P_h V with
 //                   P_h read from TMEM (M = 128, N = D, K = 128).  With two
 //                   heads, head A's MMAs run while head B's softmax works and
 //                   vice versa; with one head, S is double-buffered and S of
-//                   block j+1 is issued before PV of block j.
+//                   block j+1 is issued before PV of block j.  At head_dim 64
+//                   (P in its own columns) one warp issues the S products and
+//                   a second warp the PV products: the tensor pipe runs one
+//                   thread's MMAs into one accumulator after another with its
+//                   latency (about 300 cycles) between chains, and short
+//                   chains (4 and 8 MMAs) are all this head dim has, so two
+//                   issuing threads keep it busy where one cannot.
 //   softmax         load the S row from TMEM, clear masked entries, keep the
 //                   running max and sum in base 2 with the scale folded in,
 //                   write P as bf16 over the S columns, and rescale O in TMEM
@@ -71,14 +77,18 @@ struct FwdCfg {
   static constexpr int OFF_BAR = OFF_META + 16 * ((VS * 4 + 15) / 16);
   // q_full[QB] q_empty[QB] k_full[KS] k_empty[KS] v_full[VS] v_empty[VS]
   // s_full[NH*SB] p_full[NH*SB] o_full[NH] o_free[NH] mma_done
-  // (OVL) s_free[NH] p_free[NH] o_written[NH]
-  static constexpr int NBAR = 2 * QB + 2 * KS + 2 * VS + 2 * NH * SB + 2 * NH + 1 + (OVL ? 3 * NH : 0);
+  // (OVL) s_free[NH] p_free[NH] o_written[NH] mma_done2
+  static constexpr int NBAR = 2 * QB + 2 * KS + 2 * VS + 2 * NH * SB + 2 * NH + 1 + (OVL ? 3 * NH + 1 : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TM_S = 0;                            // S(h, b) at (h * SB + b) * 128
   static constexpr int TM_P = NH * SB * 128;                // (OVL) packed P(h) at TM_P + h * 64
   static constexpr int TM_O = TM_P + (OVL ? NH * 64 : 0);  // O(h) at TM_O + h * D
-  static constexpr int THREADS = NH * 128 + 64;
+  // softmax warpgroups, the producer warp and the MMA warp; with OVL a
+  // second MMA warp: one issues the S products, the other the PV products,
+  // so the tensor pipe overlaps their chains (one thread's MMAs into one
+  // accumulator after another run with the pipe's latency between chains)
+  static constexpr int THREADS = NH * 128 + (OVL ? 96 : 64);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TM_O + NH * D <= 512, "TMEM budget");
 };
@@ -150,13 +160,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   uint64_t* s_free = mma_done + 1;          // [NH] (OVL) S(h) loaded by the softmax
   uint64_t* p_free = s_free + NH;           // [NH] (OVL) PV(h) done reading P(h)
   uint64_t* o_written = p_free + NH;        // [NH] (OVL) the warpgroup's O rows are in shared memory
+  uint64_t* mma_done2 = o_written + NH;     // (OVL) the PV warp's MMAs are complete
   int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = fwd_items<NH>(p.nq, p.Hq, p.Hkv);
-  constexpr int PRODUCER = NH * 4, ISSUER = NH * 4 + 1;
+  constexpr int PRODUCER = NH * 4, ISSUER = NH * 4 + 1, ISSUER_PV = NH * 4 + 2;
 
   if (threadIdx.x == PRODUCER * 32) {
     for (int b = 0; b < C::QB; ++b) {
@@ -165,12 +176,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       // frees it; else the item's last S MMA does
       mbar_init(q_empty + b, C::OVL ? NH : 1);
     }
-    if (C::OVL)
+    if (C::OVL) {
       for (int h = 0; h < NH; ++h) {
         mbar_init(s_free + h, 128);
         mbar_init(p_free + h, 1);
         mbar_init(o_written + h, 128);
       }
+      mbar_init(mma_done2, 1);
+    }
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -322,40 +335,31 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         tc_fence_after();
         for (int jj = 0; jj <= n && ok; ++jj) {
           const uint32_t ks = (kc + jj) % C::KS;
-          if (jj < n) {
+          if (jj < n && !C::OVL) {  // (OVL: tested with the group's other barriers)
             if (!(ok = mbar_wait(k_full + ks, ((kc + jj) / C::KS) & 1, abort_flag))) break;
             tc_fence_after();
           }
           if constexpr (C::OVL) {
-            // S of block jj for every head, each as soon as the softmax has
-            // loaded the head's previous S; then PV of block jj-1 as the P
-            // tiles arrive
+            // S of block jj for every head once K(jj) is in and the softmax
+            // has loaded each head's previous S, the barriers tested together
+            // and the heads' MMAs issued back to back.
             if (jj < n) {
-              for (int h = 0; h < nh && ok; ++h) {
+              uint64_t* bars[1 + NH];
+              uint32_t par[1 + NH];
+              bars[0] = k_full + ks;
+              par[0] = ((kc + jj) / C::KS) & 1;
+#pragma unroll
+              for (int h = 0; h < NH; ++h) {
                 const uint32_t u = sc[h] + jj;
-                if (u >= 1 && !(ok = mbar_wait(s_free + h, (u - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                issue_s(h, u, ks);
+                bars[1 + h] = (h < nh && u >= 1) ? s_free + h : nullptr;
+                par[1 + h] = (u - 1) & 1;
               }
-              if (!ok) break;
+              if (!(ok = mbar_wait_all<1 + NH>(bars, par, abort_flag))) break;
+              tc_fence_after();
+              for (int h = 0; h < nh; ++h) issue_s(h, sc[h] + jj, ks);
               mma_commit(k_empty + ks);  // (OVL: the Q buffer is freed by the epilogue's O store)
             }
-            if (jj >= 1) {
-              const int i = jj - 1;
-              const uint32_t vs = (vc + i) % C::VS;
-              if (!(ok = mbar_wait(v_full + vs, ((vc + i) / C::VS) & 1, abort_flag))) break;
-              for (int h = 0; h < nh && ok; ++h) {
-                const uint32_t u = sc[h] + i;
-                if (!(ok = mbar_wait(p_full + h, u & 1, abort_flag))) break;
-                if (i == 0 && itv[h] > 0 && !(ok = mbar_wait(o_free + h, (itv[h] - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                issue_pv(h, u, vs, i == 0);
-                mma_commit(p_free + h);
-                if (i == n - 1) mma_commit(o_full + h);
-              }
-              if (!ok) break;
-              mma_commit(v_empty + vs);
-            }
+            // (the PV products of this item: the PV warp)
           } else if (NH == 1) {
             if (jj < n) {
               issue_s(0, sc[0] + jj, ks);
@@ -408,6 +412,57 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       }
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else if (C::OVL && warp == ISSUER_PV) {
+    // ------------------------------------------------------------ PV issuer (OVL)
+    // PV of block i for every head of the item once V(i) and that head's P
+    // tile are in (and, on the item's first block, the epilogue has read
+    // the previous item's O); each head's MMAs go out as soon as its own
+    // barriers are complete.
+    if (lane == 0) {
+      constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      uint32_t vc = 0;
+      uint32_t sc[NH], itv[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) sc[h] = itv[h] = 0;
+      bool ok = true;
+      for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
+        const int w = snake_item(rr, blockIdx.x, gridDim.x);
+        if (w >= n_items) continue;
+        int tile, h0, nh;
+        decode_item<NH>(p, w, tile, h0, nh);
+        const int n = p.q_ptr[tile + 1] - p.q_ptr[tile];
+        if (n == 0) continue;
+        for (int i = 0; i < n && ok; ++i) {
+          const uint32_t vs = (vc + i) % C::VS;
+          if (!(ok = mbar_wait(v_full + vs, ((vc + i) / C::VS) & 1, abort_flag))) break;
+          for (int h = 0; h < nh && ok; ++h) {
+            const uint32_t u = sc[h] + i;
+            uint64_t* bars[2] = {p_full + h, (i == 0 && itv[h] > 0) ? o_free + h : nullptr};
+            const uint32_t par[2] = {u & 1, (itv[h] - 1) & 1};
+            if (!(ok = mbar_wait_all<2>(bars, par, abort_flag))) break;
+            tc_fence_after();
+            // P(h) in its own TMEM columns
+#pragma unroll
+            for (int kk = 0; kk < C::BN / 16; ++kk)
+              mma_ts(tbase + C::TM_O + h * D, tbase + C::TM_P + h * 64 + kk * 8,
+                     sdesc_sw128(sV + vs * C::TILE + kk * 2048, C::PANEL, 1024), IDESC_PV, (i > 0 || kk > 0));
+            mma_commit(p_free + h);
+            if (i == n - 1) mma_commit(o_full + h);
+          }
+          if (!ok) break;
+          mma_commit(v_empty + vs);
+        }
+        vc += n;
+        for (int h = 0; h < nh; ++h) {
+          sc[h] += n;
+          itv[h] += 1;
+        }
+      }
+      mma_commit(mma_done2);
+      mbar_wait_drain(mma_done2, 0, 200000000);
     }
     __syncwarp();
   } else {
