@@ -125,6 +125,14 @@ struct BwdCfg {
   // as S^T, dK of the previous step, dP^T, dV: P^T is computed while the
   // tensor core works through the two middle products.
   static constexpr bool DQ_OVL = true, DKDV_OVL = (D == 64);
+  // At head_dim 64 the products come in short chains (S and dP: 4 MMAs, the
+  // accumulating products: 8), and the tensor pipe leaves its latency (about
+  // 300 cycles) between one thread's chains into different accumulators.
+  // There a second MMA warp issues the accumulating products (dV and dK, or
+  // dQ) while the first issues S and dP (or S^T and dP^T): the pipe
+  // overlaps the two threads' chains.
+  static constexpr bool TWO_ISSUERS = (D == 64);
+  static constexpr int THREADS = TWO_ISSUERS ? 352 : 320;
   static constexpr int TM_DQ_DS = 256 + D;                    // dq: packed dS
   static constexpr int TM_KV_P = 256 + 2 * D, TM_KV_DS = 320 + 2 * D;  // dkdv: packed P^T, dS^T
 };
@@ -202,6 +210,7 @@ struct BwdBars {
   uint64_t st_full[S], st_empty[S];
   uint64_t s_full[2], p_full[2];
   uint64_t acc_full, acc_free, mma_done;
+  uint64_t mma_done2;  // the second MMA warp's MMAs are complete (head_dim-64 kernels)
   uint64_t s_free;   // compute warpgroups have loaded S/dP: the MMA may overwrite them
   uint64_t o_written;  // (dq) every compute thread has put its output rows into the staging tile
   uint64_t o_stored;   // (dq) the staging tile's TMA store has read it
@@ -223,6 +232,7 @@ __device__ __forceinline__ void init_bars(BwdBars<S>* b) {
   mbar_init(&b->acc_full, 1);
   mbar_init(&b->acc_free, 256);
   mbar_init(&b->mma_done, 1);
+  mbar_init(&b->mma_done2, 1);
   mbar_init(&b->s_free, 256);
   mbar_init(&b->o_written, 256);
   mbar_init(&b->o_stored, 1);
@@ -250,7 +260,7 @@ struct DkdvL {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     k_bwd_dkdv(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const BwdParams p) {
   pdl_wait();  // launched with programmatic dependent launch
@@ -377,31 +387,20 @@ __global__ void __launch_bounds__(320, 1)
           }
         };
         if constexpr (C::DKDV_OVL) {
-          for (int x = 0; x <= n && ok; ++x) {
-            const uint32_t y = sc + x, s = y % S;  // global step index of this CTA
-            if (x < n) {
-              // S^T(x) as soon as the compute warpgroups have loaded S^T(x-1)
-              if (!(ok = mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag))) break;
-              if (y >= 1 && !(ok = mbar_wait(&B->s_free, (y - 1) & 1, abort_flag))) break;
-              tc_fence_after();
-              const uint32_t st = sST + s * L::ST_BYTES;
-              mma_s(st);
-              mma_dp(st);
-              mma_commit(&B->s_full[0]);
-              if (x == n - 1) mma_commit(&B->res_empty);
-            }
-            if (x >= 1) {
-              // dV, dK of the previous step from the packed region
-              const uint32_t sp = (y - 1) % S;
-              if (!(ok = mbar_wait(&B->p_full[0], (y - 1) & 1, abort_flag))) break;
-              if (x == 1 && it > 0 && !(ok = mbar_wait(&B->acc_free, (it - 1) & 1, abort_flag))) break;
-              tc_fence_after();
-              const uint32_t stp = sST + sp * L::ST_BYTES;
-              mma_acc(C::TM_ACC0, C::TM_KV_P, true, stp + L::ST_DO, x == 1);
-              mma_acc(C::TM_ACC1, C::TM_KV_DS, true, stp + L::ST_Q, x == 1);
-              mma_commit(&B->ps_free);
-              mma_commit(&B->st_empty[sp]);
-            }
+          // S^T(x) and dP^T(x) once the stage is in and the compute
+          // warpgroups have loaded S^T(x-1) and dP^T(x-1); dV and dK are the
+          // second MMA warp's
+          for (int x = 0; x < n && ok; ++x) {
+            const uint32_t y = sc + x, s = y % S;
+            uint64_t* bars[2] = {&B->st_full[s], y >= 1 ? &B->s_free : nullptr};
+            const uint32_t par[2] = {(y / S) & 1, (y - 1) & 1};
+            if (!(ok = mbar_wait_all<2>(bars, par, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t st = sST + s * L::ST_BYTES;
+            mma_s(st);
+            mma_dp(st);
+            mma_commit(&B->s_full[0]);
+            if (x == n - 1) mma_commit(&B->res_empty);
           }
         } else {
           for (int x = 0; x <= n && ok; ++x) {
@@ -433,12 +432,52 @@ __global__ void __launch_bounds__(320, 1)
             }
           }
         }
-        if (ok) mma_commit(&B->acc_full);
+        if (ok && !C::DKDV_OVL) mma_commit(&B->acc_full);  // (OVL: the second MMA warp's)
         sc += n;
         ++it;
       }
       mma_commit(&B->mma_done);
       mbar_wait_drain(&B->mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else if (C::TWO_ISSUERS && warp == 10) {
+    // ------------------------------------------------------------ dV / dK issuer (head_dim 64)
+    if (lane == 0) {
+      constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);
+      const uint32_t sST = smem_u32(smem + L::OFF_ST);
+      uint32_t sc = 0, it = 0;
+      bool ok = true;
+      for (int w = w_begin; w < w_end && ok; ++w) {
+        const DkdvItem itm = p.items[w];
+        const int n = itm.x1 - itm.x0;
+        if (n == 0) continue;
+        for (int x = 0; x < n && ok; ++x) {
+          // dV += P^T dO and dK += dS^T Q of step x, from the packed region,
+          // once the compute warpgroups have written it (and, on an item's
+          // first step, read the previous item's accumulators)
+          const uint32_t y = sc + x, sp = y % S;
+          uint64_t* bars[3] = {&B->st_full[sp], &B->p_full[0], (x == 0 && it > 0) ? &B->acc_free : nullptr};
+          const uint32_t par[3] = {(y / S) & 1, y & 1, (it - 1) & 1};
+          if (!(ok = mbar_wait_all<3>(bars, par, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t stp = sST + sp * L::ST_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tbase + C::TM_ACC0, tbase + C::TM_KV_P + kk * 8, sdesc_sw128(stp + L::ST_DO + kk * 2048, C::PANEL, 1024),
+                   IDESC_ACC, x > 0 || kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tbase + C::TM_ACC1, tbase + C::TM_KV_DS + kk * 8, sdesc_sw128(stp + L::ST_Q + kk * 2048, C::PANEL, 1024),
+                   IDESC_ACC, x > 0 || kk > 0);
+          mma_commit(&B->ps_free);
+          mma_commit(&B->st_empty[sp]);
+        }
+        if (ok) mma_commit(&B->acc_full);
+        sc += n;
+        ++it;
+      }
+      mma_commit(&B->mma_done2);
+      mbar_wait_drain(&B->mma_done2, 0, 200000000);
     }
     __syncwarp();
   } else {
@@ -643,7 +682,7 @@ struct DqL {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     k_bwd_dq(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
              const __grid_constant__ CUtensorMap mdQ, const BwdParams p) {
@@ -768,7 +807,7 @@ __global__ void __launch_bounds__(320, 1)
             mma_commit(&B->s_full[0]);
             if (x == n - 1) mma_commit(&B->res_empty);
           }
-          if (x >= 1) {
+          if (x >= 1 && !C::TWO_ISSUERS) {  // (two issuers: dQ is the second MMA warp's)
             // dQ += dS K for the previous block (K = 128 kv; dS packed in its own region)
             const uint32_t sp = (sc + x - 1) % S;
             if (!(ok = mbar_wait(&B->p_full[0], (y - 1) & 1, abort_flag))) break;
@@ -783,12 +822,48 @@ __global__ void __launch_bounds__(320, 1)
             mma_commit(&B->st_empty[sp]);
           }
         }
-        if (ok) mma_commit(&B->acc_full);
+        if (ok && !C::TWO_ISSUERS) mma_commit(&B->acc_full);
         sc += n;
         ++it;
       }
       mma_commit(&B->mma_done);
       mbar_wait_drain(&B->mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else if (C::TWO_ISSUERS && warp == 10) {
+    // ------------------------------------------------------------ dQ issuer (head_dim 64)
+    if (lane == 0) {
+      constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);
+      const uint32_t sST = smem_u32(smem + L::OFF_ST);
+      uint32_t sc = 0, it = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const int tile = p.order[w / p.Hq];
+        const int n = p.ptr[tile + 1] - p.ptr[tile];
+        if (n == 0) continue;
+        for (int x = 0; x < n && ok; ++x) {
+          // dQ += dS K of block x (K = 128 kv; dS packed in its own region)
+          // once the compute warpgroups have written dS (and, on an item's
+          // first block, read the previous item's dQ)
+          const uint32_t y = sc + x, sp = y % S;
+          uint64_t* bars[3] = {&B->st_full[sp], &B->p_full[0], (x == 0 && it > 0) ? &B->acc_free : nullptr};
+          const uint32_t par[3] = {(y / S) & 1, y & 1, (it - 1) & 1};
+          if (!(ok = mbar_wait_all<3>(bars, par, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t stp = sST + sp * L::ST_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tbase + C::TM_ACC0, tbase + C::TM_DQ_DS + kk * 8, sdesc_sw128(stp + L::ST_K + kk * 2048, C::PANEL, 1024),
+                   IDESC_ACC, (x > 0 || kk > 0));
+          mma_commit(&B->ps_free);
+          mma_commit(&B->st_empty[sp]);
+        }
+        if (ok) mma_commit(&B->acc_full);
+        sc += n;
+        ++it;
+      }
+      mma_commit(&B->mma_done2);
+      mbar_wait_drain(&B->mma_done2, 0, 200000000);
     }
     __syncwarp();
   } else {
@@ -1980,7 +2055,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   int launches = 1;
   if (p.n_items > 0) {
     ProfScope ps(s, "bwd_dkdv");
-    launch_pdl(k_bwd_dkdv<D>, dim3(KL->grid), dim3(320), DkdvL<D>::BYTES, s, mQ, mdO, mK, mV, p);
+    launch_pdl(k_bwd_dkdv<D>, dim3(KL->grid), dim3(BwdCfg<D>::THREADS), DkdvL<D>::BYTES, s, mQ, mdO, mK, mV, p);
     ++launches;
   }
   if (KL->n_splits > 0) {
@@ -2010,7 +2085,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       if (QL->n_items > 0)
         launch_pdl(k_bwd_dq_pipe<D>, dim3(QL->grid), dim3(DqpCfg<D>::THREADS), DqpL<D>::BYTES, s, mQ, mdO, mK, mV, p);
     } else {
-      launch_pdl(k_bwd_dq<D>, dim3(items < sms ? items : sms), dim3(320), DqL<D>::BYTES, s, mQ, mdO, mK, mV, mdQ, p);
+      launch_pdl(k_bwd_dq<D>, dim3(items < sms ? items : sms), dim3(BwdCfg<D>::THREADS), DqL<D>::BYTES, s, mQ, mdO, mK, mV, mdQ, p);
     }
     ++launches;
   }
