@@ -188,8 +188,10 @@ pt_status check_attn(const char* who, pt_dtype dtype, int T, int Hq, int Hkv, in
   return PT_OK;
 }
 
+// bf16 head dims with a tensor-core forward on 128 x 128 maps (the backward
+// has its own list: pt::bwd_tc_supported).
 bool use_tensor_cores(pt_dtype dtype, int D, const pt_blockmap* bm) {
-  return dtype == PT_BF16 && (D == 64 || D == 128 || D == 256) && bm->BM == 128 && bm->BN == 128;
+  return dtype == PT_BF16 && (D == 64 || D == 128 || D == 256 || D == 512) && bm->BM == 128 && bm->BN == 128;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -772,6 +772,431 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
   return 0;
 }
 
+
+// ---------------------------------------------------------------------------
+// head_dim 512 (tensor cores)
+//
+// A 128-row Q tile is 128 KB at this head dim and a 128 x 512 fp32 O
+// accumulator would take all of TMEM, so the kernel keeps the item's Q tile
+// resident in shared memory, streams K and V through a ring of four 16 KB
+// 64-column panels, and runs each item (q tile, q head) as two passes over
+// its kv blocks, one per 256-column half of O:
+//   pass 0  online softmax: S = Q K^T (8 K panels, K = 512), P over S in
+//           TMEM, O[:, 0:256] += P V[:, 0:256] (one N = 256 product from the
+//           four V panels of the half), the running max and sum as in the
+//           other forward kernels;
+//   pass 1  S again, P = exp2(s * scale * log2(e) - m) against the final
+//           reference m of pass 0 (no rescaling), O[:, 256:512] += P V.
+// Each block's 8 K panels and the previous block's 4 V panels are loaded in
+// the order the MMAs consume them (K(j), V(j-1), K(j+1), V(j), ...), so
+// every group is a multiple of four panels and a block's V panels always sit
+// in ring slots 0..3, the contiguous operand an N = 256 MMA reads.  S is
+// double-buffered (2 x 128 TMEM columns) beside the 256-column O half: S of
+// block j+1 is computed while the softmax works on block j.
+// ---------------------------------------------------------------------------
+struct Fwd512Cfg {
+  static constexpr int D = 512, NP = 8, PANEL = 128 * 128;
+  static constexpr int RING = 4;
+  static constexpr int MASKB = 128 * 16;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = OFF_Q + NP * PANEL;
+  static constexpr int OFF_MASK = OFF_RING + RING * PANEL;
+  static constexpr int OFF_META = OFF_MASK + 2 * MASKB;
+  static constexpr int OFF_BAR = OFF_META + 16;
+  // q_full q_empty ring_full[4] ring_empty[4] s_full[2] p_full[2] o_full
+  // o_free m_full[2] m_empty[2] mma_done
+  static constexpr int NBAR = 2 + 2 * RING + 2 + 2 + 2 + 4 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TM_S = 0, TM_O = 256;  // S(b) at b * 128; O half at 256
+  static constexpr int THREADS = 128 + 64;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(Fwd512Cfg::THREADS, 1)
+    k_fwd_d512(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+               const __grid_constant__ CUtensorMap mV, const FwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
+  using C = Fwd512Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* ring_full = q_empty + 1;         // [RING]
+  uint64_t* ring_empty = ring_full + C::RING;  // [RING]
+  uint64_t* s_full = ring_empty + C::RING;   // [2]
+  uint64_t* p_full = s_full + 2;             // [2]
+  uint64_t* o_full = p_full + 2;
+  uint64_t* o_free = o_full + 1;
+  uint64_t* m_full = o_free + 1;             // [2]
+  uint64_t* m_empty = m_full + 2;            // [2]
+  uint64_t* mma_done = m_empty + 2;
+  int* meta = reinterpret_cast<int*>(smem + C::OFF_META);  // mask slot of each mask buffer (-1: full tile)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.nq * p.Hq;
+  constexpr int PRODUCER = 4, ISSUER = 5;
+  const int g = p.Hq / p.Hkv;
+
+  if (threadIdx.x == PRODUCER * 32) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < C::RING; ++s) {
+      mbar_init(ring_full + s, 1);
+      mbar_init(ring_empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, 128);
+      mbar_init(m_full + b, 1);
+      mbar_init(m_empty + b, 128);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(o_free, 128);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mQ);
+    prefetch_tmap(&mK);
+    prefetch_tmap(&mV);
+  }
+  if (warp == ISSUER) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == PRODUCER) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t c = 0, mc = 0, it = 0;  // ring panels, mask buffers, items with blocks
+      bool ok = true, q_issued = false;
+      auto ring_load = [&](const CUtensorMap* map, int col, int hk, int row) -> bool {
+        const uint32_t s = c % C::RING, u = c / C::RING;
+        if (u > 0 && !mbar_wait(ring_empty + s, (u - 1) & 1, abort_flag)) return false;
+        mbar_expect_tx(ring_full + s, C::PANEL);
+        tma_load_3d(smem + C::OFF_RING + s * C::PANEL, map, ring_full + s, col, hk, row);
+        ++c;
+        return true;
+      };
+      for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
+        const int w = snake_item(rr, blockIdx.x, gridDim.x);
+        if (w >= n_items) continue;
+        const int tile = p.q_order[w / p.Hq], head = w % p.Hq, hk = head / g;
+        const int e0 = p.q_ptr[tile], n = p.q_ptr[tile + 1] - e0;
+        if (n == 0) continue;
+        q_issued = false;
+        if (it > 0 && !(ok = mbar_wait(q_empty, (it - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(q_full, C::NP * C::PANEL);
+        for (int pn = 0; pn < C::NP; ++pn)
+          tma_load_3d(smem + C::OFF_Q + pn * C::PANEL, &mQ, q_full, pn * 64, head, tile * 128);
+        q_issued = true;
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          for (int jj = 0; jj <= n && ok; ++jj) {
+            if (jj < n) {
+              const int j = p.kv_idx[e0 + jj], slot = p.pidx[e0 + jj];
+              // the block's keep mask (partial tiles) into its mask buffer
+              const uint32_t mb = mc % 2, mu = mc / 2;
+              if (mu > 0 && !(ok = mbar_wait(m_empty + mb, (mu - 1) & 1, abort_flag))) break;
+              meta[mb] = slot;  // made visible by the arrive below (release)
+              mbar_expect_tx(m_full + mb, slot >= 0 ? C::MASKB : 0);
+              if (slot >= 0)
+                bulk_load(smem + C::OFF_MASK + mb * C::MASKB, p.mask_rows + (size_t)slot * 512, C::MASKB, m_full + mb);
+              ++mc;
+              for (int pn = 0; pn < C::NP && ok; ++pn) ok = ring_load(&mK, pn * 64, hk, j * 128);
+            }
+            if (jj >= 1 && ok) {
+              const int j = p.kv_idx[e0 + jj - 1];
+              for (int q4 = 0; q4 < 4 && ok; ++q4) ok = ring_load(&mV, (hf * 4 + q4) * 64, hk, j * 128);
+            }
+          }
+        }
+        ++it;
+      }
+      if (!ok) {
+        const long long lim = 20000000;
+        if (q_issued) mbar_wait_drain(q_full, (it) & 1, lim);
+        for (uint32_t s = 0; s < C::RING && s < c; ++s) {
+          const uint32_t last = c - 1 - ((c - 1 - s) % C::RING);
+          mbar_wait_drain(ring_full + s, (last / C::RING) & 1, lim);
+        }
+        for (uint32_t b = 0; b < 2 && b < mc; ++b) {
+          const uint32_t last = mc - 1 - ((mc - 1 - b) % 2);
+          mbar_wait_drain(m_full + b, (last / 2) & 1, lim);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == ISSUER) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sR = smem_u32(smem + C::OFF_RING);
+      uint32_t c = 0, sc = 0, pvc = 0, it = 0, passes = 0;
+      bool ok = true;
+      for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
+        const int w = snake_item(rr, blockIdx.x, gridDim.x);
+        if (w >= n_items) continue;
+        const int tile = p.q_order[w / p.Hq];
+        const int n = p.q_ptr[tile + 1] - p.q_ptr[tile];
+        if (n == 0) continue;
+        if (!(ok = mbar_wait(q_full, it & 1, abort_flag))) break;
+        tc_fence_after();
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          for (int jj = 0; jj <= n && ok; ++jj) {
+            if (jj < n) {
+              // S(u) = Q K_j^T into buffer u % 2, accumulated over the 8 panels
+              const uint32_t u = sc + jj, b = u % 2;
+              for (int pn = 0; pn < C::NP && ok; ++pn) {
+                const uint32_t s = c % C::RING;
+                if (!(ok = mbar_wait(ring_full + s, (c / C::RING) & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_ss(tbase + C::TM_S + b * 128, sdesc_sw128(sQ + pn * C::PANEL + kk * 32, 16, 1024),
+                         sdesc_sw128(sR + s * C::PANEL + kk * 32, 16, 1024), IDESC_S, (pn > 0 || kk > 0));
+                mma_commit(ring_empty + s);
+                ++c;
+              }
+              if (!ok) break;
+              mma_commit(s_full + b);
+              if (hf == 1 && jj == n - 1) mma_commit(q_empty);  // the item's last read of Q
+            }
+            if (jj >= 1) {
+              // O half += P(u) V_half for block jj-1: P over S in TMEM, the four V
+              // panels of the half in ring slots 0..3 (one N = 256 operand)
+              const int i = jj - 1;
+              const uint32_t u = sc + i, b = u % 2;
+              if (!(ok = mbar_wait(p_full + b, (u / 2) & 1, abort_flag))) break;
+              if (i == 0 && passes > 0 && !(ok = mbar_wait(o_free, (passes - 1) & 1, abort_flag))) break;
+              for (int q4 = 0; q4 < 4 && ok; ++q4)
+                ok = mbar_wait(ring_full + (c + q4) % C::RING, ((c + q4) / C::RING) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ts(tbase + C::TM_O, tbase + C::TM_S + b * 128 + kk * 8,
+                       sdesc_sw128(sR + (c % C::RING) * C::PANEL + kk * 2048, C::PANEL, 1024), IDESC_PV,
+                       (i > 0 || kk > 0));
+              for (int q4 = 0; q4 < 4; ++q4) mma_commit(ring_empty + (c + q4) % C::RING);
+              c += 4;
+              mma_commit(o_full);
+              ++pvc;
+            }
+          }
+          sc += n;
+          ++passes;
+        }
+        ++it;
+      }
+      mma_commit(mma_done);
+      mbar_wait_drain(mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (q row per thread)
+    const int r = threadIdx.x;  // q row within the tile, TMEM lane
+    const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t sc = 0, pvc = 0, mc = 0, passes = 0;
+    bool ok = true;
+    for (int rr = 0; rr * (int)gridDim.x < n_items && ok; ++rr) {
+      const int w = snake_item(rr, blockIdx.x, gridDim.x);
+      if (w >= n_items) continue;
+      const int tile = p.q_order[w / p.Hq], head = w % p.Hq;
+      const int n = p.q_ptr[tile + 1] - p.q_ptr[tile];
+      const int q = tile * 128 + r;
+      __nv_bfloat16* orow = p.O + ((size_t)q * p.Hq + head) * C::D;
+      if (n == 0) {
+        if (q < p.T) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+          for (int c8 = 0; c8 < C::D / 8; ++c8) reinterpret_cast<uint4*>(orow)[c8] = z;
+          p.LSE[(size_t)head * p.T + q] = -INFINITY;
+        }
+        continue;
+      }
+      float m_use = -INFINITY, l = 0.f;
+      for (int hf = 0; hf < 2 && ok; ++hf) {
+        for (int jj = 0; jj < n; ++jj) {
+          const uint32_t u = sc + jj, b = u % 2;
+          const uint32_t mb = mc % 2;
+          ok = mbar_wait(s_full + b, (u / 2) & 1, abort_flag) && mbar_wait(m_full + mb, (mc / 2) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = tl + C::TM_S + b * 128;
+          uint32_t sr[128];
+          tmem_ld32(sb + 0, sr + 0);
+          tmem_ld32(sb + 32, sr + 32);
+          tmem_ld32(sb + 64, sr + 64);
+          tmem_ld32(sb + 96, sr + 96);
+          const int slot = meta[mb];
+          uint4 mk = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+          if (slot >= 0) mk = reinterpret_cast<const uint4*>(smem + C::OFF_MASK + mb * C::MASKB)[r];
+          mbar_arrive(m_empty + mb);  // the mask is in registers
+          ++mc;
+          tmem_ld_wait();
+          if (slot >= 0) {
+            const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (!((mw[c >> 5] >> (c & 31)) & 1u)) sr[c] = __float_as_uint(-INFINITY);
+          }
+          float ref = m_use;
+          if (hf == 0) {
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const float m_blk = mx * p.scale_log2;
+            const bool grow = m_blk > m_use + kRescaleThreshold;
+            const float m_new = grow ? m_blk : m_use;
+            if (__any_sync(0xffffffffu, grow && l > 0.f)) {
+              // O holds contributions against the old reference: once the PV in
+              // flight is done, rescale this warp's rows in place
+              ok = mbar_wait(o_full, (pvc + jj - 1) & 1, abort_flag);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const float alpha = (grow && l > 0.f) ? ex2(m_use - m_new) : 1.f;
+#pragma unroll 1
+              for (int c = 0; c < 256 / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(tl + C::TM_O + c * 32, orr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) orr[k] = __float_as_uint(__uint_as_float(orr[k]) * alpha);
+                tmem_st32(tl + C::TM_O + c * 32, orr);
+              }
+              tmem_st_wait();
+              l *= alpha;
+            }
+            m_use = m_new;
+            ref = m_new;
+          }
+          const float rf = (ref == -INFINITY) ? 0.f : ref;
+          float r8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) r8[k] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 128; c += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -rf));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -rf));
+            r8[(c >> 1) & 7] += p0 + p1;
+            sr[c >> 1] = pack_bf16(p0, p1);
+          }
+          if (hf == 0) l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+          tmem_st32(sb + 0, sr + 0);  // P over S (bf16 pairs in the first 64 columns)
+          tmem_st32(sb + 32, sr + 32);
+          tmem_st_wait();
+          if (jj > 0) {
+            // never more than one PV behind: the rescale above and the
+            // epilogue's waits rely on the parity of o_full
+            ok = mbar_wait(o_full, (pvc + jj - 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(p_full + b);
+        }
+        if (!ok) break;
+        // epilogue of the pass: this half of O / l
+        ok = mbar_wait(o_full, (pvc + n - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 256 / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tl + C::TM_O + c * 32, orr);
+          tmem_ld_wait();
+          store_rows32(orow + hf * 256 + c * 32, (size_t)p.Hq * C::D, q, p.T, orr, inv);
+        }
+        tc_fence_before();
+        mbar_arrive(o_free);
+        sc += n;
+        pvc += n;
+        ++passes;
+      }
+      if (!ok) break;
+      if (q < p.T) p.LSE[(size_t)head * p.T + q] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == ISSUER) tmem_dealloc(tbase, 512);
+}
+
+int launch_fwd512(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, float scale,
+                  const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
+  using C = Fwd512Cfg;
+  static int attr_set[64] = {0};
+  int dev = bm->device;
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_fwd_d512, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) {
+      set_error("forward kernel: cannot reserve %d bytes of shared memory: %s", C::SMEM_BYTES, cudaGetErrorString(e));
+      return 3;
+    }
+    attr_set[dev] = 1;
+  }
+  if (masks_missing(bm)) {
+    set_error("forward kernel: block map has no tile masks");
+    return 1;
+  }
+  CUtensorMap mQ, mK, mV;
+  if (!make_tmap_thd(&mQ, Q, T, Hq, C::D, 128) || !make_tmap_thd(&mK, K, T, Hkv, C::D, 128) ||
+      !make_tmap_thd(&mV, V, T, Hkv, C::D, 128))
+    return 3;
+  FwdParams p;
+  p.q_ptr = bm->q_ptr;
+  p.kv_idx = bm->kv_idx;
+  p.pidx = bm->pidx;
+  p.q_order = bm->q_order;
+  p.mask_rows = bm->mask_rows;
+  p.O = static_cast<__nv_bfloat16*>(O);
+  p.LSE = LSE;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.nq = bm->nq;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int n_items = bm->nq * Hq;
+  const int grid = n_items < num_sms(dev) ? n_items : num_sms(dev);
+  if (grid <= 0) return 0;
+  {
+    ProfScope ps(s, "fwd_tc");
+    launch_pdl(k_fwd_d512, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, mQ, mK, mV, p);
+  }
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("forward kernel launch failed: %s", cudaGetErrorString(e));
+    return 3;
+  }
+  return 0;
+}
 }  // namespace
 
 namespace {
@@ -827,6 +1252,7 @@ int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, 
     case 64: return launch_fwd<64, 2>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
     case 128: return launch_fwd<128, 2>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
     case 256: return launch_fwd<256, 1>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
+    case 512: return launch_fwd512(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
     default: set_error("tensor-core forward: head_dim %d not built", D); return 2;
   }
 }

@@ -1,7 +1,9 @@
 """Head dims above 256 (up to 512): forward and backward through the C ABI
-against the fp64 oracle.  These run on the CUDA-core kernels (fp32 math), for
-bf16 and fp32 inputs; the drafter PR reports FlexAttention failing beyond
-head_dim 256 on sm_103, which is why the library takes them at all."""
+against the fp64 oracle.  The bf16 forward at head_dim 512 on a 128 x 128 map
+runs on tensor cores (two passes over the halves of O); the other head dims
+above 256, fp32 inputs and the backward run on the CUDA-core kernels (fp32
+math).  The drafter PR reports FlexAttention failing beyond head_dim 256 on
+sm_103, which is why the library takes them at all."""
 import numpy as np
 import pytest
 
@@ -25,6 +27,18 @@ def test_bf16_fwd_bwd(D, name):
     st = small_structures()[name]
     check_fwd(st, 4, 2, D, "bf16", seed=D)
     check_bwd(st, 4, 2, D, "bf16", seed=D + 1)
+
+
+@pytest.mark.parametrize("name", ["grpo", "grpo_p0", "tree", "docs"])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (3, 3), (8, 1)])
+def test_tensor_core_fwd_head_dim_512(name, Hq, Hkv):
+    """Every element of O and LSE at head_dim 512 (tensor cores) on layouts
+    with ragged tails, an empty prompt and one-token completions."""
+    check_fwd(small_structures()[name], Hq, Hkv, 512, "bf16", seed=Hq * 7 + Hkv)
+
+
+def test_tensor_core_fwd_head_dim_512_dense_map():
+    check_fwd(small_structures()["tree"], 2, 1, 512, "bf16", seed=11, dense=True)
 
 
 @pytest.mark.parametrize("BM,BN", [(128, 128), (32, 64)])
