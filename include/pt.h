@@ -214,12 +214,12 @@ void pt_blockmap_free(pt_blockmap* bm);
  * LSE [Hq,T] (device fp32): LSE = m + ln(sum exp(s - m)) over the kept scores
  * s of the row.  scale <= 0 selects 1/sqrt(D).  The map must have been built
  * for the same T.
- * Supported: PT_BF16 with D in {64, 128, 256} and a 128 x 128 map run on
- * tensor cores; PT_BF16 with another D <= 512 that is a multiple of 8 (or
- * another tile size), and PT_F32 with 1 <= D <= 512, run on CUDA cores with
- * fp32 math.  Head dims above 256 have no tensor-core path here (a 128-row
- * fp32 accumulator of more than 256 columns leaves no TMEM for the scores);
- * the drafter PR notes that FlexAttention fails beyond 256 on sm_103.
+ * Supported: PT_BF16 with D in {64, 128, 256, 512} and a 128 x 128 map run
+ * on tensor cores (at 512 in two passes over the 256-column halves of O, S
+ * computed in both: a 128 x 512 fp32 accumulator would fill TMEM); PT_BF16
+ * with another D <= 512 that is a multiple of 8 (or another tile size), and
+ * PT_F32 with 1 <= D <= 512, run on CUDA cores with fp32 math.  The drafter
+ * PR notes that FlexAttention fails beyond head_dim 256 on sm_103.
  * Hq % Hkv == 0.  Anything else returns PT_ERR_UNSUPPORTED or
  * PT_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------- */
@@ -287,13 +287,13 @@ size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
  * own memory; a call whose map has no lists for its layout returns
  * PT_ERR_INVALID_ARG without launching anything.  The lists are kept per
  * (Hq / Hkv, Hkv, the device's SM count) for the kv-major kernel and per
- * (Hq, SM count) for the q-major kernels at head dims 128 and 256; head
- * dims 64 and 128 share the kv-major lists.  pt_attn_bwd with a workspace
+ * (Hq, SM count) for the q-major kernels at head dims 128, 256 and 512;
+ * head dims 64 and 128 share the kv-major lists.  pt_attn_bwd with a workspace
  * builds lists of its own (long columns split across SMs) beside these and
  * never replaces or frees them: every layout's lists stay with the map until
  * pt_blockmap_free.  Maps used only with the CUDA-core paths (fp32, tiles
- * other than 128 x 128, head dims other than 64, 128 and 256) need no lists,
- * and preparing them is a no-op.
+ * other than 128 x 128, head dims other than 64, 128, 256 and 512) need no
+ * lists, and preparing them is a no-op.
  * After cudaDeviceReset the library must not be used again in the process:
  * the array's looked-up address, like every map and pool, belongs to the
  * context that the reset destroyed.
@@ -442,7 +442,7 @@ pt_status pt_debug_wait_timeout(cudaStream_t stream);
 /* Builds the work lists pt_attn_bwd_noalloc needs for block map bm and head
  * layout (Hq, Hkv, D): the kv-major items packed onto the SMs (no column is
  * split, since that call has no workspace for partial sums) and, at
- * head_dims 128 and 256, the q-major items of the dQ kernels.  Allocates them
+ * head_dims 128, 256 and 512, the q-major items of the dQ kernels.  Allocates them
  * from the library's stream-ordered pool in the map's ownership (freed with
  * the map) and uploads them on `stream`.  A no-op where the backward runs on
  * the CUDA-core kernels (fp32, tiles other than 128 x 128, head dims other

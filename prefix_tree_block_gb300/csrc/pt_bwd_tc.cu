@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restric
                                                   int T, int Tpad, int Hq, float* __restrict__ delta,
                                                   float* __restrict__ lse2) {
   pdl_wait();  // launched with programmatic dependent launch
-  constexpr int TPR = D / 8;  // threads per (token, head) row
+  constexpr int VPT = D > 256 ? 2 : 1;  // 16-byte vectors of dO and O per thread (a row stays within a warp)
+  constexpr int TPR = D / (8 * VPT);    // threads per (token, head) row
   extern __shared__ float sh_delta[];  // [kPrepTokens][Hq + 1]
   const int q0 = blockIdx.x * kPrepTokens;
   const int sub = threadIdx.x % TPR;
@@ -78,15 +79,19 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restric
     const int ql = r / Hq, h = r % Hq, q = q0 + ql;
     float s = 0.f;
     if (q < T) {
-      const uint4 a = *reinterpret_cast<const uint4*>(dO + ((size_t)q * Hq + h) * D + sub * 8);
-      const uint4 b = *reinterpret_cast<const uint4*>(O + ((size_t)q * Hq + h) * D + sub * 8);
-      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float2 x = __bfloat1622float2(pa[k]), y = __bfloat1622float2(pb[k]);
-        s = fmaf(x.x, y.x, s);
-        s = fmaf(x.y, y.y, s);
+      for (int vv = 0; vv < VPT; ++vv) {
+        const int col = (vv * TPR + sub) * 8;
+        const uint4 a = *reinterpret_cast<const uint4*>(dO + ((size_t)q * Hq + h) * D + col);
+        const uint4 b = *reinterpret_cast<const uint4*>(O + ((size_t)q * Hq + h) * D + col);
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float2 x = __bfloat1622float2(pa[k]), y = __bfloat1622float2(pb[k]);
+          s = fmaf(x.x, y.x, s);
+          s = fmaf(x.y, y.y, s);
+        }
       }
     }
 #pragma unroll
@@ -154,6 +159,7 @@ struct BwdParams {
   float* partial;         // dkdv: fp32 partial sums of split columns, [slot][128][2D]
   int T, Tpad, Hq, Hkv, n_major, n_items;
   float scale, scale_log2;
+  int half;  // head_dim 512 passes: which 256-column half of the output
 };
 
 // Sum the chunk partials of every split kv-major column, in chunk order, and
@@ -1735,6 +1741,378 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 9) tmem_dealloc(tbase, 512);
 }
 
+
+// ---------------------------------------------------------------------------
+// 5. head_dim 512: six passes of one step kernel
+//
+// At D = 512 a 128-row tile is 128 KB of shared memory and a 128 x 512 fp32
+// accumulator is all of TMEM.  Each output (dV, dK, dQ) is therefore built
+// one 256-column half per pass (MODE and p.half), with S (and dP) recomputed
+// in every pass:
+//   D512_DV (kv-major): S^T = K Q^T, P^T, dV_half += P^T dO_half;
+//   D512_DK (kv-major): S^T = K Q^T, dP^T = V dO^T, dS^T, dK_half += dS^T Q_half;
+//   D512_DQ (q-major):  S = Q K^T, dP = dO V^T, dS, dQ_half += dS K_half.
+// The item's 128-row A operand of S (K, or Q) stays in shared memory; every
+// other operand streams through a ring of four 16 KB 64-column panels in the
+// order the MMAs consume them: a step's 8 B panels of S, then (with dP) its
+// 8 pairs of A and B panels of dP, then the 4 panels of the output half the
+// accumulating product reads.  Every group is a multiple of four panels, so
+// those 4 panels always sit in slots 0..3 (one N = 256 operand).  TMEM: S at
+// 0 and dP at 128 (the packed P or dS is written over the first columns just
+// read), the output half at 256.  A step's S is issued after the previous
+// step's accumulating product (which reads the packed P or dS over S).
+// ---------------------------------------------------------------------------
+enum { D512_DV = 0, D512_DK = 1, D512_DQ = 2 };
+
+struct Bwd512Cfg {
+  static constexpr int D = 512, NP = 8, PANEL = 128 * 128, RING = 4;
+  static constexpr int OFF_R = 0;
+  static constexpr int OFF_RING = OFF_R + NP * PANEL;
+  static constexpr int OFF_BAR = OFF_RING + RING * PANEL;
+  // r_full r_empty ring_full[4] ring_empty[4] s_full p_full acc_full acc_free mma_done
+  static constexpr int NBAR = 2 + 2 * RING + 5;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TM_S = 0, TM_DP = 128, TM_ACC = 256;
+  static constexpr int THREADS = 128 + 64;
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(Bwd512Cfg::THREADS, 1)
+    k_bwd_d512(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO, const BwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
+  using C = Bwd512Cfg;
+  constexpr int D = C::D;
+  constexpr bool HAS_DP = MODE != D512_DV, KV_MAJOR = MODE != D512_DQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* r_full = bars;
+  uint64_t* r_empty = bars + 1;
+  uint64_t* ring_full = bars + 2;                // [RING]
+  uint64_t* ring_empty = ring_full + C::RING;    // [RING]
+  uint64_t* s_full = ring_empty + C::RING;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* acc_full = p_full + 1;
+  uint64_t* acc_free = acc_full + 1;
+  uint64_t* mma_done = acc_free + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = p.Hq / p.Hkv;
+  const int hf = p.half;
+  const int i_begin = KV_MAJOR ? p.cta_ptr[blockIdx.x] : p.dq_cta[blockIdx.x].x;
+  const int i_end = KV_MAJOR ? p.cta_ptr[blockIdx.x + 1] : p.dq_cta[blockIdx.x].y;
+  // item k -> (major tile, its kv head or q head, steps)
+  const auto item = [&](int k, int& major, int& hh, int& n) {
+    if (KV_MAJOR) {
+      const DkdvItem it = p.items[k];
+      major = it.jb;
+      hh = it.hk;
+      n = it.x1 - it.x0;
+    } else {
+      const int4 it = p.dq_items[k];
+      major = it.x;
+      hh = it.y;
+      n = it.w;
+    }
+  };
+  // step x of item k: streamed tile (q tile or kv block), q head, mask slot
+  const auto step = [&](int k, int x, int& minor, int& head, int& slot) {
+    if (KV_MAJOR) {
+      const DkdvItem it = p.items[k];
+      const int e0 = p.ptr[it.jb], ncol = p.ptr[it.jb + 1] - e0;
+      const int e = e0 + (it.x0 + x) % ncol;
+      head = it.hk * g + (it.x0 + x) / ncol;
+      minor = p.idx[e];
+      slot = p.pidx[e];
+    } else {
+      const int4 it = p.dq_items[k];
+      minor = p.idx[it.z + x];
+      head = it.y;
+      slot = p.pidx[it.z + x];
+    }
+  };
+
+  constexpr int PRODUCER = 4, ISSUER = 5;
+  if (threadIdx.x == PRODUCER * 32) {
+    mbar_init(r_full, 1);
+    mbar_init(r_empty, 1);
+    for (int s = 0; s < C::RING; ++s) {
+      mbar_init(ring_full + s, 1);
+      mbar_init(ring_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_free, 128);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mQ);
+    prefetch_tmap(&mK);
+    prefetch_tmap(&mV);
+    prefetch_tmap(&mdO);
+  }
+  if (warp == ISSUER) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == PRODUCER) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t c = 0, it = 0;
+      bool ok = true, r_issued = false;
+      auto ring_load = [&](const CUtensorMap* map, int col, int h, int row) -> bool {
+        const uint32_t s = c % C::RING, u = c / C::RING;
+        if (u > 0 && !mbar_wait(ring_empty + s, (u - 1) & 1, abort_flag)) return false;
+        mbar_expect_tx(ring_full + s, C::PANEL);
+        tma_load_3d(smem + C::OFF_RING + s * C::PANEL, map, ring_full + s, col, h, row);
+        ++c;
+        return true;
+      };
+      for (int k = i_begin; k < i_end && ok; ++k) {
+        int major, hh, n;
+        item(k, major, hh, n);
+        if (n == 0) continue;
+        r_issued = false;
+        if (it > 0 && !(ok = mbar_wait(r_empty, (it - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(r_full, C::NP * C::PANEL);
+        // the resident A operand of S: K of kv block `major` (kv-major) or Q of q tile `major`
+        for (int pn = 0; pn < C::NP; ++pn)
+          tma_load_3d(smem + C::OFF_R + pn * C::PANEL, KV_MAJOR ? &mK : &mQ, r_full, pn * 64, hh, major * 128);
+        r_issued = true;
+        for (int x = 0; x < n && ok; ++x) {
+          int minor, head, slot;
+          step(k, x, minor, head, slot);
+          const int hk = KV_MAJOR ? hh : hh / g;  // kv head of the item
+          // S: the B panels (Q of q tile `minor`, or K of kv block `minor`)
+          for (int pn = 0; pn < C::NP && ok; ++pn)
+            ok = KV_MAJOR ? ring_load(&mQ, pn * 64, head, minor * 128) : ring_load(&mK, pn * 64, hk, minor * 128);
+          // dP: A and B panel pairs (V of the kv block and dO of the q tile)
+          if (HAS_DP)
+            for (int pn = 0; pn < C::NP && ok; ++pn) {
+              if (KV_MAJOR)
+                ok = ring_load(&mV, pn * 64, hk, major * 128) && ring_load(&mdO, pn * 64, head, minor * 128);
+              else
+                ok = ring_load(&mdO, pn * 64, hh, major * 128) && ring_load(&mV, pn * 64, hk, minor * 128);
+            }
+          // the output half's operand: dO (dV), Q (dK) or K (dQ) of the streamed tile
+          for (int q4 = 0; q4 < 4 && ok; ++q4) {
+            const int col = (4 * hf + q4) * 64;
+            ok = MODE == D512_DV ? ring_load(&mdO, col, head, minor * 128)
+                                 : (MODE == D512_DK ? ring_load(&mQ, col, head, minor * 128)
+                                                    : ring_load(&mK, col, hk, minor * 128));
+          }
+        }
+        if (!ok) break;
+        ++it;
+      }
+      if (!ok) {
+        const long long lim = 20000000;
+        if (r_issued) mbar_wait_drain(r_full, it & 1, lim);
+        for (uint32_t s = 0; s < C::RING && s < c; ++s) {
+          const uint32_t last = c - 1 - ((c - 1 - s) % C::RING);
+          mbar_wait_drain(ring_full + s, (last / C::RING) & 1, lim);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == ISSUER) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t IDESC_ACC = idesc_bf16(128, 256, false, true);
+      const uint32_t sR = smem_u32(smem + C::OFF_R), sG = smem_u32(smem + C::OFF_RING);
+      uint32_t c = 0, y = 0, it = 0;
+      bool ok = true;
+      auto wait_panel = [&](uint32_t cc) -> bool {
+        return mbar_wait(ring_full + cc % C::RING, (cc / C::RING) & 1, abort_flag);
+      };
+      for (int k = i_begin; k < i_end && ok; ++k) {
+        int major, hh, n;
+        item(k, major, hh, n);
+        if (n == 0) continue;
+        if (!(ok = mbar_wait(r_full, it & 1, abort_flag))) break;
+        tc_fence_after();
+        for (int x = 0; x <= n && ok; ++x) {
+          if (x >= 1) {
+            // the output half += X(x-1) [its 4 panels, slots 0..3], X = P or dS
+            // packed over the first columns of S or dP
+            const uint32_t yp = y + x - 1;
+            if (!(ok = mbar_wait(p_full, yp & 1, abort_flag))) break;
+            if (x == 1 && it > 0 && !(ok = mbar_wait(acc_free, (it - 1) & 1, abort_flag))) break;
+            for (int q4 = 0; q4 < 4 && ok; ++q4) ok = wait_panel(c + q4);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a = tbase + (HAS_DP ? C::TM_DP : C::TM_S);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tbase + C::TM_ACC, a + kk * 8, sdesc_sw128(sG + (c % C::RING) * C::PANEL + kk * 2048, C::PANEL, 1024),
+                     IDESC_ACC, (x > 1 || kk > 0));
+            for (int q4 = 0; q4 < 4; ++q4) mma_commit(ring_empty + (c + q4) % C::RING);
+            c += 4;
+          }
+          if (x < n) {
+            // S(x) (and dP(x)) over the columns the product above reads (issued
+            // after it on this thread, so it reads them first)
+            for (int pn = 0; pn < C::NP && ok; ++pn) {
+              if (!(ok = wait_panel(c))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(tbase + C::TM_S, sdesc_sw128(sR + pn * C::PANEL + kk * 32, 16, 1024),
+                       sdesc_sw128(sG + (c % C::RING) * C::PANEL + kk * 32, 16, 1024), IDESC_S, (pn > 0 || kk > 0));
+              mma_commit(ring_empty + c % C::RING);
+              ++c;
+            }
+            if (HAS_DP)
+              for (int pn = 0; pn < C::NP && ok; ++pn) {
+                if (!(ok = wait_panel(c) && wait_panel(c + 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_ss(tbase + C::TM_DP, sdesc_sw128(sG + (c % C::RING) * C::PANEL + kk * 32, 16, 1024),
+                         sdesc_sw128(sG + ((c + 1) % C::RING) * C::PANEL + kk * 32, 16, 1024), IDESC_S,
+                         (pn > 0 || kk > 0));
+                mma_commit(ring_empty + c % C::RING);
+                mma_commit(ring_empty + (c + 1) % C::RING);
+                c += 2;
+              }
+            if (!ok) break;
+            mma_commit(s_full);
+            if (x == n - 1) mma_commit(r_empty);
+          }
+        }
+        if (ok) mma_commit(acc_full);
+        y += n;
+        ++it;
+      }
+      mma_commit(mma_done);
+      mbar_wait_drain(mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute (major row per thread)
+    const int r = threadIdx.x;
+    const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint4* masks = reinterpret_cast<const uint4*>(p.masks);
+    uint32_t y = 0, it = 0;
+    bool ok = true;
+    for (int k = i_begin; k < i_end && ok; ++k) {
+      int major, hh, n;
+      item(k, major, hh, n);
+      const int row = major * 128 + r;  // kv token (kv-major) or q token (q-major)
+      __nv_bfloat16* out = MODE == D512_DQ ? p.out0 + ((size_t)row * p.Hq + hh) * D + hf * 256
+                                           : (MODE == D512_DV ? p.out1 : p.out0) + ((size_t)row * p.Hkv + hh) * D +
+                                                 hf * 256;  // this pass's half of the output row
+      const size_t ostride = (size_t)(MODE == D512_DQ ? p.Hq : p.Hkv) * D;
+      if (n == 0) {
+        if (row < p.T) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 32; ++c) reinterpret_cast<uint4*>(out)[c] = z;
+        }
+        continue;
+      }
+      float l2r = 0.f, dlr = 0.f;  // q-major: this row's statistics
+      if (!KV_MAJOR) {
+        l2r = p.lse2[(size_t)hh * p.Tpad + row];
+        dlr = p.delta[(size_t)hh * p.Tpad + row];
+      }
+      for (int x = 0; x < n; ++x) {
+        int minor, head, slot;
+        step(k, x, minor, head, slot);
+        uint4 mk = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+        if (slot >= 0) mk = masks[(size_t)slot * 128 + r];
+        const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
+        // kv-major: statistics of the step's 128 q columns (uniform over the warp)
+        const float4* l4 = reinterpret_cast<const float4*>(p.lse2 + (size_t)head * p.Tpad + minor * 128);
+        const float4* d4 = reinterpret_cast<const float4*>(p.delta + (size_t)head * p.Tpad + minor * 128);
+        ok = mbar_wait(s_full, (y + x) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {  // 64 columns at a time
+          uint32_t sr[64], dr[64];
+          tmem_ld32(tl + C::TM_S + 64 * h2, sr);
+          tmem_ld32(tl + C::TM_S + 64 * h2 + 32, sr + 32);
+          if (HAS_DP) {
+            tmem_ld32(tl + C::TM_DP + 64 * h2, dr);
+            tmem_ld32(tl + C::TM_DP + 64 * h2 + 32, dr + 32);
+          }
+          tmem_ld_wait();
+          uint32_t pk[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            float la[4], da[4];
+            if (KV_MAJOR) {
+              const float4 lv = l4[16 * h2 + c4];
+              la[0] = lv.x, la[1] = lv.y, la[2] = lv.z, la[3] = lv.w;
+              if (HAS_DP) {
+                const float4 dv = d4[16 * h2 + c4];
+                da[0] = dv.x, da[1] = dv.y, da[2] = dv.z, da[3] = dv.w;
+              }
+            } else {
+              la[0] = la[1] = la[2] = la[3] = l2r;
+              da[0] = da[1] = da[2] = da[3] = dlr;
+            }
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = 4 * c4 + j, cc = 64 * h2 + c;  // column within the step
+              float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[j]));
+              pr = ((mw[cc >> 5] >> (cc & 31)) & 1u) ? pr : 0.f;
+              v[j] = HAS_DP ? pr * (__uint_as_float(dr[c]) - da[j]) : pr;
+            }
+            pk[2 * c4] = pack_bf16(v[0], v[1]);
+            pk[2 * c4 + 1] = pack_bf16(v[2], v[3]);
+          }
+          // packed over the columns read first (P over S, dS over dP)
+          tmem_st32(tl + (HAS_DP ? C::TM_DP : C::TM_S) + 32 * h2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      ok = mbar_wait(acc_full, it & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float mul = MODE == D512_DV ? 1.f : p.scale;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tl + C::TM_ACC + c * 32, v);
+        tmem_ld_wait();
+        store_rows32(out + c * 32, ostride, row, p.T, v, mul);
+      }
+      tc_fence_before();
+      mbar_arrive(acc_free);
+      y += n;
+      ++it;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == ISSUER) tmem_dealloc(tbase, 512);
+}
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -2192,9 +2570,110 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   return 0;
 }
 
+
+// head_dim 512: preprocess, then the dV, dK and dQ passes of k_bwd_d512, one
+// per half of each output.
+int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
+                    int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
+                    float* lse2, bool allow_build, cudaStream_t s) {
+  constexpr int D = 512;
+  using C = Bwd512Cfg;
+  static int set_v[64] = {0}, set_k[64] = {0}, set_q[64] = {0};
+  const int dev = bm->device;
+  int rc = reserve_smem(k_bwd_d512<D512_DV>, C::BYTES, dev, set_v);
+  if (!rc) rc = reserve_smem(k_bwd_d512<D512_DK>, C::BYTES, dev, set_k);
+  if (!rc) rc = reserve_smem(k_bwd_d512<D512_DQ>, C::BYTES, dev, set_q);
+  if (rc) return rc;
+  if (masks_missing(bm)) {
+    set_error("backward kernel: block map has no tile masks");
+    return 1;
+  }
+  const int sms = num_sms(dev);
+  const pt_dkdv_lists* KL = nullptr;
+  const pt_dq_lists* QL = nullptr;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, allow_build, s, &KL))) return rc;
+  if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
+  const int Tpad = bm->nq * 128;
+  {
+    const size_t sm = sizeof(float) * kPrepTokens * ((size_t)Hq + 1);
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(k_bwd_prep<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess) {
+      set_error("backward preprocess: %d heads need %zu bytes of shared memory", Hq, sm);
+      return 3;
+    }
+    ProfScope ps(s, "bwd_prep");
+    launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s,
+               static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta,
+               lse2);
+  }
+  CUtensorMap mQ, mK, mV, mdO;
+  if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mK, K, T, Hkv, D, 128) ||
+      !make_tmap_thd(&mV, V, T, Hkv, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128))
+    return 3;
+  BwdParams p{};
+  p.delta = delta;
+  p.lse2 = lse2;
+  p.T = T;
+  p.Tpad = Tpad;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  int launches = 1;
+  // dV and dK: kv-major lists and column masks
+  p.ptr = bm->k_ptr;
+  p.idx = bm->q_idx;
+  p.pidx = bm->pidxT;
+  p.masks = bm->mask_cols;
+  p.items = static_cast<const DkdvItem*>(KL->items);
+  p.cta_ptr = static_cast<const int*>(KL->cta);
+  p.n_items = KL->n_items;
+  p.out0 = static_cast<__nv_bfloat16*>(dK);
+  p.out1 = static_cast<__nv_bfloat16*>(dV);
+  if (p.n_items > 0) {
+    for (int h = 0; h < 2; ++h) {
+      p.half = h;
+      ProfScope ps(s, "bwd_dv");
+      launch_pdl(k_bwd_d512<D512_DV>, dim3(KL->grid), dim3(C::THREADS), C::BYTES, s, mQ, mK, mV, mdO, p);
+    }
+    for (int h = 0; h < 2; ++h) {
+      p.half = h;
+      ProfScope ps(s, "bwd_dk");
+      launch_pdl(k_bwd_d512<D512_DK>, dim3(KL->grid), dim3(C::THREADS), C::BYTES, s, mQ, mK, mV, mdO, p);
+    }
+    launches += 4;
+  }
+  // dQ: q-major lists and row masks
+  p.ptr = bm->q_ptr;
+  p.idx = bm->kv_idx;
+  p.pidx = bm->pidx;
+  p.masks = bm->mask_rows;
+  p.items = nullptr;
+  p.cta_ptr = nullptr;
+  p.dq_items = static_cast<const int4*>(QL->items);
+  p.dq_cta = static_cast<const int4*>(QL->cta);
+  p.out0 = static_cast<__nv_bfloat16*>(dQ);
+  p.out1 = nullptr;
+  if ((rc = zero_empty_dq(QL, dQ, T, Hq, D, s))) return rc;
+  if (QL->n_items > 0) {
+    for (int h = 0; h < 2; ++h) {
+      p.half = h;
+      ProfScope ps(s, "bwd_dq");
+      launch_pdl(k_bwd_d512<D512_DQ>, dim3(QL->grid), dim3(C::THREADS), C::BYTES, s, mQ, mK, mV, mdO, p);
+    }
+    launches += 2;
+  }
+  count_launch(launches);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("backward launch failed: %s", cudaGetErrorString(e));
+    return 3;
+  }
+  return 0;
+}
 }  // namespace
 
-bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
+bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
 int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStream_t s) {
   if (!bwd_tc_supported(D) || bm->BM != 128 || bm->BN != 128) return 0;  // those paths keep no lists
@@ -2218,6 +2697,8 @@ int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const vo
                              partial_bytes, allow_build, s);
     case 256:
       return launch_bwd_wide(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, allow_build, s);
+    case 512:
+      return launch_bwd_d512(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, allow_build, s);
     default: set_error("tensor-core backward: head_dim %d not built", D); return 2;
   }
 }

@@ -117,18 +117,11 @@ def test_draft_workload_last_kv_head_every_element():
     assert np.all(got[0][empty] == 0) and np.all(got[2][empty] == 0)
 
 
-def test_head_dim_512_forward_every_element():
-    """Workload 7 (packed documents at head_dim 512, the tensor-core forward's
-    measurement shape): every element of O and LSE."""
+def test_head_dim_512_every_element():
+    """Workload 7 (packed documents at head_dim 512, the measurement shape of
+    the tensor-core kernels at that head dim): every element of O, LSE, dQ,
+    dK and dV."""
     cfg = W.CONFIGS[7]
     st = W.config_structure(7)
-    q, k, v, _ = W.make_tensors(st.T, cfg["Hq"], cfg["Hkv"], cfg["D"], "bf16", seed=7)
-    bm = _tree_map(st)
-    O, L = pt.attn_fwd(to_dev(q), to_dev(k), to_dev(v), bm)
-    pt.sync_status()
-    bm.free()
-    Ow, Lw = orc.attn_fwd(q, k, v, orc.structure_labels(st))
-    O, L = O.float().cpu().numpy(), L.cpu().numpy()
-    assert np.isfinite(O).all()
-    assert np.abs(O - Ow).max() <= FWD_ATOL["bf16"]
-    assert np.abs(L - Lw).max() <= LSE_ATOL["bf16"]
+    q, k, v, do = W.make_tensors(st.T, cfg["Hq"], cfg["Hkv"], cfg["D"], "bf16", seed=7)
+    _check_case(_tree_map(st), q, k, v, do, _tree_oracle(st))

@@ -1,8 +1,8 @@
 """Head dims above 256 (up to 512): forward and backward through the C ABI
-against the fp64 oracle.  The bf16 forward at head_dim 512 on a 128 x 128 map
-runs on tensor cores (two passes over the halves of O); the other head dims
-above 256, fp32 inputs and the backward run on the CUDA-core kernels (fp32
-math).  The drafter PR reports FlexAttention failing beyond head_dim 256 on
+against the fp64 oracle.  bf16 at head_dim 512 on a 128 x 128 map runs on
+tensor cores (the forward in two passes over the halves of O, the backward in
+six passes, one per half of dV, dK and dQ); the other head dims above 256 and
+fp32 inputs run on the CUDA-core kernels (fp32 math).  The drafter PR reports FlexAttention failing beyond head_dim 256 on
 sm_103, which is why the library takes them at all."""
 import numpy as np
 import pytest
@@ -39,6 +39,17 @@ def test_tensor_core_fwd_head_dim_512(name, Hq, Hkv):
 
 def test_tensor_core_fwd_head_dim_512_dense_map():
     check_fwd(small_structures()["tree"], 2, 1, 512, "bf16", seed=11, dense=True)
+
+
+@pytest.mark.parametrize("name", ["grpo", "grpo_p0", "tree", "docs"])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (3, 3), (8, 1)])
+def test_tensor_core_bwd_head_dim_512(name, Hq, Hkv):
+    """Every element of dQ, dK, dV at head_dim 512 (tensor cores), relative L2."""
+    check_bwd(small_structures()[name], Hq, Hkv, 512, "bf16", seed=Hq * 5 + Hkv)
+
+
+def test_tensor_core_bwd_head_dim_512_dense_map():
+    check_bwd(small_structures()["tree"], 2, 1, 512, "bf16", seed=12, dense=True)
 
 
 @pytest.mark.parametrize("BM,BN", [(128, 128), (32, 64)])

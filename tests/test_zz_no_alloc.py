@@ -51,8 +51,8 @@ def _pool_usage(lib):
     return used.value, reserved.value
 
 
-@pytest.mark.parametrize("dtype,D,BM", [("bf16", 64, 128), ("bf16", 128, 128), ("bf16", 256, 128), ("bf16", 96, 128),
-                                        ("bf16", 320, 128), ("f32", 32, 16)])
+@pytest.mark.parametrize("dtype,D,BM", [("bf16", 64, 128), ("bf16", 128, 128), ("bf16", 256, 128), ("bf16", 512, 128),
+                                        ("bf16", 96, 128), ("bf16", 320, 128), ("f32", 32, 16)])
 def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
     st = W.grpo_structure([(300, [100, 41, 250]), (0, [77, 129])])
     q, k, v, do = W.make_tensors(st.T, 4, 2, D, dtype, seed=D)
@@ -64,7 +64,7 @@ def test_noalloc_matches_workspace_backward_twice(lib, dtype, D, BM):
     # a fresh map of the same layout: the workspace backward above may already have built, on bm, the lists
     # the allocation-free call reads (at head_dim 256 they are the same lists)
     bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes, BM, BM)
-    if dtype == "bf16" and D in (64, 128, 256):  # the tensor-core path reads per-map work lists: refused until prepared
+    if dtype == "bf16" and D in (64, 128, 256, 512):  # the tensor-core path reads per-map work lists: refused until prepared
         _noalloc(lib, dO, Q, K, V, O, LSE, bm, code, expect=pt.PT_ERR_INVALID_ARG)
         assert b"pt_blockmap_prepare_bwd" in lib.pt_last_error()
     elif dtype == "bf16":  # the CUDA-core kernels keep no lists: no preparation needed
@@ -122,7 +122,7 @@ def test_noalloc_head_dim_limits(lib):
         rc = lib.pt_attn_bwd_noalloc(p, p, p, p, p, lse.data_ptr(), pt.PT_BF16, st.T, 2, 1, D, 0.0, bm.handle, p, p,
                                      p, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert rc == want, lib.pt_last_error()
-    bm.prepare_bwd(2, 1, 512)  # CUDA-core head dim: nothing to build
+    bm.prepare_bwd(2, 1, 512)  # the largest head dim it takes
     with pytest.raises(pt.PTError) as ei:
         bm.prepare_bwd(2, 1, 520)
     assert ei.value.status == pt.PT_ERR_UNSUPPORTED
