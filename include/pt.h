@@ -442,11 +442,11 @@ pt_status pt_debug_wait_timeout(cudaStream_t stream);
 /* Builds the work lists pt_attn_bwd_noalloc needs for block map bm and head
  * layout (Hq, Hkv, D): the kv-major items packed onto the SMs (no column is
  * split, since that call has no workspace for partial sums) and, at
- * head_dims 128, 256 and 512, the q-major items of the dQ kernels.  Allocates them
- * from the library's stream-ordered pool in the map's ownership (freed with
- * the map) and uploads them on `stream`.  A no-op where the backward runs on
- * the CUDA-core kernels (fp32, tiles other than 128 x 128, head dims other
- * than 64, 128 and 256).  Idempotent; returns PT_ERR_INVALID_ARG for a NULL
+ * head_dims 128, 256 and 512, the q-major items of the dQ kernels.
+ * Allocates them from the library's stream-ordered pool in the map's
+ * ownership (freed with the map) and uploads them on `stream`.  A no-op
+ * where the backward runs on the CUDA-core kernels (fp32, tiles other than
+ * 128 x 128, head dims other than 64, 128, 256 and 512).  Idempotent; returns PT_ERR_INVALID_ARG for a NULL
  * map or a bad head layout and PT_ERR_UNSUPPORTED for head_dim above 512, as
  * pt_attn_bwd does.  The pages have no counterpart. */
 pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv, int32_t D, cudaStream_t stream);
