@@ -423,12 +423,15 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
     bwd_ms = sum(kernels[k]["ms_per_launch"] for k in kernels if k.startswith("bwd_"))
     fwd_tf = flops_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None
     bwd_tf = 2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None
+    # head_dim 512: each backward launch builds one 256-column half of its output and recomputes S
+    # (and dP): S^T + half of dV = 3D, S^T + dP^T + half of dK (or S + dP + half of dQ) = 5D
+    wide2 = D == 512
     per_launch_flops = {  # useful-pair flops of each kernel: 2D per pair and head for each of its products
         "fwd_tc": 4.0 * D * Hq * pairs,
         "bwd_dkdv": 8.0 * D * Hq * pairs,
-        "bwd_dv": 4.0 * D * Hq * pairs,  # head_dim 256: S^T and dV
-        "bwd_dk": 6.0 * D * Hq * pairs,  # head_dim 256: S^T, dP^T and dK
-        "bwd_dq": 6.0 * D * Hq * pairs,
+        "bwd_dv": (3.0 if wide2 else 4.0) * D * Hq * pairs,  # head_dim 256: S^T and dV
+        "bwd_dk": (5.0 if wide2 else 6.0) * D * Hq * pairs,  # head_dim 256: S^T, dP^T and dK
+        "bwd_dq": (5.0 if wide2 else 6.0) * D * Hq * pairs,
         # CUDA-core kernels (fp32 inputs, head dims without a tensor-core path): useful flops
         "fwd_simt": 4.0 * D * Hq * pairs,
         "bwd_simt": 10.0 * D * Hq * pairs,
