@@ -193,6 +193,37 @@ __global__ void k_dkdv_finalize(const int4* __restrict__ splits, const float* __
   }
 }
 
+// Sum the chunk partials of every split kv-major column for one output of
+// the head_dim-256 and -512 passes: slot rows of row_floats floats whose
+// first W hold this pass's columns; the sums go to columns [col0, col0 + W)
+// of the output rows (row stride H * D), as bf16.
+template <int W>
+__global__ void k_split_finalize(const int4* __restrict__ splits, const float* __restrict__ partial, int row_floats,
+                                 int T, int H, int D, int col0, __nv_bfloat16* __restrict__ out) {
+  pdl_wait();  // launched with programmatic dependent launch
+  const int4 sp = splits[blockIdx.x];  // kv block, kv head, first slot, slot count
+  constexpr int Q4 = W / 4;
+  for (int idx = threadIdx.x; idx < 8 * Q4; idx += blockDim.x) {
+    const int r = blockIdx.y * 8 + idx / Q4, c = (idx % Q4) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < sp.w; ++k) {
+      const float4 v = *reinterpret_cast<const float4*>(partial + ((size_t)(sp.z + k) * 128 + r) * row_floats + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int kv = sp.x * 128 + r;
+    if (kv >= T) continue;
+    __nv_bfloat16* dst = out + ((size_t)kv * H + sp.y) * D + col0 + c;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  }
+}
+
 // 64 fp32 values (as bits) -> 32 bf16x2 words.
 __device__ __forceinline__ void pack64(const uint32_t* v, uint32_t* out) {
 #pragma unroll
@@ -1720,12 +1751,21 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_after();
       const float mul = MODE == WIDE_DV ? 1.f : p.scale;
+      const int slot = C::KV_MAJOR ? p.items[k].slot : -1;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tmem_ld32(tl + C::TM_ACC + hw * 128 + c * 32, v);
         tmem_ld_wait();
-        store_rows32(out + c * 32, (size_t)(MODE == WIDE_DQ ? p.Hq : p.Hkv) * D, row, p.T, v, mul);
+        if (slot < 0) {
+          store_rows32(out + c * 32, (size_t)(MODE == WIDE_DQ ? p.Hq : p.Hkv) * D, row, p.T, v, mul);
+        } else {  // one chunk of a split column: fp32 partial sums, summed later in chunk order
+          float4* prow = reinterpret_cast<float4*>(p.partial + ((size_t)slot * 128 + r) * (2 * D) + hw * 128 + c * 32);
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4)
+            prow[k4] = make_float4(__uint_as_float(v[4 * k4]) * mul, __uint_as_float(v[4 * k4 + 1]) * mul,
+                                   __uint_as_float(v[4 * k4 + 2]) * mul, __uint_as_float(v[4 * k4 + 3]) * mul);
+        }
       }
       tc_fence_before();
       mbar_arrive(&B->acc_free);
@@ -2093,12 +2133,21 @@ __global__ void __launch_bounds__(Bwd512Cfg::THREADS, 1)
       }
       tc_fence_after();
       const float mul = MODE == D512_DV ? 1.f : p.scale;
+      const int slot = KV_MAJOR ? p.items[k].slot : -1;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
         tmem_ld32(tl + C::TM_ACC + c * 32, v);
         tmem_ld_wait();
-        store_rows32(out + c * 32, ostride, row, p.T, v, mul);
+        if (slot < 0) {
+          store_rows32(out + c * 32, ostride, row, p.T, v, mul);
+        } else {  // one chunk of a split column: fp32 partial sums of this half, summed later in chunk order
+          float4* prow = reinterpret_cast<float4*>(p.partial + ((size_t)slot * 128 + r) * (2 * D) + c * 32);
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4)
+            prow[k4] = make_float4(__uint_as_float(v[4 * k4]) * mul, __uint_as_float(v[4 * k4 + 1]) * mul,
+                                   __uint_as_float(v[4 * k4 + 2]) * mul, __uint_as_float(v[4 * k4 + 3]) * mul);
+        }
       }
       tc_fence_before();
       mbar_arrive(acc_free);
@@ -2479,7 +2528,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
 // head_dim 256: preprocess, then the dV, dK and dQ passes of k_bwd_wide.
 int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
                     int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
-                    float* lse2, bool allow_build, cudaStream_t s) {
+                    float* lse2, float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s) {
   constexpr int D = 256;
   static int set_v[64] = {0}, set_k[64] = {0}, set_q[64] = {0};
   const int dev = bm->device;
@@ -2492,10 +2541,13 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
     return 1;
   }
   const int sms = num_sms(dev);
-  // kv-major items without split columns (each pass writes its outputs once)
+  // kv-major items: long columns cut into chunks that write fp32 partial sums
+  // (slots of 128 x 2D floats, of which each pass fills its D columns), when
+  // the caller's workspace has room for them; the finalize kernel sums them
+  const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
   const pt_dkdv_lists* KL = nullptr;
   const pt_dq_lists* QL = nullptr;
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, allow_build, s, &KL))) return rc;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s, &KL))) return rc;
   if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
   const int Tpad = bm->nq * 128;
   {
@@ -2534,14 +2586,28 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   p.n_items = KL->n_items;
   p.out0 = static_cast<__nv_bfloat16*>(dK);
   p.out1 = static_cast<__nv_bfloat16*>(dV);
+  p.partial = partial;
   if (p.n_items > 0) {
+    const int4* splits = static_cast<const int4*>(KL->splits);
     {
       ProfScope ps(s, "bwd_dv");
       launch_pdl(k_bwd_wide<WIDE_DV>, dim3(KL->grid), dim3(320), WideCfg<WIDE_DV>::BYTES, s, mK, mK, mdOh, mQh, p);
     }
+    if (KL->n_splits > 0) {
+      ProfScope ps(s, "bwd_dkdv_finalize");
+      launch_pdl(k_split_finalize<D>, dim3(KL->n_splits, 16), dim3(256), 0, s, splits, (const float*)partial, 2 * D, T,
+                 Hkv, D, 0, static_cast<__nv_bfloat16*>(dV));
+      ++launches;
+    }
     {
       ProfScope ps(s, "bwd_dk");
       launch_pdl(k_bwd_wide<WIDE_DK>, dim3(KL->grid), dim3(320), WideCfg<WIDE_DK>::BYTES, s, mK, mV, mQh, mdOh, p);
+    }
+    if (KL->n_splits > 0) {
+      ProfScope ps(s, "bwd_dkdv_finalize");
+      launch_pdl(k_split_finalize<D>, dim3(KL->n_splits, 16), dim3(256), 0, s, splits, (const float*)partial, 2 * D, T,
+                 Hkv, D, 0, static_cast<__nv_bfloat16*>(dK));
+      ++launches;
     }
     launches += 2;
   }
@@ -2575,7 +2641,7 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
 // per half of each output.
 int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
                     int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
-                    float* lse2, bool allow_build, cudaStream_t s) {
+                    float* lse2, float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s) {
   constexpr int D = 512;
   using C = Bwd512Cfg;
   static int set_v[64] = {0}, set_k[64] = {0}, set_q[64] = {0};
@@ -2589,9 +2655,13 @@ int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V,
     return 1;
   }
   const int sms = num_sms(dev);
+  // kv-major items: long columns cut into chunks that write fp32 partial sums
+  // of the pass's 256 columns (slots of 128 x 2D floats) when the workspace
+  // has room; the finalize kernel sums them after each pass
+  const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
   const pt_dkdv_lists* KL = nullptr;
   const pt_dq_lists* QL = nullptr;
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, allow_build, s, &KL))) return rc;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s, &KL))) return rc;
   if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
   const int Tpad = bm->nq * 128;
   {
@@ -2630,18 +2700,27 @@ int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V,
   p.n_items = KL->n_items;
   p.out0 = static_cast<__nv_bfloat16*>(dK);
   p.out1 = static_cast<__nv_bfloat16*>(dV);
+  p.partial = partial;
   if (p.n_items > 0) {
-    for (int h = 0; h < 2; ++h) {
-      p.half = h;
-      ProfScope ps(s, "bwd_dv");
-      launch_pdl(k_bwd_d512<D512_DV>, dim3(KL->grid), dim3(C::THREADS), C::BYTES, s, mQ, mK, mV, mdO, p);
-    }
-    for (int h = 0; h < 2; ++h) {
-      p.half = h;
-      ProfScope ps(s, "bwd_dk");
-      launch_pdl(k_bwd_d512<D512_DK>, dim3(KL->grid), dim3(C::THREADS), C::BYTES, s, mQ, mK, mV, mdO, p);
-    }
-    launches += 4;
+    const int4* splits = static_cast<const int4*>(KL->splits);
+    for (int m = 0; m < 2; ++m)
+      for (int h = 0; h < 2; ++h) {
+        p.half = h;
+        {
+          ProfScope ps(s, m == 0 ? "bwd_dv" : "bwd_dk");
+          if (m == 0)
+            launch_pdl(k_bwd_d512<D512_DV>, dim3(KL->grid), dim3(C::THREADS), C::BYTES, s, mQ, mK, mV, mdO, p);
+          else
+            launch_pdl(k_bwd_d512<D512_DK>, dim3(KL->grid), dim3(C::THREADS), C::BYTES, s, mQ, mK, mV, mdO, p);
+        }
+        ++launches;
+        if (KL->n_splits > 0) {
+          ProfScope ps(s, "bwd_dkdv_finalize");
+          launch_pdl(k_split_finalize<256>, dim3(KL->n_splits, 16), dim3(256), 0, s, splits, (const float*)partial,
+                     2 * D, T, Hkv, D, 256 * h, static_cast<__nv_bfloat16*>(m == 0 ? dV : dK));
+          ++launches;
+        }
+      }
   }
   // dQ: q-major lists and row masks
   p.ptr = bm->q_ptr;
@@ -2696,9 +2775,11 @@ int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const vo
       return launch_bwd<128>(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial,
                              partial_bytes, allow_build, s);
     case 256:
-      return launch_bwd_wide(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, allow_build, s);
+      return launch_bwd_wide(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial, partial_bytes,
+                             allow_build, s);
     case 512:
-      return launch_bwd_d512(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, allow_build, s);
+      return launch_bwd_d512(dO, Q, K, V, O, LSE, T, Hq, Hkv, scale, bm, dQ, dK, dV, delta, lse2, partial, partial_bytes,
+                             allow_build, s);
     default: set_error("tensor-core backward: head_dim %d not built", D); return 2;
   }
 }
