@@ -411,7 +411,7 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
 
     kernels = {}
     for name in ("blockmap_classify", "blockmap_lists", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
-                 "bwd_dkdv_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt"):
+                 "bwd_dkdv_finalize", "bwd_fused", "bwd_dq_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt"):
         n, ms = pt.profile_read(name)
         if n:
             kernels[name] = {"launches": n, "ms_per_launch": ms / n}
@@ -429,6 +429,7 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
     per_launch_flops = {  # useful-pair flops of each kernel: 2D per pair and head for each of its products
         "fwd_tc": 4.0 * D * Hq * pairs,
         "bwd_dkdv": 8.0 * D * Hq * pairs,
+        "bwd_fused": 10.0 * D * Hq * pairs,  # head_dim 64 one pass: S^T, dP^T, dV, dK, dQ
         "bwd_dv": (3.0 if wide2 else 4.0) * D * Hq * pairs,  # head_dim 256: S^T and dV
         "bwd_dk": (5.0 if wide2 else 6.0) * D * Hq * pairs,  # head_dim 256: S^T, dP^T and dK
         "bwd_dq": (5.0 if wide2 else 6.0) * D * Hq * pairs,

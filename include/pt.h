@@ -250,11 +250,18 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
 
 /* Bytes of scratch pt_attn_bwd needs: two fp32 row statistics of [Hq, Tpad]
  * entries each, Tpad = ceil(T / 128) * 128 -- Delta = rowsum(dO * O) and
- * LSE * log2(e) -- then room for fp32 partial sums, 128 x 2D floats per slot,
- * min(256, 2 * ceil(T/128) * Hq) slots, each part rounded up to 256 bytes.
- * The partial sums let the tensor-core backward split long kv-major columns
- * across SMs; a smaller workspace (at least the two statistics) is accepted
- * and only splits less. */
+ * LSE * log2(e) -- then, at head_dim 64 only, an fp32 dQ accumulator of
+ * Tpad * Hq * 64 floats, then room for fp32 partial sums, 128 x 2D floats
+ * per slot, min(256, 2 * ceil(T/128) * Hq) slots, each part rounded up to
+ * 256 bytes.  The partial sums let the tensor-core backward split long
+ * kv-major columns across SMs; a smaller workspace (at least the two
+ * statistics) is accepted and only splits less.
+ * At head_dim 64 (bf16, 128 x 128 tiles) a workspace with room for the dQ
+ * accumulator after the statistics selects the one-pass backward: dQ is
+ * summed in fp32 by asynchronous adds whose order varies, so dQ may differ
+ * between runs in its last bits.  A smaller workspace selects the two-pass
+ * backward, whose every output element is written once (run-to-run
+ * identical), with the rest of the workspace as partial-sum room. */
 size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
 
 /* ---------------------------------------------------------------------------
@@ -484,7 +491,8 @@ pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cud
  * (the default) costs one branch.  pt_profile_read synchronises the recorded
  * events and returns the number of launches and their summed duration for
  * one scope name: "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
- * "bwd_dkdv_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt",
+ * "bwd_dkdv_finalize", "bwd_fused" (the one-pass head_dim-64 backward),
+ * "bwd_dq_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt",
  * "blockmap_classify" (tile classes, list sizes, orders),
  * "blockmap_lists" (lists and masks), and the fold calls' "fold_plan",
  * "fold", "unfold", "unfold_grad", "fold_positions", "fold_mismatches".  pt_profile_reset drops every record

@@ -115,6 +115,26 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int T, int H, int D, int 
   return true;
 }
 
+bool make_tmap_acc32(CUtensorMap* map, float* base, int rows, int H) {
+  encode_tiled_fn enc = get_encode_tiled();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is unavailable from the driver");
+    return false;
+  }
+  cuuint64_t dims[3] = {64, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {64 * 4, (cuuint64_t)H * 64 * 4};
+  cuuint32_t box[3] = {32, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d) for the fp32 accumulator, rows=%d H=%d", (int)r, rows, H);
+    return false;
+  }
+  return true;
+}
+
 int num_sms(int device) {
   static int cache[64] = {0};
   if (device < 0 || device >= 64) return 148;
@@ -351,7 +371,10 @@ pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtyp
 size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D) {
   if (T <= 0 || Hq <= 0 || D <= 0) return 256;
   const size_t tpad = ((size_t)T + 127) / 128 * 128;
-  return 2 * round256(sizeof(float) * tpad * Hq) + round256(partial_slots(T, Hq) * 128 * 2 * sizeof(float) * D);
+  // head_dim 64: an fp32 dQ accumulator first, for the one-pass backward
+  const size_t dq_acc = D == 64 ? round256(sizeof(float) * tpad * Hq * D) : 0;
+  return 2 * round256(sizeof(float) * tpad * Hq) + dq_acc +
+         round256(partial_slots(T, Hq) * 128 * 2 * sizeof(float) * D);
 }
 
 pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE,

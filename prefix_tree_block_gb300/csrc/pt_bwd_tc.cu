@@ -64,7 +64,7 @@ template <int D>
 __global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restrict__ dO,
                                                   const __nv_bfloat16* __restrict__ O, const float* __restrict__ LSE,
                                                   int T, int Tpad, int Hq, float* __restrict__ delta,
-                                                  float* __restrict__ lse2) {
+                                                  float* __restrict__ lse2, float4* __restrict__ dq_acc) {
   pdl_wait();  // launched with programmatic dependent launch
   constexpr int VPT = D > 256 ? 2 : 1;  // 16-byte vectors of dO and O per thread (a row stays within a warp)
   constexpr int TPR = D / (8 * VPT);    // threads per (token, head) row
@@ -97,6 +97,10 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restric
 #pragma unroll
     for (int o = TPR / 2; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o, TPR);
     if (sub == 0) sh_delta[ql * (Hq + 1) + h] = s;
+  }
+  if (dq_acc) {  // the one-pass backward's fp32 dQ accumulator: these tokens' rows start at zero
+    float4* z = dq_acc + (size_t)q0 * Hq * (D / 4);
+    for (int i = threadIdx.x; i < rows * (D / 4); i += 256) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < rows; i += 256) {
@@ -157,6 +161,7 @@ struct BwdParams {
   const int4* dq_items;   // pipelined dq: q tile, head, first list entry, kv blocks; grouped by CTA
   const int4* dq_cta;     // pipelined dq: first item, end item, kv blocks of each CTA
   float* partial;         // dkdv: fp32 partial sums of split columns, [slot][128][2D]
+  float* dq_acc;          // one-pass kernel: fp32 dQ accumulator, [Tpad][Hq][D]
   int T, Tpad, Hq, Hkv, n_major, n_items;
   float scale, scale_log2;
   int half;  // head_dim 512 passes: which 256-column half of the output
@@ -252,6 +257,10 @@ struct BwdBars {
   uint64_t o_written;  // (dq) every compute thread has put its output rows into the staging tile
   uint64_t o_stored;   // (dq) the staging tile's TMA store has read it
   uint64_t ps_free;  // the accumulate MMAs have read the packed P/dS region
+  uint64_t dq_full;    // (one-pass kernel) a step's dQ product is in TMEM
+  uint64_t dq_free;    // (one-pass kernel) every compute thread has loaded it
+  uint64_t dq_staged;  // (one-pass kernel) every compute thread has staged its row half
+  uint64_t dq_sfree;   // (one-pass kernel) the reduce-adds have read the staging tile
 };
 
 template <int S>
@@ -274,6 +283,10 @@ __device__ __forceinline__ void init_bars(BwdBars<S>* b) {
   mbar_init(&b->o_written, 256);
   mbar_init(&b->o_stored, 1);
   mbar_init(&b->ps_free, 1);
+  mbar_init(&b->dq_full, 1);
+  mbar_init(&b->dq_free, 256);
+  mbar_init(&b->dq_staged, 256);
+  mbar_init(&b->dq_sfree, 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -693,6 +706,407 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 9) tmem_dealloc(tbase, 512);
+}
+
+// ---------------------------------------------------------------------------
+// 2b. dQ, dK and dV in one kv-major pass (head_dim 64)
+// ---------------------------------------------------------------------------
+// The kv-major kernel above with the q-major products folded in.  Each
+// step's dS^T also goes to shared memory, 128-byte swizzled, one 64-column
+// panel per compute warpgroup (kv rows x 64 q columns).  That one tile is
+// the K-major A operand of dK += dS^T Q and, read transposed, the MN-major A
+// operand of dQ_step = dS K, with K the resident tile.  dQ_step (128 q rows
+// x 64 fp32) lands in the TMEM columns that the packed dS^T needs no longer;
+// every compute thread puts its row half into a staging tile (two swizzled
+// 128 x 32 fp32 panels, one per warpgroup) and a reducer warp adds the tile
+// into an fp32 accumulator [Tpad][Hq][64] in the workspace with two tiled
+// TMA reduce-adds (a few large operations: the TMA unit takes bulk
+// operations one at a time, and one 128-byte operation per thread and step
+// kept it busier than the whole step).  The preprocess kernel zeroes the
+// accumulator and k_dq_finalize scales it and writes dQ as bf16.
+// Per kept pair the products fall from 14 D flop (S^T, dP^T, dV, dK here;
+// S, dP and dQ again in the q-major kernel) to 10 D, and the q-major
+// kernel's second exponential pass over every tile goes away.  The price is
+// dQ summed in fp32 in an order that varies from run to run.
+struct FusedL {
+  using C = BwdCfg<64>;
+  static constexpr int STAGES = 3;
+  static constexpr int OFF_K = 0, OFF_V = C::TILE;
+  static constexpr int OFF_ST = 2 * C::TILE;  // stages: Q | dO | lse2 | delta | column masks
+  static constexpr int ST_Q = 0, ST_DO = C::TILE, ST_L = 2 * C::TILE, ST_D = ST_L + 512, ST_M = ST_D + 512;
+  static constexpr int ST_BYTES = ST_M + 2048;
+  static constexpr int THREADS = 384;  // 8 compute warps, producer, two MMA warps, dQ reducer
+  static constexpr int OFF_DS = OFF_ST + STAGES * ST_BYTES;  // dS^T, two swizzled 64-column panels
+  static_assert(OFF_DS % 1024 == 0, "swizzled panel alignment");
+  // dQ staging: panel w = fp32 columns [32w, 32w + 32) of the 128 q rows,
+  // 128 bytes a row, 128-byte swizzled (the reduce-add's box layout)
+  static constexpr int OFF_DQ = OFF_DS + 2 * C::PANEL;
+  static constexpr int OFF_META = OFF_DQ + 2 * C::PANEL;
+  static constexpr int OFF_BAR = OFF_META + 64;
+  static constexpr int OFF_MISC = OFF_BAR + (int)sizeof(BwdBars<STAGES>);
+  static constexpr int BYTES = OFF_MISC + 16 + 1024;
+  static_assert(BYTES <= 232448, "shared memory budget");
+  // TMEM columns: S^T, dP^T (128 each), dV, dK, packed P^T, dQ_step (64 each)
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320, TM_P = 384, TM_DQ = 448;
+  static_assert(TM_DQ + 64 <= 512, "TMEM budget");
+};
+
+__global__ void __launch_bounds__(FusedL::THREADS, 1)
+    k_bwd_fused(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
+                const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                const __grid_constant__ CUtensorMap mAcc, const BwdParams p) {
+  pdl_wait();  // launched with programmatic dependent launch
+  constexpr int D = 64;
+  using C = BwdCfg<D>;
+  using L = FusedL;
+  constexpr int S = L::STAGES;
+  static_assert(C::TWO_ISSUERS, "warp roles");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdBars<S>* B = reinterpret_cast<BwdBars<S>*>(smem + L::OFF_BAR);
+  int* meta = reinterpret_cast<int*>(smem + L::OFF_META);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = p.Hq / p.Hkv;
+  const int w_begin = p.cta_ptr[blockIdx.x], w_end = p.cta_ptr[blockIdx.x + 1];
+
+  if (threadIdx.x == 256) {
+    init_bars<S>(B);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mQ);
+    prefetch_tmap(&mdO);
+    prefetch_tmap(&mK);
+    prefetch_tmap(&mV);
+    prefetch_tmap(&mAcc);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t sc = 0, it = 0;
+      bool ok = true, res_issued = false;
+      for (int w = w_begin; w < w_end && ok; ++w) {
+        const DkdvItem itm = p.items[w];
+        const int jb = itm.jb, hk = itm.hk;
+        const int e0 = p.ptr[jb], ncol = p.ptr[jb + 1] - e0;
+        if (itm.x1 == itm.x0) continue;
+        if (it > 0 && !(ok = mbar_wait(&B->res_empty, (it - 1) & 1, abort_flag))) break;
+        mbar_expect_tx(&B->res_full, 2 * C::TILE);
+        tma_load_3d(smem + L::OFF_K, &mK, &B->res_full, 0, hk, jb * 128);
+        tma_load_3d(smem + L::OFF_V, &mV, &B->res_full, 0, hk, jb * 128);
+        res_issued = true;
+        const int n = itm.x1 - itm.x0;
+        for (int x = 0; x < n; ++x) {
+          const int e = e0 + (itm.x0 + x) % ncol;
+          const int h = hk * g + (itm.x0 + x) / ncol, i = p.idx[e], slot = p.pidx[e];
+          const uint32_t s = sc % S, u = sc / S;
+          if (u > 0 && !(ok = mbar_wait(&B->st_empty[s], (u - 1) & 1, abort_flag))) break;
+          uint8_t* st = smem + L::OFF_ST + s * L::ST_BYTES;
+          meta[s] = slot;
+          mbar_expect_tx(&B->st_full[s], 2 * C::TILE + 1024 + (slot >= 0 ? 2048 : 0));
+          tma_load_3d(st + L::ST_Q, &mQ, &B->st_full[s], 0, h, i * 128);
+          tma_load_3d(st + L::ST_DO, &mdO, &B->st_full[s], 0, h, i * 128);
+          bulk_load(st + L::ST_L, p.lse2 + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
+          bulk_load(st + L::ST_D, p.delta + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
+          if (slot >= 0) bulk_load(st + L::ST_M, p.masks + (size_t)slot * 512, 2048, &B->st_full[s]);
+          ++sc;
+        }
+        ++it;
+      }
+      if (!ok) {
+        const long long lim = 20000000;
+        if (res_issued) mbar_wait_drain(&B->res_full, it & 1, lim);
+        for (uint32_t s = 0; s < S && s < sc; ++s) {
+          uint32_t last = sc - 1 - ((sc - 1 - s) % S);
+          mbar_wait_drain(&B->st_full[s], (last / S) & 1, lim);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ S^T / dP^T issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+      const uint32_t sK = smem_u32(smem + L::OFF_K), sV = smem_u32(smem + L::OFF_V);
+      const uint32_t sST = smem_u32(smem + L::OFF_ST);
+      uint32_t sc = 0, it = 0;
+      bool ok = true;
+      for (int w = w_begin; w < w_end && ok; ++w) {
+        const DkdvItem itm = p.items[w];
+        const int n = itm.x1 - itm.x0;
+        if (n == 0) continue;
+        if (!(ok = mbar_wait(&B->res_full, it & 1, abort_flag))) break;
+        tc_fence_after();
+        // S^T(x) = K Q^T and dP^T(x) = V dO^T once the stage is in and the
+        // compute warpgroups have loaded S^T(x-1) and dP^T(x-1)
+        for (int x = 0; x < n && ok; ++x) {
+          const uint32_t y = sc + x, s = y % S;
+          uint64_t* bars[2] = {&B->st_full[s], y >= 1 ? &B->s_free : nullptr};
+          const uint32_t par[2] = {(y / S) & 1, (y - 1) & 1};
+          if (!(ok = mbar_wait_all<2>(bars, par, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t st = sST + s * L::ST_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tbase + L::TM_S, sdesc_sw128(sK + kk * 32, 16, 1024), sdesc_sw128(st + L::ST_Q + kk * 32, 16, 1024),
+                   IDESC_S, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tbase + L::TM_DP, sdesc_sw128(sV + kk * 32, 16, 1024), sdesc_sw128(st + L::ST_DO + kk * 32, 16, 1024),
+                   IDESC_S, kk > 0);
+          mma_commit(&B->s_full[0]);
+        }
+        sc += n;
+        ++it;
+      }
+      mma_commit(&B->mma_done);
+      mbar_wait_drain(&B->mma_done, 0, 200000000);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dV / dK / dQ issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);  // A K-major (or TMEM), B MN-major
+      constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, true, true);    // A = dS read transposed (MN-major)
+      const uint32_t sK = smem_u32(smem + L::OFF_K), sDS = smem_u32(smem + L::OFF_DS);
+      const uint32_t sST = smem_u32(smem + L::OFF_ST);
+      uint32_t sc = 0, it = 0;
+      bool ok = true;
+      for (int w = w_begin; w < w_end && ok; ++w) {
+        const DkdvItem itm = p.items[w];
+        const int n = itm.x1 - itm.x0;
+        if (n == 0) continue;
+        for (int x = 0; x < n && ok; ++x) {
+          // step x once the compute warpgroups have written packed P^T and
+          // dS^T (and, on an item's first step, read the previous item's
+          // accumulators)
+          const uint32_t y = sc + x, sp = y % S;
+          uint64_t* bars[3] = {&B->st_full[sp], &B->p_full[0], (x == 0 && it > 0) ? &B->acc_free : nullptr};
+          const uint32_t par[3] = {(y / S) & 1, y & 1, (it - 1) & 1};
+          if (!(ok = mbar_wait_all<3>(bars, par, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t stp = sST + sp * L::ST_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO (A from TMEM; K = 128 q rows)
+            mma_ts(tbase + L::TM_DV, tbase + L::TM_P + kk * 8, sdesc_sw128(stp + L::ST_DO + kk * 2048, C::PANEL, 1024),
+                   IDESC_ACC, x > 0 || kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q (A: the q-column panels of dS^T)
+            mma_ss(tbase + L::TM_DK, sdesc_sw128(sDS + (kk >> 2) * C::PANEL + (kk & 3) * 32, 16, 1024),
+                   sdesc_sw128(stp + L::ST_Q + kk * 2048, C::PANEL, 1024), IDESC_ACC, x > 0 || kk > 0);
+          if (x == n - 1) mma_commit(&B->acc_full);
+          // dQ_step = dS K (M = 128 q rows, K = 128 kv rows) once the compute
+          // threads have loaded the previous step's
+          if (y > 0 && !(ok = mbar_wait(&B->dq_free, (y - 1) & 1, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tbase + L::TM_DQ, sdesc_sw128(sDS + kk * 2048, C::PANEL, 1024), sdesc_sw128(sK + kk * 2048, C::PANEL, 1024),
+                   IDESC_DQ, kk > 0);
+          mma_commit(&B->dq_full);
+          mma_commit(&B->ps_free);
+          mma_commit(&B->st_empty[sp]);
+          // dQ reads the resident K: the item's tiles are free after its last dQ
+          // (S^T and dP^T of that step were complete before its P^T existed)
+          if (x == n - 1) mma_commit(&B->res_empty);
+        }
+        sc += n;
+        ++it;
+      }
+      mma_commit(&B->mma_done2);
+      mbar_wait_drain(&B->mma_done2, 0, 200000000);
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ dQ reducer
+    if (lane == 0) {
+      uint32_t y = 0;
+      bool ok = true;
+      for (int w = w_begin; w < w_end && ok; ++w) {
+        const DkdvItem itm = p.items[w];
+        const int e0 = p.ptr[itm.jb], ncol = p.ptr[itm.jb + 1] - e0;
+        for (int x = itm.x0; x < itm.x1; ++x, ++y) {
+          // step y's dQ tile is staged: add its two panels into the accumulator
+          // rows of its q tile and head, then free the staging once read
+          const int i = p.idx[e0 + x % ncol], h = itm.hk * g + x / ncol;
+          if (!(ok = mbar_wait(&B->dq_staged, y & 1, abort_flag))) break;
+          tma_reduce_add_3d(&mAcc, smem + L::OFF_DQ, 0, h, i * 128);
+          tma_reduce_add_3d(&mAcc, smem + L::OFF_DQ + C::PANEL, 32, h, i * 128);
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&B->dq_sfree);
+        }
+      }
+      bulk_wait0();
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute (kv row per thread)
+    const int hw = warp >> 2;  // which 64 q columns of each step this warpgroup takes
+    const int r = threadIdx.x & 127;
+    const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t tS = tl + L::TM_S + 64 * hw, tP = tl + L::TM_DP + 64 * hw;
+    uint4* ds_row = reinterpret_cast<uint4*>(smem + L::OFF_DS + hw * C::PANEL + r * 128);
+    uint4* dq_row = reinterpret_cast<uint4*>(smem + L::OFF_DQ + hw * C::PANEL + r * 128);
+    const int r7 = r & 7;
+    uint32_t sc = 0, it = 0;
+    bool ok = true;
+    // dQ of step y: load this thread's row half from TMEM, release the
+    // columns, stage it for the reducer once the previous tile has been read
+    const auto dq_out = [&](uint32_t y) -> bool {
+      bool good = mbar_wait(&B->dq_full, y & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, good)) return false;
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld32(tl + L::TM_DQ + 32 * hw, v);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&B->dq_free);
+      good = y == 0 || mbar_wait(&B->dq_sfree, (y - 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, good)) return false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dq_row[k ^ r7] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      fence_proxy_async_smem();  // visible to the reducer's TMA
+      mbar_arrive(&B->dq_staged);
+      return true;
+    };
+    for (int w = w_begin; w < w_end && ok; ++w) {
+      const DkdvItem itm = p.items[w];
+      const int jb = itm.jb, hk = itm.hk;
+      const int n = itm.x1 - itm.x0;
+      const int kv = jb * 128 + r;
+      __nv_bfloat16* orow = (hw ? p.out0 : p.out1) + ((size_t)kv * p.Hkv + hk) * D;  // wg0: dV, wg1: dK
+      if (n == 0) {
+        if (kv < p.T) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+        }
+        continue;
+      }
+      for (int x = 0; x < n; ++x) {
+        const uint32_t y = sc + x, s = y % S;
+        ok = mbar_wait(&B->s_full[0], y & 1, abort_flag) && mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* st = smem + L::OFF_ST + s * L::ST_BYTES;
+        const float4* l2 = reinterpret_cast<const float4*>(st + L::ST_L) + hw * 16;
+        const float4* dl = reinterpret_cast<const float4*>(st + L::ST_D) + hw * 16;
+        const int slot = meta[s];
+        uint2 mk = make_uint2(0xffffffffu, 0xffffffffu);
+        if (slot >= 0) mk = reinterpret_cast<const uint2*>(st + L::ST_M)[2 * r + hw];
+        uint32_t pk[32], pk2[32];
+        {
+          uint32_t sr[64], dr[64];
+          tmem_ld32(tS, sr);
+          tmem_ld32(tS + 32, sr + 32);
+          tmem_ld32(tP, dr);
+          tmem_ld32(tP + 32, dr + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&B->s_free);  // S^T and dP^T are in registers: the MMA may reuse them
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 lv = l2[c4], dv = dl[c4];
+            const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int c = c4 * 4 + k;
+              const uint32_t word = c < 32 ? mk.x : mk.y;
+              float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
+              pv[k] = ((word >> (c & 31)) & 1u) ? pr : 0.f;
+              dsv[k] = pv[k] * (__uint_as_float(dr[c]) - da[k]);
+            }
+            pk[2 * c4] = pack_bf16(pv[0], pv[1]);
+            pk[2 * c4 + 1] = pack_bf16(pv[2], pv[3]);
+            pk2[2 * c4] = pack_bf16(dsv[0], dsv[1]);
+            pk2[2 * c4 + 1] = pack_bf16(dsv[2], dsv[3]);
+          }
+        }
+        // the previous step's dV, dK and dQ products must be done reading
+        // packed P^T and the dS^T panels
+        if (y > 0) {
+          ok = mbar_wait(&B->ps_free, (y - 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(tl + L::TM_P + 32 * hw, pk);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the row goes to chunk c ^ (row & 7): the 128-byte swizzle
+          ds_row[c ^ r7] = make_uint4(pk2[4 * c], pk2[4 * c + 1], pk2[4 * c + 2], pk2[4 * c + 3]);
+        fence_proxy_async_smem();  // visible to the tensor core's shared-memory reads
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&B->p_full[0]);
+        if (y > 0 && !(ok = dq_out(y - 1))) break;
+      }
+      if (!ok) break;
+      ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float mul = hw ? p.scale : 1.f;
+      const uint32_t acc = hw ? L::TM_DK : L::TM_DV;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tl + acc + c * 32, v);
+        tmem_ld_wait();
+        if (itm.slot < 0) {
+          if (kv < p.T) store_row32(orow + c * 32, v, mul);
+        } else {  // one chunk of a split column: fp32 partial sums, summed later in chunk order
+          float4* prow = reinterpret_cast<float4*>(p.partial + ((size_t)itm.slot * 128 + r) * (2 * D) + (hw ? D : 0) +
+                                                   c * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            prow[k] = make_float4(__uint_as_float(v[4 * k]) * mul, __uint_as_float(v[4 * k + 1]) * mul,
+                                  __uint_as_float(v[4 * k + 2]) * mul, __uint_as_float(v[4 * k + 3]) * mul);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&B->acc_free);
+      sc += n;
+      ++it;
+    }
+    if (ok && sc > 0) ok = dq_out(sc - 1);  // the last step's dQ
+    if (!ok) *abort_flag = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tbase, 512);
+}
+
+// dQ = scale * the one-pass kernel's fp32 accumulator, as bf16: n8 runs of 8
+// values (the rows below T come first in the accumulator's [Tpad][Hq][D]).
+__global__ void __launch_bounds__(256) k_dq_finalize(const float4* __restrict__ acc, size_t n8, float scale,
+                                                     uint4* __restrict__ dQ) {
+  pdl_wait();  // launched with programmatic dependent launch
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    dQ[i] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                       pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -2421,10 +2835,24 @@ template <int D>
 int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
                int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
                float* lse2, float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s) {
-  static int set_dkdv[64] = {0}, set_dq[64] = {0};
+  static int set_dkdv[64] = {0}, set_dq[64] = {0}, set_fused[64] = {0};
   const int dev = bm->device;
-  int rc = reserve_smem(k_bwd_dkdv<D>, DkdvL<D>::BYTES, dev, set_dkdv);
-  if (!rc) {
+  const int Tpad = bm->nq * 128;
+  // head_dim 64 with room in the workspace for an fp32 dQ accumulator: the
+  // one-pass kernel (dQ summed in an order that varies between runs); else
+  // the kv-major and q-major kernels, each output element written once
+  float* dq_acc = nullptr;
+  if constexpr (D == 64) {
+    const size_t dq_bytes = sizeof(float) * (size_t)Tpad * Hq * D;
+    if (partial && partial_bytes >= dq_bytes) {
+      dq_acc = partial;
+      partial = reinterpret_cast<float*>(reinterpret_cast<char*>(partial) + dq_bytes);
+      partial_bytes -= dq_bytes;
+    }
+  }
+  int rc = dq_acc ? reserve_smem(k_bwd_fused, FusedL::BYTES, dev, set_fused)
+                  : reserve_smem(k_bwd_dkdv<D>, DkdvL<D>::BYTES, dev, set_dkdv);
+  if (!rc && !dq_acc) {
     if constexpr (D == 128)
       rc = reserve_smem(k_bwd_dq_pipe<D>, DqpL<D>::BYTES, dev, set_dq);
     else
@@ -2441,7 +2869,6 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s, &KL))) return rc;
   const pt_dq_lists* QL = nullptr;
   if (D == 128 && (rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
-  const int Tpad = bm->nq * 128;
   {
     const size_t sm = sizeof(float) * kPrepTokens * ((size_t)Hq + 1);
     if (sm > 48 * 1024 &&
@@ -2450,7 +2877,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       return 3;
     }
     ProfScope ps(s, "bwd_prep");
-    launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s, static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
+    launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s, static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2, reinterpret_cast<float4*>(dq_acc));
   }
   CUtensorMap mQ, mdO, mK, mV, mdQ;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128) ||
@@ -2479,16 +2906,38 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   p.n_items = KL->n_items;
   p.cta_ptr = static_cast<const int*>(KL->cta);
   p.partial = partial;
+  p.dq_acc = dq_acc;
   int launches = 1;
   if (p.n_items > 0) {
-    ProfScope ps(s, "bwd_dkdv");
-    launch_pdl(k_bwd_dkdv<D>, dim3(KL->grid), dim3(BwdCfg<D>::THREADS), DkdvL<D>::BYTES, s, mQ, mdO, mK, mV, p);
+    if (dq_acc) {
+      CUtensorMap mAcc;
+      if (!make_tmap_acc32(&mAcc, dq_acc, Tpad, Hq)) return 3;
+      ProfScope ps(s, "bwd_fused");
+      launch_pdl(k_bwd_fused, dim3(KL->grid), dim3(FusedL::THREADS), FusedL::BYTES, s, mQ, mdO, mK, mV, mAcc, p);
+    } else {
+      ProfScope ps(s, "bwd_dkdv");
+      launch_pdl(k_bwd_dkdv<D>, dim3(KL->grid), dim3(BwdCfg<D>::THREADS), DkdvL<D>::BYTES, s, mQ, mdO, mK, mV, p);
+    }
     ++launches;
   }
   if (KL->n_splits > 0) {
     ProfScope ps(s, "bwd_dkdv_finalize");
     launch_pdl(k_dkdv_finalize<D>, dim3(dim3(KL->n_splits, 16)), dim3(256), 0, s, static_cast<const int4*>(KL->splits), partial, T, Hkv, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
     ++launches;
+  }
+  if (dq_acc) {
+    const size_t n8 = (size_t)T * Hq * D / 8;
+    const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
+    ProfScope ps(s, "bwd_dq_finalize");
+    launch_pdl(k_dq_finalize, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(dq_acc), n8, scale,
+               static_cast<uint4*>(dQ));
+    count_launch(launches + 1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      set_error("backward launch failed: %s", cudaGetErrorString(e));
+      return 3;
+    }
+    return 0;
   }
   // dQ
   p.ptr = bm->q_ptr;
@@ -2558,7 +3007,7 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
       return 3;
     }
     ProfScope ps(s, "bwd_prep");
-    launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s, static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2);
+    launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s, static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta, lse2, static_cast<float4*>(nullptr));
   }
   CUtensorMap mQ, mdO, mK, mV, mQh, mdOh, mKh, mVh;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128) ||
@@ -2674,7 +3123,7 @@ int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V,
     ProfScope ps(s, "bwd_prep");
     launch_pdl(k_bwd_prep<D>, dim3((unsigned)(Tpad / kPrepTokens)), dim3(256), sm, s,
                static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(O), LSE, T, Tpad, Hq, delta,
-               lse2);
+               lse2, static_cast<float4*>(nullptr));
   }
   CUtensorMap mQ, mK, mV, mdO;
   if (!make_tmap_thd(&mQ, Q, T, Hq, D, 128) || !make_tmap_thd(&mK, K, T, Hkv, D, 128) ||

@@ -212,6 +212,8 @@ encode_tiled_fn get_encode_tiled();
 // A [T, H, D] bf16 tensor as a 3-D TMA map with boxes of 64 (d) x 1 (head) x
 // rows (tokens), 128-byte swizzle.  Returns false (and sets the error) on failure.
 bool make_tmap_thd(CUtensorMap* map, const void* base, int T, int H, int D, int rows);
+// fp32 [rows][H][64], boxes of 32 columns x 1 head x 128 rows, 128-byte swizzle
+bool make_tmap_acc32(CUtensorMap* map, float* base, int rows, int H);
 
 int num_sms(int device);
 

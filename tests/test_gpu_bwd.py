@@ -77,3 +77,42 @@ def test_workload_sampled(c):
     assert rel_l2(dV.sum(axis=0), sdo) <= GRAD_RL2["bf16"]
     scale_k = np.abs(dK).sum(axis=0).max()
     assert np.abs(dK.sum(axis=0)).max() <= 1e-2 * scale_k
+
+
+@pytest.mark.parametrize("name", ["grpo", "grpo_p0", "tree", "docs"])
+def test_head_dim_64_one_pass_and_two_pass(name):
+    """At head_dim 64 the workspace picks the backward: with room for the
+    fp32 dQ accumulator the one-pass kernel (dQ added up by asynchronous
+    reduce-adds), with the two row statistics alone the kv-major and q-major
+    kernels.  Both match the oracle and each other, and each launches the
+    kernels it should."""
+    import prefix_tree_block_gb300 as pt
+    import torch
+
+    st = small_structures()[name]
+    Hq, Hkv, D = 4, 2, 64
+    q, k, v, do = W.make_tensors(st.T, Hq, Hkv, D, "bf16", seed=11)
+    Q, K, V, dO = (x.cuda() for x in (q, k, v, do))
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes)
+    O, LSE = pt.attn_fwd(Q, K, V, bm)
+    tpad = -(-st.T // 128) * 128
+    stats = 2 * (-(-(4 * tpad * Hq) // 256) * 256)
+    full = torch.empty(pt.bwd_workspace_bytes(st.T, Hq, D), dtype=torch.uint8, device="cuda")
+    small = torch.empty(stats, dtype=torch.uint8, device="cuda")
+    want = orc.attn_bwd(q, k, v, do, orc.structure_labels(st))
+    got = {}
+    for label, ws in (("one", full), ("two", small)):
+        pt.profile_reset()
+        pt.profile_enable(True)
+        res = pt.attn_bwd(dO, Q, K, V, O, LSE, bm, workspace=ws)
+        pt.sync_status()
+        n_fused = pt.profile_read("bwd_fused")[0]
+        n_dq = pt.profile_read("bwd_dq")[0]
+        pt.profile_enable(False)
+        assert (n_fused, n_dq) == ((1, 0) if label == "one" else (0, 1))
+        got[label] = [x.float().cpu().numpy() for x in res]
+        for g, w in zip(got[label], want):
+            assert rel_l2(g, w) <= GRAD_RL2["bf16"]
+    for a, b in zip(got["one"], got["two"]):
+        assert rel_l2(a, b) <= 1e-2
+    bm.free()
