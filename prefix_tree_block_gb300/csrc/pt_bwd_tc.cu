@@ -258,9 +258,11 @@ struct BwdBars {
   uint64_t o_stored;   // (dq) the staging tile's TMA store has read it
   uint64_t ps_free;  // the accumulate MMAs have read the packed P/dS region
   uint64_t dq_full;    // (one-pass kernel) a step's dQ product is in TMEM
-  uint64_t dq_free;    // (one-pass kernel) every compute thread has loaded it
-  uint64_t dq_staged;  // (one-pass kernel) every compute thread has staged its row half
+  uint64_t dq_free;    // (one-pass kernel) the dQ warpgroup has loaded it
+  uint64_t dq_staged;  // (one-pass kernel) the dQ warpgroup has staged it
   uint64_t dq_sfree;   // (one-pass kernel) the reduce-adds have read the staging tile
+  uint64_t ps_free2;   // (one-pass kernel) dV/dK and dQ have both read packed P^T and dS^T
+  uint64_t mma_done3;  // (one-pass kernel) the dQ MMA warp's MMAs are complete
 };
 
 template <int S>
@@ -284,9 +286,11 @@ __device__ __forceinline__ void init_bars(BwdBars<S>* b) {
   mbar_init(&b->o_stored, 1);
   mbar_init(&b->ps_free, 1);
   mbar_init(&b->dq_full, 1);
-  mbar_init(&b->dq_free, 256);
-  mbar_init(&b->dq_staged, 256);
+  mbar_init(&b->dq_free, 128);  // the dQ epilogue warpgroup
+  mbar_init(&b->dq_staged, 128);
   mbar_init(&b->dq_sfree, 1);
+  mbar_init(&b->ps_free2, 2);  // one commit from each accumulating MMA warp
+  mbar_init(&b->mma_done3, 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -716,14 +720,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 // panel per compute warpgroup (kv rows x 64 q columns).  That one tile is
 // the K-major A operand of dK += dS^T Q and, read transposed, the MN-major A
 // operand of dQ_step = dS K, with K the resident tile.  dQ_step (128 q rows
-// x 64 fp32) lands in the TMEM columns that the packed dS^T needs no longer;
-// every compute thread puts its row half into a staging tile (two swizzled
-// 128 x 32 fp32 panels, one per warpgroup) and a reducer warp adds the tile
-// into an fp32 accumulator [Tpad][Hq][64] in the workspace with two tiled
-// TMA reduce-adds (a few large operations: the TMA unit takes bulk
-// operations one at a time, and one 128-byte operation per thread and step
-// kept it busier than the whole step).  The preprocess kernel zeroes the
-// accumulator and k_dq_finalize scales it and writes dQ as bf16.
+// x 64 fp32) lands in the TMEM columns that the packed dS^T needs no longer.
+// Three MMA warps issue S^T/dP^T, dV/dK and dQ: the tensor pipe overlaps one
+// thread's chain into an accumulator with another's, where one thread
+// switching between accumulators would leave it idle.  A fourth warpgroup
+// loads dQ_step (a q row per thread) into a staging tile (two swizzled
+// 128 x 32 fp32 panels), and one of its threads adds the tile into an fp32
+// accumulator [Tpad][Hq][64] in the workspace with two tiled TMA reduce-adds
+// (a few large operations: the TMA unit takes bulk operations one at a time,
+// and one 128-byte operation per thread and step kept it busier than the
+// whole step).  The compute warpgroups, whose exponentials and packing bound
+// the step, thus do no dQ work.  Registers are moved to them from the other
+// two warpgroups (setmaxnreg).  The preprocess kernel zeroes the accumulator
+// and k_dq_finalize scales it and writes dQ as bf16.
 // Per kept pair the products fall from 14 D flop (S^T, dP^T, dV, dK here;
 // S, dP and dQ again in the q-major kernel) to 10 D, and the q-major
 // kernel's second exponential pass over every tile goes away.  The price is
@@ -735,7 +744,12 @@ struct FusedL {
   static constexpr int OFF_ST = 2 * C::TILE;  // stages: Q | dO | lse2 | delta | column masks
   static constexpr int ST_Q = 0, ST_DO = C::TILE, ST_L = 2 * C::TILE, ST_D = ST_L + 512, ST_M = ST_D + 512;
   static constexpr int ST_BYTES = ST_M + 2048;
-  static constexpr int THREADS = 384;  // 8 compute warps, producer, two MMA warps, dQ reducer
+  // warpgroups: two compute; producer and three MMA warps; dQ epilogue
+  static constexpr int THREADS = 512;
+  // registers per thread after reallocation; they add up to the launch's
+  // 128 per thread (the kernel must be built with exactly 128)
+  static constexpr int REG_COMPUTE = 176, REG_CTRL = 72, REG_DQ = 88, REG_LAUNCH = 128;
+  static_assert(2 * REG_COMPUTE + REG_CTRL + REG_DQ == 4 * REG_LAUNCH, "register split");
   static constexpr int OFF_DS = OFF_ST + STAGES * ST_BYTES;  // dS^T, two swizzled 64-column panels
   static_assert(OFF_DS % 1024 == 0, "swizzled panel alignment");
   // dQ staging: panel w = fp32 columns [32w, 32w + 32) of the 128 q rows,
@@ -791,6 +805,8 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp >= 8 && warp < 12) {
+  regs_dec<L::REG_CTRL>();  // the whole warpgroup, before its warps take their roles
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -875,11 +891,10 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 10) {
-    // ------------------------------------------------------------ dV / dK / dQ issuer
+    // ------------------------------------------------------------ dV / dK issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);  // A K-major (or TMEM), B MN-major
-      constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, true, true);    // A = dS read transposed (MN-major)
-      const uint32_t sK = smem_u32(smem + L::OFF_K), sDS = smem_u32(smem + L::OFF_DS);
+      const uint32_t sDS = smem_u32(smem + L::OFF_DS);
       const uint32_t sST = smem_u32(smem + L::OFF_ST);
       uint32_t sc = 0, it = 0;
       bool ok = true;
@@ -906,20 +921,8 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
             mma_ss(tbase + L::TM_DK, sdesc_sw128(sDS + (kk >> 2) * C::PANEL + (kk & 3) * 32, 16, 1024),
                    sdesc_sw128(stp + L::ST_Q + kk * 2048, C::PANEL, 1024), IDESC_ACC, x > 0 || kk > 0);
           if (x == n - 1) mma_commit(&B->acc_full);
-          // dQ_step = dS K (M = 128 q rows, K = 128 kv rows) once the compute
-          // threads have loaded the previous step's
-          if (y > 0 && !(ok = mbar_wait(&B->dq_free, (y - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tbase + L::TM_DQ, sdesc_sw128(sDS + kk * 2048, C::PANEL, 1024), sdesc_sw128(sK + kk * 2048, C::PANEL, 1024),
-                   IDESC_DQ, kk > 0);
-          mma_commit(&B->dq_full);
-          mma_commit(&B->ps_free);
+          mma_commit(&B->ps_free2);
           mma_commit(&B->st_empty[sp]);
-          // dQ reads the resident K: the item's tiles are free after its last dQ
-          // (S^T and dP^T of that step were complete before its P^T existed)
-          if (x == n - 1) mma_commit(&B->res_empty);
         }
         sc += n;
         ++it;
@@ -929,58 +932,116 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 11) {
-    // ------------------------------------------------------------ dQ reducer
+    // ------------------------------------------------------------ dQ issuer
     if (lane == 0) {
-      uint32_t y = 0;
+      constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, true, true);  // A = dS read transposed (MN-major)
+      const uint32_t sK = smem_u32(smem + L::OFF_K), sDS = smem_u32(smem + L::OFF_DS);
+      uint32_t sc = 0, it = 0;
       bool ok = true;
       for (int w = w_begin; w < w_end && ok; ++w) {
         const DkdvItem itm = p.items[w];
-        const int e0 = p.ptr[itm.jb], ncol = p.ptr[itm.jb + 1] - e0;
-        for (int x = itm.x0; x < itm.x1; ++x, ++y) {
-          // step y's dQ tile is staged: add its two panels into the accumulator
-          // rows of its q tile and head, then free the staging once read
-          const int i = p.idx[e0 + x % ncol], h = itm.hk * g + x / ncol;
-          if (!(ok = mbar_wait(&B->dq_staged, y & 1, abort_flag))) break;
-          tma_reduce_add_3d(&mAcc, smem + L::OFF_DQ, 0, h, i * 128);
-          tma_reduce_add_3d(&mAcc, smem + L::OFF_DQ + C::PANEL, 32, h, i * 128);
-          bulk_commit();
+        const int n = itm.x1 - itm.x0;
+        if (n == 0) continue;
+        if (!(ok = mbar_wait(&B->res_full, it & 1, abort_flag))) break;
+        for (int x = 0; x < n && ok; ++x) {
+          // dQ_step = dS K (M = 128 q rows, K = 128 kv rows) once dS^T is in
+          // shared memory and the dQ warpgroup has loaded the previous step's
+          const uint32_t y = sc + x;
+          uint64_t* bars[2] = {&B->p_full[0], y > 0 ? &B->dq_free : nullptr};
+          const uint32_t par[2] = {y & 1, (y - 1) & 1};
+          if (!(ok = mbar_wait_all<2>(bars, par, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tbase + L::TM_DQ, sdesc_sw128(sDS + kk * 2048, C::PANEL, 1024), sdesc_sw128(sK + kk * 2048, C::PANEL, 1024),
+                   IDESC_DQ, kk > 0);
+          mma_commit(&B->dq_full);
+          mma_commit(&B->ps_free2);
+          // dQ reads the resident K: the item's tiles are free after its last dQ
+          // (S^T and dP^T of that step were complete before its P^T existed)
+          if (x == n - 1) mma_commit(&B->res_empty);
+        }
+        sc += n;
+        ++it;
+      }
+      mma_commit(&B->mma_done3);
+      mbar_wait_drain(&B->mma_done3, 0, 200000000);
+    }
+    __syncwarp();
+  }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ epilogue (q row per thread)
+    regs_dec<L::REG_DQ>();
+    const int r = threadIdx.x & 127, r7 = r & 7;
+    const bool leader = r == 0;  // issues the reduce-adds
+    const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    uint4* row0 = reinterpret_cast<uint4*>(smem + L::OFF_DQ + r * 128);
+    uint4* row1 = reinterpret_cast<uint4*>(smem + L::OFF_DQ + C::PANEL + r * 128);
+    uint32_t y = 0;
+    bool ok = true;
+    for (int w = w_begin; w < w_end && ok; ++w) {
+      const DkdvItem itm = p.items[w];
+      const int e0 = p.ptr[itm.jb], ncol = p.ptr[itm.jb + 1] - e0;
+      for (int x = itm.x0; x < itm.x1; ++x, ++y) {
+        // step y's dQ: load it and release the TMEM columns; stage it once the
+        // previous tile's reduce-adds have read the staging tile; then add the
+        // tile into the accumulator rows of its q tile and head
+        ok = mbar_wait(&B->dq_full, y & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[32], u[32];
+        tmem_ld32(tl + L::TM_DQ, v);
+        tmem_ld32(tl + L::TM_DQ + 32, u);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&B->dq_free);
+        if (leader && y > 0) {
           bulk_wait_read0();
           mbar_arrive(&B->dq_sfree);
         }
+        ok = y == 0 || mbar_wait(&B->dq_sfree, (y - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 16-byte chunk k of a 128-byte row goes to chunk k ^ (row & 7)
+          row0[k ^ r7] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          row1[k ^ r7] = make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+        }
+        fence_proxy_async_smem();  // visible to the TMA
+        mbar_arrive(&B->dq_staged);
+        if (leader) {
+          const int i = p.idx[e0 + x % ncol], h = itm.hk * g + x / ncol;
+          ok = mbar_wait(&B->dq_staged, y & 1, abort_flag);
+          if (ok) {
+            tma_reduce_add_3d(&mAcc, smem + L::OFF_DQ, 0, h, i * 128);
+            tma_reduce_add_3d(&mAcc, smem + L::OFF_DQ + C::PANEL, 32, h, i * 128);
+            bulk_commit();
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {  // the leader's warp leaves together
+          ok = false;
+          break;
+        }
       }
-      bulk_wait0();
     }
-    __syncwarp();
+    if (leader) bulk_wait0();
+    if (!ok) *abort_flag = 1;
   } else {
     // ------------------------------------------------------------ compute (kv row per thread)
+    regs_inc<L::REG_COMPUTE>();
     const int hw = warp >> 2;  // which 64 q columns of each step this warpgroup takes
     const int r = threadIdx.x & 127;
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t tS = tl + L::TM_S + 64 * hw, tP = tl + L::TM_DP + 64 * hw;
     uint4* ds_row = reinterpret_cast<uint4*>(smem + L::OFF_DS + hw * C::PANEL + r * 128);
-    uint4* dq_row = reinterpret_cast<uint4*>(smem + L::OFF_DQ + hw * C::PANEL + r * 128);
     const int r7 = r & 7;
     uint32_t sc = 0, it = 0;
     bool ok = true;
-    // dQ of step y: load this thread's row half from TMEM, release the
-    // columns, stage it for the reducer once the previous tile has been read
-    const auto dq_out = [&](uint32_t y) -> bool {
-      bool good = mbar_wait(&B->dq_full, y & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, good)) return false;
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(tl + L::TM_DQ + 32 * hw, v);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&B->dq_free);
-      good = y == 0 || mbar_wait(&B->dq_sfree, (y - 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, good)) return false;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) dq_row[k ^ r7] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-      fence_proxy_async_smem();  // visible to the reducer's TMA
-      mbar_arrive(&B->dq_staged);
-      return true;
-    };
     for (int w = w_begin; w < w_end && ok; ++w) {
       const DkdvItem itm = p.items[w];
       const int jb = itm.jb, hk = itm.hk;
@@ -1040,7 +1101,7 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
         // the previous step's dV, dK and dQ products must be done reading
         // packed P^T and the dS^T panels
         if (y > 0) {
-          ok = mbar_wait(&B->ps_free, (y - 1) & 1, abort_flag);
+          ok = mbar_wait(&B->ps_free2, (y - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -1055,7 +1116,6 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&B->p_full[0]);
-        if (y > 0 && !(ok = dq_out(y - 1))) break;
       }
       if (!ok) break;
       ok = mbar_wait(&B->acc_full, it & 1, abort_flag);
@@ -1087,7 +1147,6 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
       sc += n;
       ++it;
     }
-    if (ok && sc > 0) ok = dq_out(sc - 1);  // the last step's dQ
     if (!ok) *abort_flag = 1;
   }
 
@@ -2831,6 +2890,22 @@ int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, 
   return 0;
 }
 
+// The one-pass kernel's register split adds up to 128 per thread at launch:
+// a build with another count would leave its setmaxnreg.inc waiting, so it
+// is then not used (the two-pass kernels run instead).
+bool fused_regs_ok(int dev) {
+  static int state[64] = {0};  // 0 unknown, 1 usable, -1 not
+  if (dev < 0 || dev >= 64) return false;
+  if (!state[dev]) {
+    cudaFuncAttributes fa{};
+    state[dev] = (cudaFuncGetAttributes(&fa, k_bwd_fused) == cudaSuccess && fa.numRegs == FusedL::REG_LAUNCH &&
+                  fa.maxThreadsPerBlock >= FusedL::THREADS)
+                     ? 1
+                     : -1;
+  }
+  return state[dev] == 1;
+}
+
 template <int D>
 int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O, const float* LSE, int T,
                int Hq, int Hkv, float scale, const pt_blockmap* bm, void* dQ, void* dK, void* dV, float* delta,
@@ -2844,7 +2919,7 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   float* dq_acc = nullptr;
   if constexpr (D == 64) {
     const size_t dq_bytes = sizeof(float) * (size_t)Tpad * Hq * D;
-    if (partial && partial_bytes >= dq_bytes) {
+    if (partial && partial_bytes >= dq_bytes && fused_regs_ok(dev)) {
       dq_acc = partial;
       partial = reinterpret_cast<float*>(reinterpret_cast<char*>(partial) + dq_bytes);
       partial_bytes -= dq_bytes;
