@@ -411,7 +411,7 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
 
     kernels = {}
     for name in ("blockmap_classify", "blockmap_lists", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
-                 "bwd_dkdv_finalize", "bwd_fused", "bwd_dq_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt"):
+                 "bwd_dkdv_finalize", "bwd_fused", "bwd_fused_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt"):
         n, ms = pt.profile_read(name)
         if n:
             kernels[name] = {"launches": n, "ms_per_launch": ms / n}

@@ -492,7 +492,8 @@ pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cud
  * events and returns the number of launches and their summed duration for
  * one scope name: "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
  * "bwd_dkdv_finalize", "bwd_fused" (the one-pass head_dim-64 backward),
- * "bwd_dq_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt",
+ * "bwd_fused_finalize" (its split columns and dQ), "bwd_dv", "bwd_dk",
+ * "bwd_dq", "bwd_simt",
  * "blockmap_classify" (tile classes, list sizes, orders),
  * "blockmap_lists" (lists and masks), and the fold calls' "fold_plan",
  * "fold", "unfold", "unfold_grad", "fold_positions", "fold_mismatches".  pt_profile_reset drops every record

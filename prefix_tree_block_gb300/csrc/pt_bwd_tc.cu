@@ -169,16 +169,16 @@ struct BwdParams {
 
 // Sum the chunk partials of every split kv-major column, in chunk order, and
 // write dV (first D columns of a slot row) and dK (last D) as bf16.
+// One 256-thread block's share of that: rows [8 yb, 8 yb + 8) of split
+// column sp (kv block, kv head, first slot, slot count); one float4 of the
+// 2D columns per thread and row pass.
 template <int D>
-__global__ void k_dkdv_finalize(const int4* __restrict__ splits, const float* __restrict__ partial, int T, int Hkv,
-                                __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV) {
-  pdl_wait();  // launched with programmatic dependent launch
-  // block (x, y): split column x, rows [8y, 8y + 8) of its 128; one float4 of
-  // 2D columns per thread and row pass
-  const int4 sp = splits[blockIdx.x];  // kv block, kv head, first slot, slot count
-  constexpr int Q4 = 2 * D / 4;        // float4 per row
+__device__ __forceinline__ void dkdv_split_rows(const int4 sp, int yb, const float* __restrict__ partial, int T,
+                                                int Hkv, __nv_bfloat16* __restrict__ dK,
+                                                __nv_bfloat16* __restrict__ dV) {
+  constexpr int Q4 = 2 * D / 4;  // float4 per row
   for (int idx = threadIdx.x; idx < 8 * Q4; idx += blockDim.x) {
-    const int r = blockIdx.y * 8 + idx / Q4, c = (idx % Q4) * 4;
+    const int r = yb * 8 + idx / Q4, c = (idx % Q4) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < sp.w; ++k) {
       const float4 v = *reinterpret_cast<const float4*>(partial + ((size_t)(sp.z + k) * 128 + r) * (2 * D) + c);
@@ -196,6 +196,14 @@ __global__ void k_dkdv_finalize(const int4* __restrict__ splits, const float* __
     pk.y = *reinterpret_cast<uint32_t*>(&hi);
     *reinterpret_cast<uint2*>(dst) = pk;
   }
+}
+
+template <int D>
+__global__ void k_dkdv_finalize(const int4* __restrict__ splits, const float* __restrict__ partial, int T, int Hkv,
+                                __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV) {
+  pdl_wait();  // launched with programmatic dependent launch
+  // block (x, y): split column x, rows [8y, 8y + 8) of its 128
+  dkdv_split_rows<D>(splits[blockIdx.x], blockIdx.y, partial, T, Hkv, dK, dV);
 }
 
 // Sum the chunk partials of every split kv-major column for one output of
@@ -732,7 +740,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 // whole step).  The compute warpgroups, whose exponentials and packing bound
 // the step, thus do no dQ work.  Registers are moved to them from the other
 // two warpgroups (setmaxnreg).  The preprocess kernel zeroes the accumulator
-// and k_dq_finalize scales it and writes dQ as bf16.
+// and k_fused_finalize scales it and writes dQ as bf16.
 // Per kept pair the products fall from 14 D flop (S^T, dP^T, dV, dK here;
 // S, dP and dQ again in the q-major kernel) to 10 D, and the q-major
 // kernel's second exponential pass over every tile goes away.  The price is
@@ -1156,12 +1164,24 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
   if (warp == 9) tmem_dealloc(tbase, 512);
 }
 
-// dQ = scale * the one-pass kernel's fp32 accumulator, as bf16: n8 runs of 8
-// values (the rows below T come first in the accumulator's [Tpad][Hq][D]).
-__global__ void __launch_bounds__(256) k_dq_finalize(const float4* __restrict__ acc, size_t n8, float scale,
-                                                     uint4* __restrict__ dQ) {
+// After the one-pass kernel, in one launch: blocks [0, 16 n_splits) sum the
+// chunk partials of the split kv-major columns into dV and dK (as
+// k_dkdv_finalize, block b: column b / 16, rows 8 (b % 16) ..), and the other
+// blocks write dQ = scale * the fp32 accumulator as bf16, grid-stride over n8
+// runs of 8 values (the rows below T come first in its [Tpad][Hq][D]).
+__global__ void __launch_bounds__(256) k_fused_finalize(const int4* __restrict__ splits, int n_splits,
+                                                        const float* __restrict__ partial, int T, int Hkv,
+                                                        __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV,
+                                                        const float4* __restrict__ acc, size_t n8, float scale,
+                                                        uint4* __restrict__ dQ) {
   pdl_wait();  // launched with programmatic dependent launch
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+  const unsigned nsb = 16u * (unsigned)n_splits;
+  if (blockIdx.x < nsb) {
+    dkdv_split_rows<64>(splits[blockIdx.x >> 4], blockIdx.x & 15, partial, T, Hkv, dK, dV);
+    return;
+  }
+  const size_t stride = (size_t)(gridDim.x - nsb) * blockDim.x;
+  for (size_t i = (blockIdx.x - nsb) * (size_t)blockDim.x + threadIdx.x; i < n8; i += stride) {
     const float4 a = acc[2 * i], b = acc[2 * i + 1];
     dQ[i] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
                        pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
@@ -2995,17 +3015,13 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
     }
     ++launches;
   }
-  if (KL->n_splits > 0) {
-    ProfScope ps(s, "bwd_dkdv_finalize");
-    launch_pdl(k_dkdv_finalize<D>, dim3(dim3(KL->n_splits, 16)), dim3(256), 0, s, static_cast<const int4*>(KL->splits), partial, T, Hkv, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
-    ++launches;
-  }
-  if (dq_acc) {
+  if (dq_acc) {  // split columns and dQ in one launch
     const size_t n8 = (size_t)T * Hq * D / 8;
-    const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
-    ProfScope ps(s, "bwd_dq_finalize");
-    launch_pdl(k_dq_finalize, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(dq_acc), n8, scale,
-               static_cast<uint4*>(dQ));
+    const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8) + 16u * KL->n_splits;
+    ProfScope ps(s, "bwd_fused_finalize");
+    launch_pdl(k_fused_finalize, dim3(blocks), dim3(256), 0, s, static_cast<const int4*>(KL->splits), KL->n_splits,
+               (const float*)partial, T, Hkv, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV),
+               reinterpret_cast<const float4*>(dq_acc), n8, scale, static_cast<uint4*>(dQ));
     count_launch(launches + 1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -3013,6 +3029,11 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       return 3;
     }
     return 0;
+  }
+  if (KL->n_splits > 0) {
+    ProfScope ps(s, "bwd_dkdv_finalize");
+    launch_pdl(k_dkdv_finalize<D>, dim3(dim3(KL->n_splits, 16)), dim3(256), 0, s, static_cast<const int4*>(KL->splits), partial, T, Hkv, static_cast<__nv_bfloat16*>(dK), static_cast<__nv_bfloat16*>(dV));
+    ++launches;
   }
   // dQ
   p.ptr = bm->q_ptr;
