@@ -413,14 +413,14 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
     for name in ("blockmap_classify", "blockmap_lists", "fwd_tc", "fwd_simt", "bwd_prep", "bwd_dkdv",
                  "bwd_dkdv_finalize", "bwd_fused", "bwd_fused_finalize", "bwd_dv", "bwd_dk", "bwd_dq", "bwd_simt"):
         n, ms = pt.profile_read(name)
-        if n:
-            kernels[name] = {"launches": n, "ms_per_launch": ms / n}
+        if n:  # (the per-kernel pass runs the same `steps` steps; some kernels launch several times a step)
+            kernels[name] = {"launches": n, "ms_per_launch": ms / n, "ms_per_step": ms / steps}
     pt.profile_reset()
 
     # ---- forward and backward fractions, roofline of the dominant kernel ----
     peak_tf, peak_gbs, peak_src = peaks()
-    fwd_ms = sum(kernels[k]["ms_per_launch"] for k in ("fwd_tc", "fwd_simt") if k in kernels)
-    bwd_ms = sum(kernels[k]["ms_per_launch"] for k in kernels if k.startswith("bwd_"))
+    fwd_ms = sum(kernels[k]["ms_per_step"] for k in ("fwd_tc", "fwd_simt") if k in kernels)
+    bwd_ms = sum(kernels[k]["ms_per_step"] for k in kernels if k.startswith("bwd_"))
     fwd_tf = flops_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None
     bwd_tf = 2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None
     # head_dim 512: each backward launch builds one 256-column half of its output and recomputes S
@@ -440,7 +440,7 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
     tc = {k: v for k, v in kernels.items() if k in per_launch_flops}
     roofline = None
     if tc:
-        dom = max(tc, key=lambda k: tc[k]["ms_per_launch"])
+        dom = max(tc, key=lambda k: tc[k]["ms_per_step"])  # the most time per step
         ach = per_launch_flops[dom] / (tc[dom]["ms_per_launch"] * 1e-3) / 1e12
         if dom.endswith("_simt"):  # fp32 FMA pipes: SMs x 128 lanes x 2 flop x max SM clock
             fp32_peak = FP32_LANES_PER_SM * num_sms() * 2 * SM_MAX_GHZ / 1e3
