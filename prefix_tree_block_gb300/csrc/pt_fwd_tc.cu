@@ -54,14 +54,18 @@ struct FwdCfg {
   static constexpr int NP = D / 64;        // 64-column panels per row
   static constexpr int PANEL = 128 * 128;  // bytes: 128 rows x 128 B
   static constexpr int TILE = NP * PANEL;
-  static constexpr int SB = NH == 1 ? 2 : 1;  // S buffers per head
-  // With TMEM to spare (head_dim 64, two heads) P goes to its own columns, so
-  // S of the next block can be computed as soon as the softmax has loaded S,
-  // and the next item's Q tiles load while this item runs.
-  static constexpr bool OVL = D == 64 && NH == 2;
+  // Head_dim 64, one head per item: two CTAs share an SM (half of TMEM,
+  // two-deep K and V rings, 256 threads each), so the softmax warpgroups of
+  // two independent items fill each other's waits.
+  static constexpr bool TWO = D == 64 && NH == 1;
+  static constexpr int SB = (NH == 1 && !TWO) ? 2 : 1;  // S buffers per head
+  // With TMEM to spare (head_dim 64) P goes to its own columns, so S of the
+  // next block can be computed as soon as the softmax has loaded S, and the
+  // next item's Q tiles load while this item runs.
+  static constexpr bool OVL = D == 64;
   static constexpr int QB = OVL ? 2 : 1;  // Q buffers
-  static constexpr int KS = D == 64 ? 4 : (D == 128 ? (NH == 2 ? 2 : 3) : 1);
-  static constexpr int VS = D == 64 ? 4 : (D == 128 ? 2 : 1);
+  static constexpr int KS = TWO ? 2 : D == 64 ? 4 : (D == 128 ? (NH == 2 ? 2 : 3) : 1);
+  static constexpr int VS = TWO ? 2 : D == 64 ? 4 : (D == 128 ? 2 : 1);
   static constexpr int MASKB = 128 * 16;  // one partial tile's row masks
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QB * NH * TILE;
@@ -70,7 +74,7 @@ struct FwdCfg {
   // (head_dim 256) 2 KB per softmax warp to turn its 32 rows of a 32-column
   // O chunk into 64-byte row segments for the stores (see the epilogue); at
   // head_dim 128 the staging's registers cost the main loop more than it saves
-  static constexpr bool OST = NH == 1;
+  static constexpr bool OST = NH == 1 && !OVL;
   static constexpr int OFF_OST = OFF_MASK + VS * MASKB;
   static constexpr int OST_BYTES = OST ? NH * 4 * 2048 : 0;
   static constexpr int OFF_META = OFF_OST + OST_BYTES;
@@ -88,9 +92,16 @@ struct FwdCfg {
   // second MMA warp: one issues the S products, the other the PV products,
   // so the tensor pipe overlaps their chains (one thread's MMAs into one
   // accumulator after another run with the pipe's latency between chains)
-  static constexpr int THREADS = NH * 128 + (OVL ? 96 : 64);
+  // (TWO) the producer and MMA warps fill a second warpgroup (one warp
+  // idle); registers move to the softmax warpgroup (setmaxnreg), the split
+  // adding up to the launch's 128 per thread (the kernel must be built with 128)
+  static constexpr int THREADS = TWO ? 256 : NH * 128 + (OVL ? 96 : 64);
+  static constexpr int CTAS_PER_SM = TWO ? 2 : 1;
+  static constexpr int TMEM_COLS = TWO ? 256 : 512;
+  static constexpr int REG_SOFTMAX = 184, REG_CTRL = 72, REG_LAUNCH = 128;
+  static_assert(!TWO || REG_SOFTMAX + REG_CTRL == 2 * REG_LAUNCH, "register split");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(TM_O + NH * D <= 512, "TMEM budget");
+  static_assert(TM_O + NH * D <= TMEM_COLS, "TMEM budget");
 };
 
 struct FwdParams {
@@ -138,7 +149,7 @@ __host__ __device__ __forceinline__ int fwd_items(int nq, int Hq, int Hkv) {
 }
 
 template <int D, int NH>
-__global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
+__global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PER_SM)
     k_fwd_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
              const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, const FwdParams p) {
   pdl_wait();  // launched with programmatic dependent launch
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     if (C::OVL) prefetch_tmap(&mO);
   }
   if (warp == ISSUER) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -217,6 +228,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp >= PRODUCER) {
+  if constexpr (C::TWO) regs_dec<C::REG_CTRL>();  // the whole warpgroup, before its warps take their roles
   if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -465,8 +478,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       mbar_wait_drain(mma_done2, 0, 200000000);
     }
     __syncwarp();
+  }  // (TWO: warp 7 has no role)
   } else {
     // ------------------------------------------------------------ softmax
+    if constexpr (C::TWO) regs_inc<C::REG_SOFTMAX>();
     const int h = warp >> 2;                   // head slot of this warpgroup
     const int r = threadIdx.x & 127;           // q row within the tile, TMEM lane
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
@@ -572,7 +587,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
           // warp's rows in place once the PV in flight is done.  With two
           // heads that is already known (S(j) was committed after PV(j-1));
           // with one head, wait for it.
-          if (NH == 1) {
+          if (NH == 1 && !C::OVL) {
             ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
               ok = false;
@@ -599,7 +614,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         tmem_st32(pb + 0, sr + 0);
         tmem_st32(pb + 32, sr + 32);
         tmem_st_wait();
-        if (NH == 1 && jj > 0) {
+        if (NH == 1 && !C::OVL && jj > 0) {
           ok = mbar_wait(o_full + h, (pvc + jj - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
@@ -611,7 +626,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       }
       if (!ok) break;
       // epilogue: O / l and LSE (one head: O committed per PV; two heads: once per item)
-      ok = mbar_wait(o_full + h, (NH == 1 ? (pvc + n - 1) : itv) & 1, abort_flag);
+      ok = mbar_wait(o_full + h, ((NH == 1 && !C::OVL) ? (pvc + n - 1) : itv) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -717,7 +732,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == ISSUER) tmem_dealloc(tbase, 512);
+  if (warp == ISSUER) tmem_dealloc(tbase, C::TMEM_COLS);
 }
 
 template <int D, int NH>
@@ -734,6 +749,19 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
       return 3;
     }
     attr_set[dev] = 1;
+  }
+  if constexpr (C::TWO) {
+    // the register split adds up to 128 per thread at launch: a build with
+    // another count would leave setmaxnreg.inc waiting, so it is refused
+    static int regs_ok[64] = {0};
+    if (dev >= 0 && dev < 64 && !regs_ok[dev]) {
+      cudaFuncAttributes fa{};
+      if (cudaFuncGetAttributes(&fa, k_fwd_tc<D, NH>) != cudaSuccess || fa.numRegs != C::REG_LAUNCH) {
+        set_error("forward kernel built with %d registers per thread, %d expected", fa.numRegs, C::REG_LAUNCH);
+        return 3;
+      }
+      regs_ok[dev] = 1;
+    }
   }
   if (masks_missing(bm)) {
     set_error("forward kernel: block map has no tile masks");
@@ -757,7 +785,8 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
   p.nq = bm->nq;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int n_items = fwd_items<NH>(bm->nq, Hq, Hkv);
-  const int grid = n_items < num_sms(dev) ? n_items : num_sms(dev);
+  const int slots = num_sms(dev) * C::CTAS_PER_SM;
+  const int grid = n_items < slots ? n_items : slots;
   if (grid <= 0) return 0;
   {
     ProfScope ps(s, "fwd_tc");
@@ -1249,7 +1278,7 @@ int wait_timeout_probe(cudaStream_t s) {
 int fwd_tc(const void* Q, const void* K, const void* V, int T, int Hq, int Hkv, int D, float scale,
            const pt_blockmap* bm, void* O, float* LSE, cudaStream_t s) {
   switch (D) {
-    case 64: return launch_fwd<64, 2>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
+    case 64: return launch_fwd<64, 1>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
     case 128: return launch_fwd<128, 2>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
     case 256: return launch_fwd<256, 1>(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
     case 512: return launch_fwd512(Q, K, V, T, Hq, Hkv, scale, bm, O, LSE, s);
