@@ -748,27 +748,42 @@ constexpr int kMaxDev = 64;
 // A large copy that another stream has queued on an engine (a training
 // step's inputs and gradients) would otherwise hold them, and with them the
 // kernels queued behind them on this stream.
-__global__ void k_stage(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, long long bytes, int vec) {
-  pdl_wait();  // launched with programmatic dependent launch
+// early: the source is host staging that the CPU filled before the launch, so
+// each thread reads its first 16 bytes before waiting for the previous kernel
+// (the read's round trip to host memory overlaps that kernel's tail); the
+// wait still precedes every write.
+__global__ void k_stage(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, long long bytes, int vec,
+                        int early) {
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long nth = (long long)gridDim.x * blockDim.x;
-  long long done = 0;
+  long long done = 0, i0 = tid;
   if (vec) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
     const long long n16 = bytes >> 4;
-    for (long long i = tid; i < n16; i += nth)
-      reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    if (early && tid < n16) {
+      const uint4 first = s4[tid];
+      pdl_wait();  // launched with programmatic dependent launch
+      d4[tid] = first;
+      i0 = tid + nth;
+    } else {
+      pdl_wait();
+    }
+    for (long long i = i0; i < n16; i += nth) d4[i] = s4[i];
     done = n16 << 4;
+  } else {
+    pdl_wait();
   }
   for (long long i = done + tid; i < bytes; i += nth) dst[i] = src[i];
 }
 
-int stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+int stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s, bool early = false) {
   if (!bytes) return 0;
   const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0) ? 1 : 0;
   const long long units = vec ? (long long)(bytes >> 4) + 1 : (long long)bytes;
   const int grid = (int)std::max(1LL, std::min<long long>((units + 255) / 256, 64));
   launch_pdl(k_stage, dim3(grid), dim3(256), 0, s, static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst),
-             (long long)bytes, vec);
+             (long long)bytes, vec, early ? 1 : 0);
   count_launch();
   if (cudaGetLastError() != cudaSuccess) {
     set_error("staging copy launch failed");
@@ -1003,7 +1018,7 @@ int upload(void* dst, const void* src, size_t bytes, int dev, cudaStream_t s) {
     g.cap = cap;
   }
   std::memcpy(g.host, src, bytes);
-  if (int rc = stage_copy(g.dev, dst, bytes, s)) return rc;
+  if (int rc = stage_copy(g.dev, dst, bytes, s, true)) return rc;  // host staging, filled above
   cudaEventRecord(g.done, s);
   g.used = true;
   return 0;
