@@ -228,6 +228,7 @@ __device__ __forceinline__ long long overlap(long long a0, long long a1, long lo
 __global__ void k_classify(int T, int BM, int BN, int nq, int nk, const int* node_of, const int* node_start,
                            const int* node_end, const int* parent, uint8_t* kinds, int* counters, int* row_cnt,
                            int* col_cnt, int* row_part) {
+  pdl_wait();  // launched with programmatic dependent launch
   long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (w >= (long long)nq * nk) return;
@@ -395,6 +396,7 @@ __global__ void k_tree_listed(int T, int tpad, int N, int* __restrict__ map_tabs
 // Exclusive scans of up to three small arrays in one block (lengths up to a
 // few hundred thousand): out[0..n] with out[n] the total.
 __global__ void k_scan3(const int* a, int na, int* oa, const int* b, int nb, int* ob, const int* c, int nc, int* oc) {
+  pdl_wait();  // launched with programmatic dependent launch
   __shared__ int sh[32];
   __shared__ int carry;
   const int* in[3] = {a, b, c};
@@ -423,6 +425,7 @@ __global__ void k_scan3(const int* a, int na, int* oa, const int* b, int nb, int
 // partial tiles row-major (slot = partial tiles in earlier rows + rank in row).
 __global__ void k_fill_rows(const uint8_t* kinds, int nq, int nk, const int* q_ptr, const int* prow_ptr, int* kv_idx,
                             uint8_t* kd, int* pidx, int2* slot_tile, long long slot_cap) {
+  pdl_wait();  // launched with programmatic dependent launch
   int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= nq) return;
   int pos = q_ptr[w], ppos = prow_ptr[w];
@@ -458,6 +461,7 @@ __global__ void k_fill_rows(const uint8_t* kinds, int nq, int nk, const int* q_p
 // entry's mask slot is found in the q tile's row (binary search by kv block).
 __global__ void k_fill_cols(const uint8_t* kinds, int nq, int nk, const int* k_ptr, int* q_idx, uint8_t* kdT,
                             const int* q_ptr, const int* kv_idx, const int* pidx, int* pidxT) {
+  pdl_wait();  // launched with programmatic dependent launch
   int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= nk) return;
   int pos = k_ptr[w];
@@ -630,6 +634,7 @@ __device__ __forceinline__ void draft_row(const DraftParams& d, int q, int& c0, 
 // counted per row from its two ranges (exact).
 __global__ void k_draft_classify(int T, int BM, int BN, int nq, int nk, DraftParams d, uint8_t* kinds, int* counters,
                                  int* row_cnt, int* col_cnt, int* row_part) {
+  pdl_wait();  // launched with programmatic dependent launch
   const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= (long long)nq * nk) return;
@@ -666,6 +671,7 @@ __global__ void k_draft_classify(int T, int BM, int BN, int nq, int nk, DraftPar
 // the transpose, one ballot per column over each warp's 32 rows.
 __global__ void k_draft_masks(int T, DraftParams d, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols,
                               long long n_known, const int* nnz_total, const int* n_full, long long p_cap) {
+  pdl_wait();  // launched with programmatic dependent launch
   const long long n_part = min(n_known >= 0 ? n_known : (long long)(*nnz_total - *n_full), p_cap);
   const int r = threadIdx.x, lane = r & 31, wi = r >> 5;
   for (long long s = blockIdx.x; s < n_part; s += gridDim.x) {
@@ -721,6 +727,7 @@ __global__ void k_dense_lists(int nq, int nk, int* q_ptr, int* kv_idx, uint8_t* 
 // #{j : cnt[j] > cnt[i] or (cnt[j] == cnt[i] and j < i)}.  One warp per
 // element; warps [0, na) order array a, the rest array b.
 __global__ void k_lpt2(const int* a, int na, int* oa, const int* b, int nb, int* ob) {
+  pdl_wait();  // launched with programmatic dependent launch
   int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= na + nb) return;
   const int* cnt = w < na ? a : b;
@@ -1149,19 +1156,20 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
       if (ntiles > 0) {
         long long threads = ntiles * 32;
         if (bm->producer == PT_PRODUCER_DRAFT)
-          k_draft_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-              bm->T, bm->BM, bm->BN, nq, nk, draft_params(bm), kinds, counters, row_cnt, col_cnt, row_part);
+          launch_pdl(k_draft_classify, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, bm->T, bm->BM, bm->BN,
+                     nq, nk, draft_params(bm), kinds, counters, row_cnt, col_cnt, row_part);
         else
-          k_classify<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(bm->T, bm->BM, bm->BN, nq, nk, bm->node_of,
-                                                                       bm->node_start, bm->node_end, bm->parent,
-                                                                       kinds, counters, row_cnt, col_cnt, row_part);
+          launch_pdl(k_classify, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, bm->T, bm->BM, bm->BN, nq,
+                     nk, bm->node_of, bm->node_start, bm->node_end, bm->parent, kinds, counters, row_cnt, col_cnt,
+                     row_part);
         PT_LAUNCHED(1);
       }
-      k_scan3<<<1, kScanBlock, 0, s>>>(row_cnt, nq, bm->q_ptr, col_cnt, nk, bm->k_ptr, row_part, nq, prow_ptr);
+      launch_pdl(k_scan3, dim3(1), dim3(kScanBlock), 0, s, row_cnt, nq, bm->q_ptr, col_cnt, nk, bm->k_ptr, row_part, nq,
+                 prow_ptr);
       PT_LAUNCHED(1);
       if (ntiles > 0) {
-        k_lpt2<<<(unsigned)(((long long)(nq + nk) * 32 + 255) / 256), 256, 0, s>>>(row_cnt, nq, bm->q_order, col_cnt,
-                                                                                nk, bm->k_order);
+        launch_pdl(k_lpt2, dim3((unsigned)(((long long)(nq + nk) * 32 + 255) / 256)), dim3(256), 0, s, row_cnt, nq,
+                   bm->q_order, col_cnt, nk, bm->k_order);
         PT_LAUNCHED(1);
       }
     }
@@ -1207,20 +1215,20 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
       ProfScope ps(s, "blockmap_lists");  // the lists and the partial tiles' masks
       if ((rc = pool_alloc(&tmpB, sizeof(int2) * (size_t)std::max<int64_t>(p_alloc, 1), dev, s))) break;
       int2* slot_tile = static_cast<int2*>(tmpB);
-      k_fill_rows<<<(nq * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, bm->q_ptr, prow_ptr, bm->kv_idx, bm->kind,
-                                                         bm->pidx, slot_tile, (long long)p_alloc);
-      k_fill_cols<<<(nk * 32 + 255) / 256, 256, 0, s>>>(kinds, nq, nk, bm->k_ptr, bm->q_idx, bm->kindT, bm->q_ptr,
-                                                         bm->kv_idx, bm->pidx, bm->pidxT);
+      launch_pdl(k_fill_rows, dim3((nq * 32 + 255) / 256), dim3(256), 0, s, kinds, nq, nk, bm->q_ptr, prow_ptr,
+                 bm->kv_idx, bm->kind, bm->pidx, slot_tile, (long long)p_alloc);
+      launch_pdl(k_fill_cols, dim3((nk * 32 + 255) / 256), dim3(256), 0, s, kinds, nq, nk, bm->k_ptr, bm->q_idx,
+                 bm->kindT, bm->q_ptr, bm->kv_idx, bm->pidx, bm->pidxT);
       PT_LAUNCHED(2);
       if (bm->mask_rows) {
         const long long grid = std::min<long long>(p_alloc, (long long)num_sms(dev) * 16);
         if (bm->producer == PT_PRODUCER_DRAFT)
-          k_draft_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, draft_params(bm), slot_tile, bm->mask_rows,
-                                                       bm->mask_cols, -1LL, bm->q_ptr + nq, counters,
-                                                       (long long)bm->p_cap);
+          launch_pdl(k_draft_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, draft_params(bm), slot_tile,
+                     bm->mask_rows, bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap);
         else
-          k_masks<<<(unsigned)grid, 128, 0, s>>>(bm->T, bm->tok, slot_tile, bm->mask_rows, bm->mask_cols, -1LL,
-                                                 bm->q_ptr + nq, counters, (long long)bm->p_cap);
+          launch_pdl(k_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, bm->tok, slot_tile, bm->mask_rows,
+                     bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap, static_cast<int*>(nullptr),
+                     -1LL);
         PT_LAUNCHED(1);
       }
     }
