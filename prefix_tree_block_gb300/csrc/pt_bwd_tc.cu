@@ -1180,11 +1180,22 @@ __global__ void __launch_bounds__(256) k_fused_finalize(const int4* __restrict__
     dkdv_split_rows<64>(splits[blockIdx.x >> 4], blockIdx.x & 15, partial, T, Hkv, dK, dV);
     return;
   }
+  // two runs per thread and pass: four 16-byte loads in flight
   const size_t stride = (size_t)(gridDim.x - nsb) * blockDim.x;
-  for (size_t i = (blockIdx.x - nsb) * (size_t)blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+  for (size_t i = (blockIdx.x - nsb) * (size_t)blockDim.x + threadIdx.x; i < n8; i += 2 * stride) {
+    const size_t i2 = i + stride;
+    const bool two = i2 < n8;
+    const float4 a = __ldcs(acc + 2 * i), b = __ldcs(acc + 2 * i + 1);
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f), d = c;
+    if (two) {
+      c = __ldcs(acc + 2 * i2);
+      d = __ldcs(acc + 2 * i2 + 1);
+    }
     dQ[i] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
                        pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
+    if (two)
+      dQ[i2] = make_uint4(pack_bf16(c.x * scale, c.y * scale), pack_bf16(c.z * scale, c.w * scale),
+                          pack_bf16(d.x * scale, d.y * scale), pack_bf16(d.z * scale, d.w * scale));
   }
 }
 
