@@ -116,3 +116,42 @@ def test_head_dim_64_one_pass_and_two_pass(name):
     for a, b in zip(got["one"], got["two"]):
         assert rel_l2(a, b) <= 1e-2
     bm.free()
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (8, 1), (6, 3)])
+def test_head_dim_64_one_pass_gqa(Hq, Hkv):
+    """The one-pass head_dim-64 backward over head layouts: MHA, one kv head
+    for eight q heads, three groups of two (dK and dV summed over each group's
+    q heads inside the kernel, dQ per q head through the accumulator)."""
+    check_bwd(small_structures()["grpo"], Hq, Hkv, 64, "bf16", seed=40 + Hq)
+
+
+def test_head_dim_64_one_pass_without_split_room():
+    """A workspace with room for the two statistics and the dQ accumulator
+    but none for partial sums: the one-pass kernel runs with no column split
+    (every kv-major column one item)."""
+    import prefix_tree_block_gb300 as pt
+    import torch
+
+    st = W.grpo_structure([(700, [300, 41, 250, 640]), (0, [77, 129])])
+    Hq, Hkv, D = 4, 2, 64
+    q, k, v, do = W.make_tensors(st.T, Hq, Hkv, D, "bf16", seed=12)
+    Q, K, V, dO = (x.cuda() for x in (q, k, v, do))
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes)
+    O, LSE = pt.attn_fwd(Q, K, V, bm)
+    tpad = -(-st.T // 128) * 128
+    r256 = lambda n: -(-n // 256) * 256
+    need = 2 * r256(4 * tpad * Hq) + r256(4 * tpad * Hq * D)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    pt.profile_reset()
+    pt.profile_enable(True)
+    res = pt.attn_bwd(dO, Q, K, V, O, LSE, bm, workspace=ws)
+    pt.sync_status()
+    n_fused = pt.profile_read("bwd_fused")[0]
+    n_split = pt.profile_read("bwd_dkdv_finalize")[0]
+    pt.profile_enable(False)
+    assert n_fused == 1 and n_split == 0
+    want = orc.attn_bwd(q, k, v, do, orc.structure_labels(st))
+    for g, w in zip((x.float().cpu().numpy() for x in res), want):
+        assert rel_l2(g, w) <= GRAD_RL2["bf16"]
+    bm.free()
