@@ -240,7 +240,10 @@ pt_status pt_attn_fwd(const void* Q, const void* K, const void* V, pt_dtype dtyp
  * (all device).  Outputs dQ [T,Hq,D], dK/dV [T,Hkv,D] (device, dtype).
  * workspace: device scratch of at least pt_bwd_workspace_bytes(T, Hq, D)
  * bytes, 256-byte aligned, owned by the caller; its contents on entry do not
- * matter.  Calls that share one workspace must not overlap on the GPU.
+ * matter.  Calls that share one workspace must not overlap on the GPU.  Its
+ * size also picks the head_dim-64 backward (see pt_bwd_workspace_bytes): the
+ * full size gives the one-pass kernel, whose dQ may differ between runs in
+ * its last bits; the two row statistics alone give the two-pass kernels.
  * Supported shapes as for pt_attn_fwd.
  * ------------------------------------------------------------------------- */
 pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* V, const void* O,

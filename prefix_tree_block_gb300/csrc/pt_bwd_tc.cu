@@ -8,7 +8,11 @@
 // V are never repeated).  Empty tiles are skipped; partial tiles use the
 // block map's 128 x 128 keep bitmasks.
 //
-// Three launches on the caller's stream:
+// At head_dim 64, when the caller's workspace holds an fp32 dQ accumulator,
+// one kv-major kernel (k_bwd_fused, section 2b) computes dQ, dK and dV in
+// one pass, dQ added into the accumulator by TMA reduce-adds (not run-to-run
+// bitwise identical), then one finalize launch converts it.  Otherwise,
+// three launches on the caller's stream:
 //  1. k_bwd_prep  (HBM-bound) Delta = rowsum(dO * O) and LSE * log2(e) into
 //                 the workspace, [Hq, Tpad] each, Tpad = ceil(T/128)*128;
 //                 padding rows get values that make them contribute nothing.
@@ -27,9 +31,9 @@
 //                 stream through; each block is split into two halves of 64
 //                 kv columns, one per warpgroup: S = Q K_half^T, dP = dO
 //                 V_half^T, dS back into TMEM, then dQ += dS K_half.
-// No atomics: every output element is written once, so results are
-// deterministic.  TMEM per CTA: 2 x (64 + 64) columns of S/dP plus the
-// accumulators (dV, dK: 2D; dQ: D) -- at most 512.
+// In the three-launch form every output element is written once (no
+// atomics), so results are deterministic.  TMEM per CTA: 2 x (64 + 64)
+// columns of S/dP plus the accumulators (dV, dK: 2D; dQ: D) -- at most 512.
 #include <cuda_bf16.h>
 
 #include <algorithm>

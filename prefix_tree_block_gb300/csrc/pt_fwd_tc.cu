@@ -6,11 +6,14 @@
 // pairs apply the tree mask element by element (here: one bit per pair from
 // the block map's precomputed 128 x 128 keep masks).
 //
-// Design (sm_103a, one persistent CTA per SM):
-//   NH softmax warpgroups (NH = 2 for head_dim <= 128, else 1).  A work item
-//   is one q tile and NH q heads that share a kv head (grouped-query
+// Design (sm_103a, persistent CTAs: one per SM, two at head_dim 64):
+//   NH softmax warpgroups (NH = 2 at head_dim 128, else 1).  A work item is
+//   one q tile and NH q heads that share a kv head (grouped-query
 //   attention), so every K/V tile loaded serves NH heads.  Warpgroup h owns
-//   head h of the item; thread t of it owns q row t of the tile.
+//   head h of the item; thread t of it owns q row t of the tile.  At head_dim
+//   64 a CTA takes one head and half of TMEM, and two CTAs share each SM:
+//   their softmax warpgroups, on independent items, fill each other's waits
+//   (where two heads of one CTA would run in lockstep on the same K/V block).
 //   producer warp   TMA: the NH Q tiles once per item, then K and V of each
 //                   listed kv block through separate multi-stage rings
 //                   (128-byte swizzled 64-column panels); with V, the tile's
