@@ -453,6 +453,34 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
                         "frac": ach / peak_tf, "traffic": MEASURED_TRAFFIC.get((workload, dom)),
                         "peak_source": f"{peak_src} bf16 burst"}
 
+    # ---- HBM-bound kernels: algorithmic bytes per step against the measured copy peak ----
+    mp = make_map()
+    nnz, n_part = mp.nnz, mp.nnz - mp.n_full
+    mp.free()
+    tpad = -(-T // 128) * 128
+    elt = 2 if dtype == "bf16" else 4
+    fused = "bwd_fused" in kernels
+    algo = {
+        # dO and O read, LSE read, Delta and LSE*log2(e) written; with the one-pass
+        # backward also its fp32 dQ accumulator zeroed
+        "bwd_prep": 2 * T * Hq * D * elt + 4 * T * Hq + 8 * tpad * Hq + (4 * tpad * Hq * D if fused else 0),
+        # the map: per listed tile its q-major and kv-major entries (18 B), 2 x 2 KB of
+        # keep bits per partial tile; tree maps also the token table (8 B) and each
+        # token's node (4 B)
+        "blockmap": 18 * nnz + 4096 * n_part + (0 if draft else 12 * tpad),
+    }
+    if fused:  # the fp32 accumulator read, dQ written
+        algo["bwd_fused_finalize"] = 4 * tpad * Hq * D + elt * T * Hq * D
+    hbm = {"peak_gbs": peak_gbs}
+    for name, nbytes in algo.items():
+        if name == "blockmap":
+            ms = sum(kernels[k]["ms_per_step"] for k in ("blockmap_classify", "blockmap_lists") if k in kernels)
+        else:
+            ms = kernels[name]["ms_per_step"] if name in kernels else 0.0
+        if ms > 0:
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            hbm[name] = {"algorithmic_bytes": int(nbytes), "ms": ms, "achieved_gbs": gbs, "frac_of_hbm": gbs / peak_gbs}
+
     # ---- dense-masked comparison (same kernels, every tile partial) ---------
     dense = None
     if with_dense:
@@ -466,7 +494,7 @@ def measure_device(workload, steps, warmup, with_dense, flush, dist, local, worl
         "frac_of_peak": value / world / peak_tf,
         "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak_tf if fwd_tf else None},
         "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak_tf if bwd_tf else None},
-        "kernels": kernels, "roofline": roofline, "dense_masked": dense, "gpu_launches": int(launches),
+        "kernels": kernels, "roofline": roofline, "hbm": hbm, "dense_masked": dense, "gpu_launches": int(launches),
         "_ctx": {"tensors": (Q, K, V, dO, q, k, v, do), "grads": (dQ, dK, dV), "make_map": make_map,
                  "host_layout": host_layout, "stream": stream, "timed": timed},
     }
@@ -654,7 +682,8 @@ def main():
                        "tiles": "128x128", "l2": "flushed before every step (256 MB write, untimed)",
                        "parallelism": f"replicas x{world}"},
             "kernels": res["kernels"], "kernel_timing": "second pass of the same steps with an event pair per kernel",
-            "roofline": res["roofline"], "dense_masked": res["dense_masked"], "sdpa_dense_mask": sdpa, "e2e": e2e,
+            "roofline": res["roofline"], "hbm": res["hbm"], "dense_masked": res["dense_masked"], "sdpa_dense_mask": sdpa,
+            "e2e": e2e,
             "gpu_launches": res["gpu_launches"], "clocks": clocks, "cpu_baseline": cpu, "fold": fold,
         }
         if others:
