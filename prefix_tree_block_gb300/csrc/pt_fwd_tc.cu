@@ -231,9 +231,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp >= PRODUCER) {
-  if constexpr (C::TWO) regs_dec<C::REG_CTRL>();  // the whole warpgroup, before its warps take their roles
-  if (warp == PRODUCER) {
+  // the roles, one lambda each, run by the warps the dispatch below picks: producer
+  const auto producer_role = [&]() {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t kc = 0, vc = 0, it = 0;
@@ -302,7 +301,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
       }
     }
     __syncwarp();
-  } else if (warp == ISSUER) {
+  };
+  // MMA issuer
+  const auto issuer_role = [&]() {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
@@ -430,7 +431,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
       mbar_wait_drain(mma_done, 0, 200000000);
     }
     __syncwarp();
-  } else if (C::OVL && warp == ISSUER_PV) {
+  };
+  // PV issuer (OVL)
+  const auto pv_role = [&]() {
     // ------------------------------------------------------------ PV issuer (OVL)
     // PV of block i for every head of the item once V(i) and that head's P
     // tile are in (and, on the item's first block, the epilogue has read
@@ -481,10 +484,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
       mbar_wait_drain(mma_done2, 0, 200000000);
     }
     __syncwarp();
-  }  // (TWO: warp 7 has no role)
-  } else {
+  };
+  // softmax warpgroups
+  const auto softmax_role = [&]() {
     // ------------------------------------------------------------ softmax
-    if constexpr (C::TWO) regs_inc<C::REG_SOFTMAX>();
     const int h = warp >> 2;                   // head slot of this warpgroup
     const int r = threadIdx.x & 127;           // q row within the tile, TMEM lane
     const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16);
@@ -730,6 +733,32 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
     }
     if (!ok) *abort_flag = 1;
     if (C::OVL && r == 0) bulk_wait0();  // this warpgroup's O stores have landed
+  };
+  if constexpr (C::TWO) {
+    // whole warpgroups take their registers first, so that each setmaxnreg
+    // dominates the code of its warpgroup (ptxas then allocates each region
+    // to its own count)
+    if (warp >= PRODUCER) {
+      regs_dec<C::REG_CTRL>();
+      if (warp == PRODUCER)
+        producer_role();
+      else if (warp == ISSUER)
+        issuer_role();
+      else if (warp == ISSUER_PV)
+        pv_role();  // (warp 7 has no role)
+    } else {
+      regs_inc<C::REG_SOFTMAX>();
+      softmax_role();
+    }
+  } else {
+    if (warp == PRODUCER)
+      producer_role();
+    else if (warp == ISSUER)
+      issuer_role();
+    else if (C::OVL && warp == ISSUER_PV)
+      pv_role();
+    else
+      softmax_role();
   }
 
   tc_fence_before();
