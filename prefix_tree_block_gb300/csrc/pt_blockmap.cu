@@ -263,10 +263,44 @@ __global__ void k_classify(int T, int BM, int BN, int nq, int nk, const int* nod
   }
 }
 
-// Tree maps whose lists the host built (128 x 128 tiles): one launch writes
-// the token table (blocks [0, tok_blocks), as k_tree_tokens) and, in the
-// other blocks, copies the node tables and the host lists from the packed
-// upload into the map and classifies every listed tile, full or partial,
+// ---------------------------------------------------------------------------
+// draft-block form ("support sequence packing in the Domino and JetSpec
+// drafts" and the DFlash-family drafter PR: draft blocks attend to the context
+// before their anchor, optionally restricted to the anchor's document and to a
+// window counted from each query's real position, and to their own block,
+// bidirectionally or causally; context rows are keys only)
+// ---------------------------------------------------------------------------
+struct DraftParams {
+  int S, bs, causal, window;
+  const int4* blk;  // per block: kept context [x, y) before any window, anchor z, keep flag w
+};
+
+DraftParams draft_params(const pt_blockmap* bm) {
+  return DraftParams{bm->d_ctx, bm->d_bs, bm->d_causal, bm->d_window, static_cast<const int4*>(bm->d_blk)};
+}
+
+// Kept keys of row q: context [c0, c1) and its own block's [b0, b1) (empty
+// ranges for context rows and dropped blocks).
+__device__ __forceinline__ void draft_row(const DraftParams& d, int q, int& c0, int& c1, int& b0, int& b1) {
+  c0 = c1 = b0 = b1 = 0;
+  if (q < d.S) return;
+  const int b = (q - d.S) / d.bs, k = (q - d.S) % d.bs;
+  const int4 bl = d.blk[b];
+  if (!bl.w) return;
+  c0 = bl.x;
+  c1 = bl.y;
+  if (d.window > 0) c0 = max(c0, bl.z + k - d.window + 1);  // real position bl.z + k minus kv < window
+  if (c1 < c0) c1 = c0;
+  b0 = d.S + b * d.bs;
+  b1 = b0 + (d.causal ? k + 1 : d.bs);
+}
+
+// Maps whose lists the host built (128 x 128 tiles; trees, and draft maps
+// with DRAFT): one launch writes the token table (trees: blocks
+// [0, tok_blocks), as k_tree_tokens) and, in the other blocks, copies the
+// node tables and the host lists from the packed upload into the map and
+// classifies every listed tile (trees: from the ancestor intervals; draft
+// maps: from each row's two key ranges), full or partial,
 // numbering partial tiles in the order they are found (a mask slot is
 // reached only through pidx and pidxT).  Packed upload (ints): counters[4]
 // (zero) | node tables[5 * N] | q_ptr[nq + 1] |
@@ -275,12 +309,14 @@ __global__ void k_classify(int T, int BM, int BN, int nq, int nk, const int* nod
 // tiles and counters[1] hands out mask slots.  A listed tile that keeps
 // nothing would mean the host's lists are wrong: it is recorded as an error
 // and kept as a partial tile (its mask is empty, so results stay exact).
+template <bool DRAFT>
 __global__ void k_tree_listed(int T, int tpad, int N, int* __restrict__ map_tabs, pt_tok* __restrict__ tok,
                               int* __restrict__ node_of, int tok_blocks, int* __restrict__ pk, int nq, int nk, int nnz,
                               int* __restrict__ q_ptr, int* __restrict__ k_ptr, int* __restrict__ q_order,
                               int* __restrict__ k_order, int* __restrict__ kv_idx, int* __restrict__ q_idx,
                               uint8_t* __restrict__ kind, int* __restrict__ pidx, uint8_t* __restrict__ kindT,
-                              int* __restrict__ pidxT, int2* __restrict__ slot_tile, long long p_cap) {
+                              int* __restrict__ pidxT, int2* __restrict__ slot_tile, long long p_cap,
+                              DraftParams d) {
   pdl_wait();  // launched with programmatic dependent launch
   // node tables (start | end | parent | tin | tout) come in the packed upload
   // and are read from there; the list blocks also copy them into the map
@@ -353,16 +389,23 @@ __global__ void k_tree_listed(int T, int tpad, int N, int* __restrict__ map_tabs
     const long long qlast = q0 + 127 < T - 1 ? q0 + 127 : T - 1;
     long long kept = 0;
     for (long long q = q0 + lane; q <= qlast; q += 32) {
-      int a = 0, b = N - 1;
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (node_end[mid] > q)
-          b = mid;
-        else
-          a = mid + 1;
+      if constexpr (DRAFT) {
+        const long long kend = k1 < T ? k1 : T;
+        int c0, c1, b0, b1;
+        draft_row(d, (int)q, c0, c1, b0, b1);
+        kept += overlap(c0, c1, k0, kend) + overlap(b0, b1, k0, kend);
+      } else {
+        int a = 0, b = N - 1;
+        while (a < b) {
+          const int mid = (a + b) >> 1;
+          if (node_end[mid] > q)
+            b = mid;
+          else
+            a = mid + 1;
+        }
+        kept += overlap(node_start[a], q + 1, k0, k1);
+        for (int u = parent[a]; u != -1; u = parent[u]) kept += overlap(node_start[u], node_end[u], k0, k1);
       }
-      kept += overlap(node_start[a], q + 1, k0, k1);
-      for (int u = parent[a]; u != -1; u = parent[u]) kept += overlap(node_start[u], node_end[u], k0, k1);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
@@ -598,38 +641,6 @@ __global__ void k_masks(int T, const pt_tok* tok, const int2* slot_tile, uint32_
   }
 }
 
-// ---------------------------------------------------------------------------
-// draft-block form ("support sequence packing in the Domino and JetSpec
-// drafts" and the DFlash-family drafter PR: draft blocks attend to the context
-// before their anchor, optionally restricted to the anchor's document and to a
-// window counted from each query's real position, and to their own block,
-// bidirectionally or causally; context rows are keys only)
-// ---------------------------------------------------------------------------
-struct DraftParams {
-  int S, bs, causal, window;
-  const int4* blk;  // per block: kept context [x, y) before any window, anchor z, keep flag w
-};
-
-DraftParams draft_params(const pt_blockmap* bm) {
-  return DraftParams{bm->d_ctx, bm->d_bs, bm->d_causal, bm->d_window, static_cast<const int4*>(bm->d_blk)};
-}
-
-// Kept keys of row q: context [c0, c1) and its own block's [b0, b1) (empty
-// ranges for context rows and dropped blocks).
-__device__ __forceinline__ void draft_row(const DraftParams& d, int q, int& c0, int& c1, int& b0, int& b1) {
-  c0 = c1 = b0 = b1 = 0;
-  if (q < d.S) return;
-  const int b = (q - d.S) / d.bs, k = (q - d.S) % d.bs;
-  const int4 bl = d.blk[b];
-  if (!bl.w) return;
-  c0 = bl.x;
-  c1 = bl.y;
-  if (d.window > 0) c0 = max(c0, bl.z + k - d.window + 1);  // real position bl.z + k minus kv < window
-  if (c1 < c0) c1 = c0;
-  b0 = d.S + b * d.bs;
-  b1 = b0 + (d.causal ? k + 1 : d.bs);
-}
-
 // Tile classes and list sizes for a draft map: one warp per tile, kept pairs
 // counted per row from its two ranges (exact).
 __global__ void k_draft_classify(int T, int BM, int BN, int nq, int nk, DraftParams d, uint8_t* kinds, int* counters,
@@ -670,8 +681,16 @@ __global__ void k_draft_classify(int T, int BM, int BN, int nq, int nk, DraftPar
 // a row's bits are its two ranges clipped to the tile; the column masks are
 // the transpose, one ballot per column over each warp's 32 rows.
 __global__ void k_draft_masks(int T, DraftParams d, const int2* slot_tile, uint32_t* mask_rows, uint32_t* mask_cols,
-                              long long n_known, const int* nnz_total, const int* n_full, long long p_cap) {
+                              long long n_known, const int* nnz_total, const int* n_full, long long p_cap,
+                              int* host_counters = nullptr, long long expect_pairs = -1) {
   pdl_wait();  // launched with programmatic dependent launch
+  // host-built lists: the kept pairs the classification found over the listed
+  // tiles (n_full[2..3], one 64-bit sum) must be every kept pair of the map
+  if (expect_pairs >= 0 && blockIdx.x == 0 && threadIdx.x == 0 &&
+      *reinterpret_cast<const unsigned long long*>(n_full + 2) != (unsigned long long)expect_pairs)
+    record_status(PT_STATUS_INVALID);
+  // the full-tile count to the host's mapped staging (host-built lists)
+  if (host_counters && blockIdx.x == 0 && threadIdx.x < 4) host_counters[threadIdx.x] = n_full[threadIdx.x];
   const long long n_part = min(n_known >= 0 ? n_known : (long long)(*nnz_total - *n_full), p_cap);
   const int r = threadIdx.x, lane = r & 31, wi = r >> 5;
   for (long long s = blockIdx.x; s < n_part; s += gridDim.x) {
@@ -1224,7 +1243,8 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
         const long long grid = std::min<long long>(p_alloc, (long long)num_sms(dev) * 16);
         if (bm->producer == PT_PRODUCER_DRAFT)
           launch_pdl(k_draft_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, draft_params(bm), slot_tile,
-                     bm->mask_rows, bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap);
+                     bm->mask_rows, bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap,
+                     static_cast<int*>(nullptr), -1LL);
         else
           launch_pdl(k_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, bm->tok, slot_tile, bm->mask_rows,
                      bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap, static_cast<int*>(nullptr),
@@ -1247,7 +1267,10 @@ int finish_map(pt_blockmap* bm, cudaStream_t s, int64_t p_bound) {
 // then two launches: tokens plus tile classes, and masks.  Nothing waits for
 // the device; the full-tile count reaches the host's staging behind an event.
 int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const std::vector<int>& row_kv, int N,
-                      const int* tab) {
+                      const int* tab, long long draft_pairs = -1) {
+  // draft maps (draft_pairs: their kept pairs in closed form) have no node
+  // tables and no token table; their tiles are classified from draft_row
+  const bool draft = bm->producer == PT_PRODUCER_DRAFT;
   const int nq = bm->nq, nk = bm->nk, dev = bm->device;
   const int* rc_row = bm->h_rc_pred;
   const int* rc_col = bm->h_rc_pred + nq;
@@ -1255,6 +1278,7 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
   const int64_t p_alloc = std::min<int64_t>(p_bound >= 0 ? p_bound : nnz, nnz);
   if (nnz * 18 + p_alloc * 4096 > ((int64_t)1 << 30) || nnz > INT_MAX / 4) {
     // too large to allocate at the bound: the device path, which sizes the lists exactly
+    if (draft) return finish_map(bm, s, p_bound);
     if (int rc = upload(bm->node_start, tab, sizeof(int) * (size_t)5 * N, dev, s)) return rc;
     k_tree_tokens<<<(bm->tpad + 255) / 256, 256, 0, s>>>(bm->T, bm->tpad, N, bm->node_end,
                                                          bm->node_start + 3 * (size_t)N,
@@ -1268,8 +1292,8 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
   }
   // every kept pair of the tree, in closed form: each node's causal triangle
   // plus its tokens times the tokens of its ancestors
-  long long expect_pairs = 0;
-  {
+  long long expect_pairs = draft ? draft_pairs : 0;
+  if (!draft) {
     const int* start = tab;
     const int* end = tab + N;
     const int* parent = tab + 2 * (size_t)N;
@@ -1284,7 +1308,7 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
   //   | node tables[5N] | q_ptr | k_ptr | q_order | k_order | kv_idx | q_idx | eT
   const size_t n_pk = 4 + 5 * (size_t)N + (size_t)(nq + 1) + (nk + 1) + nq + nk + 3 * (size_t)nnz;
   std::vector<int> pk(n_pk, 0);
-  std::copy(tab, tab + 5 * (size_t)N, pk.data() + 4);
+  if (N > 0) std::copy(tab, tab + 5 * (size_t)N, pk.data() + 4);
   int* qp = pk.data() + 4 + 5 * (size_t)N;
   int* kp = qp + nq + 1;
   int* qo = kp + nk + 1;
@@ -1329,21 +1353,32 @@ int finish_map_listed(pt_blockmap* bm, cudaStream_t s, int64_t p_bound, const st
     bm->lists_on_host = true;
     {
       ProfScope ps(s, "blockmap_classify");  // tokens, the lists into place, tile classes
-      const int tok_blocks = (bm->tpad + 255) / 256;
+      const int tok_blocks = draft ? 0 : (bm->tpad + 255) / 256;
       const long long list_work = std::max<long long>((long long)nnz * 32, 5LL * N + 2LL * nq + 2LL * nk + 2 + 2 * nnz);
       const int list_blocks = (int)std::max(1LL, std::min<long long>((list_work + 255) / 256, (long long)num_sms(dev) * 8));
-      launch_pdl(k_tree_listed, dim3(tok_blocks + list_blocks), dim3(256), 0, s,
-          bm->T, bm->tpad, N, bm->node_start, bm->tok, bm->node_of, tok_blocks, counters, nq, nk, (int)nnz, bm->q_ptr,
-          bm->k_ptr, bm->q_order, bm->k_order, bm->kv_idx, bm->q_idx, bm->kind, bm->pidx, bm->kindT, bm->pidxT,
-          slot_tile, (long long)bm->p_cap);
+      if (draft)
+        launch_pdl(k_tree_listed<true>, dim3(tok_blocks + list_blocks), dim3(256), 0, s, bm->T, bm->tpad, N,
+                   bm->node_start, bm->tok, bm->node_of, tok_blocks, counters, nq, nk, (int)nnz, bm->q_ptr, bm->k_ptr,
+                   bm->q_order, bm->k_order, bm->kv_idx, bm->q_idx, bm->kind, bm->pidx, bm->kindT, bm->pidxT,
+                   slot_tile, (long long)bm->p_cap, draft_params(bm));
+      else
+        launch_pdl(k_tree_listed<false>, dim3(tok_blocks + list_blocks), dim3(256), 0, s, bm->T, bm->tpad, N,
+                   bm->node_start, bm->tok, bm->node_of, tok_blocks, counters, nq, nk, (int)nnz, bm->q_ptr, bm->k_ptr,
+                   bm->q_order, bm->k_order, bm->kv_idx, bm->q_idx, bm->kind, bm->pidx, bm->kindT, bm->pidxT,
+                   slot_tile, (long long)bm->p_cap, DraftParams{0, 1, 0, 0, nullptr});
       PT_LAUNCHED(1);
     }
     {
       ProfScope ps(s, "blockmap_lists");  // the partial tiles' masks
       const long long grid = std::max<long long>(1, std::min<long long>(p_alloc, (long long)num_sms(dev) * 16));
-      launch_pdl(k_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, bm->tok, slot_tile, bm->mask_rows,
-                 bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap, static_cast<int*>(sl.dev),
-                 expect_pairs);
+      if (draft)
+        launch_pdl(k_draft_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, draft_params(bm), slot_tile,
+                   bm->mask_rows, bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap,
+                   static_cast<int*>(sl.dev), expect_pairs);
+      else
+        launch_pdl(k_masks, dim3((unsigned)grid), dim3(128), 0, s, bm->T, bm->tok, slot_tile, bm->mask_rows,
+                   bm->mask_cols, -1LL, bm->q_ptr + nq, counters, (long long)bm->p_cap, static_cast<int*>(sl.dev),
+                   expect_pairs);
       PT_LAUNCHED(1);
       if (cudaEventRecord(sl.ev, s) != cudaSuccess) {
         rc = 3;
@@ -1772,17 +1807,20 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
   // all of it.  Context rows keep nothing.
   const int nq_h = (int)((T + BM - 1) / BM), nk_h = (int)((T + BN - 1) / BN);
   std::vector<int> pred((size_t)nq_h + nk_h, 0);
+  std::vector<int> row_kv;  // the lists themselves: kv blocks of each q tile, ascending
   {
     std::vector<int> stamp((size_t)std::max(nk_h, 1), -1);
     for (int i = 0; i < nq_h; ++i) {
       const long long r_lo = std::max<long long>((long long)i * BM, ctx_len);
       const long long r_hi = std::min<long long>((long long)(i + 1) * BM, T);
+      const size_t row0 = row_kv.size();
       auto mark = [&](long long a, long long b) {  // kv tokens [a, b]
         for (long long j = a / BN; j <= b / BN; ++j)
           if (stamp[(size_t)j] != i) {
             stamp[(size_t)j] = i;
             ++pred[(size_t)i];
             ++pred[(size_t)nq_h + j];
+            row_kv.push_back((int)j);
           }
       };
       for (long long r = r_lo; r < r_hi;) {
@@ -1796,10 +1834,23 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
         if (x < blk[b].y) mark(x, blk[b].y - 1);
         mark(b0, b0 + (causal ? k1 : block_size - 1));
       }
+      std::sort(row_kv.begin() + row0, row_kv.end());
     }
   }
   long long nnz_exact = 0;
   for (int i = 0; i < nq_h; ++i) nnz_exact += pred[(size_t)i];
+  // every kept pair of the map in closed form: row k of a kept block keeps
+  // its context range (cut by the window) and k + 1 (causal) or all of its
+  // block's keys; the device's sum over the listed tiles must match it
+  long long draft_pairs = 0;
+  for (int b = 0; b < n_blocks; ++b) {
+    if (!blk[b].w) continue;
+    for (int k = 0; k < block_size; ++k) {
+      long long x = blk[b].x;
+      if (window > 0) x = std::max<long long>(x, (long long)blk[b].z + k - window + 1);
+      draft_pairs += std::max<long long>(0, blk[b].y - x) + (causal ? k + 1 : block_size);
+    }
+  }
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, 0, s, &bm);
   if (rc) return rc;
@@ -1818,7 +1869,7 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
   do {
     if ((rc = pool_alloc(&bm->d_blk, sizeof(int4) * blk.size(), bm->device, s))) break;
     if (n_blocks > 0 && (rc = upload(bm->d_blk, blk.data(), sizeof(int4) * (size_t)n_blocks, bm->device, s))) break;
-    rc = finish_map(bm, s, nnz_exact);  // every listed tile may be partial
+    rc = finish_map_listed(bm, s, nnz_exact, row_kv, 0, nullptr, draft_pairs);  // every listed tile may be partial
   } while (0);
   if (rc) {
     free_map(bm);
