@@ -462,7 +462,8 @@ pt_status pt_debug_wait_timeout(cudaStream_t stream);
 pt_status pt_blockmap_prepare_bwd(const pt_blockmap* bm, int32_t Hq, int32_t Hkv, int32_t D, cudaStream_t stream);
 
 /* Test hook for the device-side check of host-built lists: the next n
- * pt_build_blockmap_tree calls with 128 x 128 tiles each drop one non-empty
+ * pt_build_blockmap_tree (128 x 128 tiles) or pt_build_blockmap_draft calls
+ * each drop one non-empty
  * tile (the last entry of the longest q-tile list) from the lists the host
  * builds, keeping lengths and offsets consistent, so that only the kept-pair
  * check can notice; n <= 0 cancels.  For tests only: the maps it makes are

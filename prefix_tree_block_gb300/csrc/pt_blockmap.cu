@@ -818,8 +818,8 @@ int stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t s, bool ea
   return 0;
 }
 
-// Test hook: the next n tree builds with host-built lists drop one listed
-// tile (pt_debug_drop_listed_tile).
+// Test hook: the next n tree or draft builds with host-built lists drop one
+// listed tile (pt_debug_drop_listed_tile).
 std::atomic<int> g_drop_listed_tiles{0};
 
 // ---------------------------------------------------------------------------
@@ -871,6 +871,22 @@ void pool_free(void* p, cudaStream_t s) {
 }
 
 void debug_drop_listed_tiles(int n) { g_drop_listed_tiles.store(n > 0 ? n : 0); }
+
+// The test hook at work (pt_debug_drop_listed_tile): the last entry of the
+// longest q list leaves the host's lists (row_kv, q-major, with the row
+// lengths in pred[0, nq) and the column lengths after them), consistently.
+void maybe_drop_listed_tile(std::vector<int>& row_kv, std::vector<int>& pred, int nq) {
+  if (row_kv.empty() || g_drop_listed_tiles.load() <= 0 || g_drop_listed_tiles.fetch_sub(1) <= 0) return;
+  int i_max = 0;
+  for (int i = 1; i < nq; ++i)
+    if (pred[(size_t)i] > pred[(size_t)i_max]) i_max = i;
+  size_t pos = 0;
+  for (int i = 0; i <= i_max; ++i) pos += (size_t)pred[(size_t)i];
+  const int j = row_kv[pos - 1];
+  row_kv.erase(row_kv.begin() + (long)(pos - 1));
+  --pred[(size_t)i_max];
+  --pred[(size_t)nq + j];
+}
 
 int pool_usage(int dev, uint64_t* used, uint64_t* reserved) {
   *used = *reserved = 0;
@@ -1626,20 +1642,7 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
       std::sort(row_kv.begin() + (long)row0, row_kv.end());
     }
   }
-  if (BM == 128 && BN == 128 && !row_kv.empty() && g_drop_listed_tiles.load() > 0 &&
-      g_drop_listed_tiles.fetch_sub(1) > 0) {
-    // test hook (pt_debug_drop_listed_tile): the last entry of the longest q
-    // list leaves the host's lists, consistently (lengths and offsets)
-    int i_max = 0;
-    for (int i = 1; i < nq_h; ++i)
-      if (pred[(size_t)i] > pred[(size_t)i_max]) i_max = i;
-    size_t pos = 0;
-    for (int i = 0; i <= i_max; ++i) pos += (size_t)pred[(size_t)i];
-    const int j = row_kv[pos - 1];
-    row_kv.erase(row_kv.begin() + (long)(pos - 1));
-    --pred[(size_t)i_max];
-    --pred[(size_t)nq_h + j];
-  }
+  if (BM == 128 && BN == 128) maybe_drop_listed_tile(row_kv, pred, nq_h);
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, N, s, &bm);
   if (rc) return rc;
@@ -1837,6 +1840,7 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
       std::sort(row_kv.begin() + row0, row_kv.end());
     }
   }
+  maybe_drop_listed_tile(row_kv, pred, nq_h);
   long long nnz_exact = 0;
   for (int i = 0; i < nq_h; ++i) nnz_exact += pred[(size_t)i];
   // every kept pair of the map in closed form: row k of a kept block keeps

@@ -127,3 +127,29 @@ def test_draft_rejects_bad_arguments():
         pt.build_blockmap_draft(64, [3], 2, block_m=64, block_n=64)
     with pytest.raises(pt.PTError):  # block size below 1
         pt.build_blockmap_draft(64, [3], 0)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 5])
+def test_draft_tile_missing_from_host_lists_is_caught_on_device(seed):
+    """Draft maps at 128 x 128 tiles are built from host lists too: the device
+    classifies only the listed tiles and checks their kept pairs against the
+    map's closed-form count, so a non-empty tile dropped from the host's lists
+    (the test hook drops one) shows up as PT_ERR_INVALID_ARG at the next sync;
+    the next build is clean and matches the oracle's map."""
+    lib = pt.load_library()
+    lay = _layout(seed)
+    want = OD.mask_blockmap(OD.draft_mask(**lay), 128, 128)
+    lib.pt_debug_drop_listed_tile(1)
+    try:
+        bm = pt.build_blockmap_draft(**lay)
+        with pytest.raises(pt.PTError) as ei:
+            pt.sync_status()
+        assert ei.value.status == pt.PT_ERR_INVALID_ARG
+        assert bm.nnz == want["nnz"] - 1
+        bm.free()
+    finally:
+        lib.pt_debug_drop_listed_tile(0)
+    bm = pt.build_blockmap_draft(**lay)
+    pt.sync_status()
+    compare_blockmap(bm.export(), want)
+    bm.free()
