@@ -2695,12 +2695,100 @@ int reserve_smem(K kernel, int bytes, int dev, int* flags) {
 // call never frees lists that a kernel of another call may still be reading.
 std::mutex g_items_mu;
 
-int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, bool allow_build,
-                       cudaStream_t s, const pt_dkdv_lists** out) {
+// Exact-fill packing of the kv-major columns, used when the workspace has
+// room for the partial sums it needs: the columns (longest first, then the
+// empty ones) are laid end to end and CTA b takes the next steps up to a
+// budget of load units (steps, plus about two steps of fixed work per item:
+// the resident K/V tile and the epilogue), a column cut at a CTA's budget
+// continuing on the next CTA as another chunk.  Every CTA then carries about
+// the mean load; longest-first packing of fixed chunks left the most loaded
+// CTA 15% above it on the GRPO batch.  No chunk is cut shorter than four
+// steps (the budget grows instead).  Returns false (nothing produced) for
+// small problems, or when the chunks would need more slots than max_slots.
+bool fill_dkdv_items(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int sms, long long total,
+                     std::vector<DkdvItem>* packed, std::vector<int4>* splits, std::vector<int>* cta, int* n_slots) {
+  constexpr long long kItemCost = 2, kMinChunk = 4;
+  if (max_slots <= 0 || sms <= 0 || total < 4LL * sms) return false;
+  struct Col {
+    long long n;
+    int j, hk;
+  };
+  std::vector<Col> cols;
+  cols.reserve((size_t)nk * Hkv);
+  for (int j = 0; j < nk; ++j)
+    for (int hk = 0; hk < Hkv; ++hk) cols.push_back(Col{(long long)g * col_cnt[j], j, hk});
+  std::stable_sort(cols.begin(), cols.end(), [](const Col& a, const Col& b) { return a.n > b.n; });
+  const int G = sms;
+  long long budget = (total + kItemCost * (long long)cols.size() + G - 1) / G;
+  for (int attempt = 0; attempt < 64; ++attempt, budget += std::max(1LL, budget / 64)) {
+    std::vector<std::vector<DkdvItem>> bins(G);
+    std::vector<long long> load(G, 0);
+    std::vector<int4> spl;
+    int sl = 0, b = 0;
+    bool fits = true;
+    for (const Col& c : cols) {
+      if (c.n == 0) break;  // the empty columns come last
+      long long rem = c.n, x = 0;
+      const int first = b;
+      int pieces = 0;
+      while (rem > 0) {
+        if (b >= G) {
+          fits = false;
+          break;
+        }
+        const long long room = budget - load[b] - kItemCost;
+        if (room <= 0 || (room < rem && room < kMinChunk)) {
+          ++b;
+          continue;
+        }
+        const long long take = std::min(rem, room);
+        bins[b].push_back(DkdvItem{c.j, c.hk, (int)x, (int)(x + take), -1, 0, 0, 0});
+        load[b] += take + kItemCost;
+        x += take;
+        rem -= take;
+        ++pieces;
+        if (rem > 0) ++b;
+      }
+      if (!fits) break;
+      if (pieces > 1) {  // a cut column: each chunk writes partial sums to a slot of its own
+        int k = 0;
+        for (int bb = first; bb <= b && k < pieces; ++bb)
+          if (!bins[bb].empty() && bins[bb].back().jb == c.j && bins[bb].back().hk == c.hk)
+            bins[bb].back().slot = sl + k++;
+        spl.push_back(make_int4(c.j, c.hk, sl, pieces));
+        sl += pieces;
+        if (sl > max_slots) return false;
+      }
+    }
+    if (!fits) continue;
+    // the empty columns (their dK and dV rows are zero) on the least loaded CTAs
+    for (const Col& c : cols) {
+      if (c.n != 0) continue;
+      int bmin = 0;
+      for (int bb = 1; bb < G; ++bb)
+        if (load[bb] < load[bmin]) bmin = bb;
+      bins[bmin].push_back(DkdvItem{c.j, c.hk, 0, 0, -1, 0, 0, 0});
+      load[bmin] += kItemCost;
+    }
+    packed->clear();
+    cta->assign(G + 1, 0);
+    for (int bb = 0; bb < G; ++bb) {
+      for (const DkdvItem& it : bins[bb]) packed->push_back(it);
+      (*cta)[bb + 1] = (int)packed->size();
+    }
+    *splits = std::move(spl);
+    *n_slots = sl;
+    return true;
+  }
+  return false;
+}
+
+int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, bool exact_fill,
+                       bool allow_build, cudaStream_t s, const pt_dkdv_lists** out) {
   pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the list cache is the map's only mutable part
   std::lock_guard<std::mutex> lk(g_items_mu);
   for (const pt_dkdv_lists* e = bm->dkdv_lists; e; e = e->next)
-    if (e->g == g && e->hkv == Hkv && e->max_slots == max_slots && e->sms == sms) {
+    if (e->g == g && e->hkv == Hkv && e->max_slots == max_slots && e->sms == sms && e->exact_fill == exact_fill) {
       *out = e;
       return 0;
     }
@@ -2728,9 +2816,14 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
     cap = LLONG_MAX / 4;
   else
     while (slots_for(cap) > max_slots) cap *= 2;
-  std::vector<DkdvItem> items;
+  std::vector<DkdvItem> packed;
   std::vector<int4> splits;
-  int slot = 0;
+  int slot = 0, grid = 0;
+  std::vector<int> cta;
+  if (exact_fill && fill_dkdv_items(col_cnt, nk, g, Hkv, max_slots, sms, total, &packed, &splits, &cta, &slot)) {
+    grid = (int)cta.size() - 1;
+  } else {
+  std::vector<DkdvItem> items;
   for (int j = 0; j < nk; ++j) {
     const int n = g * col_cnt[j];
     const int nch = n == 0 ? 1 : (int)((n + cap - 1) / cap);
@@ -2750,7 +2843,7 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
                    [](const DkdvItem& a, const DkdvItem& b) { return (a.x1 - a.x0) > (b.x1 - b.x0); });
   // LPT packing; an item costs its steps plus about two steps of fixed work
   // (the resident K/V tile and the epilogue).
-  const int grid = std::min<int>(sms, std::max<int>((int)items.size(), 1));
+  grid = std::min<int>(sms, std::max<int>((int)items.size(), 1));
   std::vector<std::vector<int>> bins(grid);
   {
     using Load = std::pair<long long, int>;
@@ -2764,12 +2857,12 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
       heap.push(l);
     }
   }
-  std::vector<DkdvItem> packed;
-  std::vector<int> cta(grid + 1, 0);
+  cta.assign(grid + 1, 0);
   packed.reserve(items.size());
   for (int b = 0; b < grid; ++b) {
     for (int i : bins[b]) packed.push_back(items[i]);
     cta[b + 1] = (int)packed.size();
+  }
   }
   pt_dkdv_lists* e = new pt_dkdv_lists();
   const size_t bi = sizeof(DkdvItem) * std::max<size_t>(packed.size(), 1);
@@ -2798,6 +2891,7 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
   e->hkv = Hkv;
   e->max_slots = max_slots;
   e->sms = sms;
+  e->exact_fill = exact_fill;
   e->n_items = (int)packed.size();
   e->grid = grid;
   e->n_splits = (int)splits.size();
@@ -2976,7 +3070,10 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
   const int sms = num_sms(dev);
   const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
   const pt_dkdv_lists* KL = nullptr;
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s, &KL))) return rc;
+  // the one-pass kernel's fixed work per item is small enough that cutting
+  // columns exactly at each CTA's share pays; the kv-major kernels of the
+  // two-pass backward keep the longest-first packing
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, dq_acc != nullptr, allow_build, s, &KL))) return rc;
   const pt_dq_lists* QL = nullptr;
   if (D == 128 && (rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
   {
@@ -3107,7 +3204,7 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
   const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
   const pt_dkdv_lists* KL = nullptr;
   const pt_dq_lists* QL = nullptr;
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s, &KL))) return rc;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, false, allow_build, s, &KL))) return rc;
   if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
   const int Tpad = bm->nq * 128;
   {
@@ -3221,7 +3318,7 @@ int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V,
   const int max_slots = partial ? (int)std::min<size_t>(partial_bytes / (sizeof(float) * 128 * 2 * D), 1 << 20) : 0;
   const pt_dkdv_lists* KL = nullptr;
   const pt_dq_lists* QL = nullptr;
-  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, allow_build, s, &KL))) return rc;
+  if ((rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, max_slots, sms, false, allow_build, s, &KL))) return rc;
   if ((rc = prepare_dq_items(bm, Hq, sms, allow_build, s, &QL))) return rc;
   const int Tpad = bm->nq * 128;
   {
@@ -3319,7 +3416,7 @@ int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStrea
   const int sms = num_sms(bm->device);
   const pt_dkdv_lists* KL = nullptr;
   const pt_dq_lists* QL = nullptr;
-  int rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, true, s, &KL);
+  int rc = prepare_dkdv_items(bm, Hq / Hkv, Hkv, 0, sms, false, true, s, &KL);
   if (!rc && D >= 128) rc = prepare_dq_items(bm, Hq, sms, true, s, &QL);
   return rc;
 }

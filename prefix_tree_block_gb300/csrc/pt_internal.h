@@ -27,7 +27,8 @@ struct pt_tok {
 // Work lists of the kv-major backward kernel for one head layout.
 struct pt_dkdv_lists {
   pt_dkdv_lists* next;
-  int g, hkv, max_slots, sms;  // the key: group size, kv heads, partial-sum slots allowed, SM count
+  int g, hkv, max_slots, sms;  // the key: group size, kv heads, partial-sum slots allowed, SM count,
+  bool exact_fill;             // and the packing (columns cut at each CTA's share, or longest first)
   int n_items, n_splits, n_slots, grid;
   void* mem;     // one pool allocation: items | splits | CTA index
   void* items;   // DkdvItem[n_items] (device), grouped by the CTA that runs them

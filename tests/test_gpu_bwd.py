@@ -155,3 +155,36 @@ def test_head_dim_64_one_pass_without_split_room():
     for g, w in zip((x.float().cpu().numpy() for x in res), want):
         assert rel_l2(g, w) <= GRAD_RL2["bf16"]
     bm.free()
+
+
+def test_head_dim_64_one_pass_columns_cut_across_ctas():
+    """Long prompt columns at a size where the one-pass kernel's work lists
+    cut them at each CTA's share of the steps: chunks of one column run on
+    consecutive CTAs and write fp32 partial sums that the finalize kernel
+    adds.  Every element against the oracle, and against the two-pass
+    backward (whose columns stay whole or are cut into equal chunks)."""
+    import prefix_tree_block_gb300 as pt
+    import torch
+
+    st = W.grpo_structure([(1800, [300, 500, 410, 222]), (600, [200, 77]), (0, [129])])
+    Hq, Hkv, D = 8, 2, 64
+    q, k, v, do = W.make_tensors(st.T, Hq, Hkv, D, "bf16", seed=13)
+    Q, K, V, dO = (x.cuda() for x in (q, k, v, do))
+    bm = pt.build_blockmap_tree(st.node_lengths, st.path_ptr, st.path_nodes)
+    O, LSE = pt.attn_fwd(Q, K, V, bm)
+    tpad = -(-st.T // 128) * 128
+    stats = 2 * (-(-(4 * tpad * Hq) // 256) * 256)
+    full = torch.empty(pt.bwd_workspace_bytes(st.T, Hq, D), dtype=torch.uint8, device="cuda")
+    small = torch.empty(stats, dtype=torch.uint8, device="cuda")
+    pt.profile_reset()
+    pt.profile_enable(True)
+    one = [x.float().cpu().numpy() for x in pt.attn_bwd(dO, Q, K, V, O, LSE, bm, workspace=full)]
+    pt.sync_status()
+    assert pt.profile_read("bwd_fused")[0] == 1
+    pt.profile_enable(False)
+    two = [x.float().cpu().numpy() for x in pt.attn_bwd(dO, Q, K, V, O, LSE, bm, workspace=small)]
+    want = orc.attn_bwd(q, k, v, do, orc.structure_labels(st))
+    for a, b, w in zip(one, two, want):
+        assert rel_l2(a, w) <= GRAD_RL2["bf16"]
+        assert rel_l2(a, b) <= 1e-2
+    bm.free()
