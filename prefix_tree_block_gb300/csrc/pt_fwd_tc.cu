@@ -549,14 +549,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
         if (slot >= 0) {
           const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const float v = ((mw[c >> 5] >> (c & 31)) & 1u) ? __uint_as_float(sr[c]) : -INFINITY;
-            sr[c] = __float_as_uint(v);
-            m8[c & 7] = fmaxf(m8[c & 7], v);
+          for (int c = 0; c < 128; c += 2) {
+            const float v0 = ((mw[c >> 5] >> (c & 31)) & 1u) ? __uint_as_float(sr[c]) : -INFINITY;
+            const float v1 = ((mw[c >> 5] >> ((c + 1) & 31)) & 1u) ? __uint_as_float(sr[c + 1]) : -INFINITY;
+            sr[c] = __float_as_uint(v0);
+            sr[c + 1] = __float_as_uint(v1);
+            m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], v0, v1);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
+          for (int c = 0; c < 128; c += 2)
+            m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
         }
         const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -567,16 +570,21 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
         // below then holds only the packed P, not the 128 scores, and the
         // exponentials overlap the PV still in flight
         const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-        float r8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) r8[k] = 0.f;
+        // scale and shift two columns per packed fma, the row sum in four
+        // packed accumulators (eight chains)
+        const unsigned long long sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
+        unsigned long long r4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float p0 = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -ref), c);
-          const float p1 = ex2_mix(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -ref), c + 1);
-          r8[(c >> 1) & 7] += p0 + p1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nref2), x0, x1);
+          const float p0 = ex2_mix(x0, c), p1 = ex2_mix(x1, c + 1);
+          r4[(c >> 1) & 3] = f2_add(r4[(c >> 1) & 3], f2_pack(p0, p1));
           sr[c >> 1] = pack_bf16(p0, p1);
         }
+        float r8[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f2_unpack(r4[k], r8[2 * k], r8[2 * k + 1]);
         const float l_blk = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
         if (C::OVL && u >= 1) {
           // PV of the previous block must be done: it reads the P columns
