@@ -252,8 +252,8 @@ pt_status pt_attn_bwd(const void* dO, const void* Q, const void* K, const void* 
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of scratch pt_attn_bwd needs: two fp32 row statistics of [Hq, Tpad]
- * entries each, Tpad = ceil(T / 128) * 128 -- Delta = rowsum(dO * O) and
- * LSE * log2(e) -- then, at head_dim 64 only, an fp32 dQ accumulator of
+ * entries each, Tpad = ceil(T / 128) * 128 -- -Delta = -rowsum(dO * O) and
+ * -LSE * log2(e), stored negated -- then, at head_dim 64 only, an fp32 dQ accumulator of
  * Tpad * Hq * 64 floats, then room for fp32 partial sums, 128 x 2D floats
  * per slot, min(256, 2 * ceil(T/128) * Hq) slots, each part rounded up to
  * 256 bytes.  The partial sums let the tensor-core backward split long
@@ -276,7 +276,7 @@ size_t pt_bwd_workspace_bytes(int32_t T, int32_t Hq, int32_t D);
  * framework's caching allocator) and offers no way to hand out scratch, or a
  * latency-critical caller for which cudaMalloc, which may synchronise the
  * device, is off limits.  The call takes the same inputs and outputs as
- * pt_attn_bwd but no workspace: its scratch (the Delta and LSE*log2(e) rows)
+ * pt_attn_bwd but no workspace: its scratch (the -Delta and -LSE*log2(e) rows)
  * lives in a fixed array inside the library, and it calls no cudaMalloc,
  * cudaFree or other allocating routine.
  *

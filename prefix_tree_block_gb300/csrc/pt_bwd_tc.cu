@@ -67,8 +67,8 @@ constexpr int kPrepTokens = 8;
 template <int D>
 __global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restrict__ dO,
                                                   const __nv_bfloat16* __restrict__ O, const float* __restrict__ LSE,
-                                                  int T, int Tpad, int Hq, float* __restrict__ delta,
-                                                  float* __restrict__ lse2, float4* __restrict__ dq_acc) {
+                                                  int T, int Tpad, int Hq, float* __restrict__ ndelta,
+                                                  float* __restrict__ nlse2, float4* __restrict__ dq_acc) {
   pdl_wait();  // launched with programmatic dependent launch
   constexpr int VPT = D > 256 ? 2 : 1;  // 16-byte vectors of dO and O per thread (a row stays within a warp)
   constexpr int TPR = D / (8 * VPT);    // threads per (token, head) row
@@ -110,10 +110,12 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const __nv_bfloat16* __restric
   for (int i = threadIdx.x; i < rows; i += 256) {
     const int h = i / kPrepTokens, ql = i % kPrepTokens, q = q0 + ql;
     const size_t row = (size_t)h * Tpad + q;  // q < Tpad: Tpad is a multiple of 128
-    delta[row] = sh_delta[ql * (Hq + 1) + h];
+    // both stored negated: the kernels form s scale_log2 - LSE log2(e) and
+    // dP - Delta as one packed fma or add per column pair
+    ndelta[row] = -sh_delta[ql * (Hq + 1) + h];
     const float l = q < T ? LSE[(size_t)h * T + q] : -INFINITY;
-    // rows that keep nothing (padding) get +inf so exp2(s - lse2) = 0
-    lse2[row] = (l == -INFINITY) ? INFINITY : l * kLog2e;
+    // rows that keep nothing (padding) get -inf so exp2(s scale_log2 + nlse2) = 0
+    nlse2[row] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
   }
 }
 
@@ -156,8 +158,8 @@ struct BwdParams {
   const int* pidx;        // mask slot per entry (-1: full)
   const int* order;       // k_order or q_order
   const uint32_t* masks;  // mask_cols (dkdv) or mask_rows (dq)
-  const float* delta;     // [Hq, Tpad]
-  const float* lse2;      // [Hq, Tpad]
+  const float* ndelta;    // [Hq, Tpad]: -Delta
+  const float* nlse2;     // [Hq, Tpad]: -LSE log2(e) (-inf for rows that keep nothing)
   __nv_bfloat16* out0;    // dK (dkdv) or dQ (dq)
   __nv_bfloat16* out1;    // dV (dkdv)
   const DkdvItem* items;  // dkdv work items, grouped by CTA
@@ -242,6 +244,21 @@ __global__ void k_split_finalize(const int4* __restrict__ splits, const float* _
 }
 
 // 64 fp32 values (as bits) -> 32 bf16x2 words.
+// P = exp2(s scale_log2 - LSE log2(e)) of two columns (s0, s1: raw scores;
+// sc2: scale_log2 in both halves; nl2: the two columns' -LSE log2(e))
+__device__ __forceinline__ void p_pair(uint32_t s0, uint32_t s1, unsigned long long sc2, unsigned long long nl2,
+                                       int c, float& p0, float& p1) {
+  float x0, x1;
+  f2_unpack(f2_fma(f2_pack(__uint_as_float(s0), __uint_as_float(s1)), sc2, nl2), x0, x1);
+  p0 = ex2_mix(x0, c);
+  p1 = ex2_mix(x1, c + 1);
+}
+// dS = P (dP - Delta) of two columns (nd2: the two columns' -Delta)
+__device__ __forceinline__ void ds_pair(float p0, float p1, uint32_t d0, uint32_t d1, unsigned long long nd2,
+                                        float& ds0, float& ds1) {
+  f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(d0), __uint_as_float(d1)), nd2)), ds0, ds1);
+}
+
 __device__ __forceinline__ void pack64(const uint32_t* v, uint32_t* out) {
 #pragma unroll
   for (int c = 0; c < 32; ++c) out[c] = pack_bf16(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
@@ -394,8 +411,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             tma_load_3d(st + L::ST_Q + pn * C::PANEL, &mQ, &B->st_full[s], pn * 64, h, i * 128);
             tma_load_3d(st + L::ST_DO + pn * C::PANEL, &mdO, &B->st_full[s], pn * 64, h, i * 128);
           }
-          bulk_load(st + L::ST_L, p.lse2 + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
-          bulk_load(st + L::ST_D, p.delta + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
+          bulk_load(st + L::ST_L, p.nlse2 + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
+          bulk_load(st + L::ST_D, p.ndelta + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
           if (slot >= 0) bulk_load(st + L::ST_M, p.masks + (size_t)slot * 512, 2048, &B->st_full[s]);
           ++sc;
         }
@@ -593,18 +610,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tc_fence_before();
           mbar_arrive(&B->s_free);  // S^T and dP^T are in registers: the MMA may reuse them
           uint32_t pk2[32];
+          // scalar here: packed pairs made this kernel spill
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 lv = l2[c4], dv = dl[c4];
-            const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+            const float4 lv = l2[c4], dv = dl[c4];  // -LSE log2(e) and -Delta of the 4 columns
+            const float nla[4] = {lv.x, lv.y, lv.z, lv.w}, nda[4] = {dv.x, dv.y, dv.z, dv.w};
             float pv[4], dsv[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int c = c4 * 4 + k;
               const uint32_t word = c < 32 ? mk.x : mk.y;
-              float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
+              const float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, nla[k]), c);
               pv[k] = ((word >> (c & 31)) & 1u) ? pr : 0.f;
-              dsv[k] = pv[k] * (__uint_as_float(dr[c]) - da[k]);
+              dsv[k] = pv[k] * (__uint_as_float(dr[c]) + nda[k]);
             }
             pk[2 * c4] = pack_bf16(pv[0], pv[1]);
             pk[2 * c4 + 1] = pack_bf16(pv[2], pv[3]);
@@ -630,19 +648,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_ld32(tS, sr);
           tmem_ld32(tS + 32, sr + 32);
           tmem_ld_wait();
+          const unsigned long long sc2 = f2_splat(p.scale_log2);
           const auto pmath = [&](auto masked) {
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
-              const float4 lv = l2[c4];
-              const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+              const float4 nl = l2[c4];  // -LSE log2(e) of the 4 columns
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int c = c4 * 4 + k;
-                const float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
-                if constexpr (decltype(masked)::value)
-                  sr[c] = __float_as_uint((((c < 32 ? mk.x : mk.y) >> (c & 31)) & 1u) ? pr : 0.f);
-                else
-                  sr[c] = __float_as_uint(pr);
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int c = c4 * 4 + 2 * k2;
+                float p0, p1;
+                p_pair(sr[c], sr[c + 1], sc2, k2 ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y), c, p0, p1);
+                if constexpr (decltype(masked)::value) {
+                  const uint32_t word = c < 32 ? mk.x : mk.y;
+                  p0 = ((word >> (c & 31)) & 1u) ? p0 : 0.f;
+                  p1 = ((word >> ((c + 1) & 31)) & 1u) ? p1 : 0.f;
+                }
+                sr[c] = __float_as_uint(p0);
+                sr[c + 1] = __float_as_uint(p1);
               }
             }
           };
@@ -669,12 +691,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
-              const float4 dv = dl[c4];
-              const float da[4] = {dv.x, dv.y, dv.z, dv.w};
+              const float4 nd = dl[c4];  // -Delta of the 4 columns
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int c = c4 * 4 + k;
-                sr[c] = __float_as_uint(__uint_as_float(sr[c]) * (__uint_as_float(dr[c]) - da[k]));
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int c = c4 * 4 + 2 * k2;
+                float d0, d1;
+                ds_pair(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), dr[c], dr[c + 1],
+                        k2 ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y), d0, d1);
+                sr[c] = __float_as_uint(d0);
+                sr[c + 1] = __float_as_uint(d1);
               }
             }
           }
@@ -845,8 +870,8 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
           mbar_expect_tx(&B->st_full[s], 2 * C::TILE + 1024 + (slot >= 0 ? 2048 : 0));
           tma_load_3d(st + L::ST_Q, &mQ, &B->st_full[s], 0, h, i * 128);
           tma_load_3d(st + L::ST_DO, &mdO, &B->st_full[s], 0, h, i * 128);
-          bulk_load(st + L::ST_L, p.lse2 + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
-          bulk_load(st + L::ST_D, p.delta + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
+          bulk_load(st + L::ST_L, p.nlse2 + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
+          bulk_load(st + L::ST_D, p.ndelta + (size_t)h * p.Tpad + i * 128, 512, &B->st_full[s]);
           if (slot >= 0) bulk_load(st + L::ST_M, p.masks + (size_t)slot * 512, 2048, &B->st_full[s]);
           ++sc;
         }
@@ -1091,24 +1116,36 @@ __global__ void __launch_bounds__(FusedL::THREADS, 1)
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&B->s_free);  // S^T and dP^T are in registers: the MMA may reuse them
+          const unsigned long long sc2 = f2_splat(p.scale_log2);
+          // the keep bits only on partial tiles (uniform over the CTA)
+          const auto body = [&](auto masked) {
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 lv = l2[c4], dv = dl[c4];
-            const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
-            float pv[4], dsv[4];
+            for (int c4 = 0; c4 < 16; ++c4) {
+              const float4 nl = l2[c4], nd = dl[c4];  // -LSE log2(e) and -Delta of the 4 columns
+              float pv[4], dsv[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int c = c4 * 4 + k;
-              const uint32_t word = c < 32 ? mk.x : mk.y;
-              float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[k]), c);
-              pv[k] = ((word >> (c & 31)) & 1u) ? pr : 0.f;
-              dsv[k] = pv[k] * (__uint_as_float(dr[c]) - da[k]);
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int c = c4 * 4 + 2 * k2;
+                p_pair(sr[c], sr[c + 1], sc2, k2 ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y), c, pv[2 * k2],
+                       pv[2 * k2 + 1]);
+                if constexpr (decltype(masked)::value) {
+                  const uint32_t word = c < 32 ? mk.x : mk.y;
+                  pv[2 * k2] = ((word >> (c & 31)) & 1u) ? pv[2 * k2] : 0.f;
+                  pv[2 * k2 + 1] = ((word >> ((c + 1) & 31)) & 1u) ? pv[2 * k2 + 1] : 0.f;
+                }
+                ds_pair(pv[2 * k2], pv[2 * k2 + 1], dr[c], dr[c + 1], k2 ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y),
+                        dsv[2 * k2], dsv[2 * k2 + 1]);
+              }
+              pk[2 * c4] = pack_bf16(pv[0], pv[1]);
+              pk[2 * c4 + 1] = pack_bf16(pv[2], pv[3]);
+              pk2[2 * c4] = pack_bf16(dsv[0], dsv[1]);
+              pk2[2 * c4 + 1] = pack_bf16(dsv[2], dsv[3]);
             }
-            pk[2 * c4] = pack_bf16(pv[0], pv[1]);
-            pk[2 * c4 + 1] = pack_bf16(pv[2], pv[3]);
-            pk2[2 * c4] = pack_bf16(dsv[0], dsv[1]);
-            pk2[2 * c4 + 1] = pack_bf16(dsv[2], dsv[3]);
-          }
+          };
+          if (slot >= 0)
+            body(std::true_type{});
+          else
+            body(std::false_type{});
         }
         // the previous step's dV, dK and dQ products must be done reading
         // packed P^T and the dS^T panels
@@ -1431,8 +1468,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         continue;
       }
-      const float l2 = p.lse2[(size_t)h * p.Tpad + q];
-      const float dl = p.delta[(size_t)h * p.Tpad + q];
+      const unsigned long long nl2 = f2_splat(p.nlse2[(size_t)h * p.Tpad + q]);  // this row's -LSE log2(e)
+      const unsigned long long nd2 = f2_splat(p.ndelta[(size_t)h * p.Tpad + q]);  // and -Delta
       for (int x = 0; x < n; ++x) {
         const uint32_t y = sc + x, s = y % S;
         ok = mbar_wait(&B->s_full[0], y & 1, abort_flag) && mbar_wait(&B->st_full[s], (y / S) & 1, abort_flag);
@@ -1453,21 +1490,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&B->s_free);  // S and dP are in registers: the MMA may reuse them
-        if (slot >= 0) {
+        const unsigned long long sc2 = f2_splat(p.scale_log2);
+        const auto body = [&](auto masked) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const uint32_t word = c < 32 ? mk.x : mk.y;
-            float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
-            pr = ((word >> (c & 31)) & 1u) ? pr : 0.f;
-            dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - dl));
+          for (int c = 0; c < 64; c += 2) {
+            float p0, p1, d0, d1;
+            p_pair(sr[c], sr[c + 1], sc2, nl2, c, p0, p1);
+            if constexpr (decltype(masked)::value) {
+              const uint32_t word = c < 32 ? mk.x : mk.y;
+              p0 = ((word >> (c & 31)) & 1u) ? p0 : 0.f;
+              p1 = ((word >> ((c + 1) & 31)) & 1u) ? p1 : 0.f;
+            }
+            ds_pair(p0, p1, dr[c], dr[c + 1], nd2, d0, d1);
+            dr[c] = __float_as_uint(d0);
+            dr[c + 1] = __float_as_uint(d1);
           }
-        } else {  // full tile: no mask
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
-            dr[c] = __float_as_uint(pr * (__uint_as_float(dr[c]) - dl));
-          }
-        }
+        };
+        if (slot >= 0)
+          body(std::true_type{});
+        else  // full tile: no mask
+          body(std::false_type{});
         uint32_t pk[32];
         pack64(dr, pk);
         if (y > 0) {  // the previous dQ MMA must be done reading the dS region
@@ -1812,8 +1854,8 @@ __global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
       const int h = itm.y, e0 = itm.z, n = itm.w;
       const int q = itm.x * 128 + r;
       __nv_bfloat16* orow = p.out0 + ((size_t)q * p.Hq + h) * D + hw * (D / 2);  // this warpgroup's columns
-      const float l2 = p.lse2[(size_t)h * p.Tpad + q];
-      const float dl = p.delta[(size_t)h * p.Tpad + q];
+      const unsigned long long nl2 = f2_splat(p.nlse2[(size_t)h * p.Tpad + q]);  // this row's -LSE log2(e)
+      const unsigned long long nd2 = f2_splat(p.ndelta[(size_t)h * p.Tpad + q]);  // and -Delta
       int slot = p.pidx[e0];
       uint2 mk = slot >= 0 ? masks[(size_t)slot * 256 + 2 * r + hw] : make_uint2(0xffffffffu, 0xffffffffu);
       for (int x = 0; x < n; ++x, ++y) {
@@ -1838,17 +1880,25 @@ __global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&B->s_loaded[b]);  // dP may now overwrite S
-        if (full) {
+        const unsigned long long sc2 = f2_splat(p.scale_log2);
+        const auto pmath = [&](auto masked) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const uint32_t word = c < 32 ? mk.x : mk.y;
-            const float pr = ex2_mix(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2), c);
-            sr[c] = __float_as_uint(((word >> (c & 31)) & 1u) ? pr : 0.f);
+          for (int c = 0; c < 64; c += 2) {
+            float p0, p1;
+            p_pair(sr[c], sr[c + 1], sc2, nl2, c, p0, p1);
+            if constexpr (decltype(masked)::value) {
+              const uint32_t word = c < 32 ? mk.x : mk.y;
+              p0 = ((word >> (c & 31)) & 1u) ? p0 : 0.f;
+              p1 = ((word >> ((c + 1) & 31)) & 1u) ? p1 : 0.f;
+            }
+            sr[c] = __float_as_uint(p0);
+            sr[c + 1] = __float_as_uint(p1);
           }
-        }
+        };
+        if (full)
+          pmath(std::false_type{});
+        else
+          pmath(std::true_type{});
         ok = mbar_wait(&B->dp_full[b], ph, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -1862,9 +1912,12 @@ __global__ void __launch_bounds__(DqpCfg<D>::THREADS, 1)
           tmem_ld32(tl + col + 32, dr + 32);
           tmem_ld_wait();
 #pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2)
-            pk[c2] = pack_bf16(__uint_as_float(sr[2 * c2]) * (__uint_as_float(dr[2 * c2]) - dl),
-                               __uint_as_float(sr[2 * c2 + 1]) * (__uint_as_float(dr[2 * c2 + 1]) - dl));
+          for (int c2 = 0; c2 < 32; ++c2) {
+            float d0, d1;
+            ds_pair(__uint_as_float(sr[2 * c2]), __uint_as_float(sr[2 * c2 + 1]), dr[2 * c2], dr[2 * c2 + 1], nd2, d0,
+                    d1);
+            pk[c2] = pack_bf16(d0, d1);
+          }
         }
         tmem_st32(tl + col, pk);
         tmem_st_wait();
@@ -2191,10 +2244,10 @@ __global__ void __launch_bounds__(320, 1)
         }
         continue;
       }
-      float l2r = 0.f, dlr = 0.f;  // q-major: this row's statistics
+      float l2r = 0.f, dlr = 0.f;  // q-major: this row's -LSE log2(e) and -Delta
       if (!C::KV_MAJOR) {
-        l2r = p.lse2[(size_t)hh * p.Tpad + row];
-        dlr = p.delta[(size_t)hh * p.Tpad + row];
+        l2r = p.nlse2[(size_t)hh * p.Tpad + row];
+        dlr = p.ndelta[(size_t)hh * p.Tpad + row];
       }
       for (int x = 0; x < n; ++x) {
         int minor, head, slot;
@@ -2202,9 +2255,9 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t yy = y + 2 * x + hw, b = yy & 1;
         uint2 mk = make_uint2(0xffffffffu, 0xffffffffu);
         if (slot >= 0) mk = masks[(size_t)slot * 256 + 2 * r + hw];
-        // kv-major: statistics of this half's 64 q columns (uniform over the warp)
-        const float4* l4 = reinterpret_cast<const float4*>(p.lse2 + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
-        const float4* d4 = reinterpret_cast<const float4*>(p.delta + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
+        // kv-major: -LSE log2(e) and -Delta of this half's 64 q columns (uniform over the warp)
+        const float4* l4 = reinterpret_cast<const float4*>(p.nlse2 + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
+        const float4* d4 = reinterpret_cast<const float4*>(p.ndelta + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
         ok = mbar_wait(&B->s_full[b], (yy >> 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -2239,9 +2292,9 @@ __global__ void __launch_bounds__(320, 1)
           for (int j = 0; j < 4; ++j) {
             const int c = 4 * c4 + j;
             const uint32_t word = c < 32 ? mk.x : mk.y;
-            float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[j]));
+            float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, la[j]));
             pr = ((word >> (c & 31)) & 1u) ? pr : 0.f;
-            v[j] = C::HAS_DP ? pr * (__uint_as_float(dr[c]) - da[j]) : pr;
+            v[j] = C::HAS_DP ? pr * (__uint_as_float(dr[c]) + da[j]) : pr;
           }
           pk[2 * c4] = pack_bf16(v[0], v[1]);
           pk[2 * c4 + 1] = pack_bf16(v[2], v[3]);
@@ -2570,10 +2623,10 @@ __global__ void __launch_bounds__(Bwd512Cfg::THREADS, 1)
         }
         continue;
       }
-      float l2r = 0.f, dlr = 0.f;  // q-major: this row's statistics
+      float l2r = 0.f, dlr = 0.f;  // q-major: this row's -LSE log2(e) and -Delta
       if (!KV_MAJOR) {
-        l2r = p.lse2[(size_t)hh * p.Tpad + row];
-        dlr = p.delta[(size_t)hh * p.Tpad + row];
+        l2r = p.nlse2[(size_t)hh * p.Tpad + row];
+        dlr = p.ndelta[(size_t)hh * p.Tpad + row];
       }
       for (int x = 0; x < n; ++x) {
         int minor, head, slot;
@@ -2581,9 +2634,9 @@ __global__ void __launch_bounds__(Bwd512Cfg::THREADS, 1)
         uint4 mk = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
         if (slot >= 0) mk = masks[(size_t)slot * 128 + r];
         const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
-        // kv-major: statistics of the step's 128 q columns (uniform over the warp)
-        const float4* l4 = reinterpret_cast<const float4*>(p.lse2 + (size_t)head * p.Tpad + minor * 128);
-        const float4* d4 = reinterpret_cast<const float4*>(p.delta + (size_t)head * p.Tpad + minor * 128);
+        // kv-major: -LSE log2(e) and -Delta of the step's 128 q columns (uniform over the warp)
+        const float4* l4 = reinterpret_cast<const float4*>(p.nlse2 + (size_t)head * p.Tpad + minor * 128);
+        const float4* d4 = reinterpret_cast<const float4*>(p.ndelta + (size_t)head * p.Tpad + minor * 128);
         ok = mbar_wait(s_full, (y + x) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -2619,9 +2672,9 @@ __global__ void __launch_bounds__(Bwd512Cfg::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int c = 4 * c4 + j, cc = 64 * h2 + c;  // column within the step
-              float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -la[j]));
+              float pr = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, la[j]));
               pr = ((mw[cc >> 5] >> (cc & 31)) & 1u) ? pr : 0.f;
-              v[j] = HAS_DP ? pr * (__uint_as_float(dr[c]) - da[j]) : pr;
+              v[j] = HAS_DP ? pr * (__uint_as_float(dr[c]) + da[j]) : pr;
             }
             pk[2 * c4] = pack_bf16(v[0], v[1]);
             pk[2 * c4 + 1] = pack_bf16(v[2], v[3]);
@@ -3092,8 +3145,8 @@ int launch_bwd(const void* dO, const void* Q, const void* K, const void* V, cons
       !make_tmap_thd(&mdQ, dQ, T, Hq, D, 128))
     return 3;
   BwdParams p{};
-  p.delta = delta;
-  p.lse2 = lse2;
+  p.ndelta = delta;
+  p.nlse2 = lse2;
   p.T = T;
   p.Tpad = Tpad;
   p.Hq = Hq;
@@ -3224,8 +3277,8 @@ int launch_bwd_wide(const void* dO, const void* Q, const void* K, const void* V,
       !make_tmap_thd(&mKh, K, T, Hkv, D, 64) || !make_tmap_thd(&mVh, V, T, Hkv, D, 64))
     return 3;
   BwdParams p{};
-  p.delta = delta;
-  p.lse2 = lse2;
+  p.ndelta = delta;
+  p.nlse2 = lse2;
   p.T = T;
   p.Tpad = Tpad;
   p.Hq = Hq;
@@ -3338,8 +3391,8 @@ int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V,
       !make_tmap_thd(&mV, V, T, Hkv, D, 128) || !make_tmap_thd(&mdO, dO, T, Hq, D, 128))
     return 3;
   BwdParams p{};
-  p.delta = delta;
-  p.lse2 = lse2;
+  p.ndelta = delta;
+  p.nlse2 = lse2;
   p.T = T;
   p.Tpad = Tpad;
   p.Hq = Hq;

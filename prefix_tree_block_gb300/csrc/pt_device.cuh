@@ -99,6 +99,12 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_splat(float v) { return f2_pack(v, v); }
 // three-input maximum
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
