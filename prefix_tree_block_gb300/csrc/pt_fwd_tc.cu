@@ -1125,7 +1125,8 @@ __global__ void __launch_bounds__(Fwd512Cfg::THREADS, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sr[c]));
+            for (int c = 0; c < 128; c += 2)
+              m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
             const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                    fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float m_blk = mx * p.scale_log2;
@@ -1157,16 +1158,21 @@ __global__ void __launch_bounds__(Fwd512Cfg::THREADS, 1)
             ref = m_new;
           }
           const float rf = (ref == -INFINITY) ? 0.f : ref;
-          float r8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) r8[k] = 0.f;
+          // scale and shift two columns per packed fma, the row sum in four
+          // packed accumulators (eight chains)
+          const unsigned long long sc2 = f2_pack(p.scale_log2, p.scale_log2), nrf2 = f2_pack(-rf, -rf);
+          unsigned long long r4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int c = 0; c < 128; c += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -rf));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -rf));
-            r8[(c >> 1) & 7] += p0 + p1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nrf2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            r4[(c >> 1) & 3] = f2_add(r4[(c >> 1) & 3], f2_pack(p0, p1));
             sr[c >> 1] = pack_bf16(p0, p1);
           }
+          float r8[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) f2_unpack(r4[k], r8[2 * k], r8[2 * k + 1]);
           if (hf == 0) l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
           tmem_st32(sb + 0, sr + 0);  // P over S (bf16 pairs in the first 64 columns)
           tmem_st32(sb + 32, sr + 32);
