@@ -98,11 +98,18 @@ struct FwdCfg {
   // (TWO) the producer and MMA warps fill a second warpgroup (one warp
   // idle); registers move to the softmax warpgroup (setmaxnreg), the split
   // adding up to the launch's 128 per thread (the kernel must be built with 128)
-  static constexpr int THREADS = TWO ? 256 : NH * 128 + (OVL ? 96 : 64);
+  // (NH = 2) the producer and MMA warps fill a third warpgroup (two warps
+  // idle), so that the softmax warpgroups can take registers with setmaxnreg:
+  // with ten warps one SM sub-partition holds three of them and its 16 K
+  // registers cap every thread at 168, the launch's count; 216 for the
+  // softmax and 72 for the rest add up to it
+  static constexpr bool SPLIT = TWO || NH == 2;
+  static constexpr int THREADS = TWO ? 256 : NH == 2 ? 384 : NH * 128 + (OVL ? 96 : 64);
   static constexpr int CTAS_PER_SM = TWO ? 2 : 1;
   static constexpr int TMEM_COLS = TWO ? 256 : 512;
-  static constexpr int REG_SOFTMAX = 184, REG_CTRL = 72, REG_LAUNCH = 128;
-  static_assert(!TWO || REG_SOFTMAX + REG_CTRL == 2 * REG_LAUNCH, "register split");
+  static constexpr int REG_SOFTMAX = TWO ? 184 : 216, REG_CTRL = 72, REG_LAUNCH = TWO ? 128 : 168;
+  static_assert(!SPLIT || NH * 128 * REG_SOFTMAX + (THREADS - NH * 128) * REG_CTRL == THREADS * REG_LAUNCH,
+                "register split");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TM_O + NH * D <= TMEM_COLS, "TMEM budget");
 };
@@ -742,7 +749,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
     if (!ok) *abort_flag = 1;
     if (C::OVL && r == 0) bulk_wait0();  // this warpgroup's O stores have landed
   };
-  if constexpr (C::TWO) {
+  if constexpr (C::SPLIT) {
     // whole warpgroups take their registers first, so that each setmaxnreg
     // dominates the code of its warpgroup (ptxas then allocates each region
     // to its own count)
@@ -752,8 +759,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, FwdCfg<D, NH>::CTAS_PE
         producer_role();
       else if (warp == ISSUER)
         issuer_role();
-      else if (warp == ISSUER_PV)
-        pv_role();  // (warp 7 has no role)
+      else if (C::OVL && warp == ISSUER_PV)
+        pv_role();  // (the other warps of this warpgroup have no role)
     } else {
       regs_inc<C::REG_SOFTMAX>();
       softmax_role();
@@ -790,9 +797,9 @@ int launch_fwd(const void* Q, const void* K, const void* V, int T, int Hq, int H
     }
     attr_set[dev] = 1;
   }
-  if constexpr (C::TWO) {
-    // the register split adds up to 128 per thread at launch: a build with
-    // another count would leave setmaxnreg.inc waiting, so it is refused
+  if constexpr (C::SPLIT) {
+    // the register split adds up to the launch's count per thread: a build
+    // with another count would leave setmaxnreg.inc waiting, so it is refused
     static int regs_ok[64] = {0};
     if (dev >= 0 && dev < 64 && !regs_ok[dev]) {
       cudaFuncAttributes fa{};
