@@ -1990,7 +1990,13 @@ struct WideCfg {
   static constexpr int OFF_R = 0;
   static constexpr int OFF_L = NR * RTILE;
   static constexpr int OFF_E = OFF_L + LS * HTILE;
-  static constexpr int OFF_BAR = OFF_E + ES * HTILE;
+  // per late slot: the half-step's -LSE log2(e) and -Delta rows (kv-major),
+  // copied with its tile, and its mask slot (written by the producer)
+  static constexpr int STAT = 512;
+  static constexpr int STAT_TX = KV_MAJOR ? (HAS_DP ? 512 : 256) : 0;
+  static constexpr int OFF_STAT = OFF_E + ES * HTILE;
+  static constexpr int OFF_META = OFF_STAT + LS * STAT;
+  static constexpr int OFF_BAR = OFF_META + 16 * LS;
   static constexpr int OFF_MISC = OFF_BAR + 256;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TM_ACC = 256;  // buffers b at 128 b: S at +0, dP at +64
@@ -2013,6 +2019,7 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   WideBars* B = reinterpret_cast<WideBars*>(smem + C::OFF_BAR);
+  volatile int* meta = reinterpret_cast<volatile int*>(smem + C::OFF_META);  // [LS][4]: mask slot of the late slot's half-step
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -2112,10 +2119,16 @@ __global__ void __launch_bounds__(320, 1)
             {
               const uint32_t s = y % C::LS;
               if (y >= C::LS && !(ok = mbar_wait(&B->l_empty[s], (y / C::LS - 1) & 1, abort_flag))) break;
-              mbar_expect_tx(&B->l_full[s], C::HTILE);
+              meta[4 * s] = slot;  // made visible by the arrive below
+              mbar_expect_tx(&B->l_full[s], C::HTILE + C::STAT_TX);
 #pragma unroll
               for (int pn = 0; pn < C::NP; ++pn)
                 tma_load_3d(smem + C::OFF_L + s * C::HTILE + pn * C::HPANEL, &mL, &B->l_full[s], pn * 64, hs, row);
+              if (C::KV_MAJOR) {  // this half's 64 q rows: row is a multiple of 64, so both copies are aligned
+                uint8_t* st = smem + C::OFF_STAT + s * C::STAT;
+                bulk_load(st, p.nlse2 + (size_t)head * p.Tpad + row, 256, &B->l_full[s]);
+                if (C::HAS_DP) bulk_load(st + 256, p.ndelta + (size_t)head * p.Tpad + row, 256, &B->l_full[s]);
+              }
               ++nl;
             }
             {
@@ -2251,14 +2264,19 @@ __global__ void __launch_bounds__(320, 1)
         dlr = p.ndelta[(size_t)hh * p.Tpad + row];
       }
       for (int x = 0; x < n; ++x) {
-        int minor, head, slot;
-        step(k, x, minor, head, slot);
+        // this warpgroup's half-step yy sits in late slot yy % 2 = hw (y is even)
         const uint32_t yy = y + 2 * x + hw, b = yy & 1;
+        ok = mbar_wait(&B->l_full[hw], (yy >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const int slot = meta[4 * hw];
         uint2 mk = make_uint2(0xffffffffu, 0xffffffffu);
-        if (slot >= 0) mk = masks[(size_t)slot * 256 + 2 * r + hw];
-        // kv-major: -LSE log2(e) and -Delta of this half's 64 q columns (uniform over the warp)
-        const float4* l4 = reinterpret_cast<const float4*>(p.nlse2 + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
-        const float4* d4 = reinterpret_cast<const float4*>(p.ndelta + (size_t)head * p.Tpad + minor * 128 + 64 * hw);
+        if (slot >= 0) mk = masks[(size_t)slot * 256 + 2 * r + hw];  // in flight during the wait for S
+        // kv-major: -LSE log2(e) and -Delta of this half's 64 q columns, staged with the slot's tile
+        const float4* l4 = reinterpret_cast<const float4*>(smem + C::OFF_STAT + hw * C::STAT);
+        const float4* d4 = l4 + 16;
         ok = mbar_wait(&B->s_full[b], (yy >> 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
