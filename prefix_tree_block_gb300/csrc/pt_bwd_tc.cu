@@ -725,7 +725,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_ld32(tl + acc + c * 32, v);
         tmem_ld_wait();
         if (itm.slot < 0) {
-          if (kv < p.T) store_row32(orow + c * 32, v, mul);  // few items per CTA: the direct stores are kept
+          if constexpr (D == 128)  // eight rows of 64 contiguous bytes per store instruction
+            store_rows32(orow + c * 32, (size_t)p.Hkv * D, kv, p.T, v, mul);
+          else if (kv < p.T)  // few items per CTA at head_dim 64: the direct stores are kept
+            store_row32(orow + c * 32, v, mul);
         } else {  // one chunk of a split column: fp32 partial sums, summed later in chunk order
           float4* prow = reinterpret_cast<float4*>(p.partial + ((size_t)itm.slot * 128 + r) * (2 * D) + (hw ? D : 0) +
                                                    c * 32);
