@@ -478,6 +478,25 @@ void pt_debug_drop_listed_tile(int32_t n);
  * outputs or a negative device. */
 pt_status pt_debug_pool_usage(int32_t device, uint64_t* used_bytes, uint64_t* reserved_bytes);
 
+/* Host-only check of the backward's kv-major work lists (no GPU work): for a
+ * map whose kv block j has col_steps[j] listed q tiles (nk blocks), g q heads
+ * per kv head and Hkv kv heads, packs the items onto `ctas` CTAs exactly as
+ * pt_attn_bwd does: with exact_fill (the one-pass head_dim-64 kernel's
+ * packing) the columns laid end to end and cut at equal per-CTA budgets when
+ * max_slots partial-sum slots suffice, else longest first onto the least
+ * loaded CTA, columns longer than about one CTA's share cut into equal
+ * chunks (max_slots <= 0: none cut).  A column's steps are its (q head,
+ * listed q tile) pairs, g * col_steps[j] of them.  Writes, per item in CTA
+ * order, 5 int32 (kv block, kv head, first step, end step, slot or -1 for a
+ * whole column) to items[5 * cap_items], cta_ptr[grid + 1] (CTA b runs items
+ * [cta_ptr[b], cta_ptr[b + 1]); room for ctas + 1 entries), and *n_items,
+ * *n_slots, *grid.  PT_ERR_INVALID_ARG for bad arguments or fewer than
+ * *n_items rows of room (the counts are still written).  Meant for tests;
+ * the pages have no counterpart. */
+pt_status pt_debug_pack_dkdv(const int32_t* col_steps, int32_t nk, int32_t g, int32_t Hkv, int32_t max_slots,
+                             int32_t ctas, int32_t exact_fill, int32_t* items, int64_t cap_items, int32_t* cta_ptr,
+                             int32_t* n_items, int32_t* n_slots, int32_t* grid);
+
 /* Accuracy check of the kernels' two exp2 paths: y[i] = 2^x[i] for i < n,
  * computed with the MUFU instruction (method 0) or with the FMA-pipe
  * polynomial (method 1: Cody-Waite range reduction and a degree-3 minimax

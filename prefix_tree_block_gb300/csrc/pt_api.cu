@@ -470,6 +470,25 @@ pt_status pt_debug_pool_usage(int32_t device, uint64_t* used_bytes, uint64_t* re
   return as_status(pt::pool_usage(device, used_bytes, reserved_bytes));
 }
 
+pt_status pt_debug_pack_dkdv(const int32_t* col_steps, int32_t nk, int32_t g, int32_t Hkv, int32_t max_slots,
+                             int32_t ctas, int32_t exact_fill, int32_t* items, int64_t cap_items, int32_t* cta_ptr,
+                             int32_t* n_items, int32_t* n_slots, int32_t* grid) {
+  if (nk < 0 || (nk > 0 && !col_steps) || g < 1 || Hkv < 1 || ctas < 1 || cap_items < 0 ||
+      (cap_items > 0 && !items) || !cta_ptr || !n_items || !n_slots || !grid) {
+    set_error("pt_debug_pack_dkdv: bad arguments");
+    return PT_ERR_INVALID_ARG;
+  }
+  for (int32_t j = 0; j < nk; ++j)
+    if (col_steps[j] < 0) {
+      set_error("pt_debug_pack_dkdv: negative column length at %d", j);
+      return PT_ERR_INVALID_ARG;
+    }
+  if (pt::debug_pack_dkdv(col_steps, nk, g, Hkv, max_slots, ctas, exact_fill != 0, items, cap_items, cta_ptr, n_items,
+                          n_slots, grid))
+    return PT_ERR_INVALID_ARG;
+  return PT_OK;
+}
+
 pt_status pt_debug_exp2(const float* x, float* y, int64_t n, int32_t method, cudaStream_t stream) {
   if (n < 0 || (n > 0 && (!x || !y)) || (method != 0 && method != 1)) {
     set_error("pt_debug_exp2: bad arguments (n=%lld, method=%d)", (long long)n, method);

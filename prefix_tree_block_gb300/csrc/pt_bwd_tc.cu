@@ -2876,23 +2876,16 @@ bool fill_dkdv_items(const int* col_cnt, int nk, int g, int Hkv, int max_slots, 
   return false;
 }
 
-int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, bool exact_fill,
-                       bool allow_build, cudaStream_t s, const pt_dkdv_lists** out) {
-  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the list cache is the map's only mutable part
-  std::lock_guard<std::mutex> lk(g_items_mu);
-  for (const pt_dkdv_lists* e = bm->dkdv_lists; e; e = e->next)
-    if (e->g == g && e->hkv == Hkv && e->max_slots == max_slots && e->sms == sms && e->exact_fill == exact_fill) {
-      *out = e;
-      return 0;
-    }
-  if (!allow_build) {
-    set_error("block map's backward work lists are not prepared for this head layout "
-              "(call pt_blockmap_prepare_bwd first)");
-    return 1;
-  }
-  const int *row_cnt = nullptr, *col_cnt = nullptr;
-  if (int rc = rowcol_counts(bm, &row_cnt, &col_cnt)) return rc;
-  const int nk = bm->nk;
+// Packs the kv-major items of a map whose kv blocks have col_cnt[j] q tiles
+// listed (nk blocks), for g q heads per kv head and Hkv kv heads, onto `sms`
+// CTAs: with exact_fill the columns are cut at equal per-CTA budgets
+// (fill_dkdv_items) when max_slots allows, otherwise a column longer than
+// about one CTA's share is cut into equal chunks (as few more as max_slots
+// needs) and the items are packed longest first onto the least loaded CTA.
+// Returns the grid (CTAs that have a list); *n_slots the partial-sum slots.
+int pack_dkdv_items(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int sms, bool exact_fill,
+                    std::vector<DkdvItem>* packed_out, std::vector<int4>* splits_out, std::vector<int>* cta_out,
+                    int* n_slots) {
   long long total = 0;
   for (int j = 0; j < nk; ++j) total += (long long)g * col_cnt[j] * Hkv;
   long long cap = std::max<long long>(4, (total + sms - 1) / std::max(sms, 1));
@@ -2916,47 +2909,76 @@ int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, in
   if (exact_fill && fill_dkdv_items(col_cnt, nk, g, Hkv, max_slots, sms, total, &packed, &splits, &cta, &slot)) {
     grid = (int)cta.size() - 1;
   } else {
-  std::vector<DkdvItem> items;
-  for (int j = 0; j < nk; ++j) {
-    const int n = g * col_cnt[j];
-    const int nch = n == 0 ? 1 : (int)((n + cap - 1) / cap);
-    for (int hk = 0; hk < Hkv; ++hk) {
-      if (nch <= 1) {
-        items.push_back(DkdvItem{j, hk, 0, n, -1, 0, 0, 0});
-      } else {
-        splits.push_back(make_int4(j, hk, slot, nch));
-        for (int c = 0; c < nch; ++c)
-          items.push_back(DkdvItem{j, hk, (int)((long long)c * n / nch), (int)((long long)(c + 1) * n / nch), slot + c,
-                                   0, 0, 0});
-        slot += nch;
+    std::vector<DkdvItem> items;
+    for (int j = 0; j < nk; ++j) {
+      const int n = g * col_cnt[j];
+      const int nch = n == 0 ? 1 : (int)((n + cap - 1) / cap);
+      for (int hk = 0; hk < Hkv; ++hk) {
+        if (nch <= 1) {
+          items.push_back(DkdvItem{j, hk, 0, n, -1, 0, 0, 0});
+        } else {
+          splits.push_back(make_int4(j, hk, slot, nch));
+          for (int c = 0; c < nch; ++c)
+            items.push_back(DkdvItem{j, hk, (int)((long long)c * n / nch), (int)((long long)(c + 1) * n / nch), slot + c,
+                                     0, 0, 0});
+          slot += nch;
+        }
       }
     }
-  }
-  std::stable_sort(items.begin(), items.end(),
-                   [](const DkdvItem& a, const DkdvItem& b) { return (a.x1 - a.x0) > (b.x1 - b.x0); });
-  // LPT packing; an item costs its steps plus about two steps of fixed work
-  // (the resident K/V tile and the epilogue).
-  grid = std::min<int>(sms, std::max<int>((int)items.size(), 1));
-  std::vector<std::vector<int>> bins(grid);
-  {
-    using Load = std::pair<long long, int>;
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-    for (int b = 0; b < grid; ++b) heap.push(Load(0, b));
-    for (int i = 0; i < (int)items.size(); ++i) {
-      Load l = heap.top();
-      heap.pop();
-      bins[l.second].push_back(i);
-      l.first += (items[i].x1 - items[i].x0) + 2;
-      heap.push(l);
+    std::stable_sort(items.begin(), items.end(),
+                     [](const DkdvItem& a, const DkdvItem& b) { return (a.x1 - a.x0) > (b.x1 - b.x0); });
+    // LPT packing; an item costs its steps plus about two steps of fixed work
+    // (the resident K/V tile and the epilogue).
+    grid = std::min<int>(sms, std::max<int>((int)items.size(), 1));
+    std::vector<std::vector<int>> bins(grid);
+    {
+      using Load = std::pair<long long, int>;
+      std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+      for (int b = 0; b < grid; ++b) heap.push(Load(0, b));
+      for (int i = 0; i < (int)items.size(); ++i) {
+        Load l = heap.top();
+        heap.pop();
+        bins[l.second].push_back(i);
+        l.first += (items[i].x1 - items[i].x0) + 2;
+        heap.push(l);
+      }
+    }
+    cta.assign(grid + 1, 0);
+    packed.reserve(items.size());
+    for (int b = 0; b < grid; ++b) {
+      for (int i : bins[b]) packed.push_back(items[i]);
+      cta[b + 1] = (int)packed.size();
     }
   }
-  cta.assign(grid + 1, 0);
-  packed.reserve(items.size());
-  for (int b = 0; b < grid; ++b) {
-    for (int i : bins[b]) packed.push_back(items[i]);
-    cta[b + 1] = (int)packed.size();
+  *packed_out = std::move(packed);
+  *splits_out = std::move(splits);
+  *cta_out = std::move(cta);
+  *n_slots = slot;
+  return grid;
+}
+
+int prepare_dkdv_items(const pt_blockmap* cbm, int g, int Hkv, int max_slots, int sms, bool exact_fill,
+                       bool allow_build, cudaStream_t s, const pt_dkdv_lists** out) {
+  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the list cache is the map's only mutable part
+  std::lock_guard<std::mutex> lk(g_items_mu);
+  for (const pt_dkdv_lists* e = bm->dkdv_lists; e; e = e->next)
+    if (e->g == g && e->hkv == Hkv && e->max_slots == max_slots && e->sms == sms && e->exact_fill == exact_fill) {
+      *out = e;
+      return 0;
+    }
+  if (!allow_build) {
+    set_error("block map's backward work lists are not prepared for this head layout "
+              "(call pt_blockmap_prepare_bwd first)");
+    return 1;
   }
-  }
+  const int *row_cnt = nullptr, *col_cnt = nullptr;
+  if (int rc = rowcol_counts(bm, &row_cnt, &col_cnt)) return rc;
+  const int nk = bm->nk;
+  std::vector<DkdvItem> packed;
+  std::vector<int4> splits;
+  std::vector<int> cta;
+  int slot = 0;
+  const int grid = pack_dkdv_items(col_cnt, nk, g, Hkv, max_slots, sms, exact_fill, &packed, &splits, &cta, &slot);
   pt_dkdv_lists* e = new pt_dkdv_lists();
   const size_t bi = sizeof(DkdvItem) * std::max<size_t>(packed.size(), 1);
   const size_t bs = sizeof(int4) * std::max<size_t>(splits.size(), 1);
@@ -3501,6 +3523,29 @@ int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V,
   return 0;
 }
 }  // namespace
+
+int debug_pack_dkdv(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int ctas, bool exact_fill, int32_t* items,
+                    long long cap_items, int32_t* cta_ptr, int32_t* n_items, int32_t* n_slots, int32_t* grid) {
+  std::vector<DkdvItem> packed;
+  std::vector<int4> splits;
+  std::vector<int> cta;
+  int slots = 0;
+  const int gr = pack_dkdv_items(col_cnt, nk, g, Hkv, max_slots, ctas, exact_fill, &packed, &splits, &cta, &slots);
+  *n_items = (int32_t)packed.size();
+  *n_slots = slots;
+  *grid = gr;
+  if ((long long)packed.size() > cap_items) {
+    set_error("pt_debug_pack_dkdv: %zu items, room for %lld", packed.size(), cap_items);
+    return 1;
+  }
+  for (size_t k = 0; k < packed.size(); ++k) {
+    const DkdvItem& it = packed[k];
+    const int32_t v[5] = {it.jb, it.hk, it.x0, it.x1, it.slot};
+    std::memcpy(items + 5 * k, v, sizeof(v));
+  }
+  for (int b = 0; b <= gr; ++b) cta_ptr[b] = cta[b];
+  return 0;
+}
 
 bool bwd_tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 

@@ -193,6 +193,10 @@ int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const vo
            float* lse2, float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s);
 // Builds the work lists the allocation-free backward needs for a head layout.
 int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStream_t s);
+// Host-only: the backward's kv-major packing for given column lengths
+// (pt_debug_pack_dkdv).
+int debug_pack_dkdv(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int ctas, bool exact_fill, int32_t* items,
+                    long long cap_items, int32_t* cta_ptr, int32_t* n_items, int32_t* n_slots, int32_t* grid);
 bool bwd_tc_supported(int D);
 int wait_timeout_probe(cudaStream_t s);
 int exp2_probe(const float* x, float* y, long long n, int method, cudaStream_t s);
