@@ -478,6 +478,19 @@ void pt_debug_drop_listed_tile(int32_t n);
  * outputs or a negative device. */
 pt_status pt_debug_pool_usage(int32_t device, uint64_t* used_bytes, uint64_t* reserved_bytes);
 
+/* Host-only check of a tree map's lists (no GPU work): the q-major lists that
+ * pt_build_blockmap_tree derives on the host for the tree (node_lengths,
+ * path_ptr, path_nodes, as that call takes them) at block_m x block_n tiles,
+ * before the device classifies the listed tiles: q_ptr[nq + 1] offsets (nq =
+ * ceil(T / block_m), room for q_ptr_len entries) into kv_idx[cap], each q
+ * tile's kv blocks ascending, and *nnz the entries.  The same host checks as
+ * pt_build_blockmap_tree (PT_ERR_INVALID_ARG for a malformed tree), and
+ * PT_ERR_INVALID_ARG for too little room (*nnz is still written).  Meant for
+ * tests; the pages have no counterpart. */
+pt_status pt_debug_tree_lists(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr,
+                              const int32_t* path_nodes, int32_t n_samples, int32_t block_m, int32_t block_n,
+                              int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx, int64_t cap, int64_t* nnz);
+
 /* Host-only check of the backward's kv-major work lists (no GPU work): for a
  * map whose kv block j has col_steps[j] listed q tiles (nk blocks), g q heads
  * per kv head and Hkv kv heads, packs the items onto `ctas` CTAs exactly as

@@ -470,6 +470,19 @@ pt_status pt_debug_pool_usage(int32_t device, uint64_t* used_bytes, uint64_t* re
   return as_status(pt::pool_usage(device, used_bytes, reserved_bytes));
 }
 
+pt_status pt_debug_tree_lists(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr,
+                              const int32_t* path_nodes, int32_t n_samples, int32_t block_m, int32_t block_n,
+                              int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx, int64_t cap, int64_t* nnz) {
+  if (!q_ptr || !nnz || cap < 0 || (cap > 0 && !kv_idx)) {
+    set_error("pt_debug_tree_lists: bad output arguments");
+    return PT_ERR_INVALID_ARG;
+  }
+  if (pt::debug_tree_lists(node_lengths, n_nodes, path_ptr, path_nodes, n_samples, block_m, block_n, q_ptr, q_ptr_len,
+                           kv_idx, cap, nnz))
+    return PT_ERR_INVALID_ARG;
+  return PT_OK;
+}
+
 pt_status pt_debug_pack_dkdv(const int32_t* col_steps, int32_t nk, int32_t g, int32_t Hkv, int32_t max_slots,
                              int32_t ctas, int32_t exact_fill, int32_t* items, int64_t cap_items, int32_t* cta_ptr,
                              int32_t* n_items, int32_t* n_slots, int32_t* grid) {

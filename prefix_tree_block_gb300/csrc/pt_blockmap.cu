@@ -1505,8 +1505,11 @@ void free_map(pt_blockmap* bm) {
 
 // Tree form: validation and the Euler tour on the host (O(nodes)), token
 // coordinates and tile classes on the device.
-int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,
-               int32_t n_samples, int32_t BM, int32_t BN, cudaStream_t s, pt_blockmap** out) {
+// Checks a tree given as node lengths and sample paths and derives each
+// node's parent (-1 for a root) and the token count *T_out.  Returns 1,
+// with the error set, for a malformed tree or bad tile sizes.
+int parse_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,
+               int32_t n_samples, int32_t BM, int32_t BN, long long* T_out, std::vector<int>* parent_out) {
   if (n_nodes < 0 || n_samples < 0 || (n_nodes > 0 && !node_lengths) || !path_ptr ||
       (n_samples > 0 && !path_nodes)) {
     set_error("pt_build_blockmap_tree: null array or negative count");
@@ -1564,6 +1567,88 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
     set_error("pt_build_blockmap_tree: tile sizes must be positive (got %d x %d)", BM, BN);
     return 1;
   }
+  *T_out = T;
+  *parent_out = std::move(parent);
+  return 0;
+}
+
+// The q-major lists of a tree map, built on the host, so that nothing
+// downstream (the backward's work lists) waits for the device: q tile i
+// meets the kv blocks that its rows' kept ranges touch.  The rows of node n
+// in the tile keep every token of n's ancestors and n's own tokens up to the
+// tile's last row of n (keep = ancestor-or-self and kv <= q; ancestors come
+// first).  *row_kv: each q tile's kv blocks, ascending, tile after tile;
+// *pred: the list lengths, q tiles then kv blocks.
+void tree_host_lists(const int32_t* node_lengths, int N, const std::vector<int>& parent, long long T, int BM, int BN,
+                     std::vector<int>* row_kv_out, std::vector<int>* pred_out) {
+  std::vector<int> se((size_t)2 * std::max(N, 1));
+  int *start = se.data(), *end = start + N;
+  {
+    long long off = 0;
+    for (int i = 0; i < N; ++i) {
+      start[i] = (int)off;
+      off += node_lengths[i];
+      end[i] = (int)off;
+    }
+  }
+  const int nq_h = (int)((T + BM - 1) / BM), nk_h = (int)((T + BN - 1) / BN);
+  std::vector<int> pred((size_t)nq_h + nk_h, 0);
+  std::vector<int> row_kv;  // the q-major lists themselves, kv blocks ascending per q tile
+  {
+    std::vector<int> stamp((size_t)std::max(nk_h, 1), -1);
+    int n0 = 0;  // nodes are in token order: the first that may reach tile i
+    for (int i = 0; i < nq_h; ++i) {
+      const long long r_lo = (long long)i * BM, r_hi = std::min<long long>(r_lo + BM, T);
+      const size_t row0 = row_kv.size();
+      while (n0 < N && end[n0] <= r_lo) ++n0;
+      auto mark = [&](long long a, long long b) {  // kv tokens [a, b]
+        for (long long j = a / BN; j <= b / BN; ++j)
+          if (stamp[(size_t)j] != i) {
+            stamp[(size_t)j] = i;
+            ++pred[(size_t)i];
+            ++pred[(size_t)nq_h + j];
+            row_kv.push_back((int)j);
+          }
+      };
+      for (int n = n0; n < N && start[n] < r_hi; ++n) {
+        if (end[n] <= r_lo || node_lengths[n] == 0) continue;
+        mark(start[n], std::min<long long>(end[n], r_hi) - 1);
+        for (int a = parent[n]; a >= 0; a = parent[a])
+          if (node_lengths[a] > 0) mark(start[a], end[a] - 1);
+      }
+      std::sort(row_kv.begin() + (long)row0, row_kv.end());
+    }
+  }
+  *row_kv_out = std::move(row_kv);
+  *pred_out = std::move(pred);
+}
+
+int debug_tree_lists(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,
+                     int32_t n_samples, int32_t BM, int32_t BN, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx,
+                     int64_t cap, int64_t* nnz) {
+  long long T = 0;
+  std::vector<int> parent;
+  if (parse_tree(node_lengths, n_nodes, path_ptr, path_nodes, n_samples, BM, BN, &T, &parent)) return 1;
+  std::vector<int> pred, row_kv;
+  tree_host_lists(node_lengths, n_nodes, parent, T, BM, BN, &row_kv, &pred);
+  const long long nq = (T + BM - 1) / BM;
+  *nnz = (int64_t)row_kv.size();
+  if (q_ptr_len < nq + 1 || (int64_t)row_kv.size() > cap) {
+    set_error("pt_debug_tree_lists: room for %lld offsets and %lld entries, %lld and %zu needed", (long long)q_ptr_len,
+              (long long)cap, nq + 1, row_kv.size());
+    return 1;
+  }
+  q_ptr[0] = 0;
+  for (long long t = 0; t < nq; ++t) q_ptr[t + 1] = q_ptr[t] + pred[(size_t)t];
+  std::copy(row_kv.begin(), row_kv.end(), kv_idx);
+  return 0;
+}
+
+int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,
+               int32_t n_samples, int32_t BM, int32_t BN, cudaStream_t s, pt_blockmap** out) {
+  long long T = 0;
+  std::vector<int> parent;
+  if (parse_tree(node_lengths, n_nodes, path_ptr, path_nodes, n_samples, BM, BN, &T, &parent)) return 1;
   // Node tables in one host block: start | end | parent | tin | tout.
   // Euler tour: tin = pre-order index (children in id order), tout = tin + subtree size.
   const int N = n_nodes;
@@ -1609,39 +1694,10 @@ int build_tree(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path
     for (char c : split) m += c;
     p_bound = 2 * m * nt + nt;
   }
-  // Exact list lengths from the tree, so that nothing downstream (the
-  // backward's work lists) waits for the device: q tile i meets the kv blocks
-  // that its rows' kept ranges touch.  The rows of node n in the tile keep
-  // every token of n's ancestors and n's own tokens up to the tile's last row
-  // of n (keep = ancestor-or-self and kv <= q; ancestors come first).
-  const int nq_h = (int)((T + BM - 1) / BM), nk_h = (int)((T + BN - 1) / BN);
-  std::vector<int> pred((size_t)nq_h + nk_h, 0);
-  std::vector<int> row_kv;  // the q-major lists themselves, kv blocks ascending per q tile
-  {
-    std::vector<int> stamp((size_t)std::max(nk_h, 1), -1);
-    int n0 = 0;  // nodes are in token order: the first that may reach tile i
-    for (int i = 0; i < nq_h; ++i) {
-      const long long r_lo = (long long)i * BM, r_hi = std::min<long long>(r_lo + BM, T);
-      const size_t row0 = row_kv.size();
-      while (n0 < N && end[n0] <= r_lo) ++n0;
-      auto mark = [&](long long a, long long b) {  // kv tokens [a, b]
-        for (long long j = a / BN; j <= b / BN; ++j)
-          if (stamp[(size_t)j] != i) {
-            stamp[(size_t)j] = i;
-            ++pred[(size_t)i];
-            ++pred[(size_t)nq_h + j];
-            row_kv.push_back((int)j);
-          }
-      };
-      for (int n = n0; n < N && start[n] < r_hi; ++n) {
-        if (end[n] <= r_lo || node_lengths[n] == 0) continue;
-        mark(start[n], std::min<long long>(end[n], r_hi) - 1);
-        for (int a = parent[n]; a >= 0; a = parent[a])
-          if (node_lengths[a] > 0) mark(start[a], end[a] - 1);
-      }
-      std::sort(row_kv.begin() + (long)row0, row_kv.end());
-    }
-  }
+  // the q-major lists from the tree, on the host
+  const int nq_h = (int)((T + BM - 1) / BM);
+  std::vector<int> pred, row_kv;
+  tree_host_lists(node_lengths, N, parent, T, BM, BN, &row_kv, &pred);
   if (BM == 128 && BN == 128) maybe_drop_listed_tile(row_kv, pred, nq_h);
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, N, s, &bm);

@@ -193,6 +193,11 @@ int bwd_tc(const void* dO, const void* Q, const void* K, const void* V, const vo
            float* lse2, float* partial, size_t partial_bytes, bool allow_build, cudaStream_t s);
 // Builds the work lists the allocation-free backward needs for a head layout.
 int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStream_t s);
+// Host-only: the q-major lists a tree map's build derives on the host
+// (pt_debug_tree_lists).
+int debug_tree_lists(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,
+                     int32_t n_samples, int32_t BM, int32_t BN, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx,
+                     int64_t cap, int64_t* nnz);
 // Host-only: the backward's kv-major packing for given column lengths
 // (pt_debug_pack_dkdv).
 int debug_pack_dkdv(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int ctas, bool exact_fill, int32_t* items,
