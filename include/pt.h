@@ -491,6 +491,20 @@ pt_status pt_debug_tree_lists(const int32_t* node_lengths, int32_t n_nodes, cons
                               const int32_t* path_nodes, int32_t n_samples, int32_t block_m, int32_t block_n,
                               int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx, int64_t cap, int64_t* nnz);
 
+/* Host-only check of a draft-block map's lists (no GPU work): for the layout
+ * pt_build_blockmap_draft takes (same arguments, 128 x 128 tiles), the
+ * q-major lists its build derives on the host (q_ptr[nq + 1], nq =
+ * ceil(T / 128), room for q_ptr_len entries; kv_idx[cap], each q tile's kv
+ * blocks ascending; *nnz entries) and the closed-form count of every kept
+ * (q, kv) pair that the device's check compares its sum with (*kept_pairs).
+ * The same host checks as pt_build_blockmap_draft; PT_ERR_INVALID_ARG also
+ * for too little room (*nnz is still written).  Meant for tests; the pages
+ * have no counterpart. */
+pt_status pt_debug_draft_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                               const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                               const int32_t* anchor_doc, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx,
+                               int64_t cap, int64_t* nnz, int64_t* kept_pairs);
+
 /* Host-only check of the backward's kv-major work lists (no GPU work): for a
  * map whose kv block j has col_steps[j] listed q tiles (nk blocks), g q heads
  * per kv head and Hkv kv heads, packs the items onto `ctas` CTAs exactly as

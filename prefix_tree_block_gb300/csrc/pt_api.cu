@@ -483,6 +483,19 @@ pt_status pt_debug_tree_lists(const int32_t* node_lengths, int32_t n_nodes, cons
   return PT_OK;
 }
 
+pt_status pt_debug_draft_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                               const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                               const int32_t* anchor_doc, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx,
+                               int64_t cap, int64_t* nnz, int64_t* kept_pairs) {
+  if (!q_ptr || !nnz || !kept_pairs || cap < 0 || (cap > 0 && !kv_idx)) {
+    set_error("pt_debug_draft_lists: bad output arguments");
+    return PT_ERR_INVALID_ARG;
+  }
+  const int rc = pt::debug_draft_lists(ctx_len, n_blocks, block_size, anchors, block_keep, causal, window, ctx_doc,
+                                       anchor_doc, q_ptr, q_ptr_len, kv_idx, cap, nnz, kept_pairs);
+  return rc == 0 ? PT_OK : (rc == 2 ? PT_ERR_UNSUPPORTED : PT_ERR_INVALID_ARG);
+}
+
 pt_status pt_debug_pack_dkdv(const int32_t* col_steps, int32_t nk, int32_t g, int32_t Hkv, int32_t max_slots,
                              int32_t ctas, int32_t exact_fill, int32_t* items, int64_t cap_items, int32_t* cta_ptr,
                              int32_t* n_items, int32_t* n_slots, int32_t* grid) {

@@ -1805,9 +1805,13 @@ int build_seg(const int32_t* group_id, const int32_t* suffix_id, int32_t T, int3
   return 0;
 }
 
-int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
-                const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
-                const int32_t* anchor_doc, int32_t BM, int32_t BN, cudaStream_t s, pt_blockmap** out) {
+// Checks a draft-block layout and derives each block's context range before
+// any window, [x, y), its anchor and keep flag (int4 x, y, z, w); *T_out the
+// token count.  Returns 1 (or 2 for tiles other than 128 x 128), with the
+// error set, for a bad layout.
+int parse_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                const uint8_t* block_keep, int32_t window, const int32_t* ctx_doc, const int32_t* anchor_doc,
+                int32_t BM, int32_t BN, long long* T_out, std::vector<int4>* blk_out) {
   if (ctx_len < 0 || n_blocks < 0 || block_size < 1 || window < 0 || (n_blocks > 0 && !anchors)) {
     set_error("pt_build_blockmap_draft: negative length, block size < 1, negative window or null anchors");
     return 1;
@@ -1859,11 +1863,22 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
     }
     blk[b] = make_int4(lo, hi, anchors[b], (!block_keep || block_keep[b]) ? 1 : 0);
   }
-  // Exact list lengths on the host, as for trees.  The rows of block b in q
-  // tile i are its tokens k0..k1; row k keeps the context [x, y) cut by the
-  // window to kv >= anchor + k - window + 1 (a range that shrinks as k grows,
-  // so the rows' union is row k0's), and its own block up to k (causal) or
-  // all of it.  Context rows keep nothing.
+  *T_out = T;
+  *blk_out = std::move(blk);
+  return 0;
+}
+
+// The q-major lists of a draft-block map, built on the host as for trees.
+// The rows of block b in q tile i are its tokens k0..k1; row k keeps the
+// context [x, y) cut by the window to kv >= anchor + k - window + 1 (a range
+// that shrinks as k grows, so the rows' union is row k0's), and its own
+// block up to k (causal) or all of it.  Context rows keep nothing.  Also
+// every kept pair of the map in closed form (*pairs_out): row k of a kept
+// block keeps its context range (cut by the window) and k + 1 (causal) or
+// all of its block's keys.
+void draft_host_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const std::vector<int4>& blk,
+                      int32_t causal, int32_t window, long long T, int BM, int BN, std::vector<int>* row_kv_out,
+                      std::vector<int>* pred_out, long long* pairs_out) {
   const int nq_h = (int)((T + BM - 1) / BM), nk_h = (int)((T + BN - 1) / BN);
   std::vector<int> pred((size_t)nq_h + nk_h, 0);
   std::vector<int> row_kv;  // the lists themselves: kv blocks of each q tile, ascending
@@ -1896,12 +1911,6 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
       std::sort(row_kv.begin() + row0, row_kv.end());
     }
   }
-  maybe_drop_listed_tile(row_kv, pred, nq_h);
-  long long nnz_exact = 0;
-  for (int i = 0; i < nq_h; ++i) nnz_exact += pred[(size_t)i];
-  // every kept pair of the map in closed form: row k of a kept block keeps
-  // its context range (cut by the window) and k + 1 (causal) or all of its
-  // block's keys; the device's sum over the listed tiles must match it
   long long draft_pairs = 0;
   for (int b = 0; b < n_blocks; ++b) {
     if (!blk[b].w) continue;
@@ -1911,6 +1920,53 @@ int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int
       draft_pairs += std::max<long long>(0, blk[b].y - x) + (causal ? k + 1 : block_size);
     }
   }
+  *row_kv_out = std::move(row_kv);
+  *pred_out = std::move(pred);
+  *pairs_out = draft_pairs;
+}
+
+int debug_draft_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                      const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                      const int32_t* anchor_doc, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx, int64_t cap,
+                      int64_t* nnz, int64_t* kept_pairs) {
+  long long T = 0;
+  std::vector<int4> blk;
+  if (int rc = parse_draft(ctx_len, n_blocks, block_size, anchors, block_keep, window, ctx_doc, anchor_doc, 128, 128,
+                           &T, &blk))
+    return rc;
+  std::vector<int> row_kv, pred;
+  long long pairs = 0;
+  draft_host_lists(ctx_len, n_blocks, block_size, blk, causal, window, T, 128, 128, &row_kv, &pred, &pairs);
+  const long long nq = (T + 127) / 128;
+  *nnz = (int64_t)row_kv.size();
+  *kept_pairs = pairs;
+  if (q_ptr_len < nq + 1 || (int64_t)row_kv.size() > cap) {
+    set_error("pt_debug_draft_lists: room for %lld offsets and %lld entries, %lld and %zu needed",
+              (long long)q_ptr_len, (long long)cap, nq + 1, row_kv.size());
+    return 1;
+  }
+  q_ptr[0] = 0;
+  for (long long t = 0; t < nq; ++t) q_ptr[t + 1] = q_ptr[t] + pred[(size_t)t];
+  std::copy(row_kv.begin(), row_kv.end(), kv_idx);
+  return 0;
+}
+
+int build_draft(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                const int32_t* anchor_doc, int32_t BM, int32_t BN, cudaStream_t s, pt_blockmap** out) {
+  long long T = 0;
+  std::vector<int4> blk;
+  if (int rc = parse_draft(ctx_len, n_blocks, block_size, anchors, block_keep, window, ctx_doc, anchor_doc, BM, BN,
+                           &T, &blk))
+    return rc;
+  const int nq_h = (int)((T + BM - 1) / BM);
+  std::vector<int> pred, row_kv;
+  long long draft_pairs = 0;
+  // the device's sum of kept pairs over the listed tiles must equal draft_pairs
+  draft_host_lists(ctx_len, n_blocks, block_size, blk, causal, window, T, BM, BN, &row_kv, &pred, &draft_pairs);
+  maybe_drop_listed_tile(row_kv, pred, nq_h);
+  long long nnz_exact = 0;
+  for (int i = 0; i < nq_h; ++i) nnz_exact += pred[(size_t)i];
   pt_blockmap* bm = nullptr;
   int rc = new_map((int)T, BM, BN, 0, s, &bm);
   if (rc) return rc;

@@ -198,6 +198,12 @@ int prepare_bwd_noalloc(const pt_blockmap* bm, int Hq, int Hkv, int D, cudaStrea
 int debug_tree_lists(const int32_t* node_lengths, int32_t n_nodes, const int32_t* path_ptr, const int32_t* path_nodes,
                      int32_t n_samples, int32_t BM, int32_t BN, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx,
                      int64_t cap, int64_t* nnz);
+// Host-only: the lists and kept-pair count a draft-block map's build derives
+// on the host (pt_debug_draft_lists).
+int debug_draft_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_size, const int32_t* anchors,
+                      const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
+                      const int32_t* anchor_doc, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx, int64_t cap,
+                      int64_t* nnz, int64_t* kept_pairs);
 // Host-only: the backward's kv-major packing for given column lengths
 // (pt_debug_pack_dkdv).
 int debug_pack_dkdv(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int ctas, bool exact_fill, int32_t* items,
