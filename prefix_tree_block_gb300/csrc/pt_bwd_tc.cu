@@ -13,9 +13,11 @@
 // one pass, dQ added into the accumulator by TMA reduce-adds (not run-to-run
 // bitwise identical), then one finalize launch converts it.  Otherwise,
 // three launches on the caller's stream:
-//  1. k_bwd_prep  (HBM-bound) Delta = rowsum(dO * O) and LSE * log2(e) into
-//                 the workspace, [Hq, Tpad] each, Tpad = ceil(T/128)*128;
-//                 padding rows get values that make them contribute nothing.
+//  1. k_bwd_prep  (HBM-bound) -Delta = -rowsum(dO * O) and -LSE * log2(e)
+//                 into the workspace, [Hq, Tpad] each, Tpad = ceil(T/128)*128
+//                 (negated so that the kernels form s scale_log2 - LSE log2(e)
+//                 and dP - Delta with packed f32x2 fma and add); padding rows
+//                 get values that make them contribute nothing.
 //  2. k_bwd_dkdv  persistent, kv-major: a work item is (kv block, kv head).
 //                 K and V stay in shared memory while the q tiles of the
 //                 block's column list stream through for every q head of the
