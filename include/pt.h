@@ -505,6 +505,19 @@ pt_status pt_debug_draft_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_
                                const int32_t* anchor_doc, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx,
                                int64_t cap, int64_t* nnz, int64_t* kept_pairs);
 
+/* Host-only check of the backward's q-major work lists (no GPU work): for a
+ * map whose q tile t has row_steps[t] listed kv blocks (nq tiles) and Hq q
+ * heads, packs the (q tile, q head) items onto `ctas` CTAs exactly as the
+ * dQ kernels at head_dims 128, 256 and 512 get them: longest first onto the
+ * least loaded CTA.  Writes, per item in CTA order, 4 int32 (q tile, q head,
+ * first list entry, kv blocks) to items[4 * cap_items], per CTA 4 int32
+ * (first item, end item, kv blocks, 0) to cta_rec[4 * ctas], and *n_items,
+ * *grid and *n_empty (q tiles with no kv block, which get no item).
+ * PT_ERR_INVALID_ARG for bad arguments or fewer than *n_items rows of room.
+ * Meant for tests; the pages have no counterpart. */
+pt_status pt_debug_pack_dq(const int32_t* row_steps, int32_t nq, int32_t Hq, int32_t ctas, int32_t* items,
+                           int64_t cap_items, int32_t* cta_rec, int32_t* n_items, int32_t* grid, int32_t* n_empty);
+
 /* Host-only check of the backward's kv-major work lists (no GPU work): for a
  * map whose kv block j has col_steps[j] listed q tiles (nk blocks), g q heads
  * per kv head and Hkv kv heads, packs the items onto `ctas` CTAs exactly as

@@ -84,6 +84,7 @@ def load_library(path: Optional[str] = None):
             "pt_debug_wait_timeout": [vp],
             "pt_debug_exp2": [vp, vp, i64, i32, vp],
             "pt_debug_pack_dkdv": [vp, i32, i32, i32, i32, i32, i32, vp, i64, vp, i32p, i32p, i32p],
+            "pt_debug_pack_dq": [vp, i32, i32, i32, vp, i64, vp, i32p, i32p, i32p],
             "pt_debug_tree_lists": [vp, i32, vp, vp, i32, i32, i32, vp, i64, vp, i64, i64p],
             "pt_debug_draft_lists": [i32, i32, i32, vp, vp, i32, i32, vp, vp, vp, i64, vp, i64, i64p, i64p],
             "pt_blockmap_prepare_bwd": [vp, i32, i32, i32, vp],

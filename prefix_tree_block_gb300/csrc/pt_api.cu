@@ -496,6 +496,23 @@ pt_status pt_debug_draft_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_
   return rc == 0 ? PT_OK : (rc == 2 ? PT_ERR_UNSUPPORTED : PT_ERR_INVALID_ARG);
 }
 
+pt_status pt_debug_pack_dq(const int32_t* row_steps, int32_t nq, int32_t Hq, int32_t ctas, int32_t* items,
+                           int64_t cap_items, int32_t* cta_rec, int32_t* n_items, int32_t* grid, int32_t* n_empty) {
+  if (nq < 0 || (nq > 0 && !row_steps) || Hq < 1 || ctas < 1 || cap_items < 0 || (cap_items > 0 && !items) ||
+      !cta_rec || !n_items || !grid || !n_empty) {
+    set_error("pt_debug_pack_dq: bad arguments");
+    return PT_ERR_INVALID_ARG;
+  }
+  for (int32_t t = 0; t < nq; ++t)
+    if (row_steps[t] < 0) {
+      set_error("pt_debug_pack_dq: negative row length at %d", t);
+      return PT_ERR_INVALID_ARG;
+    }
+  if (pt::debug_pack_dq(row_steps, nq, Hq, ctas, items, cap_items, cta_rec, n_items, grid, n_empty))
+    return PT_ERR_INVALID_ARG;
+  return PT_OK;
+}
+
 pt_status pt_debug_pack_dkdv(const int32_t* col_steps, int32_t nk, int32_t g, int32_t Hkv, int32_t max_slots,
                              int32_t ctas, int32_t exact_fill, int32_t* items, int64_t cap_items, int32_t* cta_ptr,
                              int32_t* n_items, int32_t* n_slots, int32_t* grid) {

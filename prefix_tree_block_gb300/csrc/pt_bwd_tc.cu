@@ -3040,22 +3040,14 @@ int zero_empty_dq(const pt_dq_lists* L, void* dQ, int T, int Hq, int D, cudaStre
 // every (q tile, head) with at least one kv block, packed longest first onto
 // the grid's CTAs by LPT list scheduling and stored grouped by CTA, plus the
 // q tiles with no kv block at all (their dQ rows are zero).
-int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, cudaStream_t s,
-                     const pt_dq_lists** out) {
-  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the list cache is the map's only mutable part
-  std::lock_guard<std::mutex> lk(g_items_mu);
-  for (const pt_dq_lists* e = bm->dq_lists; e; e = e->next)
-    if (e->hq == Hq && e->sms == sms) {
-      *out = e;
-      return 0;
-    }
-  if (!allow_build) {
-    set_error("block map's dQ work lists are not prepared for this head count (call pt_blockmap_prepare_bwd first)");
-    return 1;
-  }
-  const int *row_cnt = nullptr, *col_cnt = nullptr;
-  if (int rc = rowcol_counts(bm, &row_cnt, &col_cnt)) return rc;
-  const int nq = bm->nq;
+// Packs the q-major items (q tile, q head, first list entry, kv blocks) of a
+// map whose q tiles have row_cnt[t] kv blocks listed (nq tiles) onto `sms`
+// CTAs, longest first onto the least loaded CTA (about two blocks of fixed
+// work per item); *cta_out: per CTA (first item, end item, kv blocks, 0);
+// *empty_out: the q tiles with no kv block.  Returns the grid, or -1 with
+// the error set if one CTA would get more than 2^31 - 1 kv blocks.
+int pack_dq_items(const int* row_cnt, int nq, int Hq, int sms, std::vector<int4>* packed_out,
+                  std::vector<int4>* cta_out, std::vector<int>* empty_out) {
   std::vector<int4> items;
   std::vector<int> empty;
   int e0 = 0;
@@ -3090,11 +3082,37 @@ int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, 
     cta[b].y = (int)packed.size();
     if (blocks[b] > INT32_MAX) {
       set_error("backward kernel: too many kv blocks for one CTA");
-      return 1;
+      return -1;
     }
     cta[b].z = (int)blocks[b];
     cta[b].w = 0;
   }
+  *packed_out = std::move(packed);
+  *cta_out = std::move(cta);
+  *empty_out = std::move(empty);
+  return grid;
+}
+
+int prepare_dq_items(const pt_blockmap* cbm, int Hq, int sms, bool allow_build, cudaStream_t s,
+                     const pt_dq_lists** out) {
+  pt_blockmap* bm = const_cast<pt_blockmap*>(cbm);  // the list cache is the map's only mutable part
+  std::lock_guard<std::mutex> lk(g_items_mu);
+  for (const pt_dq_lists* e = bm->dq_lists; e; e = e->next)
+    if (e->hq == Hq && e->sms == sms) {
+      *out = e;
+      return 0;
+    }
+  if (!allow_build) {
+    set_error("block map's dQ work lists are not prepared for this head count (call pt_blockmap_prepare_bwd first)");
+    return 1;
+  }
+  const int *row_cnt = nullptr, *col_cnt = nullptr;
+  if (int rc = rowcol_counts(bm, &row_cnt, &col_cnt)) return rc;
+  const int nq = bm->nq;
+  std::vector<int4> packed, cta;
+  std::vector<int> empty;
+  const int grid = pack_dq_items(row_cnt, nq, Hq, sms, &packed, &cta, &empty);
+  if (grid < 0) return 1;
   pt_dq_lists* e = new pt_dq_lists();
   if (!empty.empty()) {
     e->h_empty = static_cast<int*>(std::malloc(sizeof(int) * empty.size()));
@@ -3525,6 +3543,30 @@ int launch_bwd_d512(const void* dO, const void* Q, const void* K, const void* V,
   return 0;
 }
 }  // namespace
+
+int debug_pack_dq(const int* row_cnt, int nq, int Hq, int ctas, int32_t* items, long long cap_items, int32_t* cta_rec,
+                  int32_t* n_items, int32_t* grid, int32_t* n_empty) {
+  std::vector<int4> packed, cta;
+  std::vector<int> empty;
+  const int gr = pack_dq_items(row_cnt, nq, Hq, ctas, &packed, &cta, &empty);
+  if (gr < 0) return 1;
+  *n_items = (int32_t)packed.size();
+  *grid = gr;
+  *n_empty = (int32_t)empty.size();
+  if ((long long)packed.size() > cap_items) {
+    set_error("pt_debug_pack_dq: %zu items, room for %lld", packed.size(), cap_items);
+    return 1;
+  }
+  for (size_t k = 0; k < packed.size(); ++k) {
+    const int32_t v[4] = {packed[k].x, packed[k].y, packed[k].z, packed[k].w};
+    std::memcpy(items + 4 * k, v, sizeof(v));
+  }
+  for (int b = 0; b < gr; ++b) {
+    const int32_t v[4] = {cta[b].x, cta[b].y, cta[b].z, cta[b].w};
+    std::memcpy(cta_rec + 4 * b, v, sizeof(v));
+  }
+  return 0;
+}
 
 int debug_pack_dkdv(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int ctas, bool exact_fill, int32_t* items,
                     long long cap_items, int32_t* cta_ptr, int32_t* n_items, int32_t* n_slots, int32_t* grid) {

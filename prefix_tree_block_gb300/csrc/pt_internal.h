@@ -204,6 +204,10 @@ int debug_draft_lists(int32_t ctx_len, int32_t n_blocks, int32_t block_size, con
                       const uint8_t* block_keep, int32_t causal, int32_t window, const int32_t* ctx_doc,
                       const int32_t* anchor_doc, int32_t* q_ptr, int64_t q_ptr_len, int32_t* kv_idx, int64_t cap,
                       int64_t* nnz, int64_t* kept_pairs);
+// Host-only: the backward's q-major packing for given row lengths
+// (pt_debug_pack_dq).
+int debug_pack_dq(const int* row_cnt, int nq, int Hq, int ctas, int32_t* items, long long cap_items, int32_t* cta_rec,
+                  int32_t* n_items, int32_t* grid, int32_t* n_empty);
 // Host-only: the backward's kv-major packing for given column lengths
 // (pt_debug_pack_dkdv).
 int debug_pack_dkdv(const int* col_cnt, int nk, int g, int Hkv, int max_slots, int ctas, bool exact_fill, int32_t* items,

@@ -1,8 +1,10 @@
-"""CPU checks of the backward's kv-major work-list packing (host logic, no
-GPU): the items the library builds for given column lengths cover every
+"""CPU checks of the backward's work-list packing (host logic, no GPU).
+kv-major: the items the library builds for given column lengths cover every
 (kv block, kv head) column exactly once, cut columns write distinct
 partial-sum slots within the allowed number, the CTA index is consistent,
-and the exact-fill packing of the one-pass kernel evens the CTAs out."""
+and the exact-fill packing of the one-pass kernel evens the CTAs out.
+q-major: every (q tile, q head) with kv blocks is one item with its list
+offset and length, and the CTA records add up."""
 import ctypes
 
 import numpy as np
@@ -160,3 +162,48 @@ def test_bad_arguments_rejected(lib):
     assert lib.pt_debug_pack_dkdv(big.ctypes.data, 40, 4, 2, 0, CTAS, 0, items.ctypes.data, 8, cta.ctypes.data,
                                   *refs) == pt.PT_ERR_INVALID_ARG
     assert n[0].value == 80
+
+
+def pack_dq(lib, rows, hq, ctas=CTAS):
+    rows = np.ascontiguousarray(rows, np.int32)
+    cap = max(1, int((rows > 0).sum()) * hq)
+    items = np.zeros((cap, 4), np.int32)
+    rec = np.zeros((ctas, 4), np.int32)
+    n_items, grid, n_empty = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    rc = lib.pt_debug_pack_dq(rows.ctypes.data, len(rows), hq, ctas, items.ctypes.data, cap, rec.ctypes.data,
+                              ctypes.byref(n_items), ctypes.byref(grid), ctypes.byref(n_empty))
+    assert rc == pt.PT_OK, rc
+    return items[:n_items.value], rec[:grid.value], n_empty.value
+
+
+@pytest.mark.parametrize("ctas", [1, 7, CTAS])
+def test_dq_items_cover_every_row_once(lib, ctas):
+    rng = np.random.default_rng(ctas)
+    for _ in range(40):
+        nq = int(rng.integers(1, 200))
+        hq = int(rng.integers(1, 9))
+        rows = rng.integers(0, nq + 1, nq)
+        rows[rng.random(nq) < 0.2] = 0
+        items, rec, n_empty = pack_dq(lib, rows, hq, ctas)
+        offsets = np.concatenate([[0], np.cumsum(rows)[:-1]])
+        want = {(t, h): (int(offsets[t]), int(rows[t])) for t in range(nq) if rows[t] > 0 for h in range(hq)}
+        got = {(int(t), int(h)): (int(e0), int(n)) for t, h, e0, n in items}
+        assert len(got) == len(items) and got == want
+        assert n_empty == int((rows == 0).sum())
+        assert len(rec) == max(1, min(ctas, len(items)))
+        assert rec[0, 0] == 0 and rec[-1, 1] == len(items) and np.all(rec[1:, 0] == rec[:-1, 1])
+        for x, y, blocks, _ in rec:
+            assert blocks == items[x:y, 3].sum()
+        # longest first: every CTA's items in non-increasing order of length
+        for x, y, _, _ in rec:
+            assert np.all(np.diff(items[x:y, 3]) <= 0)
+
+
+def test_dq_items_balanced(lib):
+    """Longest-first packing of many items: no CTA more than one item's
+    length (plus its fixed cost) above the mean."""
+    rng = np.random.default_rng(5)
+    rows = rng.integers(1, 40, 230)
+    items, rec, _ = pack_dq(lib, rows, 8)
+    load = np.array([rec_b[2] + 2 * (rec_b[1] - rec_b[0]) for rec_b in rec])
+    assert load.max() <= load.mean() + rows.max() + 2
